@@ -1,0 +1,55 @@
+"""Seeded synthetic inputs for the W4A16 linear layer.
+
+This module only draws random numbers; it holds none of the method's
+arithmetic (no dequantisation, no packing, no products).  Both the CUDA path
+and the CPU oracle are fed from here, so that they see the same bytes.
+
+Value distributions follow the layer shapes the MARLIN paper benchmarks
+("MARLIN: Mixed-Precision Auto-Regressive Parallel Inference on LLMs",
+Section 3.4 and Figure 1): activations ~ N(0, 1) rounded to FP16, 4-bit codes
+uniform on {0..15}, FP16 scales uniform on [0.002, 0.02].  numpy's FP16 cast
+rounds to nearest-even.
+
+Generators: ``numpy.random.Generator(PCG64(SeedSequence([seed, stream])))``
+with stream 0 for activations and stream 1 for weights, so one layer's
+weights stay the same while the batch size M is swept.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = ["make_weights", "make_activations", "make_layer", "effective_group"]
+
+
+def _rng(seed: int, stream: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([int(seed), int(stream)])))
+
+
+def effective_group(K: int, groupsize: int) -> int:
+    """Group size G along K; -1 (or K) selects one scale per column."""
+    return K if groupsize in (-1, K) else int(groupsize)
+
+
+def make_weights(K: int, N: int, groupsize: int, seed: int):
+    """Codes ``q`` uint8[K][N] uniform on 0..15 and scales ``s`` float16[K/G][N]
+    uniform on [0.002, 0.02]."""
+    G = effective_group(K, groupsize)
+    if G <= 0 or K % G:
+        raise ValueError("K must be a positive multiple of the group size")
+    rng = _rng(seed, 1)
+    q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
+    s = rng.uniform(0.002, 0.02, size=(K // G, N)).astype(np.float16)
+    return q, s
+
+
+def make_activations(M: int, K: int, seed: int) -> np.ndarray:
+    """Activations ``A`` float16[M][K] drawn from N(0, 1)."""
+    rng = _rng(seed, 0)
+    return rng.standard_normal((M, K), dtype=np.float32).astype(np.float16)
+
+
+def make_layer(M: int, K: int, N: int, groupsize: int, seed: int):
+    """A, q, s of one layer from one seed (weights and activations on separate streams)."""
+    q, s = make_weights(K, N, groupsize, seed)
+    return {"A": make_activations(M, K, seed), "q": q, "s": s,
+            "G": effective_group(K, groupsize)}

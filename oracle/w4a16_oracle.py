@@ -1,0 +1,248 @@
+"""Plain float64 CPU statement of the W4A16 layer -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU legs may
+import this module.  It is independent of the CUDA library and imports nothing
+from it.
+
+Sources (page title, section):
+  [P1] "MARLIN: Mixed-Precision Auto-Regressive Parallel Inference on Large
+       Language Models" (arXiv HTML), Section 3.4 "Kernel Design" (problem
+       statement: FP16 A, K x N INT4 B, symmetric quantisation with one FP16
+       scale per column or per G consecutive weights of a column) and its
+       paragraph "Bound By Weight Loading" (memory/FLOP counts).
+  [P2] "Marlin 完全拆解：4-bit 权重如何喂满 GPU Tensor Core" (the Marlin
+       deep-dive article), section "Marlin 要解决的精确问题" (the affine
+       dequantisation B^[k,n] = s[g,n] (q[k,n] - z[g,n]), q in {0..15}),
+       section "scale 为什么有时在内环乘，有时在末尾乘" (grouped sum
+       C = sum_g s[g,n] sum_{k in g} A[m,k](q[k,n]-8) and the per-column form
+       AB = (AQ) diag(s)), and section "量化数据如何进入 Tensor Core" (the
+       symmetric zero point 8 folded into the decode).
+
+Readings taken where the pages are silent (each also listed in the design notes):
+  * zero point: the symmetric main path uses the constant z = 8; no zero tensor;
+  * group index: g = floor(k / G), K a multiple of G; G = K (or -1) is the
+    one-scale-per-column mode;
+  * q arrives as uint8[K][N] row-major (one code per byte), s as fp16[K/G][N];
+  * the reference result is the exact dense product, accumulated in float64 in
+    plain k order (numpy matmul as the summation primitive);
+  * parity bound (per element): |C - C_ref| <= 4e-3 * sum_k |A[m,k] B^[k,n]| + 1e-4;
+  * the packed weight / permuted scale layout is this library's own ABI (the
+    pages describe its purpose -- one 16-byte load per thread carrying the
+    codes of four 16x16 tensor-core blocks, 16x64 tiles stored contiguously --
+    but print no permutation table); it is defined here by a closed index
+    formula, ``packed_position`` and ``scale_position``.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+#: symmetric INT4 zero point ([P2] "量化数据如何进入 Tensor Core": the zero 8 is folded into the decode)
+Z_POINT = 8
+#: per-element tolerance of the GEMM parity check
+TOL_REL = 4e-3
+TOL_ABS = 1e-4
+
+
+# ---------------------------------------------------------------------------
+# IEEE-754 binary16, written from the format definition (1 sign bit, 5
+# exponent bits with bias 15, 10 fraction bits; subnormals at 2^-24 steps).
+# ---------------------------------------------------------------------------
+
+def fp16_bits_to_f64(bits) -> np.ndarray:
+    """Decode binary16 bit patterns (uint16) to float64 exactly."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    sign = np.where(b >> 15, -1.0, 1.0)
+    e = (b >> 10) & 0x1F
+    f = (b & 0x3FF).astype(np.float64)
+    normal = sign * np.ldexp(1.0 + f / 1024.0, (e - 15).astype(np.int64))
+    sub = sign * np.ldexp(f, -24)
+    out = np.where(e == 0, sub, normal)
+    out = np.where((e == 31) & (f == 0), sign * np.inf, out)
+    out = np.where((e == 31) & (f != 0), np.nan, out)
+    return out
+
+
+def f64_to_fp16_bits(x) -> np.ndarray:
+    """Round float64 values to binary16 with round-to-nearest, ties-to-even.
+
+    Scaling by powers of two is exact in float64, so ``np.rint`` (which rounds
+    half to even) on the scaled magnitude performs exactly one RNE rounding.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    sign = np.signbit(x).astype(np.uint16) << 15
+    a = np.abs(x)
+    out = np.zeros(x.shape, dtype=np.uint16)
+    # subnormal range |x| < 2^-14: integer multiples of 2^-24
+    sub = a < 2.0 ** -14
+    m_sub = np.rint(np.ldexp(a, 24)).astype(np.int64)  # 1024 -> smallest normal, which is bit pattern 0x0400
+    # normal range
+    with np.errstate(divide="ignore"):
+        _, E = np.frexp(a)  # a = f * 2^E, f in [0.5, 1)
+    e = E.astype(np.int64) - 1  # a in [2^e, 2^(e+1))
+    m = np.rint(np.ldexp(a, (10 - e))).astype(np.int64)  # in [1024, 2048]
+    carry = m == 2048
+    e = np.where(carry, e + 1, e)
+    m = np.where(carry, 1024, m)
+    normal_bits = ((e + 15) << 10) | (m - 1024)
+    normal_bits = np.where(e + 15 >= 31, 0x7C00, normal_bits)  # overflow -> infinity
+    bits = np.where(sub, m_sub, normal_bits)
+    bits = np.where(np.isinf(a), 0x7C00, bits)
+    bits = np.where(np.isnan(a), 0x7E00, bits)
+    out[...] = bits.astype(np.uint16)
+    return out | sign
+
+
+def _as_f64(h) -> np.ndarray:
+    """float16 array (or its uint16 bit patterns) -> float64, exactly."""
+    h = np.asarray(h)
+    if h.dtype == np.float16:
+        h = h.view(np.uint16)
+    return fp16_bits_to_f64(h)
+
+
+# ---------------------------------------------------------------------------
+# Dequantisation and the dense product ([P1] Section 3.4; [P2] sections cited above)
+# ---------------------------------------------------------------------------
+
+def _group(K: int, G: int) -> int:
+    G = K if G in (-1, K) else int(G)
+    if G <= 0 or K % G:
+        raise ValueError(f"K={K} is not a multiple of the group size {G}")
+    return G
+
+
+def dequant_exact(q, s, G: int) -> np.ndarray:
+    """B^[k, n] = s[floor(k/G), n] * (q[k, n] - 8) in float64.
+
+    An FP16 scale times an integer in [-8, 7] needs at most 11 + 4 significant
+    bits, so the float64 product is exact.
+    """
+    q = np.asarray(q)
+    K = q.shape[0]
+    G = _group(K, G)
+    if q.min(initial=0) < 0 or q.max(initial=0) > 15:
+        raise ValueError("4-bit codes must lie in 0..15")
+    s64 = _as_f64(s)
+    if s64.shape != (K // G, q.shape[1]):
+        raise ValueError("scales must have shape [K/G][N]")
+    g_of_k = np.arange(K) // G
+    return s64[g_of_k, :] * (q.astype(np.float64) - Z_POINT)
+
+
+def dequant_fp16_bits(q, s, G: int) -> np.ndarray:
+    """The FP16 dequantised weight: one RNE rounding of the exact B^ (uint16 bits)."""
+    return f64_to_fp16_bits(dequant_exact(q, s, G))
+
+
+def gemm_ref(A, q, s, G: int):
+    """C_ref[m, n] = sum_k A[m, k] B^[k, n] and Bound[m, n] = sum_k |A[m, k] B^[k, n]|.
+
+    Both in float64; numpy's matmul is the summation primitive.  Returns
+    (C_ref, Bound), each float64[M][N].
+    """
+    A64 = _as_f64(A)
+    B64 = dequant_exact(q, s, G)
+    if A64.shape[1] != B64.shape[0]:
+        raise ValueError("A is M x K and B is K x N")
+    C = A64 @ B64
+    bound = np.abs(A64) @ np.abs(B64)
+    return C, bound
+
+
+def error_excess(C_gpu, C_ref, bound) -> np.ndarray:
+    """|C_gpu - C_ref| - (4e-3 * Bound + 1e-4): an element passes iff <= 0."""
+    c = _as_f64(C_gpu) if np.asarray(C_gpu).dtype in (np.float16, np.uint16) else np.asarray(C_gpu, np.float64)
+    return np.abs(c - C_ref) - (TOL_REL * bound + TOL_ABS)
+
+
+def error_ok(C_gpu, C_ref, bound) -> bool:
+    """True iff every element lies within the parity bound (NaN fails)."""
+    ex = error_excess(C_gpu, C_ref, bound)
+    return bool(np.all(ex <= 0.0))
+
+
+# ---------------------------------------------------------------------------
+# Packed layout (this library's own ABI; purpose from [P1] Section 3.4
+# "Maximizing Loading Bandwidth" and [P2] section "直接生成 MMA 所需的寄存器 fragment")
+# ---------------------------------------------------------------------------
+
+def packed_position(k, n, K: int):
+    """Word index and bit offset of code q[k, n] in the packed uint32 stream.
+
+    The stream is uint32[N/16][K/64][32][4]: for the 16 output columns
+    nb*16 .. nb*16+15 and the 64 reduction rows kb*64 .. kb*64+63, lane L's
+    four consecutive words (one 16-byte vector) are the operand fragments of
+    the four 16 x 16 tensor-core blocks j = 0..3 (rows 16j .. 16j+15 of the
+    tile).  Inside a 16x16 block, with r = n mod 16 (the fragment row) and
+    c = k mod 16 (the fragment column):
+        lane   = 4 * (r mod 8) + floor((c mod 8) / 2)
+        slot   = floor(r / 8) + 2 * floor(c / 8) + 4 * (c mod 2)
+        bits   = [4 * slot, 4 * slot + 4)
+    Slot i < 4 is the low half and slot i + 4 the high half of the lane's
+    i-th 32-bit operand register of the m16n8k16 multiply, with the output
+    columns on the fragment's 16-row side.
+    """
+    k = np.asarray(k, dtype=np.int64)
+    n = np.asarray(n, dtype=np.int64)
+    nb, r = n // 16, n % 16
+    kb, kk = k // 64, k % 64
+    j, c = kk // 16, kk % 16
+    lane = 4 * (r % 8) + (c % 8) // 2
+    slot = r // 8 + 2 * (c // 8) + 4 * (c % 2)
+    word = ((nb * (K // 64) + kb) * 32 + lane) * 4 + j
+    return word, 4 * slot
+
+
+def scale_position(n):
+    """Column index of scale s[g, n] inside the permuted row g.
+
+    Within each block of 16 columns, fragment rows r and r + 8 (r < 8) sit
+    side by side, so a lane reads the scales of both of its rows as one pair:
+    position = 16 * floor(n / 16) + 2 * (r mod 8) + floor(r / 8), r = n mod 16.
+    """
+    n = np.asarray(n, dtype=np.int64)
+    r = n % 16
+    return (n // 16) * 16 + 2 * (r % 8) + r // 8
+
+
+def _check_layout_shape(K: int, N: int):
+    if K % 64 or N % 16 or K <= 0 or N <= 0:
+        raise ValueError("the packed layout needs K % 64 == 0 and N % 16 == 0")
+
+
+def repack(q, s, G: int):
+    """Codes uint8[K][N] and scales fp16[K/G][N] -> (packed uint32[K*N/8], permuted fp16[K/G][N])."""
+    q = np.asarray(q)
+    K, N = q.shape
+    _check_layout_shape(K, N)
+    G = _group(K, G)
+    if q.dtype != np.uint8 or q.max(initial=0) > 15:
+        raise ValueError("4-bit codes must be uint8 values in 0..15")
+    kk, nn = np.meshgrid(np.arange(K), np.arange(N), indexing="ij")
+    word, shift = packed_position(kk, nn, K)
+    nibbles = np.zeros((K * N // 8, 8), dtype=np.uint32)
+    nibbles[word.ravel(), (shift // 4).ravel()] = q.ravel()
+    packed = np.zeros(K * N // 8, dtype=np.uint32)
+    for slot in range(8):
+        packed |= nibbles[:, slot] << np.uint32(4 * slot)
+    s = np.asarray(s)
+    if s.shape != (K // G, N):
+        raise ValueError("scales must have shape [K/G][N]")
+    sp = np.empty_like(s)
+    sp[:, scale_position(np.arange(N))] = s
+    return packed, sp
+
+
+def unpack(packed, sp, K: int, N: int, G: int):
+    """Inverse of ``repack``: (packed, permuted scales) -> (q uint8[K][N], s fp16[K/G][N])."""
+    _check_layout_shape(K, N)
+    G = _group(K, G)
+    packed = np.asarray(packed, dtype=np.uint32)
+    if packed.size != K * N // 8:
+        raise ValueError("packed stream has the wrong length")
+    kk, nn = np.meshgrid(np.arange(K), np.arange(N), indexing="ij")
+    word, shift = packed_position(kk, nn, K)
+    q = ((packed[word] >> shift.astype(np.uint32)) & np.uint32(15)).astype(np.uint8)
+    sp = np.asarray(sp)
+    s = sp[:, scale_position(np.arange(N))]
+    return q, s

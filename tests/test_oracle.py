@@ -1,0 +1,313 @@
+"""Pins of the CPU oracle to things other than itself (no GPU needed).
+
+Each pin is chosen so that a plausible slip in the oracle -- a wrong zero
+point, a group index taken modulo instead of by division, a transposed
+operand, a mis-rounded FP16 conversion, a layout that is not a bijection --
+fails at least one test here.
+"""
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import w4a16_oracle as ow
+from mixed_precision_w4a16_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# --------------------------------------------------------------------------
+# binary16 encoder / decoder
+# --------------------------------------------------------------------------
+
+def _golden_fp16():
+    rows = []
+    with open(os.path.join(GOLDEN, "fp16_binary16.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            v, b = line.split()[:2]
+            rows.append((float.fromhex(v), int(b, 16)))
+    return rows
+
+
+def test_fp16_golden_encode():
+    for v, b in _golden_fp16():
+        got = int(oracle.f64_to_fp16_bits(np.array([v]))[0])
+        assert got == b, (v, hex(got), hex(b))
+
+
+def test_fp16_golden_decode():
+    for v, b in _golden_fp16():
+        back = float(oracle.fp16_bits_to_f64(np.array([b], np.uint16))[0])
+        if b == 0x7C00:
+            assert back == float("inf")
+        elif abs(v) == 0.0 or float(np.float16(v)) == v:
+            # exactly representable inputs decode to themselves (sign of zero included)
+            assert back == v and np.signbit(back) == np.signbit(v)
+
+
+def test_fp16_encoder_matches_numpy_cast():
+    # numpy's float64 -> float16 cast is an independent implementation of the same rounding.
+    rng = np.random.default_rng(123)
+    mags = np.ldexp(rng.uniform(1, 2, 200000), rng.integers(-30, 17, 200000))
+    x = mags * rng.choice([-1.0, 1.0], 200000)
+    # add exact ties at several binades
+    m = rng.integers(1024, 2048, 5000)
+    e = rng.integers(-14, 15, 5000)
+    ties = np.ldexp(m + 0.5, e - 10)
+    x = np.concatenate([x, ties, -ties])
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    got = oracle.f64_to_fp16_bits(x)
+    assert np.array_equal(got, ref)
+
+
+def test_fp16_decoder_all_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = oracle.fp16_bits_to_f64(bits)
+    finite = np.isfinite(ref)
+    assert np.array_equal(got[finite], ref[finite])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(got[np.isinf(ref)], ref[np.isinf(ref)])
+
+
+# --------------------------------------------------------------------------
+# the dense product against exact integer brute force
+# --------------------------------------------------------------------------
+
+def _exact_fp16(x) -> int:
+    """FP16 value as an integer multiple of 2^-24 (exact; uses Python's Fraction)."""
+    f = Fraction(float(x)) * (1 << 24)
+    assert f.denominator == 1
+    return int(f)
+
+
+def _brute_force(A, q, s, G):
+    """Exact C * 2^48 and Bound * 2^48 as Python integers."""
+    M, K = A.shape
+    N = q.shape[1]
+    a = [[_exact_fp16(A[m, k]) for k in range(K)] for m in range(M)]
+    sc = [[_exact_fp16(s[g, n]) for n in range(N)] for g in range(s.shape[0])]
+    C = [[0] * N for _ in range(M)]
+    B = [[0] * N for _ in range(M)]
+    for m in range(M):
+        for n in range(N):
+            acc = 0
+            bnd = 0
+            for k in range(K):
+                # the zero point, written out: codes 0..15 stand for -8..7
+                w = sc[k // G][n] * (int(q[k, n]) - 8)
+                acc += a[m][k] * w
+                bnd += abs(a[m][k] * w)
+            C[m][n] = acc
+            B[m][n] = bnd
+    return C, B
+
+
+@pytest.mark.parametrize("M,K,N,G", [(1, 128, 16, 128), (3, 256, 32, 128), (4, 256, 16, 256), (2, 192, 16, 64)])
+def test_gemm_matches_exact_brute_force(M, K, N, G):
+    q, s = synth.make_weights(K, N, G, seed=7 + K + N)
+    A = synth.make_activations(M, K, seed=11 + M)
+    C, bound = oracle.gemm_ref(A, q, s, G)
+    Ce, Be = _brute_force(A, q, s, G)
+    scale = 2.0 ** -48
+    for m in range(M):
+        for n in range(N):
+            exact = Ce[m][n] * scale
+            ebound = Be[m][n] * scale
+            assert abs(C[m, n] - exact) <= K * 2.0 ** -52 * ebound + 1e-300, (m, n)
+            assert abs(bound[m, n] - ebound) <= K * 2.0 ** -52 * ebound + 1e-300, (m, n)
+
+
+def test_planted_zero_point_mistake_is_caught(monkeypatch):
+    # A wrong zero point planted in the oracle must fail the brute-force pin.
+    M, K, N, G = 2, 128, 16, 128
+    q, s = synth.make_weights(K, N, G, seed=5)
+    A = synth.make_activations(M, K, seed=6)
+    monkeypatch.setattr(ow, "Z_POINT", 7)
+    C, _ = oracle.gemm_ref(A, q, s, G)
+    Ce, Be = _brute_force(A, q, s, G)
+    worst = max(abs(C[m, n] - Ce[m][n] * 2.0 ** -48) / (Be[m][n] * 2.0 ** -48)
+                for m in range(M) for n in range(N))
+    assert worst > 1e-3
+
+
+# --------------------------------------------------------------------------
+# closed forms and special cases
+# --------------------------------------------------------------------------
+
+def test_zero_codes_give_exact_zero():
+    K, N, G = 256, 32, 128
+    _, s = synth.make_weights(K, N, G, seed=1)
+    q = np.full((K, N), 8, np.uint8)
+    A = synth.make_activations(5, K, seed=2)
+    C, bound = oracle.gemm_ref(A, q, s, G)
+    assert np.all(C == 0.0) and np.all(bound == 0.0)
+
+
+def test_identity_rows_return_dequantised_rows():
+    K, N, G = 256, 48, 128
+    q, s = synth.make_weights(K, N, G, seed=3)
+    rows = [0, 5, 127, 128, 200, 255]
+    A = np.zeros((len(rows), K), np.float16)
+    for m, k in enumerate(rows):
+        A[m, k] = 1.0
+    C, _ = oracle.gemm_ref(A, q, s, G)
+    Bh = oracle.dequant_exact(q, s, G)
+    assert np.array_equal(C, Bh[rows, :])
+    # the FP16 dequantised weight is one RNE rounding of the exact value
+    assert np.array_equal(oracle.f64_to_fp16_bits(C), oracle.dequant_fp16_bits(q, s, G)[rows, :])
+
+
+def test_groups_are_consecutive_rows():
+    # "one scale per G consecutive weights in each column": codes 9 (value +1) in the first
+    # group only and zero elsewhere give C = G * s[0, n] for an all-ones activation row;
+    # codes 9 everywhere give G * sum_g s[g, n].
+    K, N, G = 512, 32, 128
+    _, s = synth.make_weights(K, N, G, seed=4)
+    s64 = s.astype(np.float64)
+    A = np.ones((1, K), np.float16)
+    q = np.full((K, N), 8, np.uint8)
+    q[:G, :] = 9
+    C, _ = oracle.gemm_ref(A, q, s, G)
+    assert np.array_equal(C[0], G * s64[0])
+    q[:, :] = 9
+    C, _ = oracle.gemm_ref(A, q, s, G)
+    assert np.allclose(C[0], G * s64.sum(axis=0), rtol=1e-15, atol=0)
+    q[:, :] = 0  # value -8
+    C, _ = oracle.gemm_ref(A, q, s, G)
+    assert np.allclose(C[0], -8 * G * s64.sum(axis=0), rtol=1e-15, atol=0)
+
+
+def test_per_column_mode_is_diag_scaling():
+    # group = K: AB = (A Q) diag(s), Q = q - 8 (integer matrix)
+    M, K, N = 3, 256, 32
+    q, s = synth.make_weights(K, N, -1, seed=8)
+    A = synth.make_activations(M, K, seed=9)
+    C, _ = oracle.gemm_ref(A, q, s, -1)
+    AQ = A.astype(np.float64) @ (q.astype(np.float64) - 8.0)
+    assert np.allclose(C, AQ * s.astype(np.float64)[0], rtol=1e-13, atol=1e-13)
+
+
+def test_integer_gemm_textbook():
+    # s = 1 and small integer activations: C is an integer GEMM, computed here in int64.
+    rng = np.random.default_rng(10)
+    M, K, N, G = 4, 256, 64, 128
+    Ai = rng.integers(-4, 5, (M, K))
+    q = rng.integers(0, 16, (K, N)).astype(np.uint8)
+    s = np.ones((K // G, N), np.float16)
+    C, _ = oracle.gemm_ref(Ai.astype(np.float16), q, s, G)
+    ref = Ai.astype(np.int64) @ (q.astype(np.int64) - 8)
+    assert np.array_equal(C, ref.astype(np.float64))
+
+
+def test_error_bound_semantics():
+    C_ref = np.array([[1.0, -2.0]])
+    bound = np.array([[10.0, 0.0]])
+    ok = np.array([[1.0 + 4e-2, -2.0 + 1e-4]])
+    bad = np.array([[1.0 + 4.1e-2, -2.0]])
+    assert oracle.error_ok(ok, C_ref, bound)
+    assert not oracle.error_ok(bad, C_ref, bound)
+    assert not oracle.error_ok(np.array([[np.nan, -2.0]]), C_ref, bound)
+
+
+def test_code_range_rejected():
+    q = np.full((128, 16), 16, np.uint8)
+    s = np.ones((1, 16), np.float16)
+    with pytest.raises(ValueError):
+        oracle.dequant_exact(q, s, 128)
+    with pytest.raises(ValueError):
+        oracle.repack(q, s, 128)
+
+
+# --------------------------------------------------------------------------
+# packed layout
+# --------------------------------------------------------------------------
+
+# PTX ISA, "Matrix Fragments for mma.m16n8k16 with floating point type": the A operand
+# (16 x 16, .f16) is four .f16x2 registers per lane; with groupID = lane / 4 and
+# tig = lane % 4 the eight elements a0..a7 sit at (row, col):
+ISA_A_FRAGMENT = {
+    0: (0, 0), 1: (0, 1),      # a0, a1: (groupID,     2*tig + {0,1})
+    2: (8, 0), 3: (8, 1),      # a2, a3: (groupID + 8, 2*tig + {0,1})
+    4: (0, 8), 5: (0, 9),      # a4, a5: (groupID,     2*tig + 8 + {0,1})
+    6: (8, 8), 7: (8, 9),      # a6, a7: (groupID + 8, 2*tig + 8 + {0,1})
+}
+
+
+def test_packed_layout_is_the_isa_fragment():
+    K = 64
+    for lane in range(32):
+        g, t = lane // 4, lane % 4
+        for p, (dr, dc) in ISA_A_FRAGMENT.items():
+            for j in range(4):
+                for nb in range(2):
+                    n = nb * 16 + g + dr
+                    k = 16 * j + 2 * t + dc
+                    word, shift = oracle.packed_position(k, n, K)
+                    reg, half = p // 2, p % 2
+                    # register `reg` = (low half, high half) = (a_{2reg}, a_{2reg+1}); slot = reg + 4*half
+                    assert int(word) == (nb * 32 + lane) * 4 + j
+                    assert int(shift) == 4 * (reg + 4 * half)
+
+
+def test_packed_layout_is_a_bijection():
+    K, N = 256, 96
+    kk, nn = np.meshgrid(np.arange(K), np.arange(N), indexing="ij")
+    word, shift = oracle.packed_position(kk, nn, K)
+    code = word * 8 + shift // 4
+    assert np.array_equal(np.sort(code.ravel()), np.arange(K * N))
+
+
+def test_16x64_tiles_are_contiguous_and_vectors_span_four_blocks():
+    # 16 x 64 tiles are stored contiguously (512 bytes); each lane's 16-byte vector
+    # carries codes from four distinct 16 x 16 blocks.
+    K, N = 256, 64
+    kk, nn = np.meshgrid(np.arange(K), np.arange(N), indexing="ij")
+    word, _ = oracle.packed_position(kk, nn, K)
+    tile = (nn // 16) * (K // 64) + kk // 64
+    for t in np.unique(tile):
+        w = np.unique(word[tile == t])
+        assert w.size == 128 and w[-1] - w[0] == 127 and w[0] == t * 128
+    vec = word // 4
+    blk = (kk // 16) * 1000 + nn // 16
+    for v in np.unique(vec)[:64]:
+        assert np.unique(blk[vec == v]).size == 4
+
+
+def test_scale_position_pairs_rows_r_and_r_plus_8():
+    n = np.arange(64)
+    p = oracle.scale_position(n)
+    assert np.array_equal(np.sort(p), n)
+    for r in range(8):
+        assert p[r + 8] == p[r] + 1 and p[r] % 2 == 0
+    assert np.all(p // 16 == n // 16)
+
+
+@pytest.mark.parametrize("K,N,G", [(128, 16, 128), (256, 64, 128), (512, 48, -1), (1024, 128, 128)])
+def test_repack_unpack_round_trip(K, N, G):
+    q, s = synth.make_weights(K, N, G, seed=K + N)
+    packed, sp = oracle.repack(q, s, G)
+    assert packed.dtype == np.uint32 and packed.size == K * N // 8
+    q2, s2 = oracle.unpack(packed, sp, K, N, G)
+    assert np.array_equal(q2, q)
+    assert np.array_equal(s2.view(np.uint16), s.view(np.uint16))
+
+
+def test_repack_word_decodes_to_fragment_values():
+    # Decoding one word by its nibble slots must give the lane's eight A-fragment codes.
+    K, N, G = 64, 16, 64
+    q, s = synth.make_weights(K, N, G, seed=21)
+    packed, _ = oracle.repack(q, s, G)
+    for lane in range(32):
+        g, t = lane // 4, lane % 4
+        for j in range(4):
+            w = int(packed[lane * 4 + j])
+            for p, (dr, dc) in ISA_A_FRAGMENT.items():
+                slot = p // 2 + 4 * (p % 2)
+                assert (w >> (4 * slot)) & 15 == q[16 * j + 2 * t + dc, g + dr]
