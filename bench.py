@@ -1,0 +1,461 @@
+#!/usr/bin/env python
+"""W4A16 GEMM benchmark on GB300.
+
+Default workload: the single large layer K=18432, N=73728, group 128, swept
+over batch sizes M in {1, 2, 4, 8, 16, 32, 64, 128}.  One "step" runs the
+GEMM once per M (the whole hot path over one batch of synthetic inputs per
+M).  The packed weights (679 MB) exceed the 129 MB L2, so every GEMM streams
+its weights from HBM without any flush.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload big|pr1|7b|70b|prefill]
+
+Prints one JSON line (rank 0).  ``value`` is the whole-job throughput in TB/s
+of algorithmic bytes (2MK + 0.5KN + 2(K/G)N + 2MN per GEMM) over the timed
+region; ``sweep`` gives per-M microseconds, TB/s, TFLOP/s and the fraction of
+the roofline max(bytes / HBM BW, FLOPs / dense FP16 peak).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "W4A16 GEMM µs, achieved HBM TB/s & % of roofline vs M=1..128 (1×GB300)"
+L2_BYTES = 129 * 1024 * 1024
+
+# workload name -> (description, list of (K, N, groupsize, [M ...]), seed)
+WORKLOADS = {
+    "big": ("single large layer K=18432 N=73728 group 128, M sweep 1..128",
+            [(18432, 73728, 128, [1, 2, 4, 8, 16, 32, 64, 128])], 2),
+    "pr1": ("PR1: M=16 K=1024 N=1024 group 128", [(1024, 1024, 128, [16])], 0),
+    "7b": ("7B-style decode layers, M in {1,16}, group 128",
+           [(4096, 12288, 128, [1, 16]), (4096, 4096, 128, [1, 16]), (4096, 22016, 128, [1, 16]),
+            (11008, 4096, 128, [1, 16])], 1),
+    "70b": ("70B-style layers M=32, group 128 and per-column",
+            [(8192, 10240, 128, [32]), (8192, 8192, 128, [32]), (8192, 57344, 128, [32]), (28672, 8192, 128, [32]),
+             (8192, 10240, -1, [32]), (8192, 8192, -1, [32]), (8192, 57344, -1, [32]), (28672, 8192, -1, [32])], 3),
+    "prefill": ("compute-bound prefill M in {256,512,1024}, K=8192 N=28672 group 128",
+                [(8192, 28672, 128, [256, 512, 1024])], 4),
+}
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def gemm_bytes(M, K, N, G):
+    G = K if G in (-1, K) else G
+    return 2 * M * K + K * N // 2 + 2 * (K // G) * N + 2 * M * N
+
+
+def gemm_flops(M, K, N):
+    return 2 * M * K * N
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="big")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-sample", default=None, help=argparse.SUPPRESS)  # internal: oracle timing child
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def _cpu_sample_child(spec: str):
+    """Time the oracle on a column sample of every GEMM of the workload (runs in a
+    single-threaded child process); prints JSON {seconds, scaled_seconds, sample}."""
+    import numpy as np
+    import oracle
+    from mixed_precision_w4a16_gb300 import synth
+    workload, ncols = spec.split(":")
+    ncols = int(ncols)
+    desc, layers, seed = WORKLOADS[workload]
+    total = 0.0
+    scaled = 0.0
+    for li, (K, N, G, Ms) in enumerate(layers):
+        nc = min(ncols, N)
+        q, s = synth.make_weights(K, nc, G, seed * 100 + li)  # same distributions, sample width
+        for M in Ms:
+            A = synth.make_activations(M, K, seed * 1000 + M)
+            t0 = time.perf_counter()
+            oracle.gemm_ref(A, q, s, G)
+            dt = time.perf_counter() - t0
+            total += dt
+            scaled += dt * (N / nc)
+    print(json.dumps({"seconds": total, "scaled_seconds": scaled,
+                      "sample": f"every GEMM of the workload on {ncols} of its N columns (oracle time scaled by N/cols)"}))
+
+
+def run_cpu_sample(workload: str, ncols: int):
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    out = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample", f"{workload}:{ncols}"],
+                         capture_output=True, text=True, env=env, timeout=900)
+    if out.returncode != 0:
+        raise RuntimeError(f"oracle timing failed: {out.stderr[-2000:]}")
+    return json.loads(out.stdout.strip().splitlines()[-1])
+
+
+def workload_totals(layers):
+    tb = sum(gemm_bytes(M, K, N, G) for K, N, G, Ms in layers for M in Ms)
+    tf = sum(gemm_flops(M, K, N) for K, N, G, Ms in layers for M in Ms)
+    return tb, tf
+
+
+def cpu_sample_cols(workload):
+    return {"big": 512, "pr1": 1024, "7b": 1024, "70b": 512, "prefill": 256}[workload]
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms on a reader thread; samples are time-stamped so
+    that only those taken inside the timed region are summarised."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, uuid):
+        import threading
+        self.samples = []
+        self.t_start = self.t_end = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if uuid:
+            cmd += ["-i", uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def start_timing(self):
+        self.t_start = time.time()
+
+    def stop_timing(self):
+        self.t_end = time.time()
+
+    def finish(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        inside = [p for t, p in self.samples if self.t_start is not None and self.t_start <= t <= (self.t_end or t)]
+        note = "samples inside the timed region"
+        if not inside:  # timed region shorter than one sampling period: take the nearest samples
+            near = sorted(self.samples, key=lambda tp: abs(tp[0] - (self.t_start or tp[0])))[:3]
+            inside = [p for _, p in near]
+            note = "nearest samples (timed region shorter than the sampling period)"
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [v for v in (num(p[1]) for p in inside) if v is not None]
+        smax = [v for v in (num(p[2]) for p in inside) if v is not None]
+        power = [v for v in (num(p[3]) for p in inside) if v is not None]
+        reasons = sorted({name for p in inside for name, v in zip(self.REASONS, p[5:9])
+                          if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(inside), "power_w_max": max(power) if power else None,
+                "note": note}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world, device):
+    import numpy as np
+    import torch
+    import mixed_precision_w4a16_gb300 as w
+    from mixed_precision_w4a16_gb300 import build, synth
+
+    build.build()
+    desc, layers, seed = WORKLOADS[args.workload]
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream()
+
+    # ---- inputs: seeded synthetic weights -> device repack; activations resident in HBM
+    points = []  # (K, N, G, M, [packed copies], sp copies, A_d, C_d)
+    max_ws = 0
+    for li, (K, N, G, Ms) in enumerate(layers):
+        q, s = synth.make_weights(K, N, G, seed * 100 + li)
+        q_d = torch.from_numpy(q).to(device)
+        s_d = torch.from_numpy(s).to(device)
+        del q
+        lbytes = K * N // 2
+        copies = max(1, math.ceil(3 * L2_BYTES / lbytes)) if lbytes < 2 * L2_BYTES else 1
+        packs = [w.repack(q_d, s_d, G) for _ in range(copies)]
+        del q_d, s_d
+        for M in Ms:
+            A = synth.make_activations(M, K, seed * 1000 + M)
+            A_d = torch.from_numpy(A).to(device)
+            C_d = torch.empty((M, N), dtype=torch.float16, device=device)
+            points.append({"K": K, "N": N, "G": G, "M": M, "packs": packs, "A": A, "A_d": A_d, "C_d": C_d})
+            max_ws = max(max_ws, w.w4a16_workspace_bytes(M, K, N, G))
+    ws = torch.zeros(max_ws, dtype=torch.uint8, device=device)
+    torch.cuda.synchronize()
+    launches_per_step = 0
+    for p in points:
+        plan = w.w4a16_plan(p["M"], p["K"], p["N"], p["G"])
+        p["launches"] = math.ceil(p["M"] / plan["m_chunk"])
+        launches_per_step += p["launches"]
+
+    def one_step(it, evs=None):
+        for i, p in enumerate(points):
+            packed, sp = p["packs"][it % len(p["packs"])]
+            if evs is not None:
+                evs[i][0].record(stream)
+            w.w4a16_gemm(p["A_d"], packed, sp, p["C_d"], p["M"], p["K"], p["N"], p["G"], ws, max_ws, stream)
+            if evs is not None:
+                evs[i][1].record(stream)
+
+    for it in range(args.warmup):
+        one_step(it)
+    torch.cuda.synchronize()
+    if w.w4a16_get_status(ws) != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid) if rank == 0 else None
+    time.sleep(0.3)
+
+    # ---- timed region: barrier + sync on both sides, CUDA events on the launching stream
+    per_point = [[] for _ in points]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start_timing()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    evs_all = []
+    ev0.record(stream)
+    for it in range(args.steps):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in points]
+        one_step(it, evs)
+        evs_all.append(evs)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.stop_timing()
+    if world > 1:
+        torch.distributed.barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    for evs in evs_all:
+        for i, (a, b) in enumerate(evs):
+            per_point[i].append(a.elapsed_time(b))
+    status = w.w4a16_get_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status error in timed region: {w.w4a16_status_string(status)}")
+
+    # ---- end-to-end through the public API: pinned host A in, host C out, every step
+    e2e = None
+    if not args.no_e2e:
+        hostA = [torch.from_numpy(p["A"]).pin_memory() for p in points]
+        hostC = [torch.empty(p["C_d"].shape, dtype=torch.float16).pin_memory() for p in points]
+        h2d = sum(p["M"] * p["K"] * 2 for p in points)
+        d2h = sum(p["M"] * p["N"] * 2 for p in points)
+        e_steps = max(1, min(args.steps, 50))
+        for it in range(2):
+            for i, p in enumerate(points):
+                p["A_d"].copy_(hostA[i], non_blocking=True)
+                packed, sp = p["packs"][it % len(p["packs"])]
+                w.w4a16_gemm(p["A_d"], packed, sp, p["C_d"], p["M"], p["K"], p["N"], p["G"], ws, max_ws, stream)
+                hostC[i].copy_(p["C_d"], non_blocking=True)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for it in range(e_steps):
+            for i, p in enumerate(points):
+                p["A_d"].copy_(hostA[i], non_blocking=True)
+                packed, sp = p["packs"][it % len(p["packs"])]
+                w.w4a16_gemm(p["A_d"], packed, sp, p["C_d"], p["M"], p["K"], p["N"], p["G"], ws, max_ws, stream)
+                hostC[i].copy_(p["C_d"], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1) / e_steps
+        e_ms = reduce_max(e_ms, world, device)
+        tb, _ = workload_totals(layers)
+        e2e = {"value": world * tb / (e_ms * 1e-3) / 1e12, "unit": "TB/s", "ms_per_step": e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps}
+
+    ms_per_step = reduce_max(ms_total / args.steps, world, device)
+    clocks = sampler.finish() if sampler else None
+    if rank != 0:
+        return None
+
+    tb, tf = workload_totals(layers)
+    value = world * tb / (ms_per_step * 1e-3) / 1e12
+    bw = peaks["hbm_gbs"] * 1e9
+    pk = peaks["bf16_tflops"] * 1e12  # dense FP16 equals dense BF16 on this part
+    sweep = []
+    mem_bytes = mem_time = 0.0
+    for p, ts in zip(points, per_point):
+        us = statistics.median(ts) * 1e3
+        by = gemm_bytes(p["M"], p["K"], p["N"], p["G"])
+        fl = gemm_flops(p["M"], p["K"], p["N"])
+        t_roof = max(by / bw, fl / pk)
+        mem_bound = by / bw >= fl / pk
+        if mem_bound:
+            mem_bytes += by
+            mem_time += us * 1e-6
+        sweep.append({"M": p["M"], "K": p["K"], "N": p["N"], "group": p["G"], "us": round(us, 2),
+                      "us_p10": round(sorted(ts)[len(ts) // 10] * 1e3, 2),
+                      "us_p90": round(sorted(ts)[(9 * len(ts)) // 10] * 1e3, 2),
+                      "tb_s": round(by / (us * 1e-6) / 1e12, 3), "tflops": round(fl / (us * 1e-6) / 1e12, 1),
+                      "roofline_frac": round(t_roof / (us * 1e-6), 3), "bound": "hbm" if mem_bound else "tensor",
+                      "launches": p["launches"]})
+    if mem_time > 0:
+        ach = mem_bytes / mem_time / 1e9
+        roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(ach / peaks["hbm_gbs"], 3), "traffic": None,
+                    "kernel": "gemm_mma_kernel", "over": "memory-bound points of the sweep",
+                    "peak_source": peaks["source"]}
+    else:
+        fl_t = sum(gemm_flops(p["M"], p["K"], p["N"]) for p in points)
+        t_t = sum(statistics.median(ts) * 1e-3 for ts in per_point)
+        ach = fl_t / t_t / 1e12
+        roofline = {"bound": "tensor", "achieved": round(ach, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": round(ach / peaks["bf16_tflops"], 3), "traffic": None, "kernel": "gemm_mma_kernel",
+                    "peak_source": peaks["source"]}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        ncols = cpu_sample_cols(args.workload)
+        r = run_cpu_sample(args.workload, ncols)
+        cpu = {"value": tb / r["scaled_seconds"] / 1e12, "unit": "TB/s", "cores": 1, "kind": "oracle",
+               "sample": r["sample"] + f"; measured {r['seconds']:.1f} s single-threaded"}
+
+    return {
+        "metric": METRIC, "value": round(value, 4), "unit": "TB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": desc, "gemms_per_step": len(points),
+                   "l2": "inputs larger than L2" if all(len(p["packs"]) == 1 for p in points)
+                   else "weight copies rotated to exceed 3x L2",
+                   "parallelism": f"replicas x{world}", "peaks": peaks["source"]},
+        "sweep": sweep, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+    }
+
+
+def reduce_max(x, world, device):
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle, timed as it stands on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    desc, layers, seed = WORKLOADS[args.workload]
+    tb, _ = workload_totals(layers)
+    ncols = max(16, cpu_sample_cols(args.workload) // 4)
+    for _ in range(args.warmup):
+        run_cpu_sample(args.workload, ncols)
+    secs = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        secs.append(run_cpu_sample(args.workload, ncols)["scaled_seconds"])
+    wall = time.perf_counter() - t0
+    s_step = statistics.mean(secs)
+    v = tb / s_step / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": s_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": desc, "parallelism": "single host process"},
+        "cpu_baseline": {"value": v, "unit": "TB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: every GEMM of the workload on {ncols} columns, time scaled by N/cols "
+                                   f"(wall {wall:.1f} s for {args.steps} steps)"},
+        "e2e": {"value": v, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    if args.cpu_sample:
+        _cpu_sample_child(args.cpu_sample)
+        return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    import torch
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    try:
+        out = run_ours(args, rank, world, device)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,178 @@
+/*
+ * w4a16.h -- C ABI of the GB300 (sm_103a) W4A16 linear-layer library.
+ *
+ * The operation ("MARLIN: Mixed-Precision Auto-Regressive Parallel Inference
+ * on Large Language Models", Section 3.4 "Kernel Design"; the Marlin
+ * deep-dive article "Marlin 完全拆解", section "Marlin 要解决的精确问题"):
+ *
+ *     C[M x N] = A[M x K] * B^[K x N],   B^[k, n] = s[floor(k / G), n] * (q[k, n] - 8)
+ *
+ * A and C are IEEE binary16 (FP16), q are 4-bit codes 0..15 (symmetric, zero
+ * point 8), s are FP16 scales, one per G consecutive rows of each column
+ * (G = 128) or one per column (G = K, also spelt -1).
+ *
+ * Conventions shared by every entry point:
+ *  - FP16 data are passed as uint16_t bit patterns.
+ *  - All buffers are caller-owned; the library never allocates device memory.
+ *    Device pointers must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Kernel launches are asynchronous on that stream; only the size
+ *    queries, w4a16_plan and w4a16_get_status are synchronous.
+ *  - Every call validates its arguments on the host first and returns a
+ *    w4a16_status; nothing is launched when validation fails.  The device
+ *    never traps: errors found on the device (a code above 15, a pipeline
+ *    wait that ran out of time) are recorded in a status word and returned
+ *    by w4a16_get_status.
+ *  - The library is built for sm_103a only and returns W4A16_ERR_ARCH on any
+ *    other device.  There is no CPU fallback.
+ *
+ * Shapes: K % 128 == 0, N % 64 == 0, groupsize in {128, K, -1}, M >= 0.
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define W4A16_API __attribute__((visibility("default")))
+#else
+#define W4A16_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  W4A16_OK = 0,
+  W4A16_ERR_NULL = 1,        /* a required pointer is NULL */
+  W4A16_ERR_SHAPE = 2,       /* K, N or M outside the supported shapes */
+  W4A16_ERR_GROUP = 3,       /* groupsize not in {128, K, -1} */
+  W4A16_ERR_CODE_RANGE = 4,  /* repack saw a code above 15 (device-detected) */
+  W4A16_ERR_WORKSPACE = 5,   /* workspace missing or smaller than w4a16_workspace_bytes */
+  W4A16_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed */
+  W4A16_ERR_TIMEOUT = 7,     /* a pipeline wait ran out of time (device-detected) */
+  W4A16_ERR_ARCH = 8,        /* current device is not compute capability 10.3 */
+  W4A16_ERR_ALIGN = 9        /* a device pointer is not 16-byte aligned */
+} w4a16_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+W4A16_API const char* w4a16_status_string(int status);
+
+/* Version of this ABI (incremented on any incompatible change). */
+W4A16_API int w4a16_abi_version(void);
+
+/* ---------------------------------------------------------------------------
+ * Size queries (host only, pure functions; 0 on invalid shapes).
+ * ------------------------------------------------------------------------- */
+
+/* Bytes of the packed weight stream: K * N / 2 (4 bits per weight). */
+W4A16_API size_t w4a16_packed_bytes(int K, int N);
+
+/* Number of FP16 scales: (K / G) * N, G = K for groupsize K or -1. */
+W4A16_API size_t w4a16_scales_count(int K, int N, int groupsize);
+
+/* Bytes of workspace w4a16_gemm needs for this shape on the current device.
+ * Layout: a status word, one arrival counter per output column tile, and
+ * FP32 partial-sum slots for column tiles whose K range is split between
+ * CTAs.  The caller zeroes it once (cudaMemsetAsync) before first use; every
+ * successful call leaves the counters at zero, so it can be reused on the
+ * same stream without re-zeroing.  After a call reports W4A16_ERR_TIMEOUT the
+ * caller must zero it again.  One workspace per concurrently running stream. */
+W4A16_API size_t w4a16_workspace_bytes(int M, int K, int N, int groupsize);
+
+/* ---------------------------------------------------------------------------
+ * Offline repack (the pages: MARLIN paper Section 3.4 "Maximizing Loading
+ * Bandwidth" -- 16x64 tiles stored contiguously, one 16-byte vector per thread
+ * carrying the codes of four 16x16 tensor-core blocks; deep-dive article
+ * sections "直接生成 MMA 所需的寄存器 fragment" and "全局内存布局").
+ *
+ *   q        device, uint8[K][N] row-major, codes 0..15
+ *   s        device, fp16[K/G][N] row-major scales
+ *   packed   device, uint32[K*N/8] output, layout below
+ *   scales_p device, fp16[K/G][N] output, columns permuted within 16-blocks
+ *
+ * Packed layout (this library's own ABI): uint32[N/16][K/64][32][4].  Code
+ * q[k][n] sits in word ((n/16 * K/64 + k/64) * 32 + lane) * 4 + (k%64)/16 at
+ * bits [4*slot, 4*slot+4), with r = n%16, c = k%16,
+ *   lane = 4*(r%8) + (c%8)/2,   slot = r/8 + 2*(c/8) + 4*(c%2),
+ * i.e. each word is one lane's operand fragment of a 16x16 mma.m16n8k16 block
+ * whose 16 rows are output columns.  Permuted scales: s[g][n] is stored at
+ * scales_p[g][16*(n/16) + 2*(r%8) + r/8].
+ * Codes above 15 are masked to 4 bits and flag W4A16_ERR_CODE_RANGE for
+ * w4a16_get_status(NULL, stream).
+ * ------------------------------------------------------------------------- */
+W4A16_API int w4a16_repack(const uint8_t* q, const uint16_t* s, int K, int N, int groupsize,
+                 uint32_t* packed, uint16_t* scales_p, void* stream);
+
+/* Inverse of w4a16_repack (diagnostic; the pages' layout check "repack then
+ * unpack recovers the same codes and scales", deep-dive article section
+ * "适用边界与工程陷阱").  Outputs q uint8[K][N] and s fp16[K/G][N]. */
+W4A16_API int w4a16_unpack(const uint32_t* packed, const uint16_t* scales_p, int K, int N, int groupsize,
+                 uint8_t* q, uint16_t* s, void* stream);
+
+/* Dequantised weights B^ as FP16, fp16[K][N] row-major (diagnostic):
+ * Bhat[k][n] = round_to_nearest_even(s[k/G][n] * (q[k][n] - 8)), decoded from
+ * the packed stream with the same in-register decode the GEMM uses
+ * (deep-dive article section "INT4 只是存储类型，不是这条路径的计算类型"). */
+W4A16_API int w4a16_dequant(const uint32_t* packed, const uint16_t* scales_p, int K, int N, int groupsize,
+                  uint16_t* Bhat, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * The fused W4A16 GEMM (MARLIN paper Section 3.4; deep-dive article sections
+ * "软件流水线", "并行划分" and "Split-K 与全局归约").
+ *
+ *   A         device, fp16[M][K] row-major (lda = K)
+ *   packed    device, output of w4a16_repack
+ *   scales_p  device, output of w4a16_repack
+ *   C         device, fp16[M][N] row-major (ldc = N), written, never read
+ *   workspace device, >= w4a16_workspace_bytes(M, K, N, groupsize) bytes,
+ *             zeroed by the caller before first use (see above)
+ *
+ * Accumulation is FP32; each group's partial product is scaled by its FP32
+ * scale, and split-K partials are summed in a fixed order, so repeated calls
+ * give bitwise-identical C.  M == 0 returns W4A16_OK without a launch.
+ * ------------------------------------------------------------------------- */
+W4A16_API int w4a16_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* scales_p, uint16_t* C,
+               int M, int K, int N, int groupsize, void* workspace, size_t workspace_bytes,
+               void* stream);
+
+/* Synchronises `stream`, then returns (and clears) the first error recorded on
+ * the device: the repack code-range flag and, when `workspace` is non-NULL,
+ * the GEMM status word in that workspace.  W4A16_OK when none. */
+W4A16_API int w4a16_get_status(void* workspace, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Work plan (host only; deep-dive article section "为什么规则二维网格会浪费最后
+ * 一波 SM": T = ceil(#tiles / #SMs) consecutive K-tiles per SM, wrapping into
+ * the next column).  Describes how w4a16_gemm would split a shape over
+ * `num_sms` SMs (num_sms <= 0: the current device's count).
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  int path;          /* 1 = mma.sync streaming kernel */
+  int m_tiles;       /* 8-row token tiles per launch (1, 2, 4 or 8) */
+  int m_chunk;       /* rows per launch (8 * m_tiles); launches = ceil(M / m_chunk) */
+  int n_tile;        /* output columns per work unit */
+  int k_tile;        /* reduction rows per work unit (128) */
+  int units;         /* work units per launch: (N / n_tile) * (K / k_tile) */
+  int units_per_cta; /* T */
+  int grid;          /* CTAs per launch */
+  int stages;        /* shared-memory pipeline depth */
+  int smem_bytes;    /* dynamic shared memory per CTA */
+  int threads;       /* threads per CTA */
+} w4a16_plan_t;
+
+W4A16_API int w4a16_plan(int M, int K, int N, int groupsize, int num_sms, w4a16_plan_t* out);
+
+/* Debug knob (not thread-safe): bound, in GPU clock cycles, on every pipeline
+ * wait of later w4a16_gemm launches.  0 restores the default (about one
+ * second).  A wait that runs out records W4A16_ERR_TIMEOUT and the kernel
+ * winds down without trapping. */
+W4A16_API void w4a16_debug_set_wait_cycles(long long cycles);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

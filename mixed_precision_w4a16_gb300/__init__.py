@@ -1,0 +1,231 @@
+"""GB300 (sm_103a) W4A16 linear layer: thin Python binding of ``libw4a16.so``.
+
+Every function below marshals arguments (torch tensors or raw integer device
+pointers) into the C ABI declared in ``include/w4a16.h`` and checks the
+returned status; all of the work happens in the library's CUDA kernels.
+PyTorch only provides device memory and streams.
+
+There is no CPU fallback: the first call into the library fails loudly when it
+has not been built (``python -m mixed_precision_w4a16_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "W4A16Error", "lib", "Plan",
+    "w4a16_packed_bytes", "w4a16_scales_count", "w4a16_workspace_bytes", "w4a16_plan",
+    "w4a16_repack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm", "w4a16_get_status",
+    "w4a16_debug_set_wait_cycles", "w4a16_status_string", "EXPORTED_SYMBOLS",
+    "repack", "unpack", "dequant", "gemm", "workspace_for",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libw4a16.so")
+
+EXPORTED_SYMBOLS = (
+    "w4a16_status_string", "w4a16_abi_version", "w4a16_packed_bytes", "w4a16_scales_count",
+    "w4a16_workspace_bytes", "w4a16_repack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm",
+    "w4a16_get_status", "w4a16_plan", "w4a16_debug_set_wait_cycles",
+)
+
+
+class W4A16Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {w4a16_status_string(status)} ({status})")
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "path", "m_tiles", "m_chunk", "n_tile", "k_tile", "units", "units_per_cta", "grid",
+        "stages", "smem_bytes", "threads")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -m mixed_precision_w4a16_gb300.build` "
+            "(the W4A16 path has no CPU fallback)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    sig = {
+        "w4a16_status_string": (ctypes.c_char_p, [i]),
+        "w4a16_abi_version": (i, []),
+        "w4a16_packed_bytes": (sz, [i, i]),
+        "w4a16_scales_count": (sz, [i, i, i]),
+        "w4a16_workspace_bytes": (sz, [i, i, i, i]),
+        "w4a16_repack": (i, [vp, vp, i, i, i, vp, vp, vp]),
+        "w4a16_unpack": (i, [vp, vp, i, i, i, vp, vp, vp]),
+        "w4a16_dequant": (i, [vp, vp, i, i, i, vp, vp]),
+        "w4a16_gemm": (i, [vp, vp, vp, vp, i, i, i, i, vp, sz, vp]),
+        "w4a16_get_status": (i, [vp, vp]),
+        "w4a16_plan": (i, [i, i, i, i, i, ctypes.POINTER(Plan)]),
+        "w4a16_debug_set_wait_cycles": (None, [ctypes.c_longlong]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    return L
+
+
+_LIB = None
+
+
+def _lib():
+    """The loaded library (loaded on first use; raises ImportError when it was never built)."""
+    global _LIB
+    if _LIB is None:
+        _LIB = _load()
+    return _LIB
+
+
+def __getattr__(name):
+    if name == "lib":
+        return _lib()
+    raise AttributeError(name)
+
+
+# ---------------------------------------------------------------------------
+# argument marshalling
+# ---------------------------------------------------------------------------
+
+def _ptr(x):
+    """Device pointer of a torch tensor (must be contiguous), an int, or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        if hasattr(x, "is_contiguous") and not x.is_contiguous():
+            raise ValueError("W4A16 buffers must be contiguous")
+        return x.data_ptr()
+    raise TypeError(f"expected a tensor or an integer pointer, got {type(x)!r}")
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise W4A16Error(status, where)
+
+
+# ---------------------------------------------------------------------------
+# the C ABI, one Python function per entry point
+# ---------------------------------------------------------------------------
+
+def w4a16_status_string(status: int) -> str:
+    return _lib().w4a16_status_string(int(status)).decode()
+
+
+def w4a16_packed_bytes(K: int, N: int) -> int:
+    return int(_lib().w4a16_packed_bytes(K, N))
+
+
+def w4a16_scales_count(K: int, N: int, groupsize: int) -> int:
+    return int(_lib().w4a16_scales_count(K, N, groupsize))
+
+
+def w4a16_workspace_bytes(M: int, K: int, N: int, groupsize: int) -> int:
+    return int(_lib().w4a16_workspace_bytes(M, K, N, groupsize))
+
+
+def w4a16_plan(M: int, K: int, N: int, groupsize: int, num_sms: int = 0) -> dict:
+    p = Plan()
+    _check(_lib().w4a16_plan(M, K, N, groupsize, num_sms, ctypes.byref(p)), "w4a16_plan")
+    return p.as_dict()
+
+
+def w4a16_repack(q, s, K, N, groupsize, packed, scales_p, stream=None):
+    _check(_lib().w4a16_repack(_ptr(q), _ptr(s), K, N, groupsize, _ptr(packed), _ptr(scales_p), _stream(stream)),
+           "w4a16_repack")
+
+
+def w4a16_unpack(packed, scales_p, K, N, groupsize, q, s, stream=None):
+    _check(_lib().w4a16_unpack(_ptr(packed), _ptr(scales_p), K, N, groupsize, _ptr(q), _ptr(s), _stream(stream)),
+           "w4a16_unpack")
+
+
+def w4a16_dequant(packed, scales_p, K, N, groupsize, bhat, stream=None):
+    _check(_lib().w4a16_dequant(_ptr(packed), _ptr(scales_p), K, N, groupsize, _ptr(bhat), _stream(stream)),
+           "w4a16_dequant")
+
+
+def w4a16_gemm(A, packed, scales_p, C, M, K, N, groupsize, workspace, workspace_bytes=None, stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib().w4a16_gemm(_ptr(A), _ptr(packed), _ptr(scales_p), _ptr(C), M, K, N, groupsize, _ptr(workspace),
+                          int(workspace_bytes), _stream(stream)), "w4a16_gemm")
+
+
+def w4a16_get_status(workspace=None, stream=None) -> int:
+    return int(_lib().w4a16_get_status(_ptr(workspace), _stream(stream)))
+
+
+def w4a16_debug_set_wait_cycles(cycles: int) -> None:
+    _lib().w4a16_debug_set_wait_cycles(int(cycles))
+
+
+# ---------------------------------------------------------------------------
+# conveniences: allocate outputs with torch, then call the entry points
+# ---------------------------------------------------------------------------
+
+def _group_rows(K: int, groupsize: int) -> int:
+    return 1 if groupsize in (-1, K) else K // groupsize
+
+
+def workspace_for(M: int, K: int, N: int, groupsize: int, device=None):
+    """A zeroed workspace tensor of w4a16_workspace_bytes(M, K, N, groupsize) bytes."""
+    import torch
+    nbytes = w4a16_workspace_bytes(M, K, N, groupsize)
+    if nbytes == 0:
+        raise W4A16Error(2, "w4a16_workspace_bytes")
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def repack(q, s, groupsize: int, stream=None):
+    """q uint8[K][N], s fp16[K/G][N] (CUDA tensors) -> (packed int32[K*N/8], permuted fp16[K/G][N])."""
+    import torch
+    K, N = q.shape
+    packed = torch.empty(K * N // 8, dtype=torch.int32, device=q.device)
+    sp = torch.empty_like(s)
+    w4a16_repack(q, s, K, N, groupsize, packed, sp, stream)
+    return packed, sp
+
+
+def unpack(packed, scales_p, K: int, N: int, groupsize: int, stream=None):
+    import torch
+    q = torch.empty((K, N), dtype=torch.uint8, device=packed.device)
+    s = torch.empty((_group_rows(K, groupsize), N), dtype=torch.float16, device=packed.device)
+    w4a16_unpack(packed, scales_p, K, N, groupsize, q, s, stream)
+    return q, s
+
+
+def dequant(packed, scales_p, K: int, N: int, groupsize: int, stream=None):
+    import torch
+    bhat = torch.empty((K, N), dtype=torch.float16, device=packed.device)
+    w4a16_dequant(packed, scales_p, K, N, groupsize, bhat, stream)
+    return bhat
+
+
+def gemm(A, packed, scales_p, N: int, groupsize: int, workspace=None, out=None, stream=None):
+    """C fp16[M][N] = A fp16[M][K] * dequant(packed, scales_p)."""
+    import torch
+    M, K = A.shape
+    if workspace is None:
+        workspace = workspace_for(M, K, N, groupsize, A.device)
+    C = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=A.device)
+    w4a16_gemm(A, packed, scales_p, C, M, K, N, groupsize, workspace, None, stream)
+    return C

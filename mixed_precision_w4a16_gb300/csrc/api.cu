@@ -1,0 +1,312 @@
+// C ABI of the W4A16 library: argument checks, work planning, launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/w4a16.h"
+#include "internal.h"
+
+namespace {
+
+using namespace w4a16;
+
+constexpr int kMaxDevices = 64;
+constexpr long long kDefaultWaitCycles = 2000000000LL;  // ~1 s at GB300 clocks
+constexpr size_t kStatusBytes = 256;
+
+std::atomic<long long> g_wait_cycles{0};
+
+struct DeviceInfo {
+  int ready = 0;
+  int major = 0, minor = 0;
+  int sms = 0;
+  int smem_optin = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+int current_device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return W4A16_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return W4A16_ERR_CUDA;
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return W4A16_ERR_CUDA;
+    d.ready = 1;
+  }
+  *out = &d;
+  return (d.major == 10 && d.minor == 3) ? W4A16_OK : W4A16_ERR_ARCH;
+}
+
+int effective_group(int K, int groupsize) {
+  if (groupsize == -1 || groupsize == K) return K;
+  if (groupsize == 128) return 128;
+  return 0;
+}
+
+int check_shape(int K, int N, int groupsize) {
+  if (K <= 0 || N <= 0 || K % 128 != 0 || N % 64 != 0) return W4A16_ERR_SHAPE;
+  const int G = effective_group(K, groupsize);
+  if (G == 0 || K % G != 0) return W4A16_ERR_GROUP;
+  return W4A16_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Plan of the streaming kernel for (M, K, N) over `sms` SMs with `smem_optin` bytes of shared memory.
+struct Plan {
+  MmaConfig cfg;
+  int m_chunk;
+  int KU, ntiles, units, T, grid;
+  size_t workspace;
+};
+
+Plan make_plan(int M, int K, int N, int sms, int smem_optin) {
+  Plan pl{};
+  const int mc = std::min(std::max(M, 1), 64);
+  const int mt = mc <= 8 ? 1 : mc <= 16 ? 2 : mc <= 32 ? 4 : 8;
+  const int pref = mt <= 2 ? 4 : mt == 4 ? 2 : 1;  // instantiated (m_tiles, nbw) pairs
+  const int KU = K / kKTile;
+  int nbw = pref;
+  for (; nbw > 1; nbw /= 2) {
+    const int nt = 64 * nbw;
+    if (N % nt != 0) continue;
+    if (static_cast<long long>(N / nt) * KU >= 2LL * sms) break;
+  }
+  const int NT = 64 * nbw;
+  const int fixed = mma_smem_bytes(mt, nbw, 0);
+  const int per_stage = mma_stage_bytes(mt, nbw) + 16;
+  int stages = (smem_optin - fixed) / per_stage;
+  stages = std::max(2, std::min(stages, 12));
+  pl.cfg.m_tiles = mt;
+  pl.cfg.nbw = nbw;
+  pl.cfg.n_tile = NT;
+  pl.cfg.stages = stages;
+  pl.cfg.smem_bytes = mma_smem_bytes(mt, nbw, stages);
+  pl.cfg.threads = kMmaThreads;
+  pl.m_chunk = 8 * mt;
+  pl.KU = KU;
+  pl.ntiles = N / NT;
+  pl.units = pl.ntiles * KU;
+  pl.T = (pl.units + sms - 1) / sms;
+  pl.grid = (pl.units + pl.T - 1) / pl.T;
+  const size_t counters = (static_cast<size_t>(pl.ntiles) * 4 + 255) / 256 * 256;
+  const size_t slots = 2ull * pl.grid * NT * (8 * mt) * sizeof(float);
+  pl.workspace = kStatusBytes + counters + slots;
+  return pl;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D map over A (fp16[M][K]); boxes of 64 columns x box_rows rows, 128-byte swizzle, zero fill.
+int encode_a_map(CUtensorMap* map, const uint16_t* A, int M, int K, int box_rows) {
+  auto enc = get_encoder();
+  if (!enc) return W4A16_ERR_CUDA;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(A), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* w4a16_status_string(int status) {
+  switch (status) {
+    case W4A16_OK: return "W4A16_OK";
+    case W4A16_ERR_NULL: return "W4A16_ERR_NULL";
+    case W4A16_ERR_SHAPE: return "W4A16_ERR_SHAPE";
+    case W4A16_ERR_GROUP: return "W4A16_ERR_GROUP";
+    case W4A16_ERR_CODE_RANGE: return "W4A16_ERR_CODE_RANGE";
+    case W4A16_ERR_WORKSPACE: return "W4A16_ERR_WORKSPACE";
+    case W4A16_ERR_CUDA: return "W4A16_ERR_CUDA";
+    case W4A16_ERR_TIMEOUT: return "W4A16_ERR_TIMEOUT";
+    case W4A16_ERR_ARCH: return "W4A16_ERR_ARCH";
+    case W4A16_ERR_ALIGN: return "W4A16_ERR_ALIGN";
+    default: return "W4A16_ERR_UNKNOWN";
+  }
+}
+
+int w4a16_abi_version(void) { return 1; }
+
+size_t w4a16_packed_bytes(int K, int N) {
+  if (K <= 0 || N <= 0 || K % 128 != 0 || N % 64 != 0) return 0;
+  return static_cast<size_t>(K) * static_cast<size_t>(N) / 2;
+}
+
+size_t w4a16_scales_count(int K, int N, int groupsize) {
+  if (check_shape(K, N, groupsize) != W4A16_OK) return 0;
+  return static_cast<size_t>(K / effective_group(K, groupsize)) * static_cast<size_t>(N);
+}
+
+int w4a16_plan(int M, int K, int N, int groupsize, int num_sms, w4a16_plan_t* out) {
+  if (!out) return W4A16_ERR_NULL;
+  if (M < 0) return W4A16_ERR_SHAPE;
+  const int st = check_shape(K, N, groupsize);
+  if (st != W4A16_OK) return st;
+  int sms = num_sms;
+  int smem = 232448;  // sm_100-class opt-in shared memory per block
+  if (sms <= 0) {
+    DeviceInfo* d = nullptr;
+    const int r = current_device_info(&d);
+    if (r != W4A16_OK) return r;
+    sms = d->sms;
+    smem = d->smem_optin;
+  }
+  const Plan pl = make_plan(M, K, N, sms, smem);
+  out->path = 1;
+  out->m_tiles = pl.cfg.m_tiles;
+  out->m_chunk = pl.m_chunk;
+  out->n_tile = pl.cfg.n_tile;
+  out->k_tile = kKTile;
+  out->units = pl.units;
+  out->units_per_cta = pl.T;
+  out->grid = pl.grid;
+  out->stages = pl.cfg.stages;
+  out->smem_bytes = pl.cfg.smem_bytes;
+  out->threads = pl.cfg.threads;
+  return W4A16_OK;
+}
+
+size_t w4a16_workspace_bytes(int M, int K, int N, int groupsize) {
+  if (M < 0 || check_shape(K, N, groupsize) != W4A16_OK) return 0;
+  DeviceInfo* d = nullptr;
+  if (current_device_info(&d) != W4A16_OK) return 0;
+  return make_plan(M, K, N, d->sms, d->smem_optin).workspace;
+}
+
+void w4a16_debug_set_wait_cycles(long long cycles) { g_wait_cycles.store(cycles > 0 ? cycles : 0); }
+
+int w4a16_repack(const uint8_t* q, const uint16_t* s, int K, int N, int groupsize, uint32_t* packed,
+                 uint16_t* scales_p, void* stream) {
+  const int st = check_shape(K, N, groupsize);
+  if (st != W4A16_OK) return st;
+  if (!q || !s || !packed || !scales_p) return W4A16_ERR_NULL;
+  if (!aligned16(q) || !aligned16(s) || !aligned16(packed) || !aligned16(scales_p)) return W4A16_ERR_ALIGN;
+  DeviceInfo* d = nullptr;
+  const int r = current_device_info(&d);
+  if (r != W4A16_OK) return r;
+  const cudaError_t e = launch_repack(q, s, K, N, effective_group(K, groupsize), packed, scales_p,
+                                      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
+int w4a16_unpack(const uint32_t* packed, const uint16_t* scales_p, int K, int N, int groupsize, uint8_t* q,
+                 uint16_t* s, void* stream) {
+  const int st = check_shape(K, N, groupsize);
+  if (st != W4A16_OK) return st;
+  if (!q || !s || !packed || !scales_p) return W4A16_ERR_NULL;
+  if (!aligned16(q) || !aligned16(s) || !aligned16(packed) || !aligned16(scales_p)) return W4A16_ERR_ALIGN;
+  DeviceInfo* d = nullptr;
+  const int r = current_device_info(&d);
+  if (r != W4A16_OK) return r;
+  const cudaError_t e = launch_unpack(packed, scales_p, K, N, effective_group(K, groupsize), q, s,
+                                      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
+int w4a16_dequant(const uint32_t* packed, const uint16_t* scales_p, int K, int N, int groupsize, uint16_t* Bhat,
+                  void* stream) {
+  const int st = check_shape(K, N, groupsize);
+  if (st != W4A16_OK) return st;
+  if (!packed || !scales_p || !Bhat) return W4A16_ERR_NULL;
+  if (!aligned16(packed) || !aligned16(scales_p) || !aligned16(Bhat)) return W4A16_ERR_ALIGN;
+  DeviceInfo* d = nullptr;
+  const int r = current_device_info(&d);
+  if (r != W4A16_OK) return r;
+  const cudaError_t e = launch_dequant(packed, scales_p, K, N, effective_group(K, groupsize), Bhat,
+                                       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
+int w4a16_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* scales_p, uint16_t* C, int M, int K, int N,
+               int groupsize, void* workspace, size_t workspace_bytes, void* stream) {
+  if (M < 0) return W4A16_ERR_SHAPE;
+  const int st = check_shape(K, N, groupsize);
+  if (st != W4A16_OK) return st;
+  if (M == 0) return W4A16_OK;
+  if (!A || !packed || !scales_p || !C) return W4A16_ERR_NULL;
+  if (!workspace) return W4A16_ERR_WORKSPACE;
+  if (!aligned16(A) || !aligned16(packed) || !aligned16(scales_p) || !aligned16(C) || !aligned16(workspace))
+    return W4A16_ERR_ALIGN;
+  DeviceInfo* d = nullptr;
+  const int r = current_device_info(&d);
+  if (r != W4A16_OK) return r;
+  const Plan pl = make_plan(M, K, N, d->sms, d->smem_optin);
+  if (workspace_bytes < pl.workspace) return W4A16_ERR_WORKSPACE;
+
+  CUtensorMap map;
+  const int er = encode_a_map(&map, A, M, K, pl.m_chunk);
+  if (er != W4A16_OK) return er;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  GemmParams p{};
+  p.packed = packed;
+  p.scales = scales_p;
+  p.C = C;
+  p.status = reinterpret_cast<uint32_t*>(ws);
+  p.counters = reinterpret_cast<uint32_t*>(ws + kStatusBytes);
+  p.slots = reinterpret_cast<float*>(ws + kStatusBytes + (static_cast<size_t>(pl.ntiles) * 4 + 255) / 256 * 256);
+  p.M = M;
+  p.K = K;
+  p.N = N;
+  p.G = effective_group(K, groupsize);
+  p.KU = pl.KU;
+  p.units = pl.units;
+  p.T = pl.T;
+  p.grid = pl.grid;
+  p.stages = pl.cfg.stages;
+  const long long wc = g_wait_cycles.load();
+  p.wait_limit = wc > 0 ? wc : kDefaultWaitCycles;
+  for (int m0 = 0; m0 < M; m0 += pl.m_chunk) {
+    p.m0 = m0;
+    const cudaError_t e = launch_gemm_mma(pl.cfg, map, p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return W4A16_ERR_CUDA;
+  }
+  return W4A16_OK;
+}
+
+int w4a16_get_status(void* workspace, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return W4A16_ERR_CUDA;
+  unsigned int flag = 0;
+  if (read_and_clear_repack_flag(&flag, s) != cudaSuccess) return W4A16_ERR_CUDA;
+  uint32_t word = 0;
+  if (workspace) {
+    if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return W4A16_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return W4A16_ERR_CUDA;
+    if (word && cudaMemsetAsync(workspace, 0, sizeof(word), s) != cudaSuccess) return W4A16_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return W4A16_ERR_CUDA;
+  }
+  if (flag & kDevErrCodeRange) return W4A16_ERR_CODE_RANGE;
+  if (word & kDevErrTimeout) return W4A16_ERR_TIMEOUT;
+  if (word) return W4A16_ERR_CUDA;
+  return W4A16_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,189 @@
+// Offline repack of 4-bit codes and FP16 scales into the GEMM's fragment
+// order, plus the two diagnostic inverses (unpack, dequantise).
+//
+// Layout (see include/w4a16.h): packed uint32[N/16][K/64][32][4]; word j of
+// lane L in tile (nb, kb) is L's operand fragment of the 16x16 block with
+// output columns nb*16.. and reduction rows kb*64 + 16j ..; nibble slot
+// i < 4 / i + 4 = low / high half of fragment register i.  Register i holds
+// fragment row g + 8*(i & 1) and columns 2t + 8*(i >> 1) + {0, 1}, with
+// g = L / 4 and t = L % 4 (PTX ISA, mma.m16n8k16 A-operand fragment).
+//
+// Kernels here walk the layout from the word side (word -> positions); one
+// thread owns one lane's 16-byte vector (four words), so every store of the
+// packed stream is a coalesced 16-byte store.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace w4a16 {
+
+// Repack error flag (code-range violations), read and cleared by w4a16_get_status.
+__device__ unsigned int g_repack_flag;
+
+namespace {
+
+struct VecCoord {
+  int nb, kb, lane;
+};
+
+__device__ __forceinline__ VecCoord vec_coord(long long v, int K) {
+  const int kTiles = K / 64;
+  VecCoord c;
+  c.lane = static_cast<int>(v & 31);
+  const long long tile = v >> 5;
+  c.kb = static_cast<int>(tile % kTiles);
+  c.nb = static_cast<int>(tile / kTiles);
+  return c;
+}
+
+// (row, column) inside the 16x16 block of nibble slot `slot` for lane (g, t)
+__device__ __forceinline__ void slot_rc(int slot, int g, int t, int& r, int& c) {
+  const int reg = slot & 3, e = slot >> 2;
+  r = g + 8 * (reg & 1);
+  c = 2 * t + e + 8 * (reg >> 1);
+}
+
+__global__ void repack_codes_kernel(const uint8_t* __restrict__ q, int K, int N, uint4* __restrict__ packed,
+                                    long long nvec) {
+  const long long v = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (v >= nvec) return;
+  const VecCoord vc = vec_coord(v, K);
+  const int g = vc.lane >> 2, t = vc.lane & 3;
+  uint32_t words[4];
+  uint32_t bad = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t w = 0;
+#pragma unroll
+    for (int slot = 0; slot < 8; ++slot) {
+      int r, c;
+      slot_rc(slot, g, t, r, c);
+      const long long k = vc.kb * 64LL + 16 * j + c;
+      const long long n = vc.nb * 16LL + r;
+      const uint32_t code = q[k * N + n];
+      bad |= code > 15u;
+      w |= (code & 15u) << (4 * slot);
+    }
+    words[j] = w;
+  }
+  if (bad) atomicOr(&g_repack_flag, kDevErrCodeRange);
+  packed[v] = make_uint4(words[0], words[1], words[2], words[3]);
+}
+
+// permuted position p inside a 16-column block -> fragment row r
+__device__ __forceinline__ int perm_row(int p) { return (p >> 1) + 8 * (p & 1); }
+
+__global__ void permute_scales_kernel(const uint16_t* __restrict__ s, uint16_t* __restrict__ sp, int N,
+                                      long long count, int inverse) {
+  const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (i >= count) return;
+  const long long row = i / N;
+  const int p = static_cast<int>(i % N);
+  const int src_col = (p & ~15) + perm_row(p & 15);
+  if (!inverse)
+    sp[row * N + p] = s[row * N + src_col];  // forward: natural -> permuted
+  else
+    sp[row * N + src_col] = s[row * N + p];  // inverse: permuted -> natural
+}
+
+__global__ void unpack_codes_kernel(const uint4* __restrict__ packed, int K, int N, uint8_t* __restrict__ q,
+                                    long long nvec) {
+  const long long v = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (v >= nvec) return;
+  const VecCoord vc = vec_coord(v, K);
+  const int g = vc.lane >> 2, t = vc.lane & 3;
+  const uint4 pv = packed[v];
+  const uint32_t words[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int slot = 0; slot < 8; ++slot) {
+      int r, c;
+      slot_rc(slot, g, t, r, c);
+      const long long k = vc.kb * 64LL + 16 * j + c;
+      const long long n = vc.nb * 16LL + r;
+      q[k * N + n] = static_cast<uint8_t>((words[j] >> (4 * slot)) & 15u);
+    }
+  }
+}
+
+// Bhat[k][n] = RNE(s * (q - 8)): the exact decode of the GEMM, then one FP16 multiply.
+__global__ void dequant_kernel(const uint4* __restrict__ packed, const uint16_t* __restrict__ sp, int K, int N,
+                               int G, uint16_t* __restrict__ bhat, long long nvec) {
+  const long long v = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (v >= nvec) return;
+  const VecCoord vc = vec_coord(v, K);
+  const int g = vc.lane >> 2, t = vc.lane & 3;
+  const int grp = (vc.kb * 64) / G;  // G is a multiple of 64: one group per 64-row tile
+  const uint32_t spair = *reinterpret_cast<const uint32_t*>(sp + static_cast<long long>(grp) * N + vc.nb * 16 + 2 * g);
+  const uint32_t s_row_g = (spair & 0xffffu) * 0x10001u;      // scale of fragment row g, both halves
+  const uint32_t s_row_g8 = (spair >> 16) * 0x10001u;         // scale of fragment row g + 8
+  const uint4 pv = packed[v];
+  const uint32_t words[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t a[4];
+    decode8(words[j], a);
+#pragma unroll
+    for (int reg = 0; reg < 4; ++reg) {
+      const uint32_t h = hmul2_u32(a[reg], (reg & 1) ? s_row_g8 : s_row_g);
+      const long long n = vc.nb * 16LL + g + 8 * (reg & 1);
+      const long long k = vc.kb * 64LL + 16 * j + 2 * t + 8 * (reg >> 1);
+      bhat[k * N + n] = static_cast<uint16_t>(h & 0xffffu);
+      bhat[(k + 1) * N + n] = static_cast<uint16_t>(h >> 16);
+    }
+  }
+}
+
+inline unsigned grid_for(long long n, int block) { return static_cast<unsigned>((n + block - 1) / block); }
+
+}  // namespace
+
+cudaError_t launch_repack(const uint8_t* q, const uint16_t* s, int K, int N, int G, uint32_t* packed,
+                          uint16_t* scales_p, cudaStream_t stream) {
+  const long long nvec = static_cast<long long>(K) * N / 32;
+  repack_codes_kernel<<<grid_for(nvec, 256), 256, 0, stream>>>(q, K, N, reinterpret_cast<uint4*>(packed), nvec);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long ns = static_cast<long long>(K / G) * N;
+  permute_scales_kernel<<<grid_for(ns, 256), 256, 0, stream>>>(s, scales_p, N, ns, 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpack(const uint32_t* packed, const uint16_t* scales_p, int K, int N, int G, uint8_t* q,
+                          uint16_t* s, cudaStream_t stream) {
+  const long long nvec = static_cast<long long>(K) * N / 32;
+  unpack_codes_kernel<<<grid_for(nvec, 256), 256, 0, stream>>>(reinterpret_cast<const uint4*>(packed), K, N, q,
+                                                                nvec);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long ns = static_cast<long long>(K / G) * N;
+  permute_scales_kernel<<<grid_for(ns, 256), 256, 0, stream>>>(scales_p, s, N, ns, 1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const uint32_t* packed, const uint16_t* scales_p, int K, int N, int G, uint16_t* bhat,
+                           cudaStream_t stream) {
+  const long long nvec = static_cast<long long>(K) * N / 32;
+  dequant_kernel<<<grid_for(nvec, 256), 256, 0, stream>>>(reinterpret_cast<const uint4*>(packed), scales_p, K, N,
+                                                           G, bhat, nvec);
+  return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_repack_flag(unsigned int* flag, cudaStream_t stream) {
+  cudaError_t e = cudaMemcpyFromSymbolAsync(flag, g_repack_flag, sizeof(unsigned int), 0, cudaMemcpyDeviceToHost,
+                                            stream);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return e;
+  if (*flag) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_repack_flag, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(stream);
+  }
+  return e;
+}
+
+}  // namespace w4a16

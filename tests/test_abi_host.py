@@ -1,0 +1,131 @@
+"""Host-side checks of the C ABI (no GPU): the library builds, loads, exports
+every entry point the header declares, and its pure host logic (sizes, work
+plan, argument validation) behaves as documented."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4a16.h")
+
+
+@pytest.fixture(scope="module")
+def w():
+    from mixed_precision_w4a16_gb300 import build
+    build.build()
+    import mixed_precision_w4a16_gb300 as w
+    return w
+
+
+def _declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"W4A16_API\s+[\w\s\*]+?\b(w4a16_\w+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    syms = _declared_symbols()
+    for name in ("w4a16_repack", "w4a16_gemm", "w4a16_workspace_bytes", "w4a16_get_status"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(w):
+    lib = ctypes.CDLL(w.LIB_PATH)
+    for name in _declared_symbols():
+        assert hasattr(lib, name), name
+    assert set(_declared_symbols()) <= set(w.EXPORTED_SYMBOLS) | {"w4a16_abi_version"}
+
+
+def test_library_exports_nothing_else(w):
+    # -fvisibility=hidden: only the declared C entry points are dynamic symbols
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", w.LIB_PATH], capture_output=True, text=True).stdout
+    ours = sorted(l.split()[-1] for l in out.splitlines() if " T " in l and "w4a16" in l)
+    assert ours == _declared_symbols()
+
+
+def test_sizes(w):
+    assert w.w4a16_packed_bytes(4096, 12288) == 4096 * 12288 // 2
+    assert w.w4a16_scales_count(4096, 12288, 128) == 32 * 12288
+    assert w.w4a16_scales_count(4096, 12288, -1) == 12288
+    assert w.w4a16_scales_count(4096, 12288, 4096) == 12288
+    assert w.w4a16_packed_bytes(100, 64) == 0
+    assert w.w4a16_scales_count(1024, 96, 128) == 0      # N % 64
+    assert w.w4a16_scales_count(1024, 128, 64) == 0      # unsupported group size
+
+
+def test_status_strings(w):
+    assert w.w4a16_status_string(0) == "W4A16_OK"
+    assert w.w4a16_status_string(7) == "W4A16_ERR_TIMEOUT"
+    assert w.w4a16_status_string(99) == "W4A16_ERR_UNKNOWN"
+
+
+SHAPES = [(1, 1024, 1024), (16, 1024, 1024), (16, 4096, 12288), (1, 11008, 4096), (32, 8192, 57344),
+          (64, 18432, 73728), (16, 18432, 73728), (100, 4096, 4096), (3, 128, 64), (40, 256, 192)]
+
+
+@pytest.mark.parametrize("M,K,N", SHAPES)
+def test_plan_stripes_cover_every_unit_once(w, M, K, N):
+    for sms in (152, 148, 7):
+        p = w.w4a16_plan(M, K, N, 128, sms)
+        assert p["k_tile"] == 128 and N % p["n_tile"] == 0
+        KU = K // 128
+        assert p["units"] == (N // p["n_tile"]) * KU
+        T, grid, U = p["units_per_cta"], p["grid"], p["units"]
+        assert grid <= sms and grid * T >= U and (grid - 1) * T < U
+        assert p["m_chunk"] == 8 * p["m_tiles"] and p["m_chunk"] >= min(M, 64)
+        assert p["smem_bytes"] <= 232448 and p["stages"] >= 2
+        # every unit belongs to exactly one CTA; every CTA has work
+        owner = [u // T for u in range(U)]
+        assert owner[-1] == grid - 1
+        # split column tiles: the partial-sum slot (cta, first-or-later) is unique
+        slots = set()
+        for j in range(U // KU):
+            c_first, c_last = (j * KU) // T, min(((j + 1) * KU - 1) // T, grid - 1)
+            assert c_first == owner[j * KU] and c_last == owner[(j + 1) * KU - 1]
+            if c_first == c_last:
+                continue
+            for c in range(c_first, c_last + 1):
+                slot = 2 * c if j == (c * T) // KU else 2 * c + 1
+                assert slot not in slots
+                slots.add(slot)
+        assert all(s < 2 * grid for s in slots)
+
+
+def test_plan_token_tiles(w):
+    assert [w.w4a16_plan(m, 1024, 1024, 128, 152)["m_tiles"] for m in (1, 8, 9, 16, 17, 32, 33, 64, 1000)] == \
+        [1, 1, 2, 2, 4, 4, 8, 8, 8]
+
+
+def test_plan_rejects_bad_shapes(w):
+    with pytest.raises(w.W4A16Error):
+        w.w4a16_plan(16, 1000, 1024, 128, 152)
+    with pytest.raises(w.W4A16Error):
+        w.w4a16_plan(16, 1024, 1000, 128, 152)
+    with pytest.raises(w.W4A16Error):
+        w.w4a16_plan(16, 1024, 1024, 32, 152)
+
+
+def test_gemm_validates_before_touching_the_device(w):
+    L = w.lib
+    # bad shapes, bad group, null pointers: rejected on the host with the documented codes
+    assert L.w4a16_gemm(16, 16, 16, 16, 4, 1000, 1024, 128, 16, 1 << 20, None) == 2
+    assert L.w4a16_gemm(16, 16, 16, 16, 4, 1024, 1024, 96, 16, 1 << 20, None) == 3
+    assert L.w4a16_gemm(None, 16, 16, 16, 4, 1024, 1024, 128, 16, 1 << 20, None) == 1
+    assert L.w4a16_gemm(16, 16, 16, 16, 4, 1024, 1024, 128, None, 1 << 20, None) == 5
+    assert L.w4a16_gemm(16, 16, 16, 16, -1, 1024, 1024, 128, 16, 1 << 20, None) == 2
+    # M == 0 is a no-op
+    assert L.w4a16_gemm(None, None, None, None, 0, 1024, 1024, 128, None, 0, None) == 0
+    assert L.w4a16_repack(None, 16, 1024, 1024, 128, 16, 16, None) == 1
+    assert L.w4a16_repack(16, 16, 1024, 1024, 100, 16, 16, None) == 3
+
+
+def test_entry_points_report_missing_gpu(w):
+    # On a machine without a GPU the device query fails: an error code, not a crash.
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    L = w.lib
+    assert L.w4a16_gemm(16, 16, 16, 16, 4, 1024, 1024, 128, 16, 1 << 20, None) == 6
+    assert L.w4a16_workspace_bytes(16, 1024, 1024, 128) == 0

@@ -1,0 +1,60 @@
+"""Parity at the benchmarked sizes, in the launch configuration bench.py times.
+
+The oracle computes a sample of output columns (all M rows x the first and
+last 256 columns and 2048 seeded random ones); columns are independent, so
+this is an element-by-element check of those outputs."""
+import numpy as np
+import pytest
+
+import oracle
+from mixed_precision_w4a16_gb300 import synth
+import w4a16_testlib as tl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def w():
+    return tl.lib()
+
+
+def sample_cols(N, seed=0):
+    rng = np.random.default_rng(seed)
+    cols = np.concatenate([np.arange(min(256, N)), np.arange(max(0, N - 256), N), rng.choice(N, min(2048, N), False)])
+    return np.unique(cols)
+
+
+def check_layer(w, K, N, G, Ms, seed):
+    q, s = synth.make_weights(K, N, G, seed)
+    _, _, packed, sp = tl.device_layer(w, q, s, G)
+    cols = sample_cols(N, seed)
+    qc, sc = np.ascontiguousarray(q[:, cols]), np.ascontiguousarray(s[:, cols])
+    del q
+    ws = w.workspace_for(max(Ms), K, N, G)
+    for M in Ms:
+        ws_need = w.w4a16_workspace_bytes(M, K, N, G)
+        assert ws_need <= ws.numel()
+        A = synth.make_activations(M, K, seed * 1000 + M)
+        C = tl.c_numpy(tl.run_gemm(w, A, packed, sp, N, G, workspace=ws))
+        C_ref, bound = oracle.gemm_ref(A, qc, sc, G)
+        tl.assert_within_bound(C[:, cols], C_ref, bound, f"K={K} N={N} G={G} M={M}")
+    assert w.w4a16_get_status(ws) == 0
+
+
+def test_big_layer_sweep(w):
+    check_layer(w, 18432, 73728, 128, [1, 2, 4, 8, 16, 32, 64, 128], seed=200)
+
+
+@pytest.mark.parametrize("K,N", [(4096, 12288), (4096, 4096), (4096, 22016), (11008, 4096)])
+def test_7b_decode_layers(w, K, N):
+    check_layer(w, K, N, 128, [1, 16], seed=100 + K % 97)
+
+
+@pytest.mark.parametrize("K,N", [(8192, 10240), (8192, 8192), (8192, 57344), (28672, 8192)])
+@pytest.mark.parametrize("G", [128, -1])
+def test_70b_layers(w, K, N, G):
+    check_layer(w, K, N, G, [32], seed=300 + N % 89)
+
+
+def test_prefill_layer(w):
+    check_layer(w, 8192, 28672, 128, [256, 512, 1024], seed=400)

@@ -1,0 +1,184 @@
+"""The fused W4A16 GEMM on the GPU against the CPU oracle.
+
+Bar: every element within |C - C_ref| <= 4e-3 * sum_k |A B^| + 1e-4; special
+cases that are exact in FP32/FP16 must match bit for bit; repeated calls must
+be bitwise identical (deterministic split-K reduction).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from mixed_precision_w4a16_gb300 import synth
+import w4a16_testlib as tl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def w():
+    return tl.lib()
+
+
+# token counts around every 8-row tile edge and the 64-row launch chunk
+M_EDGES = [1, 2, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 100, 128, 129]
+
+
+@pytest.mark.parametrize("M", M_EDGES)
+@pytest.mark.parametrize("G", [128, -1])
+def test_gemm_parity_small_layer(w, M, G):
+    K, N = 1024, 1024
+    A, q, s = tl.layer(M, K, N, G, seed=100 + M)
+    _, _, packed, sp = tl.device_layer(w, q, s, G)
+    C = tl.c_numpy(tl.run_gemm(w, A, packed, sp, N, G))
+    C_ref, bound = oracle.gemm_ref(A, q, s, G)
+    tl.assert_within_bound(C, C_ref, bound, f"M={M} G={G}")
+
+
+@pytest.mark.parametrize("M,K,N,G", [
+    (5, 128, 64, 128),          # one unit, one CTA
+    (16, 256, 192, 128),        # N not a multiple of 128: 64-wide tiles
+    (16, 384, 320, -1),         # K/128 odd, per-column scales
+    (3, 11008, 256, 128),       # long K: stripes split every column
+    (24, 2048, 8192, 128),      # many column tiles
+    (40, 4096, 640, -1),
+])
+def test_gemm_parity_shapes(w, M, K, N, G):
+    A, q, s = tl.layer(M, K, N, G, seed=M + K + N)
+    _, _, packed, sp = tl.device_layer(w, q, s, G)
+    C = tl.c_numpy(tl.run_gemm(w, A, packed, sp, N, G))
+    C_ref, bound = oracle.gemm_ref(A, q, s, G)
+    tl.assert_within_bound(C, C_ref, bound, f"{(M, K, N, G)}")
+
+
+@pytest.mark.parametrize("G", [128, -1])
+def test_identity_rows_return_dequantised_weights_exactly(w, G):
+    K, N = 2048, 512
+    q, s = synth.make_weights(K, N, G, seed=31)
+    rows = [0, 1, 63, 64, 127, 128, 1000, 2047, 5, 77, 1500, 640, 641, 1919, 300, 301, 999]
+    A = np.zeros((len(rows), K), np.float16)
+    for m, k in enumerate(rows):
+        A[m, k] = 1.0
+    _, _, packed, sp = tl.device_layer(w, q, s, G)
+    C = tl.c_numpy(tl.run_gemm(w, A, packed, sp, N, G))
+    ref = oracle.dequant_fp16_bits(q, s, G)[rows, :]
+    assert np.array_equal(C.view(np.uint16), ref)
+
+
+def test_integer_gemm_is_exact(w):
+    # s = 1, small integer activations: every partial sum is an exact FP32 integer below 2048
+    rng = np.random.default_rng(12)
+    M, K, N, G = 16, 256, 256, 128
+    A = rng.integers(-1, 2, (M, K)).astype(np.float16)
+    q = rng.integers(5, 12, (K, N)).astype(np.uint8)
+    s = np.ones((K // G, N), np.float16)
+    _, _, packed, sp = tl.device_layer(w, q, s, G)
+    C = tl.c_numpy(tl.run_gemm(w, A, packed, sp, N, G))
+    ref = A.astype(np.int64) @ (q.astype(np.int64) - 8)
+    assert np.abs(ref).max() < 2048
+    assert np.array_equal(C.astype(np.float64), ref.astype(np.float64))
+
+
+def test_zero_codes_give_zero(w):
+    M, K, N, G = 9, 1024, 512, 128
+    A, _, s = tl.layer(M, K, N, G, seed=3)
+    q = np.full((K, N), 8, np.uint8)
+    _, _, packed, sp = tl.device_layer(w, q, s, G)
+    C = tl.c_numpy(tl.run_gemm(w, A, packed, sp, N, G))
+    assert np.all(C.view(np.uint16) & 0x7FFF == 0)
+
+
+@pytest.mark.parametrize("M", [1, 16, 33])
+def test_repeated_calls_are_bitwise_identical(w, M):
+    torch = tl.torch_mod()
+    K, N, G = 4096, 2048, 128
+    A, q, s = tl.layer(M, K, N, G, seed=77)
+    _, _, packed, sp = tl.device_layer(w, q, s, G)
+    A_d = tl.to_dev(A)
+    ws = w.workspace_for(M, K, N, G)
+    outs = [tl.run_gemm(w, A_d, packed, sp, N, G, workspace=ws).clone() for _ in range(4)]
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    assert w.w4a16_get_status(ws) == 0
+
+
+def test_column_permutation_permutes_output(w):
+    # permuting the N columns of (q, s) permutes C's columns, bit for bit
+    M, K, N, G = 16, 2048, 512, 128
+    A, q, s = tl.layer(M, K, N, G, seed=8)
+    perm = np.random.default_rng(1).permutation(N)
+    _, _, p1, s1 = tl.device_layer(w, q, s, G)
+    _, _, p2, s2 = tl.device_layer(w, np.ascontiguousarray(q[:, perm]), np.ascontiguousarray(s[:, perm]), G)
+    C1 = tl.c_numpy(tl.run_gemm(w, A, p1, s1, N, G))
+    C2 = tl.c_numpy(tl.run_gemm(w, A, p2, s2, N, G))
+    assert np.array_equal(C1[:, perm].view(np.uint16), C2.view(np.uint16))
+
+
+def test_group_invariance(w):
+    # a scale constant over the groups of each column: group 128 and per-column agree within the bound
+    M, K, N = 16, 2048, 512
+    A, q, s1 = tl.layer(M, K, N, -1, seed=15)
+    s128 = np.repeat(s1, K // 128, axis=0)
+    _, _, pa, sa = tl.device_layer(w, q, s128, 128)
+    _, _, pb, sb = tl.device_layer(w, q, s1, -1)
+    Ca = tl.c_numpy(tl.run_gemm(w, A, pa, sa, N, 128))
+    Cb = tl.c_numpy(tl.run_gemm(w, A, pb, sb, N, -1))
+    C_ref, bound = oracle.gemm_ref(A, q, s1, -1)
+    tl.assert_within_bound(Ca, C_ref, bound, "G=128")
+    tl.assert_within_bound(Cb, C_ref, bound, "G=K")
+
+
+def test_workspace_reuse_across_shapes(w):
+    # counters are left at zero, so one zeroed workspace serves a sequence of calls
+    torch = tl.torch_mod()
+    big = max(w.w4a16_workspace_bytes(M, 4096, 4096, 128) for M in (1, 16, 32, 64))
+    ws = torch.zeros(big, dtype=torch.uint8, device="cuda")
+    for M, K, N in [(1, 4096, 4096), (16, 1024, 4096), (32, 4096, 1024), (64, 2048, 2048), (1, 4096, 4096)]:
+        A, q, s = tl.layer(M, K, N, 128, seed=M * 3 + K)
+        _, _, packed, sp = tl.device_layer(w, q, s, 128)
+        C = tl.c_numpy(tl.run_gemm(w, A, packed, sp, N, 128, workspace=ws))
+        C_ref, bound = oracle.gemm_ref(A, q, s, 128)
+        tl.assert_within_bound(C, C_ref, bound, f"{(M, K, N)}")
+    assert w.w4a16_get_status(ws) == 0
+
+
+def test_gemm_error_codes(w):
+    torch = tl.torch_mod()
+    M, K, N, G = 4, 1024, 512, 128
+    A, q, s = tl.layer(M, K, N, G, seed=2)
+    _, _, packed, sp = tl.device_layer(w, q, s, G)
+    A_d = tl.to_dev(A)
+    C = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    need = w.w4a16_workspace_bytes(M, K, N, G)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    with pytest.raises(w.W4A16Error) as e:
+        w.w4a16_gemm(A_d, packed, sp, C, M, K, N, G, ws, need - 1)
+    assert e.value.status == 5
+    with pytest.raises(w.W4A16Error) as e:
+        w.w4a16_gemm(A_d.data_ptr() + 2, packed, sp, C, M, K, N, G, ws)
+    assert e.value.status == 9
+    with pytest.raises(w.W4A16Error) as e:
+        w.w4a16_gemm(A_d, packed, sp, C, M, K, N, 256, ws)
+    assert e.value.status == 3
+    w.w4a16_gemm(A_d, packed, sp, C, 0, K, N, G, ws)  # M == 0: no-op
+
+
+def test_timeout_is_reported_and_context_survives(w):
+    # A pipeline wait bound of a few cycles makes the first wait give up: the kernel records
+    # W4A16_ERR_TIMEOUT and winds down without trapping; the context stays usable.
+    torch = tl.torch_mod()
+    M, K, N, G = 16, 4096, 4096, 128
+    A, q, s = tl.layer(M, K, N, G, seed=4)
+    _, _, packed, sp = tl.device_layer(w, q, s, G)
+    A_d = tl.to_dev(A)
+    ws = w.workspace_for(M, K, N, G)
+    try:
+        w.w4a16_debug_set_wait_cycles(1)
+        tl.run_gemm(w, A_d, packed, sp, N, G, workspace=ws)
+    finally:
+        w.w4a16_debug_set_wait_cycles(0)
+    assert w.w4a16_get_status(ws) == 7
+    ws.zero_()
+    C = tl.c_numpy(tl.run_gemm(w, A_d, packed, sp, N, G, workspace=ws))
+    C_ref, bound = oracle.gemm_ref(A, q, s, G)
+    tl.assert_within_bound(C, C_ref, bound, "after timeout")
+    assert w.w4a16_get_status(ws) == 0
