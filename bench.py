@@ -81,6 +81,7 @@ def parse_args():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="big")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only-m", type=int, default=None, help="run only this M of the sweep (profiling)")
     ap.add_argument("--cpu-sample", default=None, help=argparse.SUPPRESS)  # internal: oracle timing child
     return ap.parse_args()
 
@@ -215,6 +216,12 @@ def run_ours(args, rank, world, device):
 
     build.build()
     desc, layers, seed = WORKLOADS[args.workload]
+    if args.only_m is not None:
+        layers = [(K, N, G, [M for M in Ms if M == args.only_m]) for K, N, G, Ms in layers]
+        layers = [l for l in layers if l[3]]
+        if not layers:
+            raise SystemExit(f"M={args.only_m} is not part of workload {args.workload}")
+        desc += f" (only M={args.only_m})"
     peaks = load_peaks()
     stream = torch.cuda.current_stream()
 

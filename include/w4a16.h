@@ -171,6 +171,13 @@ W4A16_API int w4a16_plan(int M, int K, int N, int groupsize, int num_sms, w4a16_
  * winds down without trapping. */
 W4A16_API void w4a16_debug_set_wait_cycles(long long cycles);
 
+/* Failure-injection knob (not thread-safe): while enabled, w4a16_gemm launches
+ * leave the first pipeline stage of every CTA unfilled, so the consumers' first
+ * wait can only end by running out of its cycle bound.  The kernel then records
+ * W4A16_ERR_TIMEOUT, skips all output and returns; the CUDA context stays
+ * usable.  Used by the failure-detection tests; 0 disables it. */
+W4A16_API void w4a16_debug_inject_stall(int enable);
+
 #ifdef __cplusplus
 }
 #endif

@@ -17,7 +17,7 @@ __all__ = [
     "W4A16Error", "lib", "Plan",
     "w4a16_packed_bytes", "w4a16_scales_count", "w4a16_workspace_bytes", "w4a16_plan",
     "w4a16_repack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm", "w4a16_get_status",
-    "w4a16_debug_set_wait_cycles", "w4a16_status_string", "EXPORTED_SYMBOLS",
+    "w4a16_debug_set_wait_cycles", "w4a16_debug_inject_stall", "w4a16_status_string", "EXPORTED_SYMBOLS",
     "repack", "unpack", "dequant", "gemm", "workspace_for",
 ]
 
@@ -27,7 +27,7 @@ LIB_PATH = os.path.join(_PKG, "lib", "libw4a16.so")
 EXPORTED_SYMBOLS = (
     "w4a16_status_string", "w4a16_abi_version", "w4a16_packed_bytes", "w4a16_scales_count",
     "w4a16_workspace_bytes", "w4a16_repack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm",
-    "w4a16_get_status", "w4a16_plan", "w4a16_debug_set_wait_cycles",
+    "w4a16_get_status", "w4a16_plan", "w4a16_debug_set_wait_cycles", "w4a16_debug_inject_stall",
 )
 
 
@@ -66,6 +66,7 @@ def _load():
         "w4a16_get_status": (i, [vp, vp]),
         "w4a16_plan": (i, [i, i, i, i, i, ctypes.POINTER(Plan)]),
         "w4a16_debug_set_wait_cycles": (None, [ctypes.c_longlong]),
+        "w4a16_debug_inject_stall": (None, [i]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -176,6 +177,10 @@ def w4a16_get_status(workspace=None, stream=None) -> int:
 
 def w4a16_debug_set_wait_cycles(cycles: int) -> None:
     _lib().w4a16_debug_set_wait_cycles(int(cycles))
+
+
+def w4a16_debug_inject_stall(enable: bool) -> None:
+    _lib().w4a16_debug_inject_stall(1 if enable else 0)
 
 
 # ---------------------------------------------------------------------------

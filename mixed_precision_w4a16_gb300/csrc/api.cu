@@ -20,6 +20,7 @@ constexpr long long kDefaultWaitCycles = 2000000000LL;  // ~1 s at GB300 clocks
 constexpr size_t kStatusBytes = 256;
 
 std::atomic<long long> g_wait_cycles{0};
+std::atomic<int> g_stall{0};
 
 struct DeviceInfo {
   int ready = 0;
@@ -201,6 +202,8 @@ size_t w4a16_workspace_bytes(int M, int K, int N, int groupsize) {
 
 void w4a16_debug_set_wait_cycles(long long cycles) { g_wait_cycles.store(cycles > 0 ? cycles : 0); }
 
+void w4a16_debug_inject_stall(int enable) { g_stall.store(enable ? 1 : 0); }
+
 int w4a16_repack(const uint8_t* q, const uint16_t* s, int K, int N, int groupsize, uint32_t* packed,
                  uint16_t* scales_p, void* stream) {
   const int st = check_shape(K, N, groupsize);
@@ -282,6 +285,7 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* scales
   p.stages = pl.cfg.stages;
   const long long wc = g_wait_cycles.load();
   p.wait_limit = wc > 0 ? wc : kDefaultWaitCycles;
+  p.debug_stall = g_stall.load();
   for (int m0 = 0; m0 < M; m0 += pl.m_chunk) {
     p.m0 = m0;
     const cudaError_t e = launch_gemm_mma(pl.cfg, map, p, static_cast<cudaStream_t>(stream));

@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       const int kt = u - j * p.KU;
       const uint32_t st = sbase + s * L::STAGE;
       const uint32_t fb = bar_full + 8 * s;
+      if (p.debug_stall && it == 0) continue;  // leave stage 0 empty: nothing will complete its barrier
       if (lane == 0) mbar_arrive_expect_tx(fb, L::TX);
       __syncwarp();
       if (lane < NT / 16) {
@@ -141,7 +142,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     named_bar_sync(3, kMmaThreads);
     // After a timeout, make sure no copy is still landing in shared memory.
     if (*abort_flag && lane == 0) {
-      for (int it = (issued > S ? issued - S : 0); it < issued; ++it)
+      const int first_filled = p.debug_stall ? 1 : 0;
+      for (int it = max(first_filled, issued - S); it < issued; ++it)
         mbar_wait_bounded(bar_full + 8 * (it % S), (it / S) & 1, kDrainCycles, zero_flag);
     }
     return;

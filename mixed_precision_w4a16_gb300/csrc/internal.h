@@ -30,6 +30,7 @@ struct GemmParams {
   int grid;                 // CTAs
   int stages;               // pipeline depth
   long long wait_limit;     // clock cycles a pipeline wait may take
+  int debug_stall;          // 1: never fill the first stage (failure-detection test)
 };
 
 struct MmaConfig {

@@ -163,20 +163,25 @@ def test_gemm_error_codes(w):
 
 
 def test_timeout_is_reported_and_context_survives(w):
-    # A pipeline wait bound of a few cycles makes the first wait give up: the kernel records
-    # W4A16_ERR_TIMEOUT and winds down without trapping; the context stays usable.
+    # Failure injection on the host side of the wait: the first stage of every CTA is never
+    # filled, so the consumers' first wait can only end by running out of its (short) bound.
+    # The kernel records W4A16_ERR_TIMEOUT, writes nothing and returns; the context stays usable.
     torch = tl.torch_mod()
     M, K, N, G = 16, 4096, 4096, 128
     A, q, s = tl.layer(M, K, N, G, seed=4)
     _, _, packed, sp = tl.device_layer(w, q, s, G)
     A_d = tl.to_dev(A)
     ws = w.workspace_for(M, K, N, G)
+    C = torch.full((M, N), 7.0, dtype=torch.float16, device="cuda")
     try:
-        w.w4a16_debug_set_wait_cycles(1)
-        tl.run_gemm(w, A_d, packed, sp, N, G, workspace=ws)
+        w.w4a16_debug_set_wait_cycles(2_000_000)  # about a millisecond
+        w.w4a16_debug_inject_stall(True)
+        w.w4a16_gemm(A_d, packed, sp, C, M, K, N, G, ws)
     finally:
+        w.w4a16_debug_inject_stall(False)
         w.w4a16_debug_set_wait_cycles(0)
     assert w.w4a16_get_status(ws) == 7
+    assert torch.all(C == 7.0)  # nothing written after the abort
     ws.zero_()
     C = tl.c_numpy(tl.run_gemm(w, A_d, packed, sp, N, G, workspace=ws))
     C_ref, bound = oracle.gemm_ref(A, q, s, G)
