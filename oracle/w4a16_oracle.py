@@ -30,7 +30,9 @@ Readings taken where the pages are silent (each also listed in the design notes)
     pages describe its purpose -- one 16-byte load per thread carrying the
     codes of four 16x16 tensor-core blocks, 16x64 tiles stored contiguously --
     but print no permutation table); it is defined here by a closed index
-    formula, ``packed_position`` and ``scale_position``.
+    formula, ``packed_position`` and ``scale_position``: 128-column strips,
+    each stored contiguously along K, so that one work unit of the kernel is
+    one large contiguous copy.  It needs K % 64 == 0 and N % 128 == 0.
 """
 from __future__ import annotations
 
@@ -169,9 +171,11 @@ def error_ok(C_gpu, C_ref, bound) -> bool:
 def packed_position(k, n, K: int):
     """Word index and bit offset of code q[k, n] in the packed uint32 stream.
 
-    The stream is uint32[N/16][K/64][32][4]: for the 16 output columns
-    nb*16 .. nb*16+15 and the 64 reduction rows kb*64 .. kb*64+63, lane L's
-    four consecutive words (one 16-byte vector) are the operand fragments of
+    The stream is uint32[N/128][K/64][8][32][4]: output columns are cut into
+    strips of 128, and each strip is stored contiguously along K, one
+    16 x 64 tile (512 bytes) per (64-row block kb, 16-column block b) with the
+    8 column blocks of a 64-row block side by side.  Inside a tile, lane L's
+    four consecutive words (one 16-byte vector) are its operand fragments of
     the four 16 x 16 tensor-core blocks j = 0..3 (rows 16j .. 16j+15 of the
     tile).  Inside a 16x16 block, with r = n mod 16 (the fragment row) and
     c = k mod 16 (the fragment column):
@@ -184,34 +188,39 @@ def packed_position(k, n, K: int):
     """
     k = np.asarray(k, dtype=np.int64)
     n = np.asarray(n, dtype=np.int64)
-    nb, r = n // 16, n % 16
+    strip, b = n // 128, (n % 128) // 16
+    r = n % 16
     kb, kk = k // 64, k % 64
     j, c = kk // 16, kk % 16
     lane = 4 * (r % 8) + (c % 8) // 2
     slot = r // 8 + 2 * (c // 8) + 4 * (c % 2)
-    word = ((nb * (K // 64) + kb) * 32 + lane) * 4 + j
+    word = (((strip * (K // 64) + kb) * 8 + b) * 32 + lane) * 4 + j
     return word, 4 * slot
 
 
-def scale_position(n):
-    """Column index of scale s[g, n] inside the permuted row g.
+def scale_position(g, n, NG: int):
+    """Index of scale s[g, n] in the permuted scale array (NG = K/G rows of scales).
 
-    Within each block of 16 columns, fragment rows r and r + 8 (r < 8) sit
-    side by side, so a lane reads the scales of both of its rows as one pair:
-    position = 16 * floor(n / 16) + 2 * (r mod 8) + floor(r / 8), r = n mod 16.
+    Layout fp16[N/128][NG][128]: each 128-column strip keeps its NG scale rows
+    together; inside a row, every block of 16 columns puts fragment rows r and
+    r + 8 (r < 8) side by side, so one 32-bit read gives a lane both of its
+    rows' scales:
+        index = (floor(n/128) * NG + g) * 128 + 16 * floor((n mod 128)/16) + 2 * (r mod 8) + floor(r / 8),
+    with r = n mod 16.
     """
+    g = np.asarray(g, dtype=np.int64)
     n = np.asarray(n, dtype=np.int64)
     r = n % 16
-    return (n // 16) * 16 + 2 * (r % 8) + r // 8
+    return ((n // 128) * NG + g) * 128 + ((n % 128) // 16) * 16 + 2 * (r % 8) + r // 8
 
 
 def _check_layout_shape(K: int, N: int):
-    if K % 64 or N % 16 or K <= 0 or N <= 0:
-        raise ValueError("the packed layout needs K % 64 == 0 and N % 16 == 0")
+    if K % 64 or N % 128 or K <= 0 or N <= 0:
+        raise ValueError("the packed layout needs K % 64 == 0 and N % 128 == 0")
 
 
 def repack(q, s, G: int):
-    """Codes uint8[K][N] and scales fp16[K/G][N] -> (packed uint32[K*N/8], permuted fp16[K/G][N])."""
+    """Codes uint8[K][N] and scales fp16[K/G][N] -> (packed uint32[K*N/8], permuted fp16[(K/G)*N])."""
     q = np.asarray(q)
     K, N = q.shape
     _check_layout_shape(K, N)
@@ -226,10 +235,12 @@ def repack(q, s, G: int):
     for slot in range(8):
         packed |= nibbles[:, slot] << np.uint32(4 * slot)
     s = np.asarray(s)
-    if s.shape != (K // G, N):
+    NG = K // G
+    if s.shape != (NG, N):
         raise ValueError("scales must have shape [K/G][N]")
-    sp = np.empty_like(s)
-    sp[:, scale_position(np.arange(N))] = s
+    gg, nn = np.meshgrid(np.arange(NG), np.arange(N), indexing="ij")
+    sp = np.empty(NG * N, dtype=s.dtype)
+    sp[scale_position(gg, nn, NG).ravel()] = s.ravel()
     return packed, sp
 
 
@@ -243,6 +254,8 @@ def unpack(packed, sp, K: int, N: int, G: int):
     kk, nn = np.meshgrid(np.arange(K), np.arange(N), indexing="ij")
     word, shift = packed_position(kk, nn, K)
     q = ((packed[word] >> shift.astype(np.uint32)) & np.uint32(15)).astype(np.uint8)
-    sp = np.asarray(sp)
-    s = sp[:, scale_position(np.arange(N))]
+    NG = K // G
+    sp = np.asarray(sp).ravel()
+    gg, nn = np.meshgrid(np.arange(NG), np.arange(N), indexing="ij")
+    s = sp[scale_position(gg, nn, NG)]
     return q, s

@@ -217,8 +217,8 @@ def test_error_bound_semantics():
 
 
 def test_code_range_rejected():
-    q = np.full((128, 16), 16, np.uint8)
-    s = np.ones((1, 16), np.float16)
+    q = np.full((128, 128), 16, np.uint8)
+    s = np.ones((1, 128), np.float16)
     with pytest.raises(ValueError):
         oracle.dequant_exact(q, s, 128)
     with pytest.raises(ValueError):
@@ -246,7 +246,7 @@ def test_packed_layout_is_the_isa_fragment():
         g, t = lane // 4, lane % 4
         for p, (dr, dc) in ISA_A_FRAGMENT.items():
             for j in range(4):
-                for nb in range(2):
+                for nb in range(8):
                     n = nb * 16 + g + dr
                     k = 16 * j + 2 * t + dc
                     word, shift = oracle.packed_position(k, n, K)
@@ -257,7 +257,7 @@ def test_packed_layout_is_the_isa_fragment():
 
 
 def test_packed_layout_is_a_bijection():
-    K, N = 256, 96
+    K, N = 256, 384
     kk, nn = np.meshgrid(np.arange(K), np.arange(N), indexing="ij")
     word, shift = oracle.packed_position(kk, nn, K)
     code = word * 8 + shift // 4
@@ -267,10 +267,10 @@ def test_packed_layout_is_a_bijection():
 def test_16x64_tiles_are_contiguous_and_vectors_span_four_blocks():
     # 16 x 64 tiles are stored contiguously (512 bytes); each lane's 16-byte vector
     # carries codes from four distinct 16 x 16 blocks.
-    K, N = 256, 64
+    K, N = 256, 256
     kk, nn = np.meshgrid(np.arange(K), np.arange(N), indexing="ij")
     word, _ = oracle.packed_position(kk, nn, K)
-    tile = (nn // 16) * (K // 64) + kk // 64
+    tile = ((nn // 128) * (K // 64) + kk // 64) * 8 + (nn % 128) // 16
     for t in np.unique(tile):
         w = np.unique(word[tile == t])
         assert w.size == 128 and w[-1] - w[0] == 127 and w[0] == t * 128
@@ -280,28 +280,45 @@ def test_16x64_tiles_are_contiguous_and_vectors_span_four_blocks():
         assert np.unique(blk[vec == v]).size == 4
 
 
+def test_strips_are_contiguous_along_k():
+    # a 128-column strip x any run of 64-row blocks is one contiguous range of the stream
+    K, N = 512, 384
+    for strip in range(N // 128):
+        for kb0, kb1 in [(0, 8), (2, 6), (4, 8)]:
+            kk, nn = np.meshgrid(np.arange(64 * kb0, 64 * kb1), np.arange(128 * strip, 128 * strip + 128), indexing="ij")
+            w, _ = oracle.packed_position(kk, nn, K)
+            lo, hi = int(w.min()), int(w.max())
+            assert hi - lo + 1 == (kb1 - kb0) * 8 * 128 and np.unique(w).size == hi - lo + 1
+            assert lo == (strip * (K // 64) + kb0) * 1024
+
+
 def test_scale_position_pairs_rows_r_and_r_plus_8():
-    n = np.arange(64)
-    p = oracle.scale_position(n)
-    assert np.array_equal(np.sort(p), n)
-    for r in range(8):
-        assert p[r + 8] == p[r] + 1 and p[r] % 2 == 0
-    assert np.all(p // 16 == n // 16)
+    NG, N = 3, 256
+    gg, nn = np.meshgrid(np.arange(NG), np.arange(N), indexing="ij")
+    p = oracle.scale_position(gg, nn, NG)
+    assert np.array_equal(np.sort(p.ravel()), np.arange(NG * N))
+    for g in range(NG):
+        for r in range(8):
+            assert p[g, r + 8] == p[g, r] + 1 and p[g, r] % 2 == 0
+    # a strip's NG scale rows are one contiguous block of NG * 128 entries
+    for strip in range(N // 128):
+        blk = p[:, strip * 128:(strip + 1) * 128]
+        assert blk.min() == strip * NG * 128 and blk.max() == (strip + 1) * NG * 128 - 1
 
 
-@pytest.mark.parametrize("K,N,G", [(128, 16, 128), (256, 64, 128), (512, 48, -1), (1024, 128, 128)])
+@pytest.mark.parametrize("K,N,G", [(128, 128, 128), (256, 256, 128), (512, 384, -1), (1024, 128, 128)])
 def test_repack_unpack_round_trip(K, N, G):
     q, s = synth.make_weights(K, N, G, seed=K + N)
     packed, sp = oracle.repack(q, s, G)
     assert packed.dtype == np.uint32 and packed.size == K * N // 8
     q2, s2 = oracle.unpack(packed, sp, K, N, G)
     assert np.array_equal(q2, q)
-    assert np.array_equal(s2.view(np.uint16), s.view(np.uint16))
+    assert np.array_equal(np.asarray(s2).view(np.uint16), s.view(np.uint16))
 
 
 def test_repack_word_decodes_to_fragment_values():
     # Decoding one word by its nibble slots must give the lane's eight A-fragment codes.
-    K, N, G = 64, 16, 64
+    K, N, G = 64, 128, 64
     q, s = synth.make_weights(K, N, G, seed=21)
     packed, _ = oracle.repack(q, s, G)
     for lane in range(32):
