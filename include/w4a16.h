@@ -26,7 +26,7 @@
  *  - The library is built for sm_103a only and returns W4A16_ERR_ARCH on any
  *    other device.  There is no CPU fallback.
  *
- * Shapes: K % 128 == 0, N % 64 == 0, groupsize in {128, K, -1}, M >= 0.
+ * Shapes: K % 128 == 0, N % 128 == 0, groupsize in {128, K, -1}, M >= 0.
  */
 #ifndef W4A16_H
 #define W4A16_H
@@ -91,15 +91,18 @@ W4A16_API size_t w4a16_workspace_bytes(int M, int K, int N, int groupsize);
  *   q        device, uint8[K][N] row-major, codes 0..15
  *   s        device, fp16[K/G][N] row-major scales
  *   packed   device, uint32[K*N/8] output, layout below
- *   scales_p device, fp16[K/G][N] output, columns permuted within 16-blocks
+ *   scales_p device, fp16[(K/G)*N] output, layout below
  *
- * Packed layout (this library's own ABI): uint32[N/16][K/64][32][4].  Code
- * q[k][n] sits in word ((n/16 * K/64 + k/64) * 32 + lane) * 4 + (k%64)/16 at
- * bits [4*slot, 4*slot+4), with r = n%16, c = k%16,
+ * Packed layout (this library's own ABI): uint32[N/128][K/64][8][32][4].
+ * Output columns are cut into 128-column strips, each stored contiguously
+ * along K, so a kernel work unit (a strip x a run of 64-row blocks) is one
+ * contiguous copy.  Code q[k][n] sits in word
+ *   (((n/128 * K/64 + k/64) * 8 + (n%128)/16) * 32 + lane) * 4 + (k%64)/16
+ * at bits [4*slot, 4*slot+4), with r = n%16, c = k%16,
  *   lane = 4*(r%8) + (c%8)/2,   slot = r/8 + 2*(c/8) + 4*(c%2),
  * i.e. each word is one lane's operand fragment of a 16x16 mma.m16n8k16 block
- * whose 16 rows are output columns.  Permuted scales: s[g][n] is stored at
- * scales_p[g][16*(n/16) + 2*(r%8) + r/8].
+ * whose 16 rows are output columns.  Permuted scales fp16[N/128][K/G][128]:
+ * s[g][n] is stored at ((n/128) * K/G + g) * 128 + 16*((n%128)/16) + 2*(r%8) + r/8.
  * Codes above 15 are masked to 4 bits and flag W4A16_ERR_CODE_RANGE for
  * w4a16_get_status(NULL, stream).
  * ------------------------------------------------------------------------- */
@@ -151,10 +154,10 @@ W4A16_API int w4a16_get_status(void* workspace, void* stream);
  * ------------------------------------------------------------------------- */
 typedef struct {
   int path;          /* 1 = mma.sync streaming kernel */
-  int m_tiles;       /* 8-row token tiles per launch (1, 2, 4 or 8) */
+  int m_tiles;       /* 8-row token tiles per launch (1, 2 or 4) */
   int m_chunk;       /* rows per launch (8 * m_tiles); launches = ceil(M / m_chunk) */
-  int n_tile;        /* output columns per work unit */
-  int k_tile;        /* reduction rows per work unit (128) */
+  int n_tile;        /* output columns per work unit (one 128-column strip) */
+  int k_tile;        /* reduction rows per work unit (128, 256 or 512) */
   int units;         /* work units per launch: (N / n_tile) * (K / k_tile) */
   int units_per_cta; /* T */
   int grid;          /* CTAs per launch */

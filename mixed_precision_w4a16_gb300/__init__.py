@@ -205,7 +205,7 @@ def repack(q, s, groupsize: int, stream=None):
     import torch
     K, N = q.shape
     packed = torch.empty(K * N // 8, dtype=torch.int32, device=q.device)
-    sp = torch.empty_like(s)
+    sp = torch.empty(s.numel(), dtype=torch.float16, device=q.device)  # permuted: fp16[N/128][K/G][128]
     w4a16_repack(q, s, K, N, groupsize, packed, sp, stream)
     return packed, sp
 

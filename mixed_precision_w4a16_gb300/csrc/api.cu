@@ -54,7 +54,7 @@ int effective_group(int K, int groupsize) {
 }
 
 int check_shape(int K, int N, int groupsize) {
-  if (K <= 0 || N <= 0 || K % 128 != 0 || N % 64 != 0) return W4A16_ERR_SHAPE;
+  if (K <= 0 || N <= 0 || K % 128 != 0 || N % 128 != 0) return W4A16_ERR_SHAPE;
   const int G = effective_group(K, groupsize);
   if (G == 0 || K % G != 0) return W4A16_ERR_GROUP;
   return W4A16_OK;
@@ -65,42 +65,61 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Plan of the streaming kernel for (M, K, N) over `sms` SMs with `smem_optin` bytes of shared memory.
 struct Plan {
   MmaConfig cfg;
+  MmaLayout lay;
   int m_chunk;
-  int KU, ntiles, units, T, grid;
+  int srows;
+  int KU, strips, units, T, grid;
   size_t workspace;
 };
 
-Plan make_plan(int M, int K, int N, int sms, int smem_optin) {
+Plan make_plan(int M, int K, int N, int G, int sms, int smem_optin) {
   Plan pl{};
-  const int mc = std::min(std::max(M, 1), 64);
-  const int mt = mc <= 8 ? 1 : mc <= 16 ? 2 : mc <= 32 ? 4 : 8;
-  const int pref = mt <= 2 ? 4 : mt == 4 ? 2 : 1;  // instantiated (m_tiles, nbw) pairs
-  const int KU = K / kKTile;
-  int nbw = pref;
-  for (; nbw > 1; nbw /= 2) {
-    const int nt = 64 * nbw;
-    if (N % nt != 0) continue;
-    if (static_cast<long long>(N / nt) * KU >= 2LL * sms) break;
+  const int mc = std::min(std::max(M, 1), 32);
+  const int mt = mc <= 8 ? 1 : mc <= 16 ? 2 : 4;
+  const int strips = N / kStrip;
+  // Unit depth KT = 64 * kq.  Per-SM time of a unit is modelled from copy-engine
+  // measurements on GB300: ~89 ns per 4 KB of weights streamed plus ~80 ns of
+  // fixed cost for the unit's three copy operations.  Pick the kq minimising
+  // T * unit time among those that keep >= 3 pipeline stages in shared memory.
+  int best_kq = 0;
+  long long best_cost = 0;
+  const int cands[3] = {8, 4, 2};
+  for (int c = 0; c < 3; ++c) {
+    const int kq = cands[c];
+    if (K % (64 * kq) != 0) continue;
+    const int srows = (G <= 64 * kq) ? (64 * kq) / G : 1;
+    const MmaLayout l0 = mma_layout(mt, kq, srows, 0);
+    const int stages = (smem_optin - l0.smem_bytes) / (l0.stage_bytes + 16);
+    if (stages < 3 && kq != 2) continue;
+    const long long units = static_cast<long long>(strips) * (K / (64 * kq));
+    const long long T = (units + sms - 1) / sms;
+    const long long cost = T * (89LL * kq + 80);
+    if (best_kq == 0 || cost < best_cost) {
+      best_kq = kq;
+      best_cost = cost;
+    }
   }
-  const int NT = 64 * nbw;
-  const int fixed = mma_smem_bytes(mt, nbw, 0);
-  const int per_stage = mma_stage_bytes(mt, nbw) + 16;
-  int stages = (smem_optin - fixed) / per_stage;
-  stages = std::max(2, std::min(stages, 12));
+  if (!best_kq) best_kq = 2;
+  const int kq = best_kq;
+  const int KT = 64 * kq;
+  pl.srows = (G <= KT) ? KT / G : 1;
+  const MmaLayout l0 = mma_layout(mt, kq, pl.srows, 0);
+  int stages = (smem_optin - l0.smem_bytes) / (l0.stage_bytes + 16);
+  stages = std::max(2, std::min(stages, 8));
+  pl.lay = mma_layout(mt, kq, pl.srows, stages);
   pl.cfg.m_tiles = mt;
-  pl.cfg.nbw = nbw;
-  pl.cfg.n_tile = NT;
+  pl.cfg.kq = kq;
   pl.cfg.stages = stages;
-  pl.cfg.smem_bytes = mma_smem_bytes(mt, nbw, stages);
+  pl.cfg.smem_bytes = pl.lay.smem_bytes;
   pl.cfg.threads = kMmaThreads;
   pl.m_chunk = 8 * mt;
-  pl.KU = KU;
-  pl.ntiles = N / NT;
-  pl.units = pl.ntiles * KU;
+  pl.KU = K / KT;
+  pl.strips = strips;
+  pl.units = strips * pl.KU;
   pl.T = (pl.units + sms - 1) / sms;
   pl.grid = (pl.units + pl.T - 1) / pl.T;
-  const size_t counters = (static_cast<size_t>(pl.ntiles) * 4 + 255) / 256 * 256;
-  const size_t slots = 2ull * pl.grid * NT * (8 * mt) * sizeof(float);
+  const size_t counters = (static_cast<size_t>(strips) * 4 + 255) / 256 * 256;
+  const size_t slots = 2ull * pl.grid * kStrip * (8 * mt) * sizeof(float);
   pl.workspace = kStatusBytes + counters + slots;
   return pl;
 }
@@ -118,15 +137,17 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
   return fn;
 }
 
-// 2-D map over A (fp16[M][K]); boxes of 64 columns x box_rows rows, 128-byte swizzle, zero fill.
-int encode_a_map(CUtensorMap* map, const uint16_t* A, int M, int K, int box_rows) {
+// 3-D view of A (fp16[M][K]) as [K/64][M][64]: box {64, box_rows, kq} fetches the
+// kq 64-column pieces of one work unit in one copy, each piece box_rows x 128 bytes
+// with the 128-byte swizzle; rows beyond M are zero-filled.
+int encode_a_map(CUtensorMap* map, const uint16_t* A, int M, int K, int box_rows, int kq) {
   auto enc = get_encoder();
   if (!enc) return W4A16_ERR_CUDA;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-  const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
-  const cuuint32_t estr[2] = {1u, 1u};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(A), dims, strides, box, estr,
+  const cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128u};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(kq)};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t*>(A), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? W4A16_OK : W4A16_ERR_CUDA;
@@ -155,7 +176,7 @@ const char* w4a16_status_string(int status) {
 int w4a16_abi_version(void) { return 1; }
 
 size_t w4a16_packed_bytes(int K, int N) {
-  if (K <= 0 || N <= 0 || K % 128 != 0 || N % 64 != 0) return 0;
+  if (K <= 0 || N <= 0 || K % 128 != 0 || N % 128 != 0) return 0;
   return static_cast<size_t>(K) * static_cast<size_t>(N) / 2;
 }
 
@@ -178,12 +199,12 @@ int w4a16_plan(int M, int K, int N, int groupsize, int num_sms, w4a16_plan_t* ou
     sms = d->sms;
     smem = d->smem_optin;
   }
-  const Plan pl = make_plan(M, K, N, sms, smem);
+  const Plan pl = make_plan(M, K, N, effective_group(K, groupsize), sms, smem);
   out->path = 1;
   out->m_tiles = pl.cfg.m_tiles;
   out->m_chunk = pl.m_chunk;
-  out->n_tile = pl.cfg.n_tile;
-  out->k_tile = kKTile;
+  out->n_tile = kStrip;
+  out->k_tile = 64 * pl.cfg.kq;
   out->units = pl.units;
   out->units_per_cta = pl.T;
   out->grid = pl.grid;
@@ -197,7 +218,7 @@ size_t w4a16_workspace_bytes(int M, int K, int N, int groupsize) {
   if (M < 0 || check_shape(K, N, groupsize) != W4A16_OK) return 0;
   DeviceInfo* d = nullptr;
   if (current_device_info(&d) != W4A16_OK) return 0;
-  return make_plan(M, K, N, d->sms, d->smem_optin).workspace;
+  return make_plan(M, K, N, effective_group(K, groupsize), d->sms, d->smem_optin).workspace;
 }
 
 void w4a16_debug_set_wait_cycles(long long cycles) { g_wait_cycles.store(cycles > 0 ? cycles : 0); }
@@ -259,11 +280,12 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* scales
   DeviceInfo* d = nullptr;
   const int r = current_device_info(&d);
   if (r != W4A16_OK) return r;
-  const Plan pl = make_plan(M, K, N, d->sms, d->smem_optin);
+  const int G = effective_group(K, groupsize);
+  const Plan pl = make_plan(M, K, N, G, d->sms, d->smem_optin);
   if (workspace_bytes < pl.workspace) return W4A16_ERR_WORKSPACE;
 
   CUtensorMap map;
-  const int er = encode_a_map(&map, A, M, K, pl.m_chunk);
+  const int er = encode_a_map(&map, A, M, K, pl.m_chunk, pl.cfg.kq);
   if (er != W4A16_OK) return er;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -273,16 +295,25 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* scales
   p.C = C;
   p.status = reinterpret_cast<uint32_t*>(ws);
   p.counters = reinterpret_cast<uint32_t*>(ws + kStatusBytes);
-  p.slots = reinterpret_cast<float*>(ws + kStatusBytes + (static_cast<size_t>(pl.ntiles) * 4 + 255) / 256 * 256);
+  p.slots = reinterpret_cast<float*>(ws + kStatusBytes + (static_cast<size_t>(pl.strips) * 4 + 255) / 256 * 256);
   p.M = M;
   p.K = K;
   p.N = N;
-  p.G = effective_group(K, groupsize);
+  p.G = G;
+  p.kq = pl.cfg.kq;
+  p.srows = pl.srows;
   p.KU = pl.KU;
   p.units = pl.units;
   p.T = pl.T;
   p.grid = pl.grid;
   p.stages = pl.cfg.stages;
+  p.w_off = pl.lay.w_off;
+  p.s_off = pl.lay.s_off;
+  p.stage_bytes = pl.lay.stage_bytes;
+  p.tx_bytes = pl.lay.tx_bytes;
+  p.red_off = pl.lay.red_off;
+  p.bar_off = pl.lay.bar_off;
+  p.flag_off = pl.lay.flag_off;
   const long long wc = g_wait_cycles.load();
   p.wait_limit = wc > 0 ? wc : kDefaultWaitCycles;
   p.debug_stall = g_stall.load();

@@ -126,9 +126,11 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
 }
 
 // D = A * B + C, m16n8k16, A row-major FP16, B column-major FP16, FP32 accumulate.
+// A pure register operation: not volatile, so the compiler may interleave it
+// with the decode arithmetic and the shared-memory loads of other blocks.
 __device__ __forceinline__ void mma_16816(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1,
                                           const float c[4]) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
       "{%10, %11, %12, %13};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])

@@ -1,25 +1,33 @@
-// Streaming W4A16 GEMM for small batches (M <= 64 rows per launch).
+// Streaming W4A16 GEMM for small batches (up to 32 token rows per launch).
 //
 // The MARLIN paper (Section 3.4, "Bound By Weight Loading") makes the point
 // that for small M the kernel should be bound by reading the 4-bit weights
 // once.  This kernel is built around that stream on sm_103a:
 //
-//  * one producer warp issues 1-D bulk copies (TMA engine) of the packed
-//    weights (L2 evict-first) and 2-D tensor copies of the activation tile
-//    (L2 evict-last, 128-byte swizzle) into a ring of shared-memory stages,
-//    signalled by mbarriers with transaction counts;
-//  * eight consumer warps decode each 32-bit word into four FP16x2 operand
-//    registers (exact LOP3 + packed-FP16 decode) and feed
-//    mma.sync.m16n8k16 with the weights on the 16-row side and the tokens on
-//    the 8-column side (so tiny M wastes only the 8-wide slot);
-//  * each group's FP32 partial product is scaled by its FP32 scale (one FMA
-//    per accumulator instead of one FP16 multiply per weight);
-//  * work units (n_tile output columns x 128 reduction rows) are dealt to
-//    CTAs in contiguous stripes of T = ceil(units / CTAs) units running down
-//    a column tile and wrapping into the next (the deep-dive article's
-//    striped partitioning); column tiles split between CTAs are reduced
-//    through FP32 slots with an arrival counter, the last arriver summing
-//    the slots in CTA order (fixed order: deterministic, no spin waits).
+//  * a work unit is one 128-column strip x KT = 64*KQ reduction rows; the
+//    packed layout stores it as ONE contiguous chunk (KQ * 4 KB), so a single
+//    producer lane fills a pipeline stage with three copy-engine (TMA)
+//    operations: the weight chunk (1-D bulk copy, L2 evict-first), the
+//    activation tile (3-D tensor copy, 128-byte swizzle, L2 evict-last) and
+//    the unit's scale rows (1-D bulk copy); completion is tracked by an
+//    mbarrier transaction count;
+//  * eight consumer warps split each unit 2 ways along the columns (4 blocks
+//    of 16 each) and 4 ways along K (64-row pieces kq0, kq0 + 4, ...); a warp
+//    loads the activation fragments of its piece once (ldmatrix) and reuses
+//    them for its 4 column blocks;
+//  * each 32-bit word decodes to four FP16x2 operand registers (exact LOP3 +
+//    packed-FP16 decode) feeding mma.sync.m16n8k16 with the weights on the
+//    16-row side and the tokens on the 8-column side, so tiny M wastes only
+//    the 8-wide slot;
+//  * each 64-row piece's FP32 partial product is scaled by its group's FP32
+//    scale with one FMA per accumulator;
+//  * units are dealt to CTAs in contiguous stripes of T = ceil(units / CTAs)
+//    running down a strip and wrapping into the next (the deep-dive article's
+//    striped partitioning).  At a strip boundary the 4 K-split warps fold
+//    their partials through shared memory in fixed order; strips split
+//    between CTAs are reduced through FP32 slots with an arrival counter, the
+//    last arriver summing the slots in CTA order (deterministic, no spin
+//    waits).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -30,24 +38,8 @@ namespace w4a16 {
 namespace {
 
 constexpr int kConsumerWarps = 8;
+constexpr int kNbw = 4;                           // 16-column blocks per consumer warp
 constexpr long long kDrainCycles = 2000000000LL;  // bound on the final drain wait
-
-template <int MT, int NBW>
-struct Layout {
-  static constexpr int MB = 8 * MT;                 // token rows per launch
-  static constexpr int NT = 64 * NBW;               // output columns per unit
-  static constexpr int A_BOX = MB * 128;            // one 64-column activation box (bytes)
-  static constexpr int A_OFF = 0;                   // two boxes, 1024-aligned
-  static constexpr int W_OFF = 2 * A_BOX;           // NT/16 runs of 1024 bytes
-  static constexpr int S_OFF = W_OFF + NT * 64;     // NT fp16 scales
-  static constexpr int STAGE = ((S_OFF + NT * 2) + 1023) / 1024 * 1024;
-  static constexpr int TX = 2 * A_BOX + NT * 64 + NT * 2;
-  static constexpr int RED = 4 * NBW * MT * 4 * 32 * 4;  // kh = 1 partials
-  static constexpr int red_off(int stages) { return stages * STAGE; }
-  static constexpr int bar_off(int stages) { return red_off(stages) + RED; }
-  static constexpr int flag_off(int stages) { return bar_off(stages) + 16 * stages; }
-  static constexpr int total(int stages) { return 1024 + flag_off(stages) + 64; }
-};
 
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -55,24 +47,35 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
 
 __device__ __forceinline__ uint16_t f32_to_f16_bits(float x) { return __half_as_ushort(__float2half_rn(x)); }
 
-template <int MT, int NBW>
+// 3-D tensor copy global -> shared (activations viewed as [K/64][M][64]).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+template <int MT>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     gemm_mma_kernel(const __grid_constant__ CUtensorMap tmA, const GemmParams p) {
-  using L = Layout<MT, NBW>;
-  constexpr int NT = L::NT;
-  constexpr int MB = L::MB;
+  constexpr int MB = 8 * MT;
+  constexpr int A_BOX = MB * 128;  // bytes of one 64-row activation piece
+  constexpr int SLOT = 128 * MB;   // floats in one strip partial
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const int S = p.stages;
-  const uint32_t bar_full = sbase + L::bar_off(S);
+  const int KQ = p.kq;
+  const uint32_t bar_full = sbase + p.bar_off;
   const uint32_t bar_empty = bar_full + 8 * S;
-  volatile int* flags = reinterpret_cast<volatile int*>(smem + L::flag_off(S));
+  volatile int* flags = reinterpret_cast<volatile int*>(smem + p.flag_off);
   volatile int* abort_flag = flags + 0;  // set by any warp whose wait ran out
   volatile int* last_flag = flags + 1;   // "this CTA is the last arriver" broadcast
   volatile int* seg_abort = flags + 2;   // abort decision frozen for one epilogue
   volatile int* zero_flag = flags + 3;   // always 0 (for the drain wait)
-  float* red = reinterpret_cast<float*>(smem + L::red_off(S));
+  float* red = reinterpret_cast<float*>(smem + p.red_off);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -99,7 +102,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     if (lane == 0) prefetch_tensormap(&tmA);
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_a = policy_evict_last();
-    const int ktiles64 = p.K / 64;
+    const int KT = 64 * KQ;
+    const int NG = p.K / p.G;
+    const uint32_t w_bytes = static_cast<uint32_t>(KQ) * 4096u;
     int issued = 0;
     for (int it = 0; it < nunits; ++it) {
       const int s = it % S;
@@ -115,28 +120,23 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           break;
         }
       }
-      const int u = u_begin + it;
-      const int j = u / p.KU;
-      const int kt = u - j * p.KU;
-      const uint32_t st = sbase + s * L::STAGE;
-      const uint32_t fb = bar_full + 8 * s;
       if (p.debug_stall && it == 0) continue;  // leave stage 0 empty: nothing will complete its barrier
-      if (lane == 0) mbar_arrive_expect_tx(fb, L::TX);
+      if (lane == 0) {
+        const int u = u_begin + it;
+        const int j = u / p.KU;
+        const int kt = u - j * p.KU;
+        const uint32_t st = sbase + s * p.stage_bytes;
+        const uint32_t fb = bar_full + 8 * s;
+        mbar_arrive_expect_tx(fb, p.tx_bytes);
+        const uint32_t* wsrc =
+            p.packed + (static_cast<long long>(j) * (p.K / 64) + static_cast<long long>(kt) * KQ) * 1024;
+        bulk_g2s(st + p.w_off, wsrc, w_bytes, fb, pol_w);
+        tma_load_3d(st, &tmA, 0, p.m0, kt * KQ, fb, pol_a);
+        const int grp0 = (p.G <= KT) ? (kt * KT) / p.G : 0;
+        const uint16_t* ssrc = p.scales + (static_cast<long long>(j) * NG + grp0) * 128;
+        bulk_g2s(st + p.s_off, ssrc, static_cast<uint32_t>(p.srows) * 256u, fb, pol_a);
+      }
       __syncwarp();
-      if (lane < NT / 16) {
-        const long long nbg = static_cast<long long>(j) * (NT / 16) + lane;
-        const uint32_t* src = p.packed + (nbg * ktiles64 + 2LL * kt) * 128;
-        bulk_g2s(st + L::W_OFF + lane * 1024, src, 1024, fb, pol_w);
-      }
-      if (lane == 31) {
-        tma_load_2d(st + L::A_OFF, &tmA, kt * 128, p.m0, fb, pol_a);
-        tma_load_2d(st + L::A_OFF + L::A_BOX, &tmA, kt * 128 + 64, p.m0, fb, pol_a);
-      }
-      if (lane == 30) {
-        const int grp = (kt * 128) / p.G;
-        const uint16_t* src = p.scales + static_cast<long long>(grp) * p.N + static_cast<long long>(j) * NT;
-        bulk_g2s(st + L::S_OFF, src, NT * 2, fb, pol_a);
-      }
       issued = it + 1;
     }
     named_bar_sync(3, kMmaThreads);
@@ -150,14 +150,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   }
 
   // -------------------------------------------------------------------- consumers
-  const int kh = warp & 1;   // which 64-row half of the 128-row unit
-  const int ng = warp >> 1;  // which group of NBW 16-column blocks
+  const int ng = warp >> 2;  // column half of the strip: blocks 4*ng .. 4*ng + 3
+  const int kq0 = warp & 3;  // first 64-row piece of each unit (then kq0 + 4, ...)
   const int g = lane >> 2, t = lane & 3;
   const int first_col = u_begin / p.KU;
+  const int KT = 64 * KQ;
+  const bool grouped = p.G <= KT;  // G = 128: one scale row per 128 rows; else one row per strip
 
-  float acc[NBW][MT][4];
+  float acc[kNbw][MT][4];
 #pragma unroll
-  for (int i = 0; i < NBW; ++i)
+  for (int i = 0; i < kNbw; ++i)
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -167,7 +169,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   for (int it = 0; it < nunits; ++it) {
     const int s = it % S;
     const int u = u_begin + it;
-    const uint32_t st = sbase + s * L::STAGE;
+    const uint32_t st = sbase + s * p.stage_bytes;
     bool have = false;
     const bool go = __shfl_sync(0xffffffffu, *abort_flag == 0, 0);
     if (go) {
@@ -179,50 +181,59 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       }
     }
     if (have) {
-      // activation fragments of this warp's 64-row half: 4 k16 steps x MT token tiles
-      const uint32_t a_box = st + L::A_OFF + kh * L::A_BOX;
-      uint32_t bf[4][MT][2];
-      const int mi = lane >> 3, rr = lane & 7;
-      if constexpr (MT == 1) {
+      for (int kq = kq0; kq < KQ; kq += 4) {
+        // activation fragments of this 64-row piece: 4 k16 steps x MT token tiles
+        const uint32_t a_box = st + kq * A_BOX;
+        uint32_t bf[4][MT][2];
+        const int mi = lane >> 3, rr = lane & 7;
+        if constexpr (MT == 1) {
 #pragma unroll
-        for (int jj = 0; jj < 4; jj += 2) {
-          const int chunk = 2 * jj + mi;
-          ldmatrix_x4(a_box + rr * 128 + ((chunk ^ rr) << 4), bf[jj][0][0], bf[jj][0][1], bf[jj + 1][0][0],
-                      bf[jj + 1][0][1]);
-        }
-      } else {
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-          for (int mp = 0; mp < MT / 2; ++mp) {
-            const int token = (2 * mp + (mi >> 1)) * 8 + rr;
-            const int chunk = 2 * jj + (mi & 1);
-            ldmatrix_x4(a_box + token * 128 + ((chunk ^ rr) << 4), bf[jj][2 * mp][0], bf[jj][2 * mp][1],
-                        bf[jj][2 * mp + 1][0], bf[jj][2 * mp + 1][1]);
+          for (int jj = 0; jj < 4; jj += 2) {
+            const int chunk = 2 * jj + mi;
+            ldmatrix_x4(a_box + rr * 128 + ((chunk ^ rr) << 4), bf[jj][0][0], bf[jj][0][1], bf[jj + 1][0][0],
+                        bf[jj + 1][0][1]);
           }
-      }
+        } else {
 #pragma unroll
-      for (int i = 0; i < NBW; ++i) {
-        const int lnb = ng * NBW + i;
-        const uint4 wv = lds128(st + L::W_OFF + lnb * 1024 + kh * 512 + lane * 16);
-        const uint32_t sp = lds32(st + L::S_OFF + (lnb * 16 + 2 * g) * 2);
-        const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
-        float tmp[MT][4];
+          for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          uint32_t a[4];
-          decode8(words[jj], a);
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) mma_16816(tmp[mt], a, bf[jj][mt][0], bf[jj][mt][1], jj == 0 ? zero4 : tmp[mt]);
+            for (int mp = 0; mp < MT / 2; ++mp) {
+              const int token = (2 * mp + (mi >> 1)) * 8 + rr;
+              const int chunk = 2 * jj + (mi & 1);
+              ldmatrix_x4(a_box + token * 128 + ((chunk ^ rr) << 4), bf[jj][2 * mp][0], bf[jj][2 * mp][1],
+                          bf[jj][2 * mp + 1][0], bf[jj][2 * mp + 1][1]);
+            }
         }
-        const float s_lo = __half2float(__ushort_as_half(static_cast<uint16_t>(sp & 0xffffu)));
-        const float s_hi = __half2float(__ushort_as_half(static_cast<uint16_t>(sp >> 16)));
+        const int srow = grouped ? (kq * 64) / p.G : 0;
+        uint4 wv[kNbw];
+        uint32_t spv[kNbw];
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          acc[i][mt][0] = fmaf(s_lo, tmp[mt][0], acc[i][mt][0]);
-          acc[i][mt][1] = fmaf(s_lo, tmp[mt][1], acc[i][mt][1]);
-          acc[i][mt][2] = fmaf(s_hi, tmp[mt][2], acc[i][mt][2]);
-          acc[i][mt][3] = fmaf(s_hi, tmp[mt][3], acc[i][mt][3]);
+        for (int i = 0; i < kNbw; ++i) {
+          const int nb = ng * kNbw + i;
+          wv[i] = lds128(st + p.w_off + (kq * 8 + nb) * 512 + lane * 16);
+          spv[i] = lds32(st + p.s_off + (srow * 128 + nb * 16 + 2 * g) * 2);
+        }
+#pragma unroll
+        for (int i = 0; i < kNbw; ++i) {
+          const uint32_t words[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+          float tmp[MT][4];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            uint32_t a[4];
+            decode8(words[jj], a);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+              mma_16816(tmp[mt], a, bf[jj][mt][0], bf[jj][mt][1], jj == 0 ? zero4 : tmp[mt]);
+          }
+          const float s_lo = __half2float(__ushort_as_half(static_cast<uint16_t>(spv[i] & 0xffffu)));
+          const float s_hi = __half2float(__ushort_as_half(static_cast<uint16_t>(spv[i] >> 16)));
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            acc[i][mt][0] = fmaf(s_lo, tmp[mt][0], acc[i][mt][0]);
+            acc[i][mt][1] = fmaf(s_lo, tmp[mt][1], acc[i][mt][1]);
+            acc[i][mt][2] = fmaf(s_hi, tmp[mt][2], acc[i][mt][2]);
+            acc[i][mt][3] = fmaf(s_hi, tmp[mt][3], acc[i][mt][3]);
+          }
         }
       }
       __syncwarp();
@@ -233,76 +244,81 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     const bool seg_end = ((u + 1) % p.KU == 0) || (it == nunits - 1);
     if (!seg_end) continue;
     const int j = u / p.KU;
-    // 1) fold the two 64-row halves together (kh = 1 -> shared memory -> kh = 0)
-    if (kh == 1) {
+    // 1) fold the 4 K-split warps of each column half (kq0 = 1, 2, 3 -> kq0 = 0), fixed order
+    if (kq0 != 0) {
 #pragma unroll
-      for (int i = 0; i < NBW; ++i)
+      for (int i = 0; i < kNbw; ++i)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) red[(((ng * NBW + i) * MT + mt) * 4 + e) * 32 + lane] = acc[i][mt][e];
+          for (int e = 0; e < 4; ++e)
+            red[(((((kq0 - 1) * 2 + ng) * kNbw + i) * MT + mt) * 4 + e) * 32 + lane] = acc[i][mt][e];
     }
     named_bar_sync(1, kConsumerWarps * 32);
     if (warp == 0 && lane == 0) *seg_abort = *abort_flag;
-    if (kh == 0) {
+    if (kq0 == 0) {
 #pragma unroll
-      for (int i = 0; i < NBW; ++i)
+      for (int i = 0; i < kNbw; ++i)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) acc[i][mt][e] += red[(((ng * NBW + i) * MT + mt) * 4 + e) * 32 + lane];
+          for (int e = 0; e < 4; ++e) {
+            const int r0 = ((((0 * 2 + ng) * kNbw + i) * MT + mt) * 4 + e) * 32 + lane;
+            const int stride = 2 * kNbw * MT * 4 * 32;
+            acc[i][mt][e] = ((acc[i][mt][e] + red[r0]) + red[r0 + stride]) + red[r0 + 2 * stride];
+          }
     }
     named_bar_sync(1, kConsumerWarps * 32);
     const bool skip = *seg_abort != 0;
-    if (kh == 0 && !skip) {
+    if (kq0 == 0 && !skip) {
       const int c_first = (j * p.KU) / p.T;
       const int c_last = min(((j + 1) * p.KU - 1) / p.T, p.grid - 1);
+      const int sidx0 = ng * kNbw * MT * 4 * 32 + lane;  // this warp's part of a strip partial
       bool write_now = true;
       if (c_first != c_last) {
-        // 2) this column tile is split between CTAs: publish the partial, count arrivals
+        // 2) this strip is split between CTAs: publish the partial, count arrivals
         const int slot = (j == first_col) ? 2 * cta : 2 * cta + 1;
-        float* dst = p.slots + static_cast<long long>(slot) * (NT * MB);
+        float* dst = p.slots + static_cast<long long>(slot) * SLOT + sidx0;
 #pragma unroll
-        for (int i = 0; i < NBW; ++i)
+        for (int i = 0; i < kNbw; ++i)
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) dst[(((ng * NBW + i) * MT + mt) * 4 + e) * 32 + lane] = acc[i][mt][e];
+            for (int e = 0; e < 4; ++e) dst[((i * MT + mt) * 4 + e) * 32] = acc[i][mt][e];
         __threadfence();
-        named_bar_sync(2, 4 * 32);
+        named_bar_sync(2, 2 * 32);
         if (warp == 0 && lane == 0) {
           const unsigned old = atomicAdd(p.counters + j, 1u);
           *last_flag = (old == static_cast<unsigned>(c_last - c_first)) ? 1 : 0;
         }
-        named_bar_sync(2, 4 * 32);
+        named_bar_sync(2, 2 * 32);
         write_now = *last_flag != 0;
         if (write_now) {
           // 3) last arriver: sum every CTA's slot in CTA order (deterministic)
           __threadfence();
 #pragma unroll
-          for (int i = 0; i < NBW; ++i)
+          for (int i = 0; i < kNbw; ++i)
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
               for (int e = 0; e < 4; ++e) acc[i][mt][e] = 0.f;
           for (int c = c_first; c <= c_last; ++c) {
             const int cslot = (j == (c * p.T) / p.KU) ? 2 * c : 2 * c + 1;
-            const float* src = p.slots + static_cast<long long>(cslot) * (NT * MB);
+            const float* src = p.slots + static_cast<long long>(cslot) * SLOT + sidx0;
 #pragma unroll
-            for (int i = 0; i < NBW; ++i)
+            for (int i = 0; i < kNbw; ++i)
 #pragma unroll
               for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  acc[i][mt][e] += __ldcg(src + (((ng * NBW + i) * MT + mt) * 4 + e) * 32 + lane);
+                for (int e = 0; e < 4; ++e) acc[i][mt][e] += __ldcg(src + ((i * MT + mt) * 4 + e) * 32);
           }
           if (warp == 0 && lane == 0) p.counters[j] = 0u;
         }
       }
       if (write_now) {
 #pragma unroll
-        for (int i = 0; i < NBW; ++i) {
-          const int n_base = j * NT + (ng * NBW + i) * 16 + g;
+        for (int i = 0; i < kNbw; ++i) {
+          const int n_base = j * kStrip + (ng * kNbw + i) * 16 + g;
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -315,7 +331,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       }
     }
 #pragma unroll
-    for (int i = 0; i < NBW; ++i)
+    for (int i = 0; i < kNbw; ++i)
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -324,55 +340,36 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   named_bar_sync(3, kMmaThreads);
 }
 
-template <int MT, int NBW>
+template <int MT>
 cudaError_t launch_one(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream) {
-  auto kern = gemm_mma_kernel<MT, NBW>;
+  auto kern = gemm_mma_kernel<MT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem_bytes);
   if (e != cudaSuccess) return e;
   kern<<<p.grid, kMmaThreads, cfg.smem_bytes, stream>>>(tmA, p);
   return cudaGetLastError();
 }
 
-// Instantiated configurations (registers: 9 warps leave at most 168 per thread,
-// so wider token tiles get fewer column blocks per warp).
-template <int MT>
-cudaError_t launch_mt(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream) {
-  switch (cfg.nbw) {
-    case 1: return launch_one<MT, 1>(cfg, tmA, p, stream);
-    case 2:
-      if constexpr (MT <= 4) return launch_one<MT, 2>(cfg, tmA, p, stream);
-      return cudaErrorInvalidValue;
-    case 4:
-      if constexpr (MT <= 2) return launch_one<MT, 4>(cfg, tmA, p, stream);
-      return cudaErrorInvalidValue;
-    default: return cudaErrorInvalidValue;
-  }
-}
-
-template <int MT, int NBW>
-constexpr int stage_bytes_of() { return Layout<MT, NBW>::STAGE; }
-
 }  // namespace
 
-int mma_stage_bytes(int m_tiles, int nbw) {
-  const int MB = 8 * m_tiles, NT = 64 * nbw;
-  const int s_off = 2 * MB * 128 + NT * 64;
-  return (s_off + NT * 2 + 1023) / 1024 * 1024;
+MmaLayout mma_layout(int m_tiles, int kq, int srows, int stages) {
+  MmaLayout l{};
+  const int MB = 8 * m_tiles;
+  l.w_off = kq * MB * 128;        // activation pieces first (each a multiple of 1024 bytes)
+  l.s_off = l.w_off + kq * 4096;  // then the weight chunk, then the scale rows
+  l.stage_bytes = (l.s_off + srows * 256 + 1023) / 1024 * 1024;
+  l.tx_bytes = kq * MB * 128 + kq * 4096 + srows * 256;
+  l.red_off = stages * l.stage_bytes;
+  l.bar_off = l.red_off + 3 * 2 * kNbw * m_tiles * 4 * 32 * 4;
+  l.flag_off = l.bar_off + 16 * stages;
+  l.smem_bytes = 1024 + l.flag_off + 64;
+  return l;
 }
-
-int mma_smem_bytes(int m_tiles, int nbw, int stages) {
-  const int red = 4 * nbw * m_tiles * 4 * 32 * 4;
-  return 1024 + stages * mma_stage_bytes(m_tiles, nbw) + red + 16 * stages + 64;
-}
-
-static_assert(stage_bytes_of<2, 4>() == 21504, "stage layout");
 
 cudaError_t launch_gemm_mma(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream) {
   switch (cfg.m_tiles) {
-    case 1: return launch_mt<1>(cfg, tmA, p, stream);
-    case 2: return launch_mt<2>(cfg, tmA, p, stream);
-    case 4: return launch_mt<4>(cfg, tmA, p, stream);
-    case 8: return launch_mt<8>(cfg, tmA, p, stream);
+    case 1: return launch_one<1>(cfg, tmA, p, stream);
+    case 2: return launch_one<2>(cfg, tmA, p, stream);
+    case 4: return launch_one<4>(cfg, tmA, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

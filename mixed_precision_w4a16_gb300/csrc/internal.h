@@ -13,40 +13,49 @@ enum : uint32_t {
   kDevErrTimeout = 1u << 1,
 };
 
+// Shared-memory layout of one streaming-kernel configuration (byte offsets
+// from the 1024-aligned base; one stage = activation pieces, weight chunk,
+// scale rows).
+struct MmaLayout {
+  int w_off, s_off, stage_bytes, tx_bytes;
+  int red_off, bar_off, flag_off, smem_bytes;
+};
+
+MmaLayout mma_layout(int m_tiles, int kq, int srows, int stages);
+
 // Parameters of one launch of the streaming (mma.sync) GEMM kernel.
 struct GemmParams {
-  const uint32_t* packed;   // uint32[N/16][K/64][32][4]
-  const uint16_t* scales;   // permuted fp16[K/G][N]
+  const uint32_t* packed;   // uint32[N/128][K/64][8][32][4]
+  const uint16_t* scales;   // permuted fp16[N/128][K/G][128]
   uint16_t* C;              // fp16[M][N]
   uint32_t* status;         // workspace status word
-  uint32_t* counters;       // one arrival counter per column tile
-  float* slots;             // 2 * grid partial-sum slots of n_tile * 8 * m_tiles floats
+  uint32_t* counters;       // one arrival counter per 128-column strip
+  float* slots;             // 2 * grid partial-sum slots of 128 * 8 * m_tiles floats
   int M;                    // rows of A / C
   int m0;                   // first row handled by this launch
   int K, N, G;              // G: effective group size (128 or K)
-  int KU;                   // K / 128 work units per column tile
-  int units;                // (N / n_tile) * KU
+  int kq;                   // 64-row pieces per work unit (KT = 64 * kq)
+  int srows;                // scale rows per work unit
+  int KU;                   // K / KT work units per strip
+  int units;                // (N / 128) * KU
   int T;                    // units per CTA
   int grid;                 // CTAs
   int stages;               // pipeline depth
+  int w_off, s_off, stage_bytes, tx_bytes, red_off, bar_off, flag_off;
   long long wait_limit;     // clock cycles a pipeline wait may take
   int debug_stall;          // 1: never fill the first stage (failure-detection test)
 };
 
 struct MmaConfig {
-  int m_tiles;      // 8-row token tiles (1, 2, 4, 8)
-  int nbw;          // 16-column blocks per consumer warp (1, 2, 4)
-  int n_tile;       // 64 * nbw
+  int m_tiles;      // 8-row token tiles (1, 2, 4)
+  int kq;           // 64-row pieces per unit (2, 4, 8)
   int stages;
   int smem_bytes;
   int threads;
 };
 
-// shared-memory footprint of one kernel configuration
-int mma_stage_bytes(int m_tiles, int nbw);
-int mma_smem_bytes(int m_tiles, int nbw, int stages);
 constexpr int kMmaThreads = 288;  // 8 consumer warps + 1 producer warp
-constexpr int kKTile = 128;
+constexpr int kStrip = 128;       // output columns per strip / work unit
 
 cudaError_t launch_gemm_mma(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream);
 

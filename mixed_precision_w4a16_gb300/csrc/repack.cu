@@ -1,12 +1,15 @@
 // Offline repack of 4-bit codes and FP16 scales into the GEMM's fragment
 // order, plus the two diagnostic inverses (unpack, dequantise).
 //
-// Layout (see include/w4a16.h): packed uint32[N/16][K/64][32][4]; word j of
-// lane L in tile (nb, kb) is L's operand fragment of the 16x16 block with
-// output columns nb*16.. and reduction rows kb*64 + 16j ..; nibble slot
-// i < 4 / i + 4 = low / high half of fragment register i.  Register i holds
-// fragment row g + 8*(i & 1) and columns 2t + 8*(i >> 1) + {0, 1}, with
-// g = L / 4 and t = L % 4 (PTX ISA, mma.m16n8k16 A-operand fragment).
+// Layout (see include/w4a16.h): packed uint32[N/128][K/64][8][32][4] --
+// 128-column strips stored contiguously along K; inside a strip, for each
+// 64-row block, the 8 tiles of 16 columns x 64 rows follow each other.  Word
+// j of lane L in a tile is L's operand fragment of the 16x16 block with
+// reduction rows 16j ..; nibble slot i < 4 / i + 4 = low / high half of
+// fragment register i.  Register i holds fragment row g + 8*(i & 1) and
+// columns 2t + 8*(i >> 1) + {0, 1}, with g = L / 4 and t = L % 4 (PTX ISA,
+// mma.m16n8k16 A-operand fragment).  Permuted scales: fp16[N/128][K/G][128],
+// within each 16-column block fragment rows r and r + 8 side by side.
 //
 // Kernels here walk the layout from the word side (word -> positions); one
 // thread owns one lane's 16-byte vector (four words), so every store of the
@@ -24,16 +27,19 @@ __device__ unsigned int g_repack_flag;
 namespace {
 
 struct VecCoord {
-  int nb, kb, lane;
+  int nb, kb, lane;  // nb: global 16-column block
 };
 
 __device__ __forceinline__ VecCoord vec_coord(long long v, int K) {
   const int kTiles = K / 64;
   VecCoord c;
   c.lane = static_cast<int>(v & 31);
-  const long long tile = v >> 5;
-  c.kb = static_cast<int>(tile % kTiles);
-  c.nb = static_cast<int>(tile / kTiles);
+  long long t = v >> 5;
+  const int b = static_cast<int>(t & 7);
+  t >>= 3;
+  c.kb = static_cast<int>(t % kTiles);
+  const long long strip = t / kTiles;
+  c.nb = static_cast<int>(strip * 8 + b);
   return c;
 }
 
@@ -74,17 +80,20 @@ __global__ void repack_codes_kernel(const uint8_t* __restrict__ q, int K, int N,
 // permuted position p inside a 16-column block -> fragment row r
 __device__ __forceinline__ int perm_row(int p) { return (p >> 1) + 8 * (p & 1); }
 
-__global__ void permute_scales_kernel(const uint16_t* __restrict__ s, uint16_t* __restrict__ sp, int N,
+// sp index i -> (g, n): i = (strip * NG + g) * 128 + p, n = strip * 128 + 16 * (p / 16) + row(p % 16)
+__global__ void permute_scales_kernel(const uint16_t* __restrict__ s, uint16_t* __restrict__ sp, int N, int NG,
                                       long long count, int inverse) {
   const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
   if (i >= count) return;
-  const long long row = i / N;
-  const int p = static_cast<int>(i % N);
-  const int src_col = (p & ~15) + perm_row(p & 15);
+  const int p = static_cast<int>(i & 127);
+  const long long t = i >> 7;
+  const int g = static_cast<int>(t % NG);
+  const long long strip = t / NG;
+  const long long n = strip * 128 + (p & ~15) + perm_row(p & 15);
   if (!inverse)
-    sp[row * N + p] = s[row * N + src_col];  // forward: natural -> permuted
+    sp[i] = s[g * static_cast<long long>(N) + n];  // forward: natural -> permuted
   else
-    sp[row * N + src_col] = s[row * N + p];  // inverse: permuted -> natural
+    sp[g * static_cast<long long>(N) + n] = s[i];  // inverse: permuted -> natural
 }
 
 __global__ void unpack_codes_kernel(const uint4* __restrict__ packed, int K, int N, uint8_t* __restrict__ q,
@@ -116,7 +125,9 @@ __global__ void dequant_kernel(const uint4* __restrict__ packed, const uint16_t*
   const VecCoord vc = vec_coord(v, K);
   const int g = vc.lane >> 2, t = vc.lane & 3;
   const int grp = (vc.kb * 64) / G;  // G is a multiple of 64: one group per 64-row tile
-  const uint32_t spair = *reinterpret_cast<const uint32_t*>(sp + static_cast<long long>(grp) * N + vc.nb * 16 + 2 * g);
+  const int NG = K / G;
+  const long long sidx = (static_cast<long long>(vc.nb >> 3) * NG + grp) * 128 + (vc.nb & 7) * 16 + 2 * g;
+  const uint32_t spair = *reinterpret_cast<const uint32_t*>(sp + sidx);
   const uint32_t s_row_g = (spair & 0xffffu) * 0x10001u;      // scale of fragment row g, both halves
   const uint32_t s_row_g8 = (spair >> 16) * 0x10001u;         // scale of fragment row g + 8
   const uint4 pv = packed[v];
@@ -147,7 +158,7 @@ cudaError_t launch_repack(const uint8_t* q, const uint16_t* s, int K, int N, int
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long ns = static_cast<long long>(K / G) * N;
-  permute_scales_kernel<<<grid_for(ns, 256), 256, 0, stream>>>(s, scales_p, N, ns, 0);
+  permute_scales_kernel<<<grid_for(ns, 256), 256, 0, stream>>>(s, scales_p, N, K / G, ns, 0);
   return cudaGetLastError();
 }
 
@@ -159,7 +170,7 @@ cudaError_t launch_unpack(const uint32_t* packed, const uint16_t* scales_p, int 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long ns = static_cast<long long>(K / G) * N;
-  permute_scales_kernel<<<grid_for(ns, 256), 256, 0, stream>>>(scales_p, s, N, ns, 1);
+  permute_scales_kernel<<<grid_for(ns, 256), 256, 0, stream>>>(scales_p, s, N, K / G, ns, 1);
   return cudaGetLastError();
 }
 

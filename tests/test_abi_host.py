@@ -51,7 +51,8 @@ def test_sizes(w):
     assert w.w4a16_scales_count(4096, 12288, -1) == 12288
     assert w.w4a16_scales_count(4096, 12288, 4096) == 12288
     assert w.w4a16_packed_bytes(100, 64) == 0
-    assert w.w4a16_scales_count(1024, 96, 128) == 0      # N % 64
+    assert w.w4a16_scales_count(1024, 96, 128) == 0      # N % 128
+    assert w.w4a16_scales_count(1024, 192, 128) == 0
     assert w.w4a16_scales_count(1024, 128, 64) == 0      # unsupported group size
 
 
@@ -62,19 +63,19 @@ def test_status_strings(w):
 
 
 SHAPES = [(1, 1024, 1024), (16, 1024, 1024), (16, 4096, 12288), (1, 11008, 4096), (32, 8192, 57344),
-          (64, 18432, 73728), (16, 18432, 73728), (100, 4096, 4096), (3, 128, 64), (40, 256, 192)]
+          (64, 18432, 73728), (16, 18432, 73728), (100, 4096, 4096), (3, 128, 128), (40, 256, 384), (8, 11008, 4096)]
 
 
 @pytest.mark.parametrize("M,K,N", SHAPES)
 def test_plan_stripes_cover_every_unit_once(w, M, K, N):
     for sms in (152, 148, 7):
         p = w.w4a16_plan(M, K, N, 128, sms)
-        assert p["k_tile"] == 128 and N % p["n_tile"] == 0
-        KU = K // 128
+        assert p["k_tile"] in (128, 256, 512) and K % p["k_tile"] == 0 and p["n_tile"] == 128
+        KU = K // p["k_tile"]
         assert p["units"] == (N // p["n_tile"]) * KU
         T, grid, U = p["units_per_cta"], p["grid"], p["units"]
         assert grid <= sms and grid * T >= U and (grid - 1) * T < U
-        assert p["m_chunk"] == 8 * p["m_tiles"] and p["m_chunk"] >= min(M, 64)
+        assert p["m_chunk"] == 8 * p["m_tiles"] and p["m_chunk"] >= min(M, 32)
         assert p["smem_bytes"] <= 232448 and p["stages"] >= 2
         # every unit belongs to exactly one CTA; every CTA has work
         owner = [u // T for u in range(U)]
@@ -95,7 +96,7 @@ def test_plan_stripes_cover_every_unit_once(w, M, K, N):
 
 def test_plan_token_tiles(w):
     assert [w.w4a16_plan(m, 1024, 1024, 128, 152)["m_tiles"] for m in (1, 8, 9, 16, 17, 32, 33, 64, 1000)] == \
-        [1, 1, 2, 2, 4, 4, 8, 8, 8]
+        [1, 1, 2, 2, 4, 4, 4, 4, 4]
 
 
 def test_plan_rejects_bad_shapes(w):

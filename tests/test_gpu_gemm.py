@@ -35,12 +35,13 @@ def test_gemm_parity_small_layer(w, M, G):
 
 
 @pytest.mark.parametrize("M,K,N,G", [
-    (5, 128, 64, 128),          # one unit, one CTA
-    (16, 256, 192, 128),        # N not a multiple of 128: 64-wide tiles
-    (16, 384, 320, -1),         # K/128 odd, per-column scales
-    (3, 11008, 256, 128),       # long K: stripes split every column
-    (24, 2048, 8192, 128),      # many column tiles
+    (5, 128, 128, 128),         # one unit, one CTA
+    (16, 256, 384, 128),        # three strips
+    (16, 384, 640, -1),         # K/128 odd (128-row units), per-column scales
+    (3, 11008, 256, 128),       # long K: stripes split every strip
+    (24, 2048, 8192, 128),      # many strips
     (40, 4096, 640, -1),
+    (9, 1536, 1280, 128),       # K/256 odd: 256-row units
 ])
 def test_gemm_parity_shapes(w, M, K, N, G):
     A, q, s = tl.layer(M, K, N, G, seed=M + K + N)
@@ -159,6 +160,9 @@ def test_gemm_error_codes(w):
     with pytest.raises(w.W4A16Error) as e:
         w.w4a16_gemm(A_d, packed, sp, C, M, K, N, 256, ws)
     assert e.value.status == 3
+    with pytest.raises(w.W4A16Error) as e:
+        w.w4a16_gemm(A_d, packed, sp, C, M, K, 448, G, ws)
+    assert e.value.status == 2
     w.w4a16_gemm(A_d, packed, sp, C, 0, K, N, G, ws)  # M == 0: no-op
 
 

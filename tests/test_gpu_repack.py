@@ -8,8 +8,8 @@ import w4a16_testlib as tl
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = [(128, 64, 128), (256, 128, 128), (1024, 1024, 128), (512, 192, -1), (4096, 4096, 128),
-          (11008, 256, 128), (1024, 320, 1024)]
+SHAPES = [(128, 128, 128), (256, 256, 128), (1024, 1024, 128), (512, 384, -1), (4096, 4096, 128),
+          (11008, 256, 128), (1024, 640, 1024)]
 
 
 @pytest.fixture(scope="module")
@@ -24,7 +24,7 @@ def test_repack_matches_oracle_bytes(w, K, N, G):
     ref_packed, ref_sp = oracle.repack(q, s, G)
     got = packed.cpu().numpy().view(np.uint32)
     assert np.array_equal(got, ref_packed)
-    assert np.array_equal(sp.cpu().numpy().view(np.uint16), ref_sp.view(np.uint16))
+    assert np.array_equal(sp.cpu().numpy().view(np.uint16).ravel(), ref_sp.view(np.uint16))
     assert w.w4a16_get_status() == 0
 
 
@@ -49,7 +49,7 @@ def test_dequant_bit_exact(w, K, N, G):
 def test_dequant_extreme_scales_bit_exact(w):
     # scales near the FP16 range ends: products overflow to inf or land in subnormals;
     # both sides round the same exact product once.
-    K, N, G = 256, 128, 128
+    K, N, G = 256, 256, 128
     q, _ = synth.make_weights(K, N, G, seed=99)
     rng = np.random.default_rng(5)
     pool = np.array([65504.0, 8192.0, 6e-8, 2.0 ** -24, 2.0 ** -14, 1.0 / 3, -0.5, 0.0, 1e-5], np.float16)
@@ -60,10 +60,10 @@ def test_dequant_extreme_scales_bit_exact(w):
 
 
 def test_code_range_is_flagged_not_trapped(w):
-    K, N, G = 128, 64, 128
+    K, N, G = 128, 128, 128
     q, s = synth.make_weights(K, N, G, seed=1)
     q[5, 7] = 16
-    q[100, 63] = 255
+    q[100, 127] = 255
     _, _, packed, sp = tl.device_layer(w, q, s, G)
     assert w.w4a16_get_status() == 4  # W4A16_ERR_CODE_RANGE
     assert w.w4a16_get_status() == 0  # read-and-clear
@@ -75,13 +75,16 @@ def test_code_range_is_flagged_not_trapped(w):
 
 def test_repack_rejects_bad_arguments(w):
     torch = tl.torch_mod()
-    q = torch.zeros((128, 64), dtype=torch.uint8, device="cuda")
-    s = torch.zeros((1, 64), dtype=torch.float16, device="cuda")
-    packed = torch.empty(128 * 64 // 8, dtype=torch.int32, device="cuda")
+    q = torch.zeros((128, 128), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((1, 128), dtype=torch.float16, device="cuda")
+    packed = torch.empty(128 * 128 // 8, dtype=torch.int32, device="cuda")
     sp = torch.empty_like(s)
     with pytest.raises(w.W4A16Error) as e:
-        w.w4a16_repack(q, s, 128, 64, 64, packed, sp)
+        w.w4a16_repack(q, s, 128, 128, 64, packed, sp)
     assert e.value.status == 3
     with pytest.raises(w.W4A16Error) as e:
-        w.w4a16_repack(q.data_ptr() + 1, s, 128, 64, 128, packed, sp)
+        w.w4a16_repack(q.data_ptr() + 1, s, 128, 128, 128, packed, sp)
     assert e.value.status == 9
+    with pytest.raises(w.W4A16Error) as e:
+        w.w4a16_repack(q, s, 128, 64, 128, packed, sp)
+    assert e.value.status == 2
