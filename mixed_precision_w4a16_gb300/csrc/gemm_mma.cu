@@ -102,15 +102,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     if (lane == 0) prefetch_tensormap(&tmA);
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_a = policy_evict_last();
-    const int KT = 64 * KQ;
     const int NG = p.K / p.G;
     const uint32_t w_bytes = static_cast<uint32_t>(KQ) * 4096u;
     int issued = 0;
+    // incremental counters: stage s / its fill round, strip j / unit kt within the strip
+    int s = 0, round = 0;
+    int j = u_begin / p.KU, kt = u_begin - (u_begin / p.KU) * p.KU;
     for (int it = 0; it < nunits; ++it) {
-      const int s = it % S;
       if (it >= S) {
         bool ok = true;
-        if (lane == 0) ok = mbar_wait_bounded(bar_empty + 8 * s, ((it / S) - 1) & 1, p.wait_limit, abort_flag);
+        if (lane == 0) ok = mbar_wait_bounded(bar_empty + 8 * s, (round - 1) & 1, p.wait_limit, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) {
           if (lane == 0 && !*abort_flag) {
@@ -120,24 +121,30 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           break;
         }
       }
-      if (p.debug_stall && it == 0) continue;  // leave stage 0 empty: nothing will complete its barrier
-      if (lane == 0) {
-        const int u = u_begin + it;
-        const int j = u / p.KU;
-        const int kt = u - j * p.KU;
-        const uint32_t st = sbase + s * p.stage_bytes;
-        const uint32_t fb = bar_full + 8 * s;
-        mbar_arrive_expect_tx(fb, p.tx_bytes);
-        const uint32_t* wsrc =
-            p.packed + (static_cast<long long>(j) * (p.K / 64) + static_cast<long long>(kt) * KQ) * 1024;
-        bulk_g2s(st + p.w_off, wsrc, w_bytes, fb, pol_w);
-        tma_load_3d(st, &tmA, 0, p.m0, kt * KQ, fb, pol_a);
-        const int grp0 = (p.G <= KT) ? (kt * KT) / p.G : 0;
-        const uint16_t* ssrc = p.scales + (static_cast<long long>(j) * NG + grp0) * 128;
-        bulk_g2s(st + p.s_off, ssrc, static_cast<uint32_t>(p.srows) * 256u, fb, pol_a);
+      if (!(p.debug_stall && it == 0)) {  // with debug_stall, stage 0 stays empty: nothing completes its barrier
+        if (lane == 0) {
+          const uint32_t st = sbase + s * p.stage_bytes;
+          const uint32_t fb = bar_full + 8 * s;
+          mbar_arrive_expect_tx(fb, p.tx_bytes);
+          const uint32_t* wsrc =
+              p.packed + (static_cast<long long>(j) * (p.K / 64) + static_cast<long long>(kt) * KQ) * 1024;
+          bulk_g2s(st + p.w_off, wsrc, w_bytes, fb, pol_w);
+          tma_load_3d(st, &tmA, 0, p.m0, kt * KQ, fb, pol_a);
+          const int grp0 = (p.G == 128) ? kt * p.srows : 0;  // G is 128 or K (K >= KT)
+          const uint16_t* ssrc = p.scales + (static_cast<long long>(j) * NG + grp0) * 128;
+          bulk_g2s(st + p.s_off, ssrc, static_cast<uint32_t>(p.srows) * 256u, fb, pol_a);
+        }
+        __syncwarp();
+        issued = it + 1;
       }
-      __syncwarp();
-      issued = it + 1;
+      if (++s == S) {
+        s = 0;
+        ++round;
+      }
+      if (++kt == p.KU) {
+        kt = 0;
+        ++j;
+      }
     }
     named_bar_sync(3, kMmaThreads);
     // After a timeout, make sure no copy is still landing in shared memory.
@@ -154,8 +161,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const int kq0 = warp & 3;  // first 64-row piece of each unit (then kq0 + 4, ...)
   const int g = lane >> 2, t = lane & 3;
   const int first_col = u_begin / p.KU;
-  const int KT = 64 * KQ;
-  const bool grouped = p.G <= KT;  // G = 128: one scale row per 128 rows; else one row per strip
 
   float acc[kNbw][MT][4];
 #pragma unroll
@@ -166,14 +171,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       for (int e = 0; e < 4; ++e) acc[i][mt][e] = 0.f;
   const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
 
+  int s = 0, round = 0;
+  int j = first_col, kt = u_begin - first_col * p.KU;
   for (int it = 0; it < nunits; ++it) {
-    const int s = it % S;
-    const int u = u_begin + it;
     const uint32_t st = sbase + s * p.stage_bytes;
     bool have = false;
     const bool go = __shfl_sync(0xffffffffu, *abort_flag == 0, 0);
     if (go) {
-      have = mbar_wait_bounded(bar_full + 8 * s, (it / S) & 1, p.wait_limit, abort_flag);
+      have = mbar_wait_bounded(bar_full + 8 * s, round & 1, p.wait_limit, abort_flag);
       have = __all_sync(0xffffffffu, have);
       if (!have && lane == 0 && !*abort_flag) {
         *abort_flag = 1;
@@ -204,7 +209,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                           bf[jj][2 * mp + 1][0], bf[jj][2 * mp + 1][1]);
             }
         }
-        const int srow = grouped ? (kq * 64) / p.G : 0;
+        const int srow = (p.G == 128) ? (kq >> 1) : 0;
         uint4 wv[kNbw];
         uint32_t spv[kNbw];
 #pragma unroll
@@ -239,11 +244,15 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * s);
     }
-
-    // ---------------------------------------------------------- segment epilogue
-    const bool seg_end = ((u + 1) % p.KU == 0) || (it == nunits - 1);
+    if (++s == S) {
+      s = 0;
+      ++round;
+    }
+    const bool seg_end = (kt == p.KU - 1) || (it == nunits - 1);
+    if (++kt == p.KU) kt = 0;
     if (!seg_end) continue;
-    const int j = u / p.KU;
+
+    // ---------------------------------------------------------- segment epilogue (strip j)
     // 1) fold the 4 K-split warps of each column half (kq0 = 1, 2, 3 -> kq0 = 0), fixed order
     if (kq0 != 0) {
 #pragma unroll
@@ -336,6 +345,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[i][mt][e] = 0.f;
+    ++j;
   }
   named_bar_sync(3, kMmaThreads);
 }
