@@ -141,6 +141,40 @@ W4A16_API int w4a16_gemm(const uint16_t* A, const uint32_t* packed, const uint16
                int M, int K, int N, int groupsize, void* workspace, size_t workspace_bytes,
                void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Allocation-free GEMM.  The paper has no counterpart: this entry point is a
+ * convenience of this library for callers that cannot allocate device memory.
+ *
+ * Some callers cannot call cudaMalloc: code that runs while its stream is being
+ * captured into a CUDA graph (an allocation is not a stream operation and the
+ * default capture mode forbids it), serving loops that must never allocate or
+ * synchronise the device on their hot path, and plugin hosts that own all
+ * device memory and hand a kernel nothing but its inputs and outputs.  Such a
+ * caller passes A, packed, scales_p and C exactly as for w4a16_gemm (same
+ * meaning, layout and alignment) and no workspace.
+ *
+ * The scratch this call needs lives in the library itself: a file-scope device
+ * array of W4A16_NOALLOC_SCRATCH_BYTES that every GPU which loads the library
+ * holds until the process exits.  The first call on each device looks up the
+ * array's device address with that device current; make that first call
+ * before any stream capture begins.  Each call then clears the array's status
+ * word and arrival counters (cudaMemsetAsync on `stream`) and runs the same
+ * kernel as w4a16_gemm.  It calls no cudaMalloc, no cudaFree and no allocating
+ * library routine.
+ *
+ * All calls share the one array and it keeps the previous call's contents, so
+ * two calls that may execute at the same time on the GPU (for example on two
+ * streams with no ordering between them) race and corrupt each other's output:
+ * order them.  Shapes whose w4a16_workspace_bytes exceed the array are rejected
+ * with W4A16_ERR_WORKSPACE before anything is launched.  A pipeline timeout
+ * inside this call is recorded in the library's array and is not reported by
+ * w4a16_get_status; use w4a16_gemm with your own workspace to observe it.
+ * ------------------------------------------------------------------------- */
+#define W4A16_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+W4A16_API int w4a16_gemm_noalloc(const uint16_t* A, const uint32_t* packed, const uint16_t* scales_p, uint16_t* C,
+                                 int M, int K, int N, int groupsize, void* stream);
+
 /* Synchronises `stream`, then returns (and clears) the first error recorded on
  * the device: the repack code-range flag and, when `workspace` is non-NULL,
  * the GEMM status word in that workspace.  W4A16_OK when none. */

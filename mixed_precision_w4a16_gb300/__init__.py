@@ -16,7 +16,7 @@ import os
 __all__ = [
     "W4A16Error", "lib", "Plan",
     "w4a16_packed_bytes", "w4a16_scales_count", "w4a16_workspace_bytes", "w4a16_plan",
-    "w4a16_repack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm", "w4a16_get_status",
+    "w4a16_repack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm", "w4a16_gemm_noalloc", "w4a16_get_status",
     "w4a16_debug_set_wait_cycles", "w4a16_debug_inject_stall", "w4a16_status_string", "EXPORTED_SYMBOLS",
     "repack", "unpack", "dequant", "gemm", "workspace_for",
 ]
@@ -28,6 +28,7 @@ EXPORTED_SYMBOLS = (
     "w4a16_status_string", "w4a16_abi_version", "w4a16_packed_bytes", "w4a16_scales_count",
     "w4a16_workspace_bytes", "w4a16_repack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm",
     "w4a16_get_status", "w4a16_plan", "w4a16_debug_set_wait_cycles", "w4a16_debug_inject_stall",
+    "w4a16_gemm_noalloc",
 )
 
 
@@ -67,6 +68,7 @@ def _load():
         "w4a16_plan": (i, [i, i, i, i, i, ctypes.POINTER(Plan)]),
         "w4a16_debug_set_wait_cycles": (None, [ctypes.c_longlong]),
         "w4a16_debug_inject_stall": (None, [i]),
+        "w4a16_gemm_noalloc": (i, [vp, vp, vp, vp, i, i, i, i, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -169,6 +171,13 @@ def w4a16_gemm(A, packed, scales_p, C, M, K, N, groupsize, workspace, workspace_
         workspace_bytes = workspace.numel() * workspace.element_size()
     _check(_lib().w4a16_gemm(_ptr(A), _ptr(packed), _ptr(scales_p), _ptr(C), M, K, N, groupsize, _ptr(workspace),
                           int(workspace_bytes), _stream(stream)), "w4a16_gemm")
+
+
+def w4a16_gemm_noalloc(A, packed, scales_p, C, M, K, N, groupsize, stream=None):
+    """The allocation-free GEMM: same operands as w4a16_gemm, no workspace (the library's
+    own scratch array is used; calls must not overlap on the GPU)."""
+    _check(_lib().w4a16_gemm_noalloc(_ptr(A), _ptr(packed), _ptr(scales_p), _ptr(C), M, K, N, groupsize,
+                                     _stream(stream)), "w4a16_gemm_noalloc")
 
 
 def w4a16_get_status(workspace=None, stream=None) -> int:

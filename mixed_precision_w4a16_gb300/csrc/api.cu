@@ -325,6 +325,47 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* scales
   return W4A16_OK;
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant: the scratch is a file-scope device array of the
+// library, looked up once per device with cudaGetSymbolAddress.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[W4A16_NOALLOC_SCRATCH_BYTES];
+void* g_noalloc_addr[kMaxDevices];  // device address of g_noalloc_scratch, per device
+
+}  // namespace
+
+extern "C" {
+
+int w4a16_gemm_noalloc(const uint16_t* A, const uint32_t* packed, const uint16_t* scales_p, uint16_t* C, int M, int K,
+                       int N, int groupsize, void* stream) {
+  if (M < 0) return W4A16_ERR_SHAPE;
+  const int st = check_shape(K, N, groupsize);
+  if (st != W4A16_OK) return st;
+  if (M == 0) return W4A16_OK;
+  if (!A || !packed || !scales_p || !C) return W4A16_ERR_NULL;
+  DeviceInfo* d = nullptr;
+  const int r = current_device_info(&d);
+  if (r != W4A16_OK) return r;
+  const Plan pl = make_plan(M, K, N, effective_group(K, groupsize), d->sms, d->smem_optin);
+  if (pl.workspace > W4A16_NOALLOC_SCRATCH_BYTES) return W4A16_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return W4A16_ERR_CUDA;
+  if (!g_noalloc_addr[dev]) {
+    void* addr = nullptr;  // set-up on this device's first call (must precede any stream capture)
+    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || !addr) return W4A16_ERR_CUDA;
+    g_noalloc_addr[dev] = addr;
+  }
+  void* ws = g_noalloc_addr[dev];
+  // the status word and the arrival counters must start at zero; the partial-sum slots need not
+  const size_t clear = kStatusBytes + (static_cast<size_t>(pl.strips) * 4 + 255) / 256 * 256;
+  if (cudaMemsetAsync(ws, 0, clear, static_cast<cudaStream_t>(stream)) != cudaSuccess) return W4A16_ERR_CUDA;
+  return w4a16_gemm(A, packed, scales_p, C, M, K, N, groupsize, ws, W4A16_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 int w4a16_get_status(void* workspace, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return W4A16_ERR_CUDA;
