@@ -131,7 +131,40 @@ def workload_totals(layers):
 
 
 def cpu_sample_cols(workload):
-    return {"big": 512, "pr1": 1024, "7b": 1024, "70b": 512, "prefill": 256}[workload]
+    """Columns of each GEMM the oracle computes for the cpu_baseline leg (~10-20 s single-threaded)."""
+    return {"big": 12288, "pr1": 1024, "7b": 16384, "70b": 8192, "prefill": 2048}[workload]
+
+
+def kernel_source_hash():
+    """Hash of the CUDA sources; profile figures are used only for the build they were taken on."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for path in sorted(glob.glob(os.path.join(ROOT, "mixed_precision_w4a16_gb300", "csrc", "*"))):
+        if path.endswith((".cu", ".cuh", ".h")):
+            h.update(os.path.basename(path).encode())
+            with open(path, "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(name):
+    """Per-launch DRAM bytes {(M, launch): bytes} from a committed ncu summary, or None when the
+    summary was taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", name)
+    try:
+        with open(path) as f:
+            text = f.read()
+    except OSError:
+        return None
+    if f"kernel-source: {kernel_source_hash()}" not in text:
+        return None
+    out = {}
+    for line in text.splitlines():
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) == 8 and cells[0].isdigit():
+            out[(int(cells[0]), int(cells[1]))] = float(cells[5]) * 1e6
+    return out or None
 
 
 # ---------------------------------------------------------------------------
@@ -365,8 +398,18 @@ def run_ours(args, rank, world, device):
                       "launches": p["launches"]})
     if mem_time > 0:
         ach = mem_bytes / mem_time / 1e9
+        # DRAM bytes per launch over the same launches, from the committed ncu summary of this build
+        traffic = None
+        prof = profiled_traffic("gemm_mma_big_layer_traffic.md") if args.workload == "big" else None
+        if prof:
+            mem_ms = {r["M"] for r in sweep if r["bound"] == "hbm"}
+            vals = [v for (m, _), v in prof.items() if m in mem_ms]
+            if vals:
+                traffic = round(sum(vals) / len(vals))
+        n_launch = sum(p["launches"] for p, r in zip(points, sweep) if r["bound"] == "hbm")
         roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": round(ach / peaks["hbm_gbs"], 3), "traffic": None,
+                    "frac": round(ach / peaks["hbm_gbs"], 3), "traffic": traffic,
+                    "algorithmic_bytes_per_launch": round(mem_bytes / max(1, n_launch)),
                     "kernel": "gemm_mma_kernel", "over": "memory-bound points of the sweep",
                     "peak_source": peaks["source"]}
     else:
@@ -398,11 +441,14 @@ def run_ours(args, rank, world, device):
 
 
 def reduce_max(x, world, device):
+    """Max of a host number over all ranks (NCCL on GPUs, gloo on CPU)."""
     if world <= 1:
         return x
     import torch
-    t = torch.tensor([x], dtype=torch.float64, device=device)
-    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    dist = torch.distributed
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
 
@@ -415,7 +461,7 @@ def run_reference(args, rank, world):
         return None
     desc, layers, seed = WORKLOADS[args.workload]
     tb, _ = workload_totals(layers)
-    ncols = max(16, cpu_sample_cols(args.workload) // 4)
+    ncols = max(64, cpu_sample_cols(args.workload) // 32)
     for _ in range(args.warmup):
         run_cpu_sample(args.workload, ncols)
     secs = []
