@@ -13,7 +13,7 @@
 //    mbarrier transaction count;
 //  * eight consumer warps split each unit 2 ways along the columns (4 blocks
 //    of 16 each) and 4 ways along K (64-row pieces kq0, kq0 + 4, ...); a warp
-//    loads the activation fragments of its piece once (ldmatrix) and reuses
+//    loads the activation fragments of its piece once (8-byte shared loads) and reuses
 //    them for its 4 column blocks;
 //  * each 32-bit word decodes to four FP16x2 operand registers (exact LOP3 +
 //    packed-FP16 decode) feeding mma.sync.m16n8k16 with the weights on the
@@ -187,28 +187,22 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
     if (have) {
       for (int kq = kq0; kq < KQ; kq += 4) {
-        // activation fragments of this 64-row piece: 4 k16 steps x MT token tiles
+        // activation fragments of this 64-row piece: 4 k16 steps x MT token tiles.  The packed
+        // weights hold k = 4t .. 4t+3 of each 16-row block where the m16n8k16 fragment expects
+        // 2t, 2t+1, 2t+8, 2t+9, so the matching activation pair is one 8-byte load of
+        // A[token][16 jj + 4t .. 4t+3] (128-byte swizzle: 16-byte chunk c of row r is at c ^ (r & 7)).
         const uint32_t a_box = st + kq * A_BOX;
         uint32_t bf[4][MT][2];
-        const int mi = lane >> 3, rr = lane & 7;
-        if constexpr (MT == 1) {
 #pragma unroll
-          for (int jj = 0; jj < 4; jj += 2) {
-            const int chunk = 2 * jj + mi;
-            ldmatrix_x4(a_box + rr * 128 + ((chunk ^ rr) << 4), bf[jj][0][0], bf[jj][0][1], bf[jj + 1][0][0],
-                        bf[jj + 1][0][1]);
+        for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            const int token = mt * 8 + g;
+            const int chunk = 2 * jj + (t >> 1);
+            const uint2 v = lds64(a_box + token * 128 + ((chunk ^ g) << 4) + (t & 1) * 8);
+            bf[jj][mt][0] = v.x;
+            bf[jj][mt][1] = v.y;
           }
-        } else {
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-            for (int mp = 0; mp < MT / 2; ++mp) {
-              const int token = (2 * mp + (mi >> 1)) * 8 + rr;
-              const int chunk = 2 * jj + (mi & 1);
-              ldmatrix_x4(a_box + token * 128 + ((chunk ^ rr) << 4), bf[jj][2 * mp][0], bf[jj][2 * mp][1],
-                          bf[jj][2 * mp + 1][0], bf[jj][2 * mp + 1][1]);
-            }
-        }
         const int srow = (p.G == 128) ? (kq >> 1) : 0;
         uint4 wv[kNbw];
         uint32_t spv[kNbw];

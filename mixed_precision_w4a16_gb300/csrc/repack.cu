@@ -4,11 +4,13 @@
 // Layout (see include/w4a16.h): packed uint32[N/128][K/64][8][32][4] --
 // 128-column strips stored contiguously along K; inside a strip, for each
 // 64-row block, the 8 tiles of 16 columns x 64 rows follow each other.  Word
-// j of lane L in a tile is L's operand fragment of the 16x16 block with
-// reduction rows 16j ..; nibble slot i < 4 / i + 4 = low / high half of
-// fragment register i.  Register i holds fragment row g + 8*(i & 1) and
-// columns 2t + 8*(i >> 1) + {0, 1}, with g = L / 4 and t = L % 4 (PTX ISA,
-// mma.m16n8k16 A-operand fragment).  Permuted scales: fp16[N/128][K/G][128],
+// j of lane L in a tile covers the 16x16 block with reduction rows 16j ..;
+// nibble slot i < 4 / i + 4 = low / high half of register i.  Register i
+// holds block row g + 8*(i & 1) and reduction indices 4t + 2*(i >> 1) + {0, 1},
+// with g = L / 4 and t = L % 4: four consecutive k of rows g and g + 8, the
+// per-thread fragment of a 16-lane x 256-bit tensor-memory store, and (with k
+// permuted inside the block) the m16n8k16 A-operand fragment.  Permuted
+// scales: fp16[N/128][K/G][128],
 // within each 16-column block fragment rows r and r + 8 side by side.
 //
 // Kernels here walk the layout from the word side (word -> positions); one
@@ -43,11 +45,11 @@ __device__ __forceinline__ VecCoord vec_coord(long long v, int K) {
   return c;
 }
 
-// (row, column) inside the 16x16 block of nibble slot `slot` for lane (g, t)
+// (row, reduction index) inside the 16x16 block of nibble slot `slot` for lane (g, t)
 __device__ __forceinline__ void slot_rc(int slot, int g, int t, int& r, int& c) {
   const int reg = slot & 3, e = slot >> 2;
   r = g + 8 * (reg & 1);
-  c = 2 * t + e + 8 * (reg >> 1);
+  c = 4 * t + 2 * (reg >> 1) + e;
 }
 
 __global__ void repack_codes_kernel(const uint8_t* __restrict__ q, int K, int N, uint4* __restrict__ packed,
@@ -140,7 +142,7 @@ __global__ void dequant_kernel(const uint4* __restrict__ packed, const uint16_t*
     for (int reg = 0; reg < 4; ++reg) {
       const uint32_t h = hmul2_u32(a[reg], (reg & 1) ? s_row_g8 : s_row_g);
       const long long n = vc.nb * 16LL + g + 8 * (reg & 1);
-      const long long k = vc.kb * 64LL + 16 * j + 2 * t + 8 * (reg >> 1);
+      const long long k = vc.kb * 64LL + 16 * j + 4 * t + 2 * (reg >> 1);
       bhat[k * N + n] = static_cast<uint16_t>(h & 0xffffu);
       bhat[(k + 1) * N + n] = static_cast<uint16_t>(h >> 16);
     }

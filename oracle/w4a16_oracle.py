@@ -178,13 +178,18 @@ def packed_position(k, n, K: int):
     four consecutive words (one 16-byte vector) are its operand fragments of
     the four 16 x 16 tensor-core blocks j = 0..3 (rows 16j .. 16j+15 of the
     tile).  Inside a 16x16 block, with r = n mod 16 (the fragment row) and
-    c = k mod 16 (the fragment column):
-        lane   = 4 * (r mod 8) + floor((c mod 8) / 2)
-        slot   = floor(r / 8) + 2 * floor(c / 8) + 4 * (c mod 2)
+    c = k mod 16 (the reduction index inside the block):
+        lane   = 4 * (r mod 8) + floor(c / 4)
+        slot   = floor(r / 8) + 2 * floor((c mod 4) / 2) + 4 * (c mod 2)
         bits   = [4 * slot, 4 * slot + 4)
     Slot i < 4 is the low half and slot i + 4 the high half of the lane's
-    i-th 32-bit operand register of the m16n8k16 multiply, with the output
-    columns on the fragment's 16-row side.
+    i-th 32-bit register: register i holds row g + 8*(i mod 2) (g = lane/4)
+    and reduction indices 4t + 2*floor(i/2) + {0, 1} (t = lane mod 4).  Each
+    lane thus holds four consecutive k of rows g and g + 8 -- the per-thread
+    fragment of a 16-row x 256-bit tensor-memory store -- and, read as an
+    m16n8k16 A operand, the k order inside the block is the fixed permutation
+    2t + e -> 4t + e, 2t + 8 + e -> 4t + 2 + e (the activation operand is
+    loaded in the same order).
     """
     k = np.asarray(k, dtype=np.int64)
     n = np.asarray(n, dtype=np.int64)
@@ -192,8 +197,8 @@ def packed_position(k, n, K: int):
     r = n % 16
     kb, kk = k // 64, k % 64
     j, c = kk // 16, kk % 16
-    lane = 4 * (r % 8) + (c % 8) // 2
-    slot = r // 8 + 2 * (c // 8) + 4 * (c % 2)
+    lane = 4 * (r % 8) + c // 4
+    slot = r // 8 + 2 * ((c % 4) // 2) + 4 * (c % 2)
     word = (((strip * (K // 64) + kb) * 8 + b) * 32 + lane) * 4 + j
     return word, 4 * slot
 

@@ -238,9 +238,18 @@ ISA_A_FRAGMENT = {
     4: (0, 8), 5: (0, 9),      # a4, a5: (groupID,     2*tig + 8 + {0,1})
     6: (8, 8), 7: (8, 9),      # a6, a7: (groupID + 8, 2*tig + 8 + {0,1})
 }
+# The layout stores, in the lane/register the ISA assigns to fragment column 2*tig + e
+# (resp. 2*tig + 8 + e), the weight of reduction index 4*tig + e (resp. 4*tig + 2 + e).
+def PERM_K(tig, col_offset):
+    return 4 * tig + (2 if col_offset >= 8 else 0) + (col_offset % 2)
+
+# PTX ISA, tcgen05 "Matrix fragments for .16x256b": four 32-bit registers per thread,
+# (lane groupID, column 2*tig), (lane groupID, column 2*tig + 1), (lane groupID + 8,
+# column 2*tig), (lane groupID + 8, column 2*tig + 1); a 32-bit column holds two FP16 k.
+TMEM_16x256b = [(0, 0), (0, 1), (8, 0), (8, 1)]
 
 
-def test_packed_layout_is_the_isa_fragment():
+def test_packed_layout_is_the_permuted_isa_fragment():
     K = 64
     for lane in range(32):
         g, t = lane // 4, lane % 4
@@ -248,12 +257,27 @@ def test_packed_layout_is_the_isa_fragment():
             for j in range(4):
                 for nb in range(8):
                     n = nb * 16 + g + dr
-                    k = 16 * j + 2 * t + dc
+                    k = 16 * j + PERM_K(t, dc)
                     word, shift = oracle.packed_position(k, n, K)
                     reg, half = p // 2, p % 2
                     # register `reg` = (low half, high half) = (a_{2reg}, a_{2reg+1}); slot = reg + 4*half
                     assert int(word) == (nb * 32 + lane) * 4 + j
                     assert int(shift) == 4 * (reg + 4 * half)
+
+
+def test_packed_words_are_tensor_memory_store_fragments():
+    # register order (r0, r2, r1, r3) of a word is the .16x256b fragment: row g / g+8, columns 2t / 2t+1,
+    # column c holding k = 2c, 2c + 1 of the 16x16 block
+    K = 64
+    for lane in range(32):
+        g, t = lane // 4, lane % 4
+        for frag_reg, (dr, dcol) in enumerate(TMEM_16x256b):
+            reg = [0, 2, 1, 3][frag_reg]
+            for e in range(2):
+                n = g + dr
+                k = 2 * (2 * t + dcol) + e
+                word, shift = oracle.packed_position(k, n, K)
+                assert int(word) == lane * 4 and int(shift) == 4 * (reg + 4 * e)
 
 
 def test_packed_layout_is_a_bijection():
@@ -327,4 +351,4 @@ def test_repack_word_decodes_to_fragment_values():
             w = int(packed[lane * 4 + j])
             for p, (dr, dc) in ISA_A_FRAGMENT.items():
                 slot = p // 2 + 4 * (p % 2)
-                assert (w >> (4 * slot)) & 15 == q[16 * j + 2 * t + dc, g + dr]
+                assert (w >> (4 * slot)) & 15 == q[16 * j + PERM_K(t, dc), g + dr]
