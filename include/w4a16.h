@@ -187,9 +187,10 @@ W4A16_API int w4a16_get_status(void* workspace, void* stream);
  * `num_sms` SMs (num_sms <= 0: the current device's count).
  * ------------------------------------------------------------------------- */
 typedef struct {
-  int path;          /* 1 = mma.sync streaming kernel */
-  int m_tiles;       /* 8-row token tiles per launch (1, 2 or 4) */
-  int m_chunk;       /* rows per launch (8 * m_tiles); launches = ceil(M / m_chunk) */
+  int path;          /* 1 = mma.sync streaming kernel, 2 = tensor-memory (tcgen05) kernel */
+  int m_tiles;       /* m_chunk / 8 */
+  int m_chunk;       /* token rows per launch (8, 16 or 32 on path 1; a multiple of 16 up to
+                        256 on path 2); launches = ceil(M / m_chunk) */
   int n_tile;        /* output columns per work unit (one 128-column strip) */
   int k_tile;        /* reduction rows per work unit (128, 256 or 512) */
   int units;         /* work units per launch: (N / n_tile) * (K / k_tile) */
@@ -214,6 +215,12 @@ W4A16_API void w4a16_debug_set_wait_cycles(long long cycles);
  * W4A16_ERR_TIMEOUT, skips all output and returns; the CUDA context stays
  * usable.  Used by the failure-detection tests; 0 disables it. */
 W4A16_API void w4a16_debug_inject_stall(int enable);
+
+/* Kernel-selection knob (not thread-safe), for tests and measurements: 1 runs
+ * every later w4a16_gemm on the streaming mma.sync kernel, 2 on the
+ * tensor-memory (tcgen05) kernel, 0 restores the default (tcgen05 from 17 token
+ * rows on).  w4a16_workspace_bytes and w4a16_plan follow the same choice. */
+W4A16_API void w4a16_debug_force_path(int path);
 
 #ifdef __cplusplus
 }

@@ -17,7 +17,8 @@ __all__ = [
     "W4A16Error", "lib", "Plan",
     "w4a16_packed_bytes", "w4a16_scales_count", "w4a16_workspace_bytes", "w4a16_plan",
     "w4a16_repack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm", "w4a16_gemm_noalloc", "w4a16_get_status",
-    "w4a16_debug_set_wait_cycles", "w4a16_debug_inject_stall", "w4a16_status_string", "EXPORTED_SYMBOLS",
+    "w4a16_debug_set_wait_cycles", "w4a16_debug_inject_stall", "w4a16_debug_force_path", "w4a16_status_string",
+    "EXPORTED_SYMBOLS",
     "repack", "unpack", "dequant", "gemm", "workspace_for",
 ]
 
@@ -28,7 +29,7 @@ EXPORTED_SYMBOLS = (
     "w4a16_status_string", "w4a16_abi_version", "w4a16_packed_bytes", "w4a16_scales_count",
     "w4a16_workspace_bytes", "w4a16_repack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm",
     "w4a16_get_status", "w4a16_plan", "w4a16_debug_set_wait_cycles", "w4a16_debug_inject_stall",
-    "w4a16_gemm_noalloc",
+    "w4a16_gemm_noalloc", "w4a16_debug_force_path",
 )
 
 
@@ -69,6 +70,7 @@ def _load():
         "w4a16_debug_set_wait_cycles": (None, [ctypes.c_longlong]),
         "w4a16_debug_inject_stall": (None, [i]),
         "w4a16_gemm_noalloc": (i, [vp, vp, vp, vp, i, i, i, i, vp]),
+        "w4a16_debug_force_path": (None, [i]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -190,6 +192,11 @@ def w4a16_debug_set_wait_cycles(cycles: int) -> None:
 
 def w4a16_debug_inject_stall(enable: bool) -> None:
     _lib().w4a16_debug_inject_stall(1 if enable else 0)
+
+
+def w4a16_debug_force_path(path: int) -> None:
+    """0 = automatic kernel choice, 1 = streaming mma.sync kernel, 2 = tensor-memory kernel."""
+    _lib().w4a16_debug_force_path(int(path))
 
 
 # ---------------------------------------------------------------------------

@@ -62,21 +62,38 @@ int check_shape(int K, int N, int groupsize) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Plan of the streaming kernel for (M, K, N) over `sms` SMs with `smem_optin` bytes of shared memory.
+// Work plan: which kernel runs and how it splits (M, K, N) over `sms` SMs with
+// `smem_optin` bytes of shared memory per CTA.
+constexpr int kTcMinRows = 17;  // from 17 token rows on, the tensor-memory kernel runs
+
 struct Plan {
-  MmaConfig cfg;
-  MmaLayout lay;
-  int m_chunk;
+  int path;          // 1 = streaming mma.sync kernel, 2 = tensor-memory (tcgen05) kernel
+  MmaConfig cfg;     // path 1
+  MmaLayout lay;     // path 1
+  TcLayout tlay;     // path 2
+  int mb, ch;        // path 2: token rows per launch (multiple of 16), 128-row chunks per unit
+  int m_chunk;       // token rows per launch
+  int k_tile;        // reduction rows per work unit
   int srows;
-  int KU, strips, units, T, grid;
+  int KU, strips, units, T, grid, stages, smem_bytes, threads;
   size_t workspace;
 };
 
-Plan make_plan(int M, int K, int N, int G, int sms, int smem_optin) {
+void finish_split(Plan& pl, int K, int sms, size_t slot_floats) {
+  pl.KU = K / pl.k_tile;
+  pl.units = pl.strips * pl.KU;
+  pl.T = (pl.units + sms - 1) / sms;
+  pl.grid = (pl.units + pl.T - 1) / pl.T;
+  const size_t counters = (static_cast<size_t>(pl.strips) * 4 + 255) / 256 * 256;
+  pl.workspace = kStatusBytes + counters + 2ull * pl.grid * slot_floats * sizeof(float);
+}
+
+Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin) {
   Plan pl{};
+  pl.path = 1;
   const int mc = std::min(std::max(M, 1), 32);
   const int mt = mc <= 8 ? 1 : mc <= 16 ? 2 : 4;
-  const int strips = N / kStrip;
+  pl.strips = N / kStrip;
   // Unit depth KT = 64 * kq.  Per-SM time of a unit is modelled from copy-engine
   // measurements on GB300: ~89 ns per 4 KB of weights streamed plus ~80 ns of
   // fixed cost for the unit's three copy operations.  Pick the kq minimising
@@ -91,7 +108,7 @@ Plan make_plan(int M, int K, int N, int G, int sms, int smem_optin) {
     const MmaLayout l0 = mma_layout(mt, kq, srows, 0);
     const int stages = (smem_optin - l0.smem_bytes) / (l0.stage_bytes + 16);
     if (stages < 3 && kq != 2) continue;
-    const long long units = static_cast<long long>(strips) * (K / (64 * kq));
+    const long long units = static_cast<long long>(pl.strips) * (K / (64 * kq));
     const long long T = (units + sms - 1) / sms;
     const long long cost = T * (89LL * kq + 80);
     if (best_kq == 0 || cost < best_cost) {
@@ -113,15 +130,62 @@ Plan make_plan(int M, int K, int N, int G, int sms, int smem_optin) {
   pl.cfg.smem_bytes = pl.lay.smem_bytes;
   pl.cfg.threads = kMmaThreads;
   pl.m_chunk = 8 * mt;
-  pl.KU = K / KT;
-  pl.strips = strips;
-  pl.units = strips * pl.KU;
-  pl.T = (pl.units + sms - 1) / sms;
-  pl.grid = (pl.units + pl.T - 1) / pl.T;
-  const size_t counters = (static_cast<size_t>(strips) * 4 + 255) / 256 * 256;
-  const size_t slots = 2ull * pl.grid * kStrip * (8 * mt) * sizeof(float);
-  pl.workspace = kStatusBytes + counters + slots;
+  pl.k_tile = KT;
+  pl.stages = stages;
+  pl.smem_bytes = pl.lay.smem_bytes;
+  pl.threads = kMmaThreads;
+  finish_split(pl, K, sms, static_cast<size_t>(kStrip) * 8 * mt);
   return pl;
+}
+
+Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin) {
+  Plan pl{};
+  pl.path = 2;
+  pl.mb = std::min(256, (std::max(M, 1) + 15) / 16 * 16);
+  pl.strips = N / kStrip;
+  // Unit depth KT = 128 * ch: the memory time of a unit as for the streaming
+  // kernel (two 4 KB pieces per chunk) against its tensor time (128 x mb x 128*ch
+  // multiply-adds at ~4096 per SM cycle, ~2.1 ns per mb*ch); keep >= 3 stages.
+  int best = 0;
+  long long best_cost = 0;
+  const int cands[3] = {4, 2, 1};
+  for (int c = 0; c < 3; ++c) {
+    const int ch = cands[c];
+    if (K % (128 * ch) != 0) continue;
+    const int srows = (G == 128) ? ch : 1;
+    const TcLayout l0 = tc_layout(pl.mb, ch, srows, 0);
+    const int stages = (smem_optin - l0.smem_bytes) / (l0.stage_bytes + 16);
+    if (stages < 2 || (stages < 3 && ch != 1)) continue;
+    const long long units = static_cast<long long>(pl.strips) * (K / (128 * ch));
+    const long long T = (units + sms - 1) / sms;
+    const long long cost = T * std::max(178LL * ch + 80, (21LL * pl.mb * ch) / 10);
+    if (best == 0 || cost < best_cost) {
+      best = ch;
+      best_cost = cost;
+    }
+  }
+  if (!best) best = 1;
+  pl.ch = best;
+  pl.srows = (G == 128) ? pl.ch : 1;
+  const TcLayout l0 = tc_layout(pl.mb, pl.ch, pl.srows, 0);
+  int stages = (smem_optin - l0.smem_bytes) / (l0.stage_bytes + 16);
+  stages = std::max(2, std::min(stages, 8));
+  pl.tlay = tc_layout(pl.mb, pl.ch, pl.srows, stages);
+  pl.m_chunk = pl.mb;
+  pl.k_tile = 128 * pl.ch;
+  pl.stages = stages;
+  pl.smem_bytes = pl.tlay.smem_bytes;
+  pl.threads = kTcThreads;
+  finish_split(pl, K, sms, static_cast<size_t>(kStrip) * pl.mb);
+  return pl;
+}
+
+std::atomic<int> g_force_path{0};
+
+Plan make_plan(int M, int K, int N, int G, int sms, int smem_optin) {
+  const int forced = g_force_path.load();
+  const bool tc = forced == 2 || (forced == 0 && M >= kTcMinRows);
+  return tc ? make_plan_tc(M, K, N, G, sms, smem_optin) : make_plan_mma(M, K, N, G, sms, smem_optin);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
@@ -200,17 +264,17 @@ int w4a16_plan(int M, int K, int N, int groupsize, int num_sms, w4a16_plan_t* ou
     smem = d->smem_optin;
   }
   const Plan pl = make_plan(M, K, N, effective_group(K, groupsize), sms, smem);
-  out->path = 1;
-  out->m_tiles = pl.cfg.m_tiles;
+  out->path = pl.path;
+  out->m_tiles = pl.m_chunk / 8;
   out->m_chunk = pl.m_chunk;
   out->n_tile = kStrip;
-  out->k_tile = 64 * pl.cfg.kq;
+  out->k_tile = pl.k_tile;
   out->units = pl.units;
   out->units_per_cta = pl.T;
   out->grid = pl.grid;
-  out->stages = pl.cfg.stages;
-  out->smem_bytes = pl.cfg.smem_bytes;
-  out->threads = pl.cfg.threads;
+  out->stages = pl.stages;
+  out->smem_bytes = pl.smem_bytes;
+  out->threads = pl.threads;
   return W4A16_OK;
 }
 
@@ -224,6 +288,8 @@ size_t w4a16_workspace_bytes(int M, int K, int N, int groupsize) {
 void w4a16_debug_set_wait_cycles(long long cycles) { g_wait_cycles.store(cycles > 0 ? cycles : 0); }
 
 void w4a16_debug_inject_stall(int enable) { g_stall.store(enable ? 1 : 0); }
+
+void w4a16_debug_force_path(int path) { g_force_path.store(path == 1 || path == 2 ? path : 0); }
 
 int w4a16_repack(const uint8_t* q, const uint16_t* s, int K, int N, int groupsize, uint32_t* packed,
                  uint16_t* scales_p, void* stream) {
@@ -284,18 +350,62 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* scales
   const Plan pl = make_plan(M, K, N, G, d->sms, d->smem_optin);
   if (workspace_bytes < pl.workspace) return W4A16_ERR_WORKSPACE;
 
+  const long long wc = g_wait_cycles.load();
+  const long long wait_limit = wc > 0 ? wc : kDefaultWaitCycles;
+  const int stall = g_stall.load();
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  uint32_t* counters = reinterpret_cast<uint32_t*>(ws + kStatusBytes);
+  float* slots = reinterpret_cast<float*>(ws + kStatusBytes + (static_cast<size_t>(pl.strips) * 4 + 255) / 256 * 256);
+
   CUtensorMap map;
-  const int er = encode_a_map(&map, A, M, K, pl.m_chunk, pl.cfg.kq);
+  const int er = encode_a_map(&map, A, M, K, pl.m_chunk, pl.path == 2 ? 2 * pl.ch : pl.cfg.kq);
   if (er != W4A16_OK) return er;
 
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (pl.path == 2) {
+    TcParams p{};
+    p.packed = packed;
+    p.scales = scales_p;
+    p.C = C;
+    p.status = status;
+    p.counters = counters;
+    p.slots = slots;
+    p.M = M;
+    p.K = K;
+    p.N = N;
+    p.G = G;
+    p.mb = pl.mb;
+    p.ch = pl.ch;
+    p.srows = pl.srows;
+    p.KU = pl.KU;
+    p.units = pl.units;
+    p.T = pl.T;
+    p.grid = pl.grid;
+    p.stages = pl.stages;
+    p.w_off = pl.tlay.w_off;
+    p.s_off = pl.tlay.s_off;
+    p.stage_bytes = pl.tlay.stage_bytes;
+    p.tx_bytes = pl.tlay.tx_bytes;
+    p.bar_off = pl.tlay.bar_off;
+    p.flag_off = pl.tlay.flag_off;
+    p.idesc = tc_idesc(128, pl.mb);
+    p.wait_limit = wait_limit;
+    p.debug_stall = stall;
+    for (int m0 = 0; m0 < M; m0 += pl.m_chunk) {
+      p.m0 = m0;
+      if (launch_gemm_tc(pl.smem_bytes, map, p, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return W4A16_ERR_CUDA;
+    }
+    return W4A16_OK;
+  }
+
   GemmParams p{};
   p.packed = packed;
   p.scales = scales_p;
   p.C = C;
-  p.status = reinterpret_cast<uint32_t*>(ws);
-  p.counters = reinterpret_cast<uint32_t*>(ws + kStatusBytes);
-  p.slots = reinterpret_cast<float*>(ws + kStatusBytes + (static_cast<size_t>(pl.strips) * 4 + 255) / 256 * 256);
+  p.status = status;
+  p.counters = counters;
+  p.slots = slots;
   p.M = M;
   p.K = K;
   p.N = N;
@@ -314,9 +424,8 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* scales
   p.red_off = pl.lay.red_off;
   p.bar_off = pl.lay.bar_off;
   p.flag_off = pl.lay.flag_off;
-  const long long wc = g_wait_cycles.load();
-  p.wait_limit = wc > 0 ? wc : kDefaultWaitCycles;
-  p.debug_stall = g_stall.load();
+  p.wait_limit = wait_limit;
+  p.debug_stall = stall;
   for (int m0 = 0; m0 < M; m0 += pl.m_chunk) {
     p.m0 = m0;
     const cudaError_t e = launch_gemm_mma(pl.cfg, map, p, static_cast<cudaStream_t>(stream));

@@ -1,0 +1,490 @@
+// Tensor-memory W4A16 GEMM (tcgen05) for larger batches.
+//
+// Once M is large enough that the product is a real dense contraction (the
+// MARLIN paper's roofline, Section 3.4: intensity ~4M FLOP/byte), the legacy
+// mma.sync pipe is the limit.  This kernel feeds the sm_103a 5th-generation
+// tensor cores instead:
+//
+//  * a CTA owns stripes of work units exactly like the streaming kernel: one
+//    128-column strip x KT = 128*CH reduction rows per unit, loaded by one
+//    producer lane with three copy-engine operations (weights, activations as a
+//    swizzled [K/64][M][64] tile, scale rows) into a ring of shared-memory stages;
+//  * two dequant warpgroups decode the 4-bit codes to FP16 (exact q - 8, times
+//    the FP16 group scale with one RNE multiply -- the same value
+//    w4a16_dequant returns) and write them with tcgen05.st.16x256b straight into
+//    tensor memory, where they form the A operand (128 rows = the strip's
+//    output columns, K along the 32-bit columns).  The packed word of lane
+//    (g, t) is that store's fragment: rows g and g + 8, k = 4t .. 4t + 3;
+//  * one thread issues tcgen05.mma.kind::f16 (A from tensor memory, B = the
+//    activation tile through a shared-memory descriptor, FP32 accumulator
+//    D[128 x MB] in tensor memory) and tracks completion with tcgen05.commit on
+//    mbarriers that recycle the A-chunk ring and the stages;
+//  * at the end of each strip segment the first warpgroup reads D back with
+//    tcgen05.ld (one output column per thread, the tokens along registers),
+//    applies the per-column scale when G = K, and writes C -- or, for strips
+//    split between CTAs, FP32 slots reduced by the last arriver in CTA order
+//    (deterministic, no spin waits).
+//
+// Every wait is bounded; a timeout records W4A16_ERR_TIMEOUT, stops all roles,
+// drains copies and MMAs in flight and always frees the tensor memory.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace w4a16 {
+
+namespace {
+
+// warps: 0 producer, 1 MMA issuer + tensor-memory owner, 2..9 dequant (two warpgroups)
+constexpr int kDequantWarps = 8;
+constexpr int kTmemCols = 512;
+constexpr int kChunkCols = 64;           // 128 k of FP16 A = 64 32-bit columns
+constexpr int kNA = 4;                   // A chunks in flight in tensor memory
+constexpr int kDCol = kNA * kChunkCols;  // first accumulator column
+constexpr long long kDrainCycles = 2000000000LL;
+
+// ---- tcgen05 wrappers -------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem descriptor], kind::f16, FP32 accumulate
+__device__ __forceinline__ void tc_mma(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_16x256b_x4(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, "
+      "[%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes in 8-row (1024-byte) atoms.  Fields: start address >> 4 (bits
+// 0..13), leading-dimension byte offset >> 4 (16..29, unused for swizzled
+// K-major: 1), stride byte offset >> 4 (32..45: 1024 bytes between 8-row
+// groups), descriptor version 1 (46..47), layout type 2 = 128-byte swizzle
+// (61..63).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ uint16_t f32_to_f16_bits(float x) { return __half_as_ushort(__float2half_rn(x)); }
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// position of output column r (0..127) of a strip inside its permuted scale row
+__device__ __forceinline__ int scale_pos(int r) { return (r & ~15) + 2 * (r & 7) + ((r >> 3) & 1); }
+
+__global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int S = p.stages;
+  const int CH = p.ch;
+  const int KQ = 2 * CH;
+  const int MB = p.mb;
+  const int A_BOX = MB * 128;
+  const uint32_t bar_full = sbase + p.bar_off;
+  const uint32_t bar_empty = bar_full + 8 * S;
+  const uint32_t bar_afull = bar_empty + 8 * S;
+  const uint32_t bar_aempty = bar_afull + 8 * kNA;
+  const uint32_t bar_dfull = bar_aempty + 8 * kNA;
+  const uint32_t bar_dempty = bar_dfull + 8;
+  const uint32_t bar_drain = bar_dempty + 8;
+  volatile int* flags = reinterpret_cast<volatile int*>(smem + p.flag_off);
+  volatile int* abort_flag = flags + 0;
+  volatile int* last_flag = flags + 1;
+  volatile int* seg_abort = flags + 2;
+  volatile int* zero_flag = flags + 3;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(flags + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int cta = blockIdx.x;
+  const int u_begin = cta * p.T;
+  const int u_end = min(p.units, u_begin + p.T);
+  const int nunits = u_end - u_begin;
+  const int first_col = u_begin / p.KU;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int a = 0; a < kNA; ++a) {
+      mbar_init(bar_afull + 8 * a, kDequantWarps);
+      mbar_init(bar_aempty + 8 * a, 1);
+    }
+    mbar_init(bar_dfull, 1);
+    mbar_init(bar_dempty, 4);
+    mbar_init(bar_drain, 1);
+    for (int i = 0; i < 4; ++i) flags[i] = 0;  // flags[4] receives the tensor-memory address from warp 1
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto raise_abort = [&]() {
+    if (!*abort_flag) {
+      *abort_flag = 1;
+      atomicOr(p.status, kDevErrTimeout);
+    }
+  };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) prefetch_tensormap(&tmA);
+    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_a = policy_evict_last();
+    const int NG = p.K / p.G;
+    const uint32_t w_bytes = static_cast<uint32_t>(KQ) * 4096u;
+    int issued = 0;
+    int s = 0, round = 0;
+    int j = first_col, kt = u_begin - first_col * p.KU;
+    for (int it = 0; it < nunits; ++it) {
+      if (it >= S) {
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait_bounded(bar_empty + 8 * s, (round - 1) & 1, p.wait_limit, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          if (lane == 0) raise_abort();
+          break;
+        }
+      }
+      if (!(p.debug_stall && it == 0)) {  // with debug_stall, stage 0 stays empty: nothing completes its barrier
+        if (lane == 0) {
+          const uint32_t st = sbase + s * p.stage_bytes;
+          const uint32_t fb = bar_full + 8 * s;
+          mbar_arrive_expect_tx(fb, p.tx_bytes);
+          const uint32_t* wsrc =
+              p.packed + (static_cast<long long>(j) * (p.K / 64) + static_cast<long long>(kt) * KQ) * 1024;
+          bulk_g2s(st + p.w_off, wsrc, w_bytes, fb, pol_w);
+          tma_load_3d(st, &tmA, 0, p.m0, kt * KQ, fb, pol_a);
+          const int grp0 = (p.G == 128) ? kt * p.srows : 0;
+          const uint16_t* ssrc = p.scales + (static_cast<long long>(j) * NG + grp0) * 128;
+          bulk_g2s(st + p.s_off, ssrc, static_cast<uint32_t>(p.srows) * 256u, fb, pol_a);
+        }
+        __syncwarp();
+        issued = it + 1;
+      }
+      if (++s == S) {
+        s = 0;
+        ++round;
+      }
+      if (++kt == p.KU) {
+        kt = 0;
+        ++j;
+      }
+    }
+    named_bar_sync(3, kTcThreads);
+    if (*abort_flag && lane == 0) {
+      const int first_filled = p.debug_stall ? 1 : 0;
+      for (int it = max(first_filled, issued - S); it < issued; ++it)
+        mbar_wait_bounded(bar_full + 8 * (it % S), (it / S) & 1, kDrainCycles, zero_flag);
+    }
+    return;
+  }
+
+  if (warp == 1) {
+    // --------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = p.idesc;
+      const uint32_t d_tmem = tmem + kDCol;
+      int s = 0, round = 0, gc = 0, segs = 0;
+      int kt = u_begin - first_col * p.KU;
+      bool seg_first = true;
+      for (int it = 0; it < nunits && !*abort_flag; ++it) {
+        if (!mbar_wait_bounded(bar_full + 8 * s, round & 1, p.wait_limit, abort_flag)) {
+          raise_abort();
+          break;
+        }
+        const uint32_t st = sbase + s * p.stage_bytes;
+        const bool seg_end = (kt == p.KU - 1) || (it == nunits - 1);
+        bool ok = true;
+        for (int c = 0; c < CH && ok; ++c) {
+          const int a = gc % kNA;
+          if (!mbar_wait_bounded(bar_afull + 8 * a, (gc / kNA) & 1, p.wait_limit, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (seg_first && c == 0 && segs > 0) {
+            // the previous segment's accumulator must have been read out
+            if (!mbar_wait_bounded(bar_dempty, (segs - 1) & 1, p.wait_limit, abort_flag)) {
+              ok = false;
+              break;
+            }
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const int piece = 2 * c + (kk >> 2);
+            const uint64_t bdesc = smem_desc_sw128(st + piece * A_BOX + (kk & 3) * 32);
+            const uint32_t acc = (seg_first && c == 0 && kk == 0) ? 0u : 1u;
+            tc_mma(d_tmem, tmem + a * kChunkCols + kk * 8, bdesc, idesc, acc);
+          }
+          tc_commit(bar_aempty + 8 * a);  // A chunk free once these multiplies complete
+          ++gc;
+          seg_first = false;
+        }
+        if (!ok) {
+          raise_abort();
+          break;
+        }
+        tc_commit(bar_empty + 8 * s);  // stage free once the unit's multiplies complete
+        if (seg_end) {
+          tc_commit(bar_dfull);
+          ++segs;
+          seg_first = true;
+        }
+        if (++s == S) {
+          s = 0;
+          ++round;
+        }
+        if (++kt == p.KU) kt = 0;
+      }
+      // wait for every multiply issued so far before the memory is released
+      tc_commit(bar_drain);
+      mbar_wait_bounded(bar_drain, 0, kDrainCycles, zero_flag);
+    }
+    __syncwarp();
+    named_bar_sync(3, kTcThreads);
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+    return;
+  }
+
+  // ----------------------------------------------------------------- dequant
+  const int dw = warp - 2;
+  const int wg = dw >> 2;     // warpgroup: which 64-row piece of each 128-row chunk
+  const int q = warp & 3;     // tensor-memory lane quarter: rows 32q .. 32q + 31 (blocks 2q, 2q + 1)
+  const int g = lane >> 2;
+  const bool grouped = p.G == 128;
+  const int NG = p.K / p.G;
+  int s = 0, round = 0, gc = 0, segs = 0;
+  int j = first_col, kt = u_begin - first_col * p.KU;
+  for (int it = 0; it < nunits; ++it) {
+    const uint32_t st = sbase + s * p.stage_bytes;
+    const bool seg_end = (kt == p.KU - 1) || (it == nunits - 1);
+    const bool go = __shfl_sync(0xffffffffu, *abort_flag == 0, 0);
+    bool have = false;
+    if (go) {
+      have = mbar_wait_bounded(bar_full + 8 * s, round & 1, p.wait_limit, abort_flag);
+      have = __all_sync(0xffffffffu, have);
+      if (!have && lane == 0) raise_abort();
+    }
+    for (int c = 0; c < CH && have; ++c) {
+      const int a = gc % kNA;
+      if (gc >= kNA) {
+        bool ok = mbar_wait_bounded(bar_aempty + 8 * a, ((gc / kNA) - 1) & 1, p.wait_limit, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+          if (lane == 0) raise_abort();
+          have = false;
+          break;
+        }
+      }
+      tc_fence_after();
+      const int kq = 2 * c + wg;
+      const int srow = grouped ? c : 0;  // one group = one 128-row chunk
+#pragma unroll
+      for (int bi = 0; bi < 2; ++bi) {
+        const int b = 2 * q + bi;
+        const uint4 wv = lds128(st + p.w_off + (kq * 8 + b) * 512 + lane * 16);
+        uint32_t s_g = 0x3c003c00u, s_g8 = 0x3c003c00u;  // FP16x2 (1, 1)
+        if (grouped) {
+          const uint32_t sp = lds32(st + p.s_off + (srow * 128 + b * 16 + 2 * g) * 2);
+          s_g = (sp & 0xffffu) * 0x10001u;
+          s_g8 = (sp >> 16) * 0x10001u;
+        }
+        const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+        uint32_t r[16];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          uint32_t v[4];
+          decode8(words[jj], v);
+          if (grouped) {
+            v[0] = hmul2_u32(v[0], s_g);
+            v[1] = hmul2_u32(v[1], s_g8);
+            v[2] = hmul2_u32(v[2], s_g);
+            v[3] = hmul2_u32(v[3], s_g8);
+          }
+          // .16x256b fragment order: (row g, col 2t), (row g, col 2t+1), (row g+8, col 2t), (row g+8, col 2t+1)
+          r[4 * jj + 0] = v[0];
+          r[4 * jj + 1] = v[2];
+          r[4 * jj + 2] = v[1];
+          r[4 * jj + 3] = v[3];
+        }
+        tmem_st_16x256b_x4(tmem + (static_cast<uint32_t>(32 * q + 16 * bi) << 16) + a * kChunkCols + wg * 32, r);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_afull + 8 * a);
+      ++gc;
+    }
+    if (seg_end && wg == 0) {
+      // ------------------------------------------------------ epilogue (strip j)
+      named_bar_sync(1, 128);
+      if (warp == 2 && lane == 0) *seg_abort = *abort_flag;
+      named_bar_sync(1, 128);
+      if (!*seg_abort) {
+        bool ok = mbar_wait_bounded(bar_dfull, segs & 1, p.wait_limit, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok && lane == 0) raise_abort();
+        named_bar_sync(1, 128);
+        if (warp == 2 && lane == 0) *seg_abort = *abort_flag;
+        named_bar_sync(1, 128);
+      }
+      if (!*seg_abort) {
+        tc_fence_after();
+        const int row = 32 * q + lane;
+        const int n = j * kStrip + row;
+        const float scale =
+            grouped ? 1.f
+                    : __half2float(__ushort_as_half(p.scales[static_cast<long long>(j) * NG * 128 + scale_pos(row)]));
+        const int c_first = (j * p.KU) / p.T;
+        const int c_last = min(((j + 1) * p.KU - 1) / p.T, p.grid - 1);
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + kDCol;
+        const int nchunks = MB / 16;
+        if (c_first == c_last) {
+          for (int ch = 0; ch < nchunks; ++ch) {
+            uint32_t v[16];
+            tmem_ld_32x32b_x16(taddr + ch * 16, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int token = p.m0 + ch * 16 + i;
+              if (token < p.M) p.C[static_cast<long long>(token) * p.N + n] = f32_to_f16_bits(__uint_as_float(v[i]) * scale);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_dempty);
+        } else {
+          // strip split between CTAs: FP32 partial [token][row] into this CTA's slot
+          const int slot = (j == first_col) ? 2 * cta : 2 * cta + 1;
+          float* dst = p.slots + static_cast<long long>(slot) * (128 * MB);
+          for (int ch = 0; ch < nchunks; ++ch) {
+            uint32_t v[16];
+            tmem_ld_32x32b_x16(taddr + ch * 16, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) dst[(ch * 16 + i) * 128 + row] = __uint_as_float(v[i]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_dempty);
+          __threadfence();
+          named_bar_sync(2, 128);
+          if (warp == 2 && lane == 0) {
+            const unsigned old = atomicAdd(p.counters + j, 1u);
+            *last_flag = (old == static_cast<unsigned>(c_last - c_first)) ? 1 : 0;
+          }
+          named_bar_sync(2, 128);
+          if (*last_flag) {
+            __threadfence();
+            for (int m = 0; m < MB; ++m) {
+              const int token = p.m0 + m;
+              if (token >= p.M) break;
+              float acc = 0.f;
+              for (int c = c_first; c <= c_last; ++c) {
+                const int cslot = (j == (c * p.T) / p.KU) ? 2 * c : 2 * c + 1;
+                acc += __ldcg(p.slots + static_cast<long long>(cslot) * (128 * MB) + m * 128 + row);
+              }
+              p.C[static_cast<long long>(token) * p.N + n] = f32_to_f16_bits(acc * scale);
+            }
+            if (warp == 2 && lane == 0) p.counters[j] = 0u;
+          }
+        }
+      }
+      ++segs;
+    }
+    if (++s == S) {
+      s = 0;
+      ++round;
+    }
+    if (++kt == p.KU) {
+      kt = 0;
+      ++j;
+    }
+  }
+  named_bar_sync(3, kTcThreads);
+}
+
+}  // namespace
+
+TcLayout tc_layout(int mb, int ch, int srows, int stages) {
+  TcLayout l{};
+  const int kq = 2 * ch;
+  l.w_off = kq * mb * 128;
+  l.s_off = l.w_off + kq * 4096;
+  l.stage_bytes = (l.s_off + srows * 256 + 1023) / 1024 * 1024;
+  l.tx_bytes = kq * mb * 128 + kq * 4096 + srows * 256;
+  l.bar_off = stages * l.stage_bytes;
+  l.flag_off = l.bar_off + 8 * (2 * stages + 2 * kNA + 3);
+  l.smem_bytes = 1024 + l.flag_off + 64;
+  return l;
+}
+
+// instruction descriptor, kind::f16: D = F32 (bits 4..5 = 1), A = B = F16 (bits 7..12 = 0),
+// both K-major (bits 15, 16 = 0), N >> 3 in bits 17..22, M >> 4 in bits 24..28
+uint32_t tc_idesc(int m, int n) {
+  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+cudaError_t launch_gemm_tc(int smem_bytes, const CUtensorMap& tmA, const TcParams& p, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) return e;
+  gemm_tc_kernel<<<p.grid, kTcThreads, smem_bytes, stream>>>(tmA, p);
+  return cudaGetLastError();
+}
+
+}  // namespace w4a16

@@ -59,6 +59,35 @@ constexpr int kStrip = 128;       // output columns per strip / work unit
 
 cudaError_t launch_gemm_mma(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream);
 
+// ---- tensor-memory (tcgen05) GEMM ----------------------------------------
+constexpr int kTcThreads = 320;  // producer, MMA issuer, 8 dequant warps
+
+struct TcLayout {
+  int w_off, s_off, stage_bytes, tx_bytes, bar_off, flag_off, smem_bytes;
+};
+TcLayout tc_layout(int mb, int ch, int srows, int stages);
+uint32_t tc_idesc(int m, int n);
+
+struct TcParams {
+  const uint32_t* packed;
+  const uint16_t* scales;
+  uint16_t* C;
+  uint32_t* status;
+  uint32_t* counters;
+  float* slots;             // 2 * grid slots of 128 * mb floats ([token][column])
+  int M, m0, K, N, G;
+  int mb;                   // token rows of this launch padded to 16 (the MMA's N)
+  int ch;                   // 128-row chunks per work unit (KT = 128 * ch)
+  int srows;                // scale rows per unit
+  int KU, units, T, grid, stages;
+  int w_off, s_off, stage_bytes, tx_bytes, bar_off, flag_off;
+  uint32_t idesc;
+  long long wait_limit;
+  int debug_stall;
+};
+
+cudaError_t launch_gemm_tc(int smem_bytes, const CUtensorMap& tmA, const TcParams& p, cudaStream_t stream);
+
 cudaError_t launch_repack(const uint8_t* q, const uint16_t* s, int K, int N, int G, uint32_t* packed,
                           uint16_t* scales_p, cudaStream_t stream);
 cudaError_t launch_unpack(const uint32_t* packed, const uint16_t* scales_p, int K, int N, int G, uint8_t* q,

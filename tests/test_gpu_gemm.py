@@ -19,13 +19,21 @@ def w():
     return tl.lib()
 
 
+@pytest.fixture(params=[1, 2], ids=["mma_sync", "tcgen05"])
+def path(request, w):
+    """Run the test on the streaming mma.sync kernel and on the tensor-memory kernel."""
+    w.w4a16_debug_force_path(request.param)
+    yield request.param
+    w.w4a16_debug_force_path(0)
+
+
 # token counts around every 8-row tile edge and the 64-row launch chunk
 M_EDGES = [1, 2, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 100, 128, 129]
 
 
 @pytest.mark.parametrize("M", M_EDGES)
 @pytest.mark.parametrize("G", [128, -1])
-def test_gemm_parity_small_layer(w, M, G):
+def test_gemm_parity_small_layer(w, path, M, G):
     K, N = 1024, 1024
     A, q, s = tl.layer(M, K, N, G, seed=100 + M)
     _, _, packed, sp = tl.device_layer(w, q, s, G)
@@ -43,7 +51,7 @@ def test_gemm_parity_small_layer(w, M, G):
     (40, 4096, 640, -1),
     (9, 1536, 1280, 128),       # K/256 odd: 256-row units
 ])
-def test_gemm_parity_shapes(w, M, K, N, G):
+def test_gemm_parity_shapes(w, path, M, K, N, G):
     A, q, s = tl.layer(M, K, N, G, seed=M + K + N)
     _, _, packed, sp = tl.device_layer(w, q, s, G)
     C = tl.c_numpy(tl.run_gemm(w, A, packed, sp, N, G))
@@ -52,7 +60,7 @@ def test_gemm_parity_shapes(w, M, K, N, G):
 
 
 @pytest.mark.parametrize("G", [128, -1])
-def test_identity_rows_return_dequantised_weights_exactly(w, G):
+def test_identity_rows_return_dequantised_weights_exactly(w, path, G):
     K, N = 2048, 512
     q, s = synth.make_weights(K, N, G, seed=31)
     rows = [0, 1, 63, 64, 127, 128, 1000, 2047, 5, 77, 1500, 640, 641, 1919, 300, 301, 999]
@@ -65,7 +73,7 @@ def test_identity_rows_return_dequantised_weights_exactly(w, G):
     assert np.array_equal(C.view(np.uint16), ref)
 
 
-def test_integer_gemm_is_exact(w):
+def test_integer_gemm_is_exact(w, path):
     # s = 1, small integer activations: every partial sum is an exact FP32 integer below 2048
     rng = np.random.default_rng(12)
     M, K, N, G = 16, 256, 256, 128
@@ -80,7 +88,7 @@ def test_integer_gemm_is_exact(w):
 
 
 @pytest.mark.parametrize("K", [1024, 18432])
-def test_zero_codes_stay_within_the_absolute_bound(w, K):
+def test_zero_codes_stay_within_the_absolute_bound(w, path, K):
     # q == 8 everywhere: B^ = 0, so Bound = 0 and every output must satisfy |C| <= 1e-4.
     # The kernel multiplies biased codes (1024 + q or 64 + q) and removes the bias with the
     # activations' row sums, so here it sees only the cancellation error of that step;
@@ -96,7 +104,7 @@ def test_zero_codes_stay_within_the_absolute_bound(w, K):
 
 
 @pytest.mark.parametrize("M", [1, 16, 33])
-def test_repeated_calls_are_bitwise_identical(w, M):
+def test_repeated_calls_are_bitwise_identical(w, path, M):
     torch = tl.torch_mod()
     K, N, G = 4096, 2048, 128
     A, q, s = tl.layer(M, K, N, G, seed=77)
@@ -109,7 +117,7 @@ def test_repeated_calls_are_bitwise_identical(w, M):
     assert w.w4a16_get_status(ws) == 0
 
 
-def test_column_block_permutation_permutes_output(w):
+def test_column_block_permutation_permutes_output(w, path):
     # Permuting the 16-column blocks of (q, s) permutes C's columns bit for bit.  (A column's
     # place inside its block picks its decode bias, 256 or 16, so only block moves are exact;
     # any column permutation still agrees within the parity bound, as every parity test shows.)
@@ -124,7 +132,7 @@ def test_column_block_permutation_permutes_output(w):
     assert np.array_equal(C1[:, perm].view(np.uint16), C2.view(np.uint16))
 
 
-def test_group_invariance(w):
+def test_group_invariance(w, path):
     # a scale constant over the groups of each column: group 128 and per-column agree within the bound
     M, K, N = 16, 2048, 512
     A, q, s1 = tl.layer(M, K, N, -1, seed=15)
@@ -138,7 +146,7 @@ def test_group_invariance(w):
     tl.assert_within_bound(Cb, C_ref, bound, "G=K")
 
 
-def test_workspace_reuse_across_shapes(w):
+def test_workspace_reuse_across_shapes(w, path):
     # counters are left at zero, so one zeroed workspace serves a sequence of calls
     torch = tl.torch_mod()
     big = max(w.w4a16_workspace_bytes(M, 4096, 4096, 128) for M in (1, 16, 32, 64))
@@ -176,7 +184,7 @@ def test_gemm_error_codes(w):
     w.w4a16_gemm(A_d, packed, sp, C, 0, K, N, G, ws)  # M == 0: no-op
 
 
-def test_timeout_is_reported_and_context_survives(w):
+def test_timeout_is_reported_and_context_survives(w, path):
     # Failure injection on the host side of the wait: the first stage of every CTA is never
     # filled, so the consumers' first wait can only end by running out of its (short) bound.
     # The kernel records W4A16_ERR_TIMEOUT, writes nothing and returns; the context stays usable.
