@@ -72,6 +72,7 @@ struct Plan {
   MmaLayout lay;     // path 1
   TcLayout tlay;     // path 2
   int mb, ch;        // path 2: token rows per launch (multiple of 16), 128-row chunks per unit
+  int a_stages, w_stages;  // path 2: activation / weight ring depths
   int m_chunk;       // token rows per launch
   int k_tile;        // reduction rows per work unit
   int srows;
@@ -143,37 +144,46 @@ Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin) {
   pl.path = 2;
   pl.mb = std::min(256, (std::max(M, 1) + 15) / 16 * 16);
   pl.strips = N / kStrip;
-  // Unit depth KT = 128 * ch: the memory time of a unit as for the streaming
-  // kernel (two 4 KB pieces per chunk) against its tensor time (128 x mb x 128*ch
-  // multiply-adds at ~4096 per SM cycle, ~2.1 ns per mb*ch); keep >= 3 stages.
-  int best = 0;
+  // Unit depth KT = 128 * ch for the weight ring (one copy per unit, released by
+  // the dequant warps); activations are staged per 128-row chunk (released by
+  // the multiply that reads them).  Keep >= 4 activation chunks and >= 128 KB of
+  // weights in flight; among those, minimise T * unit time (memory time as for
+  // the streaming kernel vs tensor time, ~2.1 ns per mb * ch).
+  int best = 0, best_a = 0, best_w = 0;
   long long best_cost = 0;
   const int cands[3] = {4, 2, 1};
   for (int c = 0; c < 3; ++c) {
     const int ch = cands[c];
     if (K % (128 * ch) != 0) continue;
     const int srows = (G == 128) ? ch : 1;
-    const TcLayout l0 = tc_layout(pl.mb, ch, srows, 0);
-    const int stages = (smem_optin - l0.smem_bytes) / (l0.stage_bytes + 16);
-    if (stages < 2 || (stages < 3 && ch != 1)) continue;
+    const int a_st = pl.mb <= 64 ? 6 : (pl.mb <= 128 ? 3 : 2);
+    const TcLayout l0 = tc_layout(pl.mb, ch, srows, a_st, 0);
+    const int w_st = std::min(12, (smem_optin - l0.smem_bytes) / (l0.w_stage_bytes + 16));
+    if (w_st < 2 || w_st * ch < 8) continue;
     const long long units = static_cast<long long>(pl.strips) * (K / (128 * ch));
     const long long T = (units + sms - 1) / sms;
-    const long long cost = T * std::max(178LL * ch + 80, (21LL * pl.mb * ch) / 10);
+    const long long cost = T * (std::max(178LL * ch, (21LL * pl.mb * ch) / 10) + 200);  // + per-unit sync and copy issue
     if (best == 0 || cost < best_cost) {
       best = ch;
+      best_a = a_st;
+      best_w = w_st;
       best_cost = cost;
     }
   }
-  if (!best) best = 1;
+  if (!best) {
+    best = 1;
+    best_a = 2;
+    const TcLayout l0 = tc_layout(pl.mb, 1, 1, 2, 0);
+    best_w = std::max(2, std::min(12, (smem_optin - l0.smem_bytes) / (l0.w_stage_bytes + 16)));
+  }
   pl.ch = best;
   pl.srows = (G == 128) ? pl.ch : 1;
-  const TcLayout l0 = tc_layout(pl.mb, pl.ch, pl.srows, 0);
-  int stages = (smem_optin - l0.smem_bytes) / (l0.stage_bytes + 16);
-  stages = std::max(2, std::min(stages, 8));
-  pl.tlay = tc_layout(pl.mb, pl.ch, pl.srows, stages);
+  pl.tlay = tc_layout(pl.mb, pl.ch, pl.srows, best_a, best_w);
+  pl.a_stages = best_a;
+  pl.w_stages = best_w;
   pl.m_chunk = pl.mb;
   pl.k_tile = 128 * pl.ch;
-  pl.stages = stages;
+  pl.stages = best_w;
   pl.smem_bytes = pl.tlay.smem_bytes;
   pl.threads = kTcThreads;
   finish_split(pl, K, sms, static_cast<size_t>(kStrip) * pl.mb);
@@ -359,7 +369,8 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* scales
   float* slots = reinterpret_cast<float*>(ws + kStatusBytes + (static_cast<size_t>(pl.strips) * 4 + 255) / 256 * 256);
 
   CUtensorMap map;
-  const int er = encode_a_map(&map, A, M, K, pl.m_chunk, pl.path == 2 ? 2 * pl.ch : pl.cfg.kq);
+  // activation box depth: one 128-row chunk (2 pieces) per copy on path 2, one unit (kq pieces) on path 1
+  const int er = encode_a_map(&map, A, M, K, pl.m_chunk, pl.path == 2 ? 2 : pl.cfg.kq);
   if (er != W4A16_OK) return er;
 
   if (pl.path == 2) {
@@ -376,16 +387,18 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* scales
     p.G = G;
     p.mb = pl.mb;
     p.ch = pl.ch;
+    p.na = 4;                                    // A chunks in the tensor-memory ring: 256 columns
+    p.ni = std::max(1, std::min(4, 256 / pl.mb));  // accumulators: ni * mb <= 256 columns
     p.srows = pl.srows;
     p.KU = pl.KU;
     p.units = pl.units;
     p.T = pl.T;
     p.grid = pl.grid;
-    p.stages = pl.stages;
-    p.w_off = pl.tlay.w_off;
-    p.s_off = pl.tlay.s_off;
-    p.stage_bytes = pl.tlay.stage_bytes;
-    p.tx_bytes = pl.tlay.tx_bytes;
+    p.a_stages = pl.a_stages;
+    p.w_stages = pl.w_stages;
+    p.a_stage_bytes = pl.tlay.a_stage_bytes;
+    p.w_stage_bytes = pl.tlay.w_stage_bytes;
+    p.w_base = pl.tlay.w_base;
     p.bar_off = pl.tlay.bar_off;
     p.flag_off = pl.tlay.flag_off;
     p.idesc = tc_idesc(128, pl.mb);

@@ -64,6 +64,34 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// try_wait with a suspend-time hint: the thread may sleep (up to `ns`) until
+// the phase completes instead of re-polling, leaving issue slots to other warps.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return done != 0;
+}
+
+// Like mbar_wait_bounded, but the thread sleeps between polls, leaving issue
+// slots to the warps that do the arithmetic.  For single-thread roles (copy
+// issue, MMA issue) whose waits tolerate a little wake-up latency.
+__device__ __forceinline__ bool mbar_wait_bounded_sleep(uint32_t bar, uint32_t parity, long long limit,
+                                                        const volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 2000u)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > limit) return false;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // L2 cache policies and bulk / tensor copies into shared memory
 // ---------------------------------------------------------------------------

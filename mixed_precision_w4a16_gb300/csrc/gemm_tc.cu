@@ -36,12 +36,12 @@ namespace w4a16 {
 
 namespace {
 
-// warps: 0 producer, 1 MMA issuer + tensor-memory owner, 2..9 dequant (two warpgroups)
-constexpr int kDequantWarps = 8;
+// warps: 0 weight producer, 1 MMA issuer 0 + tensor-memory owner, 2 activation producer,
+// 3..10 dequant (two warpgroups), 11..13 MMA issuers 1..3
+constexpr int kDequantWarps = 8;  // warps 3..10: two warpgroups
 constexpr int kTmemCols = 512;
 constexpr int kChunkCols = 64;           // 128 k of FP16 A = 64 32-bit columns
-constexpr int kNA = 4;                   // A chunks in flight in tensor memory
-constexpr int kDCol = kNA * kChunkCols;  // first accumulator column
+constexpr int kMaxNA = 7;                // A chunks in flight in tensor memory (p.na <= 7)
 constexpr long long kDrainCycles = 2000000000LL;
 
 // ---- tcgen05 wrappers -------------------------------------------------------
@@ -121,16 +121,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  const int S = p.stages;
+  const int SA = p.a_stages;         // activation ring, one 128-row chunk per stage (released by the MMA commit)
+  const int SW = p.w_stages;         // weight + scale ring (released by the dequant warps)
   const int CH = p.ch;
   const int KQ = 2 * CH;
   const int MB = p.mb;
   const int A_BOX = MB * 128;
-  const uint32_t bar_full = sbase + p.bar_off;
-  const uint32_t bar_empty = bar_full + 8 * S;
-  const uint32_t bar_afull = bar_empty + 8 * S;
-  const uint32_t bar_aempty = bar_afull + 8 * kNA;
-  const uint32_t bar_dfull = bar_aempty + 8 * kNA;
+  const int NA = p.na;               // A-chunk ring depth in tensor memory; the accumulators follow it
+  const int NI = p.ni;               // MMA-issuing threads, each with its own accumulator region
+  const int kDCol = NA * kChunkCols;
+  const uint32_t bar_afull = sbase + p.bar_off;      // activation stage landed
+  const uint32_t bar_aempty = bar_afull + 8 * SA;    // activation stage read by the MMAs
+  const uint32_t bar_wfull = bar_aempty + 8 * SA;    // weight stage landed
+  const uint32_t bar_wempty = bar_wfull + 8 * SW;    // weight stage read by the dequant warps
+  const uint32_t bar_cfull = bar_wempty + 8 * SW;    // A chunk written to tensor memory
+  const uint32_t bar_cempty = bar_cfull + 8 * kMaxNA;  // A chunk consumed by the MMAs
+  const uint32_t bar_dfull = bar_cempty + 8 * kMaxNA;
   const uint32_t bar_dempty = bar_dfull + 8;
   const uint32_t bar_drain = bar_dempty + 8;
   volatile int* flags = reinterpret_cast<volatile int*>(smem + p.flag_off);
@@ -147,19 +153,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   const int u_end = min(p.units, u_begin + p.T);
   const int nunits = u_end - u_begin;
   const int first_col = u_begin / p.KU;
+  const int kt0 = u_begin - first_col * p.KU;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(bar_afull + 8 * s, 1);
+      mbar_init(bar_aempty + 8 * s, 1);
     }
-    for (int a = 0; a < kNA; ++a) {
-      mbar_init(bar_afull + 8 * a, kDequantWarps);
-      mbar_init(bar_aempty + 8 * a, 1);
+    for (int s = 0; s < SW; ++s) {
+      mbar_init(bar_wfull + 8 * s, 1);
+      mbar_init(bar_wempty + 8 * s, kDequantWarps);
     }
-    mbar_init(bar_dfull, 1);
+    for (int a = 0; a < NA; ++a) {
+      mbar_init(bar_cfull + 8 * a, kDequantWarps);
+      mbar_init(bar_cempty + 8 * a, 1);
+    }
+    mbar_init(bar_dfull, NI);
     mbar_init(bar_dempty, 4);
-    mbar_init(bar_drain, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(bar_drain + 8 * i, 1);
     for (int i = 0; i < 4; ++i) flags[i] = 0;  // flags[4] receives the tensor-memory address from warp 1
     mbar_fence_init();
   }
@@ -179,20 +190,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     }
   };
 
-  if (warp == 0) {
-    // ---------------------------------------------------------------- producer
-    if (lane == 0) prefetch_tensormap(&tmA);
-    const uint64_t pol_w = policy_evict_first();
-    const uint64_t pol_a = policy_evict_last();
+  if (warp == 0 || warp == 2) {
+    // ------------------------------------------- producers: warp 0 weights + scales (one stage per unit),
+    //                                               warp 2 activations (one stage per 128-row chunk)
+    const bool wprod = warp == 0;
+    const int S = wprod ? SW : SA;
+    const uint32_t full = wprod ? bar_wfull : bar_afull;
+    const uint32_t empty = wprod ? bar_wempty : bar_aempty;
+    if (!wprod && lane == 0) prefetch_tensormap(&tmA);
+    const uint64_t pol = wprod ? policy_evict_first() : policy_evict_last();
+    const uint64_t pol_s = policy_evict_last();
     const int NG = p.K / p.G;
     const uint32_t w_bytes = static_cast<uint32_t>(KQ) * 4096u;
+    const int steps = wprod ? nunits : nunits * CH;  // stages to fill
     int issued = 0;
     int s = 0, round = 0;
-    int j = first_col, kt = u_begin - first_col * p.KU;
-    for (int it = 0; it < nunits; ++it) {
+    int j = first_col, kt = kt0, c = 0;
+    for (int it = 0; it < steps; ++it) {
       if (it >= S) {
         bool ok = true;
-        if (lane == 0) ok = mbar_wait_bounded(bar_empty + 8 * s, (round - 1) & 1, p.wait_limit, abort_flag);
+        if (lane == 0) ok = mbar_wait_bounded_sleep(empty + 8 * s, (round - 1) & 1, p.wait_limit, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) {
           if (lane == 0) raise_abort();
@@ -201,16 +218,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       }
       if (!(p.debug_stall && it == 0)) {  // with debug_stall, stage 0 stays empty: nothing completes its barrier
         if (lane == 0) {
-          const uint32_t st = sbase + s * p.stage_bytes;
-          const uint32_t fb = bar_full + 8 * s;
-          mbar_arrive_expect_tx(fb, p.tx_bytes);
-          const uint32_t* wsrc =
-              p.packed + (static_cast<long long>(j) * (p.K / 64) + static_cast<long long>(kt) * KQ) * 1024;
-          bulk_g2s(st + p.w_off, wsrc, w_bytes, fb, pol_w);
-          tma_load_3d(st, &tmA, 0, p.m0, kt * KQ, fb, pol_a);
-          const int grp0 = (p.G == 128) ? kt * p.srows : 0;
-          const uint16_t* ssrc = p.scales + (static_cast<long long>(j) * NG + grp0) * 128;
-          bulk_g2s(st + p.s_off, ssrc, static_cast<uint32_t>(p.srows) * 256u, fb, pol_a);
+          const uint32_t fb = full + 8 * s;
+          if (wprod) {
+            const uint32_t st = sbase + p.w_base + s * p.w_stage_bytes;
+            mbar_arrive_expect_tx(fb, w_bytes + static_cast<uint32_t>(p.srows) * 256u);
+            const uint32_t* wsrc =
+                p.packed + (static_cast<long long>(j) * (p.K / 64) + static_cast<long long>(kt) * KQ) * 1024;
+            bulk_g2s(st, wsrc, w_bytes, fb, pol);
+            const int grp0 = (p.G == 128) ? kt * p.srows : 0;
+            const uint16_t* ssrc = p.scales + (static_cast<long long>(j) * NG + grp0) * 128;
+            bulk_g2s(st + w_bytes, ssrc, static_cast<uint32_t>(p.srows) * 256u, fb, pol_s);
+          } else {
+            const uint32_t st = sbase + s * p.a_stage_bytes;
+            mbar_arrive_expect_tx(fb, static_cast<uint32_t>(2 * A_BOX));
+            tma_load_3d(st, &tmA, 0, p.m0, kt * KQ + 2 * c, fb, pol);
+          }
         }
         __syncwarp();
         issued = it + 1;
@@ -219,168 +241,186 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         s = 0;
         ++round;
       }
-      if (++kt == p.KU) {
-        kt = 0;
-        ++j;
+      if (wprod || ++c == CH) {
+        c = 0;
+        if (++kt == p.KU) {
+          kt = 0;
+          ++j;
+        }
       }
     }
     named_bar_sync(3, kTcThreads);
     if (*abort_flag && lane == 0) {
       const int first_filled = p.debug_stall ? 1 : 0;
       for (int it = max(first_filled, issued - S); it < issued; ++it)
-        mbar_wait_bounded(bar_full + 8 * (it % S), (it / S) & 1, kDrainCycles, zero_flag);
+        mbar_wait_bounded(full + 8 * (it % S), (it / S) & 1, kDrainCycles, zero_flag);
     }
     return;
   }
 
-  if (warp == 1) {
-    // --------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+  const int issuer = (warp == 1) ? 0 : (warp >= 11 ? warp - 10 : -1);
+  if (issuer >= 0) {
+    // ------------------------------------------------------------- MMA issuers
+    // A single thread can issue a tcgen05.mma only every ~90 cycles, far below the
+    // tensor core's rate for small N; NI threads therefore issue in parallel, each
+    // taking every NI-th 128-row chunk of a strip segment into its own accumulator.
+    if (lane == 0 && issuer < NI) {
       const uint32_t idesc = p.idesc;
-      const uint32_t d_tmem = tmem + kDCol;
-      int s = 0, round = 0, gc = 0, segs = 0;
-      int kt = u_begin - first_col * p.KU;
-      bool seg_first = true;
+      const uint32_t d_tmem = tmem + kDCol + issuer * MB;
+      int gc = 0, segs = 0, cs = 0;
+      int kt = kt0;
+      bool mine_first = true;  // next chunk of this issuer starts its accumulator for the segment
       for (int it = 0; it < nunits && !*abort_flag; ++it) {
-        if (!mbar_wait_bounded(bar_full + 8 * s, round & 1, p.wait_limit, abort_flag)) {
-          raise_abort();
-          break;
-        }
-        const uint32_t st = sbase + s * p.stage_bytes;
         const bool seg_end = (kt == p.KU - 1) || (it == nunits - 1);
         bool ok = true;
-        for (int c = 0; c < CH && ok; ++c) {
-          const int a = gc % kNA;
-          if (!mbar_wait_bounded(bar_afull + 8 * a, (gc / kNA) & 1, p.wait_limit, abort_flag)) {
+        for (int c = 0; c < CH && ok; ++c, ++gc, ++cs) {
+          if (cs % NI != issuer) continue;
+          const int sa = gc % SA;  // activation stage of this chunk
+          const int a = gc % NA;   // tensor-memory A buffer of this chunk
+          if (!mbar_wait_bounded_sleep(bar_afull + 8 * sa, (gc / SA) & 1, p.wait_limit, abort_flag) ||
+              !mbar_wait_bounded_sleep(bar_cfull + 8 * a, (gc / NA) & 1, p.wait_limit, abort_flag)) {
             ok = false;
             break;
           }
-          if (seg_first && c == 0 && segs > 0) {
-            // the previous segment's accumulator must have been read out
+          if (mine_first && segs > 0) {
+            // the previous segment's accumulators must have been read out
             if (!mbar_wait_bounded(bar_dempty, (segs - 1) & 1, p.wait_limit, abort_flag)) {
               ok = false;
               break;
             }
           }
           tc_fence_after();
+          const uint32_t st = sbase + sa * p.a_stage_bytes;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const int piece = 2 * c + (kk >> 2);
-            const uint64_t bdesc = smem_desc_sw128(st + piece * A_BOX + (kk & 3) * 32);
-            const uint32_t acc = (seg_first && c == 0 && kk == 0) ? 0u : 1u;
+            const uint64_t bdesc = smem_desc_sw128(st + (kk >> 2) * A_BOX + (kk & 3) * 32);
+            const uint32_t acc = (mine_first && kk == 0) ? 0u : 1u;
             tc_mma(d_tmem, tmem + a * kChunkCols + kk * 8, bdesc, idesc, acc);
           }
-          tc_commit(bar_aempty + 8 * a);  // A chunk free once these multiplies complete
-          ++gc;
-          seg_first = false;
+          tc_commit(bar_cempty + 8 * a);   // A chunk free once these multiplies complete
+          tc_commit(bar_aempty + 8 * sa);  // activation stage free likewise
+          mine_first = false;
         }
         if (!ok) {
           raise_abort();
           break;
         }
-        tc_commit(bar_empty + 8 * s);  // stage free once the unit's multiplies complete
         if (seg_end) {
           tc_commit(bar_dfull);
           ++segs;
-          seg_first = true;
-        }
-        if (++s == S) {
-          s = 0;
-          ++round;
+          cs = 0;
+          mine_first = true;
         }
         if (++kt == p.KU) kt = 0;
       }
-      // wait for every multiply issued so far before the memory is released
-      tc_commit(bar_drain);
-      mbar_wait_bounded(bar_drain, 0, kDrainCycles, zero_flag);
+      // wait for every multiply this thread issued before the memory is released
+      tc_commit(bar_drain + 8 * issuer);
+      mbar_wait_bounded(bar_drain + 8 * issuer, 0, kDrainCycles, zero_flag);
     }
     __syncwarp();
     named_bar_sync(3, kTcThreads);
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem, kTmemCols);
+    }
     return;
   }
 
   // ----------------------------------------------------------------- dequant
-  const int dw = warp - 2;
+  const int dw = warp - 3;
   const int wg = dw >> 2;     // warpgroup: which 64-row piece of each 128-row chunk
   const int q = warp & 3;     // tensor-memory lane quarter: rows 32q .. 32q + 31 (blocks 2q, 2q + 1)
   const int g = lane >> 2;
   const bool grouped = p.G == 128;
   const int NG = p.K / p.G;
-  int s = 0, round = 0, gc = 0, segs = 0;
-  int j = first_col, kt = u_begin - first_col * p.KU;
+  const bool epi_lead = warp == 3;  // first warp of warpgroup 0
+  int s = 0, round = 0, gc = 0, segs = 0, seg_units = 0;
+  int j = first_col, kt = kt0;
   for (int it = 0; it < nunits; ++it) {
-    const uint32_t st = sbase + s * p.stage_bytes;
+    const uint32_t st = sbase + p.w_base + s * p.w_stage_bytes;
+    ++seg_units;
     const bool seg_end = (kt == p.KU - 1) || (it == nunits - 1);
     const bool go = __shfl_sync(0xffffffffu, *abort_flag == 0, 0);
     bool have = false;
     if (go) {
-      have = mbar_wait_bounded(bar_full + 8 * s, round & 1, p.wait_limit, abort_flag);
+      have = mbar_wait_bounded(bar_wfull + 8 * s, round & 1, p.wait_limit, abort_flag);
       have = __all_sync(0xffffffffu, have);
       if (!have && lane == 0) raise_abort();
     }
-    for (int c = 0; c < CH && have; ++c) {
-      const int a = gc % kNA;
-      if (gc >= kNA) {
-        bool ok = mbar_wait_bounded(bar_aempty + 8 * a, ((gc / kNA) - 1) & 1, p.wait_limit, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) {
-          if (lane == 0) raise_abort();
-          have = false;
-          break;
-        }
-      }
-      tc_fence_after();
-      const int kq = 2 * c + wg;
-      const int srow = grouped ? c : 0;  // one group = one 128-row chunk
+    if (have) {
+      // read this warp's share of the unit's weights and scales, then release the stage
+      uint4 wv[4][2];
+      uint32_t sc[4][2];
 #pragma unroll
-      for (int bi = 0; bi < 2; ++bi) {
-        const int b = 2 * q + bi;
-        const uint4 wv = lds128(st + p.w_off + (kq * 8 + b) * 512 + lane * 16);
-        uint32_t s_g = 0x3c003c00u, s_g8 = 0x3c003c00u;  // FP16x2 (1, 1)
-        if (grouped) {
-          const uint32_t sp = lds32(st + p.s_off + (srow * 128 + b * 16 + 2 * g) * 2);
-          s_g = (sp & 0xffffu) * 0x10001u;
-          s_g8 = (sp >> 16) * 0x10001u;
-        }
-        const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
-        uint32_t r[16];
+      for (int c = 0; c < 4; ++c)
+        if (c < CH) {
+          const int kq = 2 * c + wg;
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          uint32_t v[4];
-          decode8(words[jj], v);
-          if (grouped) {
-            v[0] = hmul2_u32(v[0], s_g);
-            v[1] = hmul2_u32(v[1], s_g8);
-            v[2] = hmul2_u32(v[2], s_g);
-            v[3] = hmul2_u32(v[3], s_g8);
+          for (int bi = 0; bi < 2; ++bi) {
+            const int b = 2 * q + bi;
+            wv[c][bi] = lds128(st + (kq * 8 + b) * 512 + lane * 16);
+            sc[c][bi] = grouped ? lds32(st + KQ * 4096 + (c * 128 + b * 16 + 2 * g) * 2) : 0x3c003c00u;
           }
-          // .16x256b fragment order: (row g, col 2t), (row g, col 2t+1), (row g+8, col 2t), (row g+8, col 2t+1)
-          r[4 * jj + 0] = v[0];
-          r[4 * jj + 1] = v[2];
-          r[4 * jj + 2] = v[1];
-          r[4 * jj + 3] = v[3];
         }
-        tmem_st_16x256b_x4(tmem + (static_cast<uint32_t>(32 * q + 16 * bi) << 16) + a * kChunkCols + wg * 32, r);
-      }
-      tmem_st_wait();
-      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_afull + 8 * a);
-      ++gc;
+      if (lane == 0) mbar_arrive(bar_wempty + 8 * s);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (c >= CH || !have) break;
+        const int a = gc % NA;
+        if (gc >= NA) {
+          bool ok = mbar_wait_bounded(bar_cempty + 8 * a, ((gc / NA) - 1) & 1, p.wait_limit, abort_flag);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) {
+            if (lane == 0) raise_abort();
+            have = false;
+            break;
+          }
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int bi = 0; bi < 2; ++bi) {
+          const uint32_t spair = sc[c][bi];
+          const uint32_t s_g = (spair & 0xffffu) * 0x10001u;
+          const uint32_t s_g8 = (spair >> 16) * 0x10001u;
+          const uint32_t words[4] = {wv[c][bi].x, wv[c][bi].y, wv[c][bi].z, wv[c][bi].w};
+          uint32_t r[16];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            uint32_t v[4];
+            decode8(words[jj], v);
+            if (grouped) {
+              v[0] = hmul2_u32(v[0], s_g);
+              v[1] = hmul2_u32(v[1], s_g8);
+              v[2] = hmul2_u32(v[2], s_g);
+              v[3] = hmul2_u32(v[3], s_g8);
+            }
+            // .16x256b fragment order: (row g, col 2t), (row g, col 2t+1), (row g+8, col 2t), (row g+8, col 2t+1)
+            r[4 * jj + 0] = v[0];
+            r[4 * jj + 1] = v[2];
+            r[4 * jj + 2] = v[1];
+            r[4 * jj + 3] = v[3];
+          }
+          tmem_st_16x256b_x4(tmem + (static_cast<uint32_t>(32 * q + 16 * bi) << 16) + a * kChunkCols + wg * 32, r);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_cfull + 8 * a);
+        ++gc;
+      }
     }
     if (seg_end && wg == 0) {
       // ------------------------------------------------------ epilogue (strip j)
       named_bar_sync(1, 128);
-      if (warp == 2 && lane == 0) *seg_abort = *abort_flag;
+      if (epi_lead && lane == 0) *seg_abort = *abort_flag;
       named_bar_sync(1, 128);
       if (!*seg_abort) {
         bool ok = mbar_wait_bounded(bar_dfull, segs & 1, p.wait_limit, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok && lane == 0) raise_abort();
         named_bar_sync(1, 128);
-        if (warp == 2 && lane == 0) *seg_abort = *abort_flag;
+        if (epi_lead && lane == 0) *seg_abort = *abort_flag;
         named_bar_sync(1, 128);
       }
       if (!*seg_abort) {
@@ -394,15 +434,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         const int c_last = min(((j + 1) * p.KU - 1) / p.T, p.grid - 1);
         const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + kDCol;
         const int nchunks = MB / 16;
+        const int nact = min(NI, seg_units * CH);  // accumulator regions written in this segment
+        // sum of the active accumulator regions for tokens ch*16 .. ch*16+15 (fixed order)
+        auto load_sum = [&](int ch, float (&out)[16]) {
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(taddr + ch * 16, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) out[i] = __uint_as_float(v[i]);
+          for (int r = 1; r < nact; ++r) {
+            tmem_ld_32x32b_x16(taddr + r * MB + ch * 16, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) out[i] += __uint_as_float(v[i]);
+          }
+        };
         if (c_first == c_last) {
           for (int ch = 0; ch < nchunks; ++ch) {
-            uint32_t v[16];
-            tmem_ld_32x32b_x16(taddr + ch * 16, v);
-            tmem_ld_wait();
+            float v[16];
+            load_sum(ch, v);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int token = p.m0 + ch * 16 + i;
-              if (token < p.M) p.C[static_cast<long long>(token) * p.N + n] = f32_to_f16_bits(__uint_as_float(v[i]) * scale);
+              if (token < p.M) p.C[static_cast<long long>(token) * p.N + n] = f32_to_f16_bits(v[i] * scale);
             }
           }
           tc_fence_before();
@@ -413,18 +467,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           const int slot = (j == first_col) ? 2 * cta : 2 * cta + 1;
           float* dst = p.slots + static_cast<long long>(slot) * (128 * MB);
           for (int ch = 0; ch < nchunks; ++ch) {
-            uint32_t v[16];
-            tmem_ld_32x32b_x16(taddr + ch * 16, v);
-            tmem_ld_wait();
+            float v[16];
+            load_sum(ch, v);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) dst[(ch * 16 + i) * 128 + row] = __uint_as_float(v[i]);
+            for (int i = 0; i < 16; ++i) dst[(ch * 16 + i) * 128 + row] = v[i];
           }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_dempty);
           __threadfence();
           named_bar_sync(2, 128);
-          if (warp == 2 && lane == 0) {
+          if (epi_lead && lane == 0) {
             const unsigned old = atomicAdd(p.counters + j, 1u);
             *last_flag = (old == static_cast<unsigned>(c_last - c_first)) ? 1 : 0;
           }
@@ -441,13 +494,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
               }
               p.C[static_cast<long long>(token) * p.N + n] = f32_to_f16_bits(acc * scale);
             }
-            if (warp == 2 && lane == 0) p.counters[j] = 0u;
+            if (epi_lead && lane == 0) p.counters[j] = 0u;
           }
         }
       }
       ++segs;
     }
-    if (++s == S) {
+    if (seg_end) seg_units = 0;
+    if (++s == SW) {
       s = 0;
       ++round;
     }
@@ -461,15 +515,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
 
 }  // namespace
 
-TcLayout tc_layout(int mb, int ch, int srows, int stages) {
+TcLayout tc_layout(int mb, int ch, int srows, int a_stages, int w_stages) {
   TcLayout l{};
   const int kq = 2 * ch;
-  l.w_off = kq * mb * 128;
-  l.s_off = l.w_off + kq * 4096;
-  l.stage_bytes = (l.s_off + srows * 256 + 1023) / 1024 * 1024;
-  l.tx_bytes = kq * mb * 128 + kq * 4096 + srows * 256;
-  l.bar_off = stages * l.stage_bytes;
-  l.flag_off = l.bar_off + 8 * (2 * stages + 2 * kNA + 3);
+  l.a_stage_bytes = 2 * mb * 128;  // one 128-row chunk; a multiple of 1024 keeps the swizzle atoms aligned
+  l.w_stage_bytes = (kq * 4096 + srows * 256 + 1023) / 1024 * 1024;
+  l.w_base = a_stages * l.a_stage_bytes;
+  l.bar_off = l.w_base + w_stages * l.w_stage_bytes;
+  l.flag_off = l.bar_off + 8 * (2 * a_stages + 2 * w_stages + 2 * kMaxNA + 6);
   l.smem_bytes = 1024 + l.flag_off + 64;
   return l;
 }

@@ -60,12 +60,12 @@ constexpr int kStrip = 128;       // output columns per strip / work unit
 cudaError_t launch_gemm_mma(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream);
 
 // ---- tensor-memory (tcgen05) GEMM ----------------------------------------
-constexpr int kTcThreads = 320;  // producer, MMA issuer, 8 dequant warps
+constexpr int kTcThreads = 448;  // 2 producers, 4 MMA issuers, 8 dequant warps
 
 struct TcLayout {
-  int w_off, s_off, stage_bytes, tx_bytes, bar_off, flag_off, smem_bytes;
+  int a_stage_bytes, w_stage_bytes, w_base, bar_off, flag_off, smem_bytes;
 };
-TcLayout tc_layout(int mb, int ch, int srows, int stages);
+TcLayout tc_layout(int mb, int ch, int srows, int a_stages, int w_stages);
 uint32_t tc_idesc(int m, int n);
 
 struct TcParams {
@@ -78,9 +78,12 @@ struct TcParams {
   int M, m0, K, N, G;
   int mb;                   // token rows of this launch padded to 16 (the MMA's N)
   int ch;                   // 128-row chunks per work unit (KT = 128 * ch)
+  int na;                   // A chunks in the tensor-memory ring (64 columns each, <= 7)
+  int ni;                   // MMA-issuing threads (1..4), each with an accumulator of mb columns
   int srows;                // scale rows per unit
-  int KU, units, T, grid, stages;
-  int w_off, s_off, stage_bytes, tx_bytes, bar_off, flag_off;
+  int KU, units, T, grid;
+  int a_stages, w_stages;   // activation ring / weight ring depths
+  int a_stage_bytes, w_stage_bytes, w_base, bar_off, flag_off;
   uint32_t idesc;
   long long wait_limit;
   int debug_stall;
