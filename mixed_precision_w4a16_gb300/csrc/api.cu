@@ -73,6 +73,7 @@ struct Plan {
   TcLayout tlay;     // path 2
   int mb, ch;        // path 2: token rows per launch (multiple of 16), 128-row chunks per unit
   int a_stages, w_stages;  // path 2: activation / weight ring depths
+  int ni, na;        // path 2: MMA issuers (accumulators), A chunks in tensor memory (= a_stages)
   int m_chunk;       // token rows per launch
   int k_tile;        // reduction rows per work unit
   int srows;
@@ -142,22 +143,25 @@ Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin) {
 Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin) {
   Plan pl{};
   pl.path = 2;
-  pl.mb = std::min(256, (std::max(M, 1) + 15) / 16 * 16);
+  pl.mb = std::min(128, (std::max(M, 1) + 15) / 16 * 16);
   pl.strips = N / kStrip;
+  // Tensor memory (512 columns): ni accumulators of mb columns (ni * mb <= 256),
+  // the rest for the ring of 64-column A chunks.  Activation stages pair with the
+  // A buffers (one per chunk in flight).
+  pl.ni = std::max(1, std::min(4, 256 / pl.mb));
+  pl.na = std::min(6, (512 - pl.ni * pl.mb) / 64);
   // Unit depth KT = 128 * ch for the weight ring (one copy per unit, released by
-  // the dequant warps); activations are staged per 128-row chunk (released by
-  // the multiply that reads them).  Keep >= 4 activation chunks and >= 128 KB of
-  // weights in flight; among those, minimise T * unit time (memory time as for
-  // the streaming kernel vs tensor time, ~2.1 ns per mb * ch).
-  int best = 0, best_a = 0, best_w = 0;
+  // the dequant warps).  Keep >= 8 chunks of weights in flight; among the
+  // candidates, minimise T * unit time (memory time as for the streaming kernel
+  // vs tensor time, ~2.1 ns per mb * ch).
+  int best = 0, best_w = 0;
   long long best_cost = 0;
   const int cands[3] = {4, 2, 1};
   for (int c = 0; c < 3; ++c) {
     const int ch = cands[c];
     if (K % (128 * ch) != 0) continue;
     const int srows = (G == 128) ? ch : 1;
-    const int a_st = pl.mb <= 64 ? 6 : (pl.mb <= 128 ? 3 : 2);
-    const TcLayout l0 = tc_layout(pl.mb, ch, srows, a_st, 0);
+    const TcLayout l0 = tc_layout(pl.mb, ch, srows, pl.na, 0);
     const int w_st = std::min(12, (smem_optin - l0.smem_bytes) / (l0.w_stage_bytes + 16));
     if (w_st < 2 || w_st * ch < 8) continue;
     const long long units = static_cast<long long>(pl.strips) * (K / (128 * ch));
@@ -165,21 +169,19 @@ Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin) {
     const long long cost = T * (std::max(178LL * ch, (21LL * pl.mb * ch) / 10) + 200);  // + per-unit sync and copy issue
     if (best == 0 || cost < best_cost) {
       best = ch;
-      best_a = a_st;
       best_w = w_st;
       best_cost = cost;
     }
   }
   if (!best) {
     best = 1;
-    best_a = 2;
-    const TcLayout l0 = tc_layout(pl.mb, 1, 1, 2, 0);
+    const TcLayout l0 = tc_layout(pl.mb, 1, 1, pl.na, 0);
     best_w = std::max(2, std::min(12, (smem_optin - l0.smem_bytes) / (l0.w_stage_bytes + 16)));
   }
   pl.ch = best;
   pl.srows = (G == 128) ? pl.ch : 1;
-  pl.tlay = tc_layout(pl.mb, pl.ch, pl.srows, best_a, best_w);
-  pl.a_stages = best_a;
+  pl.tlay = tc_layout(pl.mb, pl.ch, pl.srows, pl.na, best_w);
+  pl.a_stages = pl.na;
   pl.w_stages = best_w;
   pl.m_chunk = pl.mb;
   pl.k_tile = 128 * pl.ch;
@@ -387,8 +389,8 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* scales
     p.G = G;
     p.mb = pl.mb;
     p.ch = pl.ch;
-    p.na = 4;                                    // A chunks in the tensor-memory ring: 256 columns
-    p.ni = std::max(1, std::min(4, 256 / pl.mb));  // accumulators: ni * mb <= 256 columns
+    p.ni = pl.ni;
+    p.na = pl.na;
     p.srows = pl.srows;
     p.KU = pl.KU;
     p.units = pl.units;

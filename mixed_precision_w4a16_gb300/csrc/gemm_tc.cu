@@ -9,16 +9,23 @@
 //    128-column strip x KT = 128*CH reduction rows per unit, loaded by one
 //    producer lane with three copy-engine operations (weights, activations as a
 //    swizzled [K/64][M][64] tile, scale rows) into a ring of shared-memory stages;
-//  * two dequant warpgroups decode the 4-bit codes to FP16 (exact q - 8, times
-//    the FP16 group scale with one RNE multiply -- the same value
-//    w4a16_dequant returns) and write them with tcgen05.st.16x256b straight into
-//    tensor memory, where they form the A operand (128 rows = the strip's
+//  * two teams of dequant warps (two warpgroups each) take alternate 128-row
+//    chunks; a warpgroup decodes one 64-row half of its team's chunk to FP16
+//    (exact q - 8, times the FP16 group scale with one RNE multiply -- the same
+//    value w4a16_dequant returns) and writes it with tcgen05.st.16x256b straight
+//    into tensor memory, where it forms the A operand (128 rows = the strip's
 //    output columns, K along the 32-bit columns).  The packed word of lane
-//    (g, t) is that store's fragment: rows g and g + 8, k = 4t .. 4t + 3;
-//  * one thread issues tcgen05.mma.kind::f16 (A from tensor memory, B = the
-//    activation tile through a shared-memory descriptor, FP32 accumulator
-//    D[128 x MB] in tensor memory) and tracks completion with tcgen05.commit on
-//    mbarriers that recycle the A-chunk ring and the stages;
+//    (g, t) is that store's fragment: rows g and g + 8, k = 4t .. 4t + 3.  With
+//    two teams, one team's hand-off latency (store drain, fences, barrier
+//    waits) overlaps the other team's decode arithmetic;
+//  * up to four threads, each in its own warp on its own SM sub-partition,
+//    issue tcgen05.mma.kind::f16 (A from tensor memory, B = the activation tile
+//    through a shared-memory descriptor, FP32 accumulators D[128 x MB] in
+//    tensor memory, one per issuer).  The dequant warps keep the integer and
+//    FP16 pipes busy, so an issuer gets few issue slots: its per-chunk path is
+//    one wait per barrier, one asm block with the chunk's eight multiplies and a
+//    single tcgen05.commit.  Activation stage a and tensor-memory A buffer a
+//    belong to the same chunk, so that one commit frees both;
 //  * at the end of each strip segment the first warpgroup reads D back with
 //    tcgen05.ld (one output column per thread, the tokens along registers),
 //    applies the per-column scale when G = K, and writes C -- or, for strips
@@ -36,9 +43,12 @@ namespace w4a16 {
 
 namespace {
 
-// warps: 0 weight producer, 1 MMA issuer 0 + tensor-memory owner, 2 activation producer,
-// 3..10 dequant (two warpgroups), 11..13 MMA issuers 1..3
-constexpr int kDequantWarps = 8;  // warps 3..10: two warpgroups
+// warps: 0 weight producer, 1 activation producer, 2..5 MMA issuers 0..3 (warp 2 owns the
+// tensor memory), 6..21 dequant (team 0: warps 6..13, team 1: warps 14..21)
+constexpr int kIssuerWarp0 = 2;
+constexpr int kDequantWarp0 = 6;
+constexpr int kDequantWarps = 16;  // both teams; every one releases each weight stage
+constexpr int kTeamWarps = 8;      // one team: the writers of one A chunk
 constexpr int kTmemCols = 512;
 constexpr int kChunkCols = 64;           // 128 k of FP16 A = 64 32-bit columns
 constexpr int kMaxNA = 7;                // A chunks in flight in tensor memory (p.na <= 7)
@@ -60,12 +70,34 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
-// D[tmem] (+)= A[tmem] * B[smem descriptor], kind::f16, FP32 accumulate
-__device__ __forceinline__ void tc_mma(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+// The eight multiplies of one 128-row chunk: D[tmem] (+)= A[tmem] * B[smem], kind::f16,
+// FP32 accumulate.  A: the chunk's 64 tensor-memory columns starting at `a`, 8 per
+// k16 step.  B: descriptor {lo, hi} of the chunk's activation stage; k16 step kk
+// starts (kk & 3) * 32 bytes into 64-row piece kk >> 2 (pieces `box16` * 16 bytes
+// apart).  The first multiply overwrites D when `accumulate` is 0.
+__device__ __forceinline__ void tc_mma_chunk(uint32_t d, uint32_t a, uint32_t lo, uint32_t hi, uint32_t box16,
+                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-      "r"(a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p;\n\t.reg .b32 l, l4, t;\n\t.reg .b64 b;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "mov.b64 b, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %5, p;\n\t"
+      "setp.eq.b32 p, %2, %2;\n\t"
+      "add.u32 l, %2, 2;\n\tadd.u32 t, %1, 8;\n\tmov.b64 b, {l, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t], b, %5, p;\n\t"
+      "add.u32 l, %2, 4;\n\tadd.u32 t, %1, 16;\n\tmov.b64 b, {l, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t], b, %5, p;\n\t"
+      "add.u32 l, %2, 6;\n\tadd.u32 t, %1, 24;\n\tmov.b64 b, {l, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t], b, %5, p;\n\t"
+      "add.u32 l4, %2, %4;\n\tadd.u32 t, %1, 32;\n\tmov.b64 b, {l4, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t], b, %5, p;\n\t"
+      "add.u32 l, l4, 2;\n\tadd.u32 t, %1, 40;\n\tmov.b64 b, {l, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t], b, %5, p;\n\t"
+      "add.u32 l, l4, 4;\n\tadd.u32 t, %1, 48;\n\tmov.b64 b, {l, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t], b, %5, p;\n\t"
+      "add.u32 l, l4, 6;\n\tadd.u32 t, %1, 56;\n\tmov.b64 b, {l, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t], b, %5, p;\n\t}" ::"r"(d),
+      "r"(a), "r"(lo), "r"(hi), "r"(box16), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 __device__ __forceinline__ void tmem_st_16x256b_x4(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -93,11 +125,9 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 // 0..13), leading-dimension byte offset >> 4 (16..29, unused for swizzled
 // K-major: 1), stride byte offset >> 4 (32..45: 1024 bytes between 8-row
 // groups), descriptor version 1 (46..47), layout type 2 = 128-byte swizzle
-// (61..63).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
-  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
-         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
-}
+// (61..63).  Returned as its low and high 32-bit words.
+__device__ __forceinline__ uint32_t smem_desc_sw128_lo(uint32_t saddr) { return ((saddr & 0x3FFFFu) >> 4) | (1u << 16); }
+__device__ __forceinline__ uint32_t smem_desc_sw128_hi() { return (1024u >> 4) | (1u << (46 - 32)) | (2u << (61 - 32)); }
 
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -121,22 +151,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  const int SA = p.a_stages;         // activation ring, one 128-row chunk per stage (released by the MMA commit)
   const int SW = p.w_stages;         // weight + scale ring (released by the dequant warps)
   const int CH = p.ch;
   const int KQ = 2 * CH;
   const int MB = p.mb;
   const int A_BOX = MB * 128;
-  const int NA = p.na;               // A-chunk ring depth in tensor memory; the accumulators follow it
+  // Chunk gc of the CTA uses activation stage and tensor-memory A buffer gc % NA;
+  // the accumulators follow the A buffers in tensor memory.
+  const int NA = p.na;
   const int NI = p.ni;               // MMA-issuing threads, each with its own accumulator region
   const int kDCol = NA * kChunkCols;
-  const uint32_t bar_afull = sbase + p.bar_off;      // activation stage landed
-  const uint32_t bar_aempty = bar_afull + 8 * SA;    // activation stage read by the MMAs
-  const uint32_t bar_wfull = bar_aempty + 8 * SA;    // weight stage landed
-  const uint32_t bar_wempty = bar_wfull + 8 * SW;    // weight stage read by the dequant warps
-  const uint32_t bar_cfull = bar_wempty + 8 * SW;    // A chunk written to tensor memory
-  const uint32_t bar_cempty = bar_cfull + 8 * kMaxNA;  // A chunk consumed by the MMAs
-  const uint32_t bar_dfull = bar_cempty + 8 * kMaxNA;
+  const uint32_t bar_afull = sbase + p.bar_off;        // activation stage landed
+  const uint32_t bar_wfull = bar_afull + 8 * kMaxNA;   // weight stage landed
+  const uint32_t bar_wempty = bar_wfull + 8 * SW;      // weight stage read by the dequant warps
+  const uint32_t bar_cfull = bar_wempty + 8 * SW;      // A chunk written to tensor memory
+  const uint32_t bar_consumed = bar_cfull + 8 * kMaxNA;  // chunk's multiplies done: stage and A buffer free
+  const uint32_t bar_dfull = bar_consumed + 8 * kMaxNA;
   const uint32_t bar_dempty = bar_dfull + 8;
   const uint32_t bar_drain = bar_dempty + 8;
   volatile int* flags = reinterpret_cast<volatile int*>(smem + p.flag_off);
@@ -156,25 +186,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   const int kt0 = u_begin - first_col * p.KU;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < SA; ++s) {
-      mbar_init(bar_afull + 8 * s, 1);
-      mbar_init(bar_aempty + 8 * s, 1);
-    }
     for (int s = 0; s < SW; ++s) {
       mbar_init(bar_wfull + 8 * s, 1);
       mbar_init(bar_wempty + 8 * s, kDequantWarps);
     }
     for (int a = 0; a < NA; ++a) {
-      mbar_init(bar_cfull + 8 * a, kDequantWarps);
-      mbar_init(bar_cempty + 8 * a, 1);
+      mbar_init(bar_afull + 8 * a, 1);
+      mbar_init(bar_cfull + 8 * a, kTeamWarps);
+      mbar_init(bar_consumed + 8 * a, 1);
     }
     mbar_init(bar_dfull, NI);
     mbar_init(bar_dempty, 4);
     for (int i = 0; i < 4; ++i) mbar_init(bar_drain + 8 * i, 1);
-    for (int i = 0; i < 4; ++i) flags[i] = 0;  // flags[4] receives the tensor-memory address from warp 1
+    for (int i = 0; i < 4; ++i) flags[i] = 0;  // flags[4] receives the tensor-memory address from warp 2
     mbar_fence_init();
   }
-  if (warp == 1) {
+  if (warp == kIssuerWarp0) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
     tmem_relinquish();
   }
@@ -190,13 +217,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     }
   };
 
-  if (warp == 0 || warp == 2) {
+  if (warp < kIssuerWarp0) {
     // ------------------------------------------- producers: warp 0 weights + scales (one stage per unit),
-    //                                               warp 2 activations (one stage per 128-row chunk)
+    //                                               warp 1 activations (one stage per 128-row chunk)
     const bool wprod = warp == 0;
-    const int S = wprod ? SW : SA;
+    const int S = wprod ? SW : NA;
     const uint32_t full = wprod ? bar_wfull : bar_afull;
-    const uint32_t empty = wprod ? bar_wempty : bar_aempty;
+    const uint32_t empty = wprod ? bar_wempty : bar_consumed;
     if (!wprod && lane == 0) prefetch_tensormap(&tmA);
     const uint64_t pol = wprod ? policy_evict_first() : policy_evict_last();
     const uint64_t pol_s = policy_evict_last();
@@ -229,7 +256,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             const uint16_t* ssrc = p.scales + (static_cast<long long>(j) * NG + grp0) * 128;
             bulk_g2s(st + w_bytes, ssrc, static_cast<uint32_t>(p.srows) * 256u, fb, pol_s);
           } else {
-            const uint32_t st = sbase + s * p.a_stage_bytes;
+            const uint32_t st = sbase + s * p.a_stage_bytes;  // stage s = chunk gc % NA
             mbar_arrive_expect_tx(fb, static_cast<uint32_t>(2 * A_BOX));
             tma_load_3d(st, &tmA, 0, p.m0, kt * KQ + 2 * c, fb, pol);
           }
@@ -258,48 +285,41 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     return;
   }
 
-  const int issuer = (warp == 1) ? 0 : (warp >= 11 ? warp - 10 : -1);
-  if (issuer >= 0) {
+  if (warp < kDequantWarp0) {
     // ------------------------------------------------------------- MMA issuers
     // A single thread can issue a tcgen05.mma only every ~90 cycles, far below the
     // tensor core's rate for small N; NI threads therefore issue in parallel, each
     // taking every NI-th 128-row chunk of a strip segment into its own accumulator.
+    const int issuer = warp - kIssuerWarp0;
     if (lane == 0 && issuer < NI) {
-      const uint32_t idesc = p.idesc;
       const uint32_t d_tmem = tmem + kDCol + issuer * MB;
-      int gc = 0, segs = 0, cs = 0;
-      int kt = kt0;
-      bool mine_first = true;  // next chunk of this issuer starts its accumulator for the segment
-      for (int it = 0; it < nunits && !*abort_flag; ++it) {
+      const uint32_t lo0 = smem_desc_sw128_lo(sbase);  // activation stage 0 sits at the base
+      const uint32_t hi = smem_desc_sw128_hi();
+      const uint32_t stage16 = static_cast<uint32_t>(p.a_stage_bytes) >> 4;
+      const uint32_t box16 = static_cast<uint32_t>(A_BOX) >> 4;
+      int a = 0, turn = 0, segs = 0, kt = kt0;
+      uint32_t ph = 0;
+      bool first = true;  // next chunk of this issuer starts its accumulator for the segment
+      bool ok = true;
+      for (int it = 0; it < nunits && ok && !*abort_flag; ++it) {
         const bool seg_end = (kt == p.KU - 1) || (it == nunits - 1);
-        bool ok = true;
-        for (int c = 0; c < CH && ok; ++c, ++gc, ++cs) {
-          if (cs % NI != issuer) continue;
-          const int sa = gc % SA;  // activation stage of this chunk
-          const int a = gc % NA;   // tensor-memory A buffer of this chunk
-          if (!mbar_wait_bounded_sleep(bar_afull + 8 * sa, (gc / SA) & 1, p.wait_limit, abort_flag) ||
-              !mbar_wait_bounded_sleep(bar_cfull + 8 * a, (gc / NA) & 1, p.wait_limit, abort_flag)) {
-            ok = false;
-            break;
-          }
-          if (mine_first && segs > 0) {
+        for (int c = 0; c < CH; ++c) {
+          if (turn == issuer) {
+            ok = mbar_wait_bounded_sleep(bar_afull + 8 * a, ph, p.wait_limit, abort_flag) &&
+                 mbar_wait_bounded_sleep(bar_cfull + 8 * a, ph, p.wait_limit, abort_flag);
             // the previous segment's accumulators must have been read out
-            if (!mbar_wait_bounded(bar_dempty, (segs - 1) & 1, p.wait_limit, abort_flag)) {
-              ok = false;
-              break;
-            }
+            if (ok && first && segs > 0) ok = mbar_wait_bounded(bar_dempty, (segs - 1) & 1, p.wait_limit, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            tc_mma_chunk(d_tmem, tmem + a * kChunkCols, lo0 + a * stage16, hi, box16, p.idesc, first ? 0u : 1u);
+            tc_commit(bar_consumed + 8 * a);  // stage and A buffer free once these multiplies complete
+            first = false;
           }
-          tc_fence_after();
-          const uint32_t st = sbase + sa * p.a_stage_bytes;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t bdesc = smem_desc_sw128(st + (kk >> 2) * A_BOX + (kk & 3) * 32);
-            const uint32_t acc = (mine_first && kk == 0) ? 0u : 1u;
-            tc_mma(d_tmem, tmem + a * kChunkCols + kk * 8, bdesc, idesc, acc);
+          if (++turn == NI) turn = 0;
+          if (++a == NA) {
+            a = 0;
+            ph ^= 1u;
           }
-          tc_commit(bar_cempty + 8 * a);   // A chunk free once these multiplies complete
-          tc_commit(bar_aempty + 8 * sa);  // activation stage free likewise
-          mine_first = false;
         }
         if (!ok) {
           raise_abort();
@@ -308,8 +328,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         if (seg_end) {
           tc_commit(bar_dfull);
           ++segs;
-          cs = 0;
-          mine_first = true;
+          turn = 0;
+          first = true;
         }
         if (++kt == p.KU) kt = 0;
       }
@@ -319,7 +339,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     }
     __syncwarp();
     named_bar_sync(3, kTcThreads);
-    if (warp == 1) {
+    if (warp == kIssuerWarp0) {
       tc_fence_after();
       tmem_dealloc(tmem, kTmemCols);
     }
@@ -327,19 +347,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   }
 
   // ----------------------------------------------------------------- dequant
-  const int dw = warp - 3;
-  const int wg = dw >> 2;     // warpgroup: which 64-row piece of each 128-row chunk
-  const int q = warp & 3;     // tensor-memory lane quarter: rows 32q .. 32q + 31 (blocks 2q, 2q + 1)
+  const int dw = warp - kDequantWarp0;
+  const int team = dw >> 3;          // this team writes the chunks with gc % 2 == team
+  const int wg = (dw >> 2) & 1;      // which 64-row half of each 128-row chunk
+  const int q = warp & 3;            // tensor-memory lane quarter: rows 32q .. 32q + 31 (blocks 2q, 2q + 1)
   const int g = lane >> 2;
   const bool grouped = p.G == 128;
   const int NG = p.K / p.G;
-  const bool epi_lead = warp == 3;  // first warp of warpgroup 0
-  int s = 0, round = 0, gc = 0, segs = 0, seg_units = 0;
+  const bool epi_lead = warp == kDequantWarp0;  // first warp of team 0, warpgroup 0
+  const bool epi_group = team == 0 && wg == 0;
+  int s = 0, round = 0, segs = 0, seg_units = 0;
   int j = first_col, kt = kt0;
   for (int it = 0; it < nunits; ++it) {
     const uint32_t st = sbase + p.w_base + s * p.w_stage_bytes;
     ++seg_units;
     const bool seg_end = (kt == p.KU - 1) || (it == nunits - 1);
+    const int c0 = (team - it * CH) & 1;  // this team's first chunk of the unit (then every second one)
     const bool go = __shfl_sync(0xffffffffu, *abort_flag == 0, 0);
     bool have = false;
     if (go) {
@@ -348,28 +371,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       if (!have && lane == 0) raise_abort();
     }
     if (have) {
-      // read this warp's share of the unit's weights and scales, then release the stage
-      uint4 wv[4][2];
-      uint32_t sc[4][2];
+      // read this warp's share of the team's chunks and their scales, then release the stage
+      uint4 wv[2][2];
+      uint32_t sc[2][2];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = c0 + 2 * cc;
         if (c < CH) {
           const int kq = 2 * c + wg;
 #pragma unroll
           for (int bi = 0; bi < 2; ++bi) {
             const int b = 2 * q + bi;
-            wv[c][bi] = lds128(st + (kq * 8 + b) * 512 + lane * 16);
-            sc[c][bi] = grouped ? lds32(st + KQ * 4096 + (c * 128 + b * 16 + 2 * g) * 2) : 0x3c003c00u;
+            wv[cc][bi] = lds128(st + (kq * 8 + b) * 512 + lane * 16);
+            sc[cc][bi] = grouped ? lds32(st + KQ * 4096 + (c * 128 + b * 16 + 2 * g) * 2) : 0x3c003c00u;
           }
         }
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_wempty + 8 * s);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = c0 + 2 * cc;
         if (c >= CH || !have) break;
+        const int gc = it * CH + c;
         const int a = gc % NA;
         if (gc >= NA) {
-          bool ok = mbar_wait_bounded(bar_cempty + 8 * a, ((gc / NA) - 1) & 1, p.wait_limit, abort_flag);
+          bool ok = mbar_wait_bounded(bar_consumed + 8 * a, ((gc / NA) - 1) & 1, p.wait_limit, abort_flag);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) {
             if (lane == 0) raise_abort();
@@ -380,10 +407,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         tc_fence_after();
 #pragma unroll
         for (int bi = 0; bi < 2; ++bi) {
-          const uint32_t spair = sc[c][bi];
+          const uint32_t spair = sc[cc][bi];
           const uint32_t s_g = (spair & 0xffffu) * 0x10001u;
           const uint32_t s_g8 = (spair >> 16) * 0x10001u;
-          const uint32_t words[4] = {wv[c][bi].x, wv[c][bi].y, wv[c][bi].z, wv[c][bi].w};
+          const uint32_t words[4] = {wv[cc][bi].x, wv[cc][bi].y, wv[cc][bi].z, wv[cc][bi].w};
           uint32_t r[16];
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
@@ -407,10 +434,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_cfull + 8 * a);
-        ++gc;
       }
     }
-    if (seg_end && wg == 0) {
+    if (seg_end && epi_group) {
       // ------------------------------------------------------ epilogue (strip j)
       named_bar_sync(1, 128);
       if (epi_lead && lane == 0) *seg_abort = *abort_flag;
@@ -522,7 +548,7 @@ TcLayout tc_layout(int mb, int ch, int srows, int a_stages, int w_stages) {
   l.w_stage_bytes = (kq * 4096 + srows * 256 + 1023) / 1024 * 1024;
   l.w_base = a_stages * l.a_stage_bytes;
   l.bar_off = l.w_base + w_stages * l.w_stage_bytes;
-  l.flag_off = l.bar_off + 8 * (2 * a_stages + 2 * w_stages + 2 * kMaxNA + 6);
+  l.flag_off = l.bar_off + 8 * (3 * kMaxNA + 2 * w_stages + 6);
   l.smem_bytes = 1024 + l.flag_off + 64;
   return l;
 }

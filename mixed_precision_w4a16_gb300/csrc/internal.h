@@ -60,7 +60,7 @@ constexpr int kStrip = 128;       // output columns per strip / work unit
 cudaError_t launch_gemm_mma(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream);
 
 // ---- tensor-memory (tcgen05) GEMM ----------------------------------------
-constexpr int kTcThreads = 448;  // 2 producers, 4 MMA issuers, 8 dequant warps
+constexpr int kTcThreads = 704;  // 2 producers, 4 MMA issuers, 16 dequant warps (two teams)
 
 struct TcLayout {
   int a_stage_bytes, w_stage_bytes, w_base, bar_off, flag_off, smem_bytes;

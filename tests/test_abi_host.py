@@ -75,7 +75,7 @@ def test_plan_stripes_cover_every_unit_once(w, M, K, N):
         assert p["units"] == (N // p["n_tile"]) * KU
         T, grid, U = p["units_per_cta"], p["grid"], p["units"]
         assert grid <= sms and grid * T >= U and (grid - 1) * T < U
-        assert p["m_chunk"] == 8 * p["m_tiles"] and p["m_chunk"] >= min(M, 32 if p["path"] == 1 else 256)
+        assert p["m_chunk"] == 8 * p["m_tiles"] and p["m_chunk"] >= min(M, 32 if p["path"] == 1 else 128)
         assert p["smem_bytes"] <= 232448 and p["stages"] >= 2
         # every unit belongs to exactly one CTA; every CTA has work
         owner = [u // T for u in range(U)]
@@ -99,9 +99,9 @@ def test_plan_token_tiles_and_kernel_choice(w):
     # up to 16 rows: streaming mma.sync kernel, 8-row token tiles
     assert [p["path"] for p in plans] == [1, 1, 1, 1, 2, 2, 2, 2, 2, 2]
     assert [p["m_chunk"] for p in plans[:4]] == [8, 8, 16, 16]
-    # from 17 rows: tensor-memory kernel, tokens padded to 16 (the MMA's N), at most 256 per launch
-    assert [p["m_chunk"] for p in plans[4:]] == [32, 32, 48, 64, 256, 256]
-    assert all(p["threads"] == 320 for p in plans[4:]) and all(p["threads"] == 288 for p in plans[:4])
+    # from 17 rows: tensor-memory kernel, tokens padded to 16 (the MMA's N), at most 128 per launch
+    assert [p["m_chunk"] for p in plans[4:]] == [32, 32, 48, 64, 128, 128]
+    assert all(p["threads"] == 704 for p in plans[4:]) and all(p["threads"] == 288 for p in plans[:4])
 
 
 def test_force_path_knob(w):
