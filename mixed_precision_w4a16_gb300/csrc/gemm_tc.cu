@@ -510,15 +510,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           named_bar_sync(2, 128);
           if (*last_flag) {
             __threadfence();
-            for (int m = 0; m < MB; ++m) {
-              const int token = p.m0 + m;
-              if (token >= p.M) break;
-              float acc = 0.f;
+            // sum the partials in CTA order, 8 tokens at a time: the 8 loads of one
+            // slot are independent, so their latencies overlap
+            for (int m0 = 0; m0 < MB && p.m0 + m0 < p.M; m0 += 8) {
+              float acc[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) acc[i] = 0.f;
               for (int c = c_first; c <= c_last; ++c) {
                 const int cslot = (j == (c * p.T) / p.KU) ? 2 * c : 2 * c + 1;
-                acc += __ldcg(p.slots + static_cast<long long>(cslot) * (128 * MB) + m * 128 + row);
+                const float* src = p.slots + static_cast<long long>(cslot) * (128 * MB) + m0 * 128 + row;
+                float t[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) t[i] = __ldcg(src + i * 128);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] += t[i];
               }
-              p.C[static_cast<long long>(token) * p.N + n] = f32_to_f16_bits(acc * scale);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int token = p.m0 + m0 + i;
+                if (token < p.M) p.C[static_cast<long long>(token) * p.N + n] = f32_to_f16_bits(acc[i] * scale);
+              }
             }
             if (epi_lead && lane == 0) p.counters[j] = 0u;
           }
