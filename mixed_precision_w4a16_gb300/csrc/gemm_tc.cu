@@ -49,6 +49,7 @@ constexpr int kIssuerWarp0 = 2;
 constexpr int kDequantWarp0 = 6;
 constexpr int kDequantWarps = 16;  // both teams; every one releases each weight stage
 constexpr int kTeamWarps = 8;      // one team: the writers of one A chunk
+constexpr int kEpiThreads = 32 * kTeamWarps;  // team 0 runs the epilogue
 constexpr int kTmemCols = 512;
 constexpr int kChunkCols = 64;           // 128 k of FP16 A = 64 32-bit columns
 constexpr int kMaxNA = 7;                // A chunks in flight in tensor memory (p.na <= 7)
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       mbar_init(bar_consumed + 8 * a, 1);
     }
     mbar_init(bar_dfull, NI);
-    mbar_init(bar_dempty, 4);
+    mbar_init(bar_dempty, kTeamWarps);
     for (int i = 0; i < 4; ++i) mbar_init(bar_drain + 8 * i, 1);
     for (int i = 0; i < 4; ++i) flags[i] = 0;  // flags[4] receives the tensor-memory address from warp 2
     mbar_fence_init();
@@ -354,8 +355,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   const int g = lane >> 2;
   const bool grouped = p.G == 128;
   const int NG = p.K / p.G;
-  const bool epi_lead = warp == kDequantWarp0;  // first warp of team 0, warpgroup 0
-  const bool epi_group = team == 0 && wg == 0;
+  const bool epi_lead = warp == kDequantWarp0;  // first warp of team 0
+  const bool epi_group = team == 0;  // team 0 reads the accumulators out, each warpgroup half of the tokens
   int s = 0, round = 0, segs = 0, seg_units = 0;
   int j = first_col, kt = kt0;
   for (int it = 0; it < nunits; ++it) {
@@ -438,16 +439,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     }
     if (seg_end && epi_group) {
       // ------------------------------------------------------ epilogue (strip j)
-      named_bar_sync(1, 128);
+      named_bar_sync(1, kEpiThreads);
       if (epi_lead && lane == 0) *seg_abort = *abort_flag;
-      named_bar_sync(1, 128);
+      named_bar_sync(1, kEpiThreads);
       if (!*seg_abort) {
         bool ok = mbar_wait_bounded(bar_dfull, segs & 1, p.wait_limit, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok && lane == 0) raise_abort();
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kEpiThreads);
         if (epi_lead && lane == 0) *seg_abort = *abort_flag;
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kEpiThreads);
       }
       if (!*seg_abort) {
         tc_fence_after();
@@ -460,6 +461,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         const int c_last = min(((j + 1) * p.KU - 1) / p.T, p.grid - 1);
         const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + kDCol;
         const int nchunks = MB / 16;
+        const int half = (nchunks + 1) >> 1;       // 16-token groups of warpgroup 0; warpgroup 1 takes the rest
+        const int ch_lo = wg * half, ch_hi = min(nchunks, ch_lo + half);
         const int nact = min(NI, seg_units * CH);  // accumulator regions written in this segment
         // sum of the active accumulator regions for tokens ch*16 .. ch*16+15 (fixed order)
         auto load_sum = [&](int ch, float (&out)[16]) {
@@ -476,7 +479,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           }
         };
         if (c_first == c_last) {
-          for (int ch = 0; ch < nchunks; ++ch) {
+          for (int ch = ch_lo; ch < ch_hi; ++ch) {
             float v[16];
             load_sum(ch, v);
 #pragma unroll
@@ -492,7 +495,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           // strip split between CTAs: FP32 partial [token][row] into this CTA's slot
           const int slot = (j == first_col) ? 2 * cta : 2 * cta + 1;
           float* dst = p.slots + static_cast<long long>(slot) * (128 * MB);
-          for (int ch = 0; ch < nchunks; ++ch) {
+          for (int ch = ch_lo; ch < ch_hi; ++ch) {
             float v[16];
             load_sum(ch, v);
 #pragma unroll
@@ -502,17 +505,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_dempty);
           __threadfence();
-          named_bar_sync(2, 128);
+          named_bar_sync(2, kEpiThreads);
           if (epi_lead && lane == 0) {
             const unsigned old = atomicAdd(p.counters + j, 1u);
             *last_flag = (old == static_cast<unsigned>(c_last - c_first)) ? 1 : 0;
           }
-          named_bar_sync(2, 128);
+          named_bar_sync(2, kEpiThreads);
           if (*last_flag) {
             __threadfence();
             // sum the partials in CTA order, 8 tokens at a time: the 8 loads of one
             // slot are independent, so their latencies overlap
-            for (int m0 = 0; m0 < MB && p.m0 + m0 < p.M; m0 += 8) {
+            for (int m0 = 16 * ch_lo; m0 < 16 * ch_hi && p.m0 + m0 < p.M; m0 += 8) {
               float acc[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i) acc[i] = 0.f;
