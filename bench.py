@@ -12,8 +12,11 @@ its weights from HBM without any flush.
 
 Prints one JSON line (rank 0).  ``value`` is the whole-job throughput in TB/s
 of algorithmic bytes (2MK + 0.5KN + 2(K/G)N + 2MN per GEMM) over the timed
-region; ``sweep`` gives per-M microseconds, TB/s, TFLOP/s and the fraction of
-the roofline max(bytes / HBM BW, FLOPs / dense FP16 peak).
+region; ``sweep`` gives per-M microseconds, TB/s, TFLOP/s, the fraction of
+the roofline max(bytes / HBM BW, FLOPs / dense FP16 peak), the kernel that
+ran, and for context a cuBLAS FP16 GEMM (FP32 accumulation) on the
+dequantised weights.  ``roofline`` describes the kernel with the largest share
+of the step's device time (``roofline_by_kernel`` lists every kernel).
 """
 from __future__ import annotations
 
@@ -31,6 +34,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "W4A16 GEMM µs, achieved HBM TB/s & % of roofline vs M=1..128 (1×GB300)"
+KERNEL_OF_PATH = {1: "gemm_mma_kernel", 2: "gemm_tc_kernel"}
 L2_BYTES = 129 * 1024 * 1024
 
 # workload name -> (description, list of (K, N, groupsize, [M ...]), seed)
@@ -82,6 +86,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--only-m", type=int, default=None, help="run only this M of the sweep (profiling)")
+    ap.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS FP16 GEMM on the dequantised weights")
     ap.add_argument("--cpu-sample", default=None, help=argparse.SUPPRESS)  # internal: oracle timing child
     return ap.parse_args()
 
@@ -149,8 +154,8 @@ def kernel_source_hash():
 
 
 def profiled_traffic(name):
-    """Per-launch DRAM bytes {(M, launch): bytes} from a committed ncu summary, or None when the
-    summary was taken on other kernel sources."""
+    """Per-launch DRAM bytes {(kernel, M, launch): bytes} from a committed ncu summary, or None when
+    the summary was taken on other kernel sources."""
     path = os.path.join(ROOT, "profiles", name)
     try:
         with open(path) as f:
@@ -162,8 +167,8 @@ def profiled_traffic(name):
     out = {}
     for line in text.splitlines():
         cells = [c.strip() for c in line.strip().strip("|").split("|")]
-        if len(cells) == 8 and cells[0].isdigit():
-            out[(int(cells[0]), int(cells[1]))] = float(cells[5]) * 1e6
+        if len(cells) == 9 and cells[0].startswith("gemm_") and cells[1].isdigit():
+            out[(cells[0], int(cells[1]), int(cells[2]))] = float(cells[6]) * 1e6
     return out or None
 
 
@@ -282,6 +287,7 @@ def run_ours(args, rank, world, device):
     for p in points:
         plan = w.w4a16_plan(p["M"], p["K"], p["N"], p["G"])
         p["launches"] = math.ceil(p["M"] / plan["m_chunk"])
+        p["kernel"] = KERNEL_OF_PATH[plan["path"]]
         launches_per_step += p["launches"]
 
     def one_step(it, evs=None):
@@ -370,6 +376,33 @@ def run_ours(args, rank, world, device):
         e2e = {"value": world * tb / (e_ms * 1e-3) / 1e12, "unit": "TB/s", "ms_per_step": e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps}
 
+    # ---- context: cuBLAS FP16 GEMM (FP32 accumulation) on the dequantised weights, same A
+    cublas_us = None
+    if not args.no_cublas and rank == 0:
+        torch.backends.cuda.matmul.allow_fp16_reduced_precision_reduction = False
+        cublas_us = []
+        bhat_cache = {}
+        for p in points:
+            key = (p["K"], p["N"], p["G"], id(p["packs"]))
+            if key not in bhat_cache:
+                bhat_cache.clear()
+                packed, sp = p["packs"][0]
+                bhat_cache[key] = w.dequant(packed, sp, p["K"], p["N"], p["G"])
+            bhat = bhat_cache[key]
+            out = torch.empty_like(p["C_d"])
+            for _ in range(3):
+                torch.matmul(p["A_d"], bhat, out=out)
+            reps = 10
+            c0 = torch.cuda.Event(enable_timing=True)
+            c1 = torch.cuda.Event(enable_timing=True)
+            c0.record(stream)
+            for _ in range(reps):
+                torch.matmul(p["A_d"], bhat, out=out)
+            c1.record(stream)
+            torch.cuda.synchronize()
+            cublas_us.append(c0.elapsed_time(c1) / reps * 1e3)
+        bhat_cache.clear()
+
     ms_per_step = reduce_max(ms_total / args.steps, world, device)
     clocks = sampler.finish() if sampler else None
     if rank != 0:
@@ -380,45 +413,64 @@ def run_ours(args, rank, world, device):
     bw = peaks["hbm_gbs"] * 1e9
     pk = peaks["bf16_tflops"] * 1e12  # dense FP16 equals dense BF16 on this part
     sweep = []
-    mem_bytes = mem_time = 0.0
     for p, ts in zip(points, per_point):
         us = statistics.median(ts) * 1e3
         by = gemm_bytes(p["M"], p["K"], p["N"], p["G"])
         fl = gemm_flops(p["M"], p["K"], p["N"])
         t_roof = max(by / bw, fl / pk)
         mem_bound = by / bw >= fl / pk
-        if mem_bound:
-            mem_bytes += by
-            mem_time += us * 1e-6
         sweep.append({"M": p["M"], "K": p["K"], "N": p["N"], "group": p["G"], "us": round(us, 2),
                       "us_p10": round(sorted(ts)[len(ts) // 10] * 1e3, 2),
                       "us_p90": round(sorted(ts)[(9 * len(ts)) // 10] * 1e3, 2),
                       "tb_s": round(by / (us * 1e-6) / 1e12, 3), "tflops": round(fl / (us * 1e-6) / 1e12, 1),
                       "roofline_frac": round(t_roof / (us * 1e-6), 3), "bound": "hbm" if mem_bound else "tensor",
-                      "launches": p["launches"]})
-    if mem_time > 0:
-        ach = mem_bytes / mem_time / 1e9
-        # DRAM bytes per launch over the same launches, from the committed ncu summary of this build
+                      "launches": p["launches"], "kernel": p["kernel"]})
+        if cublas_us is not None:
+            cu = cublas_us[len(sweep) - 1]
+            sweep[-1]["cublas_fp16_us"] = round(cu, 2)
+            sweep[-1]["speedup_vs_cublas"] = round(cu / us, 3)
+    roofline_by_kernel = []
+    for kname in sorted({p["kernel"] for p in points}):
+        rows = [(p, r) for p, r in zip(points, sweep) if p["kernel"] == kname]
+        t_all = sum(r["us"] for _, r in rows)
+        mem = [(p, r) for p, r in rows if r["bound"] == "hbm"]
+        ten = [(p, r) for p, r in rows if r["bound"] == "tensor"]
+        entry = {"kernel": kname, "us_per_step": round(t_all, 2), "points": [r["M"] for _, r in rows]}
+        if mem:
+            by = sum(gemm_bytes(p["M"], p["K"], p["N"], p["G"]) for p, _ in mem)
+            t = sum(r["us"] for _, r in mem) * 1e-6
+            nl = sum(p["launches"] for p, _ in mem)
+            entry["hbm"] = {"achieved": round(by / t / 1e9, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": round(by / t / 1e9 / peaks["hbm_gbs"], 3), "points": [r["M"] for _, r in mem],
+                            "algorithmic_bytes_per_launch": round(by / nl), "launches": nl}
+        if ten:
+            fl = sum(gemm_flops(p["M"], p["K"], p["N"]) for p, _ in ten)
+            t = sum(r["us"] for _, r in ten) * 1e-6
+            entry["tensor"] = {"achieved": round(fl / t / 1e12, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                               "frac": round(fl / t / 1e12 / peaks["bf16_tflops"], 3),
+                               "points": [r["M"] for _, r in ten]}
+        roofline_by_kernel.append(entry)
+    # the dominant kernel: the largest share of the step's device time
+    dom = max(roofline_by_kernel, key=lambda e: e["us_per_step"])
+    prof = profiled_traffic("gemm_big_layer_traffic.md") if args.workload == "big" else None
+    if "hbm" in dom:
         traffic = None
-        prof = profiled_traffic("gemm_mma_big_layer_traffic.md") if args.workload == "big" else None
         if prof:
-            mem_ms = {r["M"] for r in sweep if r["bound"] == "hbm"}
-            vals = [v for (m, _), v in prof.items() if m in mem_ms]
+            vals = [v for (k, m, _), v in prof.items() if k == dom["kernel"] and m in dom["hbm"]["points"]]
             if vals:
                 traffic = round(sum(vals) / len(vals))
-        n_launch = sum(p["launches"] for p, r in zip(points, sweep) if r["bound"] == "hbm")
-        roofline = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": round(ach / peaks["hbm_gbs"], 3), "traffic": traffic,
-                    "algorithmic_bytes_per_launch": round(mem_bytes / max(1, n_launch)),
-                    "kernel": "gemm_mma_kernel", "over": "memory-bound points of the sweep",
+        h = dom["hbm"]
+        roofline = {"bound": "hbm", "achieved": h["achieved"], "peak": h["peak"], "unit": "GB/s",
+                    "frac": h["frac"], "traffic": traffic,
+                    "algorithmic_bytes_per_launch": h["algorithmic_bytes_per_launch"],
+                    "kernel": dom["kernel"], "over": f"its memory-bound points M={h['points']}",
+                    "share_of_step": round(dom["us_per_step"] / sum(e["us_per_step"] for e in roofline_by_kernel), 3),
                     "peak_source": peaks["source"]}
     else:
-        fl_t = sum(gemm_flops(p["M"], p["K"], p["N"]) for p in points)
-        t_t = sum(statistics.median(ts) * 1e-3 for ts in per_point)
-        ach = fl_t / t_t / 1e12
-        roofline = {"bound": "tensor", "achieved": round(ach, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                    "frac": round(ach / peaks["bf16_tflops"], 3), "traffic": None, "kernel": "gemm_mma_kernel",
-                    "peak_source": peaks["source"]}
+        t = dom["tensor"]
+        roofline = {"bound": "tensor", "achieved": t["achieved"], "peak": t["peak"], "unit": "TFLOP/s",
+                    "frac": t["frac"], "traffic": None, "kernel": dom["kernel"],
+                    "over": f"its points M={t['points']}", "peak_source": peaks["source"]}
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -435,7 +487,8 @@ def run_ours(args, rank, world, device):
                    "l2": "inputs larger than L2" if all(len(p["packs"]) == 1 for p in points)
                    else "weight copies rotated to exceed 3x L2",
                    "parallelism": f"replicas x{world}", "peaks": peaks["source"]},
-        "sweep": sweep, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "sweep": sweep, "roofline": roofline, "roofline_by_kernel": roofline_by_kernel,
+        "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
     }
 
