@@ -348,6 +348,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   }
 
   // ----------------------------------------------------------------- dequant
+  // The decode shares the SM's half-rate integer / FP16 issue with every
+  // integer instruction around it, so the loop keeps its bookkeeping small:
+  // ring positions advance by counters, addresses by offsets fixed here.
   const int dw = warp - kDequantWarp0;
   const int team = dw >> 3;          // this team writes the chunks with gc % 2 == team
   const int wg = (dw >> 2) & 1;      // which 64-row half of each 128-row chunk
@@ -357,13 +360,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   const int NG = p.K / p.G;
   const bool epi_lead = warp == kDequantWarp0;  // first warp of team 0
   const bool epi_group = team == 0;  // team 0 reads the accumulators out, each warpgroup half of the tokens
+  // byte offsets inside a weight stage: packed block (kq = 2c + wg, b = 2q + bi) and its scale pair
+  const uint32_t w_lane = static_cast<uint32_t>((wg * 8 + 2 * q) * 512 + lane * 16);
+  const uint32_t s_lane = static_cast<uint32_t>(KQ * 4096 + 2 * q * 32 + 4 * g);
+  // tensor-memory address of this warp's first store: lanes 32q.., columns of half wg
+  const uint32_t t_warp = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(wg * 32);
+  // this team's chunks are gc = team, team + 2, ...: A buffer a = gc % NA, phase ph = (gc / NA) & 1
+  int a = team, tcount = 0;
+  uint32_t ph = 0;
+  const int reuse_from = (NA - team + 1) >> 1;  // team chunks before this team's first gc >= NA
+  uint32_t st = sbase + p.w_base;    // weight stage s
   int s = 0, round = 0, segs = 0, seg_units = 0;
   int j = first_col, kt = kt0;
   for (int it = 0; it < nunits; ++it) {
-    const uint32_t st = sbase + p.w_base + s * p.w_stage_bytes;
     ++seg_units;
     const bool seg_end = (kt == p.KU - 1) || (it == nunits - 1);
-    const int c0 = (team - it * CH) & 1;  // this team's first chunk of the unit (then every second one)
+    const int c0 = (CH & 1) ? ((team ^ it) & 1) : team;  // this team's first chunk of the unit (then every second one)
     const bool go = __shfl_sync(0xffffffffu, *abort_flag == 0, 0);
     bool have = false;
     if (go) {
@@ -379,12 +391,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       for (int cc = 0; cc < 2; ++cc) {
         const int c = c0 + 2 * cc;
         if (c < CH) {
-          const int kq = 2 * c + wg;
 #pragma unroll
           for (int bi = 0; bi < 2; ++bi) {
-            const int b = 2 * q + bi;
-            wv[cc][bi] = lds128(st + (kq * 8 + b) * 512 + lane * 16);
-            sc[cc][bi] = grouped ? lds32(st + KQ * 4096 + (c * 128 + b * 16 + 2 * g) * 2) : 0x3c003c00u;
+            wv[cc][bi] = lds128(st + w_lane + c * 8192 + bi * 512);
+            sc[cc][bi] = grouped ? lds32(st + s_lane + c * 256 + bi * 32) : 0x3c003c00u;
           }
         }
       }
@@ -392,12 +402,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       if (lane == 0) mbar_arrive(bar_wempty + 8 * s);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        const int c = c0 + 2 * cc;
-        if (c >= CH || !have) break;
-        const int gc = it * CH + c;
-        const int a = gc % NA;
-        if (gc >= NA) {
-          bool ok = mbar_wait_bounded(bar_consumed + 8 * a, ((gc / NA) - 1) & 1, p.wait_limit, abort_flag);
+        if (c0 + 2 * cc >= CH || !have) break;
+        if (tcount >= reuse_from) {
+          bool ok = mbar_wait_bounded(bar_consumed + 8 * a, ph ^ 1u, p.wait_limit, abort_flag);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) {
             if (lane == 0) raise_abort();
@@ -408,9 +415,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         tc_fence_after();
 #pragma unroll
         for (int bi = 0; bi < 2; ++bi) {
-          const uint32_t spair = sc[cc][bi];
-          const uint32_t s_g = (spair & 0xffffu) * 0x10001u;
-          const uint32_t s_g8 = (spair >> 16) * 0x10001u;
+          const uint32_t s_g = __byte_perm(sc[cc][bi], 0u, 0x1010u);   // scale of row g in both halves
+          const uint32_t s_g8 = __byte_perm(sc[cc][bi], 0u, 0x3232u);  // scale of row g + 8
           const uint32_t words[4] = {wv[cc][bi].x, wv[cc][bi].y, wv[cc][bi].z, wv[cc][bi].w};
           uint32_t r[16];
 #pragma unroll
@@ -429,12 +435,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             r[4 * jj + 2] = v[1];
             r[4 * jj + 3] = v[3];
           }
-          tmem_st_16x256b_x4(tmem + (static_cast<uint32_t>(32 * q + 16 * bi) << 16) + a * kChunkCols + wg * 32, r);
+          tmem_st_16x256b_x4(t_warp + (static_cast<uint32_t>(16 * bi) << 16) + a * kChunkCols, r);
         }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_cfull + 8 * a);
+        ++tcount;
+        a += 2;
+        if (a >= NA) {
+          a -= NA;
+          ph ^= 1u;
+        }
       }
     }
     if (seg_end && epi_group) {
@@ -541,9 +553,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       ++segs;
     }
     if (seg_end) seg_units = 0;
+    st += p.w_stage_bytes;
     if (++s == SW) {
       s = 0;
       ++round;
+      st = sbase + p.w_base;
     }
     if (++kt == p.KU) {
       kt = 0;
