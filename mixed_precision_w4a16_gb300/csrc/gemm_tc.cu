@@ -43,10 +43,10 @@ namespace w4a16 {
 
 namespace {
 
-// warps: 0 weight producer, 1 activation producer, 2..5 MMA issuers 0..3 (warp 2 owns the
-// tensor memory), 6..21 dequant (team 0: warps 6..13, team 1: warps 14..21)
+// warps: 0 weight producer, 1 activation producer, 2..3 MMA issuers 0..1 (warp 2 owns the
+// tensor memory), 4..19 dequant (team 0: warps 4..11, team 1: warps 12..19)
 constexpr int kIssuerWarp0 = 2;
-constexpr int kDequantWarp0 = 6;
+constexpr int kDequantWarp0 = 4;
 constexpr int kDequantWarps = 16;  // both teams; every one releases each weight stage
 constexpr int kTeamWarps = 8;      // one team: the writers of one A chunk
 constexpr int kEpiThreads = 32 * kTeamWarps;  // team 0 runs the epilogue
