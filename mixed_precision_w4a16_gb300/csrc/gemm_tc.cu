@@ -43,10 +43,12 @@ namespace w4a16 {
 
 namespace {
 
-// warps: 0 weight producer, 1 activation producer, 2..3 MMA issuers 0..1 (warp 2 owns the
-// tensor memory), 4..19 dequant (team 0: warps 4..11, team 1: warps 12..19)
-constexpr int kIssuerWarp0 = 2;
-constexpr int kDequantWarp0 = 4;
+// warps: 0 weight producer, 1..2 activation producers (even / odd chunks), 3..4 MMA
+// issuers 0..1 (warp 3 owns the tensor memory), 5..20 dequant (team 0: warps 5..12,
+// team 1: warps 13..20)
+constexpr int kActWarp0 = 1;
+constexpr int kIssuerWarp0 = 3;
+constexpr int kDequantWarp0 = 5;
 constexpr int kDequantWarps = 16;  // both teams; every one releases each weight stage
 constexpr int kTeamWarps = 8;      // one team: the writers of one A chunk
 constexpr int kEpiThreads = 32 * kTeamWarps;  // team 0 runs the epilogue
@@ -218,26 +220,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     }
   };
 
-  if (warp < kIssuerWarp0) {
-    // ------------------------------------------- producers: warp 0 weights + scales (one stage per unit),
-    //                                               warp 1 activations (one stage per 128-row chunk)
-    const bool wprod = warp == 0;
-    const int S = wprod ? SW : NA;
-    const uint32_t full = wprod ? bar_wfull : bar_afull;
-    const uint32_t empty = wprod ? bar_wempty : bar_consumed;
-    if (!wprod && lane == 0) prefetch_tensormap(&tmA);
-    const uint64_t pol = wprod ? policy_evict_first() : policy_evict_last();
+  if (warp == 0) {
+    // ------------------------------------------- producer: weights + scale rows, one stage per unit
+    const uint64_t pol = policy_evict_first();
     const uint64_t pol_s = policy_evict_last();
     const int NG = p.K / p.G;
     const uint32_t w_bytes = static_cast<uint32_t>(KQ) * 4096u;
-    const int steps = wprod ? nunits : nunits * CH;  // stages to fill
     int issued = 0;
     int s = 0, round = 0;
-    int j = first_col, kt = kt0, c = 0;
-    for (int it = 0; it < steps; ++it) {
-      if (it >= S) {
+    int j = first_col, kt = kt0;
+    for (int it = 0; it < nunits; ++it) {
+      if (it >= SW) {
         bool ok = true;
-        if (lane == 0) ok = mbar_wait_bounded_sleep(empty + 8 * s, (round - 1) & 1, p.wait_limit, abort_flag);
+        if (lane == 0) ok = mbar_wait_bounded_sleep(bar_wempty + 8 * s, (round - 1) & 1, p.wait_limit, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) {
           if (lane == 0) raise_abort();
@@ -246,42 +241,82 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       }
       if (!(p.debug_stall && it == 0)) {  // with debug_stall, stage 0 stays empty: nothing completes its barrier
         if (lane == 0) {
-          const uint32_t fb = full + 8 * s;
-          if (wprod) {
-            const uint32_t st = sbase + p.w_base + s * p.w_stage_bytes;
-            mbar_arrive_expect_tx(fb, w_bytes + static_cast<uint32_t>(p.srows) * 256u);
-            const uint32_t* wsrc =
-                p.packed + (static_cast<long long>(j) * (p.K / 64) + static_cast<long long>(kt) * KQ) * 1024;
-            bulk_g2s(st, wsrc, w_bytes, fb, pol);
-            const int grp0 = (p.G == 128) ? kt * p.srows : 0;
-            const uint16_t* ssrc = p.scales + (static_cast<long long>(j) * NG + grp0) * 128;
-            bulk_g2s(st + w_bytes, ssrc, static_cast<uint32_t>(p.srows) * 256u, fb, pol_s);
-          } else {
-            const uint32_t st = sbase + s * p.a_stage_bytes;  // stage s = chunk gc % NA
-            mbar_arrive_expect_tx(fb, static_cast<uint32_t>(2 * A_BOX));
-            tma_load_3d(st, &tmA, 0, p.m0, kt * KQ + 2 * c, fb, pol);
-          }
+          const uint32_t fb = bar_wfull + 8 * s;
+          const uint32_t st = sbase + p.w_base + s * p.w_stage_bytes;
+          mbar_arrive_expect_tx(fb, w_bytes + static_cast<uint32_t>(p.srows) * 256u);
+          const uint32_t* wsrc =
+              p.packed + (static_cast<long long>(j) * (p.K / 64) + static_cast<long long>(kt) * KQ) * 1024;
+          bulk_g2s(st, wsrc, w_bytes, fb, pol);
+          const int grp0 = (p.G == 128) ? kt * p.srows : 0;
+          const uint16_t* ssrc = p.scales + (static_cast<long long>(j) * NG + grp0) * 128;
+          bulk_g2s(st + w_bytes, ssrc, static_cast<uint32_t>(p.srows) * 256u, fb, pol_s);
         }
         __syncwarp();
         issued = it + 1;
       }
-      if (++s == S) {
+      if (++s == SW) {
         s = 0;
         ++round;
       }
-      if (wprod || ++c == CH) {
-        c = 0;
-        if (++kt == p.KU) {
-          kt = 0;
-          ++j;
-        }
+      if (++kt == p.KU) {
+        kt = 0;
+        ++j;
       }
     }
     named_bar_sync(3, kTcThreads);
     if (*abort_flag && lane == 0) {
       const int first_filled = p.debug_stall ? 1 : 0;
-      for (int it = max(first_filled, issued - S); it < issued; ++it)
-        mbar_wait_bounded(full + 8 * (it % S), (it / S) & 1, kDrainCycles, zero_flag);
+      for (int it = max(first_filled, issued - SW); it < issued; ++it)
+        mbar_wait_bounded(bar_wfull + 8 * (it % SW), (it / SW) & 1, kDrainCycles, zero_flag);
+    }
+    return;
+  }
+
+  if (warp < kIssuerWarp0) {
+    // ------------------------------- activation producers: chunk gc's tile into stage gc % NA, warp
+    // kActWarp0 + (gc & 1) for chunk gc (NA is even, so each producer owns every other stage).  One
+    // thread's loop is slow while the dequant warps hold the issue slots; two share the chunks.
+    const int ap = warp - kActWarp0;
+    int last = -1;  // last chunk whose copy this lane issued
+    if (lane == 0) {
+      prefetch_tensormap(&tmA);
+      const uint64_t pol = policy_evict_last();
+      const int nch = nunits * CH;
+      int a = ap, c = ap, kt = kt0;
+      uint32_t ph = 0;  // phase bit (gc / NA) & 1 of chunk gc's stage
+      while (c >= CH) {
+        c -= CH;
+        if (++kt == p.KU) kt = 0;
+      }
+      for (int gc = ap; gc < nch; gc += 2) {
+        if (gc >= NA &&
+            !mbar_wait_bounded_sleep(bar_consumed + 8 * a, ph ^ 1u, p.wait_limit, abort_flag)) {
+          raise_abort();
+          break;
+        }
+        if (!(p.debug_stall && gc == 0)) {  // with debug_stall, stage 0 stays empty
+          mbar_arrive_expect_tx(bar_afull + 8 * a, static_cast<uint32_t>(2 * A_BOX));
+          tma_load_3d(sbase + a * p.a_stage_bytes, &tmA, 0, p.m0, kt * KQ + 2 * c, bar_afull + 8 * a, pol);
+          last = gc;
+        }
+        a += 2;
+        if (a >= NA) {
+          a -= NA;
+          ph ^= 1u;
+        }
+        c += 2;
+        while (c >= CH) {
+          c -= CH;
+          if (++kt == p.KU) kt = 0;
+        }
+      }
+    }
+    __syncwarp();
+    named_bar_sync(3, kTcThreads);
+    if (*abort_flag && lane == 0) {
+      // copies possibly in flight: this producer's latest one on each of its stages
+      for (int gc = last; gc >= 0 && gc > last - NA; gc -= 2)
+        mbar_wait_bounded(bar_afull + 8 * (gc % NA), (gc / NA) & 1, kDrainCycles, zero_flag);
     }
     return;
   }

@@ -60,7 +60,7 @@ constexpr int kStrip = 128;       // output columns per strip / work unit
 cudaError_t launch_gemm_mma(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream);
 
 // ---- tensor-memory (tcgen05) GEMM ----------------------------------------
-constexpr int kTcThreads = 640;  // 2 producers, 2 MMA issuers, 16 dequant warps (two teams)
+constexpr int kTcThreads = 672;  // 3 producers, 2 MMA issuers, 16 dequant warps (two teams)
 constexpr int kTcMaxIssuers = 2;
 
 struct TcLayout {
