@@ -324,8 +324,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   if (warp < kDequantWarp0) {
     // ------------------------------------------------------------- MMA issuers
     // A single thread can issue a tcgen05.mma only every ~90 cycles, far below the
-    // tensor core's rate for small N; NI threads therefore issue in parallel, each
-    // taking every NI-th 128-row chunk of a strip segment into its own accumulator.
+    // tensor core's rate for small N; NI threads therefore issue in parallel, issuer i
+    // taking the chunks gc = i mod NI into its own accumulator.  The loop visits only
+    // those chunks: a starved thread pays for every instruction.
     const int issuer = warp - kIssuerWarp0;
     if (lane == 0 && issuer < NI) {
       const uint32_t d_tmem = tmem + kDCol + issuer * MB;
@@ -333,27 +334,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       const uint32_t hi = smem_desc_sw128_hi();
       const uint32_t stage16 = static_cast<uint32_t>(p.a_stage_bytes) >> 4;
       const uint32_t box16 = static_cast<uint32_t>(A_BOX) >> 4;
-      int a = 0, turn = 0, segs = 0, kt = kt0;
-      uint32_t ph = 0;
+      int a = issuer, segs = 0, kt = kt0;  // a = gc % NA of this issuer's next chunk
+      uint32_t ph = 0;                     // phase bit (gc / NA) & 1
       bool first = true;  // next chunk of this issuer starts its accumulator for the segment
       bool ok = true;
-      for (int it = 0; it < nunits && ok && !*abort_flag; ++it) {
+      for (int it = 0; it < nunits; ++it) {
         const bool seg_end = (kt == p.KU - 1) || (it == nunits - 1);
-        for (int c = 0; c < CH; ++c) {
-          if (turn == issuer) {
-            ok = mbar_wait_bounded_sleep(bar_afull + 8 * a, ph, p.wait_limit, abort_flag) &&
-                 mbar_wait_bounded_sleep(bar_cfull + 8 * a, ph, p.wait_limit, abort_flag);
-            // the previous segment's accumulators must have been read out
-            if (ok && first && segs > 0) ok = mbar_wait_bounded(bar_dempty, (segs - 1) & 1, p.wait_limit, abort_flag);
-            if (!ok) break;
-            tc_fence_after();
-            tc_mma_chunk(d_tmem, tmem + a * kChunkCols, lo0 + a * stage16, hi, box16, p.idesc, first ? 0u : 1u);
-            tc_commit(bar_consumed + 8 * a);  // stage and A buffer free once these multiplies complete
-            first = false;
-          }
-          if (++turn == NI) turn = 0;
-          if (++a == NA) {
-            a = 0;
+        const int c0 = (NI == 1) ? 0 : ((CH & 1) ? ((issuer ^ it) & 1) : issuer);  // first own chunk of the unit
+        for (int c = c0; c < CH; c += NI) {
+          ok = mbar_wait_bounded_sleep(bar_afull + 8 * a, ph, p.wait_limit, abort_flag) &&
+               mbar_wait_bounded_sleep(bar_cfull + 8 * a, ph, p.wait_limit, abort_flag);
+          // the previous segment's accumulators must have been read out
+          if (ok && first && segs > 0) ok = mbar_wait_bounded(bar_dempty, (segs - 1) & 1, p.wait_limit, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          tc_mma_chunk(d_tmem, tmem + a * kChunkCols, lo0 + a * stage16, hi, box16, p.idesc, first ? 0u : 1u);
+          tc_commit(bar_consumed + 8 * a);  // stage and A buffer free once these multiplies complete
+          first = false;
+          a += NI;
+          if (a >= NA) {
+            a -= NA;
             ph ^= 1u;
           }
         }
@@ -364,7 +364,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         if (seg_end) {
           tc_commit(bar_dfull);
           ++segs;
-          turn = 0;
           first = true;
         }
         if (++kt == p.KU) kt = 0;
@@ -506,11 +505,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                     : __half2float(__ushort_as_half(p.scales[static_cast<long long>(j) * NG * 128 + scale_pos(row)]));
         const int c_first = (j * p.KU) / p.T;
         const int c_last = min(((j + 1) * p.KU - 1) / p.T, p.grid - 1);
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + kDCol;
         const int nchunks = MB / 16;
         const int half = (nchunks + 1) >> 1;       // 16-token groups of warpgroup 0; warpgroup 1 takes the rest
         const int ch_lo = wg * half, ch_hi = min(nchunks, ch_lo + half);
-        const int nact = min(NI, seg_units * CH);  // accumulator regions written in this segment
+        // accumulator regions written in this segment: chunk gc went to issuer gc % NI
+        const int nseg = seg_units * CH;
+        const int nact = min(NI, nseg);
+        const int r_first = (nseg >= NI) ? 0 : (((it - seg_units + 1) * CH) % NI);
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + kDCol + r_first * MB;
         // sum of the active accumulator regions for tokens ch*16 .. ch*16+15 (fixed order)
         auto load_sum = [&](int ch, float (&out)[16]) {
           uint32_t v[16];
