@@ -148,7 +148,8 @@ Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin) {
   // Tensor memory (512 columns): ni accumulators of mb columns (ni * mb <= 256),
   // the rest for the ring of 64-column A chunks.  Activation stages pair with the
   // A buffers (one per chunk in flight).
-  pl.ni = std::max(1, std::min(kTcMaxIssuers, 256 / pl.mb));
+  pl.ni = 1;  // a power of two: issuer i takes the chunks gc = i mod ni
+  while (2 * pl.ni <= std::min(kTcMaxIssuers, 256 / pl.mb)) pl.ni *= 2;
   pl.na = std::min(6, (512 - pl.ni * pl.mb) / 64) & ~1;  // even: two activation producers take alternate chunks
   // Unit depth KT = 128 * ch for the weight ring (one copy per unit, released by
   // the dequant warps).  Keep >= 8 chunks of weights in flight; among the

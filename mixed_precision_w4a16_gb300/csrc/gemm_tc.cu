@@ -43,12 +43,12 @@ namespace w4a16 {
 
 namespace {
 
-// warps: 0 weight producer, 1..2 activation producers (even / odd chunks), 3..4 MMA
-// issuers 0..1 (warp 3 owns the tensor memory), 5..20 dequant (team 0: warps 5..12,
-// team 1: warps 13..20)
+// warps: 0 weight producer, 1..2 activation producers (even / odd chunks), 3..6 MMA
+// issuers 0..3 (warp 3 owns the tensor memory), 7..22 dequant (team 0: warps 7..14,
+// team 1: warps 15..22)
 constexpr int kActWarp0 = 1;
 constexpr int kIssuerWarp0 = 3;
-constexpr int kDequantWarp0 = 5;
+constexpr int kDequantWarp0 = 7;
 constexpr int kDequantWarps = 16;  // both teams; every one releases each weight stage
 constexpr int kTeamWarps = 8;      // one team: the writers of one A chunk
 constexpr int kEpiThreads = 32 * kTeamWarps;  // team 0 runs the epilogue
@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       bool ok = true;
       for (int it = 0; it < nunits; ++it) {
         const bool seg_end = (kt == p.KU - 1) || (it == nunits - 1);
-        const int c0 = (NI == 1) ? 0 : ((CH & 1) ? ((issuer ^ it) & 1) : issuer);  // first own chunk of the unit
+        const int c0 = (issuer - it * CH) & (NI - 1);  // first own chunk of the unit (NI is a power of two)
         for (int c = c0; c < CH; c += NI) {
           ok = mbar_wait_bounded_sleep(bar_afull + 8 * a, ph, p.wait_limit, abort_flag) &&
                mbar_wait_bounded_sleep(bar_cfull + 8 * a, ph, p.wait_limit, abort_flag);
@@ -508,20 +508,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         const int nchunks = MB / 16;
         const int half = (nchunks + 1) >> 1;       // 16-token groups of warpgroup 0; warpgroup 1 takes the rest
         const int ch_lo = wg * half, ch_hi = min(nchunks, ch_lo + half);
-        // accumulator regions written in this segment: chunk gc went to issuer gc % NI
+        // accumulator regions written in this segment: chunk gc went to issuer gc % NI,
+        // summed in a fixed order starting at the segment's first chunk
         const int nseg = seg_units * CH;
         const int nact = min(NI, nseg);
-        const int r_first = (nseg >= NI) ? 0 : (((it - seg_units + 1) * CH) % NI);
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + kDCol + r_first * MB;
+        const int r_first = (nseg >= NI) ? 0 : (((it - seg_units + 1) * CH) & (NI - 1));
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + kDCol;
         // sum of the active accumulator regions for tokens ch*16 .. ch*16+15 (fixed order)
         auto load_sum = [&](int ch, float (&out)[16]) {
           uint32_t v[16];
-          tmem_ld_32x32b_x16(taddr + ch * 16, v);
+          tmem_ld_32x32b_x16(taddr + r_first * MB + ch * 16, v);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i) out[i] = __uint_as_float(v[i]);
-          for (int r = 1; r < nact; ++r) {
-            tmem_ld_32x32b_x16(taddr + r * MB + ch * 16, v);
+          for (int t = 1; t < nact; ++t) {
+            tmem_ld_32x32b_x16(taddr + ((r_first + t) & (NI - 1)) * MB + ch * 16, v);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 16; ++i) out[i] += __uint_as_float(v[i]);

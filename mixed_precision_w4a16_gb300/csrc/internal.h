@@ -60,8 +60,8 @@ constexpr int kStrip = 128;       // output columns per strip / work unit
 cudaError_t launch_gemm_mma(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream);
 
 // ---- tensor-memory (tcgen05) GEMM ----------------------------------------
-constexpr int kTcThreads = 672;  // 3 producers, 2 MMA issuers, 16 dequant warps (two teams)
-constexpr int kTcMaxIssuers = 2;
+constexpr int kTcThreads = 736;  // 3 producers, 4 MMA issuers, 16 dequant warps (two teams)
+constexpr int kTcMaxIssuers = 4;
 
 struct TcLayout {
   int a_stage_bytes, w_stage_bytes, w_base, bar_off, flag_off, smem_bytes;
