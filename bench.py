@@ -8,7 +8,7 @@ M).  The packed weights (679 MB) exceed the 129 MB L2, so every GEMM streams
 its weights from HBM without any flush.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload big|pr1|7b|70b|prefill]
+                    [--workload big|pr1|7b|70b|prefill|profile_m32|profile_m8]
 
 Prints one JSON line (rank 0).  ``value`` is the whole-job throughput in TB/s
 of algorithmic bytes (2MK + 0.5KN + 2(K/G)N + 2MN per GEMM) over the timed
@@ -50,6 +50,9 @@ WORKLOADS = {
              (8192, 10240, -1, [32]), (8192, 8192, -1, [32]), (8192, 57344, -1, [32]), (28672, 8192, -1, [32])], 3),
     "prefill": ("compute-bound prefill M in {256,512,1024}, K=8192 N=28672 group 128",
                 [(8192, 28672, 128, [256, 512, 1024])], 4),
+    # small cases of the big layer's kernels for full ncu captures (weights still larger than L2)
+    "profile_m32": ("profiling case M=32 K=18432 N=16384 group 128", [(18432, 16384, 128, [32])], 2),
+    "profile_m8": ("profiling case M=8 K=18432 N=16384 group 128", [(18432, 16384, 128, [8])], 2),
 }
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -137,7 +140,8 @@ def workload_totals(layers):
 
 def cpu_sample_cols(workload):
     """Columns of each GEMM the oracle computes for the cpu_baseline leg (~10-20 s single-threaded)."""
-    return {"big": 12288, "pr1": 1024, "7b": 16384, "70b": 8192, "prefill": 2048}[workload]
+    return {"big": 12288, "pr1": 1024, "7b": 16384, "70b": 8192, "prefill": 2048,
+            "profile_m32": 4096, "profile_m8": 4096}[workload]
 
 
 def kernel_source_hash():
