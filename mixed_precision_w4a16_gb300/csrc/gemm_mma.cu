@@ -186,7 +186,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       }
     }
     if (have) {
-      for (int kq = kq0; kq < KQ; kq += 4) {
+      // this warp's pieces kq0, kq0 + 4 of the unit (KQ <= 8), unrolled so the second piece's
+      // loads and decode can overlap the first piece's multiply chain
+#pragma unroll
+      for (int pc = 0; pc < 2; ++pc) {
+        const int kq = kq0 + 4 * pc;
+        if (kq >= KQ) break;
         // activation fragments of this 64-row piece: 4 k16 steps x MT token tiles.  The packed
         // weights hold k = 4t .. 4t+3 of each 16-row block where the m16n8k16 fragment expects
         // 2t, 2t+1, 2t+8, 2t+9, so the matching activation pair is one 8-byte load of
