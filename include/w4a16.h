@@ -54,7 +54,8 @@ typedef enum {
   W4A16_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed */
   W4A16_ERR_TIMEOUT = 7,     /* a pipeline wait ran out of time (device-detected) */
   W4A16_ERR_ARCH = 8,        /* current device is not compute capability 10.3 */
-  W4A16_ERR_ALIGN = 9        /* a device pointer is not 16-byte aligned */
+  W4A16_ERR_ALIGN = 9,       /* a device pointer is not 16-byte aligned */
+  W4A16_ERR_VALUE = 10       /* quantisation saw a non-finite w / s (zero, NaN or infinite input; device-detected) */
 } w4a16_status;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -108,6 +109,26 @@ W4A16_API size_t w4a16_workspace_bytes(int M, int K, int N, int groupsize);
  * ------------------------------------------------------------------------- */
 W4A16_API int w4a16_repack(const uint8_t* q, const uint16_t* s, int K, int N, int groupsize,
                  uint32_t* packed, uint16_t* scales_p, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Fused quantise + repack from FP16 weights and given FP16 scales (the
+ * original Layer.pack step, deep-dive article section "可复现的调用链": the
+ * weights are divided by the scale, rounded, offset by 8 and clamped to
+ * [0, 15], then laid out like w4a16_repack).
+ *
+ *   w         device, fp16[K][N] row-major: the weights to quantise
+ *   s         device, fp16[K/G][N] row-major: their scales (any sign)
+ *   packed    device, uint32[K*N/8], written: same layout as w4a16_repack
+ *   scales_p  device, fp16[K/G*N], written: s permuted as by w4a16_repack
+ *
+ * Per weight: q = clamp(rint(w / s) + 8, 0, 15), where w / s is the IEEE
+ * float32 quotient of the two FP16 values (correctly rounded) and rint
+ * rounds half to even.  A quotient that is NaN or infinite (s = 0, or a
+ * NaN / infinite input) stores code 8 and flags W4A16_ERR_VALUE for
+ * w4a16_get_status(NULL, stream).  Inputs and outputs must not overlap.
+ * ------------------------------------------------------------------------- */
+W4A16_API int w4a16_quantize_repack(const uint16_t* w, const uint16_t* s, int K, int N, int groupsize,
+                          uint32_t* packed, uint16_t* scales_p, void* stream);
 
 /* Inverse of w4a16_repack (diagnostic; the pages' layout check "repack then
  * unpack recovers the same codes and scales", deep-dive article section

@@ -16,10 +16,11 @@ import os
 __all__ = [
     "W4A16Error", "lib", "Plan",
     "w4a16_packed_bytes", "w4a16_scales_count", "w4a16_workspace_bytes", "w4a16_plan",
-    "w4a16_repack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm", "w4a16_gemm_noalloc", "w4a16_get_status",
+    "w4a16_repack", "w4a16_quantize_repack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm", "w4a16_gemm_noalloc",
+    "w4a16_get_status",
     "w4a16_debug_set_wait_cycles", "w4a16_debug_inject_stall", "w4a16_debug_force_path", "w4a16_status_string",
     "EXPORTED_SYMBOLS",
-    "repack", "unpack", "dequant", "gemm", "workspace_for",
+    "repack", "quantize_repack", "unpack", "dequant", "gemm", "workspace_for",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -29,7 +30,7 @@ EXPORTED_SYMBOLS = (
     "w4a16_status_string", "w4a16_abi_version", "w4a16_packed_bytes", "w4a16_scales_count",
     "w4a16_workspace_bytes", "w4a16_repack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm",
     "w4a16_get_status", "w4a16_plan", "w4a16_debug_set_wait_cycles", "w4a16_debug_inject_stall",
-    "w4a16_gemm_noalloc", "w4a16_debug_force_path",
+    "w4a16_gemm_noalloc", "w4a16_debug_force_path", "w4a16_quantize_repack",
 )
 
 
@@ -71,6 +72,7 @@ def _load():
         "w4a16_debug_inject_stall": (None, [i]),
         "w4a16_gemm_noalloc": (i, [vp, vp, vp, vp, i, i, i, i, vp]),
         "w4a16_debug_force_path": (None, [i]),
+        "w4a16_quantize_repack": (i, [vp, vp, i, i, i, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -158,6 +160,11 @@ def w4a16_repack(q, s, K, N, groupsize, packed, scales_p, stream=None):
            "w4a16_repack")
 
 
+def w4a16_quantize_repack(w, s, K, N, groupsize, packed, scales_p, stream=None):
+    _check(_lib().w4a16_quantize_repack(_ptr(w), _ptr(s), K, N, groupsize, _ptr(packed), _ptr(scales_p),
+                                        _stream(stream)), "w4a16_quantize_repack")
+
+
 def w4a16_unpack(packed, scales_p, K, N, groupsize, q, s, stream=None):
     _check(_lib().w4a16_unpack(_ptr(packed), _ptr(scales_p), K, N, groupsize, _ptr(q), _ptr(s), _stream(stream)),
            "w4a16_unpack")
@@ -223,6 +230,17 @@ def repack(q, s, groupsize: int, stream=None):
     packed = torch.empty(K * N // 8, dtype=torch.int32, device=q.device)
     sp = torch.empty(s.numel(), dtype=torch.float16, device=q.device)  # permuted: fp16[N/128][K/G][128]
     w4a16_repack(q, s, K, N, groupsize, packed, sp, stream)
+    return packed, sp
+
+
+def quantize_repack(w, s, groupsize: int, stream=None):
+    """w fp16[K][N], s fp16[K/G][N] (CUDA tensors) -> (packed int32[K*N/8], permuted fp16[K/G][N])
+    with q = clamp(rint(w / s) + 8, 0, 15)."""
+    import torch
+    K, N = w.shape
+    packed = torch.empty(K * N // 8, dtype=torch.int32, device=w.device)
+    sp = torch.empty(s.numel(), dtype=torch.float16, device=w.device)
+    w4a16_quantize_repack(w, s, K, N, groupsize, packed, sp, stream)
     return packed, sp
 
 

@@ -246,6 +246,7 @@ const char* w4a16_status_string(int status) {
     case W4A16_ERR_TIMEOUT: return "W4A16_ERR_TIMEOUT";
     case W4A16_ERR_ARCH: return "W4A16_ERR_ARCH";
     case W4A16_ERR_ALIGN: return "W4A16_ERR_ALIGN";
+    case W4A16_ERR_VALUE: return "W4A16_ERR_VALUE";
     default: return "W4A16_ERR_UNKNOWN";
   }
 }
@@ -315,6 +316,20 @@ int w4a16_repack(const uint8_t* q, const uint16_t* s, int K, int N, int groupsiz
   if (r != W4A16_OK) return r;
   const cudaError_t e = launch_repack(q, s, K, N, effective_group(K, groupsize), packed, scales_p,
                                       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
+int w4a16_quantize_repack(const uint16_t* w, const uint16_t* s, int K, int N, int groupsize, uint32_t* packed,
+                          uint16_t* scales_p, void* stream) {
+  const int st = check_shape(K, N, groupsize);
+  if (st != W4A16_OK) return st;
+  if (!w || !s || !packed || !scales_p) return W4A16_ERR_NULL;
+  if (!aligned16(w) || !aligned16(s) || !aligned16(packed) || !aligned16(scales_p)) return W4A16_ERR_ALIGN;
+  DeviceInfo* d = nullptr;
+  const int r = current_device_info(&d);
+  if (r != W4A16_OK) return r;
+  const cudaError_t e = launch_quantize_repack(w, s, K, N, effective_group(K, groupsize), packed, scales_p,
+                                               static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
 }
 
@@ -505,6 +520,7 @@ int w4a16_get_status(void* workspace, void* stream) {
     if (cudaStreamSynchronize(s) != cudaSuccess) return W4A16_ERR_CUDA;
   }
   if (flag & kDevErrCodeRange) return W4A16_ERR_CODE_RANGE;
+  if (flag & kDevErrValue) return W4A16_ERR_VALUE;
   if (word & kDevErrTimeout) return W4A16_ERR_TIMEOUT;
   if (word) return W4A16_ERR_CUDA;
   return W4A16_OK;

@@ -11,6 +11,7 @@ namespace w4a16 {
 enum : uint32_t {
   kDevErrCodeRange = 1u << 0,
   kDevErrTimeout = 1u << 1,
+  kDevErrValue = 1u << 2,
 };
 
 // Shared-memory layout of one streaming-kernel configuration (byte offsets
@@ -94,6 +95,8 @@ cudaError_t launch_gemm_tc(int smem_bytes, const CUtensorMap& tmA, const TcParam
 
 cudaError_t launch_repack(const uint8_t* q, const uint16_t* s, int K, int N, int G, uint32_t* packed,
                           uint16_t* scales_p, cudaStream_t stream);
+cudaError_t launch_quantize_repack(const uint16_t* w, const uint16_t* s, int K, int N, int G, uint32_t* packed,
+                                   uint16_t* scales_p, cudaStream_t stream);
 cudaError_t launch_unpack(const uint32_t* packed, const uint16_t* scales_p, int K, int N, int G, uint8_t* q,
                           uint16_t* s, cudaStream_t stream);
 cudaError_t launch_dequant(const uint32_t* packed, const uint16_t* scales_p, int K, int N, int G, uint16_t* bhat,

@@ -79,6 +79,45 @@ __global__ void repack_codes_kernel(const uint8_t* __restrict__ q, int K, int N,
   packed[v] = make_uint4(words[0], words[1], words[2], words[3]);
 }
 
+// Quantise FP16 weights with their FP16 scales straight into the packed layout
+// (the original Layer.pack step, deep-dive article section "可复现的调用链"):
+// q = clamp(rint(w / s) + 8, 0, 15), the quotient an IEEE float32 division,
+// rint rounding half to even.  Same word-side walk as repack_codes_kernel.
+__global__ void quantize_codes_kernel(const uint16_t* __restrict__ w, const uint16_t* __restrict__ s, int K, int N,
+                                      int G, uint4* __restrict__ packed, long long nvec) {
+  const long long v = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (v >= nvec) return;
+  const VecCoord vc = vec_coord(v, K);
+  const int g = vc.lane >> 2, t = vc.lane & 3;
+  uint32_t words[4];
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int slot = 0; slot < 8; ++slot) {
+      int r, c;
+      slot_rc(slot, g, t, r, c);
+      const long long k = vc.kb * 64LL + 16 * j + c;
+      const long long n = vc.nb * 16LL + r;
+      const float wf = __half2float(__ushort_as_half(w[k * N + n]));
+      const float sf = __half2float(__ushort_as_half(s[(k / G) * N + n]));
+      const float quot = __fdiv_rn(wf, sf);
+      uint32_t code = 8u;
+      if (isfinite(quot)) {
+        const float qf = fminf(fmaxf(rintf(quot) + 8.0f, 0.0f), 15.0f);
+        code = static_cast<uint32_t>(qf);
+      } else {
+        bad = true;
+      }
+      word |= code << (4 * slot);
+    }
+    words[j] = word;
+  }
+  if (bad) atomicOr(&g_repack_flag, kDevErrValue);
+  packed[v] = make_uint4(words[0], words[1], words[2], words[3]);
+}
+
 // permuted position p inside a 16-column block -> fragment row r
 __device__ __forceinline__ int perm_row(int p) { return (p >> 1) + 8 * (p & 1); }
 
@@ -157,6 +196,18 @@ cudaError_t launch_repack(const uint8_t* q, const uint16_t* s, int K, int N, int
                           uint16_t* scales_p, cudaStream_t stream) {
   const long long nvec = static_cast<long long>(K) * N / 32;
   repack_codes_kernel<<<grid_for(nvec, 256), 256, 0, stream>>>(q, K, N, reinterpret_cast<uint4*>(packed), nvec);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long ns = static_cast<long long>(K / G) * N;
+  permute_scales_kernel<<<grid_for(ns, 256), 256, 0, stream>>>(s, scales_p, N, K / G, ns, 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_repack(const uint16_t* w, const uint16_t* s, int K, int N, int G, uint32_t* packed,
+                                   uint16_t* scales_p, cudaStream_t stream) {
+  const long long nvec = static_cast<long long>(K) * N / 32;
+  quantize_codes_kernel<<<grid_for(nvec, 256), 256, 0, stream>>>(w, s, K, N, G, reinterpret_cast<uint4*>(packed),
+                                                                  nvec);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long ns = static_cast<long long>(K / G) * N;

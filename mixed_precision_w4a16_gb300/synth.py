@@ -18,7 +18,7 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["make_weights", "make_activations", "make_layer", "effective_group"]
+__all__ = ["make_weights", "make_fp16_weights", "make_activations", "make_layer", "effective_group"]
 
 
 def _rng(seed: int, stream: int) -> np.random.Generator:
@@ -40,6 +40,22 @@ def make_weights(K: int, N: int, groupsize: int, seed: int):
     q = rng.integers(0, 16, size=(K, N), dtype=np.uint8)
     s = rng.uniform(0.002, 0.02, size=(K // G, N)).astype(np.float16)
     return q, s
+
+
+def make_fp16_weights(K: int, N: int, groupsize: int, seed: int, signed_scales: bool = False):
+    """Unquantised weights ``w`` float16[K][N] ~ N(0, 0.05) and scales ``s``
+    float16[K/G][N] uniform on [0.01, 0.03] (optionally with random signs), the
+    inputs of quantise-and-repack: w / s is mostly inside the 4-bit range, with
+    some values beyond it on either side."""
+    G = effective_group(K, groupsize)
+    if G <= 0 or K % G:
+        raise ValueError("K must be a positive multiple of the group size")
+    rng = _rng(seed, 2)
+    w = (rng.standard_normal((K, N), dtype=np.float32) * np.float32(0.05)).astype(np.float16)
+    s = rng.uniform(0.01, 0.03, size=(K // G, N))
+    if signed_scales:
+        s = s * rng.choice(np.array([-1.0, 1.0]), size=s.shape)
+    return w, s.astype(np.float16)
 
 
 def make_activations(M: int, K: int, seed: int) -> np.ndarray:

@@ -26,6 +26,7 @@ from .w4a16_oracle import (  # noqa: F401
     error_excess,
     packed_position,
     scale_position,
+    quantize,
     repack,
     unpack,
     TOL_REL,

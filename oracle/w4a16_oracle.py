@@ -224,6 +224,35 @@ def _check_layout_shape(K: int, N: int):
         raise ValueError("the packed layout needs K % 64 == 0 and N % 128 == 0")
 
 
+def quantize(w, s, G: int) -> np.ndarray:
+    """4-bit codes of FP16 weights w[K][N] with FP16 scales s[K/G][N], the step
+    before the repack ([P2] section "可复现的调用链": the original Layer.pack
+    divides the weights by the scale, rounds, adds the offset 8 and clamps to
+    [0, 15]):
+
+        q[k, n] = clamp(rint(w[k, n] / s[floor(k/G), n]) + 8, 0, 15).
+
+    Readings taken (the page prints no code): the quotient is the IEEE float32
+    division of the two FP16 values (both are exact in float32, the division
+    rounds once, to nearest); "round" is to nearest with ties to even.  A NaN
+    or infinite quotient (a zero, NaN or infinite input) is an error.
+    """
+    w64 = _as_f64(w)
+    if w64.ndim != 2:
+        raise ValueError("weights must have shape [K][N]")
+    K, N = w64.shape
+    G = _group(K, G)
+    s64 = _as_f64(s)
+    if s64.shape != (K // G, N):
+        raise ValueError("scales must have shape [K/G][N]")
+    with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
+        quot = w64.astype(np.float32) / s64[np.arange(K) // G, :].astype(np.float32)
+    if not np.all(np.isfinite(quot)):
+        raise ValueError("w / s is NaN or infinite (zero, NaN or infinite input)")
+    q = np.clip(np.rint(quot).astype(np.float64) + Z_POINT, 0, 15)
+    return q.astype(np.uint8)
+
+
 def repack(q, s, G: int):
     """Codes uint8[K][N] and scales fp16[K/G][N] -> (packed uint32[K*N/8], permuted fp16[(K/G)*N])."""
     q = np.asarray(q)

@@ -1,0 +1,90 @@
+"""Fused quantise + repack from FP16 weights on the GPU against the CPU oracle
+(byte exact): q = clamp(rint(w / s) + 8, 0, 15) in the packed layout."""
+import numpy as np
+import pytest
+
+import oracle
+from mixed_precision_w4a16_gb300 import synth
+import w4a16_testlib as tl
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(128, 128, 128), (256, 384, 128), (1024, 1024, 128), (512, 384, -1), (4096, 512, 128),
+          (11008, 256, 128), (1024, 640, 1024)]
+
+
+@pytest.fixture(scope="module")
+def w():
+    return tl.lib()
+
+
+def _quantize_on_device(w, wt, s, G):
+    torch = tl.torch_mod()
+    packed, sp = w.quantize_repack(tl.to_dev(wt), tl.to_dev(s), G)
+    torch.cuda.synchronize()
+    return packed.cpu().numpy().view(np.uint32), sp.cpu().numpy().view(np.uint16).ravel()
+
+
+@pytest.mark.parametrize("K,N,G", SHAPES)
+@pytest.mark.parametrize("signed", [False, True])
+def test_quantize_repack_matches_oracle_bytes(w, K, N, G, signed):
+    wt, s = synth.make_fp16_weights(K, N, G, seed=K + 5 * N, signed_scales=signed)
+    got_packed, got_sp = _quantize_on_device(w, wt, s, G)
+    ref_packed, ref_sp = oracle.repack(oracle.quantize(wt, s, G), s, G)
+    assert np.array_equal(got_packed, ref_packed)
+    assert np.array_equal(got_sp, ref_sp.view(np.uint16))
+    assert w.w4a16_get_status() == 0
+
+
+def test_quantize_ties_and_clamps(w):
+    """Exact half-integer quotients round to even; out-of-range quotients clamp."""
+    K, N = 128, 128
+    vals = np.array([0.5, 1.5, 2.5, 3.5, -0.5, -1.5, -2.5, -3.5, 7.5, -8.5, 8.0, -9.0, 7.0, -8.0, 1000.0, -1000.0])
+    wt = np.tile(vals, K * N // 16).reshape(K, N)
+    for scale in (1.0, 0.25):
+        wts = (wt * scale).astype(np.float16)
+        s = np.full((1, N), scale, dtype=np.float16)
+        got_packed, _ = _quantize_on_device(w, wts, s, -1)
+        want = np.tile(np.array([8, 10, 10, 12, 8, 6, 6, 4, 15, 0, 15, 0, 15, 0, 15, 0], np.uint8), K * N // 16)
+        assert np.array_equal(got_packed, oracle.repack(want.reshape(K, N), s, -1)[0])
+
+
+@pytest.mark.parametrize("K,N,G", [(1024, 512, 128), (512, 384, -1)])
+def test_quantize_of_dequantised_weights_recovers_packed_stream(w, K, N, G):
+    """quantise_repack(dequant(packed)) == packed: the device round trip through FP16 weights."""
+    q, s = synth.make_weights(K, N, G, seed=77 + K)
+    _, s_d, packed, sp = tl.device_layer(w, q, s, G)
+    bhat = w.dequant(packed, sp, K, N, G)
+    packed2, sp2 = w.quantize_repack(bhat, s_d, G)
+    tl.torch_mod().cuda.synchronize()
+    assert np.array_equal(packed2.cpu().numpy(), packed.cpu().numpy())
+    assert np.array_equal(sp2.cpu().numpy(), sp.cpu().numpy())
+
+
+def test_zero_scale_is_reported_and_cleared(w):
+    K, N, G = 256, 128, 128
+    wt, s = synth.make_fp16_weights(K, N, G, seed=5)
+    s[1, 7] = 0.0
+    got_packed, _ = _quantize_on_device(w, wt, s, G)
+    assert w.w4a16_get_status() == 10  # W4A16_ERR_VALUE
+    assert w.w4a16_get_status() == 0   # read and cleared
+    # every other code is still the oracle's; the column with the zero scale stores code 8 there
+    s_ok = s.copy()
+    s_ok[1, 7] = 1.0
+    ref_q = oracle.quantize(wt, s_ok, G)
+    ref_q[128:256, 7] = 8
+    assert np.array_equal(got_packed, oracle.repack(ref_q, s, G)[0])
+
+
+def test_quantize_full_k_sampled_strips(w):
+    """K = 18432 (the big layer's depth), N = 8192; four 128-column strips checked byte for byte."""
+    K, N, G = 18432, 8192, 128
+    wt, s = synth.make_fp16_weights(K, N, G, seed=2)
+    got_packed, got_sp = _quantize_on_device(w, wt, s, G)
+    words_per_strip = K * 128 // 8
+    for j in (0, 17, 40, N // 128 - 1):
+        cols = slice(128 * j, 128 * (j + 1))
+        ref_packed, ref_sp = oracle.repack(oracle.quantize(wt[:, cols], s[:, cols], G), s[:, cols], G)
+        assert np.array_equal(got_packed[j * words_per_strip:(j + 1) * words_per_strip], ref_packed)
+        sps = (K // G) * 128
+        assert np.array_equal(got_sp[j * sps:(j + 1) * sps], ref_sp.view(np.uint16))

@@ -352,3 +352,79 @@ def test_repack_word_decodes_to_fragment_values():
             for p, (dr, dc) in ISA_A_FRAGMENT.items():
                 slot = p // 2 + 4 * (p % 2)
                 assert (w >> (4 * slot)) & 15 == q[16 * j + PERM_K(t, dc), g + dr]
+
+
+# ---------------------------------------------------------------------------
+# quantise (the Layer.pack step: divide by the scale, round, add 8, clamp)
+# ---------------------------------------------------------------------------
+
+def _f32_round_exact(fr: Fraction) -> Fraction:
+    """The float32 nearest to an exact rational (ties to even), found by exact
+    comparison with the neighbouring float32 values -- independent of any
+    floating-point division."""
+    x = np.float32(float(fr))  # within one float32 ulp of the answer
+    cands = {np.nextafter(x, np.float32(-np.inf)), x, np.nextafter(x, np.float32(np.inf))}
+    best = None
+    for c in sorted(cands, key=float):
+        d = abs(Fraction(float(c)) - fr)
+        if best is None or d < best[0] or (d == best[0] and (int(np.float32(c).view(np.uint32)) & 1) == 0):
+            best = (d, c)
+    return Fraction(float(best[1]))
+
+
+def _round_half_even(fr: Fraction) -> int:
+    f = fr.numerator // fr.denominator
+    rem = fr - f
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and f % 2 == 1):
+        return f + 1
+    return f
+
+
+def _h(values):
+    return np.asarray(values, dtype=np.float16)
+
+
+def test_quantize_matches_exact_rational_arithmetic():
+    """Every code equals clamp(round_half_even(f32(w / s)) + 8), computed with exact
+    rationals and an independent float32 rounding (pins the division precision,
+    the rounding, the offset and the clamp)."""
+    rng = np.random.default_rng(31)
+    K, N, G = 256, 16, 128
+    s = _h(rng.uniform(0.002, 0.05, (K // G, N)) * rng.choice([-1, 1], (K // G, N)))
+    w = _h(rng.normal(0, 0.15, (K, N)))
+    q = oracle.quantize(w, s, G)
+    for k in range(K):
+        for n in range(N):
+            fr = Fraction(float(w[k, n])) / Fraction(float(s[k // G, n]))
+            want = min(max(_round_half_even(_f32_round_exact(fr)) + 8, 0), 15)
+            assert q[k, n] == want, (k, n, float(w[k, n]), float(s[k // G, n]))
+
+
+@pytest.mark.parametrize("G", [128, -1])
+def test_quantize_inverts_dequantisation(G):
+    """quantise(RNE(s (q - 8)), s) == q for every code, positive and negative scales."""
+    rng = np.random.default_rng(32)
+    K, N = 256, 64
+    NG = 2 if G == 128 else 1
+    q = np.tile(np.arange(16, dtype=np.uint8), K * N // 16).reshape(K, N)
+    rng.shuffle(q.ravel())
+    s = _h(rng.uniform(0.001, 3.0, (NG, N)) * rng.choice([-1, 1], (NG, N)))
+    w = oracle.dequant_fp16_bits(q, s, G).view(np.float16)
+    assert np.array_equal(oracle.quantize(w, s, G), q)
+
+
+def test_quantize_ties_round_to_even_and_clamp():
+    w = _h([[0.5, 1.5, 2.5, 3.5, -0.5, -1.5, -2.5, -3.5, 7.5, -8.5, 8.0, -9.0, 7.0, -8.0, 1000.0, -1000.0]])
+    s = _h(np.ones((1, 16)))
+    want = [8, 10, 10, 12, 8, 6, 6, 4, 15, 0, 15, 0, 15, 0, 15, 0]
+    assert oracle.quantize(w, s, 1).ravel().tolist() == want
+    # the same ties with a scale of 0.25 and the weights scaled by it (all exact)
+    assert oracle.quantize(_h(w.astype(np.float64) * 0.25), _h(np.full((1, 16), 0.25)), 1).ravel().tolist() == want
+
+
+def test_quantize_rejects_non_finite_quotients():
+    w = _h(np.ones((128, 1)))
+    with pytest.raises(ValueError):
+        oracle.quantize(w, _h(np.zeros((1, 1))), 128)
+    with pytest.raises(ValueError):
+        oracle.quantize(_h(np.full((128, 1), np.inf)), _h(np.ones((1, 1))), 128)
