@@ -90,6 +90,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--only-m", type=int, default=None, help="run only this M of the sweep (profiling)")
     ap.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS FP16 GEMM on the dequantised weights")
+    ap.add_argument("--no-offline", action="store_true", help="skip timing the offline repack / quantise steps")
     ap.add_argument("--cpu-sample", default=None, help=argparse.SUPPRESS)  # internal: oracle timing child
     return ap.parse_args()
 
@@ -267,6 +268,8 @@ def run_ours(args, rank, world, device):
     peaks = load_peaks()
     stream = torch.cuda.current_stream()
 
+    offline = None
+    peaks_for_offline = load_peaks()
     # ---- inputs: seeded synthetic weights -> device repack; activations resident in HBM
     points = []  # (K, N, G, M, [packed copies], sp copies, A_d, C_d)
     max_ws = 0
@@ -278,6 +281,8 @@ def run_ours(args, rank, world, device):
         lbytes = K * N // 2
         copies = max(1, math.ceil(3 * L2_BYTES / lbytes)) if lbytes < 2 * L2_BYTES else 1
         packs = [w.repack(q_d, s_d, G) for _ in range(copies)]
+        if li == 0 and rank == 0 and not args.no_offline:
+            offline = time_offline_steps(w, torch, q_d, s_d, K, N, G, seed, peaks_for_offline)
         del q_d, s_d
         for M in Ms:
             A = synth.make_activations(M, K, seed * 1000 + M)
@@ -493,8 +498,44 @@ def run_ours(args, rank, world, device):
                    "parallelism": f"replicas x{world}", "peaks": peaks["source"]},
         "sweep": sweep, "roofline": roofline, "roofline_by_kernel": roofline_by_kernel,
         "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+        "gpu_launches": launches_per_step * args.steps, "clocks": clocks, "offline": offline,
     }
+
+
+def time_offline_steps(w, torch, q_d, s_d, K, N, G, seed, peaks):
+    """Device time of the offline steps on the first layer of the workload (outside the
+    timed region): w4a16_repack (codes uint8 in, packed + permuted scales out) and
+    w4a16_quantize_repack (FP16 weights in), against the HBM roofline of their bytes."""
+    from mixed_precision_w4a16_gb300 import synth
+    wt, s16 = synth.make_fp16_weights(K, N, G, seed)
+    w_d = torch.from_numpy(wt).to(q_d.device)
+    s2_d = torch.from_numpy(s16).to(q_d.device)
+    del wt
+    NG = K // synth.effective_group(K, G)
+    out = {}
+    for name, fn, in_bytes in (
+            ("repack", lambda: w.repack(q_d, s_d, G), K * N + 2 * NG * N),
+            ("quantize_repack", lambda: w.quantize_repack(w_d, s2_d, G), 2 * K * N + 2 * NG * N)):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        reps = 5
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / reps * 1e3
+        nbytes = in_bytes + K * N // 2 + 2 * NG * N  # inputs read once + packed stream and scales written once
+        out[name] = {"us": round(us, 1), "bytes": nbytes, "gb_s": round(nbytes / (us * 1e-6) / 1e9, 1),
+                     "roofline_frac": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 3),
+                     "shape": f"K={K} N={N} G={G}"}
+    if w.w4a16_get_status() != 0:
+        raise RuntimeError("device status error in the offline steps")
+    del w_d, s2_d
+    return out
 
 
 def reduce_max(x, world, device):
