@@ -58,9 +58,13 @@ WORKLOADS = {
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+ZERO_POINTS = False  # set from --zero-points: the GEMM also reads a zero code per scale and a bias per column
+
+
 def gemm_bytes(M, K, N, G):
     G = K if G in (-1, K) else G
-    return 2 * M * K + K * N // 2 + 2 * (K // G) * N + 2 * M * N
+    extra = (K // G) * N + 2 * N if ZERO_POINTS else 0
+    return 2 * M * K + K * N // 2 + 2 * (K // G) * N + 2 * M * N + extra
 
 
 def gemm_flops(M, K, N):
@@ -91,6 +95,8 @@ def parse_args():
     ap.add_argument("--only-m", type=int, default=None, help="run only this M of the sweep (profiling)")
     ap.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS FP16 GEMM on the dequantised weights")
     ap.add_argument("--no-offline", action="store_true", help="skip timing the offline repack / quantise steps")
+    ap.add_argument("--zero-points", action="store_true",
+                    help="run every GEMM with a zero point per group and a bias (w4a16_gemm_zp)")
     ap.add_argument("--cpu-sample", default=None, help=argparse.SUPPRESS)  # internal: oracle timing child
     return ap.parse_args()
 
@@ -259,6 +265,8 @@ def run_ours(args, rank, world, device):
 
     build.build()
     desc, layers, seed = WORKLOADS[args.workload]
+    global ZERO_POINTS
+    ZERO_POINTS = bool(args.zero_points)
     if args.only_m is not None:
         layers = [(K, N, G, [M for M in Ms if M == args.only_m]) for K, N, G, Ms in layers]
         layers = [l for l in layers if l[3]]
@@ -281,6 +289,12 @@ def run_ours(args, rank, world, device):
         lbytes = K * N // 2
         copies = max(1, math.ceil(3 * L2_BYTES / lbytes)) if lbytes < 2 * L2_BYTES else 1
         packs = [w.repack(q_d, s_d, G) for _ in range(copies)]
+        zp_d = bias_d = None
+        if args.zero_points:
+            rng_z = np.random.default_rng(seed * 100 + li + 7)
+            NG = q_d.shape[0] // synth.effective_group(K, G)
+            zp_d = w.repack_zeros(torch.from_numpy(rng_z.integers(0, 16, (NG, N)).astype(np.uint8)).to(device), K, G)
+            bias_d = torch.from_numpy(rng_z.normal(0, 1.0, N).astype(np.float16)).to(device)
         if li == 0 and rank == 0 and not args.no_offline:
             offline = time_offline_steps(w, torch, q_d, s_d, K, N, G, seed, peaks_for_offline)
         del q_d, s_d
@@ -288,7 +302,8 @@ def run_ours(args, rank, world, device):
             A = synth.make_activations(M, K, seed * 1000 + M)
             A_d = torch.from_numpy(A).to(device)
             C_d = torch.empty((M, N), dtype=torch.float16, device=device)
-            points.append({"K": K, "N": N, "G": G, "M": M, "packs": packs, "A": A, "A_d": A_d, "C_d": C_d})
+            points.append({"K": K, "N": N, "G": G, "M": M, "packs": packs, "A": A, "A_d": A_d, "C_d": C_d,
+                           "zp": zp_d, "bias": bias_d})
             max_ws = max(max_ws, w.w4a16_workspace_bytes(M, K, N, G))
     ws = torch.zeros(max_ws, dtype=torch.uint8, device=device)
     torch.cuda.synchronize()
@@ -299,12 +314,19 @@ def run_ours(args, rank, world, device):
         p["kernel"] = KERNEL_OF_PATH[plan["path"]]
         launches_per_step += p["launches"]
 
+    def gemm_call(p, packed, sp):
+        if args.zero_points:
+            w.w4a16_gemm_zp(p["A_d"], packed, sp, p["zp"], p["bias"], p["C_d"], p["M"], p["K"], p["N"], p["G"], ws,
+                            max_ws, stream)
+        else:
+            w.w4a16_gemm(p["A_d"], packed, sp, p["C_d"], p["M"], p["K"], p["N"], p["G"], ws, max_ws, stream)
+
     def one_step(it, evs=None):
         for i, p in enumerate(points):
             packed, sp = p["packs"][it % len(p["packs"])]
             if evs is not None:
                 evs[i][0].record(stream)
-            w.w4a16_gemm(p["A_d"], packed, sp, p["C_d"], p["M"], p["K"], p["N"], p["G"], ws, max_ws, stream)
+            gemm_call(p, packed, sp)
             if evs is not None:
                 evs[i][1].record(stream)
 
@@ -363,7 +385,7 @@ def run_ours(args, rank, world, device):
             for i, p in enumerate(points):
                 p["A_d"].copy_(hostA[i], non_blocking=True)
                 packed, sp = p["packs"][it % len(p["packs"])]
-                w.w4a16_gemm(p["A_d"], packed, sp, p["C_d"], p["M"], p["K"], p["N"], p["G"], ws, max_ws, stream)
+                gemm_call(p, packed, sp)
                 hostC[i].copy_(p["C_d"], non_blocking=True)
         torch.cuda.synchronize()
         if world > 1:
@@ -375,7 +397,7 @@ def run_ours(args, rank, world, device):
             for i, p in enumerate(points):
                 p["A_d"].copy_(hostA[i], non_blocking=True)
                 packed, sp = p["packs"][it % len(p["packs"])]
-                w.w4a16_gemm(p["A_d"], packed, sp, p["C_d"], p["M"], p["K"], p["N"], p["G"], ws, max_ws, stream)
+                gemm_call(p, packed, sp)
                 hostC[i].copy_(p["C_d"], non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
@@ -495,7 +517,8 @@ def run_ours(args, rank, world, device):
         "config": {"workload": desc, "gemms_per_step": len(points),
                    "l2": "inputs larger than L2" if all(len(p["packs"]) == 1 for p in points)
                    else "weight copies rotated to exceed 3x L2",
-                   "parallelism": f"replicas x{world}", "peaks": peaks["source"]},
+                   "parallelism": f"replicas x{world}", "peaks": peaks["source"],
+                   "variant": "zero point per group + bias" if args.zero_points else "symmetric (z = 8)"},
         "sweep": sweep, "roofline": roofline, "roofline_by_kernel": roofline_by_kernel,
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "clocks": clocks, "offline": offline,

@@ -154,13 +154,48 @@ W4A16_API int w4a16_dequant(const uint32_t* packed, const uint16_t* scales_p, in
  *   workspace device, >= w4a16_workspace_bytes(M, K, N, groupsize) bytes,
  *             zeroed by the caller before first use (see above)
  *
- * Accumulation is FP32; each group's partial product is scaled by its FP32
- * scale, and split-K partials are summed in a fixed order, so repeated calls
- * give bitwise-identical C.  M == 0 returns W4A16_OK without a launch.
+ * Accumulation is FP32.  Up to 16 token rows, each group's partial product is
+ * scaled by its FP32 scale; from 17 rows on, the weights are dequantised to
+ * FP16 (RNE(s * (q - 8)), the value w4a16_dequant returns) before the
+ * tensor-core multiply.  Split-K partials are summed in a fixed order, so
+ * repeated calls give bitwise-identical C.  M == 0 returns W4A16_OK without a
+ * launch.
  * ------------------------------------------------------------------------- */
 W4A16_API int w4a16_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* scales_p, uint16_t* C,
                int M, int K, int N, int groupsize, void* workspace, size_t workspace_bytes,
                void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Zero points and bias (the affine form of the deep-dive article, section
+ * "Marlin 要解决的精确问题": B^[k, n] = s[g, n] * (q[k, n] - z[g, n]); the
+ * production variant with a zero point per group and a bias, section
+ * "Marlin 已从一个 Kernel 变成一族实现").
+ *
+ * w4a16_repack_zeros: zero codes z uint8[K/G][N] row-major (values 0..15, one
+ * per byte, G as for the scales) -> zeros_p uint8[(K/G)*N] in the permuted
+ * order of the scales (z[g][n] at the index w4a16_repack gives s[g][n]).
+ * Codes above 15 are masked to 4 bits and flag W4A16_ERR_CODE_RANGE for
+ * w4a16_get_status(NULL, stream).
+ *
+ * w4a16_gemm_zp: w4a16_gemm with optional zero points and bias:
+ *   C[m][n] = RNE( sum_k A[m][k] * s[k/G][n] * (q[k][n] - z[k/G][n]) + bias[n] )
+ * accumulated in FP32.  zeros_p = NULL means z = 8 (the symmetric codes of
+ * w4a16_gemm); bias (fp16[N]) = NULL means no bias.  Same operands, workspace
+ * (w4a16_workspace_bytes covers both forms), determinism and errors as
+ * w4a16_gemm; zeros_p and bias, when given, are 16-byte aligned device
+ * pointers.
+ *
+ * w4a16_dequant_zp: Bhat[k][n] = RNE(s[k/G][n] * (q[k][n] - z[k/G][n]))
+ * (diagnostic, like w4a16_dequant).
+ * ------------------------------------------------------------------------- */
+W4A16_API int w4a16_repack_zeros(const uint8_t* z, int K, int N, int groupsize, uint8_t* zeros_p, void* stream);
+
+W4A16_API int w4a16_gemm_zp(const uint16_t* A, const uint32_t* packed, const uint16_t* scales_p,
+                            const uint8_t* zeros_p, const uint16_t* bias, uint16_t* C, int M, int K, int N,
+                            int groupsize, void* workspace, size_t workspace_bytes, void* stream);
+
+W4A16_API int w4a16_dequant_zp(const uint32_t* packed, const uint16_t* scales_p, const uint8_t* zeros_p, int K,
+                               int N, int groupsize, uint16_t* Bhat, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Allocation-free GEMM.  The paper has no counterpart: this entry point is a

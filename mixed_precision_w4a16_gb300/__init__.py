@@ -17,10 +17,11 @@ __all__ = [
     "W4A16Error", "lib", "Plan",
     "w4a16_packed_bytes", "w4a16_scales_count", "w4a16_workspace_bytes", "w4a16_plan",
     "w4a16_repack", "w4a16_quantize_repack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm", "w4a16_gemm_noalloc",
-    "w4a16_get_status",
+    "w4a16_get_status", "w4a16_repack_zeros", "w4a16_gemm_zp", "w4a16_dequant_zp",
     "w4a16_debug_set_wait_cycles", "w4a16_debug_inject_stall", "w4a16_debug_force_path", "w4a16_status_string",
     "EXPORTED_SYMBOLS",
-    "repack", "quantize_repack", "unpack", "dequant", "gemm", "workspace_for",
+    "repack", "quantize_repack", "unpack", "dequant", "gemm", "workspace_for", "repack_zeros", "gemm_zp",
+    "dequant_zp",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -30,7 +31,8 @@ EXPORTED_SYMBOLS = (
     "w4a16_status_string", "w4a16_abi_version", "w4a16_packed_bytes", "w4a16_scales_count",
     "w4a16_workspace_bytes", "w4a16_repack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm",
     "w4a16_get_status", "w4a16_plan", "w4a16_debug_set_wait_cycles", "w4a16_debug_inject_stall",
-    "w4a16_gemm_noalloc", "w4a16_debug_force_path", "w4a16_quantize_repack",
+    "w4a16_gemm_noalloc", "w4a16_debug_force_path", "w4a16_quantize_repack", "w4a16_repack_zeros",
+    "w4a16_gemm_zp", "w4a16_dequant_zp",
 )
 
 
@@ -73,6 +75,9 @@ def _load():
         "w4a16_gemm_noalloc": (i, [vp, vp, vp, vp, i, i, i, i, vp]),
         "w4a16_debug_force_path": (None, [i]),
         "w4a16_quantize_repack": (i, [vp, vp, i, i, i, vp, vp, vp]),
+        "w4a16_repack_zeros": (i, [vp, i, i, i, vp, vp]),
+        "w4a16_gemm_zp": (i, [vp, vp, vp, vp, vp, vp, i, i, i, i, vp, sz, vp]),
+        "w4a16_dequant_zp": (i, [vp, vp, vp, i, i, i, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -182,6 +187,23 @@ def w4a16_gemm(A, packed, scales_p, C, M, K, N, groupsize, workspace, workspace_
                           int(workspace_bytes), _stream(stream)), "w4a16_gemm")
 
 
+def w4a16_repack_zeros(z, K, N, groupsize, zeros_p, stream=None):
+    _check(_lib().w4a16_repack_zeros(_ptr(z), K, N, groupsize, _ptr(zeros_p), _stream(stream)), "w4a16_repack_zeros")
+
+
+def w4a16_gemm_zp(A, packed, scales_p, zeros_p, bias, C, M, K, N, groupsize, workspace, workspace_bytes=None,
+                  stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib().w4a16_gemm_zp(_ptr(A), _ptr(packed), _ptr(scales_p), _ptr(zeros_p), _ptr(bias), _ptr(C), M, K, N,
+                                groupsize, _ptr(workspace), int(workspace_bytes), _stream(stream)), "w4a16_gemm_zp")
+
+
+def w4a16_dequant_zp(packed, scales_p, zeros_p, K, N, groupsize, bhat, stream=None):
+    _check(_lib().w4a16_dequant_zp(_ptr(packed), _ptr(scales_p), _ptr(zeros_p), K, N, groupsize, _ptr(bhat),
+                                   _stream(stream)), "w4a16_dequant_zp")
+
+
 def w4a16_gemm_noalloc(A, packed, scales_p, C, M, K, N, groupsize, stream=None):
     """The allocation-free GEMM: same operands as w4a16_gemm, no workspace (the library's
     own scratch array is used; calls must not overlap on the GPU)."""
@@ -257,6 +279,33 @@ def dequant(packed, scales_p, K: int, N: int, groupsize: int, stream=None):
     bhat = torch.empty((K, N), dtype=torch.float16, device=packed.device)
     w4a16_dequant(packed, scales_p, K, N, groupsize, bhat, stream)
     return bhat
+
+
+def repack_zeros(z, K: int, groupsize: int, stream=None):
+    """z uint8[K/G][N] zero codes (CUDA tensor) -> zeros_p uint8[(K/G)*N], permuted like the scales."""
+    import torch
+    N = z.shape[1]
+    zp = torch.empty(z.numel(), dtype=torch.uint8, device=z.device)
+    w4a16_repack_zeros(z, K, N, groupsize, zp, stream)
+    return zp
+
+
+def dequant_zp(packed, scales_p, zeros_p, K: int, N: int, groupsize: int, stream=None):
+    import torch
+    bhat = torch.empty((K, N), dtype=torch.float16, device=packed.device)
+    w4a16_dequant_zp(packed, scales_p, zeros_p, K, N, groupsize, bhat, stream)
+    return bhat
+
+
+def gemm_zp(A, packed, scales_p, zeros_p, bias, N: int, groupsize: int, workspace=None, out=None, stream=None):
+    """C fp16[M][N] = A * (s (q - z)) + bias; zeros_p / bias may be None."""
+    import torch
+    M, K = A.shape
+    if workspace is None:
+        workspace = workspace_for(M, K, N, groupsize, A.device)
+    C = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=A.device)
+    w4a16_gemm_zp(A, packed, scales_p, zeros_p, bias, C, M, K, N, groupsize, workspace, None, stream)
+    return C
 
 
 def gemm(A, packed, scales_p, N: int, groupsize: int, workspace=None, out=None, stream=None):

@@ -90,7 +90,7 @@ void finish_split(Plan& pl, int K, int sms, size_t slot_floats) {
   pl.workspace = kStatusBytes + counters + 2ull * pl.grid * slot_floats * sizeof(float);
 }
 
-Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin) {
+Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin, bool zp) {
   Plan pl{};
   pl.path = 1;
   const int mc = std::min(std::max(M, 1), 32);
@@ -107,7 +107,7 @@ Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin) {
     const int kq = cands[c];
     if (K % (64 * kq) != 0) continue;
     const int srows = (G <= 64 * kq) ? (64 * kq) / G : 1;
-    const MmaLayout l0 = mma_layout(mt, kq, srows, 0);
+    const MmaLayout l0 = mma_layout(mt, kq, srows, 0, zp);
     const int stages = (smem_optin - l0.smem_bytes) / (l0.stage_bytes + 16);
     if (stages < 3 && kq != 2) continue;
     const long long units = static_cast<long long>(pl.strips) * (K / (64 * kq));
@@ -122,10 +122,10 @@ Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin) {
   const int kq = best_kq;
   const int KT = 64 * kq;
   pl.srows = (G <= KT) ? KT / G : 1;
-  const MmaLayout l0 = mma_layout(mt, kq, pl.srows, 0);
+  const MmaLayout l0 = mma_layout(mt, kq, pl.srows, 0, zp);
   int stages = (smem_optin - l0.smem_bytes) / (l0.stage_bytes + 16);
   stages = std::max(2, std::min(stages, 8));
-  pl.lay = mma_layout(mt, kq, pl.srows, stages);
+  pl.lay = mma_layout(mt, kq, pl.srows, stages, zp);
   pl.cfg.m_tiles = mt;
   pl.cfg.kq = kq;
   pl.cfg.stages = stages;
@@ -140,7 +140,7 @@ Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin) {
   return pl;
 }
 
-Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin) {
+Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin, bool zp) {
   Plan pl{};
   pl.path = 2;
   pl.mb = std::min(128, (std::max(M, 1) + 15) / 16 * 16);
@@ -162,7 +162,7 @@ Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin) {
     const int ch = cands[c];
     if (K % (128 * ch) != 0) continue;
     const int srows = (G == 128) ? ch : 1;
-    const TcLayout l0 = tc_layout(pl.mb, ch, srows, pl.na, 0);
+    const TcLayout l0 = tc_layout(pl.mb, ch, srows, pl.na, 0, zp);
     const int w_st = std::min(12, (smem_optin - l0.smem_bytes) / (l0.w_stage_bytes + 16));
     if (w_st < 2 || w_st * ch < 8) continue;
     const long long units = static_cast<long long>(pl.strips) * (K / (128 * ch));
@@ -176,12 +176,12 @@ Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin) {
   }
   if (!best) {
     best = 1;
-    const TcLayout l0 = tc_layout(pl.mb, 1, 1, pl.na, 0);
+    const TcLayout l0 = tc_layout(pl.mb, 1, 1, pl.na, 0, zp);
     best_w = std::max(2, std::min(12, (smem_optin - l0.smem_bytes) / (l0.w_stage_bytes + 16)));
   }
   pl.ch = best;
   pl.srows = (G == 128) ? pl.ch : 1;
-  pl.tlay = tc_layout(pl.mb, pl.ch, pl.srows, pl.na, best_w);
+  pl.tlay = tc_layout(pl.mb, pl.ch, pl.srows, pl.na, best_w, zp);
   pl.a_stages = pl.na;
   pl.w_stages = best_w;
   pl.m_chunk = pl.mb;
@@ -195,10 +195,11 @@ Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin) {
 
 std::atomic<int> g_force_path{0};
 
-Plan make_plan(int M, int K, int N, int G, int sms, int smem_optin) {
+// zp: the GEMM reads zero points (their rows take shared-memory stage space next to the scales)
+Plan make_plan(int M, int K, int N, int G, int sms, int smem_optin, bool zp = false) {
   const int forced = g_force_path.load();
   const bool tc = forced == 2 || (forced == 0 && M >= kTcMinRows);
-  return tc ? make_plan_tc(M, K, N, G, sms, smem_optin) : make_plan_mma(M, K, N, G, sms, smem_optin);
+  return tc ? make_plan_tc(M, K, N, G, sms, smem_optin, zp) : make_plan_mma(M, K, N, G, sms, smem_optin, zp);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
@@ -296,7 +297,10 @@ size_t w4a16_workspace_bytes(int M, int K, int N, int groupsize) {
   if (M < 0 || check_shape(K, N, groupsize) != W4A16_OK) return 0;
   DeviceInfo* d = nullptr;
   if (current_device_info(&d) != W4A16_OK) return 0;
-  return make_plan(M, K, N, effective_group(K, groupsize), d->sms, d->smem_optin).workspace;
+  // enough for the GEMM with and without zero points
+  const int G = effective_group(K, groupsize);
+  return std::max(make_plan(M, K, N, G, d->sms, d->smem_optin, false).workspace,
+                  make_plan(M, K, N, G, d->sms, d->smem_optin, true).workspace);
 }
 
 void w4a16_debug_set_wait_cycles(long long cycles) { g_wait_cycles.store(cycles > 0 ? cycles : 0); }
@@ -356,26 +360,33 @@ int w4a16_dequant(const uint32_t* packed, const uint16_t* scales_p, int K, int N
   DeviceInfo* d = nullptr;
   const int r = current_device_info(&d);
   if (r != W4A16_OK) return r;
-  const cudaError_t e = launch_dequant(packed, scales_p, K, N, effective_group(K, groupsize), Bhat,
+  const cudaError_t e = launch_dequant(packed, scales_p, nullptr, K, N, effective_group(K, groupsize), Bhat,
                                        static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
 }
 
-int w4a16_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* scales_p, uint16_t* C, int M, int K, int N,
-               int groupsize, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The GEMM behind w4a16_gemm and w4a16_gemm_zp (zeros_p and bias may be null).
+int gemm_impl(const uint16_t* A, const uint32_t* packed, const uint16_t* scales_p, const uint8_t* zeros_p,
+              const uint16_t* bias, uint16_t* C, int M, int K, int N, int groupsize, void* workspace,
+              size_t workspace_bytes, void* stream) {
   if (M < 0) return W4A16_ERR_SHAPE;
   const int st = check_shape(K, N, groupsize);
   if (st != W4A16_OK) return st;
   if (M == 0) return W4A16_OK;
   if (!A || !packed || !scales_p || !C) return W4A16_ERR_NULL;
   if (!workspace) return W4A16_ERR_WORKSPACE;
-  if (!aligned16(A) || !aligned16(packed) || !aligned16(scales_p) || !aligned16(C) || !aligned16(workspace))
+  if (!aligned16(A) || !aligned16(packed) || !aligned16(scales_p) || !aligned16(C) || !aligned16(workspace) ||
+      (zeros_p && !aligned16(zeros_p)) || (bias && !aligned16(bias)))
     return W4A16_ERR_ALIGN;
   DeviceInfo* d = nullptr;
   const int r = current_device_info(&d);
   if (r != W4A16_OK) return r;
   const int G = effective_group(K, groupsize);
-  const Plan pl = make_plan(M, K, N, G, d->sms, d->smem_optin);
+  const Plan pl = make_plan(M, K, N, G, d->sms, d->smem_optin, zeros_p != nullptr);
   if (workspace_bytes < pl.workspace) return W4A16_ERR_WORKSPACE;
 
   const long long wc = g_wait_cycles.load();
@@ -395,6 +406,8 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* scales
     TcParams p{};
     p.packed = packed;
     p.scales = scales_p;
+    p.zeros = zeros_p;
+    p.bias = bias;
     p.C = C;
     p.status = status;
     p.counters = counters;
@@ -417,6 +430,7 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* scales
     p.a_stage_bytes = pl.tlay.a_stage_bytes;
     p.w_stage_bytes = pl.tlay.w_stage_bytes;
     p.w_base = pl.tlay.w_base;
+    p.z_off = pl.tlay.z_off;
     p.bar_off = pl.tlay.bar_off;
     p.flag_off = pl.tlay.flag_off;
     p.idesc = tc_idesc(128, pl.mb);
@@ -433,6 +447,8 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* scales
   GemmParams p{};
   p.packed = packed;
   p.scales = scales_p;
+  p.zeros = zeros_p;
+  p.bias = bias;
   p.C = C;
   p.status = status;
   p.counters = counters;
@@ -450,6 +466,7 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* scales
   p.stages = pl.cfg.stages;
   p.w_off = pl.lay.w_off;
   p.s_off = pl.lay.s_off;
+  p.z_off = pl.lay.z_off;
   p.stage_bytes = pl.lay.stage_bytes;
   p.tx_bytes = pl.lay.tx_bytes;
   p.red_off = pl.lay.red_off;
@@ -463,6 +480,48 @@ int w4a16_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* scales
     if (e != cudaSuccess) return W4A16_ERR_CUDA;
   }
   return W4A16_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int w4a16_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* scales_p, uint16_t* C, int M, int K, int N,
+               int groupsize, void* workspace, size_t workspace_bytes, void* stream) {
+  return gemm_impl(A, packed, scales_p, nullptr, nullptr, C, M, K, N, groupsize, workspace, workspace_bytes, stream);
+}
+
+int w4a16_gemm_zp(const uint16_t* A, const uint32_t* packed, const uint16_t* scales_p, const uint8_t* zeros_p,
+                  const uint16_t* bias, uint16_t* C, int M, int K, int N, int groupsize, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  return gemm_impl(A, packed, scales_p, zeros_p, bias, C, M, K, N, groupsize, workspace, workspace_bytes, stream);
+}
+
+int w4a16_repack_zeros(const uint8_t* z, int K, int N, int groupsize, uint8_t* zeros_p, void* stream) {
+  const int st = check_shape(K, N, groupsize);
+  if (st != W4A16_OK) return st;
+  if (!z || !zeros_p) return W4A16_ERR_NULL;
+  if (!aligned16(z) || !aligned16(zeros_p)) return W4A16_ERR_ALIGN;
+  DeviceInfo* d = nullptr;
+  const int r = current_device_info(&d);
+  if (r != W4A16_OK) return r;
+  const cudaError_t e =
+      launch_repack_zeros(z, K, N, effective_group(K, groupsize), zeros_p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
+int w4a16_dequant_zp(const uint32_t* packed, const uint16_t* scales_p, const uint8_t* zeros_p, int K, int N,
+                     int groupsize, uint16_t* Bhat, void* stream) {
+  const int st = check_shape(K, N, groupsize);
+  if (st != W4A16_OK) return st;
+  if (!packed || !scales_p || !zeros_p || !Bhat) return W4A16_ERR_NULL;
+  if (!aligned16(packed) || !aligned16(scales_p) || !aligned16(zeros_p) || !aligned16(Bhat)) return W4A16_ERR_ALIGN;
+  DeviceInfo* d = nullptr;
+  const int r = current_device_info(&d);
+  if (r != W4A16_OK) return r;
+  const cudaError_t e = launch_dequant(packed, scales_p, zeros_p, K, N, effective_group(K, groupsize), Bhat,
+                                       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -224,4 +224,22 @@ __device__ __forceinline__ void decode8(uint32_t w, uint32_t a[4]) {
   a[3] = hfma2_u32(lop3_and_or(w8, kHi, kBase), kSixteenth, kMinus72);
 }
 
+// The decode with a zero point z per row instead of the constant 8 (the affine
+// form B^ = s (q - z) of the deep-dive article, section "Marlin 要解决的精确问题").
+// Rows g (registers 0, 2) are always low nibbles, rows g + 8 (registers 1, 3)
+// always high nibbles, so each needs one constant: c_lo = 1024 + z_g in both
+// halves (0x6400 | z), c_hi = -(64 + z_{g+8}) in both halves (0xD400 | z << 4).
+// (1024 + q) - (1024 + z) and (1024 + 16q) / 16 - (64 + z) are exact in FP16.
+__device__ __forceinline__ uint32_t zp_const_lo(uint32_t z) { return (0x6400u | z) * 0x10001u; }
+__device__ __forceinline__ uint32_t zp_const_hi(uint32_t z) { return (0xD400u | (z << 4)) * 0x10001u; }
+__device__ __forceinline__ void decode8_zp(uint32_t w, uint32_t c_lo, uint32_t c_hi, uint32_t a[4]) {
+  constexpr uint32_t kLo = 0x000f000fu, kHi = 0x00f000f0u, kBase = 0x64006400u;
+  constexpr uint32_t kSixteenth = 0x2c002c00u;  // 1/16
+  const uint32_t w8 = w >> 8;
+  a[0] = hsub2_u32(lop3_and_or(w, kLo, kBase), c_lo);
+  a[1] = hfma2_u32(lop3_and_or(w, kHi, kBase), kSixteenth, c_hi);
+  a[2] = hsub2_u32(lop3_and_or(w8, kLo, kBase), c_lo);
+  a[3] = hfma2_u32(lop3_and_or(w8, kHi, kBase), kSixteenth, c_hi);
+}
+
 }  // namespace w4a16

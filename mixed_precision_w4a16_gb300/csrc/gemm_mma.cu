@@ -57,7 +57,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-template <int MT>
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// ZP: codes carry a zero point per group and column (p.zeros), else the constant 8.
+template <int MT, bool ZP>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     gemm_mma_kernel(const __grid_constant__ CUtensorMap tmA, const GemmParams p) {
   constexpr int MB = 8 * MT;
@@ -133,6 +140,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           const int grp0 = (p.G == 128) ? kt * p.srows : 0;  // G is 128 or K (K >= KT)
           const uint16_t* ssrc = p.scales + (static_cast<long long>(j) * NG + grp0) * 128;
           bulk_g2s(st + p.s_off, ssrc, static_cast<uint32_t>(p.srows) * 256u, fb, pol_a);
+          if (ZP)  // the zero codes of the same scale rows, permuted the same way
+            bulk_g2s(st + p.z_off, p.zeros + (static_cast<long long>(j) * NG + grp0) * 128,
+                     static_cast<uint32_t>(p.srows) * 128u, fb, pol_a);
         }
         __syncwarp();
         issued = it + 1;
@@ -211,20 +221,27 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         const int srow = (p.G == 128) ? (kq >> 1) : 0;
         uint4 wv[kNbw];
         uint32_t spv[kNbw];
+        uint32_t zpv[kNbw];
 #pragma unroll
         for (int i = 0; i < kNbw; ++i) {
           const int nb = ng * kNbw + i;
           wv[i] = lds128(st + p.w_off + (kq * 8 + nb) * 512 + lane * 16);
           spv[i] = lds32(st + p.s_off + (srow * 128 + nb * 16 + 2 * g) * 2);
+          zpv[i] = ZP ? lds_u16(st + p.z_off + srow * 128 + nb * 16 + 2 * g) : 0u;  // (z of row g, z of row g + 8)
         }
 #pragma unroll
         for (int i = 0; i < kNbw; ++i) {
           const uint32_t words[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+          const uint32_t c_lo = ZP ? zp_const_lo(zpv[i] & 15u) : 0u;
+          const uint32_t c_hi = ZP ? zp_const_hi((zpv[i] >> 8) & 15u) : 0u;
           float tmp[MT][4];
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
             uint32_t a[4];
-            decode8(words[jj], a);
+            if (ZP)
+              decode8_zp(words[jj], c_lo, c_hi, a);
+            else
+              decode8(words[jj], a);
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
               mma_16816(tmp[mt], a, bf[jj][mt][0], bf[jj][mt][1], jj == 0 ? zero4 : tmp[mt]);
@@ -333,7 +350,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             for (int e = 0; e < 4; ++e) {
               const int token = p.m0 + mt * 8 + 2 * t + (e & 1);
               const int n = n_base + 8 * (e >> 1);
-              if (token < p.M) p.C[static_cast<long long>(token) * p.N + n] = f32_to_f16_bits(acc[i][mt][e]);
+              float c = acc[i][mt][e];
+              if (p.bias) c += __half2float(__ushort_as_half(p.bias[n]));
+              if (token < p.M) p.C[static_cast<long long>(token) * p.N + n] = f32_to_f16_bits(c);
             }
         }
       }
@@ -349,9 +368,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   named_bar_sync(3, kMmaThreads);
 }
 
-template <int MT>
+template <int MT, bool ZP>
 cudaError_t launch_one(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream) {
-  auto kern = gemm_mma_kernel<MT>;
+  auto kern = gemm_mma_kernel<MT, ZP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem_bytes);
   if (e != cudaSuccess) return e;
   kern<<<p.grid, kMmaThreads, cfg.smem_bytes, stream>>>(tmA, p);
@@ -360,13 +379,15 @@ cudaError_t launch_one(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmP
 
 }  // namespace
 
-MmaLayout mma_layout(int m_tiles, int kq, int srows, int stages) {
+MmaLayout mma_layout(int m_tiles, int kq, int srows, int stages, bool zp) {
   MmaLayout l{};
   const int MB = 8 * m_tiles;
   l.w_off = kq * MB * 128;        // activation pieces first (each a multiple of 1024 bytes)
   l.s_off = l.w_off + kq * 4096;  // then the weight chunk, then the scale rows
-  l.stage_bytes = (l.s_off + srows * 256 + 1023) / 1024 * 1024;
-  l.tx_bytes = kq * MB * 128 + kq * 4096 + srows * 256;
+  l.z_off = l.s_off + srows * 256;  // then, with zero points, their rows (128 bytes each)
+  const int zbytes = zp ? srows * 128 : 0;
+  l.stage_bytes = (l.z_off + zbytes + 1023) / 1024 * 1024;
+  l.tx_bytes = kq * MB * 128 + kq * 4096 + srows * 256 + zbytes;
   l.red_off = stages * l.stage_bytes;
   l.bar_off = l.red_off + 3 * 2 * kNbw * m_tiles * 4 * 32 * 4;
   l.flag_off = l.bar_off + 16 * stages;
@@ -375,10 +396,11 @@ MmaLayout mma_layout(int m_tiles, int kq, int srows, int stages) {
 }
 
 cudaError_t launch_gemm_mma(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream) {
+  const bool zp = p.zeros != nullptr;
   switch (cfg.m_tiles) {
-    case 1: return launch_one<1>(cfg, tmA, p, stream);
-    case 2: return launch_one<2>(cfg, tmA, p, stream);
-    case 4: return launch_one<4>(cfg, tmA, p, stream);
+    case 1: return zp ? launch_one<1, true>(cfg, tmA, p, stream) : launch_one<1, false>(cfg, tmA, p, stream);
+    case 2: return zp ? launch_one<2, true>(cfg, tmA, p, stream) : launch_one<2, false>(cfg, tmA, p, stream);
+    case 4: return zp ? launch_one<4, true>(cfg, tmA, p, stream) : launch_one<4, false>(cfg, tmA, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

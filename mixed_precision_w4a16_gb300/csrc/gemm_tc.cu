@@ -150,6 +150,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 // position of output column r (0..127) of a strip inside its permuted scale row
 __device__ __forceinline__ int scale_pos(int r) { return (r & ~15) + 2 * (r & 7) + ((r >> 3) & 1); }
 
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// ZP: codes carry a zero point per group and column (p.zeros), else the constant 8.
+// BIAS: p.bias is added to C.  Both are compile-time so the plain layer's build is unchanged.
+template <bool ZP, bool BIAS>
 __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -243,13 +252,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         if (lane == 0) {
           const uint32_t fb = bar_wfull + 8 * s;
           const uint32_t st = sbase + p.w_base + s * p.w_stage_bytes;
-          mbar_arrive_expect_tx(fb, w_bytes + static_cast<uint32_t>(p.srows) * 256u);
+          mbar_arrive_expect_tx(fb, w_bytes + static_cast<uint32_t>(p.srows) * (ZP ? 384u : 256u));
           const uint32_t* wsrc =
               p.packed + (static_cast<long long>(j) * (p.K / 64) + static_cast<long long>(kt) * KQ) * 1024;
           bulk_g2s(st, wsrc, w_bytes, fb, pol);
           const int grp0 = (p.G == 128) ? kt * p.srows : 0;
           const uint16_t* ssrc = p.scales + (static_cast<long long>(j) * NG + grp0) * 128;
           bulk_g2s(st + w_bytes, ssrc, static_cast<uint32_t>(p.srows) * 256u, fb, pol_s);
+          if (ZP)  // the zero codes of the same scale rows, permuted the same way
+            bulk_g2s(st + p.z_off, p.zeros + (static_cast<long long>(j) * NG + grp0) * 128,
+                     static_cast<uint32_t>(p.srows) * 128u, fb, pol_s);
         }
         __syncwarp();
         issued = it + 1;
@@ -397,6 +409,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   // byte offsets inside a weight stage: packed block (kq = 2c + wg, b = 2q + bi) and its scale pair
   const uint32_t w_lane = static_cast<uint32_t>((wg * 8 + 2 * q) * 512 + lane * 16);
   const uint32_t s_lane = static_cast<uint32_t>(KQ * 4096 + 2 * q * 32 + 4 * g);
+  const uint32_t z_lane = static_cast<uint32_t>(p.z_off + 2 * q * 16 + 2 * g);  // zero pair of rows g, g + 8
   // tensor-memory address of this warp's first store: lanes 32q.., columns of half wg
   const uint32_t t_warp = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(wg * 32);
   // this team's chunks are gc = team, team + 2, ...: A buffer a = gc % NA, phase ph = (gc / NA) & 1
@@ -421,6 +434,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       // read this warp's share of the team's chunks and their scales, then release the stage
       uint4 wv[2][2];
       uint32_t sc[2][2];
+      uint32_t zc[2][2];
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int c = c0 + 2 * cc;
@@ -429,6 +443,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           for (int bi = 0; bi < 2; ++bi) {
             wv[cc][bi] = lds128(st + w_lane + c * 8192 + bi * 512);
             sc[cc][bi] = grouped ? lds32(st + s_lane + c * 256 + bi * 32) : 0x3c003c00u;
+            zc[cc][bi] = ZP ? lds_u16(st + z_lane + (grouped ? c * 128 : 0) + bi * 16) : 0u;
           }
         }
       }
@@ -452,11 +467,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           const uint32_t s_g = __byte_perm(sc[cc][bi], 0u, 0x1010u);   // scale of row g in both halves
           const uint32_t s_g8 = __byte_perm(sc[cc][bi], 0u, 0x3232u);  // scale of row g + 8
           const uint32_t words[4] = {wv[cc][bi].x, wv[cc][bi].y, wv[cc][bi].z, wv[cc][bi].w};
+          const uint32_t c_lo = ZP ? zp_const_lo(zc[cc][bi] & 15u) : 0u;
+          const uint32_t c_hi = ZP ? zp_const_hi((zc[cc][bi] >> 8) & 15u) : 0u;
           uint32_t r[16];
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
             uint32_t v[4];
-            decode8(words[jj], v);
+            if (ZP)
+              decode8_zp(words[jj], c_lo, c_hi, v);
+            else
+              decode8(words[jj], v);
             if (grouped) {
               v[0] = hmul2_u32(v[0], s_g);
               v[1] = hmul2_u32(v[1], s_g8);
@@ -503,6 +523,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         const float scale =
             grouped ? 1.f
                     : __half2float(__ushort_as_half(p.scales[static_cast<long long>(j) * NG * 128 + scale_pos(row)]));
+        const float bias_n = BIAS ? __half2float(__ushort_as_half(p.bias[n])) : 0.f;
         const int c_first = (j * p.KU) / p.T;
         const int c_last = min(((j + 1) * p.KU - 1) / p.T, p.grid - 1);
         const int nchunks = MB / 16;
@@ -535,7 +556,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int token = p.m0 + ch * 16 + i;
-              if (token < p.M) p.C[static_cast<long long>(token) * p.N + n] = f32_to_f16_bits(v[i] * scale);
+              if (token < p.M) p.C[static_cast<long long>(token) * p.N + n] = f32_to_f16_bits(BIAS ? v[i] * scale + bias_n : v[i] * scale);
             }
           }
           tc_fence_before();
@@ -581,7 +602,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 const int token = p.m0 + m0 + i;
-                if (token < p.M) p.C[static_cast<long long>(token) * p.N + n] = f32_to_f16_bits(acc[i] * scale);
+                if (token < p.M)
+                  p.C[static_cast<long long>(token) * p.N + n] = f32_to_f16_bits(BIAS ? acc[i] * scale + bias_n : acc[i] * scale);
               }
             }
             if (epi_lead && lane == 0) p.counters[j] = 0u;
@@ -607,11 +629,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
 
 }  // namespace
 
-TcLayout tc_layout(int mb, int ch, int srows, int a_stages, int w_stages) {
+TcLayout tc_layout(int mb, int ch, int srows, int a_stages, int w_stages, bool zp) {
   TcLayout l{};
   const int kq = 2 * ch;
   l.a_stage_bytes = 2 * mb * 128;  // one 128-row chunk; a multiple of 1024 keeps the swizzle atoms aligned
-  l.w_stage_bytes = (kq * 4096 + srows * 256 + 1023) / 1024 * 1024;
+  l.z_off = kq * 4096 + srows * 256;  // weight stage: packed chunk, scale rows, then (with zero points) zero rows
+  l.w_stage_bytes = (l.z_off + (zp ? srows * 128 : 0) + 1023) / 1024 * 1024;
   l.w_base = a_stages * l.a_stage_bytes;
   l.bar_off = l.w_base + w_stages * l.w_stage_bytes;
   l.flag_off = l.bar_off + 8 * (3 * kMaxNA + 2 * w_stages + 6);
@@ -626,9 +649,11 @@ uint32_t tc_idesc(int m, int n) {
 }
 
 cudaError_t launch_gemm_tc(int smem_bytes, const CUtensorMap& tmA, const TcParams& p, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  auto kern = p.zeros ? (p.bias ? gemm_tc_kernel<true, true> : gemm_tc_kernel<true, false>)
+                      : (p.bias ? gemm_tc_kernel<false, true> : gemm_tc_kernel<false, false>);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
-  gemm_tc_kernel<<<p.grid, kTcThreads, smem_bytes, stream>>>(tmA, p);
+  kern<<<p.grid, kTcThreads, smem_bytes, stream>>>(tmA, p);
   return cudaGetLastError();
 }
 

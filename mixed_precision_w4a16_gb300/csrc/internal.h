@@ -18,16 +18,18 @@ enum : uint32_t {
 // from the 1024-aligned base; one stage = activation pieces, weight chunk,
 // scale rows).
 struct MmaLayout {
-  int w_off, s_off, stage_bytes, tx_bytes;
+  int w_off, s_off, z_off, stage_bytes, tx_bytes;  // z_off: zero-point rows (with zero points only)
   int red_off, bar_off, flag_off, smem_bytes;
 };
 
-MmaLayout mma_layout(int m_tiles, int kq, int srows, int stages);
+MmaLayout mma_layout(int m_tiles, int kq, int srows, int stages, bool zp);
 
 // Parameters of one launch of the streaming (mma.sync) GEMM kernel.
 struct GemmParams {
   const uint32_t* packed;   // uint32[N/128][K/64][8][32][4]
   const uint16_t* scales;   // permuted fp16[N/128][K/G][128]
+  const uint8_t* zeros;     // permuted zero codes uint8[N/128][K/G][128], or null (z = 8)
+  const uint16_t* bias;     // fp16[N] added to C, or null
   uint16_t* C;              // fp16[M][N]
   uint32_t* status;         // workspace status word
   uint32_t* counters;       // one arrival counter per 128-column strip
@@ -42,7 +44,7 @@ struct GemmParams {
   int T;                    // units per CTA
   int grid;                 // CTAs
   int stages;               // pipeline depth
-  int w_off, s_off, stage_bytes, tx_bytes, red_off, bar_off, flag_off;
+  int w_off, s_off, z_off, stage_bytes, tx_bytes, red_off, bar_off, flag_off;
   long long wait_limit;     // clock cycles a pipeline wait may take
   int debug_stall;          // 1: never fill the first stage (failure-detection test)
 };
@@ -59,20 +61,23 @@ constexpr int kMmaThreads = 288;  // 8 consumer warps + 1 producer warp
 constexpr int kStrip = 128;       // output columns per strip / work unit
 
 cudaError_t launch_gemm_mma(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream);
+// with zero points (p.zeros != null) the kernels are built with the per-row zero decode
 
 // ---- tensor-memory (tcgen05) GEMM ----------------------------------------
 constexpr int kTcThreads = 736;  // 3 producers, 4 MMA issuers, 16 dequant warps (two teams)
 constexpr int kTcMaxIssuers = 4;
 
 struct TcLayout {
-  int a_stage_bytes, w_stage_bytes, w_base, bar_off, flag_off, smem_bytes;
+  int a_stage_bytes, w_stage_bytes, w_base, z_off, bar_off, flag_off, smem_bytes;  // z_off: within a weight stage
 };
-TcLayout tc_layout(int mb, int ch, int srows, int a_stages, int w_stages);
+TcLayout tc_layout(int mb, int ch, int srows, int a_stages, int w_stages, bool zp);
 uint32_t tc_idesc(int m, int n);
 
 struct TcParams {
   const uint32_t* packed;
   const uint16_t* scales;
+  const uint8_t* zeros;     // permuted zero codes, or null (z = 8)
+  const uint16_t* bias;     // fp16[N], or null
   uint16_t* C;
   uint32_t* status;
   uint32_t* counters;
@@ -85,7 +90,7 @@ struct TcParams {
   int srows;                // scale rows per unit
   int KU, units, T, grid;
   int a_stages, w_stages;   // activation ring / weight ring depths
-  int a_stage_bytes, w_stage_bytes, w_base, bar_off, flag_off;
+  int a_stage_bytes, w_stage_bytes, w_base, z_off, bar_off, flag_off;
   uint32_t idesc;
   long long wait_limit;
   int debug_stall;
@@ -97,10 +102,11 @@ cudaError_t launch_repack(const uint8_t* q, const uint16_t* s, int K, int N, int
                           uint16_t* scales_p, cudaStream_t stream);
 cudaError_t launch_quantize_repack(const uint16_t* w, const uint16_t* s, int K, int N, int G, uint32_t* packed,
                                    uint16_t* scales_p, cudaStream_t stream);
+cudaError_t launch_repack_zeros(const uint8_t* z, int K, int N, int G, uint8_t* zeros_p, cudaStream_t stream);
 cudaError_t launch_unpack(const uint32_t* packed, const uint16_t* scales_p, int K, int N, int G, uint8_t* q,
                           uint16_t* s, cudaStream_t stream);
-cudaError_t launch_dequant(const uint32_t* packed, const uint16_t* scales_p, int K, int N, int G, uint16_t* bhat,
-                           cudaStream_t stream);
+cudaError_t launch_dequant(const uint32_t* packed, const uint16_t* scales_p, const uint8_t* zeros_p, int K, int N,
+                           int G, uint16_t* bhat, cudaStream_t stream);
 cudaError_t read_and_clear_repack_flag(unsigned int* flag, cudaStream_t stream);
 
 }  // namespace w4a16

@@ -159,8 +159,26 @@ __global__ void unpack_codes_kernel(const uint4* __restrict__ packed, int K, int
 }
 
 // Bhat[k][n] = RNE(s * (q - 8)): the exact decode of the GEMM, then one FP16 multiply.
-__global__ void dequant_kernel(const uint4* __restrict__ packed, const uint16_t* __restrict__ sp, int K, int N,
-                               int G, uint16_t* __restrict__ bhat, long long nvec) {
+// zero codes uint8[K/G][N] -> the scales' permuted order (uint8[N/128][K/G][128]); codes above 15 flag
+__global__ void permute_zeros_kernel(const uint8_t* __restrict__ z, uint8_t* __restrict__ zp, int N, int NG,
+                                     long long count) {
+  const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (i >= count) return;
+  const int p = static_cast<int>(i & 127);
+  const long long t = i >> 7;
+  const int g = static_cast<int>(t % NG);
+  const long long strip = t / NG;
+  const long long n = strip * 128 + (p & ~15) + perm_row(p & 15);
+  const uint8_t code = z[g * static_cast<long long>(N) + n];
+  if (code > 15) atomicOr(&g_repack_flag, kDevErrCodeRange);
+  zp[i] = code & 15;
+}
+
+// Bhat[k][n] = RNE(s * (q - z)): the exact decode of the GEMM (z = 8 without zero points), then one
+// FP16 multiply.
+__global__ void dequant_kernel(const uint4* __restrict__ packed, const uint16_t* __restrict__ sp,
+                               const uint8_t* __restrict__ zp, int K, int N, int G, uint16_t* __restrict__ bhat,
+                               long long nvec) {
   const long long v = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
   if (v >= nvec) return;
   const VecCoord vc = vec_coord(v, K);
@@ -171,12 +189,21 @@ __global__ void dequant_kernel(const uint4* __restrict__ packed, const uint16_t*
   const uint32_t spair = *reinterpret_cast<const uint32_t*>(sp + sidx);
   const uint32_t s_row_g = (spair & 0xffffu) * 0x10001u;      // scale of fragment row g, both halves
   const uint32_t s_row_g8 = (spair >> 16) * 0x10001u;         // scale of fragment row g + 8
+  uint32_t c_lo = 0, c_hi = 0;
+  if (zp) {
+    const uint32_t zpair = *reinterpret_cast<const uint16_t*>(zp + sidx);  // zero codes of rows g, g + 8
+    c_lo = zp_const_lo(zpair & 15u);
+    c_hi = zp_const_hi((zpair >> 8) & 15u);
+  }
   const uint4 pv = packed[v];
   const uint32_t words[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     uint32_t a[4];
-    decode8(words[j], a);
+    if (zp)
+      decode8_zp(words[j], c_lo, c_hi, a);
+    else
+      decode8(words[j], a);
 #pragma unroll
     for (int reg = 0; reg < 4; ++reg) {
       const uint32_t h = hmul2_u32(a[reg], (reg & 1) ? s_row_g8 : s_row_g);
@@ -227,11 +254,17 @@ cudaError_t launch_unpack(const uint32_t* packed, const uint16_t* scales_p, int 
   return cudaGetLastError();
 }
 
-cudaError_t launch_dequant(const uint32_t* packed, const uint16_t* scales_p, int K, int N, int G, uint16_t* bhat,
-                           cudaStream_t stream) {
+cudaError_t launch_dequant(const uint32_t* packed, const uint16_t* scales_p, const uint8_t* zeros_p, int K, int N,
+                           int G, uint16_t* bhat, cudaStream_t stream) {
   const long long nvec = static_cast<long long>(K) * N / 32;
-  dequant_kernel<<<grid_for(nvec, 256), 256, 0, stream>>>(reinterpret_cast<const uint4*>(packed), scales_p, K, N,
-                                                           G, bhat, nvec);
+  dequant_kernel<<<grid_for(nvec, 256), 256, 0, stream>>>(reinterpret_cast<const uint4*>(packed), scales_p, zeros_p,
+                                                           K, N, G, bhat, nvec);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack_zeros(const uint8_t* z, int K, int N, int G, uint8_t* zeros_p, cudaStream_t stream) {
+  const long long count = static_cast<long long>(K / G) * N;
+  permute_zeros_kernel<<<grid_for(count, 256), 256, 0, stream>>>(z, zeros_p, N, K / G, count);
   return cudaGetLastError();
 }
 

@@ -27,6 +27,10 @@ from .w4a16_oracle import (  # noqa: F401
     packed_position,
     scale_position,
     quantize,
+    dequant_exact_zp,
+    dequant_fp16_bits_zp,
+    gemm_ref_zp,
+    repack_zeros,
     repack,
     unpack,
     TOL_REL,

@@ -151,6 +151,66 @@ def gemm_ref(A, q, s, G: int):
     return C, bound
 
 
+# ---------------------------------------------------------------------------
+# Zero points and bias ([P2] section "Marlin 要解决的精确问题": the affine form
+# B^[k,n] = s[g,n] (q[k,n] - z[g,n]); section "Marlin 已从一个 Kernel 变成一族实现":
+# the production variants with a zero point per group and a bias)
+# ---------------------------------------------------------------------------
+
+def dequant_exact_zp(q, s, z, G: int) -> np.ndarray:
+    """B^[k, n] = s[floor(k/G), n] * (q[k, n] - z[floor(k/G), n]) in float64 (exact:
+    an FP16 scale times an integer in [-15, 15]).  Readings taken: z are 4-bit
+    codes 0..15 (an integer zero point per group and column), shaped like s."""
+    q = np.asarray(q)
+    K, N = q.shape
+    G = _group(K, G)
+    z = np.asarray(z)
+    if z.shape != (K // G, N):
+        raise ValueError("zero points must have shape [K/G][N]")
+    if q.min(initial=0) < 0 or q.max(initial=0) > 15 or z.min(initial=0) < 0 or z.max(initial=0) > 15:
+        raise ValueError("codes and zero points must lie in 0..15")
+    s64 = _as_f64(s)
+    if s64.shape != (K // G, N):
+        raise ValueError("scales must have shape [K/G][N]")
+    g_of_k = np.arange(K) // G
+    return s64[g_of_k, :] * (q.astype(np.float64) - z.astype(np.float64)[g_of_k, :])
+
+
+def dequant_fp16_bits_zp(q, s, z, G: int) -> np.ndarray:
+    """RNE(s (q - z)) as FP16 bit patterns."""
+    return f64_to_fp16_bits(dequant_exact_zp(q, s, z, G))
+
+
+def gemm_ref_zp(A, q, s, z, bias, G: int):
+    """C_ref[m, n] = sum_k A[m, k] B^[k, n] + bias[n] and Bound[m, n] = sum_k |A[m, k] B^[k, n]| + |bias[n]|,
+    B^ with zero points (z None: the symmetric z = 8; bias None: no bias).  Reading taken: the bias joins
+    the absolute sum of the parity bound, so the FP16 rounding of a result dominated by the bias is covered."""
+    if z is None:
+        z = np.full(np.asarray(s).shape, Z_POINT, dtype=np.uint8)
+    Bh = dequant_exact_zp(q, s, z, G)
+    A64 = _as_f64(A)
+    C = A64 @ Bh
+    bound = np.abs(A64) @ np.abs(Bh)
+    if bias is not None:
+        b64 = _as_f64(bias).reshape(1, -1)
+        C = C + b64
+        bound = bound + np.abs(b64)
+    return C, bound
+
+
+def repack_zeros(z, G: int, K: int):
+    """Zero codes uint8[K/G][N] -> uint8[(K/G)*N] in the permuted order of the scales (``scale_position``)."""
+    z = np.asarray(z)
+    G = _group(K, G)
+    NG, N = z.shape
+    if NG != K // G or z.dtype != np.uint8 or z.max(initial=0) > 15:
+        raise ValueError("zero points must be uint8 codes 0..15 of shape [K/G][N]")
+    gg, nn = np.meshgrid(np.arange(NG), np.arange(N), indexing="ij")
+    zp = np.empty(NG * N, dtype=np.uint8)
+    zp[scale_position(gg, nn, NG).ravel()] = z.ravel()
+    return zp
+
+
 def error_excess(C_gpu, C_ref, bound) -> np.ndarray:
     """|C_gpu - C_ref| - (4e-3 * Bound + 1e-4): an element passes iff <= 0."""
     c = _as_f64(C_gpu) if np.asarray(C_gpu).dtype in (np.float16, np.uint16) else np.asarray(C_gpu, np.float64)

@@ -90,9 +90,8 @@ def test_integer_gemm_is_exact(w, path):
 @pytest.mark.parametrize("K", [1024, 18432])
 def test_zero_codes_stay_within_the_absolute_bound(w, path, K):
     # q == 8 everywhere: B^ = 0, so Bound = 0 and every output must satisfy |C| <= 1e-4.
-    # The kernel multiplies biased codes (1024 + q or 64 + q) and removes the bias with the
-    # activations' row sums, so here it sees only the cancellation error of that step;
-    # long K (many groups) is its worst case.
+    # The decode yields q - 8 exactly, so C must come out zero however long K is (a decode that
+    # offset the codes and removed the offset afterwards would fail here on long K).
     M, N, G = 9, 512, 128
     A, _, s = tl.layer(M, K, N, G, seed=3)
     q = np.full((K, N), 8, np.uint8)

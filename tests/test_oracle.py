@@ -428,3 +428,121 @@ def test_quantize_rejects_non_finite_quotients():
         oracle.quantize(w, _h(np.zeros((1, 1))), 128)
     with pytest.raises(ValueError):
         oracle.quantize(_h(np.full((128, 1), np.inf)), _h(np.ones((1, 1))), 128)
+
+
+# ---------------------------------------------------------------------------
+# zero points and bias
+# ---------------------------------------------------------------------------
+
+def _brute_force_zp(A, q, s, z, bias, G):
+    """Exact (C - bias) * 2^48 and Bound * 2^48 as Python integers, zero points written out."""
+    M, K = A.shape
+    N = q.shape[1]
+    a = [[_exact_fp16(A[m, k]) for k in range(K)] for m in range(M)]
+    sc = [[_exact_fp16(s[g, n]) for n in range(N)] for g in range(s.shape[0])]
+    C = [[0] * N for _ in range(M)]
+    B = [[0] * N for _ in range(M)]
+    for m in range(M):
+        for n in range(N):
+            acc = bnd = 0
+            for k in range(K):
+                wv = sc[k // G][n] * (int(q[k, n]) - int(z[k // G, n]))
+                acc += a[m][k] * wv
+                bnd += abs(a[m][k] * wv)
+            C[m][n] = acc
+            B[m][n] = bnd
+    return C, B
+
+
+def _zp_inputs(K, N, G, seed):
+    rng = np.random.default_rng(seed)
+    q, s = synth.make_weights(K, N, G, seed=seed)
+    z = rng.integers(0, 16, (K // synth.effective_group(K, G), N)).astype(np.uint8)
+    bias = rng.normal(0, 1.0, N).astype(np.float16)
+    return q, s, z, bias
+
+
+@pytest.mark.parametrize("M,K,N,G", [(1, 128, 16, 128), (3, 256, 16, 128), (2, 256, 16, 256)])
+def test_gemm_zp_matches_exact_brute_force(M, K, N, G):
+    q, s, z, bias = _zp_inputs(K, N, G, 40 + K)
+    A = synth.make_activations(M, K, seed=41 + M)
+    C, bound = oracle.gemm_ref_zp(A, q, s, z, bias, G)
+    Ce, Be = _brute_force_zp(A, q, s, z, bias, G)
+    for m in range(M):
+        for n in range(N):
+            exact = Ce[m][n] * 2.0 ** -48 + float(bias[n])
+            ebound = Be[m][n] * 2.0 ** -48 + abs(float(bias[n]))
+            assert abs(C[m, n] - exact) <= K * 2.0 ** -52 * ebound + 1e-300, (m, n)
+            assert abs(bound[m, n] - ebound) <= K * 2.0 ** -52 * ebound + 1e-300, (m, n)
+
+
+def test_planted_zero_point_row_mistake_is_caught(monkeypatch):
+    # using the zero point of the next group (a wrong group index for z) must fail the brute force
+    M, K, N, G = 2, 256, 16, 128
+    q, s, z, bias = _zp_inputs(K, N, G, 50)
+    A = synth.make_activations(M, K, seed=51)
+    real = ow.dequant_exact_zp
+    monkeypatch.setattr(ow, "dequant_exact_zp", lambda q_, s_, z_, G_: real(q_, s_, np.roll(z_, 1, axis=0), G_))
+    C, _ = oracle.gemm_ref_zp(A, q, s, z, None, G)
+    Ce, Be = _brute_force_zp(A, q, s, z, None, G)
+    worst = max(abs(C[m, n] - Ce[m][n] * 2.0 ** -48) / (Be[m][n] * 2.0 ** -48 + 1e-30)
+                for m in range(M) for n in range(N))
+    assert worst > 1e-3
+
+
+def test_zero_point_eight_is_the_symmetric_layer():
+    K, N, G = 256, 32, 128
+    q, s = synth.make_weights(K, N, G, seed=60)
+    A = synth.make_activations(3, K, seed=61)
+    z8 = np.full((K // G, N), 8, np.uint8)
+    C0, B0 = oracle.gemm_ref(A, q, s, G)
+    C1, B1 = oracle.gemm_ref_zp(A, q, s, z8, None, G)
+    assert np.array_equal(C0, C1) and np.array_equal(B0, B1)
+
+
+def test_codes_equal_to_zero_points_give_the_bias():
+    K, N, G = 256, 32, 128
+    _, s, z, bias = _zp_inputs(K, N, G, 62)
+    q = np.repeat(z, G, axis=0)
+    A = synth.make_activations(4, K, seed=63)
+    C, bound = oracle.gemm_ref_zp(A, q, s, z, bias, G)
+    assert np.array_equal(C, np.tile(bias.astype(np.float64), (4, 1)))
+    assert np.array_equal(bound, np.tile(np.abs(bias.astype(np.float64)), (4, 1)))
+
+
+def test_identity_rows_with_zero_points():
+    K, N, G = 256, 48, 128
+    q, s, z, _ = _zp_inputs(K, N, G, 64)
+    rows = [0, 127, 128, 255]
+    A = np.zeros((len(rows), K), np.float16)
+    for m, k in enumerate(rows):
+        A[m, k] = 1.0
+    C, _ = oracle.gemm_ref_zp(A, q, s, z, None, G)
+    # the rows of s (q - z), written out per element
+    for m, k in enumerate(rows):
+        want = np.array([float(s[k // G, n]) * (int(q[k, n]) - int(z[k // G, n])) for n in range(N)])
+        assert np.array_equal(C[m], want)
+
+
+def test_integer_gemm_with_zero_points_textbook():
+    rng = np.random.default_rng(65)
+    M, K, N, G = 3, 256, 32, 128
+    Ai = rng.integers(-4, 5, (M, K))
+    q = rng.integers(0, 16, (K, N)).astype(np.uint8)
+    z = rng.integers(0, 16, (K // G, N)).astype(np.uint8)
+    s = np.ones((K // G, N), np.float16)
+    C, _ = oracle.gemm_ref_zp(Ai.astype(np.float16), q, s, z, None, G)
+    ref = Ai.astype(np.int64) @ (q.astype(np.int64) - np.repeat(z.astype(np.int64), G, axis=0))
+    assert np.array_equal(C, ref.astype(np.float64))
+
+
+def test_repack_zeros_follows_the_scale_permutation():
+    K, N, G = 512, 256, 128
+    _, s, z, _ = _zp_inputs(K, N, G, 66)
+    _, sp = oracle.repack(np.zeros((K, N), np.uint8), s, G)
+    zp = oracle.repack_zeros(z, G, K)
+    # wherever the scale of (g, n) went, its zero point went too
+    for g in range(K // G):
+        for n in (0, 7, 8, 15, 16, 127, 128, 255):
+            i = int(oracle.scale_position(g, n, K // G))
+            assert sp[i] == s[g, n] and zp[i] == z[g, n]
