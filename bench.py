@@ -151,16 +151,19 @@ def cpu_sample_cols(workload):
             "profile_m32": 4096, "profile_m8": 4096}[workload]
 
 
+# the files that decide what the GEMM kernels execute and how the work is split
+GEMM_SOURCES = ("common.cuh", "gemm_launch.cu", "gemm_mma.cu", "gemm_tc.cu", "internal.h")
+
+
 def kernel_source_hash():
-    """Hash of the CUDA sources; profile figures are used only for the build they were taken on."""
-    import glob
+    """Hash of the GEMM kernels' sources and their work planning; profile figures are used only
+    for the build they were taken on."""
     import hashlib
     h = hashlib.sha256()
-    for path in sorted(glob.glob(os.path.join(ROOT, "mixed_precision_w4a16_gb300", "csrc", "*"))):
-        if path.endswith((".cu", ".cuh", ".h")):
-            h.update(os.path.basename(path).encode())
-            with open(path, "rb") as f:
-                h.update(f.read())
+    for name in GEMM_SOURCES:
+        h.update(name.encode())
+        with open(os.path.join(ROOT, "mixed_precision_w4a16_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 

@@ -1,0 +1,258 @@
+// Work planning and launch of the GEMM kernels: which kernel runs for a given
+// (M, K, N, G), how the work splits over the SMs, the shared- and tensor-memory
+// layouts, the activation tensor map, and the launches over token-row chunks.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "../../include/w4a16.h"
+#include "internal.h"
+
+namespace w4a16 {
+
+namespace {
+
+constexpr int kTcMinRows = 17;  // from 17 token rows on, the tensor-memory kernel runs
+
+void finish_split(Plan& pl, int K, int sms, size_t slot_floats) {
+  pl.KU = K / pl.k_tile;
+  pl.units = pl.strips * pl.KU;
+  pl.T = (pl.units + sms - 1) / sms;
+  pl.grid = (pl.units + pl.T - 1) / pl.T;
+  pl.workspace = kStatusBytes + counter_bytes(pl.strips) + 2ull * pl.grid * slot_floats * sizeof(float);
+}
+
+Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin, bool zp) {
+  Plan pl{};
+  pl.path = 1;
+  const int mc = std::min(std::max(M, 1), 32);
+  const int mt = mc <= 8 ? 1 : mc <= 16 ? 2 : 4;
+  pl.strips = N / kStrip;
+  // Unit depth KT = 64 * kq.  Per-SM time of a unit is modelled from copy-engine
+  // measurements on GB300: ~89 ns per 4 KB of weights streamed plus ~80 ns of
+  // fixed cost for the unit's three copy operations.  Pick the kq minimising
+  // T * unit time among those that keep >= 3 pipeline stages in shared memory.
+  int best_kq = 0;
+  long long best_cost = 0;
+  const int cands[3] = {8, 4, 2};
+  for (int c = 0; c < 3; ++c) {
+    const int kq = cands[c];
+    if (K % (64 * kq) != 0) continue;
+    const int srows = (G <= 64 * kq) ? (64 * kq) / G : 1;
+    const MmaLayout l0 = mma_layout(mt, kq, srows, 0, zp);
+    const int stages = (smem_optin - l0.smem_bytes) / (l0.stage_bytes + 16);
+    if (stages < 3 && kq != 2) continue;
+    const long long units = static_cast<long long>(pl.strips) * (K / (64 * kq));
+    const long long T = (units + sms - 1) / sms;
+    const long long cost = T * (89LL * kq + 80);
+    if (best_kq == 0 || cost < best_cost) {
+      best_kq = kq;
+      best_cost = cost;
+    }
+  }
+  if (!best_kq) best_kq = 2;
+  const int kq = best_kq;
+  const int KT = 64 * kq;
+  pl.srows = (G <= KT) ? KT / G : 1;
+  const MmaLayout l0 = mma_layout(mt, kq, pl.srows, 0, zp);
+  int stages = (smem_optin - l0.smem_bytes) / (l0.stage_bytes + 16);
+  stages = std::max(2, std::min(stages, 8));
+  pl.lay = mma_layout(mt, kq, pl.srows, stages, zp);
+  pl.cfg.m_tiles = mt;
+  pl.cfg.kq = kq;
+  pl.cfg.stages = stages;
+  pl.cfg.smem_bytes = pl.lay.smem_bytes;
+  pl.cfg.threads = kMmaThreads;
+  pl.m_chunk = 8 * mt;
+  pl.k_tile = KT;
+  pl.stages = stages;
+  pl.smem_bytes = pl.lay.smem_bytes;
+  pl.threads = kMmaThreads;
+  finish_split(pl, K, sms, static_cast<size_t>(kStrip) * 8 * mt);
+  return pl;
+}
+
+Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin, bool zp) {
+  Plan pl{};
+  pl.path = 2;
+  pl.mb = std::min(128, (std::max(M, 1) + 15) / 16 * 16);
+  pl.strips = N / kStrip;
+  // Tensor memory (512 columns): ni accumulators of mb columns (ni * mb <= 256),
+  // the rest for the ring of 64-column A chunks.  Activation stages pair with the
+  // A buffers (one per chunk in flight).
+  pl.ni = 1;  // a power of two: issuer i takes the chunks gc = i mod ni
+  while (2 * pl.ni <= std::min(kTcMaxIssuers, 256 / pl.mb)) pl.ni *= 2;
+  pl.na = std::min(6, (512 - pl.ni * pl.mb) / 64) & ~1;  // even: two activation producers take alternate chunks
+  // Unit depth KT = 128 * ch for the weight ring (one copy per unit, released by
+  // the dequant warps).  Keep >= 8 chunks of weights in flight; among the
+  // candidates, minimise T * unit time (memory time as for the streaming kernel
+  // vs tensor time, ~2.1 ns per mb * ch).
+  int best = 0, best_w = 0;
+  long long best_cost = 0;
+  const int cands[3] = {4, 2, 1};
+  for (int c = 0; c < 3; ++c) {
+    const int ch = cands[c];
+    if (K % (128 * ch) != 0) continue;
+    const int srows = (G == 128) ? ch : 1;
+    const TcLayout l0 = tc_layout(pl.mb, ch, srows, pl.na, 0, zp);
+    const int w_st = std::min(12, (smem_optin - l0.smem_bytes) / (l0.w_stage_bytes + 16));
+    if (w_st < 2 || w_st * ch < 8) continue;
+    const long long units = static_cast<long long>(pl.strips) * (K / (128 * ch));
+    const long long T = (units + sms - 1) / sms;
+    const long long cost = T * (std::max(178LL * ch, (21LL * pl.mb * ch) / 10) + 200);  // + per-unit sync and copy issue
+    if (best == 0 || cost < best_cost) {
+      best = ch;
+      best_w = w_st;
+      best_cost = cost;
+    }
+  }
+  if (!best) {
+    best = 1;
+    const TcLayout l0 = tc_layout(pl.mb, 1, 1, pl.na, 0, zp);
+    best_w = std::max(2, std::min(12, (smem_optin - l0.smem_bytes) / (l0.w_stage_bytes + 16)));
+  }
+  pl.ch = best;
+  pl.srows = (G == 128) ? pl.ch : 1;
+  pl.tlay = tc_layout(pl.mb, pl.ch, pl.srows, pl.na, best_w, zp);
+  pl.a_stages = pl.na;
+  pl.w_stages = best_w;
+  pl.m_chunk = pl.mb;
+  pl.k_tile = 128 * pl.ch;
+  pl.stages = best_w;
+  pl.smem_bytes = pl.tlay.smem_bytes;
+  pl.threads = kTcThreads;
+  finish_split(pl, K, sms, static_cast<size_t>(kStrip) * pl.mb);
+  return pl;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 3-D view of A (fp16[M][K]) as [K/64][M][64]: box {64, box_rows, kq} fetches the
+// kq 64-column pieces of one work unit in one copy, each piece box_rows x 128 bytes
+// with the 128-byte swizzle; rows beyond M are zero-filled.
+int encode_a_map(CUtensorMap* map, const uint16_t* A, int M, int K, int box_rows, int kq) {
+  auto enc = get_encoder();
+  if (!enc) return W4A16_ERR_CUDA;
+  const cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128u};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(kq)};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t*>(A), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
+}  // namespace
+
+Plan make_plan(int M, int K, int N, int G, int sms, int smem_optin, bool zp, int forced_path) {
+  const bool tc = forced_path == 2 || (forced_path != 1 && M >= kTcMinRows);
+  return tc ? make_plan_tc(M, K, N, G, sms, smem_optin, zp) : make_plan_mma(M, K, N, G, sms, smem_optin, zp);
+}
+
+int run_gemm(const Plan& pl, const GemmCall& c) {
+  uint8_t* ws = static_cast<uint8_t*>(c.workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  uint32_t* counters = reinterpret_cast<uint32_t*>(ws + kStatusBytes);
+  float* slots = reinterpret_cast<float*>(ws + kStatusBytes + counter_bytes(pl.strips));
+
+  CUtensorMap map;
+  // activation box depth: one 128-row chunk (2 pieces) per copy on path 2, one unit (kq pieces) on path 1
+  const int er = encode_a_map(&map, c.A, c.M, c.K, pl.m_chunk, pl.path == 2 ? 2 : pl.cfg.kq);
+  if (er != W4A16_OK) return er;
+
+  if (pl.path == 2) {
+    TcParams p{};
+    p.packed = c.packed;
+    p.scales = c.scales;
+    p.zeros = c.zeros;
+    p.bias = c.bias;
+    p.C = c.C;
+    p.status = status;
+    p.counters = counters;
+    p.slots = slots;
+    p.M = c.M;
+    p.K = c.K;
+    p.N = c.N;
+    p.G = c.G;
+    p.mb = pl.mb;
+    p.ch = pl.ch;
+    p.ni = pl.ni;
+    p.na = pl.na;
+    p.srows = pl.srows;
+    p.KU = pl.KU;
+    p.units = pl.units;
+    p.T = pl.T;
+    p.grid = pl.grid;
+    p.a_stages = pl.a_stages;
+    p.w_stages = pl.w_stages;
+    p.a_stage_bytes = pl.tlay.a_stage_bytes;
+    p.w_stage_bytes = pl.tlay.w_stage_bytes;
+    p.w_base = pl.tlay.w_base;
+    p.z_off = pl.tlay.z_off;
+    p.bar_off = pl.tlay.bar_off;
+    p.flag_off = pl.tlay.flag_off;
+    p.idesc = tc_idesc(128, pl.mb);
+    p.wait_limit = c.wait_limit;
+    p.debug_stall = c.debug_stall;
+    for (int m0 = 0; m0 < c.M; m0 += pl.m_chunk) {
+      p.m0 = m0;
+      if (launch_gemm_tc(pl.smem_bytes, map, p, c.stream) != cudaSuccess)
+        return W4A16_ERR_CUDA;
+    }
+    return W4A16_OK;
+  }
+
+  GemmParams p{};
+  p.packed = c.packed;
+  p.scales = c.scales;
+  p.zeros = c.zeros;
+  p.bias = c.bias;
+  p.C = c.C;
+  p.status = status;
+  p.counters = counters;
+  p.slots = slots;
+  p.M = c.M;
+  p.K = c.K;
+  p.N = c.N;
+  p.G = c.G;
+  p.kq = pl.cfg.kq;
+  p.srows = pl.srows;
+  p.KU = pl.KU;
+  p.units = pl.units;
+  p.T = pl.T;
+  p.grid = pl.grid;
+  p.stages = pl.cfg.stages;
+  p.w_off = pl.lay.w_off;
+  p.s_off = pl.lay.s_off;
+  p.z_off = pl.lay.z_off;
+  p.stage_bytes = pl.lay.stage_bytes;
+  p.tx_bytes = pl.lay.tx_bytes;
+  p.red_off = pl.lay.red_off;
+  p.bar_off = pl.lay.bar_off;
+  p.flag_off = pl.lay.flag_off;
+  p.wait_limit = c.wait_limit;
+  p.debug_stall = c.debug_stall;
+  for (int m0 = 0; m0 < c.M; m0 += pl.m_chunk) {
+    p.m0 = m0;
+    const cudaError_t e = launch_gemm_mma(pl.cfg, map, p, c.stream);
+    if (e != cudaSuccess) return W4A16_ERR_CUDA;
+  }
+  return W4A16_OK;
+}
+
+}  // namespace w4a16

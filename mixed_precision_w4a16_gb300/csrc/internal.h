@@ -109,4 +109,46 @@ cudaError_t launch_dequant(const uint32_t* packed, const uint16_t* scales_p, con
                            int G, uint16_t* bhat, cudaStream_t stream);
 cudaError_t read_and_clear_repack_flag(unsigned int* flag, cudaStream_t stream);
 
+// ---- work planning and launch of one GEMM (gemm_launch.cu) ------------------
+constexpr size_t kStatusBytes = 256;  // workspace head: the status word
+// bytes of the per-strip arrival counters that follow the status word
+inline size_t counter_bytes(int strips) { return (static_cast<size_t>(strips) * 4 + 255) / 256 * 256; }
+
+// Which kernel runs and how it splits (M, K, N) over `sms` SMs with `smem_optin`
+// bytes of shared memory per CTA.
+struct Plan {
+  int path;          // 1 = streaming mma.sync kernel, 2 = tensor-memory (tcgen05) kernel
+  MmaConfig cfg;     // path 1
+  MmaLayout lay;     // path 1
+  TcLayout tlay;     // path 2
+  int mb, ch;        // path 2: token rows per launch (multiple of 16), 128-row chunks per unit
+  int a_stages, w_stages;  // path 2: activation / weight ring depths
+  int ni, na;        // path 2: MMA issuers (accumulators), A chunks in tensor memory (= a_stages)
+  int m_chunk;       // token rows per launch
+  int k_tile;        // reduction rows per work unit
+  int srows;
+  int KU, strips, units, T, grid, stages, smem_bytes, threads;
+  size_t workspace;
+};
+
+// forced_path: 0 = by M, 1 = streaming kernel, 2 = tensor-memory kernel; zp: the GEMM reads
+// zero points (their rows take shared-memory stage space next to the scales)
+Plan make_plan(int M, int K, int N, int G, int sms, int smem_optin, bool zp, int forced_path);
+
+struct GemmCall {
+  const uint16_t* A;
+  const uint32_t* packed;
+  const uint16_t* scales;  // permuted
+  const uint8_t* zeros;    // permuted, or null
+  const uint16_t* bias;    // or null
+  uint16_t* C;
+  int M, K, N, G;
+  void* workspace;         // >= plan.workspace bytes; status word and counters zero
+  long long wait_limit;
+  int debug_stall;
+  cudaStream_t stream;
+};
+// Launches the planned kernels over all token-row chunks; returns a W4A16 status.
+int run_gemm(const Plan& pl, const GemmCall& c);
+
 }  // namespace w4a16
