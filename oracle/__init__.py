@@ -27,6 +27,8 @@ from .w4a16_oracle import (  # noqa: F401
     packed_position,
     scale_position,
     quantize,
+    quantize_zp,
+    minmax_scales,
     dequant_exact_zp,
     dequant_fp16_bits_zp,
     gemm_ref_zp,

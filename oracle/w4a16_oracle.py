@@ -9,7 +9,9 @@ Sources (page title, section):
        Language Models" (arXiv HTML), Section 3.4 "Kernel Design" (problem
        statement: FP16 A, K x N INT4 B, symmetric quantisation with one FP16
        scale per column or per G consecutive weights of a column) and its
-       paragraph "Bound By Weight Loading" (memory/FLOP counts).
+       paragraph "Bound By Weight Loading" (memory/FLOP counts); Section 2.2
+       "Mixed-Precision Inference on LLMs", paragraph "Weight Quantization"
+       (the min-max rule for the step and the zero).
   [P2] "Marlin 完全拆解：4-bit 权重如何喂满 GPU Tensor Core" (the Marlin
        deep-dive article), section "Marlin 要解决的精确问题" (the affine
        dequantisation B^[k,n] = s[g,n] (q[k,n] - z[g,n]), q in {0..15}),
@@ -310,6 +312,86 @@ def quantize(w, s, G: int) -> np.ndarray:
     if not np.all(np.isfinite(quot)):
         raise ValueError("w / s is NaN or infinite (zero, NaN or infinite input)")
     q = np.clip(np.rint(quot).astype(np.float64) + Z_POINT, 0, 15)
+    return q.astype(np.uint8)
+
+
+def minmax_scales(w, G: int, symmetric: bool = True):
+    """Scales (and zero codes) of FP16 weights w[K][N] by the min-max rule of
+    [P1] Section 2.2, paragraph "Weight Quantization": uniform quantisation of
+    a vector v to b bits maps min(v) to code 0 and max(v) to code 2^b - 1, so
+    the step is s = (max(v) - min(v)) / (2^b - 1); here b = 4 and v is one
+    group (G consecutive rows of one column).
+
+    Readings taken, so that the result fits the kernels' formats:
+      * asymmetric (``symmetric=False``): the kernels store the zero point as
+        a 4-bit code z with B^ = s (q - z), so the range is widened to contain
+        0: lo = min(min v, 0), hi = max(max v, 0), s = (hi - lo) / 15 and
+        z = clamp(rint(-lo / s), 0, 15);
+      * symmetric (z = 8): the range is [-a, a] with a = max |v|, so
+        s = 2a / 15;
+      * arithmetic: hi - lo (or 2a) and the division by 15 in IEEE float32,
+        one round-to-nearest each, then the scale rounded to FP16 (RNE);
+        the zero code's quotient -lo / s in float32 with that FP16 s;
+      * a group whose FP16 scale comes out 0 (all weights 0, or a range below
+        FP16's reach) takes s = 1, so its codes reproduce 0;
+      * a NaN or infinite weight is an error.
+
+    Returns (s fp16[K/G][N], z uint8[K/G][N] or None when symmetric).
+    """
+    w64 = _as_f64(w)
+    if w64.ndim != 2:
+        raise ValueError("weights must have shape [K][N]")
+    K, N = w64.shape
+    G = _group(K, G)
+    if not np.all(np.isfinite(w64)):
+        raise ValueError("weights must be finite")
+    grp = w64.reshape(K // G, G, N)
+    lo = grp.min(axis=1)
+    hi = grp.max(axis=1)
+    if symmetric:
+        a = np.maximum(np.abs(lo), np.abs(hi))
+        span = np.float32(2.0) * a.astype(np.float32)            # exact: a doubling
+    else:
+        lo = np.minimum(lo, 0.0)
+        hi = np.maximum(hi, 0.0)
+        span = hi.astype(np.float32) - lo.astype(np.float32)     # one float32 rounding
+    s32 = span / np.float32(15.0)                                 # one float32 rounding
+    s16 = s32.astype(np.float16)                                  # RNE to FP16
+    s16[s16 == 0] = np.float16(1.0)
+    if symmetric:
+        return s16, None
+    zq = (-lo).astype(np.float32) / s16.astype(np.float32)
+    z = np.clip(np.rint(zq), 0, 15).astype(np.uint8)
+    return s16, z
+
+
+def quantize_zp(w, s, z, G: int) -> np.ndarray:
+    """4-bit codes with a zero code per group and column: the step before the
+    repack for the asymmetric format,
+
+        q[k, n] = clamp(rint(w[k, n] / s[floor(k/G), n]) + z[floor(k/G), n], 0, 15),
+
+    so that s (q - z) is the nearest point of the grid to w inside the code
+    range.  The quotient, rounding and errors are those of ``quantize``
+    (float32 division, ties to even; a NaN or infinite quotient is an error).
+    """
+    w64 = _as_f64(w)
+    if w64.ndim != 2:
+        raise ValueError("weights must have shape [K][N]")
+    K, N = w64.shape
+    G = _group(K, G)
+    s64 = _as_f64(s)
+    z = np.asarray(z)
+    if s64.shape != (K // G, N) or z.shape != (K // G, N):
+        raise ValueError("scales and zero codes must have shape [K/G][N]")
+    if z.min(initial=0) < 0 or z.max(initial=0) > 15:
+        raise ValueError("zero codes must lie in 0..15")
+    rows = np.arange(K) // G
+    with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
+        quot = w64.astype(np.float32) / s64[rows, :].astype(np.float32)
+    if not np.all(np.isfinite(quot)):
+        raise ValueError("w / s is NaN or infinite (zero, NaN or infinite input)")
+    q = np.clip(np.rint(quot).astype(np.float64) + z.astype(np.float64)[rows, :], 0, 15)
     return q.astype(np.uint8)
 
 

@@ -546,3 +546,146 @@ def test_repack_zeros_follows_the_scale_permutation():
         for n in (0, 7, 8, 15, 16, 127, 128, 255):
             i = int(oracle.scale_position(g, n, K // G))
             assert sp[i] == s[g, n] and zp[i] == z[g, n]
+
+
+# ---------------------------------------------------------------------------
+# min-max scale rule (MARLIN paper, Section 2.2, "Weight Quantization")
+# ---------------------------------------------------------------------------
+
+def _fp16_is_nearest(h: np.float16, x: Fraction) -> bool:
+    """h is an FP16 value nearest to x (its FP16 neighbours are not closer)."""
+    d = abs(Fraction(float(h)) - x)
+    for nb in (np.nextafter(h, np.float16(-np.inf)), np.nextafter(h, np.float16(np.inf))):
+        if np.isfinite(nb) and abs(Fraction(float(nb)) - x) < d:
+            return False
+    return True
+
+
+def _minmax_groups(rng, G, N):
+    """Weights [2G][N]: groups of mixed sign, all positive, all negative, tiny and wide ranges."""
+    w = rng.normal(0, 0.05, (2 * G, N))
+    w[:, 1] = np.abs(w[:, 1]) + 0.01          # all positive
+    w[:, 2] = -np.abs(w[:, 2]) - 0.02         # all negative
+    w[:, 3] *= 1e-4                           # small range (subnormal FP16 scale)
+    w[:, 4] *= 300.0                          # wide range
+    w[:G, 5] = 0.0                            # one all-zero group
+    return _h(w)
+
+
+@pytest.mark.parametrize("symmetric", [True, False])
+def test_minmax_scales_match_exact_rational_arithmetic(symmetric):
+    """Each scale is the FP16 nearest to f32(f32(span) / 15), span = hi - lo (or 2 max|v|), and each zero
+    code is clamp(round_half_even(f32(-lo / s)), 0, 15), all computed with exact rationals (pins the
+    divisor 2^4 - 1, the widened range, the symmetric range and the zero code's rounding)."""
+    rng = np.random.default_rng(71)
+    G, N = 128, 12
+    w = _minmax_groups(rng, G, N)
+    s, z = oracle.minmax_scales(w, G, symmetric=symmetric)
+    assert s.dtype == np.float16 and s.shape == (2, N)
+    assert (z is None) == symmetric
+    for g in range(2):
+        for n in range(N):
+            v = [Fraction(float(x)) for x in w[g * G:(g + 1) * G, n]]
+            if symmetric:
+                span = 2 * max(abs(min(v)), abs(max(v)))
+            else:
+                lo, hi = min(min(v), Fraction(0)), max(max(v), Fraction(0))
+                span = _f32_round_exact(hi - lo)
+            s32 = _f32_round_exact(span / 15)
+            if s32 <= Fraction(1, 2 ** 25):               # rounds to FP16 zero: s = 1
+                assert float(s[g, n]) == 1.0, (g, n)
+            else:
+                assert _fp16_is_nearest(s[g, n], s32), (g, n, float(s[g, n]), float(s32))
+            if not symmetric:
+                zq = _f32_round_exact(-lo / Fraction(float(s[g, n])))
+                assert z[g, n] == min(max(_round_half_even(zq), 0), 15), (g, n)
+
+
+def test_minmax_zero_range_group_takes_unit_scale():
+    w = _h(np.zeros((256, 2)))
+    w[128:, 1] = 0.25
+    s, z = oracle.minmax_scales(w, 128, symmetric=False)
+    assert float(s[0, 0]) == 1.0 and z[0, 0] == 0
+    assert np.all(oracle.dequant_exact_zp(oracle.quantize_zp(w, s, z, 128), s, z, 128)[:128] == 0.0)
+    s, _ = oracle.minmax_scales(w, 128, symmetric=True)
+    assert float(s[0, 0]) == 1.0 and np.all(oracle.quantize(w, s, 128)[:128] == 8)
+
+
+def test_minmax_exact_grid_is_reproduced():
+    """Weights on the grid c*k: asymmetric k in -7..8 gives s = c, z = 7; symmetric k in -7..7 with
+    one weight 7.5c gives s = c (both exact), and every grid weight comes back exactly."""
+    c = 2.0 ** -6
+    ks = np.array(list(range(-7, 9)) * 8, dtype=np.float64)        # 128 rows, each k 8 times
+    w = _h((c * ks).reshape(128, 1))
+    s, z = oracle.minmax_scales(w, 128, symmetric=False)
+    assert float(s[0, 0]) == c and z[0, 0] == 7
+    q = oracle.quantize_zp(w, s, z, 128)
+    assert np.array_equal(q.ravel(), (ks + 7).astype(np.uint8))
+    assert np.array_equal(oracle.dequant_exact_zp(q, s, z, 128), w.astype(np.float64))
+    ks2 = np.array((list(range(-7, 8)) * 9)[:127] + [7.5])
+    w2 = _h((c * ks2).reshape(128, 1))
+    s2, _ = oracle.minmax_scales(w2, 128, symmetric=True)
+    assert float(s2[0, 0]) == c
+    q2 = oracle.quantize(w2, s2, 128)
+    assert np.array_equal(q2.ravel()[:127], (ks2[:127] + 8).astype(np.uint8))
+    assert q2[127, 0] == 15                          # 7.5 rounds to 8 (even), clamped: error c/2
+
+
+@pytest.mark.parametrize("symmetric", [True, False])
+def test_minmax_reconstruction_error_bound(symmetric):
+    """The point of the rule: every weight is reproduced within half a step where its code is not
+    clamped (exactly, by the tie argument), and within a step anywhere; the group minimum gets code 0
+    (asymmetric, lo < 0) and the maximum a code >= 14."""
+    rng = np.random.default_rng(72)
+    G, N = 128, 64
+    w = _minmax_groups(rng, G, N)
+    w64 = w.astype(np.float64)
+    s, z = oracle.minmax_scales(w, G, symmetric=symmetric)
+    if symmetric:
+        q = oracle.quantize(w, s, G)
+        Bh = oracle.dequant_exact(q, s, G)
+        zz = np.full(s.shape, 8)
+    else:
+        q = oracle.quantize_zp(w, s, z, G)
+        Bh = oracle.dequant_exact_zp(q, s, z, G)
+        zz = z.astype(np.int64)
+    step = np.repeat(s.astype(np.float64), G, axis=0)
+    err = np.abs(Bh - w64)
+    inner = (q > 0) & (q < 15)
+    assert np.all(err[inner] <= step[inner] / 2)
+    lim = (0.5 * (1 + 14 * 2.0 ** -10)) if symmetric else 1.0
+    assert np.all(err <= lim * step * (1 + 2.0 ** -10) + 2.0 ** -24)
+    if not symmetric:
+        for g in range(2):
+            blk, zq = w64[g * G:(g + 1) * G], zz[g]
+            for n in range(N):
+                col = blk[:, n]
+                if col.min() < 0 and zq[n] < 15:
+                    assert q[g * G + int(np.argmin(col)), n] == 0, (g, n)
+                if col.max() > 0:
+                    assert q[g * G + int(np.argmax(col)), n] >= 14, (g, n)
+
+
+def test_minmax_rejects_non_finite_weights():
+    w = _h(np.ones((128, 2)))
+    w[5, 1] = np.inf
+    for sym in (True, False):
+        with pytest.raises(ValueError):
+            oracle.minmax_scales(w, 128, symmetric=sym)
+
+
+def test_quantize_zp_matches_exact_rational_arithmetic():
+    rng = np.random.default_rng(73)
+    K, N, G = 256, 8, 128
+    s = _h(rng.uniform(0.002, 0.05, (K // G, N)))
+    z = rng.integers(0, 16, (K // G, N)).astype(np.uint8)
+    w = _h(rng.normal(0, 0.15, (K, N)))
+    q = oracle.quantize_zp(w, s, z, G)
+    for k in range(K):
+        for n in range(N):
+            fr = Fraction(float(w[k, n])) / Fraction(float(s[k // G, n]))
+            want = min(max(_round_half_even(_f32_round_exact(fr)) + int(z[k // G, n]), 0), 15)
+            assert q[k, n] == want, (k, n)
+    # z = 8 everywhere is the symmetric quantiser
+    z8 = np.full((K // G, N), 8, np.uint8)
+    assert np.array_equal(oracle.quantize_zp(w, s, z8, G), oracle.quantize(w, s, G))
