@@ -530,8 +530,9 @@ def run_ours(args, rank, world, device):
 
 def time_offline_steps(w, torch, q_d, s_d, K, N, G, seed, peaks):
     """Device time of the offline steps on the first layer of the workload (outside the
-    timed region): w4a16_repack (codes uint8 in, packed + permuted scales out) and
-    w4a16_quantize_repack (FP16 weights in), against the HBM roofline of their bytes."""
+    timed region): w4a16_repack (codes uint8 in, packed + permuted scales out),
+    w4a16_quantize_repack (FP16 weights in) and w4a16_minmax_scales (FP16 weights in,
+    scales and zero codes out), against the HBM roofline of the bytes each reads and writes once."""
     from mixed_precision_w4a16_gb300 import synth
     wt, s16 = synth.make_fp16_weights(K, N, G, seed)
     w_d = torch.from_numpy(wt).to(q_d.device)
@@ -539,9 +540,11 @@ def time_offline_steps(w, torch, q_d, s_d, K, N, G, seed, peaks):
     del wt
     NG = K // synth.effective_group(K, G)
     out = {}
-    for name, fn, in_bytes in (
-            ("repack", lambda: w.repack(q_d, s_d, G), K * N + 2 * NG * N),
-            ("quantize_repack", lambda: w.quantize_repack(w_d, s2_d, G), 2 * K * N + 2 * NG * N)):
+    packed_out = K * N // 2 + 2 * NG * N  # packed stream and permuted scales, written once
+    for name, fn, nbytes in (
+            ("repack", lambda: w.repack(q_d, s_d, G), K * N + 2 * NG * N + packed_out),
+            ("quantize_repack", lambda: w.quantize_repack(w_d, s2_d, G), 2 * K * N + 2 * NG * N + packed_out),
+            ("minmax_scales", lambda: w.minmax_scales(w_d, G, symmetric=False), 2 * K * N + 3 * NG * N)):
         for _ in range(2):
             fn()
         torch.cuda.synchronize()
@@ -554,7 +557,6 @@ def time_offline_steps(w, torch, q_d, s_d, K, N, G, seed, peaks):
         e1.record()
         torch.cuda.synchronize()
         us = e0.elapsed_time(e1) / reps * 1e3
-        nbytes = in_bytes + K * N // 2 + 2 * NG * N  # inputs read once + packed stream and scales written once
         out[name] = {"us": round(us, 1), "bytes": nbytes, "gb_s": round(nbytes / (us * 1e-6) / 1e9, 1),
                      "roofline_frac": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 3),
                      "shape": f"K={K} N={N} G={G}"}

@@ -130,6 +130,37 @@ W4A16_API int w4a16_repack(const uint8_t* q, const uint16_t* s, int K, int N, in
 W4A16_API int w4a16_quantize_repack(const uint16_t* w, const uint16_t* s, int K, int N, int groupsize,
                           uint32_t* packed, uint16_t* scales_p, void* stream);
 
+/* w4a16_quantize_repack with a zero code per group and column (the
+ * asymmetric format of w4a16_gemm_zp): q = clamp(rint(w / s) + z, 0, 15),
+ * same quotient, rounding and errors.  z: device, uint8[K/G][N] row-major
+ * codes 0..15 (NULL: the offset 8, i.e. w4a16_quantize_repack).  The zero
+ * codes themselves go through w4a16_repack_zeros for the GEMM. */
+W4A16_API int w4a16_quantize_repack_zp(const uint16_t* w, const uint16_t* s, const uint8_t* z, int K, int N,
+                                       int groupsize, uint32_t* packed, uint16_t* scales_p, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Scales (and zero codes) of FP16 weights by the min-max rule (MARLIN paper,
+ * Section 2.2 "Mixed-Precision Inference on LLMs", paragraph "Weight
+ * Quantization": the step is (max - min) / (2^b - 1), the minimum maps to
+ * code 0), per group of G consecutive rows of one column.
+ *
+ *   w   device, fp16[K][N] row-major: the weights
+ *   s   device, fp16[K/G][N] row-major, written: the scales
+ *   z   device, uint8[K/G][N] row-major, written: zero codes -- or NULL
+ *
+ * z = NULL: symmetric rule for the offset-8 format, s = RNE_fp16(f32(2 a) / 15)
+ * with a = max |w| over the group.  z given: asymmetric rule with the range
+ * widened to contain 0 (lo = min(min w, 0), hi = max(max w, 0)):
+ * s = RNE_fp16(f32(hi - lo) / 15), z = clamp(rint(f32(-lo / s)), 0, 15).
+ * Every step is one IEEE float32 rounding (f32), rint ties to even.  A scale
+ * that rounds to 0 (all-zero group) is written as 1.  A NaN or infinite
+ * weight writes s = 1 (z = 0) for its group and flags W4A16_ERR_VALUE for
+ * w4a16_get_status(NULL, stream).  Feed s (and z) to
+ * w4a16_quantize_repack(_zp).  Inputs and outputs must not overlap.
+ * ------------------------------------------------------------------------- */
+W4A16_API int w4a16_minmax_scales(const uint16_t* w, int K, int N, int groupsize, uint16_t* s, uint8_t* z,
+                                  void* stream);
+
 /* Inverse of w4a16_repack (diagnostic; the pages' layout check "repack then
  * unpack recovers the same codes and scales", deep-dive article section
  * "适用边界与工程陷阱").  Outputs q uint8[K][N] and s fp16[K/G][N]. */

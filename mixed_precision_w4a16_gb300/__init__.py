@@ -17,11 +17,12 @@ __all__ = [
     "W4A16Error", "lib", "Plan",
     "w4a16_packed_bytes", "w4a16_scales_count", "w4a16_workspace_bytes", "w4a16_plan",
     "w4a16_repack", "w4a16_quantize_repack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm", "w4a16_gemm_noalloc",
-    "w4a16_get_status", "w4a16_repack_zeros", "w4a16_gemm_zp", "w4a16_dequant_zp",
+    "w4a16_get_status", "w4a16_repack_zeros", "w4a16_gemm_zp", "w4a16_dequant_zp", "w4a16_quantize_repack_zp",
+    "w4a16_minmax_scales",
     "w4a16_debug_set_wait_cycles", "w4a16_debug_inject_stall", "w4a16_debug_force_path", "w4a16_status_string",
     "EXPORTED_SYMBOLS",
     "repack", "quantize_repack", "unpack", "dequant", "gemm", "workspace_for", "repack_zeros", "gemm_zp",
-    "dequant_zp",
+    "dequant_zp", "minmax_scales",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -32,7 +33,7 @@ EXPORTED_SYMBOLS = (
     "w4a16_workspace_bytes", "w4a16_repack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm",
     "w4a16_get_status", "w4a16_plan", "w4a16_debug_set_wait_cycles", "w4a16_debug_inject_stall",
     "w4a16_gemm_noalloc", "w4a16_debug_force_path", "w4a16_quantize_repack", "w4a16_repack_zeros",
-    "w4a16_gemm_zp", "w4a16_dequant_zp",
+    "w4a16_gemm_zp", "w4a16_dequant_zp", "w4a16_quantize_repack_zp", "w4a16_minmax_scales",
 )
 
 
@@ -78,6 +79,8 @@ def _load():
         "w4a16_repack_zeros": (i, [vp, i, i, i, vp, vp]),
         "w4a16_gemm_zp": (i, [vp, vp, vp, vp, vp, vp, i, i, i, i, vp, sz, vp]),
         "w4a16_dequant_zp": (i, [vp, vp, vp, i, i, i, vp, vp]),
+        "w4a16_quantize_repack_zp": (i, [vp, vp, vp, i, i, i, vp, vp, vp]),
+        "w4a16_minmax_scales": (i, [vp, i, i, i, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -170,6 +173,16 @@ def w4a16_quantize_repack(w, s, K, N, groupsize, packed, scales_p, stream=None):
                                         _stream(stream)), "w4a16_quantize_repack")
 
 
+def w4a16_quantize_repack_zp(w, s, z, K, N, groupsize, packed, scales_p, stream=None):
+    _check(_lib().w4a16_quantize_repack_zp(_ptr(w), _ptr(s), _ptr(z), K, N, groupsize, _ptr(packed),
+                                           _ptr(scales_p), _stream(stream)), "w4a16_quantize_repack_zp")
+
+
+def w4a16_minmax_scales(w, K, N, groupsize, s, z, stream=None):
+    _check(_lib().w4a16_minmax_scales(_ptr(w), K, N, groupsize, _ptr(s), _ptr(z), _stream(stream)),
+           "w4a16_minmax_scales")
+
+
 def w4a16_unpack(packed, scales_p, K, N, groupsize, q, s, stream=None):
     _check(_lib().w4a16_unpack(_ptr(packed), _ptr(scales_p), K, N, groupsize, _ptr(q), _ptr(s), _stream(stream)),
            "w4a16_unpack")
@@ -255,15 +268,29 @@ def repack(q, s, groupsize: int, stream=None):
     return packed, sp
 
 
-def quantize_repack(w, s, groupsize: int, stream=None):
+def quantize_repack(w, s, groupsize: int, z=None, stream=None):
     """w fp16[K][N], s fp16[K/G][N] (CUDA tensors) -> (packed int32[K*N/8], permuted fp16[K/G][N])
-    with q = clamp(rint(w / s) + 8, 0, 15)."""
+    with q = clamp(rint(w / s) + 8, 0, 15), or + z (uint8[K/G][N] zero codes) when z is given."""
     import torch
     K, N = w.shape
     packed = torch.empty(K * N // 8, dtype=torch.int32, device=w.device)
     sp = torch.empty(s.numel(), dtype=torch.float16, device=w.device)
-    w4a16_quantize_repack(w, s, K, N, groupsize, packed, sp, stream)
+    if z is None:
+        w4a16_quantize_repack(w, s, K, N, groupsize, packed, sp, stream)
+    else:
+        w4a16_quantize_repack_zp(w, s, z, K, N, groupsize, packed, sp, stream)
     return packed, sp
+
+
+def minmax_scales(w, groupsize: int, symmetric: bool = True, stream=None):
+    """w fp16[K][N] (CUDA tensor) -> (s fp16[K/G][N], z uint8[K/G][N] or None) by the min-max rule:
+    symmetric for the offset-8 format, else with zero codes."""
+    import torch
+    K, N = w.shape
+    s = torch.empty((_group_rows(K, groupsize), N), dtype=torch.float16, device=w.device)
+    z = None if symmetric else torch.empty((_group_rows(K, groupsize), N), dtype=torch.uint8, device=w.device)
+    w4a16_minmax_scales(w, K, N, groupsize, s, z, stream)
+    return s, z
 
 
 def unpack(packed, scales_p, K: int, N: int, groupsize: int, stream=None):

@@ -159,15 +159,34 @@ int w4a16_repack(const uint8_t* q, const uint16_t* s, int K, int N, int groupsiz
 
 int w4a16_quantize_repack(const uint16_t* w, const uint16_t* s, int K, int N, int groupsize, uint32_t* packed,
                           uint16_t* scales_p, void* stream) {
+  return w4a16_quantize_repack_zp(w, s, nullptr, K, N, groupsize, packed, scales_p, stream);
+}
+
+int w4a16_quantize_repack_zp(const uint16_t* w, const uint16_t* s, const uint8_t* z, int K, int N, int groupsize,
+                             uint32_t* packed, uint16_t* scales_p, void* stream) {
   const int st = check_shape(K, N, groupsize);
   if (st != W4A16_OK) return st;
   if (!w || !s || !packed || !scales_p) return W4A16_ERR_NULL;
-  if (!aligned16(w) || !aligned16(s) || !aligned16(packed) || !aligned16(scales_p)) return W4A16_ERR_ALIGN;
+  if (!aligned16(w) || !aligned16(s) || !aligned16(packed) || !aligned16(scales_p) || (z && !aligned16(z)))
+    return W4A16_ERR_ALIGN;
   DeviceInfo* d = nullptr;
   const int r = current_device_info(&d);
   if (r != W4A16_OK) return r;
-  const cudaError_t e = launch_quantize_repack(w, s, K, N, effective_group(K, groupsize), packed, scales_p,
+  const cudaError_t e = launch_quantize_repack(w, s, z, K, N, effective_group(K, groupsize), packed, scales_p,
                                                static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
+int w4a16_minmax_scales(const uint16_t* w, int K, int N, int groupsize, uint16_t* s, uint8_t* z, void* stream) {
+  const int st = check_shape(K, N, groupsize);
+  if (st != W4A16_OK) return st;
+  if (!w || !s) return W4A16_ERR_NULL;
+  if (!aligned16(w) || !aligned16(s) || (z && !aligned16(z))) return W4A16_ERR_ALIGN;
+  DeviceInfo* d = nullptr;
+  const int r = current_device_info(&d);
+  if (r != W4A16_OK) return r;
+  const cudaError_t e = launch_minmax_scales(w, K, N, effective_group(K, groupsize), s, z,
+                                             static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
 }
 

@@ -1,5 +1,6 @@
 // Offline repack of 4-bit codes and FP16 scales into the GEMM's fragment
-// order, plus the two diagnostic inverses (unpack, dequantise).
+// order, the quantiser in front of it (min-max scales, codes from FP16
+// weights), plus the two diagnostic inverses (unpack, dequantise).
 //
 // Layout (see include/w4a16.h): packed uint32[N/128][K/64][8][32][4] --
 // 128-column strips stored contiguously along K; inside a strip, for each
@@ -83,8 +84,10 @@ __global__ void repack_codes_kernel(const uint8_t* __restrict__ q, int K, int N,
 // (the original Layer.pack step, deep-dive article section "可复现的调用链"):
 // q = clamp(rint(w / s) + 8, 0, 15), the quotient an IEEE float32 division,
 // rint rounding half to even.  Same word-side walk as repack_codes_kernel.
-__global__ void quantize_codes_kernel(const uint16_t* __restrict__ w, const uint16_t* __restrict__ s, int K, int N,
-                                      int G, uint4* __restrict__ packed, long long nvec) {
+// z: zero codes uint8[K/G][N] row-major, or null for the symmetric offset 8
+__global__ void quantize_codes_kernel(const uint16_t* __restrict__ w, const uint16_t* __restrict__ s,
+                                      const uint8_t* __restrict__ z, int K, int N, int G, uint4* __restrict__ packed,
+                                      long long nvec) {
   const long long v = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
   if (v >= nvec) return;
   const VecCoord vc = vec_coord(v, K);
@@ -101,11 +104,13 @@ __global__ void quantize_codes_kernel(const uint16_t* __restrict__ w, const uint
       const long long k = vc.kb * 64LL + 16 * j + c;
       const long long n = vc.nb * 16LL + r;
       const float wf = __half2float(__ushort_as_half(w[k * N + n]));
-      const float sf = __half2float(__ushort_as_half(s[(k / G) * N + n]));
+      const long long gi = (k / G) * N + n;
+      const float sf = __half2float(__ushort_as_half(s[gi]));
       const float quot = __fdiv_rn(wf, sf);
       uint32_t code = 8u;
       if (isfinite(quot)) {
-        const float qf = fminf(fmaxf(rintf(quot) + 8.0f, 0.0f), 15.0f);
+        const float off = z ? static_cast<float>(z[gi]) : 8.0f;
+        const float qf = fminf(fmaxf(rintf(quot) + off, 0.0f), 15.0f);
         code = static_cast<uint32_t>(qf);
       } else {
         bad = true;
@@ -122,6 +127,59 @@ __global__ void quantize_codes_kernel(const uint16_t* __restrict__ w, const uint
 __device__ __forceinline__ int perm_row(int p) { return (p >> 1) + 8 * (p & 1); }
 
 // sp index i -> (g, n): i = (strip * NG + g) * 128 + p, n = strip * 128 + 16 * (p / 16) + row(p % 16)
+// Scales (and zero codes) by the min-max rule: one thread per group and pair
+// of adjacent columns walks the group's G rows (a 4-byte load per row; the
+// warp's loads of one row are 128 contiguous bytes).  The arithmetic is the
+// rule's, one IEEE float32 rounding per step: span = hi - lo (or 2 max|v|),
+// s = RNE_fp16(span / 15), z = clamp(rint(-lo / s), 0, 15).  A scale that
+// rounds to 0 becomes 1; a non-finite weight flags kDevErrValue and leaves
+// s = 1 (and z = 0) for its group.
+__global__ void minmax_scales_kernel(const uint16_t* __restrict__ w, int N, int G, uint16_t* __restrict__ s,
+                                     uint8_t* __restrict__ z) {
+  const int c2 = blockIdx.x * blockDim.x + threadIdx.x;  // column pair
+  if (2 * c2 >= N) return;
+  const int g = blockIdx.y;
+  const uint32_t* col = reinterpret_cast<const uint32_t*>(w + static_cast<size_t>(g) * G * N) + c2;
+  const size_t stride = static_cast<size_t>(N / 2);
+  float lo0 = INFINITY, lo1 = INFINITY, hi0 = -INFINITY, hi1 = -INFINITY;
+  bool bad0 = false, bad1 = false;
+#pragma unroll 8
+  for (int r = 0; r < G; ++r) {
+    const uint32_t v = __ldg(col + r * stride);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v));
+    bad0 |= !isfinite(f.x);
+    bad1 |= !isfinite(f.y);
+    lo0 = fminf(lo0, f.x);
+    hi0 = fmaxf(hi0, f.x);
+    lo1 = fminf(lo1, f.y);
+    hi1 = fmaxf(hi1, f.y);
+  }
+  const float los[2] = {lo0, lo1}, his[2] = {hi0, hi1};
+  const bool bads[2] = {bad0, bad1};
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    float lo = los[j], hi = his[j];
+    const bool bad = bads[j];
+    float span;
+    if (z) {
+      lo = fminf(lo, 0.0f);
+      hi = fmaxf(hi, 0.0f);
+      span = __fsub_rn(hi, lo);
+    } else {
+      span = 2.0f * fmaxf(fabsf(lo), fabsf(hi));  // exact
+    }
+    __half sh = __float2half_rn(__fdiv_rn(span, 15.0f));
+    if (bad || __half2float(sh) == 0.0f) sh = __float2half_rn(1.0f);
+    const size_t o = static_cast<size_t>(g) * N + 2 * c2 + j;
+    s[o] = __half_as_ushort(sh);
+    if (z) {
+      const float zq = __fdiv_rn(-lo, __half2float(sh));
+      z[o] = bad ? 0 : static_cast<uint8_t>(fminf(fmaxf(rintf(zq), 0.0f), 15.0f));
+    }
+  }
+  if (bad0 || bad1) atomicOr(&g_repack_flag, kDevErrValue);
+}
+
 __global__ void permute_scales_kernel(const uint16_t* __restrict__ s, uint16_t* __restrict__ sp, int N, int NG,
                                       long long count, int inverse) {
   const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
@@ -230,15 +288,22 @@ cudaError_t launch_repack(const uint8_t* q, const uint16_t* s, int K, int N, int
   return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_repack(const uint16_t* w, const uint16_t* s, int K, int N, int G, uint32_t* packed,
-                                   uint16_t* scales_p, cudaStream_t stream) {
+cudaError_t launch_quantize_repack(const uint16_t* w, const uint16_t* s, const uint8_t* z, int K, int N, int G,
+                                   uint32_t* packed, uint16_t* scales_p, cudaStream_t stream) {
   const long long nvec = static_cast<long long>(K) * N / 32;
-  quantize_codes_kernel<<<grid_for(nvec, 256), 256, 0, stream>>>(w, s, K, N, G, reinterpret_cast<uint4*>(packed),
+  quantize_codes_kernel<<<grid_for(nvec, 256), 256, 0, stream>>>(w, s, z, K, N, G, reinterpret_cast<uint4*>(packed),
                                                                   nvec);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long ns = static_cast<long long>(K / G) * N;
   permute_scales_kernel<<<grid_for(ns, 256), 256, 0, stream>>>(s, scales_p, N, K / G, ns, 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_minmax_scales(const uint16_t* w, int K, int N, int G, uint16_t* s, uint8_t* z,
+                                 cudaStream_t stream) {
+  const dim3 grid(grid_for(N / 2, 256), static_cast<unsigned>(K / G));
+  minmax_scales_kernel<<<grid, 256, 0, stream>>>(w, N, G, s, z);
   return cudaGetLastError();
 }
 

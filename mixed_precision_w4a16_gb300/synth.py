@@ -58,6 +58,23 @@ def make_fp16_weights(K: int, N: int, groupsize: int, seed: int, signed_scales: 
     return w, s.astype(np.float16)
 
 
+def make_raw_weights(K: int, N: int, seed: int) -> np.ndarray:
+    """Unquantised weights float16[K][N] ~ N(0, 0.05) for the scale-finding step,
+    with some columns of other shapes: every 16th column (from 1) all positive,
+    (from 2) all negative, (from 3) scaled by 1e-4 (FP16 subnormal steps),
+    (from 4) scaled by 300, and the first rows of column 5 all zero (a zero
+    range in its first group)."""
+    rng = _rng(seed, 3)
+    w = rng.standard_normal((K, N), dtype=np.float32) * np.float32(0.05)
+    w[:, 1::16] = np.abs(w[:, 1::16]) + np.float32(0.01)
+    w[:, 2::16] = -np.abs(w[:, 2::16]) - np.float32(0.02)
+    w[:, 3::16] *= np.float32(1e-4)
+    w[:, 4::16] *= np.float32(300.0)
+    if N > 5:
+        w[: min(K, 128), 5] = 0.0
+    return w.astype(np.float16)
+
+
 def make_activations(M: int, K: int, seed: int) -> np.ndarray:
     """Activations ``A`` float16[M][K] drawn from N(0, 1)."""
     rng = _rng(seed, 0)

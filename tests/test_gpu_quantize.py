@@ -1,5 +1,6 @@
-"""Fused quantise + repack from FP16 weights on the GPU against the CPU oracle
-(byte exact): q = clamp(rint(w / s) + 8, 0, 15) in the packed layout."""
+"""The offline quantiser on the GPU against the CPU oracle (byte exact): fused
+quantise + repack from FP16 weights, q = clamp(rint(w / s) + 8, 0, 15) (or + z)
+in the packed layout, and the min-max scales and zero codes in front of it."""
 import numpy as np
 import pytest
 
@@ -88,3 +89,106 @@ def test_quantize_full_k_sampled_strips(w):
         assert np.array_equal(got_packed[j * words_per_strip:(j + 1) * words_per_strip], ref_packed)
         sps = (K // G) * 128
         assert np.array_equal(got_sp[j * sps:(j + 1) * sps], ref_sp.view(np.uint16))
+
+
+# ---------------------------------------------------------------------------
+# min-max scales (MARLIN paper, Section 2.2, "Weight Quantization")
+# ---------------------------------------------------------------------------
+
+MINMAX_SHAPES = [(128, 128, 128), (256, 384, 128), (1024, 512, -1), (4096, 256, 128), (1024, 640, 1024)]
+
+
+def _minmax_on_device(w, wt, G, symmetric):
+    torch = tl.torch_mod()
+    s, z = w.minmax_scales(tl.to_dev(wt), G, symmetric=symmetric)
+    torch.cuda.synchronize()
+    return s.cpu().numpy(), (None if z is None else z.cpu().numpy())
+
+
+@pytest.mark.parametrize("K,N,G", MINMAX_SHAPES)
+@pytest.mark.parametrize("symmetric", [True, False])
+def test_minmax_scales_match_oracle_bits(w, K, N, G, symmetric):
+    wt = synth.make_raw_weights(K, N, seed=K + 3 * N)
+    s, z = _minmax_on_device(w, wt, G, symmetric)
+    s_ref, z_ref = oracle.minmax_scales(wt, G, symmetric=symmetric)
+    assert np.array_equal(s.view(np.uint16), s_ref.view(np.uint16))
+    if symmetric:
+        assert z is None and z_ref is None
+    else:
+        assert np.array_equal(z, z_ref)
+    assert w.w4a16_get_status() == 0
+
+
+@pytest.mark.parametrize("symmetric", [True, False])
+def test_minmax_then_quantize_repack_matches_oracle(w, symmetric):
+    """The whole offline step on the device (scales, codes, packed layout, permuted zeros) against
+    the oracle, byte for byte."""
+    torch = tl.torch_mod()
+    K, N, G = 2048, 384, 128
+    wt = synth.make_raw_weights(K, N, seed=91)
+    wd = tl.to_dev(wt)
+    s, z = w.minmax_scales(wd, G, symmetric=symmetric)
+    packed, sp = w.quantize_repack(wd, s, G, z=z)
+    zp = None if z is None else w.repack_zeros(z, K, G)
+    torch.cuda.synchronize()
+    s_ref, z_ref = oracle.minmax_scales(wt, G, symmetric=symmetric)
+    q_ref = oracle.quantize(wt, s_ref, G) if symmetric else oracle.quantize_zp(wt, s_ref, z_ref, G)
+    ref_packed, ref_sp = oracle.repack(q_ref, s_ref, G)
+    assert np.array_equal(packed.cpu().numpy().view(np.uint32), ref_packed)
+    assert np.array_equal(sp.cpu().numpy().view(np.uint16).ravel(), ref_sp.view(np.uint16))
+    if not symmetric:
+        assert np.array_equal(zp.cpu().numpy(), oracle.repack_zeros(z_ref, G, K))
+    assert w.w4a16_get_status() == 0
+
+
+@pytest.mark.parametrize("M", [5, 40])
+def test_gemm_on_minmax_quantised_weights(w, M):
+    """Quantise with the asymmetric min-max rule on the device, then run the zero-point GEMM: within
+    the parity bound of the oracle's product of the oracle's codes."""
+    torch = tl.torch_mod()
+    K, N, G = 1024, 512, 128
+    wt = synth.make_raw_weights(K, N, seed=92)
+    A = synth.make_activations(M, K, seed=93)
+    wd = tl.to_dev(wt)
+    s, z = w.minmax_scales(wd, G, symmetric=False)
+    packed, sp = w.quantize_repack(wd, s, G, z=z)
+    zp = w.repack_zeros(z, K, G)
+    C = w.gemm_zp(tl.to_dev(A), packed, sp, zp, None, N, G)
+    torch.cuda.synchronize()
+    s_ref, z_ref = oracle.minmax_scales(wt, G, symmetric=False)
+    C_ref, bound = oracle.gemm_ref_zp(A, oracle.quantize_zp(wt, s_ref, z_ref, G), s_ref, z_ref, None, G)
+    assert oracle.error_ok(C.cpu().numpy(), C_ref, bound)
+
+
+def test_minmax_non_finite_weight_is_reported(w):
+    K, N, G = 256, 128, 128
+    wt = synth.make_raw_weights(K, N, seed=94)
+    wt[130, 9] = np.float16(np.inf)
+    for symmetric in (True, False):
+        s, z = _minmax_on_device(w, wt, G, symmetric)
+        assert w.w4a16_get_status() == 10   # W4A16_ERR_VALUE
+        assert w.w4a16_get_status() == 0
+        assert float(s[1, 9]) == 1.0 and (z is None or z[1, 9] == 0)
+        # every other group is the oracle's
+        ok = wt.copy()
+        ok[130, 9] = 0
+        s_ref, z_ref = oracle.minmax_scales(ok, G, symmetric=symmetric)
+        mask = np.ones(s.shape, bool)
+        mask[1, 9] = False
+        assert np.array_equal(s.view(np.uint16)[mask], s_ref.view(np.uint16)[mask])
+        if z is not None:
+            assert np.array_equal(z[mask], z_ref[mask])
+
+
+@pytest.mark.parametrize("G", [128, -1])
+def test_minmax_full_k_sampled_columns(w, G):
+    """K = 18432 (the big layer's depth), N = 8192: sampled columns against the oracle."""
+    K, N = 18432, 8192
+    wt = synth.make_raw_weights(K, N, seed=95)
+    for symmetric in (True, False):
+        s, z = _minmax_on_device(w, wt, G, symmetric)
+        cols = np.array([0, 1, 2, 3, 4, 5, 777, 4096, N - 2, N - 1])
+        s_ref, z_ref = oracle.minmax_scales(wt[:, cols], G, symmetric=symmetric)
+        assert np.array_equal(s[:, cols].view(np.uint16), s_ref.view(np.uint16))
+        if not symmetric:
+            assert np.array_equal(z[:, cols], z_ref)
