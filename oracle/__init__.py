@@ -29,6 +29,8 @@ from .w4a16_oracle import (  # noqa: F401
     quantize,
     quantize_zp,
     minmax_scales,
+    moe_gemm_ref,
+    check_expert_offsets,
     dequant_exact_zp,
     dequant_fp16_bits_zp,
     gemm_ref_zp,

@@ -18,7 +18,9 @@ Sources (page title, section):
        section "scale 为什么有时在内环乘，有时在末尾乘" (grouped sum
        C = sum_g s[g,n] sum_{k in g} A[m,k](q[k,n]-8) and the per-column form
        AB = (AQ) diag(s)), and section "量化数据如何进入 Tensor Core" (the
-       symmetric zero point 8 folded into the decode).
+       symmetric zero point 8 folded into the decode), and section
+       "适用边界与工程陷阱" (MoE layers: one GEMM per expert on the rows
+       routed to it).
 
 Readings taken where the pages are silent (each also listed in the design notes):
   * zero point: the symmetric main path uses the constant z = 8; no zero tensor;
@@ -313,6 +315,49 @@ def quantize(w, s, G: int) -> np.ndarray:
         raise ValueError("w / s is NaN or infinite (zero, NaN or infinite input)")
     q = np.clip(np.rint(quot).astype(np.float64) + Z_POINT, 0, 15)
     return q.astype(np.uint8)
+
+
+# ---------------------------------------------------------------------------
+# Grouped expert GEMM ([P2] section "适用边界与工程陷阱", items 1 and 4: an MoE
+# layer regroups the tokens by expert, so every expert's GEMM has its own,
+# usually small, M, and the grouped GEMM schedules differently from a dense one)
+# ---------------------------------------------------------------------------
+
+def check_expert_offsets(offsets, M: int) -> np.ndarray:
+    """offsets int[E+1]: 0 = offsets[0] <= offsets[1] <= ... <= offsets[E] = M."""
+    off = np.asarray(offsets, dtype=np.int64)
+    if off.ndim != 1 or off.size < 2 or off[0] != 0 or off[-1] != M or np.any(np.diff(off) < 0):
+        raise ValueError("expert offsets must rise from 0 to M")
+    return off
+
+
+def moe_gemm_ref(A, offsets, q, s, G: int):
+    """C_ref[m, n] = sum_k A[m, k] B^_e[k, n], e the expert that owns row m, and the
+    matching Bound, each float64[M][N].
+
+    Readings taken: the rows of A are already sorted by expert; expert e owns
+    rows offsets[e] .. offsets[e+1] - 1 (an expert may own none); every expert
+    has its own codes q[e] uint8[K][N] and scales s[e] fp16[K/G][N] with the
+    same K, N and G; the symmetric zero point 8, no bias.  Each expert's block
+    of rows is the plain product ``gemm_ref`` of that expert's weights.
+    """
+    A = np.asarray(A)
+    if A.ndim != 2:
+        raise ValueError("A must be fp16[M][K]")
+    M = A.shape[0]
+    off = check_expert_offsets(offsets, M)
+    E = off.size - 1
+    q = np.asarray(q)
+    if q.ndim != 3 or q.shape[0] != E:
+        raise ValueError("q must be uint8[E][K][N]")
+    N = q.shape[2]
+    C = np.zeros((M, N))
+    bound = np.zeros((M, N))
+    for e in range(E):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi > lo:
+            C[lo:hi], bound[lo:hi] = gemm_ref(A[lo:hi], q[e], s[e], G)
+    return C, bound
 
 
 def minmax_scales(w, G: int, symmetric: bool = True):

@@ -689,3 +689,47 @@ def test_quantize_zp_matches_exact_rational_arithmetic():
     # z = 8 everywhere is the symmetric quantiser
     z8 = np.full((K // G, N), 8, np.uint8)
     assert np.array_equal(oracle.quantize_zp(w, s, z8, G), oracle.quantize(w, s, G))
+
+
+# ---------------------------------------------------------------------------
+# grouped expert GEMM
+# ---------------------------------------------------------------------------
+
+def test_moe_gemm_integer_brute_force():
+    """Integer activations and unit scales: every row is its own expert's integer product, the owner found
+    by a binary search of the offsets (independent of the oracle's slicing); pins the row ownership at
+    every boundary, empty experts and the per-expert weights."""
+    rng = np.random.default_rng(81)
+    K, N, G = 256, 16, 128
+    off = np.array([0, 3, 3, 4, 9, 9, 12])            # experts 1 and 4 own no rows
+    E, M = off.size - 1, int(off[-1])
+    A = rng.integers(-3, 4, (M, K))
+    q = rng.integers(0, 16, (E, K, N)).astype(np.uint8)
+    s = np.ones((E, K // G, N), np.float16)
+    C, bound = oracle.moe_gemm_ref(A.astype(np.float16), off, q, s, G)
+    for m in range(M):
+        e = int(np.searchsorted(off, m, side="right")) - 1
+        want = A[m].astype(np.int64) @ (q[e].astype(np.int64) - 8)
+        assert np.array_equal(C[m], want.astype(np.float64)), m
+        assert np.array_equal(bound[m], (np.abs(A[m]).astype(np.int64) @ np.abs(q[e].astype(np.int64) - 8)))
+
+
+def test_moe_gemm_with_one_shared_weight_is_the_dense_product():
+    rng = np.random.default_rng(82)
+    K, N, G, E = 256, 32, 128, 5
+    q1, s1 = synth.make_weights(K, N, G, seed=83)
+    A = synth.make_activations(20, K, seed=84)
+    off = np.array([0, 2, 2, 11, 19, 20])
+    C, bound = oracle.moe_gemm_ref(A, off, np.stack([q1] * E), np.stack([s1] * E), G)
+    C_d, bound_d = oracle.gemm_ref(A, q1, s1, G)
+    assert np.array_equal(C, C_d) and np.array_equal(bound, bound_d)
+
+
+def test_moe_gemm_rejects_bad_offsets():
+    K, N, G = 128, 8, 128
+    q = np.zeros((2, K, N), np.uint8)
+    s = np.ones((2, 1, N), np.float16)
+    A = np.zeros((4, K), np.float16)
+    for off in ([1, 2, 4], [0, 3, 2], [0, 2, 5], [0, 4]):
+        with pytest.raises(ValueError):
+            oracle.moe_gemm_ref(A, off, q, s, G)
