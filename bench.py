@@ -55,6 +55,13 @@ WORKLOADS = {
     "profile_m8": ("profiling case M=8 K=18432 N=16384 group 128", [(18432, 16384, 128, [8])], 2),
 }
 
+# grouped expert GEMM sweep: (description, experts, top-k, K, N, groupsize, [tokens ...])
+MOE_CONFIGS = [
+    ("8 experts top-2, K=4096 N=14336 (Mixtral-style expert up-projection)", 8, 2, 4096, 14336, 128, [1, 4, 16, 64]),
+    ("128 experts top-8, K=2048 N=1536 (Qwen3-30B-A3B-style fused gate/up)", 128, 8, 2048, 1536, 128, [1, 16, 64]),
+    ("256 experts top-8, K=7168 N=4096 (DeepSeek-V3-style fused gate/up)", 256, 8, 7168, 4096, 128, [1, 16, 64]),
+]
+
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -95,6 +102,8 @@ def parse_args():
     ap.add_argument("--only-m", type=int, default=None, help="run only this M of the sweep (profiling)")
     ap.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS FP16 GEMM on the dequantised weights")
     ap.add_argument("--no-offline", action="store_true", help="skip timing the offline repack / quantise steps")
+    ap.add_argument("--no-moe", action="store_true", help="skip the grouped expert (MoE) GEMM sweep")
+    ap.add_argument("--no-ablation", action="store_true", help="skip the Figure 12 ablation sweep")
     ap.add_argument("--zero-points", action="store_true",
                     help="run every GEMM with a zero point per group and a bias (w4a16_gemm_zp)")
     ap.add_argument("--cpu-sample", default=None, help=argparse.SUPPRESS)  # internal: oracle timing child
@@ -506,6 +515,13 @@ def run_ours(args, rank, world, device):
                     "frac": t["frac"], "traffic": None, "kernel": dom["kernel"],
                     "over": f"its points M={t['points']}", "peak_source": peaks["source"]}
 
+    moe = None
+    if rank == 0 and not args.no_moe and args.workload == "big":
+        moe = time_moe(w, torch, device, peaks)
+    ablation = None
+    if rank == 0 and not args.no_ablation and args.workload == "big" and not args.zero_points:
+        ablation = time_ablations(w, torch, points, ws, max_ws, stream)
+
     cpu = None
     if not args.no_cpu_baseline:
         ncols = cpu_sample_cols(args.workload)
@@ -525,7 +541,113 @@ def run_ours(args, rank, world, device):
         "sweep": sweep, "roofline": roofline, "roofline_by_kernel": roofline_by_kernel,
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "clocks": clocks, "offline": offline,
+        "moe": moe, "ablation": ablation,
     }
+
+
+ABLATIONS = [("full design", 0), ("no evict-first on weights", 1), ("2 pipeline stages", 2),
+             ("no activation swizzle", 4), ("all three", 7)]
+
+
+def time_ablations(w, torch, points, ws, max_ws, stream):
+    """The MARLIN paper's Figure 12 ablations re-run on this library's kernels (outside the timed
+    region): per M of the sweep, the median device time of one GEMM with each switch of
+    w4a16_debug_ablate, and the slowdown against the full design.  The no-swizzle switch applies
+    to the streaming kernel only (M <= 16)."""
+    out = {"variants": [name for name, _ in ABLATIONS], "points": []}
+    try:
+        for p in points:
+            row = {"M": p["M"], "kernel": p["kernel"], "us": {}}
+            for name, flags in ABLATIONS:
+                w.w4a16_debug_ablate(flags)
+                times = []
+                for it in range(8):
+                    packed, sp = p["packs"][it % len(p["packs"])]
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    w.w4a16_gemm(p["A_d"], packed, sp, p["C_d"], p["M"], p["K"], p["N"], p["G"], ws, max_ws, stream)
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    if it >= 2:
+                        times.append(e0.elapsed_time(e1) * 1e3)
+                row["us"][name] = round(statistics.median(times), 1)
+            full = row["us"]["full design"]
+            row["slowdown"] = {k: round(v / full, 3) for k, v in row["us"].items() if k != "full design"}
+            out["points"].append(row)
+    finally:
+        w.w4a16_debug_ablate(0)
+    if w.w4a16_get_status(ws) != 0:
+        raise RuntimeError("device status error in the ablation sweep")
+    return out
+
+
+def time_moe(w, torch, device, peaks):
+    """Grouped expert GEMM (outside the timed region): one w4a16_moe_gemm over every expert of an
+    MoE layer, for routed batches of a few sizes.  The weights are random packed words (random
+    4-bit codes) and scales generated on the device; each timed call follows an L2 flush.  Bytes
+    are algorithmic: each expert that owns rows read once, plus A and C.  For context, the same
+    work as one w4a16_gemm launch per expert that owns rows."""
+    import numpy as np
+    from mixed_precision_w4a16_gb300 import synth
+    gen = torch.Generator(device=device)
+    gen.manual_seed(11)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+    out = []
+    for ci, (desc, E, topk, K, N, G, token_list) in enumerate(MOE_CONFIGS):
+        NG = K // synth.effective_group(K, G)
+        wpe, spe = K * N // 8, NG * N
+        packed = torch.randint(-2 ** 31, 2 ** 31, (E * wpe,), dtype=torch.int32, device=device, generator=gen)
+        sp = (torch.rand(E * spe, device=device, generator=gen) * 0.018 + 0.002).to(torch.float16)
+        for tokens in token_list:
+            counts = synth.make_expert_rows(tokens, topk, E, seed=100 * ci + tokens)
+            offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+            M = int(offsets[-1])
+            max_rows = int(counts.max())
+            A_d = torch.from_numpy(synth.make_activations(M, K, seed=7)).to(device)
+            C_d = torch.empty((M, N), dtype=torch.float16, device=device)
+            off_d = torch.from_numpy(offsets).to(device)
+            ws = w.moe_workspace_for(E, M, max_rows, K, N, G, device)
+            active = [e for e in range(E) if counts[e] > 0]
+            dense_ws = torch.zeros(max(w.w4a16_workspace_bytes(int(counts[e]), K, N, G) for e in active),
+                                   dtype=torch.uint8, device=device)
+
+            def grouped():
+                w.w4a16_moe_gemm(A_d, packed, sp, off_d, C_d, E, M, max_rows, K, N, G, ws)
+
+            def per_expert():
+                for e in active:
+                    lo, hi = int(offsets[e]), int(offsets[e + 1])
+                    w.w4a16_gemm(A_d[lo:hi], packed[e * wpe:(e + 1) * wpe], sp[e * spe:(e + 1) * spe], C_d[lo:hi],
+                                 hi - lo, K, N, G, dense_ws)
+
+            res = {}
+            for name, fn in (("grouped", grouped), ("per_expert", per_expert)):
+                for _ in range(3):
+                    fn()
+                times = []
+                for _ in range(10):
+                    flush.fill_(1)
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    fn()
+                    e1.record()
+                    torch.cuda.synchronize()
+                    times.append(e0.elapsed_time(e1) * 1e3)
+                res[name] = statistics.median(times)
+            if w.w4a16_get_status(ws) != 0:
+                raise RuntimeError("device status error in the grouped GEMM")
+            nbytes = len(active) * (K * N // 2 + 2 * NG * N) + 2 * M * K + 2 * M * N
+            gbs = nbytes / (res["grouped"] * 1e-6) / 1e9
+            out.append({"config": desc, "tokens": tokens, "rows": M, "active_experts": len(active),
+                        "max_rows_per_expert": max_rows, "us": round(res["grouped"], 1), "bytes": nbytes,
+                        "gb_s": round(gbs, 1), "roofline_frac": round(gbs / peaks["hbm_gbs"], 3),
+                        "per_expert_launches_us": round(res["per_expert"], 1)})
+            del A_d, C_d, ws, dense_ws
+        del packed, sp
+    del flush
+    return out
 
 
 def time_offline_steps(w, torch, q_d, s_d, K, N, G, seed, peaks):

@@ -229,6 +229,42 @@ W4A16_API int w4a16_dequant_zp(const uint32_t* packed, const uint16_t* scales_p,
                                int N, int groupsize, uint16_t* Bhat, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Grouped expert GEMM (MoE).  The deep-dive article, section "适用边界与工程
+ * 陷阱" (items 1 and 4), notes that an MoE layer regroups the tokens by
+ * expert, so every expert's GEMM has its own small M, and that the grouped
+ * GEMM schedules differently from a dense layer.  One call runs all experts:
+ *
+ *   C[m][n] = sum_k A[m][k] * Bhat_e[k][n]   for the expert e that owns row m
+ *
+ *   A               device, fp16[M][K] row-major, rows sorted by expert
+ *   packed          device, E layers of w4a16_repack output back to back
+ *                   (expert e at word e * K * N / 8)
+ *   scales_p        device, E permuted scale arrays back to back (expert e at
+ *                   element e * (K/G) * N)
+ *   expert_offsets  device, int32[E + 1]: expert e owns rows
+ *                   expert_offsets[e] .. expert_offsets[e+1] - 1; they must
+ *                   rise from 0 to M (an expert may own no rows)
+ *   C               device, fp16[M][N] row-major, written
+ *   max_rows        a bound on the rows of any one expert (<= 0: M).  It picks
+ *                   the row-segment height: 8 rows when max_rows <= 8, else
+ *                   16; an expert with more rows is split into segments, each
+ *                   of which streams that expert's weights once.  A bound that
+ *                   is too low only costs speed.
+ *
+ * Symmetric codes (z = 8), no bias; 1 <= E <= 2048, M <= 2^24, K, N, G as for
+ * w4a16_gemm.  The offsets are read on the device only, so the call needs no
+ * host synchronisation (CUDA-graph capturable).  Offsets that do not rise from
+ * 0 to M leave C unwritten and record W4A16_ERR_VALUE for
+ * w4a16_get_status(workspace, stream).  The workspace (size from
+ * w4a16_moe_workspace_bytes) follows the rules of w4a16_gemm's workspace.
+ * ------------------------------------------------------------------------- */
+W4A16_API size_t w4a16_moe_workspace_bytes(int E, int M, int max_rows, int K, int N, int groupsize);
+
+W4A16_API int w4a16_moe_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* scales_p,
+                             const int32_t* expert_offsets, uint16_t* C, int E, int M, int max_rows, int K, int N,
+                             int groupsize, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Allocation-free GEMM.  The paper has no counterpart: this entry point is a
  * convenience of this library for callers that cannot allocate device memory.
  *
@@ -308,6 +344,20 @@ W4A16_API void w4a16_debug_inject_stall(int enable);
  * tensor-memory (tcgen05) kernel, 0 restores the default (tcgen05 from 17 token
  * rows on).  w4a16_workspace_bytes and w4a16_plan follow the same choice. */
 W4A16_API void w4a16_debug_force_path(int path);
+
+/* Ablation switches: the MARLIN paper's Figure 12 ablations (discussed in the
+ * deep-dive article, section "性能结果应该怎样读"), re-run on this library's
+ * kernels.  `flags` is a bit mask, applied to every later GEMM call of the
+ * process (0 restores the full design):
+ *   1  the weight stream loses its L2 evict-first hint (evict-normal instead);
+ *   2  the weight pipeline is 2 stages deep (streaming kernel: stages; tensor-
+ *      memory kernel: weight ring);
+ *   4  the activation tile is stored without the 128-byte XOR swizzle
+ *      (streaming kernel and grouped GEMM only; the tensor-memory kernel's
+ *      operand descriptors require the swizzled layout).
+ * The results stay bitwise identical: none of the switches changes the order
+ * of the arithmetic.  Diagnostic: not for concurrent use with GEMM calls. */
+W4A16_API void w4a16_debug_ablate(int flags);
 
 #ifdef __cplusplus
 }

@@ -18,11 +18,12 @@ __all__ = [
     "w4a16_packed_bytes", "w4a16_scales_count", "w4a16_workspace_bytes", "w4a16_plan",
     "w4a16_repack", "w4a16_quantize_repack", "w4a16_unpack", "w4a16_dequant", "w4a16_gemm", "w4a16_gemm_noalloc",
     "w4a16_get_status", "w4a16_repack_zeros", "w4a16_gemm_zp", "w4a16_dequant_zp", "w4a16_quantize_repack_zp",
-    "w4a16_minmax_scales",
+    "w4a16_minmax_scales", "w4a16_moe_workspace_bytes", "w4a16_moe_gemm", "w4a16_debug_ablate",
+    "ABLATE_NO_EVICT_FIRST", "ABLATE_STAGES_2", "ABLATE_NO_SWIZZLE",
     "w4a16_debug_set_wait_cycles", "w4a16_debug_inject_stall", "w4a16_debug_force_path", "w4a16_status_string",
     "EXPORTED_SYMBOLS",
     "repack", "quantize_repack", "unpack", "dequant", "gemm", "workspace_for", "repack_zeros", "gemm_zp",
-    "dequant_zp", "minmax_scales",
+    "dequant_zp", "minmax_scales", "moe_gemm", "moe_workspace_for",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -34,6 +35,7 @@ EXPORTED_SYMBOLS = (
     "w4a16_get_status", "w4a16_plan", "w4a16_debug_set_wait_cycles", "w4a16_debug_inject_stall",
     "w4a16_gemm_noalloc", "w4a16_debug_force_path", "w4a16_quantize_repack", "w4a16_repack_zeros",
     "w4a16_gemm_zp", "w4a16_dequant_zp", "w4a16_quantize_repack_zp", "w4a16_minmax_scales",
+    "w4a16_moe_workspace_bytes", "w4a16_moe_gemm", "w4a16_debug_ablate",
 )
 
 
@@ -75,12 +77,15 @@ def _load():
         "w4a16_debug_inject_stall": (None, [i]),
         "w4a16_gemm_noalloc": (i, [vp, vp, vp, vp, i, i, i, i, vp]),
         "w4a16_debug_force_path": (None, [i]),
+        "w4a16_debug_ablate": (None, [i]),
         "w4a16_quantize_repack": (i, [vp, vp, i, i, i, vp, vp, vp]),
         "w4a16_repack_zeros": (i, [vp, i, i, i, vp, vp]),
         "w4a16_gemm_zp": (i, [vp, vp, vp, vp, vp, vp, i, i, i, i, vp, sz, vp]),
         "w4a16_dequant_zp": (i, [vp, vp, vp, i, i, i, vp, vp]),
         "w4a16_quantize_repack_zp": (i, [vp, vp, vp, i, i, i, vp, vp, vp]),
         "w4a16_minmax_scales": (i, [vp, i, i, i, vp, vp, vp]),
+        "w4a16_moe_workspace_bytes": (sz, [i, i, i, i, i, i]),
+        "w4a16_moe_gemm": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -183,6 +188,19 @@ def w4a16_minmax_scales(w, K, N, groupsize, s, z, stream=None):
            "w4a16_minmax_scales")
 
 
+def w4a16_moe_workspace_bytes(E, M, max_rows, K, N, groupsize) -> int:
+    return int(_lib().w4a16_moe_workspace_bytes(E, M, max_rows, K, N, groupsize))
+
+
+def w4a16_moe_gemm(A, packed, scales_p, expert_offsets, C, E, M, max_rows, K, N, groupsize, workspace,
+                   workspace_bytes=None, stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib().w4a16_moe_gemm(_ptr(A), _ptr(packed), _ptr(scales_p), _ptr(expert_offsets), _ptr(C), E, M,
+                                 max_rows, K, N, groupsize, _ptr(workspace), int(workspace_bytes),
+                                 _stream(stream)), "w4a16_moe_gemm")
+
+
 def w4a16_unpack(packed, scales_p, K, N, groupsize, q, s, stream=None):
     _check(_lib().w4a16_unpack(_ptr(packed), _ptr(scales_p), K, N, groupsize, _ptr(q), _ptr(s), _stream(stream)),
            "w4a16_unpack")
@@ -239,6 +257,17 @@ def w4a16_debug_inject_stall(enable: bool) -> None:
 def w4a16_debug_force_path(path: int) -> None:
     """0 = automatic kernel choice, 1 = streaming mma.sync kernel, 2 = tensor-memory kernel."""
     _lib().w4a16_debug_force_path(int(path))
+
+
+#: ablation switches of w4a16_debug_ablate (the MARLIN paper's Figure 12), combinable
+ABLATE_NO_EVICT_FIRST = 1
+ABLATE_STAGES_2 = 2
+ABLATE_NO_SWIZZLE = 4
+
+
+def w4a16_debug_ablate(flags: int) -> None:
+    """Remove design choices for every later GEMM call: ABLATE_* bits, 0 = the full design."""
+    _lib().w4a16_debug_ablate(int(flags))
 
 
 # ---------------------------------------------------------------------------
@@ -343,4 +372,28 @@ def gemm(A, packed, scales_p, N: int, groupsize: int, workspace=None, out=None, 
         workspace = workspace_for(M, K, N, groupsize, A.device)
     C = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=A.device)
     w4a16_gemm(A, packed, scales_p, C, M, K, N, groupsize, workspace, None, stream)
+    return C
+
+
+def moe_workspace_for(E: int, M: int, max_rows: int, K: int, N: int, groupsize: int, device=None):
+    """A zeroed workspace tensor for w4a16_moe_gemm."""
+    import torch
+    nbytes = w4a16_moe_workspace_bytes(E, M, max_rows, K, N, groupsize)
+    if nbytes == 0:
+        raise W4A16Error(2, "w4a16_moe_workspace_bytes")
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def moe_gemm(A, packed, scales_p, expert_offsets, N: int, groupsize: int, max_rows: int = 0, workspace=None,
+             out=None, stream=None):
+    """Grouped expert GEMM: A fp16[M][K] (rows sorted by expert), packed / scales_p the E experts'
+    repacked layers concatenated, expert_offsets int32[E+1] on the device -> C fp16[M][N]."""
+    import torch
+    M, K = A.shape
+    E = expert_offsets.numel() - 1
+    if workspace is None:
+        workspace = moe_workspace_for(E, M, max_rows, K, N, groupsize, A.device)
+    C = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=A.device)
+    w4a16_moe_gemm(A, packed, scales_p, expert_offsets, C, E, M, max_rows, K, N, groupsize, workspace, None,
+                   stream)
     return C

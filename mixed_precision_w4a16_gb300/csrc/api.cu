@@ -61,9 +61,10 @@ int check_shape(int K, int N, int groupsize) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 std::atomic<int> g_force_path{0};
+std::atomic<int> g_ablate{0};
 
 Plan plan_for(int M, int K, int N, int G, const DeviceInfo* d, bool zp) {
-  return make_plan(M, K, N, G, d->sms, d->smem_optin, zp, g_force_path.load());
+  return make_plan(M, K, N, G, d->sms, d->smem_optin, zp, g_force_path.load(), g_ablate.load());
 }
 
 }  // namespace
@@ -113,7 +114,8 @@ int w4a16_plan(int M, int K, int N, int groupsize, int num_sms, w4a16_plan_t* ou
     sms = d->sms;
     smem = d->smem_optin;
   }
-  const Plan pl = make_plan(M, K, N, effective_group(K, groupsize), sms, smem, false, g_force_path.load());
+  const Plan pl =
+      make_plan(M, K, N, effective_group(K, groupsize), sms, smem, false, g_force_path.load(), g_ablate.load());
   out->path = pl.path;
   out->m_tiles = pl.m_chunk / 8;
   out->m_chunk = pl.m_chunk;
@@ -142,6 +144,8 @@ void w4a16_debug_set_wait_cycles(long long cycles) { g_wait_cycles.store(cycles 
 void w4a16_debug_inject_stall(int enable) { g_stall.store(enable ? 1 : 0); }
 
 void w4a16_debug_force_path(int path) { g_force_path.store(path == 1 || path == 2 ? path : 0); }
+
+void w4a16_debug_ablate(int flags) { g_ablate.store(flags & (kAblateNoEvictFirst | kAblateStages2 | kAblateNoSwizzle)); }
 
 int w4a16_repack(const uint8_t* q, const uint16_t* s, int K, int N, int groupsize, uint32_t* packed,
                  uint16_t* scales_p, void* stream) {
@@ -239,7 +243,8 @@ int gemm_impl(const uint16_t* A, const uint32_t* packed, const uint16_t* scales_
   const int r = current_device_info(&d);
   if (r != W4A16_OK) return r;
   const int G = effective_group(K, groupsize);
-  const Plan pl = plan_for(M, K, N, G, d, zeros_p != nullptr);
+  const int ablate = g_ablate.load();  // one read: the plan and the launch see the same switches
+  const Plan pl = make_plan(M, K, N, G, d->sms, d->smem_optin, zeros_p != nullptr, g_force_path.load(), ablate);
   if (workspace_bytes < pl.workspace) return W4A16_ERR_WORKSPACE;
 
   const long long wc = g_wait_cycles.load();
@@ -257,6 +262,7 @@ int gemm_impl(const uint16_t* A, const uint32_t* packed, const uint16_t* scales_
   c.workspace = workspace;
   c.wait_limit = wc > 0 ? wc : kDefaultWaitCycles;
   c.debug_stall = g_stall.load();
+  c.ablate = ablate;
   c.stream = static_cast<cudaStream_t>(stream);
   return run_gemm(pl, c);
 }
@@ -301,6 +307,76 @@ int w4a16_dequant_zp(const uint32_t* packed, const uint16_t* scales_p, const uin
   const cudaError_t e = launch_dequant(packed, scales_p, zeros_p, K, N, effective_group(K, groupsize), Bhat,
                                        static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Grouped expert GEMM
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kMoeMaxRows = 1 << 24;
+
+// Checks the grouped GEMM's sizes and plans it on this device (status in *st).
+Plan moe_plan(int E, int M, int max_rows, int K, int N, int groupsize, int ablate, int* st) {
+  Plan pl{};
+  *st = check_shape(K, N, groupsize);
+  if (*st != W4A16_OK) return pl;
+  if (E < 1 || E > kMoeMaxExperts || M < 0 || M > kMoeMaxRows) {
+    *st = W4A16_ERR_SHAPE;
+    return pl;
+  }
+  DeviceInfo* d = nullptr;
+  *st = current_device_info(&d);
+  if (*st != W4A16_OK) return pl;
+  const int rows = (max_rows <= 0 || max_rows > M) ? std::max(M, 1) : max_rows;
+  pl = make_plan_moe(E, std::max(M, 1), rows, K, N, effective_group(K, groupsize), d->sms, d->smem_optin, ablate);
+  // the counters (one per segment and strip) and the unit count stay well inside int
+  if (static_cast<long long>(pl.max_seg) * pl.strips * pl.KU > (1LL << 30)) *st = W4A16_ERR_SHAPE;
+  return pl;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t w4a16_moe_workspace_bytes(int E, int M, int max_rows, int K, int N, int groupsize) {
+  int st = 0;
+  const Plan pl = moe_plan(E, M, max_rows, K, N, groupsize, 0, &st);
+  return st == W4A16_OK ? pl.workspace : 0;
+}
+
+int w4a16_moe_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* scales_p, const int32_t* expert_offsets,
+                   uint16_t* C, int E, int M, int max_rows, int K, int N, int groupsize, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  int st = 0;
+  const int ablate = g_ablate.load();
+  const Plan pl = moe_plan(E, M, max_rows, K, N, groupsize, ablate, &st);
+  if (st != W4A16_OK) return st;
+  if (M == 0) return W4A16_OK;
+  if (!A || !packed || !scales_p || !expert_offsets || !C) return W4A16_ERR_NULL;
+  if (!workspace) return W4A16_ERR_WORKSPACE;
+  if (!aligned16(A) || !aligned16(packed) || !aligned16(scales_p) || !aligned16(C) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(expert_offsets) & 3u) != 0)
+    return W4A16_ERR_ALIGN;
+  if (workspace_bytes < pl.workspace) return W4A16_ERR_WORKSPACE;
+  const long long wc = g_wait_cycles.load();
+  GemmCall c{};
+  c.A = A;
+  c.packed = packed;
+  c.scales = scales_p;
+  c.C = C;
+  c.M = M;
+  c.K = K;
+  c.N = N;
+  c.G = effective_group(K, groupsize);
+  c.workspace = workspace;
+  c.wait_limit = wc > 0 ? wc : kDefaultWaitCycles;
+  c.debug_stall = g_stall.load();
+  c.ablate = ablate;
+  c.stream = static_cast<cudaStream_t>(stream);
+  return run_moe_gemm(pl, c, expert_offsets);
 }
 
 }  // extern "C"
@@ -360,6 +436,7 @@ int w4a16_get_status(void* workspace, void* stream) {
   if (flag & kDevErrCodeRange) return W4A16_ERR_CODE_RANGE;
   if (flag & kDevErrValue) return W4A16_ERR_VALUE;
   if (word & kDevErrTimeout) return W4A16_ERR_TIMEOUT;
+  if (word & kDevErrValue) return W4A16_ERR_VALUE;
   if (word) return W4A16_ERR_CUDA;
   return W4A16_OK;
 }

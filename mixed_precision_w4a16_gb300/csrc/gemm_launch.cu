@@ -25,7 +25,10 @@ void finish_split(Plan& pl, int K, int sms, size_t slot_floats) {
   pl.workspace = kStatusBytes + counter_bytes(pl.strips) + 2ull * pl.grid * slot_floats * sizeof(float);
 }
 
-Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin, bool zp) {
+// moe_E > 0: the grouped expert GEMM (its expert tables take shared memory), with up
+// to moe_cols row segments sharing the SMs
+Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin, bool zp, int moe_E = 0, int moe_cols = 1,
+                   int ablate = 0) {
   Plan pl{};
   pl.path = 1;
   const int mc = std::min(std::max(M, 1), 32);
@@ -42,10 +45,10 @@ Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin, bool zp)
     const int kq = cands[c];
     if (K % (64 * kq) != 0) continue;
     const int srows = (G <= 64 * kq) ? (64 * kq) / G : 1;
-    const MmaLayout l0 = mma_layout(mt, kq, srows, 0, zp);
+    const MmaLayout l0 = mma_layout(mt, kq, srows, 0, zp, moe_E);
     const int stages = (smem_optin - l0.smem_bytes) / (l0.stage_bytes + 16);
     if (stages < 3 && kq != 2) continue;
-    const long long units = static_cast<long long>(pl.strips) * (K / (64 * kq));
+    const long long units = static_cast<long long>(pl.strips) * moe_cols * (K / (64 * kq));
     const long long T = (units + sms - 1) / sms;
     const long long cost = T * (89LL * kq + 80);
     if (best_kq == 0 || cost < best_cost) {
@@ -57,10 +60,11 @@ Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin, bool zp)
   const int kq = best_kq;
   const int KT = 64 * kq;
   pl.srows = (G <= KT) ? KT / G : 1;
-  const MmaLayout l0 = mma_layout(mt, kq, pl.srows, 0, zp);
+  const MmaLayout l0 = mma_layout(mt, kq, pl.srows, 0, zp, moe_E);
   int stages = (smem_optin - l0.smem_bytes) / (l0.stage_bytes + 16);
   stages = std::max(2, std::min(stages, 8));
-  pl.lay = mma_layout(mt, kq, pl.srows, stages, zp);
+  if (ablate & kAblateStages2) stages = 2;
+  pl.lay = mma_layout(mt, kq, pl.srows, stages, zp, moe_E);
   pl.cfg.m_tiles = mt;
   pl.cfg.kq = kq;
   pl.cfg.stages = stages;
@@ -75,7 +79,43 @@ Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin, bool zp)
   return pl;
 }
 
-Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin, bool zp) {
+GemmParams mma_params(const Plan& pl, const GemmCall& c, uint32_t* status, uint32_t* counters, float* slots) {
+  GemmParams p{};
+  p.packed = c.packed;
+  p.scales = c.scales;
+  p.zeros = c.zeros;
+  p.bias = c.bias;
+  p.C = c.C;
+  p.status = status;
+  p.counters = counters;
+  p.slots = slots;
+  p.M = c.M;
+  p.K = c.K;
+  p.N = c.N;
+  p.G = c.G;
+  p.kq = pl.cfg.kq;
+  p.srows = pl.srows;
+  p.KU = pl.KU;
+  p.units = pl.units;
+  p.T = pl.T;
+  p.grid = pl.grid;
+  p.stages = pl.cfg.stages;
+  p.w_off = pl.lay.w_off;
+  p.s_off = pl.lay.s_off;
+  p.z_off = pl.lay.z_off;
+  p.stage_bytes = pl.lay.stage_bytes;
+  p.tx_bytes = pl.lay.tx_bytes;
+  p.red_off = pl.lay.red_off;
+  p.bar_off = pl.lay.bar_off;
+  p.flag_off = pl.lay.flag_off;
+  p.moe_off = pl.lay.moe_off;
+  p.wait_limit = c.wait_limit;
+  p.debug_stall = c.debug_stall;
+  p.ablate = c.ablate;
+  return p;
+}
+
+Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin, bool zp, int ablate = 0) {
   Plan pl{};
   pl.path = 2;
   pl.mb = std::min(128, (std::max(M, 1) + 15) / 16 * 16);
@@ -114,6 +154,7 @@ Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin, bool zp) 
     const TcLayout l0 = tc_layout(pl.mb, 1, 1, pl.na, 0, zp);
     best_w = std::max(2, std::min(12, (smem_optin - l0.smem_bytes) / (l0.w_stage_bytes + 16)));
   }
+  if (ablate & kAblateStages2) best_w = 2;
   pl.ch = best;
   pl.srows = (G == 128) ? pl.ch : 1;
   pl.tlay = tc_layout(pl.mb, pl.ch, pl.srows, pl.na, best_w, zp);
@@ -144,7 +185,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
 // 3-D view of A (fp16[M][K]) as [K/64][M][64]: box {64, box_rows, kq} fetches the
 // kq 64-column pieces of one work unit in one copy, each piece box_rows x 128 bytes
 // with the 128-byte swizzle; rows beyond M are zero-filled.
-int encode_a_map(CUtensorMap* map, const uint16_t* A, int M, int K, int box_rows, int kq) {
+int encode_a_map(CUtensorMap* map, const uint16_t* A, int M, int K, int box_rows, int kq, bool swizzle = true) {
   auto enc = get_encoder();
   if (!enc) return W4A16_ERR_CUDA;
   const cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
@@ -152,16 +193,36 @@ int encode_a_map(CUtensorMap* map, const uint16_t* A, int M, int K, int box_rows
   const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(kq)};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t*>(A), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? W4A16_OK : W4A16_ERR_CUDA;
 }
 
 }  // namespace
 
-Plan make_plan(int M, int K, int N, int G, int sms, int smem_optin, bool zp, int forced_path) {
+Plan make_plan_moe(int E, int M, int max_rows, int K, int N, int G, int sms, int smem_optin, int ablate) {
+  // experts that can own rows, and the row segments (8 * m_tiles rows of one expert) they can need
+  const int active = std::max(1, std::min(E, M));
+  // Segment height: 8 rows when no expert has more, else 16.  Measured on GB300 (8 experts
+  // K=4096 N=14336; 128 x K=2048 N=1536; 256 x K=7168 N=4096), 16-row segments beat 32-row
+  // ones even at 32 rows per expert on average: an expert streamed twice at the 16-row
+  // rate costs less than once at the 32-row rate of this kernel.
+  Plan pl = make_plan_mma(max_rows <= 8 ? 8 : 16, K, N, G, sms, smem_optin, false, E, active, ablate);
+  pl.moe_E = E;
+  pl.max_seg = active + (M + pl.m_chunk - 1) / pl.m_chunk;
+  pl.grid = sms;  // persistent: the kernel spreads the segments it finds over all CTAs
+  pl.units = 0;   // decided on the device
+  pl.T = 0;
+  const size_t counters = static_cast<size_t>(pl.max_seg) * pl.strips;
+  pl.workspace = kStatusBytes + (counters * 4 + 255) / 256 * 256 +
+                 2ull * pl.grid * (static_cast<size_t>(kStrip) * pl.m_chunk) * sizeof(float);
+  return pl;
+}
+
+Plan make_plan(int M, int K, int N, int G, int sms, int smem_optin, bool zp, int forced_path, int ablate) {
   const bool tc = forced_path == 2 || (forced_path != 1 && M >= kTcMinRows);
-  return tc ? make_plan_tc(M, K, N, G, sms, smem_optin, zp) : make_plan_mma(M, K, N, G, sms, smem_optin, zp);
+  return tc ? make_plan_tc(M, K, N, G, sms, smem_optin, zp, ablate)
+            : make_plan_mma(M, K, N, G, sms, smem_optin, zp, 0, 1, ablate);
 }
 
 int run_gemm(const Plan& pl, const GemmCall& c) {
@@ -172,7 +233,9 @@ int run_gemm(const Plan& pl, const GemmCall& c) {
 
   CUtensorMap map;
   // activation box depth: one 128-row chunk (2 pieces) per copy on path 2, one unit (kq pieces) on path 1
-  const int er = encode_a_map(&map, c.A, c.M, c.K, pl.m_chunk, pl.path == 2 ? 2 : pl.cfg.kq);
+  // the no-swizzle ablation applies to the streaming kernel only
+  const bool swz = pl.path == 2 || !(c.ablate & kAblateNoSwizzle);
+  const int er = encode_a_map(&map, c.A, c.M, c.K, pl.m_chunk, pl.path == 2 ? 2 : pl.cfg.kq, swz);
   if (er != W4A16_OK) return er;
 
   if (pl.path == 2) {
@@ -209,6 +272,7 @@ int run_gemm(const Plan& pl, const GemmCall& c) {
     p.idesc = tc_idesc(128, pl.mb);
     p.wait_limit = c.wait_limit;
     p.debug_stall = c.debug_stall;
+    p.ablate = c.ablate & ~kAblateNoSwizzle;
     for (int m0 = 0; m0 < c.M; m0 += pl.m_chunk) {
       p.m0 = m0;
       if (launch_gemm_tc(pl.smem_bytes, map, p, c.stream) != cudaSuccess)
@@ -217,42 +281,33 @@ int run_gemm(const Plan& pl, const GemmCall& c) {
     return W4A16_OK;
   }
 
-  GemmParams p{};
-  p.packed = c.packed;
-  p.scales = c.scales;
-  p.zeros = c.zeros;
-  p.bias = c.bias;
-  p.C = c.C;
-  p.status = status;
-  p.counters = counters;
-  p.slots = slots;
-  p.M = c.M;
-  p.K = c.K;
-  p.N = c.N;
-  p.G = c.G;
-  p.kq = pl.cfg.kq;
-  p.srows = pl.srows;
-  p.KU = pl.KU;
-  p.units = pl.units;
-  p.T = pl.T;
-  p.grid = pl.grid;
-  p.stages = pl.cfg.stages;
-  p.w_off = pl.lay.w_off;
-  p.s_off = pl.lay.s_off;
-  p.z_off = pl.lay.z_off;
-  p.stage_bytes = pl.lay.stage_bytes;
-  p.tx_bytes = pl.lay.tx_bytes;
-  p.red_off = pl.lay.red_off;
-  p.bar_off = pl.lay.bar_off;
-  p.flag_off = pl.lay.flag_off;
-  p.wait_limit = c.wait_limit;
-  p.debug_stall = c.debug_stall;
+  GemmParams p = mma_params(pl, c, status, counters, slots);
   for (int m0 = 0; m0 < c.M; m0 += pl.m_chunk) {
     p.m0 = m0;
     const cudaError_t e = launch_gemm_mma(pl.cfg, map, p, c.stream);
     if (e != cudaSuccess) return W4A16_ERR_CUDA;
   }
   return W4A16_OK;
+}
+
+int run_moe_gemm(const Plan& pl, const GemmCall& c, const int* expert_off) {
+  uint8_t* ws = static_cast<uint8_t*>(c.workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  uint32_t* counters = reinterpret_cast<uint32_t*>(ws + kStatusBytes);
+  const size_t ncount = static_cast<size_t>(pl.max_seg) * pl.strips;
+  float* slots = reinterpret_cast<float*>(ws + kStatusBytes + (ncount * 4 + 255) / 256 * 256);
+  CUtensorMap map;
+  const int er = encode_a_map(&map, c.A, c.M, c.K, pl.m_chunk, pl.cfg.kq, !(c.ablate & kAblateNoSwizzle));
+  if (er != W4A16_OK) return er;
+  GemmParams p = mma_params(pl, c, status, counters, slots);
+  p.m0 = 0;
+  p.expert_off = expert_off;
+  p.E = pl.moe_E;
+  p.strips = pl.strips;
+  p.max_seg = pl.max_seg;
+  p.w_stride = static_cast<long long>(c.K) * c.N / 8;
+  p.s_stride = static_cast<long long>(c.K / c.G) * c.N;
+  return launch_moe_mma(pl.cfg, map, p, c.stream) == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
 }
 
 }  // namespace w4a16

@@ -27,7 +27,14 @@
 //    their partials through shared memory in fixed order; strips split
 //    between CTAs are reduced through FP32 slots with an arrival counter, the
 //    last arriver summing the slots in CTA order (deterministic, no spin
-//    waits).
+//    waits);
+//  * the grouped expert GEMM (MOE) runs the same pipeline over the rows of
+//    all experts in one launch: a column of work units is one strip of one
+//    row segment (up to 8*MT rows of one expert; MT = 1 or 2), so an expert's weights are
+//    streamed once per segment and experts without rows cost nothing.  Each
+//    CTA derives the segment table from the device-side expert offsets in
+//    its prologue (a block-wide prefix sum), so the launch needs no host
+//    synchronisation.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -57,6 +64,103 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Column of work units in a grouped expert GEMM: expert e, its row segment ci
+// (rows off[e] + MB * ci ..), strip j.  pref[e] = row segments of the experts
+// before e, pref[E] = all of them.
+struct SegPos {
+  int e, ci, j;
+};
+
+// Column jj (segment jj / strips, strip jj % strips); jj < pref[E] * strips.
+__device__ __forceinline__ SegPos seg_locate(const int* pref, int E, int strips, int jj) {
+  const int seg = jj / strips;
+  int lo = 0, hi = E;  // pref[lo] <= seg < pref[hi]; experts without rows have pref[e] == pref[e + 1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pref[mid] <= seg)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return SegPos{lo, seg - pref[lo], jj - seg * strips};
+}
+
+// The next column (call only while one exists).
+__device__ __forceinline__ void seg_next(SegPos& sp, const int* pref, int E, int strips) {
+  if (++sp.j < strips) return;
+  sp.j = 0;
+  if (++sp.ci < pref[sp.e + 1] - pref[sp.e]) return;
+  sp.ci = 0;
+  do {
+    ++sp.e;
+  } while (sp.e < E && pref[sp.e + 1] == pref[sp.e]);
+}
+
+// Grouped-GEMM prologue, run by every thread of the CTA: copies the expert
+// offsets to shared memory (offs), checks them (0 = off[0] <= ... <= off[E] = M)
+// and writes the segment prefix (pref) with a block-wide scan.  Returns the
+// number of segments, or -1 (status flagged) when the offsets are invalid or
+// need more segments than the workspace holds; the result is the same in
+// every thread.  The caller's next __syncthreads publishes pref.
+template <int MB>
+__device__ int moe_prologue(const GemmParams& p, int* pref, int* offs, int* scan, int warp, int lane) {
+  const int E = p.E;
+  const int per = (E + kMmaThreads - 1) / kMmaThreads;
+  const int e0 = threadIdx.x * per;
+  bool bad = false;
+  long long local = 0;
+  for (int i = 0; i < per; ++i) {
+    const int e = e0 + i;
+    if (e < E) {
+      const int lo = p.expert_off[e], hi = p.expert_off[e + 1];
+      offs[e] = lo;
+      const long long rows = static_cast<long long>(hi) - lo;
+      bad |= rows < 0 || rows > p.M;
+      if (rows > 0 && rows <= p.M) local += (rows + MB - 1) / MB;
+    }
+  }
+  if (threadIdx.x == 0) {
+    const int last = p.expert_off[E];
+    offs[E] = last;
+    bad |= p.expert_off[0] != 0 || last != p.M;
+  }
+  const int mine = static_cast<int>(min(local, static_cast<long long>(p.max_seg) + 1));  // no overflow below
+  int incl = mine;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) scan[1 + warp] = incl;
+  bad = __syncthreads_or(bad);
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int w = 0; w < kMmaThreads / 32; ++w) {
+      const int v = scan[1 + w];
+      scan[1 + w] = run;
+      run += v;
+    }
+    scan[0] = run;
+  }
+  __syncthreads();
+  const int total = scan[0];
+  if (bad || total > p.max_seg) {
+    if (threadIdx.x == 0) atomicOr(p.status, kDevErrValue);
+    return -1;
+  }
+  int run = scan[1 + warp] + incl - mine;
+  for (int i = 0; i < per; ++i) {
+    const int e = e0 + i;
+    if (e < E) {
+      pref[e] = run;
+      const int rows = offs[e + 1] - offs[e];
+      if (rows > 0) run += (rows + MB - 1) / MB;
+    }
+  }
+  if (threadIdx.x == 0) pref[E] = total;
+  return total;
+}
+
 __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
@@ -64,7 +168,8 @@ __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
 }
 
 // ZP: codes carry a zero point per group and column (p.zeros), else the constant 8.
-template <int MT, bool ZP>
+// MOE: grouped expert GEMM over p.E experts (p.expert_off), else one GEMM on rows p.m0 ..
+template <int MT, bool ZP, bool MOE>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     gemm_mma_kernel(const __grid_constant__ CUtensorMap tmA, const GemmParams p) {
   constexpr int MB = 8 * MT;
@@ -87,9 +192,23 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
-  const int u_begin = cta * p.T;
-  const int u_end = min(p.units, u_begin + p.T);
-  const int nunits = u_end - u_begin;
+  int units = p.units, T = p.T;
+  const int* pref = nullptr;  // grouped GEMM: segment prefix per expert [E + 1]
+  const int* offs = nullptr;  // grouped GEMM: expert row offsets [E + 1]
+  if (MOE) {
+    int* s_pref = reinterpret_cast<int*>(smem + p.moe_off);
+    int* s_offs = s_pref + (p.E + 1);
+    int* scan = s_offs + (p.E + 1);
+    const int nseg = moe_prologue<MB>(p, s_pref, s_offs, scan, warp, lane);
+    if (nseg < 0) return;  // invalid offsets: every thread leaves here, before any copy
+    pref = s_pref;
+    offs = s_offs;
+    units = nseg * p.strips * p.KU;
+    T = (units + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+  }
+  const int u_begin = cta * T;
+  const int u_end = min(units, u_begin + T);
+  const int nunits = max(0, u_end - u_begin);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -107,14 +226,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) prefetch_tensormap(&tmA);
-    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_w = (p.ablate & kAblateNoEvictFirst) ? policy_evict_normal() : policy_evict_first();
     const uint64_t pol_a = policy_evict_last();
     const int NG = p.K / p.G;
     const uint32_t w_bytes = static_cast<uint32_t>(KQ) * 4096u;
     int issued = 0;
     // incremental counters: stage s / its fill round, strip j / unit kt within the strip
     int s = 0, round = 0;
-    int j = u_begin / p.KU, kt = u_begin - (u_begin / p.KU) * p.KU;
+    int j = nunits > 0 ? u_begin / p.KU : 0, kt = u_begin - j * p.KU;
+    SegPos sp{0, 0, 0};
+    if (MOE && nunits > 0) sp = seg_locate(pref, p.E, p.strips, j);
     for (int it = 0; it < nunits; ++it) {
       if (it >= S) {
         bool ok = true;
@@ -133,12 +254,21 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           const uint32_t st = sbase + s * p.stage_bytes;
           const uint32_t fb = bar_full + 8 * s;
           mbar_arrive_expect_tx(fb, p.tx_bytes);
+          int strip = j, row0 = p.m0;
+          const uint32_t* pk = p.packed;
+          const uint16_t* sc = p.scales;
+          if (MOE) {
+            strip = sp.j;
+            row0 = offs[sp.e] + MB * sp.ci;
+            pk += sp.e * p.w_stride;
+            sc += sp.e * p.s_stride;
+          }
           const uint32_t* wsrc =
-              p.packed + (static_cast<long long>(j) * (p.K / 64) + static_cast<long long>(kt) * KQ) * 1024;
+              pk + (static_cast<long long>(strip) * (p.K / 64) + static_cast<long long>(kt) * KQ) * 1024;
           bulk_g2s(st + p.w_off, wsrc, w_bytes, fb, pol_w);
-          tma_load_3d(st, &tmA, 0, p.m0, kt * KQ, fb, pol_a);
+          tma_load_3d(st, &tmA, 0, row0, kt * KQ, fb, pol_a);
           const int grp0 = (p.G == 128) ? kt * p.srows : 0;  // G is 128 or K (K >= KT)
-          const uint16_t* ssrc = p.scales + (static_cast<long long>(j) * NG + grp0) * 128;
+          const uint16_t* ssrc = sc + (static_cast<long long>(strip) * NG + grp0) * 128;
           bulk_g2s(st + p.s_off, ssrc, static_cast<uint32_t>(p.srows) * 256u, fb, pol_a);
           if (ZP)  // the zero codes of the same scale rows, permuted the same way
             bulk_g2s(st + p.z_off, p.zeros + (static_cast<long long>(j) * NG + grp0) * 128,
@@ -154,6 +284,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       if (++kt == p.KU) {
         kt = 0;
         ++j;
+        if (MOE && it + 1 < nunits) seg_next(sp, pref, p.E, p.strips);
       }
     }
     named_bar_sync(3, kMmaThreads);
@@ -170,7 +301,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const int ng = warp >> 2;  // column half of the strip: blocks 4*ng .. 4*ng + 3
   const int kq0 = warp & 3;  // first 64-row piece of each unit (then kq0 + 4, ...)
   const int g = lane >> 2, t = lane & 3;
-  const int first_col = u_begin / p.KU;
+  const int swz = (p.ablate & kAblateNoSwizzle) ? 0 : g;  // row-dependent XOR of the 16-byte chunks
+  const int first_col = nunits > 0 ? u_begin / p.KU : 0;
+  SegPos sp{0, 0, 0};
+  if (MOE && nunits > 0) sp = seg_locate(pref, p.E, p.strips, first_col);
 
   float acc[kNbw][MT][4];
 #pragma unroll
@@ -205,7 +339,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         // activation fragments of this 64-row piece: 4 k16 steps x MT token tiles.  The packed
         // weights hold k = 4t .. 4t+3 of each 16-row block where the m16n8k16 fragment expects
         // 2t, 2t+1, 2t+8, 2t+9, so the matching activation pair is one 8-byte load of
-        // A[token][16 jj + 4t .. 4t+3] (128-byte swizzle: 16-byte chunk c of row r is at c ^ (r & 7)).
+        // A[token][16 jj + 4t .. 4t+3] (128-byte swizzle: 16-byte chunk c of row r is at c ^ (r & 7);
+        // without it, at c).
         const uint32_t a_box = st + kq * A_BOX;
         uint32_t bf[4][MT][2];
 #pragma unroll
@@ -214,7 +349,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           for (int mt = 0; mt < MT; ++mt) {
             const int token = mt * 8 + g;
             const int chunk = 2 * jj + (t >> 1);
-            const uint2 v = lds64(a_box + token * 128 + ((chunk ^ g) << 4) + (t & 1) * 8);
+            const uint2 v = lds64(a_box + token * 128 + ((chunk ^ swz) << 4) + (t & 1) * 8);
             bf[jj][mt][0] = v.x;
             bf[jj][mt][1] = v.y;
           }
@@ -296,8 +431,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     named_bar_sync(1, kConsumerWarps * 32);
     const bool skip = *seg_abort != 0;
     if (kq0 == 0 && !skip) {
-      const int c_first = (j * p.KU) / p.T;
-      const int c_last = min(((j + 1) * p.KU - 1) / p.T, p.grid - 1);
+      const int c_first = (j * p.KU) / T;
+      const int c_last = min(((j + 1) * p.KU - 1) / T, static_cast<int>(gridDim.x) - 1);
       const int sidx0 = ng * kNbw * MT * 4 * 32 + lane;  // this warp's part of a strip partial
       bool write_now = true;
       if (c_first != c_last) {
@@ -328,7 +463,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 #pragma unroll
               for (int e = 0; e < 4; ++e) acc[i][mt][e] = 0.f;
           for (int c = c_first; c <= c_last; ++c) {
-            const int cslot = (j == (c * p.T) / p.KU) ? 2 * c : 2 * c + 1;
+            const int cslot = (j == (c * T) / p.KU) ? 2 * c : 2 * c + 1;
             const float* src = p.slots + static_cast<long long>(cslot) * SLOT + sidx0;
 #pragma unroll
             for (int i = 0; i < kNbw; ++i)
@@ -341,18 +476,24 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
       }
       if (write_now) {
+        int strip = j, row0 = p.m0, row_end = p.M;
+        if (MOE) {
+          strip = sp.j;
+          row0 = offs[sp.e] + MB * sp.ci;
+          row_end = min(row0 + MB, offs[sp.e + 1]);
+        }
 #pragma unroll
         for (int i = 0; i < kNbw; ++i) {
-          const int n_base = j * kStrip + (ng * kNbw + i) * 16 + g;
+          const int n_base = strip * kStrip + (ng * kNbw + i) * 16 + g;
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int token = p.m0 + mt * 8 + 2 * t + (e & 1);
+              const int token = row0 + mt * 8 + 2 * t + (e & 1);
               const int n = n_base + 8 * (e >> 1);
               float c = acc[i][mt][e];
               if (p.bias) c += __half2float(__ushort_as_half(p.bias[n]));
-              if (token < p.M) p.C[static_cast<long long>(token) * p.N + n] = f32_to_f16_bits(c);
+              if (token < row_end) p.C[static_cast<long long>(token) * p.N + n] = f32_to_f16_bits(c);
             }
         }
       }
@@ -364,13 +505,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[i][mt][e] = 0.f;
     ++j;
+    if (MOE && it + 1 < nunits) seg_next(sp, pref, p.E, p.strips);
   }
   named_bar_sync(3, kMmaThreads);
 }
 
-template <int MT, bool ZP>
+template <int MT, bool ZP, bool MOE = false>
 cudaError_t launch_one(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream) {
-  auto kern = gemm_mma_kernel<MT, ZP>;
+  auto kern = gemm_mma_kernel<MT, ZP, MOE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem_bytes);
   if (e != cudaSuccess) return e;
   kern<<<p.grid, kMmaThreads, cfg.smem_bytes, stream>>>(tmA, p);
@@ -379,7 +521,7 @@ cudaError_t launch_one(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmP
 
 }  // namespace
 
-MmaLayout mma_layout(int m_tiles, int kq, int srows, int stages, bool zp) {
+MmaLayout mma_layout(int m_tiles, int kq, int srows, int stages, bool zp, int moe_E) {
   MmaLayout l{};
   const int MB = 8 * m_tiles;
   l.w_off = kq * MB * 128;        // activation pieces first (each a multiple of 1024 bytes)
@@ -391,7 +533,10 @@ MmaLayout mma_layout(int m_tiles, int kq, int srows, int stages, bool zp) {
   l.red_off = stages * l.stage_bytes;
   l.bar_off = l.red_off + 3 * 2 * kNbw * m_tiles * 4 * 32 * 4;
   l.flag_off = l.bar_off + 16 * stages;
-  l.smem_bytes = 1024 + l.flag_off + 64;
+  l.moe_off = l.flag_off + 64;
+  // grouped GEMM: segment prefix and offsets ([E + 1] ints each), then the scan's 1 + 9 ints
+  const int moe_bytes = moe_E > 0 ? (2 * (moe_E + 1) + 1 + kMmaThreads / 32) * 4 : 0;
+  l.smem_bytes = 1024 + l.moe_off + (moe_bytes + 15) / 16 * 16;
   return l;
 }
 
@@ -401,6 +546,14 @@ cudaError_t launch_gemm_mma(const MmaConfig& cfg, const CUtensorMap& tmA, const 
     case 1: return zp ? launch_one<1, true>(cfg, tmA, p, stream) : launch_one<1, false>(cfg, tmA, p, stream);
     case 2: return zp ? launch_one<2, true>(cfg, tmA, p, stream) : launch_one<2, false>(cfg, tmA, p, stream);
     case 4: return zp ? launch_one<4, true>(cfg, tmA, p, stream) : launch_one<4, false>(cfg, tmA, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_moe_mma(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream) {
+  switch (cfg.m_tiles) {
+    case 1: return launch_one<1, false, true>(cfg, tmA, p, stream);
+    case 2: return launch_one<2, false, true>(cfg, tmA, p, stream);  // segments are at most 16 rows
     default: return cudaErrorInvalidValue;
   }
 }

@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
 
   if (warp == 0) {
     // ------------------------------------------- producer: weights + scale rows, one stage per unit
-    const uint64_t pol = policy_evict_first();
+    const uint64_t pol = (p.ablate & kAblateNoEvictFirst) ? policy_evict_normal() : policy_evict_first();
     const uint64_t pol_s = policy_evict_last();
     const int NG = p.K / p.G;
     const uint32_t w_bytes = static_cast<uint32_t>(KQ) * 4096u;

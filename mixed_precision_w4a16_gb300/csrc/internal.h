@@ -14,15 +14,24 @@ enum : uint32_t {
   kDevErrValue = 1u << 2,
 };
 
+// Ablation switches (the MARLIN paper's Figure 12, re-run on these kernels): each
+// removes one design choice; they combine as a bit mask.
+enum : int {
+  kAblateNoEvictFirst = 1,  // weight stream without the L2 evict-first hint (evict-normal)
+  kAblateStages2 = 2,       // weight pipeline depth 2
+  kAblateNoSwizzle = 4,     // activation tile without the 128-byte XOR swizzle (streaming kernel)
+};
+
 // Shared-memory layout of one streaming-kernel configuration (byte offsets
 // from the 1024-aligned base; one stage = activation pieces, weight chunk,
 // scale rows).
 struct MmaLayout {
   int w_off, s_off, z_off, stage_bytes, tx_bytes;  // z_off: zero-point rows (with zero points only)
-  int red_off, bar_off, flag_off, smem_bytes;
+  int red_off, bar_off, flag_off, moe_off, smem_bytes;  // moe_off: expert tables of the grouped GEMM
 };
 
-MmaLayout mma_layout(int m_tiles, int kq, int srows, int stages, bool zp);
+// moe_E: experts of a grouped GEMM (0 for a plain GEMM); their tables take shared memory
+MmaLayout mma_layout(int m_tiles, int kq, int srows, int stages, bool zp, int moe_E = 0);
 
 // Parameters of one launch of the streaming (mma.sync) GEMM kernel.
 struct GemmParams {
@@ -47,7 +56,18 @@ struct GemmParams {
   int w_off, s_off, z_off, stage_bytes, tx_bytes, red_off, bar_off, flag_off;
   long long wait_limit;     // clock cycles a pipeline wait may take
   int debug_stall;          // 1: never fill the first stage (failure-detection test)
+  int ablate;               // kAblate* bits
+  // grouped expert GEMM only (the kernel derives units and T from the offsets; grid = gridDim.x):
+  const int* expert_off;    // device int32[E + 1]: rows of expert e are [off[e], off[e + 1])
+  int E;                    // experts
+  int strips;               // N / 128
+  int max_seg;              // row segments the counters were sized for
+  long long w_stride;       // packed words per expert (K * N / 8)
+  long long s_stride;       // permuted scales per expert ((K / G) * N)
+  int moe_off;              // shared-memory offset of the expert tables
 };
+
+constexpr int kMoeMaxExperts = 2048;
 
 struct MmaConfig {
   int m_tiles;      // 8-row token tiles (1, 2, 4)
@@ -61,6 +81,8 @@ constexpr int kMmaThreads = 288;  // 8 consumer warps + 1 producer warp
 constexpr int kStrip = 128;       // output columns per strip / work unit
 
 cudaError_t launch_gemm_mma(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream);
+// grouped expert GEMM: one launch over all experts (p.expert_off set, p.M = rows of A)
+cudaError_t launch_moe_mma(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream);
 // with zero points (p.zeros != null) the kernels are built with the per-row zero decode
 
 // ---- tensor-memory (tcgen05) GEMM ----------------------------------------
@@ -94,6 +116,7 @@ struct TcParams {
   uint32_t idesc;
   long long wait_limit;
   int debug_stall;
+  int ablate;               // kAblate* bits (no-swizzle does not apply to this kernel)
 };
 
 cudaError_t launch_gemm_tc(int smem_bytes, const CUtensorMap& tmA, const TcParams& p, cudaStream_t stream);
@@ -130,12 +153,13 @@ struct Plan {
   int k_tile;        // reduction rows per work unit
   int srows;
   int KU, strips, units, T, grid, stages, smem_bytes, threads;
+  int moe_E, max_seg;  // grouped expert GEMM: experts, row segments the counters are sized for
   size_t workspace;
 };
 
 // forced_path: 0 = by M, 1 = streaming kernel, 2 = tensor-memory kernel; zp: the GEMM reads
 // zero points (their rows take shared-memory stage space next to the scales)
-Plan make_plan(int M, int K, int N, int G, int sms, int smem_optin, bool zp, int forced_path);
+Plan make_plan(int M, int K, int N, int G, int sms, int smem_optin, bool zp, int forced_path, int ablate = 0);
 
 struct GemmCall {
   const uint16_t* A;
@@ -148,9 +172,16 @@ struct GemmCall {
   void* workspace;         // >= plan.workspace bytes; status word and counters zero
   long long wait_limit;
   int debug_stall;
+  int ablate;              // kAblate* bits; the plan must have been made with the same bits
   cudaStream_t stream;
 };
 // Launches the planned kernels over all token-row chunks; returns a W4A16 status.
 int run_gemm(const Plan& pl, const GemmCall& c);
+
+// Grouped expert GEMM over M expert-sorted rows (streaming kernel; max_rows bounds the
+// rows of any one expert and picks the row-segment height, 8 or 16).
+Plan make_plan_moe(int E, int M, int max_rows, int K, int N, int G, int sms, int smem_optin, int ablate = 0);
+// c.M = rows of A and C, c.packed / c.scales = E stacked layers; zeros and bias unused.
+int run_moe_gemm(const Plan& pl, const GemmCall& c, const int* expert_off);
 
 }  // namespace w4a16

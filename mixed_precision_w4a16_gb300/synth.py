@@ -18,7 +18,8 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["make_weights", "make_fp16_weights", "make_activations", "make_layer", "effective_group"]
+__all__ = ["make_weights", "make_fp16_weights", "make_raw_weights", "make_activations", "make_layer",
+           "make_expert_rows", "make_moe_layer", "effective_group"]
 
 
 def _rng(seed: int, stream: int) -> np.random.Generator:
@@ -86,3 +87,36 @@ def make_layer(M: int, K: int, N: int, groupsize: int, seed: int):
     q, s = make_weights(K, N, groupsize, seed)
     return {"A": make_activations(M, K, seed), "q": q, "s": s,
             "G": effective_group(K, groupsize)}
+
+
+def make_expert_rows(tokens: int, topk: int, E: int, seed: int, skew: float = 0.0) -> np.ndarray:
+    """Rows per expert of a top-k routed batch, int64[E] summing to tokens * topk:
+    each token picks topk distinct experts with probabilities proportional to
+    (rank + 1) ** -skew over a random ranking of the experts (skew 0: uniform;
+    larger: a few hot experts, many cold or empty ones)."""
+    if topk > E:
+        raise ValueError("topk must not exceed the number of experts")
+    rng = _rng(seed, 4)
+    p = (np.arange(E) + 1.0) ** -float(skew)
+    p = p[rng.permutation(E)]
+    p /= p.sum()
+    counts = np.zeros(E, dtype=np.int64)
+    for _ in range(tokens):
+        counts[rng.choice(E, size=topk, replace=False, p=p)] += 1
+    return counts
+
+
+def make_moe_layer(tokens: int, topk: int, E: int, K: int, N: int, groupsize: int, seed: int, skew: float = 0.0,
+                   counts=None):
+    """An expert-grouped layer: offsets int32[E+1] (rows of expert e are offsets[e] ..
+    offsets[e+1] - 1), activations A float16[M][K] with M = sum of the counts (rows
+    already sorted by expert), and per-expert codes q uint8[E][K][N] and scales
+    s float16[E][K/G][N] (expert e drawn from seed * 1000 + e)."""
+    if counts is None:
+        counts = make_expert_rows(tokens, topk, E, seed, skew)
+    counts = np.asarray(counts, dtype=np.int64)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    M = int(offsets[-1])
+    qs = [make_weights(K, N, groupsize, seed * 1000 + e) for e in range(E)]
+    return {"offsets": offsets, "A": make_activations(M, K, seed), "q": np.stack([x[0] for x in qs]),
+            "s": np.stack([x[1] for x in qs]), "G": effective_group(K, groupsize)}

@@ -115,6 +115,33 @@ def test_force_path_knob(w):
     assert w.w4a16_plan(200, 1024, 1024, 128, 152)["path"] == 2
 
 
+def test_ablation_switch_sets_two_stages(w):
+    full = [w.w4a16_plan(m, 4096, 4096, 128, 152) for m in (4, 64)]
+    assert all(p["stages"] > 2 for p in full)
+    try:
+        w.w4a16_debug_ablate(w.ABLATE_STAGES_2)
+        abl = [w.w4a16_plan(m, 4096, 4096, 128, 152) for m in (4, 64)]
+        assert [p["stages"] for p in abl] == [2, 2]
+        # nothing else of the plan changes: same kernel, tiles and split
+        for a, f in zip(abl, full):
+            assert {k: v for k, v in a.items() if k not in ("stages", "smem_bytes")} == \
+                {k: v for k, v in f.items() if k not in ("stages", "smem_bytes")}
+        w.w4a16_debug_ablate(w.ABLATE_NO_EVICT_FIRST | w.ABLATE_NO_SWIZZLE)
+        assert [w.w4a16_plan(m, 4096, 4096, 128, 152) for m in (4, 64)] == full
+    finally:
+        w.w4a16_debug_ablate(0)
+    assert [w.w4a16_plan(m, 4096, 4096, 128, 152) for m in (4, 64)] == full
+
+
+def test_moe_gemm_validates_before_touching_the_device(w):
+    L = w.lib
+    # E out of range, bad K, null pointers, M == 0
+    assert L.w4a16_moe_gemm(16, 16, 16, 16, 16, 0, 8, 8, 1024, 1024, 128, 16, 1 << 20, None) == 2
+    assert L.w4a16_moe_gemm(16, 16, 16, 16, 16, 4097, 8, 8, 1024, 1024, 128, 16, 1 << 20, None) == 2
+    assert L.w4a16_moe_gemm(16, 16, 16, 16, 16, 4, 8, 8, 1000, 1024, 128, 16, 1 << 20, None) == 2
+    assert L.w4a16_moe_gemm(16, 16, 16, 16, 16, 4, -1, 8, 1024, 1024, 128, 16, 1 << 20, None) == 2
+
+
 def test_plan_rejects_bad_shapes(w):
     with pytest.raises(w.W4A16Error):
         w.w4a16_plan(16, 1000, 1024, 128, 152)
