@@ -19,7 +19,7 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = ["make_weights", "make_fp16_weights", "make_raw_weights", "make_activations", "make_layer",
-           "make_expert_rows", "make_moe_layer", "effective_group"]
+           "make_expert_rows", "make_moe_layer", "make_weights_24", "effective_group"]
 
 
 def _rng(seed: int, stream: int) -> np.random.Generator:
@@ -120,3 +120,23 @@ def make_moe_layer(tokens: int, topk: int, E: int, K: int, N: int, groupsize: in
     qs = [make_weights(K, N, groupsize, seed * 1000 + e) for e in range(E)]
     return {"offsets": offsets, "A": make_activations(M, K, seed), "q": np.stack([x[0] for x in qs]),
             "s": np.stack([x[1] for x in qs]), "G": effective_group(K, groupsize)}
+
+
+def make_weights_24(K: int, N: int, groupsize: int, seed: int):
+    """2:4-sparse codes: in every group of four consecutive rows of a column two
+    positions (one of the six pairs, uniform) hold codes uniform on 0..15 and
+    the other two hold 8 (a zero weight); scales as ``make_weights``.  Returns
+    dense q uint8[K][N] and s float16[K/G][N]."""
+    G = effective_group(K, groupsize)
+    if G <= 0 or K % G or K % 4:
+        raise ValueError("K must be a positive multiple of the group size and of 4")
+    rng = _rng(seed, 5)
+    pairs = np.array([(0, 1), (0, 2), (0, 3), (1, 2), (1, 3), (2, 3)])
+    choice = pairs[rng.integers(0, 6, size=(K // 4, N))]          # [K/4][N][2]
+    vals = rng.integers(0, 16, size=(K // 4, N, 2), dtype=np.uint8)
+    q = np.full((K // 4, 4, N), 8, dtype=np.uint8)
+    gi, ni = np.meshgrid(np.arange(K // 4), np.arange(N), indexing="ij")
+    for j in range(2):
+        q[gi, choice[:, :, j], ni] = vals[:, :, j]
+    s = rng.uniform(0.002, 0.02, size=(K // G, N)).astype(np.float16)
+    return q.reshape(K, N), s

@@ -30,6 +30,9 @@ from .w4a16_oracle import (  # noqa: F401
     quantize_zp,
     minmax_scales,
     moe_gemm_ref,
+    sparse24_compress,
+    sparse24_expand,
+    gemm24_ref,
     check_expert_offsets,
     dequant_exact_zp,
     dequant_fp16_bits_zp,

@@ -11,7 +11,8 @@ Sources (page title, section):
        scale per column or per G consecutive weights of a column) and its
        paragraph "Bound By Weight Loading" (memory/FLOP counts); Section 2.2
        "Mixed-Precision Inference on LLMs", paragraph "Weight Quantization"
-       (the min-max rule for the step and the zero).
+       (the min-max rule for the step and the zero); Section 2.1.1 "Modern
+       Tensor Core Units" (the 2:4 sparse format: values plus positions).
   [P2] "Marlin 完全拆解：4-bit 权重如何喂满 GPU Tensor Core" (the Marlin
        deep-dive article), section "Marlin 要解决的精确问题" (the affine
        dequantisation B^[k,n] = s[g,n] (q[k,n] - z[g,n]), q in {0..15}),
@@ -20,7 +21,8 @@ Sources (page title, section):
        AB = (AQ) diag(s)), and section "量化数据如何进入 Tensor Core" (the
        symmetric zero point 8 folded into the decode), and section
        "适用边界与工程陷阱" (MoE layers: one GEMM per expert on the rows
-       routed to it).
+       routed to it), and section "Sparse-Marlin 再叠加 2:4 结构化稀疏"
+       (2:4 sparse weights: 4-bit kept values plus 2-bit positions).
 
 Readings taken where the pages are silent (each also listed in the design notes):
   * zero point: the symmetric main path uses the constant z = 8; no zero tensor;
@@ -315,6 +317,74 @@ def quantize(w, s, G: int) -> np.ndarray:
         raise ValueError("w / s is NaN or infinite (zero, NaN or infinite input)")
     q = np.clip(np.rint(quot).astype(np.float64) + Z_POINT, 0, 15)
     return q.astype(np.uint8)
+
+
+# ---------------------------------------------------------------------------
+# 2:4 structured sparsity ([P1] Section 2.1.1 "Modern Tensor Core Units": the
+# 2:4 format splits the sparse operand into vectors of four along the reduction
+# dimension, keeps two values of each and stores them with a metadata
+# structure giving each kept value's position inside its group of four;
+# [P2] section "Sparse-Marlin 再叠加 2:4 结构化稀疏": the kept weights stay
+# 4-bit codes, the positions are 2-bit metadata)
+# ---------------------------------------------------------------------------
+
+def sparse24_compress(q):
+    """Dense codes uint8[K][N] with at most two codes != 8 (the zero weight) in
+    every group of four consecutive rows of a column -> (qc uint8[K/2][N],
+    idx uint8[K/2][N]): kept entry j (0, 1) of group i of column n is row
+    2i + j, holding the code qc and its position idx in 0..3 inside the group.
+
+    Readings taken: a pruned weight is the code 8 (B^ = 0); the kept positions
+    are those of the codes != 8 in increasing order, and a group with fewer
+    than two such codes is filled up with its lowest remaining positions, then
+    the two positions are sorted (so idx0 < idx1 always).
+    """
+    q = np.asarray(q)
+    if q.ndim != 2 or q.shape[0] % 4:
+        raise ValueError("codes must be uint8[K][N] with K a multiple of 4")
+    K, N = q.shape
+    if q.min(initial=0) < 0 or q.max(initial=0) > 15:
+        raise ValueError("codes must lie in 0..15")
+    qc = np.empty((K // 2, N), dtype=np.uint8)
+    idx = np.empty((K // 2, N), dtype=np.uint8)
+    for i in range(K // 4):
+        grp = q[4 * i:4 * i + 4, :]
+        for n in range(N):
+            nz = [p for p in range(4) if grp[p, n] != Z_POINT]
+            if len(nz) > 2:
+                raise ValueError(f"group {i} of column {n} has {len(nz)} non-zero weights (2:4 allows 2)")
+            for p in range(4):
+                if len(nz) == 2:
+                    break
+                if p not in nz:
+                    nz.append(p)
+            nz.sort()
+            for j in range(2):
+                qc[2 * i + j, n] = grp[nz[j], n]
+                idx[2 * i + j, n] = nz[j]
+    return qc, idx
+
+
+def sparse24_expand(qc, idx):
+    """Inverse of ``sparse24_compress``: dense codes with 8 at every pruned position."""
+    qc = np.asarray(qc)
+    idx = np.asarray(idx)
+    K2, N = qc.shape
+    if idx.shape != (K2, N) or K2 % 2:
+        raise ValueError("qc and idx must both be uint8[K/2][N]")
+    if np.any(idx[0::2] >= idx[1::2]) or idx.max(initial=0) > 3:
+        raise ValueError("the two positions of a group must rise inside 0..3")
+    q = np.full((2 * K2, N), Z_POINT, dtype=np.uint8)
+    cols = np.arange(N)
+    for j in range(K2):
+        q[4 * (j // 2) + idx[j].astype(np.int64), cols] = qc[j]
+    return q
+
+
+def gemm24_ref(A, qc, idx, s, G: int):
+    """The 2:4-sparse layer's product: the dense product ``gemm_ref`` of the expanded codes
+    (pruned weights are exact zeros)."""
+    return gemm_ref(A, sparse24_expand(qc, idx), s, G)
 
 
 # ---------------------------------------------------------------------------

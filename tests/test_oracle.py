@@ -733,3 +733,54 @@ def test_moe_gemm_rejects_bad_offsets():
     for off in ([1, 2, 4], [0, 3, 2], [0, 2, 5], [0, 4]):
         with pytest.raises(ValueError):
             oracle.moe_gemm_ref(A, off, q, s, G)
+
+
+# ---------------------------------------------------------------------------
+# 2:4 structured sparsity
+# ---------------------------------------------------------------------------
+
+def test_sparse24_compress_keeps_the_nonzero_positions_in_order():
+    q = np.full((8, 3), 8, np.uint8)
+    q[0:4, 0] = [3, 8, 8, 12]       # positions 0 and 3
+    q[4:8, 0] = [8, 5, 8, 8]        # one non-zero at 1: filled up with 0 -> (0, 1)
+    q[0:4, 1] = [8, 8, 8, 8]        # none: (0, 1)
+    q[4:8, 1] = [8, 8, 9, 1]        # (2, 3)
+    q[0:4, 2] = [8, 8, 0, 8]        # one at 2: filled with 0 -> (0, 2)
+    q[4:8, 2] = [15, 8, 8, 8]       # one at 0: filled with 1 -> (0, 1)
+    qc, idx = oracle.sparse24_compress(q)
+    assert idx[:, 0].tolist() == [0, 3, 0, 1] and qc[:, 0].tolist() == [3, 12, 8, 5]
+    assert idx[:, 1].tolist() == [0, 1, 2, 3] and qc[:, 1].tolist() == [8, 8, 9, 1]
+    assert idx[:, 2].tolist() == [0, 2, 0, 1] and qc[:, 2].tolist() == [8, 0, 15, 8]
+
+
+def test_sparse24_round_trip_and_structure():
+    q, _ = synth.make_weights_24(256, 64, 128, seed=41)
+    # the generator's structure: at most two codes != 8 in every group of four
+    assert np.all((q.reshape(64, 4, 64) != 8).sum(axis=1) <= 2)
+    qc, idx = oracle.sparse24_compress(q)
+    assert np.all(idx[0::2] < idx[1::2]) and idx.max() <= 3
+    assert np.array_equal(oracle.sparse24_expand(qc, idx), q)
+
+
+def test_sparse24_rejects_three_nonzeros_and_bad_positions():
+    q = np.full((4, 1), 8, np.uint8)
+    q[:3, 0] = [1, 2, 3]
+    with pytest.raises(ValueError):
+        oracle.sparse24_compress(q)
+    with pytest.raises(ValueError):
+        oracle.sparse24_expand(np.zeros((2, 1), np.uint8), np.array([[2], [1]], np.uint8))
+
+
+def test_gemm24_integer_brute_force_over_kept_entries():
+    """C = sum over groups and kept entries of A[m, 4i + idx] (qc - 8): the sparse sum written out,
+    against the oracle's dense product of the expanded codes (pins the position arithmetic)."""
+    rng = np.random.default_rng(42)
+    M, K, N, G = 3, 128, 8, 128
+    q, _ = synth.make_weights_24(K, N, G, seed=43)
+    qc, idx = oracle.sparse24_compress(q)
+    Ai = rng.integers(-4, 5, (M, K))
+    C, _ = oracle.gemm24_ref(Ai.astype(np.float16), qc, idx, np.ones((1, N), np.float16), G)
+    for m in range(M):
+        for n in range(N):
+            want = sum(int(Ai[m, 4 * (j // 2) + int(idx[j, n])]) * (int(qc[j, n]) - 8) for j in range(K // 2))
+            assert C[m, n] == want, (m, n)
