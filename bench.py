@@ -104,6 +104,7 @@ def parse_args():
     ap.add_argument("--no-offline", action="store_true", help="skip timing the offline repack / quantise steps")
     ap.add_argument("--no-moe", action="store_true", help="skip the grouped expert (MoE) GEMM sweep")
     ap.add_argument("--no-ablation", action="store_true", help="skip the Figure 12 ablation sweep")
+    ap.add_argument("--no-sparse", action="store_true", help="skip the 2:4-sparse GEMM sweep")
     ap.add_argument("--zero-points", action="store_true",
                     help="run every GEMM with a zero point per group and a bias (w4a16_gemm_zp)")
     ap.add_argument("--cpu-sample", default=None, help=argparse.SUPPRESS)  # internal: oracle timing child
@@ -521,6 +522,9 @@ def run_ours(args, rank, world, device):
     ablation = None
     if rank == 0 and not args.no_ablation and args.workload == "big" and not args.zero_points:
         ablation = time_ablations(w, torch, points, ws, max_ws, stream)
+    sparse24 = None
+    if rank == 0 and not args.no_sparse and args.workload == "big" and not args.zero_points:
+        sparse24 = time_sparse24(w, torch, device, peaks, {r["M"]: r["us"] for r in sweep})
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -541,8 +545,65 @@ def run_ours(args, rank, world, device):
         "sweep": sweep, "roofline": roofline, "roofline_by_kernel": roofline_by_kernel,
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "clocks": clocks, "offline": offline,
-        "moe": moe, "ablation": ablation,
+        "moe": moe, "ablation": ablation, "sparse24": sparse24,
     }
+
+
+def gemm24_bytes(M, K, N, G):
+    """Algorithmic bytes of the 2:4-sparse GEMM: 3 bits per weight (two 4-bit codes and two
+    2-bit positions per group of four) instead of 4."""
+    G = K if G in (-1, K) else G
+    return 2 * M * K + 3 * K * N // 8 + 2 * (K // G) * N + 2 * M * N
+
+
+def time_sparse24(w, torch, device, peaks, dense_us):
+    """2:4-sparse GEMM on the big layer (outside the timed region): the packed stream is random
+    codes with random rising position pairs (each of the six pairs equally likely), generated on
+    the device; the weights (510 MB) exceed L2.  Compared with the dense GEMM of the sweep at the
+    same M."""
+    K, N, G = 18432, 73728, 128
+    gen = torch.Generator(device=device)
+    gen.manual_seed(13)
+    packed = torch.randint(-2 ** 31, 2 ** 31, (3 * K * N // 32,), dtype=torch.int32, device=device, generator=gen)
+    pieces = packed.view(-1, 768)                       # per 128-column strip and 64-row piece
+    lut = torch.tensor([4, 8, 12, 9, 13, 14], dtype=torch.int64, device=device)  # rising pairs (i0 | i1 << 2)
+    shifts = 4 * torch.arange(8, device=device, dtype=torch.int64)
+    for c0 in range(0, pieces.shape[0], 16384):
+        blk = pieces[c0:c0 + 16384]
+        nib = lut[torch.randint(0, 6, (blk.shape[0], 256, 8), device=device, generator=gen)]
+        meta = (nib << shifts).sum(-1)
+        blk[:, 512:] = torch.where(meta >= 2 ** 31, meta - 2 ** 32, meta).to(torch.int32)
+    del nib, meta
+    sp = (torch.rand(K // G * N, device=device, generator=gen) * 0.018 + 0.002).to(torch.float16)
+    out = []
+    for M in (1, 8, 16):
+        A_d = torch.randn(M, K, device=device, generator=gen).to(torch.float16)
+        C_d = torch.empty((M, N), dtype=torch.float16, device=device)
+        ws = torch.zeros(w.w4a16_workspace_bytes_24(M, K, N, G), dtype=torch.uint8, device=device)
+        for _ in range(3):
+            w.w4a16_gemm_24(A_d, packed, sp, C_d, M, K, N, G, ws)
+        times = []
+        for _ in range(20):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            w.w4a16_gemm_24(A_d, packed, sp, C_d, M, K, N, G, ws)
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3)
+        us = statistics.median(times)
+        nbytes = gemm24_bytes(M, K, N, G)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        entry = {"M": M, "K": K, "N": N, "group": G, "us": round(us, 1), "bytes": nbytes, "gb_s": round(gbs, 1),
+                 "roofline_frac": round(gbs / peaks["hbm_gbs"], 3)}
+        if M in dense_us:
+            entry["dense_us"] = dense_us[M]
+            entry["speedup_vs_dense"] = round(dense_us[M] / us, 3)
+        out.append(entry)
+        if w.w4a16_get_status(ws) != 0:
+            raise RuntimeError("device status error in the 2:4 sweep")
+    del packed, sp
+    return out
 
 
 ABLATIONS = [("full design", 0), ("no evict-first on weights", 1), ("2 pipeline stages", 2),

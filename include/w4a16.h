@@ -229,6 +229,53 @@ W4A16_API int w4a16_dequant_zp(const uint32_t* packed, const uint16_t* scales_p,
                                int N, int groupsize, uint16_t* Bhat, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * 2:4-sparse W4A16 (the Sparse-Marlin analogue).  The MARLIN paper, Section
+ * 2.1.1 "Modern Tensor Core Units", describes the 2:4 format: in every vector
+ * of four along the reduction dimension two values are kept, with metadata
+ * giving their positions; the deep-dive article, section "Sparse-Marlin 再叠加
+ * 2:4 结构化稀疏", keeps them as 4-bit codes with 2-bit positions.  Here a
+ * pruned weight is the code 8 (B^ = 0), and a layer is 2:4 sparse when every
+ * group of four consecutive rows k = 4i .. 4i + 3 of every column holds at
+ * most two codes != 8.  Its product is the dense one of those codes:
+ * C = A * B^ exactly as for w4a16_gemm.  Shapes and groups as for w4a16_gemm.
+ *
+ * w4a16_packed24_bytes: bytes of the packed 2:4 stream, 3 K N / 8 (3 bits per
+ * weight: two 4-bit codes and two 2-bit positions per group of four).
+ *
+ * w4a16_repack_24: dense codes q uint8[K][N] (2:4 as above) and scales
+ * s fp16[K/G][N] -> packed24 (uint32[3 K N / 32], this library's layout:
+ * per 128-column strip and 64-row piece, 2048 bytes of codes then 1024 bytes
+ * of positions in the lane order of the sparse tensor-core instruction) and
+ * scales_p (permuted exactly as by w4a16_repack).  The kept positions of a
+ * group are those of its codes != 8, filled up with its lowest other
+ * positions.  A group with three or more codes != 8 flags W4A16_ERR_VALUE for
+ * w4a16_get_status(NULL, stream) (its stored entries are then unspecified).
+ *
+ * w4a16_unpack_24: packed24 -> dense codes q uint8[K][N] (8 at pruned
+ * positions); positions that are not a rising pair flag W4A16_ERR_VALUE.
+ * It checks a stream of unknown origin before w4a16_gemm_24 reads it.
+ *
+ * w4a16_gemm_24: C fp16[M][N] = A fp16[M][K] * B^ from packed24 and
+ * scales_p, computed with the sparse tensor-core MMA; any M >= 0 (16 token
+ * rows per launch).  packed24 must come from w4a16_repack_24 (or have passed
+ * w4a16_unpack_24 without an error): its positions feed the tensor cores'
+ * metadata operand, which requires rising pairs.  The workspace (size from
+ * w4a16_workspace_bytes_24) follows the rules of w4a16_gemm's.
+ * ------------------------------------------------------------------------- */
+W4A16_API size_t w4a16_packed24_bytes(int K, int N);
+
+W4A16_API int w4a16_repack_24(const uint8_t* q, const uint16_t* s, int K, int N, int groupsize, uint32_t* packed24,
+                              uint16_t* scales_p, void* stream);
+
+W4A16_API int w4a16_unpack_24(const uint32_t* packed24, int K, int N, uint8_t* q, void* stream);
+
+W4A16_API size_t w4a16_workspace_bytes_24(int M, int K, int N, int groupsize);
+
+W4A16_API int w4a16_gemm_24(const uint16_t* A, const uint32_t* packed24, const uint16_t* scales_p, uint16_t* C,
+                            int M, int K, int N, int groupsize, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/* ---------------------------------------------------------------------------
  * Grouped expert GEMM (MoE).  The deep-dive article, section "适用边界与工程
  * 陷阱" (items 1 and 4), notes that an MoE layer regroups the tokens by
  * expert, so every expert's GEMM has its own small M, and that the grouped

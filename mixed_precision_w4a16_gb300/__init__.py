@@ -20,10 +20,11 @@ __all__ = [
     "w4a16_get_status", "w4a16_repack_zeros", "w4a16_gemm_zp", "w4a16_dequant_zp", "w4a16_quantize_repack_zp",
     "w4a16_minmax_scales", "w4a16_moe_workspace_bytes", "w4a16_moe_gemm", "w4a16_debug_ablate",
     "ABLATE_NO_EVICT_FIRST", "ABLATE_STAGES_2", "ABLATE_NO_SWIZZLE",
+    "w4a16_packed24_bytes", "w4a16_repack_24", "w4a16_unpack_24", "w4a16_workspace_bytes_24", "w4a16_gemm_24",
     "w4a16_debug_set_wait_cycles", "w4a16_debug_inject_stall", "w4a16_debug_force_path", "w4a16_status_string",
     "EXPORTED_SYMBOLS",
     "repack", "quantize_repack", "unpack", "dequant", "gemm", "workspace_for", "repack_zeros", "gemm_zp",
-    "dequant_zp", "minmax_scales", "moe_gemm", "moe_workspace_for",
+    "dequant_zp", "minmax_scales", "moe_gemm", "moe_workspace_for", "repack_24", "unpack_24", "gemm_24",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -36,6 +37,7 @@ EXPORTED_SYMBOLS = (
     "w4a16_gemm_noalloc", "w4a16_debug_force_path", "w4a16_quantize_repack", "w4a16_repack_zeros",
     "w4a16_gemm_zp", "w4a16_dequant_zp", "w4a16_quantize_repack_zp", "w4a16_minmax_scales",
     "w4a16_moe_workspace_bytes", "w4a16_moe_gemm", "w4a16_debug_ablate",
+    "w4a16_packed24_bytes", "w4a16_repack_24", "w4a16_unpack_24", "w4a16_workspace_bytes_24", "w4a16_gemm_24",
 )
 
 
@@ -78,6 +80,11 @@ def _load():
         "w4a16_gemm_noalloc": (i, [vp, vp, vp, vp, i, i, i, i, vp]),
         "w4a16_debug_force_path": (None, [i]),
         "w4a16_debug_ablate": (None, [i]),
+        "w4a16_packed24_bytes": (sz, [i, i]),
+        "w4a16_repack_24": (i, [vp, vp, i, i, i, vp, vp, vp]),
+        "w4a16_unpack_24": (i, [vp, i, i, vp, vp]),
+        "w4a16_workspace_bytes_24": (sz, [i, i, i, i]),
+        "w4a16_gemm_24": (i, [vp, vp, vp, vp, i, i, i, i, vp, sz, vp]),
         "w4a16_quantize_repack": (i, [vp, vp, i, i, i, vp, vp, vp]),
         "w4a16_repack_zeros": (i, [vp, i, i, i, vp, vp]),
         "w4a16_gemm_zp": (i, [vp, vp, vp, vp, vp, vp, i, i, i, i, vp, sz, vp]),
@@ -199,6 +206,30 @@ def w4a16_moe_gemm(A, packed, scales_p, expert_offsets, C, E, M, max_rows, K, N,
     _check(_lib().w4a16_moe_gemm(_ptr(A), _ptr(packed), _ptr(scales_p), _ptr(expert_offsets), _ptr(C), E, M,
                                  max_rows, K, N, groupsize, _ptr(workspace), int(workspace_bytes),
                                  _stream(stream)), "w4a16_moe_gemm")
+
+
+def w4a16_packed24_bytes(K, N) -> int:
+    return int(_lib().w4a16_packed24_bytes(K, N))
+
+
+def w4a16_repack_24(q, s, K, N, groupsize, packed24, scales_p, stream=None):
+    _check(_lib().w4a16_repack_24(_ptr(q), _ptr(s), K, N, groupsize, _ptr(packed24), _ptr(scales_p),
+                                  _stream(stream)), "w4a16_repack_24")
+
+
+def w4a16_unpack_24(packed24, K, N, q, stream=None):
+    _check(_lib().w4a16_unpack_24(_ptr(packed24), K, N, _ptr(q), _stream(stream)), "w4a16_unpack_24")
+
+
+def w4a16_workspace_bytes_24(M, K, N, groupsize) -> int:
+    return int(_lib().w4a16_workspace_bytes_24(M, K, N, groupsize))
+
+
+def w4a16_gemm_24(A, packed24, scales_p, C, M, K, N, groupsize, workspace, workspace_bytes=None, stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib().w4a16_gemm_24(_ptr(A), _ptr(packed24), _ptr(scales_p), _ptr(C), M, K, N, groupsize,
+                                _ptr(workspace), int(workspace_bytes), _stream(stream)), "w4a16_gemm_24")
 
 
 def w4a16_unpack(packed, scales_p, K, N, groupsize, q, s, stream=None):
@@ -396,4 +427,36 @@ def moe_gemm(A, packed, scales_p, expert_offsets, N: int, groupsize: int, max_ro
     C = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=A.device)
     w4a16_moe_gemm(A, packed, scales_p, expert_offsets, C, E, M, max_rows, K, N, groupsize, workspace, None,
                    stream)
+    return C
+
+
+def repack_24(q, s, groupsize: int, stream=None):
+    """2:4-sparse dense codes q uint8[K][N], s fp16[K/G][N] (CUDA tensors) -> (packed24 int32[3*K*N/32],
+    permuted scales fp16[K/G*N])."""
+    import torch
+    K, N = q.shape
+    packed = torch.empty(3 * K * N // 32, dtype=torch.int32, device=q.device)
+    sp = torch.empty(s.numel(), dtype=torch.float16, device=q.device)
+    w4a16_repack_24(q, s, K, N, groupsize, packed, sp, stream)
+    return packed, sp
+
+
+def unpack_24(packed24, K: int, N: int, stream=None):
+    import torch
+    q = torch.empty((K, N), dtype=torch.uint8, device=packed24.device)
+    w4a16_unpack_24(packed24, K, N, q, stream)
+    return q
+
+
+def gemm_24(A, packed24, scales_p, N: int, groupsize: int, workspace=None, out=None, stream=None):
+    """C fp16[M][N] = A fp16[M][K] * dequant of the 2:4-sparse packed24."""
+    import torch
+    M, K = A.shape
+    if workspace is None:
+        nbytes = w4a16_workspace_bytes_24(M, K, N, groupsize)
+        if nbytes == 0:
+            raise W4A16Error(2, "w4a16_workspace_bytes_24")
+        workspace = torch.zeros(nbytes, dtype=torch.uint8, device=A.device)
+    C = out if out is not None else torch.empty((M, N), dtype=torch.float16, device=A.device)
+    w4a16_gemm_24(A, packed24, scales_p, C, M, K, N, groupsize, workspace, None, stream)
     return C

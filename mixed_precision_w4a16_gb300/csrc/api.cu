@@ -9,6 +9,7 @@
 
 #include "../../include/w4a16.h"
 #include "internal.h"
+#include "sparse24.h"
 
 namespace {
 
@@ -382,6 +383,87 @@ int w4a16_moe_gemm(const uint16_t* A, const uint32_t* packed, const uint16_t* sc
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
+// 2:4-sparse W4A16
+// ---------------------------------------------------------------------------
+extern "C" {
+
+size_t w4a16_packed24_bytes(int K, int N) {
+  if (K <= 0 || N <= 0 || K % 128 != 0 || N % 128 != 0) return 0;
+  return static_cast<size_t>(K) * static_cast<size_t>(N) * 3 / 8;
+}
+
+int w4a16_repack_24(const uint8_t* q, const uint16_t* s, int K, int N, int groupsize, uint32_t* packed24,
+                    uint16_t* scales_p, void* stream) {
+  const int st = check_shape(K, N, groupsize);
+  if (st != W4A16_OK) return st;
+  if (!q || !s || !packed24 || !scales_p) return W4A16_ERR_NULL;
+  if (!aligned16(q) || !aligned16(s) || !aligned16(packed24) || !aligned16(scales_p)) return W4A16_ERR_ALIGN;
+  DeviceInfo* d = nullptr;
+  const int r = current_device_info(&d);
+  if (r != W4A16_OK) return r;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (launch_repack24(q, K, N, packed24, cs) != cudaSuccess) return W4A16_ERR_CUDA;
+  return launch_permute_scales(s, K, N, effective_group(K, groupsize), scales_p, cs) == cudaSuccess
+             ? W4A16_OK
+             : W4A16_ERR_CUDA;
+}
+
+int w4a16_unpack_24(const uint32_t* packed24, int K, int N, uint8_t* q, void* stream) {
+  if (K <= 0 || N <= 0 || K % 128 != 0 || N % 128 != 0) return W4A16_ERR_SHAPE;
+  if (!packed24 || !q) return W4A16_ERR_NULL;
+  if (!aligned16(packed24) || !aligned16(q)) return W4A16_ERR_ALIGN;
+  DeviceInfo* d = nullptr;
+  const int r = current_device_info(&d);
+  if (r != W4A16_OK) return r;
+  return launch_unpack24(packed24, K, N, q, static_cast<cudaStream_t>(stream)) == cudaSuccess ? W4A16_OK
+                                                                                              : W4A16_ERR_CUDA;
+}
+
+size_t w4a16_workspace_bytes_24(int M, int K, int N, int groupsize) {
+  if (M < 0 || check_shape(K, N, groupsize) != W4A16_OK) return 0;
+  DeviceInfo* d = nullptr;
+  if (current_device_info(&d) != W4A16_OK) return 0;
+  return make_plan24(M, K, N, effective_group(K, groupsize), d->sms, d->smem_optin, 0).workspace;
+}
+
+int w4a16_gemm_24(const uint16_t* A, const uint32_t* packed24, const uint16_t* scales_p, uint16_t* C, int M, int K,
+                  int N, int groupsize, void* workspace, size_t workspace_bytes, void* stream) {
+  if (M < 0) return W4A16_ERR_SHAPE;
+  const int st = check_shape(K, N, groupsize);
+  if (st != W4A16_OK) return st;
+  if (M == 0) return W4A16_OK;
+  if (!A || !packed24 || !scales_p || !C) return W4A16_ERR_NULL;
+  if (!workspace) return W4A16_ERR_WORKSPACE;
+  if (!aligned16(A) || !aligned16(packed24) || !aligned16(scales_p) || !aligned16(C) || !aligned16(workspace))
+    return W4A16_ERR_ALIGN;
+  DeviceInfo* d = nullptr;
+  const int r = current_device_info(&d);
+  if (r != W4A16_OK) return r;
+  const int G = effective_group(K, groupsize);
+  const int ablate = g_ablate.load();
+  const Plan24 pl = make_plan24(M, K, N, G, d->sms, d->smem_optin, ablate);
+  if (workspace_bytes < pl.workspace) return W4A16_ERR_WORKSPACE;
+  const long long wc = g_wait_cycles.load();
+  GemmCall c{};
+  c.A = A;
+  c.packed = packed24;
+  c.scales = scales_p;
+  c.C = C;
+  c.M = M;
+  c.K = K;
+  c.N = N;
+  c.G = G;
+  c.workspace = workspace;
+  c.wait_limit = wc > 0 ? wc : kDefaultWaitCycles;
+  c.debug_stall = g_stall.load();
+  c.ablate = ablate;
+  c.stream = static_cast<cudaStream_t>(stream);
+  return run_gemm24(pl, c);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
 // Allocation-free variant: the scratch is a file-scope device array of the
 // library, looked up once per device with cudaGetSymbolAddress.
 // ---------------------------------------------------------------------------
@@ -423,8 +505,10 @@ int w4a16_gemm_noalloc(const uint16_t* A, const uint32_t* packed, const uint16_t
 int w4a16_get_status(void* workspace, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return W4A16_ERR_CUDA;
-  unsigned int flag = 0;
+  unsigned int flag = 0, flag24 = 0;
   if (read_and_clear_repack_flag(&flag, s) != cudaSuccess) return W4A16_ERR_CUDA;
+  if (read_and_clear_sparse_flag(&flag24, s) != cudaSuccess) return W4A16_ERR_CUDA;
+  flag |= flag24;
   uint32_t word = 0;
   if (workspace) {
     if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)

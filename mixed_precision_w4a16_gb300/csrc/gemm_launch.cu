@@ -182,10 +182,12 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
   return fn;
 }
 
+}  // namespace
+
 // 3-D view of A (fp16[M][K]) as [K/64][M][64]: box {64, box_rows, kq} fetches the
 // kq 64-column pieces of one work unit in one copy, each piece box_rows x 128 bytes
-// with the 128-byte swizzle; rows beyond M are zero-filled.
-int encode_a_map(CUtensorMap* map, const uint16_t* A, int M, int K, int box_rows, int kq, bool swizzle = true) {
+// (128-byte swizzle unless the no-swizzle ablation asks otherwise); rows beyond M are zero-filled.
+int encode_a_map(CUtensorMap* map, const uint16_t* A, int M, int K, int box_rows, int kq, bool swizzle) {
   auto enc = get_encoder();
   if (!enc) return W4A16_ERR_CUDA;
   const cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
@@ -197,8 +199,6 @@ int encode_a_map(CUtensorMap* map, const uint16_t* A, int M, int K, int box_rows
                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? W4A16_OK : W4A16_ERR_CUDA;
 }
-
-}  // namespace
 
 Plan make_plan_moe(int E, int M, int max_rows, int K, int N, int G, int sms, int smem_optin, int ablate) {
   // experts that can own rows, and the row segments (8 * m_tiles rows of one expert) they can need

@@ -157,6 +157,11 @@ struct Plan {
   size_t workspace;
 };
 
+// Tensor map of the activations A fp16[M][K] viewed as [K/64][M][64]: box {64, box_rows, kq}
+// fetches kq 64-column pieces of box_rows rows (128-byte swizzle unless `swizzle` is false);
+// rows beyond M read as zero.
+int encode_a_map(CUtensorMap* map, const uint16_t* A, int M, int K, int box_rows, int kq, bool swizzle = true);
+
 // forced_path: 0 = by M, 1 = streaming kernel, 2 = tensor-memory kernel; zp: the GEMM reads
 // zero points (their rows take shared-memory stage space next to the scales)
 Plan make_plan(int M, int K, int N, int G, int sms, int smem_optin, bool zp, int forced_path, int ablate = 0);

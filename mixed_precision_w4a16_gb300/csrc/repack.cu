@@ -21,6 +21,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "sparse24.h"
 
 namespace w4a16 {
 
@@ -304,6 +305,12 @@ cudaError_t launch_minmax_scales(const uint16_t* w, int K, int N, int G, uint16_
                                  cudaStream_t stream) {
   const dim3 grid(grid_for(N / 2, 256), static_cast<unsigned>(K / G));
   minmax_scales_kernel<<<grid, 256, 0, stream>>>(w, N, G, s, z);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_scales(const uint16_t* s, int K, int N, int G, uint16_t* scales_p, cudaStream_t stream) {
+  const long long ns = static_cast<long long>(K / G) * N;
+  permute_scales_kernel<<<grid_for(ns, 256), 256, 0, stream>>>(s, scales_p, N, K / G, ns, 0);
   return cudaGetLastError();
 }
 
