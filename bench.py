@@ -8,7 +8,7 @@ M).  The packed weights (679 MB) exceed the 129 MB L2, so every GEMM streams
 its weights from HBM without any flush.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload big|pr1|7b|70b|prefill|profile_m32|profile_m8]
+                    [--workload big|pr1|7b|70b|prefill|profile_m32|profile_m8|profile_m16]
 
 Prints one JSON line (rank 0).  ``value`` is the whole-job throughput in TB/s
 of algorithmic bytes (2MK + 0.5KN + 2(K/G)N + 2MN per GEMM) over the timed
@@ -53,6 +53,7 @@ WORKLOADS = {
     # small cases of the big layer's kernels for full ncu captures (weights still larger than L2)
     "profile_m32": ("profiling case M=32 K=18432 N=16384 group 128", [(18432, 16384, 128, [32])], 2),
     "profile_m8": ("profiling case M=8 K=18432 N=16384 group 128", [(18432, 16384, 128, [8])], 2),
+    "profile_m16": ("profiling case M=16 K=18432 N=16384 group 128", [(18432, 16384, 128, [16])], 2),
 }
 
 # grouped expert GEMM sweep: (description, experts, top-k, K, N, groupsize, [tokens ...])
@@ -105,6 +106,9 @@ def parse_args():
     ap.add_argument("--no-moe", action="store_true", help="skip the grouped expert (MoE) GEMM sweep")
     ap.add_argument("--no-ablation", action="store_true", help="skip the Figure 12 ablation sweep")
     ap.add_argument("--no-sparse", action="store_true", help="skip the 2:4-sparse GEMM sweep")
+    ap.add_argument("--moe-config", type=int, default=None, help="run only this entry of the MoE sweep (profiling)")
+    ap.add_argument("--no-per-expert", action="store_true",
+                    help="skip the one-launch-per-expert comparison of the MoE sweep (profiling)")
     ap.add_argument("--zero-points", action="store_true",
                     help="run every GEMM with a zero point per group and a bias (w4a16_gemm_zp)")
     ap.add_argument("--cpu-sample", default=None, help=argparse.SUPPRESS)  # internal: oracle timing child
@@ -158,7 +162,7 @@ def workload_totals(layers):
 def cpu_sample_cols(workload):
     """Columns of each GEMM the oracle computes for the cpu_baseline leg (~10-20 s single-threaded)."""
     return {"big": 12288, "pr1": 1024, "7b": 16384, "70b": 8192, "prefill": 2048,
-            "profile_m32": 4096, "profile_m8": 4096}[workload]
+            "profile_m32": 4096, "profile_m8": 4096, "profile_m16": 4096}[workload]
 
 
 # the files that decide what the GEMM kernels execute and how the work is split
@@ -518,7 +522,7 @@ def run_ours(args, rank, world, device):
 
     moe = None
     if rank == 0 and not args.no_moe and args.workload == "big":
-        moe = time_moe(w, torch, device, peaks)
+        moe = time_moe(w, torch, device, peaks, args.moe_config, not args.no_per_expert)
     ablation = None
     if rank == 0 and not args.no_ablation and args.workload == "big" and not args.zero_points:
         ablation = time_ablations(w, torch, points, ws, max_ws, stream)
@@ -643,7 +647,7 @@ def time_ablations(w, torch, points, ws, max_ws, stream):
     return out
 
 
-def time_moe(w, torch, device, peaks):
+def time_moe(w, torch, device, peaks, only_config=None, per_expert_context=True):
     """Grouped expert GEMM (outside the timed region): one w4a16_moe_gemm over every expert of an
     MoE layer, for routed batches of a few sizes.  The weights are random packed words (random
     4-bit codes) and scales generated on the device; each timed call follows an L2 flush.  Bytes
@@ -656,6 +660,8 @@ def time_moe(w, torch, device, peaks):
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
     out = []
     for ci, (desc, E, topk, K, N, G, token_list) in enumerate(MOE_CONFIGS):
+        if only_config is not None and ci != only_config:
+            continue
         NG = K // synth.effective_group(K, G)
         wpe, spe = K * N // 8, NG * N
         packed = torch.randint(-2 ** 31, 2 ** 31, (E * wpe,), dtype=torch.int32, device=device, generator=gen)
@@ -682,8 +688,10 @@ def time_moe(w, torch, device, peaks):
                     w.w4a16_gemm(A_d[lo:hi], packed[e * wpe:(e + 1) * wpe], sp[e * spe:(e + 1) * spe], C_d[lo:hi],
                                  hi - lo, K, N, G, dense_ws)
 
-            res = {}
+            res = {"per_expert": None}
             for name, fn in (("grouped", grouped), ("per_expert", per_expert)):
+                if name == "per_expert" and not per_expert_context:
+                    continue
                 for _ in range(3):
                     fn()
                 times = []
@@ -704,7 +712,7 @@ def time_moe(w, torch, device, peaks):
             out.append({"config": desc, "tokens": tokens, "rows": M, "active_experts": len(active),
                         "max_rows_per_expert": max_rows, "us": round(res["grouped"], 1), "bytes": nbytes,
                         "gb_s": round(gbs, 1), "roofline_frac": round(gbs / peaks["hbm_gbs"], 3),
-                        "per_expert_launches_us": round(res["per_expert"], 1)})
+                        "per_expert_launches_us": None if res["per_expert"] is None else round(res["per_expert"], 1)})
             del A_d, C_d, ws, dense_ws
         del packed, sp
     del flush
