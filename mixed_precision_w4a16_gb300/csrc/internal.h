@@ -86,7 +86,7 @@ cudaError_t launch_moe_mma(const MmaConfig& cfg, const CUtensorMap& tmA, const G
 // with zero points (p.zeros != null) the kernels are built with the per-row zero decode
 
 // ---- tensor-memory (tcgen05) GEMM ----------------------------------------
-constexpr int kTcThreads = 736;  // 3 producers, 4 MMA issuers, 16 dequant warps (two teams)
+constexpr int kTcThreads = 768;  // 3 producers, 4 MMA issuers, 1 idle, 16 dequant warps (two teams)
 constexpr int kTcMaxIssuers = 4;
 
 struct TcLayout {
