@@ -34,14 +34,15 @@ Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin, bool zp,
   const int mc = std::min(std::max(M, 1), 32);
   const int mt = mc <= 8 ? 1 : mc <= 16 ? 2 : 4;
   pl.strips = N / kStrip;
-  // Unit depth KT = 64 * kq.  Per-SM time of a unit is modelled from copy-engine
-  // measurements on GB300: ~89 ns per 4 KB of weights streamed plus ~80 ns of
-  // fixed cost for the unit's three copy operations.  Pick the kq minimising
-  // T * unit time among those that keep >= 3 pipeline stages in shared memory.
+  // Unit depth KT = 64 * kq (kq up to 16: each of the 4 K-split warps takes every
+  // fourth piece).  Per-SM time of a unit is modelled from copy-engine measurements
+  // on GB300: ~89 ns per 4 KB of weights streamed plus ~80 ns of fixed cost for the
+  // unit's three copy operations.  Pick the kq minimising T * unit time among those
+  // that keep >= 3 pipeline stages in shared memory.
   int best_kq = 0;
   long long best_cost = 0;
-  const int cands[3] = {8, 4, 2};
-  for (int c = 0; c < 3; ++c) {
+  const int cands[5] = {16, 12, 8, 4, 2};
+  for (int c = 0; c < 5; ++c) {
     const int kq = cands[c];
     if (K % (64 * kq) != 0) continue;
     const int srows = (G <= 64 * kq) ? (64 * kq) / G : 1;

@@ -12,7 +12,8 @@
 //    the unit's scale rows (1-D bulk copy); completion is tracked by an
 //    mbarrier transaction count;
 //  * eight consumer warps split each unit 2 ways along the columns (4 blocks
-//    of 16 each) and 4 ways along K (64-row pieces kq0, kq0 + 4, ...); a warp
+//    of 16 each) and 4 ways along K (64-row pieces kq0, kq0 + 4, ...; up to 16
+//    pieces per unit); a warp
 //    loads the activation fragments of its piece once (8-byte shared loads) and reuses
 //    them for its 4 column blocks;
 //  * each 32-bit word decodes to four FP16x2 operand registers (exact LOP3 +
@@ -330,10 +331,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       }
     }
     if (have) {
-      // this warp's pieces kq0, kq0 + 4 of the unit (KQ <= 8), unrolled so the second piece's
+      // this warp's pieces kq0, kq0 + 4, ... of the unit (KQ <= 16), unrolled so the next piece's
       // loads and decode can overlap the first piece's multiply chain
 #pragma unroll
-      for (int pc = 0; pc < 2; ++pc) {
+      for (int pc = 0; pc < 4; ++pc) {
         const int kq = kq0 + 4 * pc;
         if (kq >= KQ) break;
         // activation fragments of this 64-row piece: 4 k16 steps x MT token tiles.  The packed

@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
     if (have) {
 #pragma unroll
-      for (int pc = 0; pc < 2; ++pc) {
+      for (int pc = 0; pc < 4; ++pc) {
         const int kq = kq0 + 4 * pc;
         if (kq >= KQ) break;
         // activations: MMA m (reduction rows 32m .. 32m + 31 of the piece) wants in register q of lane
@@ -528,8 +528,8 @@ Plan24 make_plan24(int M, int K, int N, int G, int sms, int smem_optin, int abla
   // weights per 64-row piece (~67 ns of copy-engine time each, plus ~80 ns per unit).
   int best_kq = 0;
   long long best_cost = 0;
-  const int cands[3] = {8, 4, 2};
-  for (int c = 0; c < 3; ++c) {
+  const int cands[5] = {16, 12, 8, 4, 2};
+  for (int c = 0; c < 5; ++c) {
     const int kq = cands[c];
     if (K % (64 * kq) != 0) continue;
     const int srows = (G <= 64 * kq) ? (64 * kq) / G : 1;
