@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 
   // -------------------------------------------------------------------- consumers
   const int ng = warp >> 2;  // column half: blocks 4*ng .. 4*ng + 3
-  const int kq0 = warp & 3;  // first 64-row piece of each unit (then kq0 + 4)
+  const int kq0 = warp & 3;  // first 64-row piece of each unit (then kq0 + 4, ...)
   const int g = lane >> 2, t = lane & 3;
   const int swz = (p.ablate & kAblateNoSwizzle) ? 0 : g;
   const int first_col = nunits > 0 ? u_begin / p.KU : 0;
