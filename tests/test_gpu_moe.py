@@ -171,3 +171,18 @@ def test_moe_large_layer_sampled_experts(w):
         lo, hi = int(off[e]), int(off[e + 1])
         C_ref, bound = oracle.gemm_ref(lay["A"][lo:hi], lay["q"][e], lay["s"][e], G)
         tl.assert_within_bound(C[lo:hi], C_ref, bound, f"expert {e} rows {lo}..{hi}")
+
+
+@pytest.mark.parametrize("E", [289, 1000, 2048])
+def test_moe_many_experts_exercise_the_multi_expert_scan(w, E):
+    """E > 288 experts: each thread of the prologue's scan owns several experts (up to 8 at the
+    2048 maximum); most own no rows, the rows sit at the first, last and scattered experts."""
+    K, N, G = 256, 128, 128
+    counts = np.zeros(E, dtype=np.int64)
+    for e, c in ((0, 3), (1, 0), (287, 9), (288, 2), (E // 2, 17), (E - 2, 1), (E - 1, 5)):
+        counts[e] = c
+    lay = synth.make_moe_layer(0, 0, E, K, N, G, seed=E, counts=counts)
+    C = _run(w, lay, N, 0)
+    C_ref, bound = oracle.moe_gemm_ref(lay["A"], lay["offsets"], lay["q"], lay["s"], G)
+    tl.assert_within_bound(C, C_ref, bound, f"E={E}")
+    assert w.w4a16_get_status() == 0
