@@ -186,3 +186,27 @@ def test_moe_many_experts_exercise_the_multi_expert_scan(w, E):
     C_ref, bound = oracle.moe_gemm_ref(lay["A"], lay["offsets"], lay["q"], lay["s"], G)
     tl.assert_within_bound(C, C_ref, bound, f"E={E}")
     assert w.w4a16_get_status() == 0
+
+
+def test_moe_timeout_is_reported_and_context_survives(w):
+    torch = tl.torch_mod()
+    K, N, G = 2048, 1024, 128
+    lay = synth.make_moe_layer(16, 2, 8, K, N, G, seed=75)
+    packed, sp = _device_experts(w, lay["q"], lay["s"], G)
+    M = int(lay["offsets"][-1])
+    ws = w.moe_workspace_for(8, M, 8, K, N, G)
+    C = torch.full((M, N), 7.0, dtype=torch.float16, device="cuda")
+    A_d, off_d = tl.to_dev(lay["A"]), tl.to_dev(lay["offsets"])
+    try:
+        w.w4a16_debug_set_wait_cycles(2_000_000)  # about a millisecond
+        w.w4a16_debug_inject_stall(True)
+        w.moe_gemm(A_d, packed, sp, off_d, N, G, max_rows=8, workspace=ws, out=C)
+    finally:
+        w.w4a16_debug_inject_stall(False)
+        w.w4a16_debug_set_wait_cycles(0)
+    assert w.w4a16_get_status(ws) == 7
+    assert bool((C == 7.0).all())
+    ws.zero_()
+    C2 = _run(w, lay, N, 8, packed, sp, ws)
+    C_ref, bound = oracle.moe_gemm_ref(lay["A"], lay["offsets"], lay["q"], lay["s"], G)
+    tl.assert_within_bound(C2, C_ref, bound, "after timeout")

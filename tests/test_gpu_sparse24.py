@@ -132,3 +132,33 @@ def test_gemm24_big_layer_sampled_strips(w):
         cols = slice(128 * j, 128 * (j + 1))
         C_ref, bound = oracle.gemm_ref(A, q[:, cols], s[:, cols], G)
         tl.assert_within_bound(C[:, cols], C_ref, bound, f"strip {j}")
+
+
+def test_gemm24_timeout_is_reported_and_context_survives(w):
+    """Failure injection on the host side of the wait: the first stage of every CTA is never filled,
+    so the consumers' first wait runs out of its short bound; W4A16_ERR_TIMEOUT, nothing written,
+    and the next call on a re-zeroed workspace is correct."""
+    torch = tl.torch_mod()
+    M, K, N, G = 8, 4096, 2048, 128
+    q, s = synth.make_weights_24(K, N, G, seed=61)
+    A = synth.make_activations(M, K, seed=62)
+    packed, sp = _device24(w, q, s, G)
+    A_d = tl.to_dev(A)
+    ws = torch.zeros(w.w4a16_workspace_bytes_24(M, K, N, G), dtype=torch.uint8, device="cuda")
+    C = torch.full((M, N), 7.0, dtype=torch.float16, device="cuda")
+    try:
+        w.w4a16_debug_set_wait_cycles(2_000_000)  # about a millisecond
+        w.w4a16_debug_inject_stall(True)
+        w.w4a16_gemm_24(A_d, packed, sp, C, M, K, N, G, ws)
+    finally:
+        w.w4a16_debug_inject_stall(False)
+        w.w4a16_debug_set_wait_cycles(0)
+    assert w.w4a16_get_status(ws) == 7
+    assert torch.all(C == 7.0)
+    ws.zero_()
+    C2 = w.gemm_24(A_d, packed, sp, N, G, workspace=ws)
+    torch.cuda.synchronize()
+    qc, idx = oracle.sparse24_compress(q)
+    C_ref, bound = oracle.gemm24_ref(A, qc, idx, s, G)
+    tl.assert_within_bound(C2.cpu().numpy(), C_ref, bound, "after timeout")
+    assert w.w4a16_get_status(ws) == 0
