@@ -423,7 +423,7 @@ size_t w4a16_workspace_bytes_24(int M, int K, int N, int groupsize) {
   if (M < 0 || check_shape(K, N, groupsize) != W4A16_OK) return 0;
   DeviceInfo* d = nullptr;
   if (current_device_info(&d) != W4A16_OK) return 0;
-  return make_plan24(M, K, N, effective_group(K, groupsize), d->sms, d->smem_optin, 0).workspace;
+  return make_plan24(M, K, N, effective_group(K, groupsize), d->sms, d->smem_optin, g_ablate.load()).workspace;
 }
 
 int w4a16_gemm_24(const uint16_t* A, const uint32_t* packed24, const uint16_t* scales_p, uint16_t* C, int M, int K,
@@ -441,7 +441,7 @@ int w4a16_gemm_24(const uint16_t* A, const uint32_t* packed24, const uint16_t* s
   if (r != W4A16_OK) return r;
   const int G = effective_group(K, groupsize);
   const int ablate = g_ablate.load();
-  const Plan24 pl = make_plan24(M, K, N, G, d->sms, d->smem_optin, ablate);
+  const Plan pl = make_plan24(M, K, N, G, d->sms, d->smem_optin, ablate);
   if (workspace_bytes < pl.workspace) return W4A16_ERR_WORKSPACE;
   const long long wc = g_wait_cycles.load();
   GemmCall c{};
@@ -458,7 +458,7 @@ int w4a16_gemm_24(const uint16_t* A, const uint32_t* packed24, const uint16_t* s
   c.debug_stall = g_stall.load();
   c.ablate = ablate;
   c.stream = static_cast<cudaStream_t>(stream);
-  return run_gemm24(pl, c);
+  return run_gemm(pl, c);
 }
 
 }  // extern "C"

@@ -178,6 +178,19 @@ __device__ __forceinline__ void mma_16816(float d[4], const uint32_t a[4], uint3
         "f"(c[3]));
 }
 
+// D = A (2:4 compressed 16 x 16, f16) x B (32 x 8, f16) + C with metadata e and
+// sparsity selector SEL (which pair of lanes in each quad supplies the metadata).
+template <int SEL>
+__device__ __forceinline__ void mma_sp_16832(float d[4], const uint32_t a[4], const uint32_t b[4], uint32_t e,
+                                             const float c[4]) {
+  asm volatile(
+      "mma.sp::ordered_metadata.sync.aligned.m16n8k32.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9, %10, %11}, {%12, %13, %14, %15}, %16, %17;"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "f"(c[0]),
+        "f"(c[1]), "f"(c[2]), "f"(c[3]), "r"(e), "n"(SEL));
+}
+
 // ---------------------------------------------------------------------------
 // 4-bit -> FP16x2 decode (the Marlin deep-dive article, section "INT4 只是存储
 // 类型": build FP16 bit patterns with LOP3, then one packed FP16 op).

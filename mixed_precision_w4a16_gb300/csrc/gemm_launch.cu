@@ -26,12 +26,15 @@ void finish_split(Plan& pl, int K, int sms, size_t slot_floats) {
 }
 
 // moe_E > 0: the grouped expert GEMM (its expert tables take shared memory), with up
-// to moe_cols row segments sharing the SMs
+// to moe_cols row segments sharing the SMs.  sp24: the 2:4-sparse stream (3 KB per piece,
+// at most 16 token rows per launch).
 Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin, bool zp, int moe_E = 0, int moe_cols = 1,
-                   int ablate = 0) {
+                   int ablate = 0, bool sp24 = false) {
   Plan pl{};
   pl.path = 1;
-  const int mc = std::min(std::max(M, 1), 32);
+  pl.sp24 = sp24;
+  const int piece_bytes = sp24 ? kPiece24Words * 4 : 4096;
+  const int mc = std::min(std::max(M, 1), sp24 ? 16 : 32);
   const int mt = mc <= 8 ? 1 : mc <= 16 ? 2 : 4;
   pl.strips = N / kStrip;
   // Unit depth KT = 64 * kq (kq up to 16: each of the 4 K-split warps takes every
@@ -39,6 +42,7 @@ Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin, bool zp,
   // on GB300: ~89 ns per 4 KB of weights streamed plus ~80 ns of fixed cost for the
   // unit's three copy operations.  Pick the kq minimising T * unit time among those
   // that keep >= 3 pipeline stages in shared memory.
+  const long long piece_ns = 89LL * piece_bytes / 4096;
   int best_kq = 0;
   long long best_cost = 0;
   const int cands[5] = {16, 12, 8, 4, 2};
@@ -46,12 +50,12 @@ Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin, bool zp,
     const int kq = cands[c];
     if (K % (64 * kq) != 0) continue;
     const int srows = (G <= 64 * kq) ? (64 * kq) / G : 1;
-    const MmaLayout l0 = mma_layout(mt, kq, srows, 0, zp, moe_E);
+    const MmaLayout l0 = mma_layout(mt, kq, srows, 0, zp, moe_E, piece_bytes);
     const int stages = (smem_optin - l0.smem_bytes) / (l0.stage_bytes + 16);
     if (stages < 3 && kq != 2) continue;
     const long long units = static_cast<long long>(pl.strips) * moe_cols * (K / (64 * kq));
     const long long T = (units + sms - 1) / sms;
-    const long long cost = T * (89LL * kq + 80);
+    const long long cost = T * (piece_ns * kq + 80);
     if (best_kq == 0 || cost < best_cost) {
       best_kq = kq;
       best_cost = cost;
@@ -61,11 +65,11 @@ Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin, bool zp,
   const int kq = best_kq;
   const int KT = 64 * kq;
   pl.srows = (G <= KT) ? KT / G : 1;
-  const MmaLayout l0 = mma_layout(mt, kq, pl.srows, 0, zp, moe_E);
+  const MmaLayout l0 = mma_layout(mt, kq, pl.srows, 0, zp, moe_E, piece_bytes);
   int stages = (smem_optin - l0.smem_bytes) / (l0.stage_bytes + 16);
   stages = std::max(2, std::min(stages, 8));
   if (ablate & kAblateStages2) stages = 2;
-  pl.lay = mma_layout(mt, kq, pl.srows, stages, zp, moe_E);
+  pl.lay = mma_layout(mt, kq, pl.srows, stages, zp, moe_E, piece_bytes);
   pl.cfg.m_tiles = mt;
   pl.cfg.kq = kq;
   pl.cfg.stages = stages;
@@ -220,6 +224,10 @@ Plan make_plan_moe(int E, int M, int max_rows, int K, int N, int G, int sms, int
   return pl;
 }
 
+Plan make_plan24(int M, int K, int N, int G, int sms, int smem_optin, int ablate) {
+  return make_plan_mma(M, K, N, G, sms, smem_optin, false, 0, 1, ablate, true);
+}
+
 Plan make_plan(int M, int K, int N, int G, int sms, int smem_optin, bool zp, int forced_path, int ablate) {
   const bool tc = forced_path == 2 || (forced_path != 1 && M >= kTcMinRows);
   return tc ? make_plan_tc(M, K, N, G, sms, smem_optin, zp, ablate)
@@ -285,7 +293,8 @@ int run_gemm(const Plan& pl, const GemmCall& c) {
   GemmParams p = mma_params(pl, c, status, counters, slots);
   for (int m0 = 0; m0 < c.M; m0 += pl.m_chunk) {
     p.m0 = m0;
-    const cudaError_t e = launch_gemm_mma(pl.cfg, map, p, c.stream);
+    const cudaError_t e =
+        pl.sp24 ? launch_gemm_sp24(pl.cfg, map, p, c.stream) : launch_gemm_mma(pl.cfg, map, p, c.stream);
     if (e != cudaSuccess) return W4A16_ERR_CUDA;
   }
   return W4A16_OK;

@@ -35,7 +35,18 @@
 //    streamed once per segment and experts without rows cost nothing.  Each
 //    CTA derives the segment table from the device-side expert offsets in
 //    its prologue (a block-wide prefix sum), so the launch needs no host
-//    synchronisation.
+//    synchronisation;
+//  * the 2:4-sparse variant (SP24; the Sparse-Marlin analogue: the MARLIN
+//    paper, Section 2.1.1 "Modern Tensor Core Units", keeps two of every four
+//    weights along K with their positions as metadata) runs the same pipeline
+//    on a stream of 3 KB per strip and 64-row piece and multiplies with
+//    mma.sp::ordered_metadata.m16n8k32, two per piece (sparsity selectors 0
+//    and 1).  Metadata lane layout, read off a GB300 by an in-bounds probe
+//    that flips one nibble per MMA: with selector s the lanes t = 2s, 2s + 1
+//    of each quad supply it; lane (g, 2s + r) holds in nibbles 0..3 the
+//    position pairs of row g for the MMA's groups 4r .. 4r + 3, in nibbles
+//    4..7 those of row g + 8.  So each lane loads one useful metadata word
+//    per piece (the stream is laid out by w4a16_repack_24, sparse24.cu).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -170,7 +181,8 @@ __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
 
 // ZP: codes carry a zero point per group and column (p.zeros), else the constant 8.
 // MOE: grouped expert GEMM over p.E experts (p.expert_off), else one GEMM on rows p.m0 ..
-template <int MT, bool ZP, bool MOE>
+// SP24: p.packed is the 2:4-sparse stream (no zero points, no experts).
+template <int MT, bool ZP, bool MOE, bool SP24>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     gemm_mma_kernel(const __grid_constant__ CUtensorMap tmA, const GemmParams p) {
   constexpr int MB = 8 * MT;
@@ -230,7 +242,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     const uint64_t pol_w = (p.ablate & kAblateNoEvictFirst) ? policy_evict_normal() : policy_evict_first();
     const uint64_t pol_a = policy_evict_last();
     const int NG = p.K / p.G;
-    const uint32_t w_bytes = static_cast<uint32_t>(KQ) * 4096u;
+    constexpr uint32_t kPieceWords = SP24 ? kPiece24Words : 1024u;  // packed words per 64-row piece
+    const uint32_t w_bytes = static_cast<uint32_t>(KQ) * kPieceWords * 4u;
     int issued = 0;
     // incremental counters: stage s / its fill round, strip j / unit kt within the strip
     int s = 0, round = 0;
@@ -265,7 +278,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             sc += sp.e * p.s_stride;
           }
           const uint32_t* wsrc =
-              pk + (static_cast<long long>(strip) * (p.K / 64) + static_cast<long long>(kt) * KQ) * 1024;
+              pk + (static_cast<long long>(strip) * (p.K / 64) + static_cast<long long>(kt) * KQ) * kPieceWords;
           bulk_g2s(st + p.w_off, wsrc, w_bytes, fb, pol_w);
           tma_load_3d(st, &tmA, 0, row0, kt * KQ, fb, pol_a);
           const int grp0 = (p.G == 128) ? kt * p.srows : 0;  // G is 128 or K (K >= KT)
@@ -337,7 +350,54 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       for (int pc = 0; pc < 4; ++pc) {
         const int kq = kq0 + 4 * pc;
         if (kq >= KQ) break;
-        // activation fragments of this 64-row piece: 4 k16 steps x MT token tiles.  The packed
+if constexpr (SP24) {
+          // activations: sparse MMA m (reduction rows 32m .. 32m + 31 of the piece) wants in register q
+          // of lane (g, t) the pair A[token][32m + 8q + 2t .. + 1]: a 4-byte load from 16-byte chunk
+          // 4m + q of the swizzled tile
+          const uint32_t a_box = st + kq * A_BOX;
+          uint32_t bf[2][MT][4];
+#pragma unroll
+          for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                bf[m][mt][q] = lds32(a_box + (mt * 8 + g) * 128 + (((4 * m + q) ^ swz) << 4) + 4 * t);
+          const int srow = (p.G == 128) ? (kq >> 1) : 0;
+          // the piece: 2048 bytes of code pairs [8 blocks][32 lanes][2 words], then 1024 bytes of
+          // position words [8][32][1]
+          const uint32_t wpiece = st + p.w_off + kq * (kPiece24Words * 4);
+          uint2 cw[kNbw];
+          uint32_t mw[kNbw], spv[kNbw];
+#pragma unroll
+          for (int i = 0; i < kNbw; ++i) {
+            const int nb = ng * kNbw + i;
+            cw[i] = lds64(wpiece + (nb * 32 + lane) * 8);
+            mw[i] = lds32(wpiece + 2048 + (nb * 32 + lane) * 4);
+            spv[i] = lds32(st + p.s_off + (srow * 128 + nb * 16 + 2 * g) * 2);
+          }
+#pragma unroll
+          for (int i = 0; i < kNbw; ++i) {
+            float tmp[MT][4];
+            uint32_t a[4];
+            decode8(cw[i].x, a);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) mma_sp_16832<0>(tmp[mt], a, bf[0][mt], mw[i], zero4);
+            decode8(cw[i].y, a);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) mma_sp_16832<1>(tmp[mt], a, bf[1][mt], mw[i], tmp[mt]);
+            const float s_lo = __half2float(__ushort_as_half(static_cast<uint16_t>(spv[i] & 0xffffu)));
+            const float s_hi = __half2float(__ushort_as_half(static_cast<uint16_t>(spv[i] >> 16)));
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              acc[i][mt][0] = fmaf(s_lo, tmp[mt][0], acc[i][mt][0]);
+              acc[i][mt][1] = fmaf(s_lo, tmp[mt][1], acc[i][mt][1]);
+              acc[i][mt][2] = fmaf(s_hi, tmp[mt][2], acc[i][mt][2]);
+              acc[i][mt][3] = fmaf(s_hi, tmp[mt][3], acc[i][mt][3]);
+            }
+          }
+        } else {
+                // activation fragments of this 64-row piece: 4 k16 steps x MT token tiles.  The packed
         // weights hold k = 4t .. 4t+3 of each 16-row block where the m16n8k16 fragment expects
         // 2t, 2t+1, 2t+8, 2t+9, so the matching activation pair is one 8-byte load of
         // A[token][16 jj + 4t .. 4t+3] (128-byte swizzle: 16-byte chunk c of row r is at c ^ (r & 7);
@@ -391,6 +451,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             acc[i][mt][2] = fmaf(s_hi, tmp[mt][2], acc[i][mt][2]);
             acc[i][mt][3] = fmaf(s_hi, tmp[mt][3], acc[i][mt][3]);
           }
+        }
         }
       }
       __syncwarp();
@@ -511,9 +572,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   named_bar_sync(3, kMmaThreads);
 }
 
-template <int MT, bool ZP, bool MOE = false>
+template <int MT, bool ZP, bool MOE = false, bool SP24 = false>
 cudaError_t launch_one(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream) {
-  auto kern = gemm_mma_kernel<MT, ZP, MOE>;
+  auto kern = gemm_mma_kernel<MT, ZP, MOE, SP24>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem_bytes);
   if (e != cudaSuccess) return e;
   kern<<<p.grid, kMmaThreads, cfg.smem_bytes, stream>>>(tmA, p);
@@ -522,15 +583,15 @@ cudaError_t launch_one(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmP
 
 }  // namespace
 
-MmaLayout mma_layout(int m_tiles, int kq, int srows, int stages, bool zp, int moe_E) {
+MmaLayout mma_layout(int m_tiles, int kq, int srows, int stages, bool zp, int moe_E, int piece_bytes) {
   MmaLayout l{};
   const int MB = 8 * m_tiles;
   l.w_off = kq * MB * 128;        // activation pieces first (each a multiple of 1024 bytes)
-  l.s_off = l.w_off + kq * 4096;  // then the weight chunk, then the scale rows
+  l.s_off = l.w_off + kq * piece_bytes;  // then the weight chunk, then the scale rows
   l.z_off = l.s_off + srows * 256;  // then, with zero points, their rows (128 bytes each)
   const int zbytes = zp ? srows * 128 : 0;
   l.stage_bytes = (l.z_off + zbytes + 1023) / 1024 * 1024;
-  l.tx_bytes = kq * MB * 128 + kq * 4096 + srows * 256 + zbytes;
+  l.tx_bytes = kq * MB * 128 + kq * piece_bytes + srows * 256 + zbytes;
   l.red_off = stages * l.stage_bytes;
   l.bar_off = l.red_off + 3 * 2 * kNbw * m_tiles * 4 * 32 * 4;
   l.flag_off = l.bar_off + 16 * stages;
@@ -555,6 +616,14 @@ cudaError_t launch_moe_mma(const MmaConfig& cfg, const CUtensorMap& tmA, const G
   switch (cfg.m_tiles) {
     case 1: return launch_one<1, false, true>(cfg, tmA, p, stream);
     case 2: return launch_one<2, false, true>(cfg, tmA, p, stream);  // segments are at most 16 rows
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_gemm_sp24(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream) {
+  switch (cfg.m_tiles) {
+    case 1: return launch_one<1, false, false, true>(cfg, tmA, p, stream);
+    case 2: return launch_one<2, false, false, true>(cfg, tmA, p, stream);  // 16 token rows per launch
     default: return cudaErrorInvalidValue;
   }
 }

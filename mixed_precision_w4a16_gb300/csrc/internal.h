@@ -30,8 +30,13 @@ struct MmaLayout {
   int red_off, bar_off, flag_off, moe_off, smem_bytes;  // moe_off: expert tables of the grouped GEMM
 };
 
-// moe_E: experts of a grouped GEMM (0 for a plain GEMM); their tables take shared memory
-MmaLayout mma_layout(int m_tiles, int kq, int srows, int stages, bool zp, int moe_E = 0);
+// moe_E: experts of a grouped GEMM (0 for a plain GEMM); their tables take shared memory.
+// piece_bytes: packed weights per 64-row piece of a strip (4096 dense, 3072 for 2:4).
+MmaLayout mma_layout(int m_tiles, int kq, int srows, int stages, bool zp, int moe_E = 0, int piece_bytes = 4096);
+
+// 2:4-sparse packed stream: 32-bit words per 64-row piece of one 128-column strip
+// (codes: 8 column blocks x 32 lanes x 2 words; positions: 8 x 32 x 1 word).
+constexpr int kPiece24Words = 768;
 
 // Parameters of one launch of the streaming (mma.sync) GEMM kernel.
 struct GemmParams {
@@ -83,10 +88,12 @@ constexpr int kStrip = 128;       // output columns per strip / work unit
 cudaError_t launch_gemm_mma(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream);
 // grouped expert GEMM: one launch over all experts (p.expert_off set, p.M = rows of A)
 cudaError_t launch_moe_mma(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream);
+// 2:4-sparse weights (p.packed is the packed 2:4 stream; m_tiles 1 or 2)
+cudaError_t launch_gemm_sp24(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream);
 // with zero points (p.zeros != null) the kernels are built with the per-row zero decode
 
 // ---- tensor-memory (tcgen05) GEMM ----------------------------------------
-constexpr int kTcThreads = 768;  // 3 producers, 4 MMA issuers, 1 idle, 16 dequant warps (two teams)
+constexpr int kTcThreads = 736;  // 3 producers, 4 MMA issuers, 16 dequant warps (two teams)
 constexpr int kTcMaxIssuers = 4;
 
 struct TcLayout {
@@ -154,6 +161,7 @@ struct Plan {
   int srows;
   int KU, strips, units, T, grid, stages, smem_bytes, threads;
   int moe_E, max_seg;  // grouped expert GEMM: experts, row segments the counters are sized for
+  bool sp24;           // path 1 on the 2:4-sparse packed stream
   size_t workspace;
 };
 
@@ -188,5 +196,8 @@ int run_gemm(const Plan& pl, const GemmCall& c);
 Plan make_plan_moe(int E, int M, int max_rows, int K, int N, int G, int sms, int smem_optin, int ablate = 0);
 // c.M = rows of A and C, c.packed / c.scales = E stacked layers; zeros and bias unused.
 int run_moe_gemm(const Plan& pl, const GemmCall& c, const int* expert_off);
+
+// 2:4-sparse GEMM on the streaming kernel (run with run_gemm; c.packed = the packed 2:4 stream).
+Plan make_plan24(int M, int K, int N, int G, int sms, int smem_optin, int ablate);
 
 }  // namespace w4a16
