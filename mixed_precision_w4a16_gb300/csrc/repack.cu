@@ -54,12 +54,31 @@ __device__ __forceinline__ void slot_rc(int slot, int g, int t, int& r, int& c) 
   c = 4 * t + 2 * (reg >> 1) + e;
 }
 
-__global__ void repack_codes_kernel(const uint8_t* __restrict__ q, int K, int N, uint4* __restrict__ packed,
-                                    long long nvec) {
-  const long long v = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
-  if (v >= nvec) return;
-  const VecCoord vc = vec_coord(v, K);
-  const int g = vc.lane >> 2, t = vc.lane & 3;
+// One CTA of 256 threads per 64-row x 128-column tile (one strip, one 64-row block):
+// the tile's codes are read row by row into shared memory (coalesced 16-byte loads),
+// then thread (block b, lane) assembles its four words from there and writes its
+// 16-byte vector; the CTA's 256 vectors are consecutive in the packed stream.  The
+// rows are padded so that the four lanes t of a quad, which read rows 4 apart, hit
+// different banks.
+constexpr int kTileThreads = 256;
+constexpr int kCodeRow = 136;  // bytes per shared row of codes (128 + 8)
+constexpr int kHalfRow = 132;  // halves per shared row of FP16 weights (128 + 4)
+
+__global__ void __launch_bounds__(kTileThreads) repack_codes_kernel(const uint8_t* __restrict__ q, int K, int N,
+                                                                    uint4* __restrict__ packed) {
+  __shared__ __align__(16) uint8_t tile[64][kCodeRow];
+  const int kTiles = K / 64;
+  const int kb = static_cast<int>(blockIdx.x % kTiles);
+  const long long strip = blockIdx.x / kTiles;
+  for (int i = threadIdx.x; i < 64 * 8; i += kTileThreads) {  // 64 rows x 8 16-byte pieces
+    const int r = i >> 3, c16 = i & 7;
+    const uint4 v = *reinterpret_cast<const uint4*>(q + (kb * 64LL + r) * N + strip * 128 + 16 * c16);
+    *reinterpret_cast<uint2*>(&tile[r][16 * c16]) = make_uint2(v.x, v.y);
+    *reinterpret_cast<uint2*>(&tile[r][16 * c16 + 8]) = make_uint2(v.z, v.w);
+  }
+  __syncthreads();
+  const int b = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
   uint32_t words[4];
   uint32_t bad = 0;
 #pragma unroll
@@ -69,30 +88,50 @@ __global__ void repack_codes_kernel(const uint8_t* __restrict__ q, int K, int N,
     for (int slot = 0; slot < 8; ++slot) {
       int r, c;
       slot_rc(slot, g, t, r, c);
-      const long long k = vc.kb * 64LL + 16 * j + c;
-      const long long n = vc.nb * 16LL + r;
-      const uint32_t code = q[k * N + n];
+      const uint32_t code = tile[16 * j + c][16 * b + r];
       bad |= code > 15u;
       w |= (code & 15u) << (4 * slot);
     }
     words[j] = w;
   }
   if (bad) atomicOr(&g_repack_flag, kDevErrCodeRange);
-  packed[v] = make_uint4(words[0], words[1], words[2], words[3]);
+  packed[static_cast<long long>(blockIdx.x) * kTileThreads + threadIdx.x] = make_uint4(words[0], words[1], words[2], words[3]);
 }
 
 // Quantise FP16 weights with their FP16 scales straight into the packed layout
 // (the original Layer.pack step, deep-dive article section "可复现的调用链"):
 // q = clamp(rint(w / s) + 8, 0, 15), the quotient an IEEE float32 division,
 // rint rounding half to even.  Same word-side walk as repack_codes_kernel.
-// z: zero codes uint8[K/G][N] row-major, or null for the symmetric offset 8
-__global__ void quantize_codes_kernel(const uint16_t* __restrict__ w, const uint16_t* __restrict__ s,
-                                      const uint8_t* __restrict__ z, int K, int N, int G, uint4* __restrict__ packed,
-                                      long long nvec) {
-  const long long v = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
-  if (v >= nvec) return;
-  const VecCoord vc = vec_coord(v, K);
-  const int g = vc.lane >> 2, t = vc.lane & 3;
+// z: zero codes uint8[K/G][N] row-major, or null for the symmetric offset 8.  Tiled like
+// repack_codes_kernel: the 64-row tile lies inside one group (G is 128 or K), so its 128
+// scales (and zero codes) are one row.
+__global__ void __launch_bounds__(kTileThreads) quantize_codes_kernel(const uint16_t* __restrict__ w,
+                                                                      const uint16_t* __restrict__ s,
+                                                                      const uint8_t* __restrict__ z, int K, int N,
+                                                                      int G, uint4* __restrict__ packed) {
+  __shared__ __align__(16) uint16_t tile[64][kHalfRow];
+  __shared__ float scale[128];
+  __shared__ float recip[128];
+  __shared__ float offset[128];
+  const int kTiles = K / 64;
+  const int kb = static_cast<int>(blockIdx.x % kTiles);
+  const long long strip = blockIdx.x / kTiles;
+  for (int i = threadIdx.x; i < 64 * 16; i += kTileThreads) {  // 64 rows x 16 16-byte pieces
+    const int r = i >> 4, c8 = i & 15;
+    const uint4 v = *reinterpret_cast<const uint4*>(w + (kb * 64LL + r) * N + strip * 128 + 8 * c8);
+    *reinterpret_cast<uint2*>(&tile[r][8 * c8]) = make_uint2(v.x, v.y);
+    *reinterpret_cast<uint2*>(&tile[r][8 * c8 + 4]) = make_uint2(v.z, v.w);
+  }
+  if (threadIdx.x < 128) {
+    const long long gi = ((kb * 64LL) / G) * N + strip * 128 + threadIdx.x;
+    const float sf = __half2float(__ushort_as_half(s[gi]));
+    scale[threadIdx.x] = sf;
+    recip[threadIdx.x] = __frcp_rn(sf);
+    offset[threadIdx.x] = z ? static_cast<float>(z[gi]) : 8.0f;
+  }
+  __syncthreads();
+  const int b = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
   uint32_t words[4];
   bool bad = false;
 #pragma unroll
@@ -102,16 +141,17 @@ __global__ void quantize_codes_kernel(const uint16_t* __restrict__ w, const uint
     for (int slot = 0; slot < 8; ++slot) {
       int r, c;
       slot_rc(slot, g, t, r, c);
-      const long long k = vc.kb * 64LL + 16 * j + c;
-      const long long n = vc.nb * 16LL + r;
-      const float wf = __half2float(__ushort_as_half(w[k * N + n]));
-      const long long gi = (k / G) * N + n;
-      const float sf = __half2float(__ushort_as_half(s[gi]));
-      const float quot = __fdiv_rn(wf, sf);
+      const int col = 16 * b + r;
+      const float wf = __half2float(__ushort_as_half(tile[16 * j + c][col]));
+      // w * RN(1/s) is within 1.5 ulp of w / s; away from the half-integers it rounds to the
+      // same integer as the correctly rounded quotient, which is taken only near them
+      const float approx = wf * recip[col];
+      const float frac = fabsf(approx - truncf(approx));
+      const bool near_tie = fabsf(frac - 0.5f) <= 0x1p-22f * fabsf(approx);  // twice the error bound 2^-23 |w/s|
+      const float quot = (isfinite(approx) && !near_tie) ? approx : __fdiv_rn(wf, scale[col]);
       uint32_t code = 8u;
       if (isfinite(quot)) {
-        const float off = z ? static_cast<float>(z[gi]) : 8.0f;
-        const float qf = fminf(fmaxf(rintf(quot) + off, 0.0f), 15.0f);
+        const float qf = fminf(fmaxf(rintf(quot) + offset[col], 0.0f), 15.0f);
         code = static_cast<uint32_t>(qf);
       } else {
         bad = true;
@@ -121,7 +161,7 @@ __global__ void quantize_codes_kernel(const uint16_t* __restrict__ w, const uint
     words[j] = word;
   }
   if (bad) atomicOr(&g_repack_flag, kDevErrValue);
-  packed[v] = make_uint4(words[0], words[1], words[2], words[3]);
+  packed[static_cast<long long>(blockIdx.x) * kTileThreads + threadIdx.x] = make_uint4(words[0], words[1], words[2], words[3]);
 }
 
 // permuted position p inside a 16-column block -> fragment row r
@@ -280,8 +320,8 @@ inline unsigned grid_for(long long n, int block) { return static_cast<unsigned>(
 
 cudaError_t launch_repack(const uint8_t* q, const uint16_t* s, int K, int N, int G, uint32_t* packed,
                           uint16_t* scales_p, cudaStream_t stream) {
-  const long long nvec = static_cast<long long>(K) * N / 32;
-  repack_codes_kernel<<<grid_for(nvec, 256), 256, 0, stream>>>(q, K, N, reinterpret_cast<uint4*>(packed), nvec);
+  const unsigned tiles = static_cast<unsigned>(static_cast<long long>(N / 128) * (K / 64));
+  repack_codes_kernel<<<tiles, kTileThreads, 0, stream>>>(q, K, N, reinterpret_cast<uint4*>(packed));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long ns = static_cast<long long>(K / G) * N;
@@ -291,9 +331,8 @@ cudaError_t launch_repack(const uint8_t* q, const uint16_t* s, int K, int N, int
 
 cudaError_t launch_quantize_repack(const uint16_t* w, const uint16_t* s, const uint8_t* z, int K, int N, int G,
                                    uint32_t* packed, uint16_t* scales_p, cudaStream_t stream) {
-  const long long nvec = static_cast<long long>(K) * N / 32;
-  quantize_codes_kernel<<<grid_for(nvec, 256), 256, 0, stream>>>(w, s, z, K, N, G, reinterpret_cast<uint4*>(packed),
-                                                                  nvec);
+  const unsigned tiles = static_cast<unsigned>(static_cast<long long>(N / 128) * (K / 64));
+  quantize_codes_kernel<<<tiles, kTileThreads, 0, stream>>>(w, s, z, K, N, G, reinterpret_cast<uint4*>(packed));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long ns = static_cast<long long>(K / G) * N;
