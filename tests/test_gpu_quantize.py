@@ -192,3 +192,20 @@ def test_minmax_full_k_sampled_columns(w, G):
         assert np.array_equal(s[:, cols].view(np.uint16), s_ref.view(np.uint16))
         if not symmetric:
             assert np.array_equal(z[:, cols], z_ref)
+
+
+def test_quantize_quotients_near_half_integers_match_oracle(w):
+    """Weights placed at (x + 1/2 + delta) * s for random FP16 scales (inexact reciprocals) and tiny
+    delta of either sign: the quotients sit next to the rounding boundaries, where the kernel must
+    fall back to the correctly rounded division; codes byte for byte against the oracle."""
+    rng = np.random.default_rng(97)
+    K, N, G = 512, 512, 128
+    s = rng.uniform(0.003, 0.05, size=(K // G, N)).astype(np.float16)
+    x = rng.integers(-9, 8, size=(K, N)).astype(np.float64)
+    delta = rng.choice([-1.0, 1.0], size=(K, N)) * 10.0 ** rng.uniform(-7, -2, size=(K, N))
+    delta[rng.random((K, N)) < 0.2] = 0.0
+    wt = ((x + 0.5 + delta) * np.repeat(s.astype(np.float64), G, axis=0)).astype(np.float16)
+    got_packed, got_sp = _quantize_on_device(w, wt, s, G)
+    ref_packed, _ = oracle.repack(oracle.quantize(wt, s, G), s, G)
+    assert np.array_equal(got_packed, ref_packed)
+    assert w.w4a16_get_status() == 0
