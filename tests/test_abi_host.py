@@ -173,3 +173,22 @@ def test_entry_points_report_missing_gpu(w):
     L = w.lib
     assert L.w4a16_gemm(16, 16, 16, 16, 4, 1024, 1024, 128, 16, 1 << 20, None) == 6
     assert L.w4a16_workspace_bytes(16, 1024, 1024, 128) == 0
+
+
+def test_sparse_and_quantiser_entry_points_validate_on_the_host(w):
+    L = w.lib
+    # 2:4: sizes, bad shapes, null pointers, M == 0
+    assert L.w4a16_packed24_bytes(1024, 1024) == 1024 * 1024 * 3 // 8
+    assert L.w4a16_packed24_bytes(1000, 1024) == 0
+    assert L.w4a16_gemm_24(16, 16, 16, 16, 4, 1000, 1024, 128, 16, 1 << 20, None) == 2
+    assert L.w4a16_gemm_24(None, 16, 16, 16, 4, 1024, 1024, 128, 16, 1 << 20, None) == 1
+    assert L.w4a16_gemm_24(16, 16, 16, 16, 4, 1024, 1024, 128, None, 1 << 20, None) == 5
+    assert L.w4a16_gemm_24(None, None, None, None, 0, 1024, 1024, 128, None, 0, None) == 0
+    assert L.w4a16_repack_24(None, 16, 1024, 1024, 128, 16, 16, None) == 1
+    assert L.w4a16_repack_24(16, 16, 1024, 1024, 96, 16, 16, None) == 3
+    assert L.w4a16_unpack_24(16, 1000, 1024, 16, None) == 2
+    # quantiser: bad group, null scales, misaligned weights
+    assert L.w4a16_minmax_scales(16, 1024, 1024, 96, 16, None, None) == 3
+    assert L.w4a16_minmax_scales(16, 1024, 1024, 128, None, None, None) == 1
+    assert L.w4a16_minmax_scales(17, 1024, 1024, 128, 16, None, None) == 9   # W4A16_ERR_ALIGN
+    assert L.w4a16_quantize_repack_zp(16, 16, 17, 1024, 1024, 128, 16, 16, None) == 9
