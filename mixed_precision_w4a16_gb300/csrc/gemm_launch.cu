@@ -41,7 +41,8 @@ Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin, bool zp,
   // fourth piece).  Per-SM time of a unit is modelled from copy-engine measurements
   // on GB300: ~89 ns per 4 KB of weights streamed plus ~80 ns of fixed cost for the
   // unit's three copy operations.  Pick the kq minimising T * unit time among those
-  // that keep >= 3 pipeline stages in shared memory.
+  // that keep >= 2 pipeline stages in shared memory (measured: two 64 KB stages beat
+  // three 48 KB ones; the bytes in flight matter, not the stage count).
   const long long piece_ns = 89LL * piece_bytes / 4096;
   int best_kq = 0;
   long long best_cost = 0;
@@ -52,7 +53,7 @@ Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin, bool zp,
     const int srows = (G <= 64 * kq) ? (64 * kq) / G : 1;
     const MmaLayout l0 = mma_layout(mt, kq, srows, 0, zp, moe_E, piece_bytes);
     const int stages = (smem_optin - l0.smem_bytes) / (l0.stage_bytes + 16);
-    if (stages < 3 && kq != 2) continue;
+    if (stages < 2) continue;
     const long long units = static_cast<long long>(pl.strips) * moe_cols * (K / (64 * kq));
     const long long T = (units + sms - 1) / sms;
     const long long cost = T * (piece_ns * kq + 80);

@@ -70,7 +70,9 @@ SHAPES = [(1, 1024, 1024), (16, 1024, 1024), (16, 4096, 12288), (1, 11008, 4096)
 def test_plan_stripes_cover_every_unit_once(w, M, K, N):
     for sms in (152, 148, 7):
         p = w.w4a16_plan(M, K, N, 128, sms)
-        assert p["k_tile"] in (128, 256, 512) and K % p["k_tile"] == 0 and p["n_tile"] == 128
+        # streaming kernel: 2..16 pieces of 64 rows; tensor-memory kernel: 1..4 chunks of 128 rows
+        allowed = (128, 256, 512, 768, 1024) if p["path"] == 1 else (128, 256, 512)
+        assert p["k_tile"] in allowed and K % p["k_tile"] == 0 and p["n_tile"] == 128
         KU = K // p["k_tile"]
         assert p["units"] == (N // p["n_tile"]) * KU
         T, grid, U = p["units_per_cta"], p["grid"], p["units"]
@@ -115,22 +117,31 @@ def test_force_path_knob(w):
     assert w.w4a16_plan(200, 1024, 1024, 128, 152)["path"] == 2
 
 
+# a streaming-kernel case and a tensor-memory case whose full-design plans are deeper than 2 stages
+ABLATION_CASES = ((4, 4096, 1024), (64, 4096, 4096))
+
+
+def _plans(w):
+    return [w.w4a16_plan(m, k, n, 128, 152) for m, k, n in ABLATION_CASES]
+
+
 def test_ablation_switch_sets_two_stages(w):
-    full = [w.w4a16_plan(m, 4096, 4096, 128, 152) for m in (4, 64)]
+    full = _plans(w)
+    assert [p["path"] for p in full] == [1, 2]
     assert all(p["stages"] > 2 for p in full)
     try:
         w.w4a16_debug_ablate(w.ABLATE_STAGES_2)
-        abl = [w.w4a16_plan(m, 4096, 4096, 128, 152) for m in (4, 64)]
+        abl = _plans(w)
         assert [p["stages"] for p in abl] == [2, 2]
         # nothing else of the plan changes: same kernel, tiles and split
         for a, f in zip(abl, full):
             assert {k: v for k, v in a.items() if k not in ("stages", "smem_bytes")} == \
                 {k: v for k, v in f.items() if k not in ("stages", "smem_bytes")}
         w.w4a16_debug_ablate(w.ABLATE_NO_EVICT_FIRST | w.ABLATE_NO_SWIZZLE)
-        assert [w.w4a16_plan(m, 4096, 4096, 128, 152) for m in (4, 64)] == full
+        assert _plans(w) == full
     finally:
         w.w4a16_debug_ablate(0)
-    assert [w.w4a16_plan(m, 4096, 4096, 128, 152) for m in (4, 64)] == full
+    assert _plans(w) == full
 
 
 def test_moe_gemm_validates_before_touching_the_device(w):
