@@ -203,3 +203,15 @@ def test_sparse_and_quantiser_entry_points_validate_on_the_host(w):
     assert L.w4a16_minmax_scales(16, 1024, 1024, 128, None, None, None) == 1
     assert L.w4a16_minmax_scales(17, 1024, 1024, 128, 16, None, None) == 9   # W4A16_ERR_ALIGN
     assert L.w4a16_quantize_repack_zp(16, 16, 17, 1024, 1024, 128, 16, 16, None) == 9
+
+
+def test_big_layer_plans_are_the_measured_ones(w):
+    """The plans the benchmark numbers were measured with (K = 18432, N = 73728, G = 128, 152 SMs):
+    streaming kernel with 16-piece (1024-row) units in 2 stages up to M = 16, tensor-memory kernel
+    with 512-row units above."""
+    for M in (1, 8, 16):
+        p = w.w4a16_plan(M, 18432, 73728, 128, 152)
+        assert (p["path"], p["k_tile"], p["stages"], p["m_chunk"]) == (1, 1024, 2, 8 if M <= 8 else 16)
+    for M in (32, 64, 128):
+        p = w.w4a16_plan(M, 18432, 73728, 128, 152)
+        assert (p["path"], p["k_tile"], p["m_chunk"]) == (2, 512, M)
