@@ -42,7 +42,8 @@ Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin, bool zp,
   // on GB300: ~89 ns per 4 KB of weights streamed plus ~80 ns of fixed cost for the
   // unit's three copy operations.  Pick the kq minimising T * unit time among those
   // that keep >= 2 pipeline stages in shared memory (measured: two 64 KB stages beat
-  // three 48 KB ones; the bytes in flight matter, not the stage count).
+  // three 48 KB and five 32 KB ones, with fewer bytes in flight -- the per-unit costs
+  // weigh more than the pipeline depth).
   const long long piece_ns = 89LL * piece_bytes / 4096;
   int best_kq = 0;
   long long best_cost = 0;
