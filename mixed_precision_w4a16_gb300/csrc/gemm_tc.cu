@@ -354,8 +354,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         const bool seg_end = (kt == p.KU - 1) || (it == nunits - 1);
         const int c0 = (issuer - it * CH) & (NI - 1);  // first own chunk of the unit (NI is a power of two)
         for (int c = c0; c < CH; c += NI) {
-          ok = mbar_wait_bounded_sleep(bar_afull + 8 * a, ph, p.wait_limit, abort_flag) &&
-               mbar_wait_bounded_sleep(bar_cfull + 8 * a, ph, p.wait_limit, abort_flag);
+          // The A chunk first.  Its arrival means that this team's chunk gc - NA was decoded
+          // after the multiplies of chunk gc - NA completed, and those had waited for that chunk's
+          // activation copy; only then does the parity wait on the activation stage (shared with
+          // chunks of other issuers when NA is not a multiple of NI) name a unique phase.  Waited
+          // the other way round, an activation copy still in flight for chunk gc - NA could be
+          // taken for chunk gc's.
+          ok = mbar_wait_bounded_sleep(bar_cfull + 8 * a, ph, p.wait_limit, abort_flag) &&
+               mbar_wait_bounded_sleep(bar_afull + 8 * a, ph, p.wait_limit, abort_flag);
           // the previous segment's accumulators must have been read out
           if (ok && first && segs > 0) ok = mbar_wait_bounded(bar_dempty, (segs - 1) & 1, p.wait_limit, abort_flag);
           if (!ok) break;
