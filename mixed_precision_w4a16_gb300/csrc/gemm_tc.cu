@@ -380,6 +380,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           break;
         }
         if (seg_end) {
+          // An issuer without a chunk in this segment (fewer chunks than issuers: a CTA's range
+          // ending just past a strip boundary) has not waited for the previous segment's
+          // read-out; without that wait its commit could complete the previous phase of
+          // bar_dfull, ahead of another issuer's multiplies.
+          if (first && segs > 0 && !mbar_wait_bounded(bar_dempty, (segs - 1) & 1, p.wait_limit, abort_flag)) {
+            raise_abort();
+            break;
+          }
           tc_commit(bar_dfull);
           ++segs;
           first = true;

@@ -215,3 +215,30 @@ def test_big_layer_plans_are_the_measured_ones(w):
     for M in (32, 64, 128):
         p = w.w4a16_plan(M, 18432, 73728, 128, 152)
         assert (p["path"], p["k_tile"], p["m_chunk"]) == (2, 512, M)
+
+
+def _segments_with_idle_issuers(w, M, K, N):
+    """Count the CTA segments after a CTA's first whose chunks are fewer than the MMA issuers
+    of the tensor-memory plan (the case the GPU test on these shapes exists for)."""
+    p = w.w4a16_plan(M, K, N, 128, 152)
+    assert p["path"] == 2
+    ch, KU, T, units = p["k_tile"] // 128, K // p["k_tile"], p["units_per_cta"], p["units"]
+    mb = p["m_chunk"]
+    ni = 1
+    while 2 * ni <= min(4, 256 // mb):
+        ni *= 2
+    hits = 0
+    for u0 in range(0, units, T):
+        u1 = min(units, u0 + T)
+        lengths, start = [], u0
+        for u in range(u0, u1):
+            if u % KU == KU - 1 or u == u1 - 1:
+                lengths.append(u - start + 1)
+                start = u + 1
+        hits += sum(1 for L in lengths[1:] if L * ch < ni)
+    return hits
+
+
+@pytest.mark.parametrize("M,K,N", [(32, 11008, 4096), (64, 11008, 4096), (32, 2816, 4096)])
+def test_idle_issuer_shapes_have_short_segments(w, M, K, N):
+    assert _segments_with_idle_issuers(w, M, K, N) > 0
