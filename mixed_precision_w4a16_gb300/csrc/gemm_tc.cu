@@ -44,11 +44,19 @@ namespace w4a16 {
 namespace {
 
 // warps: 0 weight producer, 1..2 activation producers (even / odd chunks), 3..6 MMA
-// issuers 0..3 (warp 3 owns the tensor memory), 7..22 dequant (team 0: warps 7..14,
-// team 1: warps 15..22)
+// issuers 0..3 (warp 3 owns the tensor memory), 7 idle (it completes the second
+// warpgroup), 8..23 dequant (team 0: warps 8..15, team 1: warps 16..23)
 constexpr int kActWarp0 = 1;
 constexpr int kIssuerWarp0 = 3;
-constexpr int kDequantWarp0 = 7;
+constexpr int kDequantWarp0 = 8;
+// Register split (setmaxnreg): the two helper warpgroups drop to kHelperRegs per thread and
+// the four dequant warpgroups rise to kDequantRegs.  The launch allocates numRegs * kTcThreads;
+// the rise must be covered by what the drop releases, which launch_gemm_tc checks before it
+// launches (an uncovered rise would wait forever).
+constexpr int kHelperRegs = 40;
+constexpr int kDequantRegs = 96;
+constexpr int kHelperThreads = 32 * kDequantWarp0;
+constexpr int kDequantThreads = kTcThreads - kHelperThreads;
 constexpr int kDequantWarps = 16;  // both teams; every one releases each weight stage
 constexpr int kTeamWarps = 8;      // one team: the writers of one A chunk
 constexpr int kEpiThreads = 32 * kTeamWarps;  // team 0 runs the epilogue
@@ -221,6 +229,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // warpgroup-uniform: warps 0..7 are warpgroups 0 and 1, warps 8..23 warpgroups 2..5
+  if (warp < kDequantWarp0)
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kHelperRegs));
+  else
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kDequantRegs));
 
   auto raise_abort = [&]() {
     if (!*abort_flag) {
@@ -665,7 +678,13 @@ uint32_t tc_idesc(int m, int n) {
 cudaError_t launch_gemm_tc(int smem_bytes, const CUtensorMap& tmA, const TcParams& p, cudaStream_t stream) {
   auto kern = p.zeros ? (p.bias ? gemm_tc_kernel<true, true> : gemm_tc_kernel<true, false>)
                       : (p.bias ? gemm_tc_kernel<false, true> : gemm_tc_kernel<false, false>);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  cudaFuncAttributes fa{};
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (static_cast<long long>(fa.numRegs) * kTcThreads <
+      static_cast<long long>(kHelperRegs) * kHelperThreads + static_cast<long long>(kDequantRegs) * kDequantThreads)
+    return cudaErrorInvalidConfiguration;  // the register split would not be covered
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
   kern<<<p.grid, kTcThreads, smem_bytes, stream>>>(tmA, p);
   return cudaGetLastError();

@@ -93,7 +93,7 @@ cudaError_t launch_gemm_sp24(const MmaConfig& cfg, const CUtensorMap& tmA, const
 // with zero points (p.zeros != null) the kernels are built with the per-row zero decode
 
 // ---- tensor-memory (tcgen05) GEMM ----------------------------------------
-constexpr int kTcThreads = 736;  // 3 producers, 4 MMA issuers, 16 dequant warps (two teams)
+constexpr int kTcThreads = 768;  // 3 producers, 4 MMA issuers, 1 idle warp, 16 dequant warps (two teams)
 constexpr int kTcMaxIssuers = 4;
 
 struct TcLayout {

@@ -103,7 +103,7 @@ def test_plan_token_tiles_and_kernel_choice(w):
     assert [p["m_chunk"] for p in plans[:4]] == [8, 8, 16, 16]
     # from 17 rows: tensor-memory kernel, tokens padded to 16 (the MMA's N), at most 128 per launch
     assert [p["m_chunk"] for p in plans[4:]] == [32, 32, 48, 64, 128, 128]
-    assert all(p["threads"] == 736 for p in plans[4:]) and all(p["threads"] == 288 for p in plans[:4])
+    assert all(p["threads"] == 768 for p in plans[4:]) and all(p["threads"] == 288 for p in plans[:4])
 
 
 def test_force_path_knob(w):
