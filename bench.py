@@ -36,6 +36,10 @@ if ROOT not in sys.path:
 METRIC = "W4A16 GEMM µs, achieved HBM TB/s & % of roofline vs M=1..128 (1×GB300)"
 KERNEL_OF_PATH = {1: "gemm_mma_kernel", 2: "gemm_tc_kernel"}
 L2_BYTES = 129 * 1024 * 1024
+# roofline time below which a GEMM is also timed inside a CUDA graph (there the host's launch
+# overhead, not the kernel, sets a single launch's time), and the minimum launches in that graph
+GRAPH_BELOW_US = 5.0
+GRAPH_LAUNCHES = 20
 
 # workload name -> (description, list of (K, N, groupsize, [M ...]), seed)
 WORKLOADS = {
@@ -99,6 +103,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="big")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph timing of layers under 5 us")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--only-m", type=int, default=None, help="run only this M of the sweep (profiling)")
     ap.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS FP16 GEMM on the dequantised weights")
@@ -451,6 +456,43 @@ def run_ours(args, rank, world, device):
             cublas_us.append(c0.elapsed_time(c1) / reps * 1e3)
         bhat_cache.clear()
 
+    # ---- layers whose roofline time is under GRAPH_BELOW_US: time per GEMM inside a CUDA graph of
+    # many launches as well (launch overhead amortised), next to the single-launch figure above
+    graph_us = {}
+    if rank == 0 and not args.no_graph:
+        def graph_gemm(p, packed, sp):  # on the current (capturing) stream
+            if args.zero_points:
+                w.w4a16_gemm_zp(p["A_d"], packed, sp, p["zp"], p["bias"], p["C_d"], p["M"], p["K"], p["N"], p["G"],
+                                ws, max_ws)
+            else:
+                w.w4a16_gemm(p["A_d"], packed, sp, p["C_d"], p["M"], p["K"], p["N"], p["G"], ws, max_ws)
+
+        for i, p in enumerate(points):
+            t_roof = max(gemm_bytes(p["M"], p["K"], p["N"], p["G"]) / (peaks["hbm_gbs"] * 1e9),
+                         gemm_flops(p["M"], p["K"], p["N"]) / (peaks["bf16_tflops"] * 1e12))
+            if t_roof * 1e6 >= GRAPH_BELOW_US:
+                continue
+            nl = max(GRAPH_LAUNCHES, len(p["packs"]))  # every L2-rotation copy once per replay
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for k in range(nl):
+                    packed, sp = p["packs"][k % len(p["packs"])]
+                    graph_gemm(p, packed, sp)
+            g.replay()
+            torch.cuda.synchronize()
+            reps = 20
+            g0 = torch.cuda.Event(enable_timing=True)
+            g1 = torch.cuda.Event(enable_timing=True)
+            g0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            g1.record(stream)
+            torch.cuda.synchronize()
+            graph_us[i] = (g0.elapsed_time(g1) / (reps * nl) * 1e3, nl)
+            del g
+        if graph_us and w.w4a16_get_status(ws) != 0:
+            raise RuntimeError("device status error in the CUDA-graph timing")
+
     ms_per_step = reduce_max(ms_total / args.steps, world, device)
     clocks = sampler.finish() if sampler else None
     if rank != 0:
@@ -473,6 +515,11 @@ def run_ours(args, rank, world, device):
                       "tb_s": round(by / (us * 1e-6) / 1e12, 3), "tflops": round(fl / (us * 1e-6) / 1e12, 1),
                       "roofline_frac": round(t_roof / (us * 1e-6), 3), "bound": "hbm" if mem_bound else "tensor",
                       "launches": p["launches"], "kernel": p["kernel"]})
+        if len(sweep) - 1 in graph_us:
+            gus, nl = graph_us[len(sweep) - 1]
+            sweep[-1]["graph_us"] = round(gus, 2)
+            sweep[-1]["graph_launches"] = nl
+            sweep[-1]["graph_roofline_frac"] = round(t_roof / (gus * 1e-6), 3)
         if cublas_us is not None:
             cu = cublas_us[len(sweep) - 1]
             sweep[-1]["cublas_fp16_us"] = round(cu, 2)
