@@ -131,6 +131,29 @@ def test_column_block_permutation_permutes_output(w, path):
     assert np.array_equal(C1[:, perm].view(np.uint16), C2.view(np.uint16))
 
 
+def _linearity_excess(C1, C2, C12, b1, b2, b12):
+    """How far C(A1 + A2) - C(A1) - C(A2) exceeds the sum of the three GEMMs' error bounds
+    (each |C - C_ref| <= 4e-3 * Bound + 1e-4, and the reference is linear in A)."""
+    C1, C2, C12 = (np.asarray(c, dtype=np.float64) for c in (C1, C2, C12))
+    return np.abs(C12 - C1 - C2) - (4e-3 * (b1 + b2 + b12) + 3e-4)
+
+
+def test_linearity_in_activations(w, path):
+    # A1, A2 and A1 + A2 are all exact in FP16 (multiples of 1/16 up to 2 in magnitude)
+    M, K, N, G = 24, 2048, 1024, 128
+    rng = np.random.default_rng(79)
+    A1 = (rng.integers(-16, 17, (M, K)) / 16).astype(np.float16)
+    A2 = (rng.integers(-16, 17, (M, K)) / 16).astype(np.float16)
+    A12 = (A1.astype(np.float64) + A2.astype(np.float64)).astype(np.float16)
+    assert np.array_equal(A12.astype(np.float64), A1.astype(np.float64) + A2.astype(np.float64))
+    q, s = synth.make_weights(K, N, G, 80)
+    _, _, packed, sp = tl.device_layer(w, q, s, G)
+    C1, C2, C12 = (tl.c_numpy(tl.run_gemm(w, A, packed, sp, N, G)) for A in (A1, A2, A12))
+    b1, b2, b12 = (oracle.gemm_ref(A, q, s, G)[1] for A in (A1, A2, A12))
+    ex = _linearity_excess(C1, C2, C12, b1, b2, b12)
+    assert np.all(ex <= 0), f"{int(np.sum(ex > 0))} elements break linearity beyond the bounds"
+
+
 def test_group_invariance(w, path):
     # a scale constant over the groups of each column: group 128 and per-column agree within the bound
     M, K, N = 16, 2048, 512
