@@ -40,6 +40,8 @@ L2_BYTES = 129 * 1024 * 1024
 # overhead, not the kernel, sets a single launch's time), and the minimum launches in that graph
 GRAPH_BELOW_US = 5.0
 GRAPH_LAUNCHES = 20
+# columns of the first layer on which the oracle's repack is timed for the CPU baseline
+REPACK_SAMPLE_COLS = 1024
 
 # workload name -> (description, list of (K, N, groupsize, [M ...]), seed)
 WORKLOADS = {
@@ -130,14 +132,24 @@ def _cpu_sample_child(spec: str):
     import numpy as np
     import oracle
     from mixed_precision_w4a16_gb300 import synth
-    workload, ncols = spec.split(":")
+    workload, ncols, *opts = spec.split(":")
     ncols = int(ncols)
+    time_repack = "repack" in opts
     desc, layers, seed = WORKLOADS[workload]
     total = 0.0
     scaled = 0.0
+    repack = None
     for li, (K, N, G, Ms) in enumerate(layers):
         nc = min(ncols, N)
         q, s = synth.make_weights(K, nc, G, seed * 100 + li)  # same distributions, sample width
+        if li == 0 and time_repack:  # the offline repack of the first layer, on its first REPACK_SAMPLE_COLS columns
+            nr = min(REPACK_SAMPLE_COLS, nc)
+            qr, sr = np.ascontiguousarray(q[:, :nr]), np.ascontiguousarray(s[:, :nr])
+            t0 = time.perf_counter()
+            oracle.repack(qr, sr, G)
+            dt = time.perf_counter() - t0
+            repack = {"seconds": dt, "scaled_seconds": dt * (N / nr), "shape": f"K={K} N={N} G={G}",
+                      "sample": f"{nr} of its N columns, time scaled by N/cols"}
         for M in Ms:
             A = synth.make_activations(M, K, seed * 1000 + M)
             t0 = time.perf_counter()
@@ -145,13 +157,14 @@ def _cpu_sample_child(spec: str):
             dt = time.perf_counter() - t0
             total += dt
             scaled += dt * (N / nc)
-    print(json.dumps({"seconds": total, "scaled_seconds": scaled,
+    print(json.dumps({"seconds": total, "scaled_seconds": scaled, "repack": repack,
                       "sample": f"every GEMM of the workload on {ncols} of its N columns (oracle time scaled by N/cols)"}))
 
 
-def run_cpu_sample(workload: str, ncols: int):
+def run_cpu_sample(workload: str, ncols: int, repack: bool = False):
     env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    out = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample", f"{workload}:{ncols}"],
+    spec = f"{workload}:{ncols}" + (":repack" if repack else "")
+    out = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample", spec],
                          capture_output=True, text=True, env=env, timeout=900)
     if out.returncode != 0:
         raise RuntimeError(f"oracle timing failed: {out.stderr[-2000:]}")
@@ -580,9 +593,12 @@ def run_ours(args, rank, world, device):
     cpu = None
     if not args.no_cpu_baseline:
         ncols = cpu_sample_cols(args.workload)
-        r = run_cpu_sample(args.workload, ncols)
+        r = run_cpu_sample(args.workload, ncols, repack=True)
         cpu = {"value": tb / r["scaled_seconds"] / 1e12, "unit": "TB/s", "cores": 1, "kind": "oracle",
                "sample": r["sample"] + f"; measured {r['seconds']:.1f} s single-threaded"}
+        if r.get("repack"):
+            cpu["oracle_repack_us"] = round(r["repack"]["scaled_seconds"] * 1e6, 1)
+            cpu["oracle_repack_sample"] = f"{r['repack']['shape']}, {r['repack']['sample']}"
 
     return {
         "metric": METRIC, "value": round(value, 4), "unit": "TB/s", "n_gpus": world, "steps": args.steps,
