@@ -234,6 +234,7 @@ class ClockSampler:
         import threading
         self.samples = []
         self.t_start = self.t_end = None
+        self.static = self.read_once(uuid)
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
         if uuid:
             cmd += ["-i", uuid]
@@ -244,6 +245,28 @@ class ClockSampler:
             return
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+
+    @staticmethod
+    def read_once(uuid):
+        """Memory clock (current, max) and ECC mode, read once before the timed region; {} if
+        nvidia-smi cannot tell."""
+        cmd = ["nvidia-smi", "--query-gpu=clocks.mem,clocks.max.mem,ecc.mode.current", "--format=csv,noheader,nounits"]
+        if uuid:
+            cmd += ["-i", uuid]
+        try:
+            out = subprocess.run(cmd, capture_output=True, text=True, timeout=20)
+            parts = [p.strip() for p in out.stdout.strip().splitlines()[0].split(",")]
+        except Exception:
+            return {}
+        if out.returncode != 0 or len(parts) != 3:
+            return {}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        return {"mem_mhz": num(parts[0]), "mem_max_mhz": num(parts[1]), "ecc": parts[2]}
 
     def _read(self):
         for line in self.proc.stdout:
@@ -259,7 +282,8 @@ class ClockSampler:
 
     def finish(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0,
+                    **self.static}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -285,7 +309,7 @@ class ClockSampler:
                           if v.lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
                 "reasons": reasons, "samples": len(inside), "power_w_max": max(power) if power else None,
-                "note": note}
+                "note": note, **self.static}
 
 
 # ---------------------------------------------------------------------------
