@@ -242,3 +242,47 @@ def _segments_with_idle_issuers(w, M, K, N):
 @pytest.mark.parametrize("M,K,N", [(32, 11008, 4096), (64, 11008, 4096), (32, 2816, 4096)])
 def test_idle_issuer_shapes_have_short_segments(w, M, K, N):
     assert _segments_with_idle_issuers(w, M, K, N) > 0
+
+
+def _split_reduction_check(units, T, grid, KU):
+    """The kernels' split-strip bookkeeping against brute force.  A CTA c owns units
+    [c*T, min(units, (c+1)*T)); strip j owns units [j*KU, (j+1)*KU).  For a strip, the kernels
+    take the contributing CTAs as c_first = j*KU // T .. c_last = min(((j+1)*KU - 1) // T, grid - 1);
+    a CTA writes its partial of the strip into slot 2c if the strip is the CTA's first, else
+    2c + 1, and the last arriver reads slot 2c if j == (c*T) // KU, else 2c + 1."""
+    assert (grid - 1) * T < units <= grid * T
+    for j in range(units // KU):
+        lo, hi = j * KU, (j + 1) * KU
+        brute = [c for c in range(grid) if c * T < hi and min(units, (c + 1) * T) > lo]
+        c_first, c_last = (j * KU) // T, min(((j + 1) * KU - 1) // T, grid - 1)
+        assert brute == list(range(c_first, c_last + 1)), (units, T, KU, j)
+        if c_first == c_last:
+            continue  # one CTA holds the whole strip and writes C directly
+        slots = []
+        for c in brute:
+            first_col = (c * T) // KU
+            last_col = (min(units, (c + 1) * T) - 1) // KU
+            assert j in (first_col, last_col), "a split strip is a CTA's first or last strip"
+            written = 2 * c if j == first_col else 2 * c + 1
+            read = 2 * c if j == (c * T) // KU else 2 * c + 1
+            assert written == read
+            slots.append(written)
+        assert len(set(slots)) == len(slots) and max(slots) < 2 * grid
+
+
+@pytest.mark.parametrize("M", [1, 16, 32, 128])
+def test_split_strip_slots_and_counters_cover_each_strip_once(w, M):
+    for K, N in [(1024, 1024), (4096, 4096), (4096, 22016), (11008, 4096), (2816, 4096), (8192, 57344),
+                 (28672, 8192), (18432, 73728), (384, 640), (128, 128), (7168, 4096)]:
+        for G in (128, -1):
+            p = w.w4a16_plan(M, K, N, G, 152)
+            _split_reduction_check(p["units"], p["units_per_cta"], p["grid"], K // p["k_tile"])
+
+
+def test_split_strip_bookkeeping_brute_force_small_grids():
+    for KU in range(1, 13):
+        for strips in range(1, 9):
+            units = KU * strips
+            for sms in range(1, 40):
+                T = (units + sms - 1) // sms
+                _split_reduction_check(units, T, (units + T - 1) // T, KU)
