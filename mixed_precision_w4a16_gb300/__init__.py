@@ -169,6 +169,10 @@ def w4a16_workspace_bytes(M: int, K: int, N: int, groupsize: int) -> int:
     return int(_lib().w4a16_workspace_bytes(M, K, N, groupsize))
 
 
+def w4a16_abi_version() -> int:
+    return int(_lib().w4a16_abi_version())
+
+
 def w4a16_plan(M: int, K: int, N: int, groupsize: int, num_sms: int = 0) -> dict:
     p = Plan()
     _check(_lib().w4a16_plan(M, K, N, groupsize, num_sms, ctypes.byref(p)), "w4a16_plan")

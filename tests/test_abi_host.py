@@ -37,6 +37,12 @@ def test_library_exports_every_declared_symbol(w):
     assert set(_declared_symbols()) <= set(w.EXPORTED_SYMBOLS) | {"w4a16_abi_version"}
 
 
+def test_binding_has_every_entry_point_under_its_c_name(w):
+    missing = [name for name in _declared_symbols() if not callable(getattr(w, name, None))]
+    assert not missing, missing
+    assert w.w4a16_abi_version() == 1
+
+
 def test_library_exports_nothing_else(w):
     # -fvisibility=hidden: only the declared C entry points are dynamic symbols
     import subprocess
