@@ -100,9 +100,13 @@ W4A16_API size_t w4a16_workspace_bytes(int M, int K, int N, int groupsize);
  * contiguous copy.  Code q[k][n] sits in word
  *   (((n/128 * K/64 + k/64) * 8 + (n%128)/16) * 32 + lane) * 4 + (k%64)/16
  * at bits [4*slot, 4*slot+4), with r = n%16, c = k%16,
- *   lane = 4*(r%8) + (c%8)/2,   slot = r/8 + 2*(c/8) + 4*(c%2),
- * i.e. each word is one lane's operand fragment of a 16x16 mma.m16n8k16 block
- * whose 16 rows are output columns.  Permuted scales fp16[N/128][K/G][128]:
+ *   lane = 4*(r%8) + c/4,   slot = r/8 + 2*((c%4)/2) + 4*(c%2),
+ * i.e. register i of lane L = 4g + t (slot i low half, slot i + 4 high half)
+ * holds row g + 8*(i%2) at k = 4t + 2*(i/2) + {0, 1}: each lane owns four
+ * consecutive k of rows g and g + 8 of a 16x16 block whose 16 rows are output
+ * columns (the per-thread fragment of a tcgen05.st.16x256b store; the
+ * mma.m16n8k16 kernel reads the activations in the same k order).
+ * Permuted scales fp16[N/128][K/G][128]:
  * s[g][n] is stored at ((n/128) * K/G + g) * 128 + 16*((n%128)/16) + 2*(r%8) + r/8.
  * Codes above 15 are masked to 4 bits and flag W4A16_ERR_CODE_RANGE for
  * w4a16_get_status(NULL, stream).
