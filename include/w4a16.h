@@ -331,18 +331,19 @@ W4A16_API int w4a16_moe_gemm(const uint16_t* A, const uint32_t* packed, const ui
  * array of W4A16_NOALLOC_SCRATCH_BYTES that every GPU which loads the library
  * holds until the process exits.  The first call on each device looks up the
  * array's device address with that device current; make that first call
- * before any stream capture begins.  Each call then clears the array's status
- * word and arrival counters (cudaMemsetAsync on `stream`) and runs the same
- * kernel as w4a16_gemm.  It calls no cudaMalloc, no cudaFree and no allocating
- * library routine.
+ * before any stream capture begins.  Each call then clears the array's
+ * arrival counters (cudaMemsetAsync on `stream`) and runs the same kernel as
+ * w4a16_gemm, so its result is bitwise identical to w4a16_gemm's.  It calls
+ * no cudaMalloc, no cudaFree and no allocating library routine.
  *
  * All calls share the one array and it keeps the previous call's contents, so
  * two calls that may execute at the same time on the GPU (for example on two
  * streams with no ordering between them) race and corrupt each other's output:
  * order them.  Shapes whose w4a16_workspace_bytes exceed the array are rejected
  * with W4A16_ERR_WORKSPACE before anything is launched.  A pipeline timeout
- * inside this call is recorded in the library's array and is not reported by
- * w4a16_get_status; use w4a16_gemm with your own workspace to observe it.
+ * inside this call is recorded in the status word at the head of the
+ * library's array; later calls leave that word alone, and
+ * w4a16_get_status(NULL, stream) reports it (W4A16_ERR_TIMEOUT) and clears it.
  * ------------------------------------------------------------------------- */
 #define W4A16_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
 
@@ -351,7 +352,9 @@ W4A16_API int w4a16_gemm_noalloc(const uint16_t* A, const uint32_t* packed, cons
 
 /* Synchronises `stream`, then returns (and clears) the first error recorded on
  * the device: the repack code-range flag and, when `workspace` is non-NULL,
- * the GEMM status word in that workspace.  W4A16_OK when none. */
+ * the GEMM status word in that workspace.  With `workspace` NULL, the status
+ * word of w4a16_gemm_noalloc's array takes its place once a call of that entry
+ * point has set the array up on the current device.  W4A16_OK when none. */
 W4A16_API int w4a16_get_status(void* workspace, void* stream);
 
 /* ---------------------------------------------------------------------------

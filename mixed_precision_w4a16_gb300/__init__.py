@@ -270,6 +270,10 @@ def w4a16_dequant_zp(packed, scales_p, zeros_p, K, N, groupsize, bhat, stream=No
                                    _stream(stream)), "w4a16_dequant_zp")
 
 
+# Size of the library's scratch array used by w4a16_gemm_noalloc (W4A16_NOALLOC_SCRATCH_BYTES).
+W4A16_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
+
+
 def w4a16_gemm_noalloc(A, packed, scales_p, C, M, K, N, groupsize, stream=None):
     """The allocation-free GEMM: same operands as w4a16_gemm, no workspace (the library's
     own scratch array is used; calls must not overlap on the GPU)."""

@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/w4a16.h"
 #include "internal.h"
@@ -21,26 +22,38 @@ constexpr long long kDefaultWaitCycles = 2000000000LL;  // ~1 s at GB300 clocks
 std::atomic<long long> g_wait_cycles{0};
 std::atomic<int> g_stall{0};
 
+// Per-device attributes, filled on the device's first use.  Host threads may call
+// the library concurrently: the fields are written once under g_dev_mutex and
+// published by the release store of `ready`; readers acquire it first.
 struct DeviceInfo {
-  int ready = 0;
+  std::atomic<int> ready{0};
   int major = 0, minor = 0;
   int sms = 0;
   int smem_optin = 0;
 };
 DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
 
 int current_device_info(DeviceInfo** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return W4A16_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return W4A16_ERR_CUDA;
   DeviceInfo& d = g_dev[dev];
-  if (!d.ready) {
-    if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-      return W4A16_ERR_CUDA;
-    d.ready = 1;
+  if (!d.ready.load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (!d.ready.load(std::memory_order_relaxed)) {
+      int major = 0, minor = 0, sms = 0, smem = 0;
+      if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return W4A16_ERR_CUDA;
+      d.major = major;
+      d.minor = minor;
+      d.sms = sms;
+      d.smem_optin = smem;
+      d.ready.store(1, std::memory_order_release);
+    }
   }
   *out = &d;
   return (d.major == 10 && d.minor == 3) ? W4A16_OK : W4A16_ERR_ARCH;
@@ -470,7 +483,16 @@ int w4a16_gemm_24(const uint16_t* A, const uint32_t* packed24, const uint16_t* s
 namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[W4A16_NOALLOC_SCRATCH_BYTES];
-void* g_noalloc_addr[kMaxDevices];  // device address of g_noalloc_scratch, per device
+// Device address of g_noalloc_scratch, per device; null until that device's first call.
+// Concurrent first calls may both look it up; they store the same address.
+std::atomic<void*> g_noalloc_addr[kMaxDevices];
+
+// The scratch array of the current device, or null if no call has set it up yet.
+void* noalloc_scratch_if_ready() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  return g_noalloc_addr[dev].load(std::memory_order_acquire);
+}
 
 }  // namespace
 
@@ -490,15 +512,20 @@ int w4a16_gemm_noalloc(const uint16_t* A, const uint32_t* packed, const uint16_t
   if (pl.workspace > W4A16_NOALLOC_SCRATCH_BYTES) return W4A16_ERR_WORKSPACE;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return W4A16_ERR_CUDA;
-  if (!g_noalloc_addr[dev]) {
+  void* ws = g_noalloc_addr[dev].load(std::memory_order_acquire);
+  if (!ws) {
     void* addr = nullptr;  // set-up on this device's first call (must precede any stream capture)
     if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || !addr) return W4A16_ERR_CUDA;
-    g_noalloc_addr[dev] = addr;
+    g_noalloc_addr[dev].store(addr, std::memory_order_release);
+    ws = addr;
   }
-  void* ws = g_noalloc_addr[dev];
-  // the status word and the arrival counters must start at zero; the partial-sum slots need not
-  const size_t clear = kStatusBytes + counter_bytes(pl.strips);
-  if (cudaMemsetAsync(ws, 0, clear, static_cast<cudaStream_t>(stream)) != cudaSuccess) return W4A16_ERR_CUDA;
+  // The arrival counters must start at zero (a timed-out call can leave them set); the
+  // partial-sum slots need not.  The status word at the head is left alone: it is
+  // sticky until w4a16_get_status(NULL, stream) reads and clears it, so a timeout in
+  // one call stays visible however many calls follow.
+  if (cudaMemsetAsync(static_cast<uint8_t*>(ws) + kStatusBytes, 0, counter_bytes(pl.strips),
+                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return W4A16_ERR_CUDA;
   return w4a16_gemm(A, packed, scales_p, C, M, K, N, groupsize, ws, W4A16_NOALLOC_SCRATCH_BYTES, stream);
 }
 
@@ -510,6 +537,9 @@ int w4a16_get_status(void* workspace, void* stream) {
   if (read_and_clear_sparse_flag(&flag24, s) != cudaSuccess) return W4A16_ERR_CUDA;
   flag |= flag24;
   uint32_t word = 0;
+  // Without a workspace, the allocation-free GEMM's status word (in the library's
+  // scratch array, if a call has set it up on this device) is the one reported.
+  if (!workspace) workspace = noalloc_scratch_if_ready();
   if (workspace) {
     if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
       return W4A16_ERR_CUDA;

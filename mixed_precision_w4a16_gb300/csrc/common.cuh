@@ -193,17 +193,27 @@ __device__ __forceinline__ void mma_sp_16832(float d[4], const uint32_t a[4], co
 
 // ---------------------------------------------------------------------------
 // 4-bit -> FP16x2 decode (the Marlin deep-dive article, section "INT4 只是存储
-// 类型": build FP16 bit patterns with LOP3, then one packed FP16 op).
+// 类型，不是这条路径的计算类型": the codes become FP16 values by placing their
+// bits inside FP16 bit patterns, with no integer-to-float conversion).
 //
-// Derivation from binary16: 0x6400 is 1024.0 and its ulp is 1, so OR-ing a
-// code q into the low fraction bits gives exactly 1024 + q; subtracting
-// 1032 (0x6408) gives q - 8.  A code sitting 4 bits higher gives
-// 1024 + 16q; times 1/16 (0x2C00) minus 72 (0xD480) gives q - 8.  Every
-// intermediate is an integer below 2048 or an exact power-of-two multiple,
-// so the decode is exact.
+// Construction, from the binary16 format (10 fraction bits; an exponent e
+// gives the fraction's least significant bit the weight 2^(e - 10)):
+//  * a code in bits 0..3 of a half: choose e = 10 (pattern 0x6400 = 1024.0,
+//    lsb weight 1), so OR-ing the nibble in gives exactly 1024 + q;
+//  * a code in bits 4..7 of a half: choose e = 6 (pattern 0x5400 = 64.0, lsb
+//    weight 1/16), so the nibble's bit 4 weighs 16/16 = 1 and OR-ing it in gives
+//    exactly 64 + q.
+// One packed subtraction of the same pattern with the zero point added to the
+// fraction (1024 + 8 = 0x6408, 64 + 8 = 0x5480) then leaves q - 8: both
+// operands and the difference are exactly representable, so the result is
+// exact.  A zero point z replaces the 8 in that constant (0x6400 | z,
+// 0x5400 | z << 4).
 //
 // Word layout: nibble slot i (bits 4i..4i+3) for i < 4 is the low half and
-// slot i + 4 the high half of operand register i.
+// slot i + 4 the high half of operand register i.  Register i holds slots i
+// and i + 4, i.e. nibble position (i & 1) of byte (i >> 1) in each half word:
+// registers 0 and 2 take position 0 (bits 0..3 of the half after shifting the
+// word right by 8 * (i >> 1)), registers 1 and 3 position 1 (bits 4..7).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
@@ -218,11 +228,6 @@ __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
   return d;
 }
 
-__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
 
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -230,35 +235,41 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   return d;
 }
 
-// One packed word -> four FP16x2 registers holding (q - 8) exactly.
-__device__ __forceinline__ void decode8(uint32_t w, uint32_t a[4]) {
-  constexpr uint32_t kLo = 0x000f000fu, kHi = 0x00f000f0u, kBase = 0x64006400u;
-  constexpr uint32_t k1032 = 0x64086408u;  // 1032.0 in both halves
-  constexpr uint32_t kSixteenth = 0x2c002c00u;  // 1/16
-  constexpr uint32_t kMinus72 = 0xd480d480u;  // -72.0
-  const uint32_t w8 = w >> 8;
-  a[0] = hsub2_u32(lop3_and_or(w, kLo, kBase), k1032);
-  a[1] = hfma2_u32(lop3_and_or(w, kHi, kBase), kSixteenth, kMinus72);
-  a[2] = hsub2_u32(lop3_and_or(w8, kLo, kBase), k1032);
-  a[3] = hfma2_u32(lop3_and_or(w8, kHi, kBase), kSixteenth, kMinus72);
+// Per nibble position p of a half word: the mask selecting it in both halves,
+// the exponent pattern whose fraction lsb weighs 2^-4p, and how a zero point z
+// sits in that pattern's fraction.
+template <int P>
+struct NibblePos {
+  static constexpr uint32_t mask = 0x000f000fu << (4 * P);
+  static constexpr uint32_t base = P == 0 ? 0x64006400u : 0x54005400u;  // 1024.0 / 64.0 in both halves
+  __device__ static constexpr uint32_t offset(uint32_t z) { return ((base & 0xffffu) | (z << (4 * P))) * 0x10001u; }
+};
+
+// The codes of position P of `w` (in both halves), biased by the base: exactly
+// base + q as FP16; subtracting base + z leaves q - z.
+template <int P>
+__device__ __forceinline__ uint32_t nibbles_minus(uint32_t w, uint32_t base_plus_z) {
+  return hsub2_u32(lop3_and_or(w, NibblePos<P>::mask, NibblePos<P>::base), base_plus_z);
 }
 
-// The decode with a zero point z per row instead of the constant 8 (the affine
-// form B^ = s (q - z) of the deep-dive article, section "Marlin 要解决的精确问题").
-// Rows g (registers 0, 2) are always low nibbles, rows g + 8 (registers 1, 3)
-// always high nibbles, so each needs one constant: c_lo = 1024 + z_g in both
-// halves (0x6400 | z), c_hi = -(64 + z_{g+8}) in both halves (0xD400 | z << 4).
-// (1024 + q) - (1024 + z) and (1024 + 16q) / 16 - (64 + z) are exact in FP16.
-__device__ __forceinline__ uint32_t zp_const_lo(uint32_t z) { return (0x6400u | z) * 0x10001u; }
-__device__ __forceinline__ uint32_t zp_const_hi(uint32_t z) { return (0xD400u | (z << 4)) * 0x10001u; }
+// Zero-point constants (base + z in both halves) of positions 0 and 1.
+__device__ __forceinline__ uint32_t zp_const_lo(uint32_t z) { return NibblePos<0>::offset(z); }
+__device__ __forceinline__ uint32_t zp_const_hi(uint32_t z) { return NibblePos<1>::offset(z); }
+
+// One packed word -> four FP16x2 registers holding (q - z) exactly, the zero
+// point given per register position by its constant (c_lo for the codes of
+// rows g, registers 0 and 2; c_hi for rows g + 8, registers 1 and 3).
 __device__ __forceinline__ void decode8_zp(uint32_t w, uint32_t c_lo, uint32_t c_hi, uint32_t a[4]) {
-  constexpr uint32_t kLo = 0x000f000fu, kHi = 0x00f000f0u, kBase = 0x64006400u;
-  constexpr uint32_t kSixteenth = 0x2c002c00u;  // 1/16
-  const uint32_t w8 = w >> 8;
-  a[0] = hsub2_u32(lop3_and_or(w, kLo, kBase), c_lo);
-  a[1] = hfma2_u32(lop3_and_or(w, kHi, kBase), kSixteenth, c_hi);
-  a[2] = hsub2_u32(lop3_and_or(w8, kLo, kBase), c_lo);
-  a[3] = hfma2_u32(lop3_and_or(w8, kHi, kBase), kSixteenth, c_hi);
+  const uint32_t w8 = w >> 8;  // byte 1 of each half moved to byte 0
+  a[0] = nibbles_minus<0>(w, c_lo);
+  a[1] = nibbles_minus<1>(w, c_hi);
+  a[2] = nibbles_minus<0>(w8, c_lo);
+  a[3] = nibbles_minus<1>(w8, c_hi);
+}
+
+// The symmetric format: zero point 8 everywhere.
+__device__ __forceinline__ void decode8(uint32_t w, uint32_t a[4]) {
+  decode8_zp(w, NibblePos<0>::offset(8u), NibblePos<1>::offset(8u), a);
 }
 
 }  // namespace w4a16
