@@ -133,7 +133,7 @@ int w4a16_plan(int M, int K, int N, int groupsize, int num_sms, w4a16_plan_t* ou
   out->path = pl.path;
   out->m_tiles = pl.m_chunk / 8;
   out->m_chunk = pl.m_chunk;
-  out->n_tile = kStrip;
+  out->n_tile = pl.path == 2 ? kTcStrips * kStrip : kStrip;  // the tensor-memory kernel's units span a strip pair
   out->k_tile = pl.k_tile;
   out->units = pl.units;
   out->units_per_cta = pl.T;

@@ -127,65 +127,58 @@ Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin, bool zp, 
   pl.path = 2;
   pl.mb = std::min(128, (std::max(M, 1) + 15) / 16 * 16);
   pl.strips = N / kStrip;
-  // Tensor memory (512 columns): ni accumulators of mb columns (ni * mb <= 256),
-  // the rest for the ring of 64-column A chunks.  Activation stages pair with the
-  // A buffers (one per chunk in flight).
-  pl.ni = 1;  // a power of two: issuer i takes the chunks gc = i mod ni
-  while (2 * pl.ni <= std::min(kTcMaxIssuers, 256 / pl.mb)) pl.ni *= 2;
-  pl.na = std::min(6, (512 - pl.ni * pl.mb) / 64) & ~1;  // even: two activation producers take alternate chunks
-  // Unit depth KT = 128 * ch for the weight ring (one copy per unit, released by
-  // the dequant warps).  Keep >= 8 chunks of weights in flight; among the
-  // candidates, minimise T * unit time (memory time as for the streaming kernel
-  // vs tensor time, ~2.1 ns per mb * ch).
-  int best = 0, best_w = 0;
-  long long best_cost = 0;
-  const int cands[3] = {4, 2, 1};
-  for (int c = 0; c < 3; ++c) {
-    const int ch = cands[c];
-    if (K % (128 * ch) != 0) continue;
-    const int srows = (G == 128) ? ch : 1;
-    const TcLayout l0 = tc_layout(pl.mb, ch, srows, pl.na, 0, zp);
-    const int w_st = std::min(12, (smem_optin - l0.smem_bytes) / (l0.w_stage_bytes + 16));
-    if (w_st < 2 || w_st * ch < 8) continue;
-    const long long units = static_cast<long long>(pl.strips) * (K / (128 * ch));
-    const long long T = (units + sms - 1) / sms;
-    const long long cost = T * (std::max(178LL * ch, (21LL * pl.mb * ch) / 10) + 200);  // + per-unit sync and copy issue
-    if (best == 0 || cost < best_cost) {
-      best = ch;
-      best_w = w_st;
-      best_cost = cost;
-    }
-  }
-  if (!best) {
-    best = 1;
-    const TcLayout l0 = tc_layout(pl.mb, 1, 1, pl.na, 0, zp);
-    best_w = std::max(2, std::min(12, (smem_optin - l0.smem_bytes) / (l0.w_stage_bytes + 16)));
-  }
-  if (ablate & kAblateStages2) best_w = 2;
-  pl.ch = best;
+  const int pairs = (pl.strips + kTcStrips - 1) / kTcStrips;
+  // Tensor memory (512 columns): per strip an accumulator of mb columns and a ring of A
+  // buffers of 64 columns (128 k of FP16) each.
+  pl.ni = kTcStrips;  // one MMA issuer per strip
+  pl.na = std::min(kTcMaxNA, (512 / kTcStrips - pl.mb) / 64);
+  // Unit depth: four 128-row chunks per strip when K allows (each dequant warpgroup then
+  // decodes two chunks per unit and pays the unit's stage wait and loop work once for both),
+  // else two (a unit still feeds all four warpgroups), one when K is an odd multiple of 128.
+  pl.ch = (K % 512 == 0) ? 4 : (K % 256 == 0) ? 2 : 1;
   pl.srows = (G == 128) ? pl.ch : 1;
-  pl.tlay = tc_layout(pl.mb, pl.ch, pl.srows, pl.na, best_w, zp);
-  pl.a_stages = pl.na;
-  pl.w_stages = best_w;
+  // Rings: the weight ring keeps about 100 KB of weights in flight for the HBM latency; the
+  // activation ring takes the rest (up to 8 stages: it hides the L2 latency of the tiles).
+  // Activation tiles of 128 tokens are 32 KB: there the activation ring gets the larger share.
+  const TcLayout l0 = tc_layout(pl.mb, pl.ch, pl.srows, 0, 0, zp);
+  const int budget = smem_optin - l0.smem_bytes;
+  int sw = std::max(2, std::min(kTcMaxSW, (100 * 1024 + l0.w_stage_bytes - 1) / l0.w_stage_bytes));
+  if (pl.mb > 64) sw = 2;
+  if (ablate & kAblateStages2) sw = 2;
+  if (pl.ch == 1) sw &= ~1;  // one-chunk units: an even weight ring (each warpgroup meets every unit of a stage)
+  int ns = std::min(kTcMaxNS, (budget - sw * l0.w_stage_bytes) / l0.a_stage_bytes);
+  while (ns < 2 && sw > 2) {
+    sw -= (pl.ch == 1) ? 2 : 1;
+    ns = std::min(kTcMaxNS, (budget - sw * l0.w_stage_bytes) / l0.a_stage_bytes);
+  }
+  pl.w_stages = sw;
+  pl.a_stages = std::max(2, ns);
+  pl.tlay = tc_layout(pl.mb, pl.ch, pl.srows, pl.a_stages, pl.w_stages, zp);
   pl.m_chunk = pl.mb;
   pl.k_tile = 128 * pl.ch;
-  pl.stages = best_w;
+  pl.stages = pl.w_stages;
   pl.smem_bytes = pl.tlay.smem_bytes;
   pl.threads = kTcThreads;
-  finish_split(pl, K, sms, static_cast<size_t>(kStrip) * pl.mb);
+  pl.KU = K / pl.k_tile;
+  pl.units = pairs * pl.KU;
+  pl.T = (pl.units + sms - 1) / sms;
+  pl.grid = (pl.units + pl.T - 1) / pl.T;
+  pl.workspace = kStatusBytes + counter_bytes(pl.strips) +
+                 2ull * pl.grid * (static_cast<size_t>(kTcStrips) * kStrip * pl.mb) * sizeof(float);
   return pl;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  // looked up once; a function-local static is initialised exactly once even with concurrent callers
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return nullptr;
+  }();
   return fn;
 }
 
@@ -263,9 +256,9 @@ int run_gemm(const Plan& pl, const GemmCall& c) {
     p.K = c.K;
     p.N = c.N;
     p.G = c.G;
+    p.strips = pl.strips;
     p.mb = pl.mb;
     p.ch = pl.ch;
-    p.ni = pl.ni;
     p.na = pl.na;
     p.srows = pl.srows;
     p.KU = pl.KU;
@@ -277,6 +270,7 @@ int run_gemm(const Plan& pl, const GemmCall& c) {
     p.a_stage_bytes = pl.tlay.a_stage_bytes;
     p.w_stage_bytes = pl.tlay.w_stage_bytes;
     p.w_base = pl.tlay.w_base;
+    p.s_off = pl.tlay.s_off;
     p.z_off = pl.tlay.z_off;
     p.bar_off = pl.tlay.bar_off;
     p.flag_off = pl.tlay.flag_off;

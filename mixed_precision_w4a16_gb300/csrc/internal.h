@@ -93,11 +93,18 @@ cudaError_t launch_gemm_sp24(const MmaConfig& cfg, const CUtensorMap& tmA, const
 // with zero points (p.zeros != null) the kernels are built with the per-row zero decode
 
 // ---- tensor-memory (tcgen05) GEMM ----------------------------------------
-constexpr int kTcThreads = 768;  // 3 producers, 4 MMA issuers, 1 idle warp, 16 dequant warps (two teams)
-constexpr int kTcMaxIssuers = 4;
+// 2 single-thread copy producers, 2 MMA issuers (one per strip of a unit), 16 dequant warps
+constexpr int kTcThreads = 640;
+constexpr int kTcStrips = 2;      // 128-column strips per work unit
+constexpr int kTcMaxNA = 3;       // A buffers per strip in tensor memory
+constexpr int kTcMaxNS = 8;       // activation stages
+constexpr int kTcMaxSW = 8;       // weight stages
 
+// Shared-memory layout of one tensor-memory-kernel configuration (byte offsets from the
+// 1024-aligned base): activation stages, then weight stages (each: both strips' packed
+// chunks, their scale rows at s_off, their zero-code rows at z_off), barriers, flags.
 struct TcLayout {
-  int a_stage_bytes, w_stage_bytes, w_base, z_off, bar_off, flag_off, smem_bytes;  // z_off: within a weight stage
+  int a_stage_bytes, w_stage_bytes, w_base, s_off, z_off, bar_off, flag_off, smem_bytes;
 };
 TcLayout tc_layout(int mb, int ch, int srows, int a_stages, int w_stages, bool zp);
 uint32_t tc_idesc(int m, int n);
@@ -109,17 +116,17 @@ struct TcParams {
   const uint16_t* bias;     // fp16[N], or null
   uint16_t* C;
   uint32_t* status;
-  uint32_t* counters;
-  float* slots;             // 2 * grid slots of 128 * mb floats ([token][column])
+  uint32_t* counters;       // one per strip pair
+  float* slots;             // 2 * grid slots of 2 * 128 * mb floats ([strip][token][column])
   int M, m0, K, N, G;
+  int strips;               // N / 128 (the last pair has one strip when odd)
   int mb;                   // token rows of this launch padded to 16 (the MMA's N)
   int ch;                   // 128-row chunks per work unit (KT = 128 * ch)
-  int na;                   // A chunks in the tensor-memory ring (64 columns each, <= 7)
-  int ni;                   // MMA-issuing threads (1..4), each with an accumulator of mb columns
-  int srows;                // scale rows per unit
-  int KU, units, T, grid;
+  int na;                   // A buffers per strip (64 tensor-memory columns each)
+  int srows;                // scale rows per strip and unit
+  int KU, units, T, grid;   // units per strip pair, units, units per CTA, CTAs
   int a_stages, w_stages;   // activation ring / weight ring depths
-  int a_stage_bytes, w_stage_bytes, w_base, z_off, bar_off, flag_off;
+  int a_stage_bytes, w_stage_bytes, w_base, s_off, z_off, bar_off, flag_off;
   uint32_t idesc;
   long long wait_limit;
   int debug_stall;

@@ -1,14 +1,15 @@
 """Discrete-event model of the tensor-memory GEMM kernel's barrier protocol.
 
-The kernel's roles (weight producer, two activation producers, NI MMA issuers, two dequant
-teams and the epilogue) hand work to each other through mbarriers in shared memory.  A parity
-wait on an mbarrier only tells the phase it names from the phase just before it, so a wait that
-runs while the barrier is two phases behind passes at once.  Whether that can happen depends on
-the order in which the roles' waits and the asynchronous work (copies landing, multiplies
-completing) interleave, which a GPU run samples only at its own timing.
+The kernel's roles (weight producer, activation producer, one MMA issuer per strip of a
+two-strip work unit, four dequant warpgroups and their shared epilogue) hand work to each
+other through mbarriers in shared memory.  A parity wait on an mbarrier only tells the phase it
+names from the phase just before it, so a wait that runs while the barrier is two phases
+behind passes at once.  Whether that can happen depends on the order in which the roles' waits
+and the asynchronous work (copies landing, multiplies completing) interleave, which a GPU run
+samples only at its own timing.
 
 This model restates each role's loop of gemm_tc_kernel (its waits, arrivals, copies, multiplies
-and commits, in the kernel's order) and runs it under random interleavings. Each step is one
+and commits, in the kernel's order) and runs it under random interleavings.  Each step is one
 role's next action or the completion of one asynchronous operation, taken uniformly among those
 that can proceed.  It checks after every step:
   * every parity wait that passes finds the phase it meant completed (no aliasing);
@@ -18,6 +19,11 @@ that can proceed.  It checks after every step:
   * nothing overwrites a stage or A buffer that a multiply or a reader still needs;
   * each segment's read-out sees all of that segment's multiplies completed;
   * the run ends (no role is left waiting).
+
+Roles, as in the kernel: warpgroup w of the dequant warps serves strip s = w & 1 of each unit
+and the chunks gs with gs % 2 == w >> 1 of that strip (gs = unit * CH + chunk); before it
+signals a chunk it waits for the chunk's activation stage, so strip s's issuer (one warp, in
+chunk order) waits on the chunk's A-buffer barrier alone.
 
 The model is host-side test code; switches select variants of the protocol, so the tests can
 show that the checks catch the orderings that are wrong.
@@ -68,45 +74,45 @@ class Barrier:
 
 @dataclass
 class Config:
-    NA: int          # A buffers in tensor memory (activation stages too, unless `decoupled`)
-    NI: int          # MMA issuers
+    NA: int          # A buffers per strip in tensor memory
+    NS: int          # activation stages
     CH: int          # 128-row chunks per unit
     SW: int          # weight stages
     nunits: int      # units of this CTA
-    KU: int          # units per strip
-    kt0: int = 0     # unit index within its strip of the CTA's first unit
-    NAS: int = 0     # activation stages when `decoupled` (0: = NA)
-    decoupled: bool = False   # activation ring with its own empty barriers and a second commit
-    afull_first: bool = False  # issuer waits for the activations before the A chunk
-    idle_wait: bool = True     # an issuer without a chunk in a segment waits for the last read-out
-
-    def __post_init__(self):
-        if not self.NAS:
-            self.NAS = self.NA
+    KU: int          # units per strip pair
+    kt0: int = 0     # unit index within its strip pair of the CTA's first unit
+    idle_wempty: bool = True   # dequant warpgroups without a chunk in a unit do not touch its stage
+    dequant_consumed_wait: bool = True  # the dequant waits for the A buffer's previous multiplies
+    dequant_afull_wait: bool = True     # the dequant waits for the chunk's activation stage before
+                                        # signalling the chunk (the issuer then waits on one barrier)
 
     @property
     def nch(self):
         return self.nunits * self.CH
+
+    @property
+    def wreaders(self):
+        return 4 if self.CH >= 2 else 2   # warpgroups that read each unit's weight stage
 
 
 class Model:
     def __init__(self, cfg: Config):
         c = self.cfg = cfg
         self.wfull = [Barrier(f"wfull[{s}]", 1) for s in range(c.SW)]
-        self.wempty = [Barrier(f"wempty[{s}]", 16) for s in range(c.SW)]
-        self.afull = [Barrier(f"afull[{a}]", 1) for a in range(c.NAS)]
-        self.aempty = [Barrier(f"aempty[{a}]", 1) for a in range(c.NAS)]
-        self.cfull = [Barrier(f"cfull[{a}]", 8) for a in range(c.NA)]
-        self.consumed = [Barrier(f"consumed[{a}]", 1) for a in range(c.NA)]
-        self.dfull = Barrier("dfull", c.NI)
-        self.dempty = Barrier("dempty", 8)
+        self.wempty = [Barrier(f"wempty[{s}]", 4 * c.wreaders) for s in range(c.SW)]
+        self.afull = [Barrier(f"afull[{a}]", 1) for a in range(c.NS)]
+        self.aempty = [Barrier(f"aempty[{a}]", 2) for a in range(c.NS)]
+        self.cfull = [[Barrier(f"cfull[{s}][{a}]", 4) for a in range(c.NA)] for s in range(2)]
+        self.consumed = [[Barrier(f"consumed[{s}][{a}]", 1) for a in range(c.NA)] for s in range(2)]
+        self.dfull = Barrier("dfull", 2)
+        self.dempty = Barrier("dempty", 16)
         self.w_content = {}        # weight stage -> unit whose copy landed there
         self.w_reads = {}          # unit -> dequant warps that have read it
         self.a_content = {}        # activation stage -> chunk whose copy landed there
         self.a_inflight = {}       # activation stage -> chunk whose copy is in flight
-        self.decoded = {}          # A buffer -> chunk decoded into it
-        self.mma_done = set()      # chunks whose multiplies completed
-        self.epi_done = 0          # segments read out
+        self.decoded = [{}, {}]    # per strip: A buffer -> chunk decoded into it
+        self.mma_done = [set(), set()]  # per strip: chunks whose multiplies completed
+        self.epi_reads = {}        # segment -> warpgroups that have read it out
         # segments of this CTA: [first chunk, last chunk + 1)
         self.segments = []
         start, kt = 0, c.kt0
@@ -127,111 +133,109 @@ class Model:
             s = it % c.SW
             if it >= c.SW:
                 yield ("wait", self.wempty[s], it // c.SW - 1)
-                self.require(self.w_reads.get(it - c.SW, 0) == 16,
+                self.require(self.w_reads.get(it - c.SW, 0) == 4 * c.wreaders,
                              f"weight copy of unit {it} overwrites stage {s} before unit {it - c.SW} was read")
             yield ("copy", self.wfull[s], lambda s=s, it=it: self.w_content.__setitem__(s, it))
 
-    def act_producer(self, p):
+    def act_producer(self):
         c = self.cfg
-        for gc in range(p, c.nch, 2):
-            a = gc % c.NAS
-            if gc >= c.NAS:
-                yield ("wait", (self.aempty if c.decoupled else self.consumed)[a], gc // c.NAS - 1)
-                self.require(gc - c.NAS in self.mma_done,
-                             f"activation copy of chunk {gc} overwrites stage {a} while chunk {gc - c.NAS} is multiplied")
-            self.a_inflight[a] = gc
+        for gs in range(c.nch):
+            a = gs % c.NS
+            if gs >= c.NS:
+                yield ("wait", self.aempty[a], gs // c.NS - 1)
+                self.require(all(gs - c.NS in d for d in self.mma_done),
+                             f"activation copy of chunk {gs} overwrites stage {a} while chunk {gs - c.NS} is "
+                             f"multiplied")
+            self.a_inflight[a] = gs
 
-            def land(a=a, gc=gc):
-                self.a_content[a] = gc
+            def land(a=a, gs=gs):
+                self.a_content[a] = gs
             yield ("copy", self.afull[a], land)
 
-    def issuer(self, i):
+    def issuer(self, s):
         c = self.cfg
         segs, first, kt = 0, True, c.kt0
         for it in range(c.nunits):
             seg_end = kt == c.KU - 1 or it == c.nunits - 1
-            for cc in range((i - it * c.CH) % c.NI, c.CH, c.NI):
-                gc = it * c.CH + cc
-                a, sa = gc % c.NA, gc % c.NAS
-                waits = [("wait", self.cfull[a], gc // c.NA), ("wait", self.afull[sa], gc // c.NAS)]
-                if c.afull_first:
-                    waits.reverse()
-                for w in waits:
-                    yield w
+            for cc in range(c.CH):
+                gs = it * c.CH + cc
+                a, st = gs % c.NA, gs % c.NS
+                yield ("wait", self.cfull[s][a], gs // c.NA)
+                if not c.dequant_afull_wait:
+                    yield ("wait", self.afull[st], gs // c.NS)
                 if first and segs > 0:
                     yield ("wait", self.dempty, segs - 1)
-                self.require(self.a_content.get(sa) == gc and self.a_inflight.get(sa) == gc,
-                             f"multiply of chunk {gc} reads activation stage {sa} holding chunk "
-                             f"{self.a_content.get(sa)} (copy in flight: {self.a_inflight.get(sa)})")
-                self.require(self.decoded.get(a) == gc,
-                             f"multiply of chunk {gc} reads A buffer {a} holding chunk {self.decoded.get(a)}")
-                if first:
-                    self.require(self.epi_done >= segs,
-                                 f"chunk {gc} restarts issuer {i}'s accumulator before segment {segs - 1} was read out")
-                yield ("mma", i, gc)
-                yield ("commit", i, self.consumed[a])
-                if c.decoupled:
-                    yield ("commit", i, self.aempty[sa])
+                self.require(self.a_content.get(st) == gs and self.a_inflight.get(st) == gs,
+                             f"multiply of chunk {gs} reads activation stage {st} holding chunk "
+                             f"{self.a_content.get(st)} (copy in flight: {self.a_inflight.get(st)})")
+                self.require(self.decoded[s].get(a) == gs,
+                             f"strip {s}: multiply of chunk {gs} reads A buffer {a} holding chunk "
+                             f"{self.decoded[s].get(a)}")
+                if first and segs > 0:
+                    self.require(self.epi_reads.get(segs - 1, 0) == 4,
+                                 f"strip {s}: chunk {gs} restarts the accumulator before segment {segs - 1} was "
+                                 f"read out")
+                yield ("mma", s, gs)
+                yield ("commit", s, self.consumed[s][a])
+                yield ("commit", s, self.aempty[st])
                 first = False
             if seg_end:
-                if c.idle_wait and first and segs > 0:
-                    yield ("wait", self.dempty, segs - 1)
-                yield ("commit", i, self.dfull)
+                yield ("commit", s, self.dfull)
                 segs, first = segs + 1, True
             kt = (kt + 1) % c.KU
 
-    def team(self, t):
+    def warpgroup(self, w):
         c = self.cfg
-        tcount, reuse_from = 0, (c.NA - t + 1) // 2
+        s, r = w & 1, w >> 1
         segs, kt = 0, c.kt0
         for it in range(c.nunits):
-            s = it % c.SW
+            ws = it % c.SW
             seg_end = kt == c.KU - 1 or it == c.nunits - 1
-            yield ("wait", self.wfull[s], it // c.SW)
-            self.require(self.w_content.get(s) == it, f"team {t} reads unit {it} from stage {s} holding unit "
-                                                      f"{self.w_content.get(s)}")
-            self.w_reads[it] = self.w_reads.get(it, 0) + 8
-            yield ("arrive", self.wempty[s], 8)
-            c0 = ((t ^ it) & 1) if c.CH & 1 else t
-            for cc in range(c0, c.CH, 2):
-                gc = it * c.CH + cc
-                a = gc % c.NA
-                if tcount >= reuse_from:
-                    yield ("wait", self.consumed[a], gc // c.NA - 1)
-                if gc >= c.NA:
-                    self.require(gc - c.NA in self.mma_done,
-                                 f"decode of chunk {gc} overwrites A buffer {a} while chunk {gc - c.NA} is multiplied")
-                self.decoded[a] = gc
-                yield ("arrive", self.cfull[a], 8)
-                tcount += 1
-            if seg_end and t == 0:
+            mine = [gs for gs in range(it * c.CH, (it + 1) * c.CH) if gs % 2 == r]
+            if mine or not c.idle_wempty:
+                yield ("wait", self.wfull[ws], it // c.SW)
+                self.require(self.w_content.get(ws) == it, f"warpgroup {w} reads unit {it} from stage {ws} holding "
+                                                           f"unit {self.w_content.get(ws)}")
+                self.w_reads[it] = self.w_reads.get(it, 0) + 4
+                yield ("arrive", self.wempty[ws], 4)
+            for gs in mine:
+                a = gs % c.NA
+                if gs >= c.NA and c.dequant_consumed_wait:
+                    yield ("wait", self.consumed[s][a], gs // c.NA - 1)
+                if gs >= c.NA:
+                    self.require(gs - c.NA in self.mma_done[s],
+                                 f"strip {s}: decode of chunk {gs} overwrites A buffer {a} while chunk {gs - c.NA} "
+                                 f"is multiplied")
+                self.decoded[s][a] = gs
+                if c.dequant_afull_wait:
+                    yield ("wait", self.afull[gs % c.NS], gs // c.NS)
+                yield ("arrive", self.cfull[s][a], 4)
+            if seg_end:
                 yield ("wait", self.dfull, segs)
                 lo, hi = self.segments[segs]
-                pending = [g for g in range(lo, hi) if g not in self.mma_done]
-                self.require(not pending, f"read-out of segment {segs} while chunks {pending} are still multiplied")
-                self.epi_done += 1
-                yield ("arrive", self.dempty, 8)
-            if seg_end:
+                pending = [(t, g) for t in range(2) for g in range(lo, hi) if g not in self.mma_done[t]]
+                self.require(not pending, f"read-out of segment {segs} while {pending} are still multiplied")
+                self.epi_reads[segs] = self.epi_reads.get(segs, 0) + 1
+                yield ("arrive", self.dempty, 4)
                 segs += 1
             kt = (kt + 1) % c.KU
 
     # ---- scheduler ------------------------------------------------------------------------
-    def run(self, rng: random.Random, max_steps: int = 200000):
-        c = self.cfg
-        roles = [self.weight_producer(), self.act_producer(0), self.act_producer(1)]
-        roles += [self.issuer(i) for i in range(c.NI)] + [self.team(0), self.team(1)]
+    def run(self, rng: random.Random, max_steps: int = 400000):
+        roles = [self.weight_producer(), self.act_producer(), self.issuer(0), self.issuer(1)]
+        roles += [self.warpgroup(w) for w in range(4)]
         nxt = {}
         for r in roles:
             self._advance(r, nxt)
         copies = []                                   # (barrier, on-land) in flight
-        fifos = {i: deque() for i in range(c.NI)}     # per issuer: multiplies and commits, in order
+        fifos = {s: deque() for s in range(2)}        # per issuer: multiplies and commits, in order
         for _ in range(max_steps):
             choices = []
             for r, act in nxt.items():
                 if act[0] != "wait" or act[1].parity_passes(act[2]):
                     choices.append(("role", r))
             choices += [("copy", j) for j in range(len(copies))]
-            choices += [("fifo", i) for i, q in fifos.items() if q]
+            choices += [("fifo", s) for s, q in fifos.items() if q]
             if not choices:
                 if nxt:
                     stuck = ", ".join(f"{a[1].name} phase {a[2]}" for a in nxt.values() if a[0] == "wait")
@@ -245,7 +249,7 @@ class Model:
             elif kind == "fifo":
                 item = fifos[x].popleft()
                 if item[0] == "mma":
-                    self.mma_done.add(item[1])
+                    self.mma_done[x].add(item[1])
                 else:
                     item[1].arrive(1)
             else:

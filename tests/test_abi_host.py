@@ -76,11 +76,12 @@ SHAPES = [(1, 1024, 1024), (16, 1024, 1024), (16, 4096, 12288), (1, 11008, 4096)
 def test_plan_stripes_cover_every_unit_once(w, M, K, N):
     for sms in (152, 148, 7):
         p = w.w4a16_plan(M, K, N, 128, sms)
-        # streaming kernel: 2..16 pieces of 64 rows; tensor-memory kernel: 1..4 chunks of 128 rows
+        # streaming kernel: 2..16 pieces of 64 rows, one strip; tensor-memory kernel: 1, 2 or 4 chunks of
+        # 128 rows, a strip pair (the last pair has one strip when N / 128 is odd)
         allowed = (128, 256, 512, 768, 1024) if p["path"] == 1 else (128, 256, 512)
-        assert p["k_tile"] in allowed and K % p["k_tile"] == 0 and p["n_tile"] == 128
+        assert p["k_tile"] in allowed and K % p["k_tile"] == 0 and p["n_tile"] == 128 * p["path"]
         KU = K // p["k_tile"]
-        assert p["units"] == (N // p["n_tile"]) * KU
+        assert p["units"] == -(-N // p["n_tile"]) * KU
         T, grid, U = p["units_per_cta"], p["grid"], p["units"]
         assert grid <= sms and grid * T >= U and (grid - 1) * T < U
         assert p["m_chunk"] == 8 * p["m_tiles"] and p["m_chunk"] >= min(M, 32 if p["path"] == 1 else 128)
@@ -109,7 +110,7 @@ def test_plan_token_tiles_and_kernel_choice(w):
     assert [p["m_chunk"] for p in plans[:4]] == [8, 8, 16, 16]
     # from 17 rows: tensor-memory kernel, tokens padded to 16 (the MMA's N), at most 128 per launch
     assert [p["m_chunk"] for p in plans[4:]] == [32, 32, 48, 64, 128, 128]
-    assert all(p["threads"] == 768 for p in plans[4:]) and all(p["threads"] == 288 for p in plans[:4])
+    assert all(p["threads"] == 640 for p in plans[4:]) and all(p["threads"] == 288 for p in plans[:4])
 
 
 def test_force_path_knob(w):
@@ -123,8 +124,9 @@ def test_force_path_knob(w):
     assert w.w4a16_plan(200, 1024, 1024, 128, 152)["path"] == 2
 
 
-# a streaming-kernel case and a tensor-memory case whose full-design plans are deeper than 2 stages
-ABLATION_CASES = ((4, 4096, 1024), (64, 4096, 4096))
+# a streaming-kernel case and a tensor-memory case (two-chunk units: K a multiple of 256, not 512)
+# whose full-design plans are deeper than 2 stages
+ABLATION_CASES = ((4, 4096, 1024), (64, 4352, 4096))
 
 
 def _plans(w):
@@ -214,40 +216,33 @@ def test_sparse_and_quantiser_entry_points_validate_on_the_host(w):
 def test_big_layer_plans_are_the_measured_ones(w):
     """The plans the benchmark numbers were measured with (K = 18432, N = 73728, G = 128, 152 SMs):
     streaming kernel with 16-piece (1024-row) units in 2 stages up to M = 16, tensor-memory kernel
-    with 512-row units above."""
+    with units of a strip pair x 512 rows above."""
     for M in (1, 8, 16):
         p = w.w4a16_plan(M, 18432, 73728, 128, 152)
         assert (p["path"], p["k_tile"], p["stages"], p["m_chunk"]) == (1, 1024, 2, 8 if M <= 8 else 16)
     for M in (32, 64, 128):
         p = w.w4a16_plan(M, 18432, 73728, 128, 152)
-        assert (p["path"], p["k_tile"], p["m_chunk"]) == (2, 512, M)
+        assert (p["path"], p["k_tile"], p["n_tile"], p["m_chunk"]) == (2, 512, 256, M)
 
 
-def _segments_with_idle_issuers(w, M, K, N):
-    """Count the CTA segments after a CTA's first whose chunks are fewer than the MMA issuers
-    of the tensor-memory plan (the case the GPU test on these shapes exists for)."""
-    p = w.w4a16_plan(M, K, N, 128, 152)
-    assert p["path"] == 2
-    ch, KU, T, units = p["k_tile"] // 128, K // p["k_tile"], p["units_per_cta"], p["units"]
+@pytest.mark.parametrize("M", [17, 32, 48, 64, 80, 128, 1000])
+@pytest.mark.parametrize("K,N", [(11008, 4096), (2816, 4096), (18432, 73728), (8192, 28672), (384, 384), (128, 640)])
+def test_tensor_memory_plans_stay_inside_the_modelled_protocol(w, M, K, N):
+    """The ring depths the planner picks are those the host protocol model checks: one-chunk
+    units (K an odd multiple of 128) need an even weight ring; the A buffers per strip and the
+    accumulators fit the 512 tensor-memory columns (checked again before launch)."""
+    try:
+        w.w4a16_debug_force_path(2)
+        p = w.w4a16_plan(M, K, N, 128, 152)
+    finally:
+        w.w4a16_debug_force_path(0)
+    ch = p["k_tile"] // 128
+    assert ch in (1, 2, 4) and ch == (4 if K % 512 == 0 else 2 if K % 256 == 0 else 1)
+    assert p["stages"] >= 2 and (ch == 2 or p["stages"] % 2 == 0)
     mb = p["m_chunk"]
-    ni = 1
-    while 2 * ni <= min(4, 256 // mb):
-        ni *= 2
-    hits = 0
-    for u0 in range(0, units, T):
-        u1 = min(units, u0 + T)
-        lengths, start = [], u0
-        for u in range(u0, u1):
-            if u % KU == KU - 1 or u == u1 - 1:
-                lengths.append(u - start + 1)
-                start = u + 1
-        hits += sum(1 for L in lengths[1:] if L * ch < ni)
-    return hits
-
-
-@pytest.mark.parametrize("M,K,N", [(32, 11008, 4096), (64, 11008, 4096), (32, 2816, 4096)])
-def test_idle_issuer_shapes_have_short_segments(w, M, K, N):
-    assert _segments_with_idle_issuers(w, M, K, N) > 0
+    assert mb % 16 == 0 and 16 <= mb <= 128
+    na = min(3, (256 - mb) // 64)
+    assert na >= 2 and 2 * (na * 64 + mb) <= 512
 
 
 def _split_reduction_check(units, T, grid, KU):
