@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     const uint32_t box16 = static_cast<uint32_t>(MB * 128) >> 4;
     const uint32_t cfull0 = bar_cfull + 8 * (s * kTcMaxNA), consumed0 = bar_consumed + 8 * (s * kTcMaxNA);
     int a = 0, st = 0, segs = 0, kt = kt0, j = first_pair;
-    uint32_t ph = 0;           // phase bit of A buffer a
+    uint32_t ph = 0, sph = 0;  // phase bits of A buffer a and activation stage st
     bool first = true;         // the next chunk starts the accumulator of a segment
     bool ok = true;
     for (int it = 0; it < nunits; ++it) {
@@ -368,10 +368,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       const bool real = 2 * j + s < p.strips;  // the last pair of an odd strip count has one strip
       for (int c = 0; c < CH; ++c) {
         // The A chunk was written after the multiplies of chunk gs - NA completed (the dequant
-        // waits for them), and this warp waited for chunk gs - NA's A chunk before; so the
-        // parity wait names a unique phase.  The chunk's writers also waited for its activation
-        // stage before signalling it, so one wait covers both operands.
-        ok = mbar_wait_bounded_sleep(cfull0 + 8 * a, ph, p.wait_limit, abort_flag);
+        // waits for them), and this warp waited for chunk gs - NA's A chunk and activation stage
+        // before; so both parity waits name a unique phase.  Both spin: a sleeping wait wakes
+        // a few hundred cycles late, and this warp's chunk-to-chunk latency sets the pace.
+        ok = mbar_wait_bounded(cfull0 + 8 * a, ph, p.wait_limit, abort_flag) &&
+             mbar_wait_bounded(bar_afull + 8 * st, sph, p.wait_limit, abort_flag);
         // the previous segment's accumulator must have been read out
         if (ok && first && segs > 0) ok = mbar_wait_bounded(bar_dempty, (segs - 1) & 1, p.wait_limit, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
@@ -386,7 +387,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           a = 0;
           ph ^= 1u;
         }
-        if (++st == NS) st = 0;
+        if (++st == NS) {
+          st = 0;
+          sph ^= 1u;
+        }
       }
       if (!ok) {
         if (lane == 0) raise_abort();
@@ -437,8 +441,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   const uint32_t cfull0 = bar_cfull + 8 * (s * kTcMaxNA), consumed0 = bar_consumed + 8 * (s * kTcMaxNA);
   // ring position of this warpgroup's next chunk gs (= r, r + 2, ...): A buffer a = gs % NA, phase bit
   // ph = (gs / NA) & 1
-  int gs = r, a = r, ast = r % NS;
-  uint32_t ph = 0, aph = 0;  // and its activation stage ast = gs % NS, phase bit aph = (gs / NS) & 1
+  int gs = r, a = r;
+  uint32_t ph = 0;
   uint32_t stw = sbase + p.w_base;  // weight stage ws
   int ws = 0, wround = 0, segs = 0;
   int j = first_pair, kt = kt0;
@@ -524,18 +528,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             tmem_st_wait();
           }
           tc_fence_before();
-          if (q == 0) {
-            // the chunk's activation stage must have landed before the issuer is told to go:
-            // the issuer then waits on this chunk's barrier alone.  Parity-safe: this warpgroup
-            // waited for the stage's use two phases back (its own chunk gs - 2 NS) before.
-            bool ok = mbar_wait_bounded(bar_afull + 8 * ast, aph, wlim, abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) {
-              if (lane == 0) raise_abort();
-              have = false;
-              break;
-            }
-          }
           __syncwarp();
           if (lane == 0) mbar_arrive(cfull0 + 8 * a);
           gs += 2;
@@ -543,11 +535,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           if (a >= NA) {
             a -= NA;
             ph ^= 1u;
-          }
-          ast += 2;
-          if (ast >= NS) {
-            ast -= NS;
-            aph ^= 1u;
           }
         }
       }

@@ -21,9 +21,8 @@ that can proceed.  It checks after every step:
   * the run ends (no role is left waiting).
 
 Roles, as in the kernel: warpgroup w of the dequant warps serves strip s = w & 1 of each unit
-and the chunks gs with gs % 2 == w >> 1 of that strip (gs = unit * CH + chunk); before it
-signals a chunk it waits for the chunk's activation stage, so strip s's issuer (one warp, in
-chunk order) waits on the chunk's A-buffer barrier alone.
+and the chunks gs with gs % 2 == w >> 1 of that strip (gs = unit * CH + chunk); strip s's
+issuer (one warp, in chunk order) waits for a chunk's A buffer, then for its activation stage.
 
 The model is host-side test code; switches select variants of the protocol, so the tests can
 show that the checks catch the orderings that are wrong.
@@ -83,8 +82,8 @@ class Config:
     kt0: int = 0     # unit index within its strip pair of the CTA's first unit
     idle_wempty: bool = True   # dequant warpgroups without a chunk in a unit do not touch its stage
     dequant_consumed_wait: bool = True  # the dequant waits for the A buffer's previous multiplies
-    dequant_afull_wait: bool = True     # the dequant waits for the chunk's activation stage before
-                                        # signalling the chunk (the issuer then waits on one barrier)
+    dequant_afull_wait: bool = False    # the dequant (instead of the issuer) waits for the chunk's
+                                        # activation stage before signalling the chunk
 
     @property
     def nch(self):

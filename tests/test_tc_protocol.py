@@ -15,6 +15,7 @@ from tc_protocol_model import Config, explore
 PLANNED = [
     ("m32_ch4", Config(NA=3, NS=8, CH=4, SW=2, nunits=8, KU=36, kt0=33)),
     ("m64_ch4", Config(NA=3, NS=4, CH=4, SW=2, nunits=8, KU=36, kt0=33)),
+    ("m64_ch4_short", Config(NA=3, NS=5, CH=4, SW=2, nunits=10, KU=3, kt0=1)),
     ("m128_ch4", Config(NA=2, NS=2, CH=4, SW=2, nunits=8, KU=16, kt0=13)),
     ("m32_ch2", Config(NA=3, NS=8, CH=2, SW=4, nunits=12, KU=43, kt0=38)),
     ("m64_ch2", Config(NA=3, NS=6, CH=2, SW=3, nunits=12, KU=43, kt0=38)),
@@ -59,6 +60,7 @@ def test_odd_activation_ring_is_safe():
     assert err is None, err
 
 
-def test_issuer_waiting_for_the_activations_itself_is_safe_too():
-    err = explore(Config(NA=3, NS=7, CH=2, SW=3, nunits=10, KU=43, kt0=38, dequant_afull_wait=False), seeds=120)
+def test_dequant_waiting_for_the_activations_instead_is_safe_too():
+    err = explore(Config(NA=3, NS=7, CH=2, SW=3, nunits=10, KU=43, kt0=38, dequant_afull_wait=True), seeds=120)
     assert err is None, err
+
