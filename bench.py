@@ -38,7 +38,7 @@ KERNEL_OF_PATH = {1: "gemm_mma_kernel", 2: "gemm_tc_kernel"}
 L2_BYTES = 129 * 1024 * 1024
 # roofline time below which a GEMM is also timed inside a CUDA graph (there the host's launch
 # overhead, not the kernel, sets a single launch's time), and the minimum launches in that graph
-GRAPH_BELOW_US = 5.0
+GRAPH_BELOW_US = 20.0
 GRAPH_LAUNCHES = 20
 # columns of the first layer on which the oracle's repack is timed for the CPU baseline
 REPACK_SAMPLE_COLS = 1024
@@ -879,7 +879,7 @@ def time_sparse24(w, torch, device, peaks, dense_us):
     del nib, meta
     sp = (torch.rand(K // G * N, device=device, generator=gen) * 0.018 + 0.002).to(torch.float16)
     out = []
-    for M in (1, 8, 16):
+    for M in (1, 8, 16, 32, 64):
         A_d = torch.randn(M, K, device=device, generator=gen).to(torch.float16)
         C_d = torch.empty((M, N), dtype=torch.float16, device=device)
         ws = torch.zeros(w.w4a16_workspace_bytes_24(M, K, N, G), dtype=torch.uint8, device=device)

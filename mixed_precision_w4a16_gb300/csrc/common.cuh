@@ -134,6 +134,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Programmatic dependent launch.  A GEMM launched with the programmatic-serialization
+// attribute may start while the previous kernel of its stream is still running: its CTAs
+// set up barriers and tensor memory, then wait here until that kernel has completed and its
+// writes are visible, before touching any global memory (so inputs just written by a repack or
+// by the layer before stay safe).  The kernels allow their own dependents to launch at once:
+// every GEMM grid is a single wave, so a dependent CTA only takes an SM that is free.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -26,15 +26,15 @@ void finish_split(Plan& pl, int K, int sms, size_t slot_floats) {
 }
 
 // moe_E > 0: the grouped expert GEMM (its expert tables take shared memory), with up
-// to moe_cols row segments sharing the SMs.  sp24: the 2:4-sparse stream (3 KB per piece,
-// at most 16 token rows per launch).
+// to moe_cols row segments sharing the SMs.  sp24: the 2:4-sparse stream (3 KB per piece).
+// Up to 32 token rows per launch.
 Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin, bool zp, int moe_E = 0, int moe_cols = 1,
                    int ablate = 0, bool sp24 = false) {
   Plan pl{};
   pl.path = 1;
   pl.sp24 = sp24;
   const int piece_bytes = sp24 ? kPiece24Words * 4 : 4096;
-  const int mc = std::min(std::max(M, 1), sp24 ? 16 : 32);
+  const int mc = std::min(std::max(M, 1), 32);
   const int mt = mc <= 8 ? 1 : mc <= 16 ? 2 : 4;
   pl.strips = N / kStrip;
   // Unit depth KT = 64 * kq (kq up to 16: each of the 4 K-split warps takes every

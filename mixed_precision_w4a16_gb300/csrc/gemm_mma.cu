@@ -205,6 +205,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
+  pdl_launch_dependents();
+  if (MOE) pdl_wait();  // the expert offsets below may come from the previous kernel
   int units = p.units, T = p.T;
   const int* pref = nullptr;  // grouped GEMM: segment prefix per expert [E + 1]
   const int* offs = nullptr;  // grouped GEMM: expert row offsets [E + 1]
@@ -234,6 +236,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     flags[3] = 0;
     mbar_fence_init();
   }
+  if (!MOE) pdl_wait();  // the previous kernel of the stream has completed: global memory is safe
   __syncthreads();
 
   if (warp == kConsumerWarps) {
@@ -575,10 +578,10 @@ if constexpr (SP24) {
 template <int MT, bool ZP, bool MOE = false, bool SP24 = false>
 cudaError_t launch_one(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream) {
   auto kern = gemm_mma_kernel<MT, ZP, MOE, SP24>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem_bytes);
+  static int smem_cache[64];
+  cudaError_t e = ensure_smem(kern, cfg.smem_bytes, smem_cache);
   if (e != cudaSuccess) return e;
-  kern<<<p.grid, kMmaThreads, cfg.smem_bytes, stream>>>(tmA, p);
-  return cudaGetLastError();
+  return launch_overlapped(kern, p.grid, kMmaThreads, cfg.smem_bytes, stream, tmA, p);
 }
 
 }  // namespace
@@ -623,7 +626,8 @@ cudaError_t launch_moe_mma(const MmaConfig& cfg, const CUtensorMap& tmA, const G
 cudaError_t launch_gemm_sp24(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream) {
   switch (cfg.m_tiles) {
     case 1: return launch_one<1, false, false, true>(cfg, tmA, p, stream);
-    case 2: return launch_one<2, false, false, true>(cfg, tmA, p, stream);  // 16 token rows per launch
+    case 2: return launch_one<2, false, false, true>(cfg, tmA, p, stream);
+    case 4: return launch_one<4, false, false, true>(cfg, tmA, p, stream);  // 32 token rows per launch
     default: return cudaErrorInvalidValue;
   }
 }

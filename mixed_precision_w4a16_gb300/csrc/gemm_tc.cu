@@ -241,6 +241,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
     tmem_relinquish();
   }
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel of the stream has completed: global memory is safe
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -686,10 +688,11 @@ cudaError_t launch_gemm_tc(int smem_bytes, const CUtensorMap& tmA, const TcParam
     return cudaErrorInvalidConfiguration;  // outside what the ring protocol and tensor memory allow
   auto kern = p.zeros ? (p.bias ? gemm_tc_kernel<true, true> : gemm_tc_kernel<true, false>)
                       : (p.bias ? gemm_tc_kernel<false, true> : gemm_tc_kernel<false, false>);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  static int smem_cache[4][64];  // per kernel variant
+  const int variant = (p.zeros ? 2 : 0) + (p.bias ? 1 : 0);
+  cudaError_t e = ensure_smem(kern, smem_bytes, smem_cache[variant]);
   if (e != cudaSuccess) return e;
-  kern<<<p.grid, kTcThreads, smem_bytes, stream>>>(tmA, p);
-  return cudaGetLastError();
+  return launch_overlapped(kern, p.grid, kTcThreads, smem_bytes, stream, tmA, p);
 }
 
 }  // namespace w4a16

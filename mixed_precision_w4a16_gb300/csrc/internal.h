@@ -7,6 +7,44 @@
 
 namespace w4a16 {
 
+// Launch of a GEMM kernel that may overlap the tail of the previous kernel in its stream
+// (programmatic dependent launch; the kernel waits with griddepcontrol.wait before any global
+// memory access).  Captured into a CUDA graph it becomes a programmatic edge.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kern)(KArgs...), int grid, int block, int smem, cudaStream_t stream,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(block));
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` once per device (the attribute
+// call costs a driver round trip; later launches that need no more skip it).  `cache` is
+// the kernel's own table of the largest limit set per device.
+template <typename Kern>
+cudaError_t ensure_smem(Kern kern, int bytes, int (&cache)[64]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (__atomic_load_n(&cache[dev], __ATOMIC_ACQUIRE) >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  int cur = __atomic_load_n(&cache[dev], __ATOMIC_RELAXED);
+  while (cur < bytes && !__atomic_compare_exchange_n(&cache[dev], &cur, bytes, true, __ATOMIC_RELEASE,
+                                                     __ATOMIC_RELAXED)) {
+  }
+  return cudaSuccess;
+}
+
 // status bits recorded in the workspace status word / the repack flag
 enum : uint32_t {
   kDevErrCodeRange = 1u << 0,
@@ -88,7 +126,7 @@ constexpr int kStrip = 128;       // output columns per strip / work unit
 cudaError_t launch_gemm_mma(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream);
 // grouped expert GEMM: one launch over all experts (p.expert_off set, p.M = rows of A)
 cudaError_t launch_moe_mma(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream);
-// 2:4-sparse weights (p.packed is the packed 2:4 stream; m_tiles 1 or 2)
+// 2:4-sparse weights (p.packed is the packed 2:4 stream; m_tiles 1, 2 or 4)
 cudaError_t launch_gemm_sp24(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream);
 // with zero points (p.zeros != null) the kernels are built with the per-row zero decode
 

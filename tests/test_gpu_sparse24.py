@@ -43,7 +43,7 @@ def test_repack_unpack_round_trip(w, K, N, G):
     assert w.w4a16_get_status() == 0
 
 
-@pytest.mark.parametrize("M", [1, 5, 8, 13, 16, 33])
+@pytest.mark.parametrize("M", [1, 5, 8, 13, 16, 17, 32, 33, 64, 70])
 @pytest.mark.parametrize("K,N,G", [(1024, 512, 128), (2048, 384, -1), (768, 1280, 128)])
 def test_gemm24_matches_oracle(w, M, K, N, G):
     q, s = synth.make_weights_24(K, N, G, seed=3 * M + K)
@@ -121,9 +121,10 @@ def test_ablations_leave_the_sparse_result_bitwise_unchanged(w):
         w.w4a16_debug_ablate(0)
 
 
-def test_gemm24_big_layer_sampled_strips(w):
-    """K = 18432 (the big layer's depth), N = 8192, M = 16: four 128-column strips against the oracle."""
-    K, N, G, M = 18432, 8192, 128, 16
+@pytest.mark.parametrize("M", [16, 32, 64])
+def test_gemm24_big_layer_sampled_strips(w, M):
+    """K = 18432 (the big layer's depth), N = 8192: four 128-column strips against the oracle."""
+    K, N, G = 18432, 8192, 128
     q, s = synth.make_weights_24(K, N, G, seed=51)
     A = synth.make_activations(M, K, seed=52)
     packed, sp = _device24(w, q, s, G)
