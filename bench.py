@@ -114,6 +114,8 @@ def parse_args():
     ap.add_argument("--no-ablation", action="store_true", help="skip the Figure 12 ablation sweep")
     ap.add_argument("--no-sparse", action="store_true", help="skip the 2:4-sparse GEMM sweep")
     ap.add_argument("--no-prefill", action="store_true", help="skip the compute-bound prefill layer")
+    ap.add_argument("--min-reps", type=int, default=50,
+                    help="launches per GEMM in the per-M statistics (200 below 10 us); fewer only for profiling")
     ap.add_argument("--moe-config", type=int, default=None, help="run only this entry of the MoE sweep (profiling)")
     ap.add_argument("--no-per-expert", action="store_true",
                     help="skip the one-launch-per-expert comparison of the MoE sweep (profiling)")
@@ -585,7 +587,7 @@ def run_ours(args, rank, world, device):
         for i, p in enumerate(points):
             t_roof = max(gemm_bytes(p["M"], p["K"], p["N"], p["G"]) / (peaks["hbm_gbs"] * 1e9),
                          gemm_flops(p["M"], p["K"], p["N"]) / (peaks["bf16_tflops"] * 1e12))
-            reps = max(args.steps, 200 if t_roof < 10e-6 else 50)
+            reps = max(args.steps, 4 * args.min_reps if t_roof < 10e-6 else args.min_reps)
             pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
             for it, (a, b) in enumerate(pairs):
                 packed, sp = p["packs"][it % len(p["packs"])]
@@ -748,7 +750,7 @@ def run_ours(args, rank, world, device):
 
     prefill = None
     if rank == 0 and not args.no_prefill and args.workload == "big" and not args.zero_points:
-        prefill = time_prefill(w, torch, device, peaks, stream, not args.no_cublas)
+        prefill = time_prefill(w, torch, device, peaks, stream, not args.no_cublas, args.min_reps)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -781,7 +783,7 @@ def run_ours(args, rank, world, device):
 PREFILL = (8192, 28672, 128, (256, 512, 1024))
 
 
-def time_prefill(w, torch, device, peaks, stream, with_cublas=True):
+def time_prefill(w, torch, device, peaks, stream, with_cublas=True, min_reps=50):
     """The compute-bound prefill layer (K=8192, N=28672, group 128, M in {256, 512, 1024}),
     outside the timed region: per M the median of 50 launches, cycling through weight copies
     that together exceed 3x L2 (one copy, 117 MB, would fit), against the dense FP16 tensor peak
@@ -807,7 +809,7 @@ def time_prefill(w, torch, device, peaks, stream, with_cublas=True):
         for it in range(3):
             packed, sp = packs[it % copies]
             w.w4a16_gemm(A_d, packed, sp, C_d, M, K, N, G, ws, ws_bytes, stream)
-        reps = 50
+        reps = max(1, min_reps)
         pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
         for it, (a, b) in enumerate(pairs):
             packed, sp = packs[it % copies]
@@ -824,7 +826,7 @@ def time_prefill(w, torch, device, peaks, stream, with_cublas=True):
         tflops = fl / (us * 1e-6) / 1e12
         t_roof = max(by / (peaks["hbm_gbs"] * 1e9), fl / (peaks["bf16_tflops"] * 1e12))
         entry = {"M": M, "K": K, "N": N, "group": G, "us": round(us, 2), "us_p10": round(ts[reps // 10], 2),
-                 "us_p90": round(ts[(9 * reps) // 10], 2), "reps": reps, "tflops": round(tflops, 1),
+                 "us_p90": round(ts[min(reps - 1, (9 * reps) // 10)], 2), "reps": reps, "tflops": round(tflops, 1),
                  "frac_of_tensor_peak": round(tflops / peaks["bf16_tflops"], 3),
                  "frac_of_sustained_tensor_peak": round(tflops / peaks["bf16_tflops_sustained"], 3),
                  "roofline_frac": round(t_roof / (us * 1e-6), 3), "bytes": by,
