@@ -461,25 +461,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         if (!have && lane == 0) raise_abort();
       }
       if (have) {
-        // this warp's words, scales and zero codes of its (up to two) chunks, then release the stage
-        uint4 wv[2][2][2];  // [chunk][block bi][64-row piece h]
-        uint32_t sc[2][2];
-        uint32_t zc[2][2];
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = c0 + 2 * cc;
-          if (c < CH && real) {
+        // This warp's words, scales and zero codes of one chunk at a time: the second chunk's are
+        // read once the first chunk's stores are issued, and the stage is released after the last
+        // read (it is refilled for a unit two units on, so holding it a chunk longer costs nothing).
+        uint4 wv[2][2];  // [block bi][64-row piece h]
+        uint32_t sc[2];
+        uint32_t zc[2];
+        auto load_chunk = [&](int c) {
+          if (real) {
 #pragma unroll
             for (int bi = 0; bi < 2; ++bi) {
 #pragma unroll
-              for (int h = 0; h < 2; ++h) wv[cc][bi][h] = lds128(stw + w_lane + (2 * c + h) * 4096 + bi * 512);
-              sc[cc][bi] = grouped ? lds32(stw + s_lane + c * 256 + bi * 32) : 0x3c003c00u;
-              zc[cc][bi] = ZP ? lds_u16(stw + z_lane + (grouped ? c * 128 : 0) + bi * 16) : 0u;
+              for (int h = 0; h < 2; ++h) wv[bi][h] = lds128(stw + w_lane + (2 * c + h) * 4096 + bi * 512);
+              sc[bi] = grouped ? lds32(stw + s_lane + c * 256 + bi * 32) : 0x3c003c00u;
+              zc[bi] = ZP ? lds_u16(stw + z_lane + (grouped ? c * 128 : 0) + bi * 16) : 0u;
             }
           }
+        };
+        load_chunk(c0);
+        if (c0 + 2 >= CH) {  // the warp's only chunk of the unit: release the stage now
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_wempty + 8 * ws);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_wempty + 8 * ws);
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           if (c0 + 2 * cc >= CH) break;
@@ -496,13 +499,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           if (real) {
 #pragma unroll
             for (int bi = 0; bi < 2; ++bi) {
-              const uint32_t s_g = __byte_perm(sc[cc][bi], 0u, 0x1010u);   // scale of row g in both halves
-              const uint32_t s_g8 = __byte_perm(sc[cc][bi], 0u, 0x3232u);  // scale of row g + 8
-              const uint32_t c_lo = ZP ? zp_const_lo(zc[cc][bi] & 15u) : 0u;
-              const uint32_t c_hi = ZP ? zp_const_hi((zc[cc][bi] >> 8) & 15u) : 0u;
+              const uint32_t s_g = __byte_perm(sc[bi], 0u, 0x1010u);   // scale of row g in both halves
+              const uint32_t s_g8 = __byte_perm(sc[bi], 0u, 0x3232u);  // scale of row g + 8
+              const uint32_t c_lo = ZP ? zp_const_lo(zc[bi] & 15u) : 0u;
+              const uint32_t c_hi = ZP ? zp_const_hi((zc[bi] >> 8) & 15u) : 0u;
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
-                const uint32_t words[4] = {wv[cc][bi][h].x, wv[cc][bi][h].y, wv[cc][bi][h].z, wv[cc][bi][h].w};
+                const uint32_t words[4] = {wv[bi][h].x, wv[bi][h].y, wv[bi][h].z, wv[bi][h].w};
                 uint32_t rr[16];
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
@@ -527,8 +530,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                                        static_cast<uint32_t>(a * kChunkCols + 32 * h), rr);
               }
             }
-            tmem_st_wait();
           }
+          if (cc == 0 && c0 + 2 < CH) {  // the second chunk's words, then release the stage
+            load_chunk(c0 + 2);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_wempty + 8 * ws);
+          }
+          if (real) tmem_st_wait();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(cfull0 + 8 * a);
