@@ -453,13 +453,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     const int c0 = (CH & 1) ? ((r ^ it) & 1) : r;  // this warpgroup's first chunk of the unit (then every second)
     const bool real = 2 * j + s < strips;
     if (c0 < CH) {
-      const bool go = __shfl_sync(0xffffffffu, *abort_flag == 0, 0);
       bool have = false;
-      if (go) {
+      if (!*abort_flag) {
         have = mbar_wait_bounded(bar_wfull + 8 * ws, wround & 1, wlim, abort_flag);
-        have = __all_sync(0xffffffffu, have);
         if (!have && lane == 0) raise_abort();
       }
+      have = __all_sync(0xffffffffu, have);
       if (have) {
         // This warp's words, scales and zero codes of one chunk at a time: the second chunk's are
         // read once the first chunk's stores are issued, and the stage is released after the last
@@ -487,9 +486,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         for (int cc = 0; cc < 2; ++cc) {
           if (c0 + 2 * cc >= CH) break;
           if (gs >= NA) {  // A buffer a is free once the multiplies of chunk gs - NA have completed
-            bool ok = mbar_wait_bounded(consumed0 + 8 * a, ph ^ 1u, wlim, abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) {
+            const bool ok = mbar_wait_bounded(consumed0 + 8 * a, ph ^ 1u, wlim, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) {
               if (lane == 0) raise_abort();
               have = false;
               break;
