@@ -105,7 +105,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="big")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph timing of layers under 5 us")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph timing of layers under 20 us")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--only-m", type=int, default=None, help="run only this M of the sweep (profiling)")
     ap.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS FP16 GEMM on the dequantised weights")
