@@ -368,9 +368,11 @@ typedef struct {
   int m_tiles;       /* m_chunk / 8 */
   int m_chunk;       /* token rows per launch (8, 16 or 32 on path 1; a multiple of 16 up to
                         256 on path 2); launches = ceil(M / m_chunk) */
-  int n_tile;        /* output columns per work unit (one 128-column strip) */
-  int k_tile;        /* reduction rows per work unit (128, 256 or 512) */
-  int units;         /* work units per launch: (N / n_tile) * (K / k_tile) */
+  int n_tile;        /* output columns per work unit: 128 (path 1, and path 2 in its wide
+                        mode) or 256 (path 2, a strip pair) */
+  int k_tile;        /* reduction rows per work unit (path 1: 128 to 1024; path 2: 128, 256
+                        or 512) */
+  int units;         /* work units per launch: ceil(N / n_tile) * (K / k_tile) */
   int units_per_cta; /* T */
   int grid;          /* CTAs per launch */
   int stages;        /* shared-memory pipeline depth */
@@ -394,9 +396,13 @@ W4A16_API void w4a16_debug_set_wait_cycles(long long cycles);
 W4A16_API void w4a16_debug_inject_stall(int enable);
 
 /* Kernel-selection knob (not thread-safe), for tests and measurements: 1 runs
- * every later w4a16_gemm on the streaming mma.sync kernel, 2 on the
- * tensor-memory (tcgen05) kernel, 0 restores the default (tcgen05 from 17 token
- * rows on).  w4a16_workspace_bytes and w4a16_plan follow the same choice. */
+ * every later w4a16_gemm on the streaming mma.sync kernel; 2 on the
+ * tensor-memory (tcgen05) kernel, in strip pairs up to 128 token rows and in
+ * its wide mode (one strip per unit, up to 256 token rows per launch) above;
+ * 3 on the tensor-memory kernel in strip pairs only; 4 on the tensor-memory
+ * kernel in its wide mode wherever K is a multiple of 512 (strip pairs
+ * otherwise); 0 restores the default (the mma.sync kernel up to 16 token rows,
+ * then as 2).  w4a16_workspace_bytes and w4a16_plan follow the same choice. */
 W4A16_API void w4a16_debug_force_path(int path);
 
 /* Ablation switches: the MARLIN paper's Figure 12 ablations (discussed in the

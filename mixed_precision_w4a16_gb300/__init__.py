@@ -294,7 +294,8 @@ def w4a16_debug_inject_stall(enable: bool) -> None:
 
 
 def w4a16_debug_force_path(path: int) -> None:
-    """0 = automatic kernel choice, 1 = streaming mma.sync kernel, 2 = tensor-memory kernel."""
+    """0 = automatic kernel choice, 1 = streaming mma.sync kernel, 2 = tensor-memory kernel (mode by M),
+    3 = tensor-memory kernel in strip pairs only, 4 = tensor-memory kernel in its wide mode where K allows."""
     _lib().w4a16_debug_force_path(int(path))
 
 

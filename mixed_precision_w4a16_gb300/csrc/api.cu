@@ -133,7 +133,7 @@ int w4a16_plan(int M, int K, int N, int groupsize, int num_sms, w4a16_plan_t* ou
   out->path = pl.path;
   out->m_tiles = pl.m_chunk / 8;
   out->m_chunk = pl.m_chunk;
-  out->n_tile = pl.path == 2 ? kTcStrips * kStrip : kStrip;  // the tensor-memory kernel's units span a strip pair
+  out->n_tile = pl.path == 2 ? pl.us * kStrip : kStrip;  // tensor-memory kernel: a strip pair, or one strip (wide)
   out->k_tile = pl.k_tile;
   out->units = pl.units;
   out->units_per_cta = pl.T;
@@ -157,7 +157,7 @@ void w4a16_debug_set_wait_cycles(long long cycles) { g_wait_cycles.store(cycles 
 
 void w4a16_debug_inject_stall(int enable) { g_stall.store(enable ? 1 : 0); }
 
-void w4a16_debug_force_path(int path) { g_force_path.store(path == 1 || path == 2 ? path : 0); }
+void w4a16_debug_force_path(int path) { g_force_path.store(path >= 1 && path <= 4 ? path : 0); }
 
 void w4a16_debug_ablate(int flags) { g_ablate.store(flags & (kAblateNoEvictFirst | kAblateStages2 | kAblateNoSwizzle)); }
 

@@ -15,7 +15,8 @@ namespace w4a16 {
 
 namespace {
 
-constexpr int kTcMinRows = 17;  // from 17 token rows on, the tensor-memory kernel runs
+constexpr int kTcMinRows = 17;   // from 17 token rows on, the tensor-memory kernel runs
+constexpr int kTcWideRows = 129; // from 129 on, in its wide mode (one strip per unit, 256 rows per launch)
 
 void finish_split(Plan& pl, int K, int sms, size_t slot_floats) {
   pl.KU = K / pl.k_tile;
@@ -122,25 +123,39 @@ GemmParams mma_params(const Plan& pl, const GemmCall& c, uint32_t* status, uint3
   return p;
 }
 
-Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin, bool zp, int ablate = 0) {
+// wide: one strip per unit and up to 256 token rows per launch (needs K % 512 == 0), else the
+// strip-pair mode with up to 128.
+Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin, bool zp, int ablate, bool wide) {
   Plan pl{};
   pl.path = 2;
-  pl.mb = std::min(128, (std::max(M, 1) + 15) / 16 * 16);
+  wide = wide && K % 512 == 0;
+  pl.us = wide ? 1 : kTcStrips;
   pl.strips = N / kStrip;
-  const int pairs = (pl.strips + kTcStrips - 1) / kTcStrips;
+  const int cols = (pl.strips + pl.us - 1) / pl.us;  // unit columns: strip pairs, or strips
   // Tensor memory (512 columns): per strip an accumulator of mb columns and a ring of A
   // buffers of 64 columns (128 k of FP16) each.
-  pl.ni = kTcStrips;  // one MMA issuer per strip
-  pl.na = std::min(kTcMaxNA, (512 / kTcStrips - pl.mb) / 64);
-  // Unit depth: four 128-row chunks per strip when K allows (each dequant warpgroup then
-  // decodes two chunks per unit and pays the unit's stage wait and loop work once for both),
-  // else two (a unit still feeds all four warpgroups), one when K is an odd multiple of 128.
-  pl.ch = (K % 512 == 0) ? 4 : (K % 256 == 0) ? 2 : 1;
+  pl.ni = pl.us;  // one MMA issuer per strip
+  if (wide) {
+    // Four A buffers (one per dequant warpgroup) and an accumulator of up to 256 token
+    // columns; the token rows are dealt evenly to the launches.
+    const int launches = (std::max(M, 1) + 255) / 256;
+    pl.mb = std::min(256, ((std::max(M, 1) + launches - 1) / launches + 15) / 16 * 16);
+    pl.na = 4;
+    pl.ch = 4;
+  } else {
+    pl.mb = std::min(128, (std::max(M, 1) + 15) / 16 * 16);
+    pl.na = std::min(3, (512 / kTcStrips - pl.mb) / 64);
+    // Unit depth: four 128-row chunks per strip when K allows (each dequant warpgroup then
+    // decodes two chunks per unit and pays the unit's stage wait and loop work once for both),
+    // else two (a unit still feeds all four warpgroups), one when K is an odd multiple of 128.
+    pl.ch = (K % 512 == 0) ? 4 : (K % 256 == 0) ? 2 : 1;
+  }
   pl.srows = (G == 128) ? pl.ch : 1;
   // Rings: the weight ring keeps about 100 KB of weights in flight for the HBM latency; the
   // activation ring takes the rest (up to 8 stages: it hides the L2 latency of the tiles).
-  // Activation tiles of 128 tokens are 32 KB: there the activation ring gets the larger share.
-  const TcLayout l0 = tc_layout(pl.mb, pl.ch, pl.srows, 0, 0, zp);
+  // Activation tiles of 128 tokens and more are 32 KB and up: there the activation ring gets
+  // the larger share.
+  const TcLayout l0 = tc_layout(pl.us, pl.mb, pl.ch, pl.srows, 0, 0, zp);
   const int budget = smem_optin - l0.smem_bytes;
   int sw = std::max(2, std::min(kTcMaxSW, (100 * 1024 + l0.w_stage_bytes - 1) / l0.w_stage_bytes));
   if (pl.mb > 64) sw = 2;
@@ -153,18 +168,18 @@ Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin, bool zp, 
   }
   pl.w_stages = sw;
   pl.a_stages = std::max(2, ns);
-  pl.tlay = tc_layout(pl.mb, pl.ch, pl.srows, pl.a_stages, pl.w_stages, zp);
+  pl.tlay = tc_layout(pl.us, pl.mb, pl.ch, pl.srows, pl.a_stages, pl.w_stages, zp);
   pl.m_chunk = pl.mb;
   pl.k_tile = 128 * pl.ch;
   pl.stages = pl.w_stages;
   pl.smem_bytes = pl.tlay.smem_bytes;
   pl.threads = kTcThreads;
   pl.KU = K / pl.k_tile;
-  pl.units = pairs * pl.KU;
+  pl.units = cols * pl.KU;
   pl.T = (pl.units + sms - 1) / sms;
   pl.grid = (pl.units + pl.T - 1) / pl.T;
   pl.workspace = kStatusBytes + counter_bytes(pl.strips) +
-                 2ull * pl.grid * (static_cast<size_t>(kTcStrips) * kStrip * pl.mb) * sizeof(float);
+                 2ull * pl.grid * (static_cast<size_t>(pl.us) * kStrip * pl.mb) * sizeof(float);
   return pl;
 }
 
@@ -224,8 +239,9 @@ Plan make_plan24(int M, int K, int N, int G, int sms, int smem_optin, int ablate
 }
 
 Plan make_plan(int M, int K, int N, int G, int sms, int smem_optin, bool zp, int forced_path, int ablate) {
-  const bool tc = forced_path == 2 || (forced_path != 1 && M >= kTcMinRows);
-  return tc ? make_plan_tc(M, K, N, G, sms, smem_optin, zp, ablate)
+  const bool tc = forced_path >= 2 || (forced_path != 1 && M >= kTcMinRows);
+  const bool wide = forced_path == 4 || (forced_path != 3 && M >= kTcWideRows);
+  return tc ? make_plan_tc(M, K, N, G, sms, smem_optin, zp, ablate, wide)
             : make_plan_mma(M, K, N, G, sms, smem_optin, zp, 0, 1, ablate);
 }
 
@@ -257,6 +273,7 @@ int run_gemm(const Plan& pl, const GemmCall& c) {
     p.N = c.N;
     p.G = c.G;
     p.strips = pl.strips;
+    p.us = pl.us;
     p.mb = pl.mb;
     p.ch = pl.ch;
     p.na = pl.na;

@@ -5,20 +5,23 @@
 // mma.sync pipe is the limit.  This kernel feeds the sm_103a 5th-generation
 // tensor cores instead.
 //
-//  * Work unit: a PAIR of 128-column strips x KT = 128*CH reduction rows.  Both
-//    strips' packed chunks (each contiguous along K) and their scale rows are
+//  * Work unit: a PAIR of 128-column strips x KT = 128*CH reduction rows (US = 2),
+//    or, in the wide mode for more than 128 token rows (US = 1), one strip whose
+//    decoded chunks feed multiplies of up to 256 tokens.  The unit's strips'
+//    packed chunks (each contiguous along K) and their scale rows are
 //    streamed into a ring of weight stages by one producer lane (bulk copies, L2
 //    evict-first); the activation tile of each 128-row chunk ([2][MB][64] FP16,
 //    128-byte swizzle) comes through a separate ring from a second producer lane
 //    (3-D tensor copy, L2 evict-last) and serves the multiplies of both strips,
-//    so activations are read from L2 once per 256 output columns.
-//  * Dequant: four warpgroups.  Warpgroup w serves strip w & 1 and the chunks
-//    gs = w >> 1, w >> 1 + 2, ... of it; each of its warps decodes its 32-column
+//    so activations are read from L2 once per 256 output columns (pair mode).
+//  * Dequant: four warpgroups.  Warpgroup w serves strip w % US and the chunks
+//    gs = w / US, w / US + 4 / US, ... of it; each of its warps decodes its 32-column
 //    lane quarter of a whole 128-row chunk (16 packed words per thread: exact
 //    q - 8, times the FP16 group scale with one RNE multiply -- the value
 //    w4a16_dequant returns) and writes it with tcgen05.st.16x256b into that
 //    strip's ring of A buffers in tensor memory (the packed word of lane (g, t)
-//    is that store's fragment: rows g and g + 8, k = 4t .. 4t + 3).
+//    is that store's fragment: rows g and g + 8, k = 4t .. 4t + 3).  In the wide
+//    mode each warpgroup owns one of four A buffers.
 //  * Multiply: one thread per strip issues the chunk's eight
 //    tcgen05.mma.kind::f16 (A = the chunk in tensor memory, 128 rows = the
 //    strip's output columns; B = the activation stage through a shared-memory
@@ -26,7 +29,7 @@
 //    strip), then commits the A buffer and the activation stage.  One issuer
 //    per strip completes its chunks in order, which is what makes every parity
 //    wait of the ring protocol name a unique phase.
-//  * Epilogue, at the end of each strip-pair segment, by all sixteen dequant
+//  * Epilogue, at the end of each unit-column segment, by all sixteen dequant
 //    warps: tcgen05.ld of the accumulators (one output column per thread, 16
 //    tokens per load), the per-column scale when G = K, the bias, and C -- or,
 //    for pairs split between CTAs, FP32 slots reduced by the last arriver in CTA
@@ -179,10 +182,14 @@ constexpr int kBarDempty = kBarDfull + 1;
 constexpr int kBarDrain = kBarDempty + 1;
 constexpr int kBarCount = kBarDrain + 2;
 
+// US: strips per work unit -- 2 (a strip pair, one issuer and two warpgroups per strip), or 1
+// (wide mode: one issuer, four warpgroups each owning one of four A buffers, CH = 4).
 // ZP: codes carry a zero point per group and column (p.zeros), else the constant 8.
-// BIAS: p.bias is added to C.  Both are compile-time so the plain layer's build is unchanged.
-template <bool ZP, bool BIAS>
+// BIAS: p.bias is added to C.  All three are compile-time so the plain layer's build is unchanged.
+template <int US, bool ZP, bool BIAS>
 __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const TcParams p) {
+  static_assert(US == 1 || US == 2, "one or two strips per unit");
+  constexpr int RK = 4 / US;  // warpgroups per strip: each takes every RK-th chunk of it
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -220,18 +227,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   if (threadIdx.x == 0) {
     for (int s = 0; s < SW; ++s) {
       mbar_init(bar_wfull + 8 * s, 1);
-      // units of one chunk are read by two warpgroups (one per strip), deeper units by all four
-      mbar_init(bar_wempty + 8 * s, CH >= 2 ? kDequantWarps : kDequantWarps / 2);
+      // the warpgroups with a chunk in the unit read the stage: all four, or (pair mode, units of
+      // one chunk) one per strip
+      mbar_init(bar_wempty + 8 * s, CH * US >= 4 ? kDequantWarps : 4 * CH * US);
     }
     for (int a = 0; a < NS; ++a) {
       mbar_init(bar_afull + 8 * a, 1);
-      mbar_init(bar_aempty + 8 * a, kTcStrips);  // both strips' multiplies read the stage
+      mbar_init(bar_aempty + 8 * a, US);  // every strip's multiplies read the stage
     }
     for (int i = 0; i < kTcStrips * kTcMaxNA; ++i) {
       mbar_init(bar_cfull + 8 * i, 4);      // the four warps of the writing warpgroup
       mbar_init(bar_consumed + 8 * i, 1);   // the strip's issuer
     }
-    mbar_init(bar_dfull, kTcStrips);
+    mbar_init(bar_dfull, US);
     mbar_init(bar_dempty, kDequantWarps);
     for (int i = 0; i < kTcStrips; ++i) mbar_init(bar_drain + 8 * i, 1);
     for (int i = 0; i < 4; ++i) flags[i] = 0;  // flags[4] receives the tensor-memory address
@@ -273,13 +281,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           break;
         }
         if (!(p.debug_stall && it == 0)) {  // with debug_stall, stage 0 stays empty: nothing completes its barrier
-          const int nst = (2 * j + 1 < p.strips) ? 2 : 1;
+          const int nst = (US == 2 && 2 * j + 1 < p.strips) ? 2 : 1;
           const uint32_t fb = bar_wfull + 8 * s;
           const uint32_t st = sbase + p.w_base + s * p.w_stage_bytes;
           mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nst) * (w_bytes + s_bytes + (ZP ? z_bytes : 0u)));
           const int grp0 = (p.G == 128) ? kt * p.srows : 0;
           for (int t = 0; t < nst; ++t) {
-            const long long strip = 2 * j + t;
+            const long long strip = US * j + t;
             bulk_g2s(st + t * w_bytes, p.packed + (strip * (p.K / 64) + static_cast<long long>(kt) * 2 * CH) * 1024,
                      w_bytes, fb, pol);
             bulk_g2s(st + p.s_off + t * s_bytes, p.scales + (strip * NG + grp0) * 128, s_bytes, fb, pol_s);
@@ -354,8 +362,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     // Warp s multiplies every chunk of strip s of every unit, in order.  The whole warp runs
     // the loop with warp-uniform state; each multiply and commit is issued by one elected lane.
     const int s = warp - kIssuerWarp0;
+    if (s >= US) {  // wide mode: one issuer
+      __syncwarp();
+      named_bar_sync(3, kTcThreads);
+      return;
+    }
     const uint32_t a_tmem = tmem + static_cast<uint32_t>(s * NA * kChunkCols);
-    const uint32_t d_tmem = tmem + static_cast<uint32_t>(kTcStrips * NA * kChunkCols + s * MB);
+    const uint32_t d_tmem = tmem + static_cast<uint32_t>(US * NA * kChunkCols + s * MB);
     const uint32_t lo0 = smem_desc_sw128_lo(sbase);  // activation stage 0 sits at the base
     const uint32_t hi = smem_desc_sw128_hi();
     const uint32_t stage16 = static_cast<uint32_t>(p.a_stage_bytes) >> 4;
@@ -367,7 +380,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     bool ok = true;
     for (int it = 0; it < nunits; ++it) {
       const bool seg_end = (kt == p.KU - 1) || (it == nunits - 1);
-      const bool real = 2 * j + s < p.strips;  // the last pair of an odd strip count has one strip
+      const bool real = US * j + s < p.strips;  // the last pair of an odd strip count has one strip
       for (int c = 0; c < CH; ++c) {
         // The A chunk was written after the multiplies of chunk gs - NA completed (the dequant
         // waits for them), and this warp waited for chunk gs - NA's A chunk and activation stage
@@ -383,7 +396,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         if (real)
           tc_mma_chunk(d_tmem, a_tmem + a * kChunkCols, lo0 + st * stage16, hi, box16, p.idesc, first ? 0u : 1u);
         tc_commit_warp(consumed0 + 8 * a);     // A buffer free once these multiplies complete
-        tc_commit_warp(bar_aempty + 8 * st);   // activation stage: one of its two strips done
+        tc_commit_warp(bar_aempty + 8 * st);   // activation stage: one of its strips done
         first = false;
         if (++a == NA) {
           a = 0;
@@ -426,8 +439,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   const int KU = p.KU, strips = p.strips, w_stage_bytes = p.w_stage_bytes;
   const long long wlim = p.wait_limit;
   const int wg = dw >> 2;
-  const int s = wg & 1;               // strip of the pair this warpgroup serves
-  const int r = wg >> 1;              // it takes that strip's chunks gs with gs % 2 == r
+  const int s = wg % US;              // strip of the unit this warpgroup serves
+  const int r = wg / US;              // it takes that strip's chunks gs with gs % RK == r
   const int q = warp & 3;             // tensor-memory lane quarter: rows 32q .. 32q + 31 (blocks 2q, 2q + 1)
   const int g = lane >> 2;
   const bool grouped = p.G == 128;
@@ -441,8 +454,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   // tensor-memory address of this warp's lane quarter in this strip's A ring
   const uint32_t t_warp = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(s * NA * kChunkCols);
   const uint32_t cfull0 = bar_cfull + 8 * (s * kTcMaxNA), consumed0 = bar_consumed + 8 * (s * kTcMaxNA);
-  // ring position of this warpgroup's next chunk gs (= r, r + 2, ...): A buffer a = gs % NA, phase bit
-  // ph = (gs / NA) & 1
+  // ring position of this warpgroup's next chunk gs (= r, r + RK, ...): A buffer a = gs % NA, phase
+  // bit ph = (gs / NA) & 1
   int gs = r, a = r;
   uint32_t ph = 0;
   uint32_t stw = sbase + p.w_base;  // weight stage ws
@@ -450,8 +463,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   int j = first_pair, kt = kt0;
   for (int it = 0; it < nunits; ++it) {
     const bool seg_end = (kt == KU - 1) || (it == nunits - 1);
-    const int c0 = (CH & 1) ? ((r ^ it) & 1) : r;  // this warpgroup's first chunk of the unit (then every second)
-    const bool real = 2 * j + s < strips;
+    // this warpgroup's first chunk of the unit (then every RK-th; the wide mode has CH = 4)
+    const int c0 = (US == 2 && (CH & 1)) ? ((r ^ it) & 1) : r;
+    const bool real = US * j + s < strips;
     if (c0 < CH) {
       bool have = false;
       if (!*abort_flag) {
@@ -478,13 +492,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           }
         };
         load_chunk(c0);
-        if (c0 + 2 >= CH) {  // the warp's only chunk of the unit: release the stage now
+        if (c0 + RK >= CH) {  // the warp's only chunk of the unit: release the stage now
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_wempty + 8 * ws);
         }
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
-          if (c0 + 2 * cc >= CH) break;
+          if (c0 + RK * cc >= CH) break;
           if (gs >= NA) {  // A buffer a is free once the multiplies of chunk gs - NA have completed
             const bool ok = mbar_wait_bounded(consumed0 + 8 * a, ph ^ 1u, wlim, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) {
@@ -529,8 +543,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
               }
             }
           }
-          if (cc == 0 && c0 + 2 < CH) {  // the second chunk's words, then release the stage
-            load_chunk(c0 + 2);
+          if (cc == 0 && c0 + RK < CH) {  // the second chunk's words, then release the stage
+            load_chunk(c0 + RK);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_wempty + 8 * ws);
           }
@@ -538,8 +552,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(cfull0 + 8 * a);
-          gs += 2;
-          a += 2;
+          gs += RK;
+          a += RK;
           if (a >= NA) {
             a -= NA;
             ph ^= 1u;
@@ -548,7 +562,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       }
     }
     if (seg_end) {
-      // ------------------------------------------------------ epilogue (strip pair j), all dequant warps
+      // ------------------------------------------------ epilogue (unit column j), all dequant warps
       named_bar_sync(1, kEpiThreads);
       if (dw == 0 && lane == 0) *seg_abort = *abort_flag;
       named_bar_sync(1, kEpiThreads);
@@ -563,28 +577,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       if (!*seg_abort) {
         tc_fence_after();
         const int row = 32 * q + lane;  // output column within its strip
-        const int nst = (2 * j + 1 < strips) ? 2 : 1;
+        const int nst = (US == 2 && 2 * j + 1 < strips) ? 2 : 1;
         const int ngrp = MB / 16;       // 16-token groups of the accumulator
         const int ntask = nst * ngrp;   // (strip, token group) read-outs, dealt to the warpgroups
         float scale[2], bias_n[2];
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          const int strip = min(2 * j + t, strips - 1);
+          const int strip = min(US * j + t, strips - 1);
           scale[t] = grouped ? 1.f
                              : __half2float(__ushort_as_half(p.scales[static_cast<long long>(strip) * NG * 128 + scale_pos(row)]));
           bias_n[t] = BIAS ? __half2float(__ushort_as_half(p.bias[strip * kStrip + row])) : 0.f;
         }
-        const uint32_t dbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(kTcStrips * NA * kChunkCols);
+        const uint32_t dbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(US * NA * kChunkCols);
         const int c_first = (j * KU) / p.T;
         const int c_last = min(((j + 1) * KU - 1) / p.T, p.grid - 1);
-        const int slot_floats = kTcStrips * MB * 128;
+        const int slot_floats = US * MB * 128;
         if (c_first == c_last) {
           for (int e = wg; e < ntask; e += 4) {
             const int t = e / ngrp, grp = e - t * ngrp;
             uint32_t v[16];
             tmem_ld_32x32b_x16(dbase + static_cast<uint32_t>(t * MB + grp * 16), v);
             tmem_ld_wait();
-            const long long n = static_cast<long long>(2 * j + t) * kStrip + row;
+            const long long n = static_cast<long long>(US * j + t) * kStrip + row;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int token = p.m0 + grp * 16 + i;
@@ -623,7 +637,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             // independent, so their latencies overlap
             for (int e = wg; e < ntask; e += 4) {
               const int t = e / ngrp, grp = e - t * ngrp;
-              const long long n = static_cast<long long>(2 * j + t) * kStrip + row;
+              const long long n = static_cast<long long>(US * j + t) * kStrip + row;
               for (int m = 0; m < 16 && p.m0 + grp * 16 + m < p.M; m += 8) {
                 float acc[8];
 #pragma unroll
@@ -667,13 +681,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
 
 }  // namespace
 
-TcLayout tc_layout(int mb, int ch, int srows, int a_stages, int w_stages, bool zp) {
+TcLayout tc_layout(int us, int mb, int ch, int srows, int a_stages, int w_stages, bool zp) {
   TcLayout l{};
   l.a_stage_bytes = 2 * mb * 128;  // one 128-row chunk: a multiple of 1024 keeps the swizzle atoms aligned
-  // weight stage: both strips' packed chunks, their scale rows, then (with zero points) their zero rows
-  l.s_off = kTcStrips * ch * kPairBytes;
-  l.z_off = l.s_off + kTcStrips * srows * 256;
-  l.w_stage_bytes = (l.z_off + (zp ? kTcStrips * srows * 128 : 0) + 1023) / 1024 * 1024;
+  // weight stage: the unit's strips' packed chunks, their scale rows, then (with zero points) their zero rows
+  l.s_off = us * ch * kPairBytes;
+  l.z_off = l.s_off + us * srows * 256;
+  l.w_stage_bytes = (l.z_off + (zp ? us * srows * 128 : 0) + 1023) / 1024 * 1024;
   l.w_base = a_stages * l.a_stage_bytes;
   l.bar_off = l.w_base + w_stages * l.w_stage_bytes;
   l.flag_off = l.bar_off + 8 * kBarCount;
@@ -688,15 +702,24 @@ uint32_t tc_idesc(int m, int n) {
 }
 
 cudaError_t launch_gemm_tc(int smem_bytes, const CUtensorMap& tmA, const TcParams& p, cudaStream_t stream) {
-  if (p.na < 2 || p.na > kTcMaxNA || p.a_stages < 2 || p.a_stages > kTcMaxNS || p.w_stages < 2 ||
-      p.w_stages > kTcMaxSW || (p.ch == 1 && (p.w_stages & 1)) || p.mb < 16 || p.mb > 128 || (p.mb & 15) ||
-      kTcStrips * (p.na * kChunkCols + p.mb) > kTmemCols)
-    return cudaErrorInvalidConfiguration;  // outside what the ring protocol and tensor memory allow
-  auto kern = p.zeros ? (p.bias ? gemm_tc_kernel<true, true> : gemm_tc_kernel<true, false>)
-                      : (p.bias ? gemm_tc_kernel<false, true> : gemm_tc_kernel<false, false>);
-  static int smem_cache[4][64];  // per kernel variant
-  const int variant = (p.zeros ? 2 : 0) + (p.bias ? 1 : 0);
-  cudaError_t e = ensure_smem(kern, smem_bytes, smem_cache[variant]);
+  // outside what the ring protocol and tensor memory allow: pair mode 2..3 A buffers per strip and
+  // up to 128 token rows, an even weight ring for one-chunk units; wide mode four A buffers, units
+  // of four chunks and up to 256 token rows
+  const bool pair_ok = p.us == 2 && p.na >= 2 && p.na <= 3 && p.mb <= 128 && !(p.ch == 1 && (p.w_stages & 1));
+  const bool wide_ok = p.us == 1 && p.na == 4 && p.ch == 4 && p.mb <= 256;
+  if (!(pair_ok || wide_ok) || p.a_stages < 2 || p.a_stages > kTcMaxNS || p.w_stages < 2 ||
+      p.w_stages > kTcMaxSW || p.mb < 16 || (p.mb & 15) || p.us * (p.na * kChunkCols + p.mb) > kTmemCols)
+    return cudaErrorInvalidConfiguration;
+  using Kern = void (*)(const CUtensorMap, const TcParams);
+  static const Kern kerns[2][2][2] = {
+      {{gemm_tc_kernel<1, false, false>, gemm_tc_kernel<1, false, true>},
+       {gemm_tc_kernel<1, true, false>, gemm_tc_kernel<1, true, true>}},
+      {{gemm_tc_kernel<2, false, false>, gemm_tc_kernel<2, false, true>},
+       {gemm_tc_kernel<2, true, false>, gemm_tc_kernel<2, true, true>}}};
+  const int zp = p.zeros ? 1 : 0, bias = p.bias ? 1 : 0;
+  const Kern kern = kerns[p.us - 1][zp][bias];
+  static int smem_cache[8][64];  // per kernel variant
+  cudaError_t e = ensure_smem(kern, smem_bytes, smem_cache[(p.us - 1) * 4 + zp * 2 + bias]);
   if (e != cudaSuccess) return e;
   return launch_overlapped(kern, p.grid, kTcThreads, smem_bytes, stream, tmA, p);
 }

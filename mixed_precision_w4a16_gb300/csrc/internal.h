@@ -133,8 +133,8 @@ cudaError_t launch_gemm_sp24(const MmaConfig& cfg, const CUtensorMap& tmA, const
 // ---- tensor-memory (tcgen05) GEMM ----------------------------------------
 // 2 single-thread copy producers, 2 MMA issuers (one per strip of a unit), 16 dequant warps
 constexpr int kTcThreads = 640;
-constexpr int kTcStrips = 2;      // 128-column strips per work unit
-constexpr int kTcMaxNA = 3;       // A buffers per strip in tensor memory
+constexpr int kTcStrips = 2;      // 128-column strips per work unit (pair mode; the wide mode has one)
+constexpr int kTcMaxNA = 4;       // A buffers per strip in tensor memory
 constexpr int kTcMaxNS = 8;       // activation stages
 constexpr int kTcMaxSW = 8;       // weight stages
 
@@ -144,7 +144,7 @@ constexpr int kTcMaxSW = 8;       // weight stages
 struct TcLayout {
   int a_stage_bytes, w_stage_bytes, w_base, s_off, z_off, bar_off, flag_off, smem_bytes;
 };
-TcLayout tc_layout(int mb, int ch, int srows, int a_stages, int w_stages, bool zp);
+TcLayout tc_layout(int us, int mb, int ch, int srows, int a_stages, int w_stages, bool zp);
 uint32_t tc_idesc(int m, int n);
 
 struct TcParams {
@@ -154,15 +154,16 @@ struct TcParams {
   const uint16_t* bias;     // fp16[N], or null
   uint16_t* C;
   uint32_t* status;
-  uint32_t* counters;       // one per strip pair
-  float* slots;             // 2 * grid slots of 2 * 128 * mb floats ([strip][token][column])
+  uint32_t* counters;       // one per unit column (strip pair, or strip in the wide mode)
+  float* slots;             // 2 * grid slots of us * 128 * mb floats ([strip][token][column])
   int M, m0, K, N, G;
   int strips;               // N / 128 (the last pair has one strip when odd)
+  int us;                   // strips per unit: 2 (pair mode) or 1 (wide mode)
   int mb;                   // token rows of this launch padded to 16 (the MMA's N)
   int ch;                   // 128-row chunks per work unit (KT = 128 * ch)
-  int na;                   // A buffers per strip (64 tensor-memory columns each)
+  int na;                   // A buffers per strip (64 tensor-memory columns each): 2..3, or 4 wide
   int srows;                // scale rows per strip and unit
-  int KU, units, T, grid;   // units per strip pair, units, units per CTA, CTAs
+  int KU, units, T, grid;   // units per unit column (strip pair or strip), units, units per CTA, CTAs
   int a_stages, w_stages;   // activation ring / weight ring depths
   int a_stage_bytes, w_stage_bytes, w_base, s_off, z_off, bar_off, flag_off;
   uint32_t idesc;
@@ -199,6 +200,7 @@ struct Plan {
   MmaLayout lay;     // path 1
   TcLayout tlay;     // path 2
   int mb, ch;        // path 2: token rows per launch (multiple of 16), 128-row chunks per unit
+  int us;            // path 2: strips per unit (2 = pair mode, 1 = wide mode)
   int a_stages, w_stages;  // path 2: activation / weight ring depths
   int ni, na;        // path 2: MMA issuers (accumulators), A chunks in tensor memory (= a_stages)
   int m_chunk;       // token rows per launch
@@ -215,7 +217,8 @@ struct Plan {
 // rows beyond M read as zero.
 int encode_a_map(CUtensorMap* map, const uint16_t* A, int M, int K, int box_rows, int kq, bool swizzle = true);
 
-// forced_path: 0 = by M, 1 = streaming kernel, 2 = tensor-memory kernel; zp: the GEMM reads
+// forced_path: 0 = by M, 1 = streaming kernel, 2 = tensor-memory kernel (mode by M), 3 = tensor-memory
+// kernel in pair mode only, 4 = tensor-memory kernel in wide mode where K allows it; zp: the GEMM reads
 // zero points (their rows take shared-memory stage space next to the scales)
 Plan make_plan(int M, int K, int N, int G, int sms, int smem_optin, bool zp, int forced_path, int ablate = 0);
 

@@ -20,9 +20,10 @@ that can proceed.  It checks after every step:
   * each segment's read-out sees all of that segment's multiplies completed;
   * the run ends (no role is left waiting).
 
-Roles, as in the kernel: warpgroup w of the dequant warps serves strip s = w & 1 of each unit
-and the chunks gs with gs % 2 == w >> 1 of that strip (gs = unit * CH + chunk); strip s's
-issuer (one warp, in chunk order) waits for a chunk's A buffer, then for its activation stage.
+Roles, as in the kernel: a unit holds US strips (2, or 1 in the wide mode for large M).  Warpgroup
+w of the dequant warps serves strip s = w % US of each unit and the chunks gs with
+gs % (4 / US) == w // US of that strip (gs = unit * CH + chunk); strip s's issuer (one warp, in
+chunk order) waits for a chunk's A buffer, then for its activation stage.
 
 The model is host-side test code; switches select variants of the protocol, so the tests can
 show that the checks catch the orderings that are wrong.
@@ -84,6 +85,7 @@ class Config:
     dequant_consumed_wait: bool = True  # the dequant waits for the A buffer's previous multiplies
     dequant_afull_wait: bool = False    # the dequant (instead of the issuer) waits for the chunk's
                                         # activation stage before signalling the chunk
+    US: int = 2      # strips per unit: 2, or 1 (wide mode: four warpgroups on one strip)
 
     @property
     def nch(self):
@@ -91,7 +93,11 @@ class Config:
 
     @property
     def wreaders(self):
-        return 4 if self.CH >= 2 else 2   # warpgroups that read each unit's weight stage
+        return min(4, self.CH * self.US)  # warpgroups that read each unit's weight stage
+
+    @property
+    def ranks(self):
+        return 4 // self.US               # warpgroups per strip
 
 
 class Model:
@@ -100,10 +106,10 @@ class Model:
         self.wfull = [Barrier(f"wfull[{s}]", 1) for s in range(c.SW)]
         self.wempty = [Barrier(f"wempty[{s}]", 4 * c.wreaders) for s in range(c.SW)]
         self.afull = [Barrier(f"afull[{a}]", 1) for a in range(c.NS)]
-        self.aempty = [Barrier(f"aempty[{a}]", 2) for a in range(c.NS)]
+        self.aempty = [Barrier(f"aempty[{a}]", c.US) for a in range(c.NS)]
         self.cfull = [[Barrier(f"cfull[{s}][{a}]", 4) for a in range(c.NA)] for s in range(2)]
         self.consumed = [[Barrier(f"consumed[{s}][{a}]", 1) for a in range(c.NA)] for s in range(2)]
-        self.dfull = Barrier("dfull", 2)
+        self.dfull = Barrier("dfull", c.US)
         self.dempty = Barrier("dempty", 16)
         self.w_content = {}        # weight stage -> unit whose copy landed there
         self.w_reads = {}          # unit -> dequant warps that have read it
@@ -142,7 +148,7 @@ class Model:
             a = gs % c.NS
             if gs >= c.NS:
                 yield ("wait", self.aempty[a], gs // c.NS - 1)
-                self.require(all(gs - c.NS in d for d in self.mma_done),
+                self.require(all(gs - c.NS in self.mma_done[t] for t in range(c.US)),
                              f"activation copy of chunk {gs} overwrites stage {a} while chunk {gs - c.NS} is "
                              f"multiplied")
             self.a_inflight[a] = gs
@@ -185,12 +191,12 @@ class Model:
 
     def warpgroup(self, w):
         c = self.cfg
-        s, r = w & 1, w >> 1
+        s, r = w % c.US, w // c.US
         segs, kt = 0, c.kt0
         for it in range(c.nunits):
             ws = it % c.SW
             seg_end = kt == c.KU - 1 or it == c.nunits - 1
-            mine = [gs for gs in range(it * c.CH, (it + 1) * c.CH) if gs % 2 == r]
+            mine = [gs for gs in range(it * c.CH, (it + 1) * c.CH) if gs % c.ranks == r]
             if mine or not c.idle_wempty:
                 yield ("wait", self.wfull[ws], it // c.SW)
                 self.require(self.w_content.get(ws) == it, f"warpgroup {w} reads unit {it} from stage {ws} holding "
@@ -212,7 +218,7 @@ class Model:
             if seg_end:
                 yield ("wait", self.dfull, segs)
                 lo, hi = self.segments[segs]
-                pending = [(t, g) for t in range(2) for g in range(lo, hi) if g not in self.mma_done[t]]
+                pending = [(t, g) for t in range(c.US) for g in range(lo, hi) if g not in self.mma_done[t]]
                 self.require(not pending, f"read-out of segment {segs} while {pending} are still multiplied")
                 self.epi_reads[segs] = self.epi_reads.get(segs, 0) + 1
                 yield ("arrive", self.dempty, 4)
@@ -221,13 +227,13 @@ class Model:
 
     # ---- scheduler ------------------------------------------------------------------------
     def run(self, rng: random.Random, max_steps: int = 400000):
-        roles = [self.weight_producer(), self.act_producer(), self.issuer(0), self.issuer(1)]
+        roles = [self.weight_producer(), self.act_producer()] + [self.issuer(s) for s in range(self.cfg.US)]
         roles += [self.warpgroup(w) for w in range(4)]
         nxt = {}
         for r in roles:
             self._advance(r, nxt)
         copies = []                                   # (barrier, on-land) in flight
-        fifos = {s: deque() for s in range(2)}        # per issuer: multiplies and commits, in order
+        fifos = {s: deque() for s in range(self.cfg.US)}  # per issuer: multiplies and commits, in order
         for _ in range(max_steps):
             choices = []
             for r, act in nxt.items():

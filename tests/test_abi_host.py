@@ -77,9 +77,12 @@ def test_plan_stripes_cover_every_unit_once(w, M, K, N):
     for sms in (152, 148, 7):
         p = w.w4a16_plan(M, K, N, 128, sms)
         # streaming kernel: 2..16 pieces of 64 rows, one strip; tensor-memory kernel: 1, 2 or 4 chunks of
-        # 128 rows, a strip pair (the last pair has one strip when N / 128 is odd)
+        # 128 rows, a strip pair (the last pair has one strip when N / 128 is odd), or in its wide mode
+        # (from 129 token rows, K a multiple of 512) 4 chunks of one strip
         allowed = (128, 256, 512, 768, 1024) if p["path"] == 1 else (128, 256, 512)
-        assert p["k_tile"] in allowed and K % p["k_tile"] == 0 and p["n_tile"] == 128 * p["path"]
+        wide = p["path"] == 2 and M >= 129 and K % 512 == 0
+        assert p["k_tile"] in allowed and K % p["k_tile"] == 0
+        assert p["n_tile"] == (128 if p["path"] == 1 or wide else 256)
         KU = K // p["k_tile"]
         assert p["units"] == -(-N // p["n_tile"]) * KU
         T, grid, U = p["units_per_cta"], p["grid"], p["units"]
@@ -104,13 +107,20 @@ def test_plan_stripes_cover_every_unit_once(w, M, K, N):
 
 
 def test_plan_token_tiles_and_kernel_choice(w):
-    plans = [w.w4a16_plan(m, 1024, 1024, 128, 152) for m in (1, 8, 9, 16, 17, 32, 33, 64, 250, 1000)]
+    ms = (1, 8, 9, 16, 17, 32, 33, 64, 128, 129, 250, 300, 1000)
+    plans = [w.w4a16_plan(m, 1024, 1024, 128, 152) for m in ms]
     # up to 16 rows: streaming mma.sync kernel, 8-row token tiles
-    assert [p["path"] for p in plans] == [1, 1, 1, 1, 2, 2, 2, 2, 2, 2]
+    assert [p["path"] for p in plans] == [1] * 4 + [2] * 9
     assert [p["m_chunk"] for p in plans[:4]] == [8, 8, 16, 16]
-    # from 17 rows: tensor-memory kernel, tokens padded to 16 (the MMA's N), at most 128 per launch
-    assert [p["m_chunk"] for p in plans[4:]] == [32, 32, 48, 64, 128, 128]
+    # from 17 rows: tensor-memory kernel, tokens padded to 16 (the MMA's N), strip pairs and at most
+    # 128 rows per launch; from 129 rows its wide mode, one strip per unit and the rows dealt evenly
+    # to launches of at most 256
+    assert [p["m_chunk"] for p in plans[4:]] == [32, 32, 48, 64, 128, 144, 256, 160, 256]
+    assert [p["n_tile"] for p in plans[4:]] == [256] * 5 + [128] * 4
     assert all(p["threads"] == 640 for p in plans[4:]) and all(p["threads"] == 288 for p in plans[:4])
+    # the wide mode needs units of four 128-row chunks: K = 768 stays in strip pairs
+    p = w.w4a16_plan(300, 768, 1024, 128, 152)
+    assert (p["n_tile"], p["m_chunk"], p["k_tile"]) == (256, 128, 256)
 
 
 def test_force_path_knob(w):
@@ -119,6 +129,13 @@ def test_force_path_knob(w):
         assert w.w4a16_plan(1, 1024, 1024, 128, 152)["path"] == 2
         w.w4a16_debug_force_path(1)
         assert w.w4a16_plan(200, 1024, 1024, 128, 152)["path"] == 1
+        w.w4a16_debug_force_path(3)  # tensor memory, strip pairs only
+        p = w.w4a16_plan(1000, 1024, 1024, 128, 152)
+        assert (p["path"], p["n_tile"], p["m_chunk"]) == (2, 256, 128)
+        w.w4a16_debug_force_path(4)  # tensor memory, wide mode wherever K allows
+        p = w.w4a16_plan(32, 1024, 1024, 128, 152)
+        assert (p["path"], p["n_tile"], p["m_chunk"]) == (2, 128, 32)
+        assert w.w4a16_plan(32, 768, 1024, 128, 152)["n_tile"] == 256
     finally:
         w.w4a16_debug_force_path(0)
     assert w.w4a16_plan(200, 1024, 1024, 128, 152)["path"] == 2
@@ -225,24 +242,34 @@ def test_big_layer_plans_are_the_measured_ones(w):
         assert (p["path"], p["k_tile"], p["n_tile"], p["m_chunk"]) == (2, 512, 256, M)
 
 
-@pytest.mark.parametrize("M", [17, 32, 48, 64, 80, 128, 1000])
+@pytest.mark.parametrize("M", [17, 32, 48, 64, 80, 128, 129, 256, 1000])
 @pytest.mark.parametrize("K,N", [(11008, 4096), (2816, 4096), (18432, 73728), (8192, 28672), (384, 384), (128, 640)])
-def test_tensor_memory_plans_stay_inside_the_modelled_protocol(w, M, K, N):
+@pytest.mark.parametrize("force", [2, 3, 4])
+def test_tensor_memory_plans_stay_inside_the_modelled_protocol(w, M, K, N, force):
     """The ring depths the planner picks are those the host protocol model checks: one-chunk
     units (K an odd multiple of 128) need an even weight ring; the A buffers per strip and the
-    accumulators fit the 512 tensor-memory columns (checked again before launch)."""
+    accumulators fit the 512 tensor-memory columns (checked again before launch).  The wide mode
+    has four-chunk units, four A buffers and one strip per unit."""
     try:
-        w.w4a16_debug_force_path(2)
+        w.w4a16_debug_force_path(force)
         p = w.w4a16_plan(M, K, N, 128, 152)
     finally:
         w.w4a16_debug_force_path(0)
     ch = p["k_tile"] // 128
-    assert ch in (1, 2, 4) and ch == (4 if K % 512 == 0 else 2 if K % 256 == 0 else 1)
-    assert p["stages"] >= 2 and (ch == 2 or p["stages"] % 2 == 0)
     mb = p["m_chunk"]
-    assert mb % 16 == 0 and 16 <= mb <= 128
-    na = min(3, (256 - mb) // 64)
-    assert na >= 2 and 2 * (na * 64 + mb) <= 512
+    assert mb % 16 == 0 and mb >= 16 and p["stages"] >= 2
+    wide = K % 512 == 0 and (force == 4 or (force == 2 and M >= 129))
+    if wide:
+        assert p["n_tile"] == 128 and ch == 4 and mb <= 256 and 4 * 64 + mb <= 512
+        launches = -(-M // mb)
+        assert launches == -(-M // 256) and mb >= -(-M // launches)
+    else:
+        assert p["n_tile"] == 256
+        assert ch in (1, 2, 4) and ch == (4 if K % 512 == 0 else 2 if K % 256 == 0 else 1)
+        assert ch == 2 or p["stages"] % 2 == 0
+        assert mb <= 128
+        na = min(3, (256 - mb) // 64)
+        assert na >= 2 and 2 * (na * 64 + mb) <= 512
 
 
 def _split_reduction_check(units, T, grid, KU):
@@ -271,7 +298,7 @@ def _split_reduction_check(units, T, grid, KU):
         assert len(set(slots)) == len(slots) and max(slots) < 2 * grid
 
 
-@pytest.mark.parametrize("M", [1, 16, 32, 128])
+@pytest.mark.parametrize("M", [1, 16, 32, 128, 256, 1000])
 def test_split_strip_slots_and_counters_cover_each_strip_once(w, M):
     for K, N in [(1024, 1024), (4096, 4096), (4096, 22016), (11008, 4096), (2816, 4096), (8192, 57344),
                  (28672, 8192), (18432, 73728), (384, 640), (128, 128), (7168, 4096)]:

@@ -57,7 +57,12 @@ def test_70b_layers(w, K, N, G):
 
 
 def test_prefill_layer(w):
-    check_layer(w, 8192, 28672, 128, [256, 512, 1024], seed=400)
+    # the tensor-memory kernel's wide mode: 256 token rows per launch (300 = two launches of 160)
+    check_layer(w, 8192, 28672, 128, [256, 300, 512, 1024], seed=400)
+
+
+def test_big_layer_wide_mode(w):
+    check_layer(w, 18432, 73728, 128, [200], seed=210)
 
 
 # K not a multiple of 512: the tensor-memory path runs 256-row units, and some CTAs' ranges end
@@ -83,9 +88,21 @@ def test_segments_with_idle_issuers(w, M, K, N):
 # about 1 of 6 runs of the 70B-style down-projection below.  The reduction order is fixed, so
 # every repetition on the same buffers must equal the first bit for bit; the first is held to
 # the oracle on sampled columns (all columns for the small shapes).
-@pytest.mark.parametrize("M,K,N,G,reps", [(32, 8192, 57344, -1, 24), (32, 11008, 4096, 128, 24),
-                                          (64, 11008, 4096, 128, 24), (32, 2816, 4096, 128, 24)])
-def test_tensor_memory_protocol_repeats(w, M, K, N, G, reps):
+# The wide mode (one strip per unit, four A buffers) is guarded the same way, at its own sizes and
+# forced onto a small token count.
+@pytest.mark.parametrize("M,K,N,G,reps,force", [
+    (32, 8192, 57344, -1, 24, 0), (32, 11008, 4096, 128, 24, 0), (64, 11008, 4096, 128, 24, 0),
+    (32, 2816, 4096, 128, 24, 0), (256, 8192, 28672, 128, 24, 0), (1000, 8192, 4096, -1, 24, 0),
+    (32, 8192, 57344, -1, 24, 4)])
+def test_tensor_memory_protocol_repeats(w, M, K, N, G, reps, force):
+    w.w4a16_debug_force_path(force)
+    try:
+        _protocol_repeats(w, M, K, N, G, reps)
+    finally:
+        w.w4a16_debug_force_path(0)
+
+
+def _protocol_repeats(w, M, K, N, G, reps):
     torch = tl.torch_mod()
     q, s = synth.make_weights(K, N, G, 800 + M + K % 7)
     _, _, packed, sp = tl.device_layer(w, q, s, G)

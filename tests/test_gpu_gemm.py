@@ -19,16 +19,19 @@ def w():
     return tl.lib()
 
 
-@pytest.fixture(params=[1, 2], ids=["mma_sync", "tcgen05"])
+@pytest.fixture(params=[1, 2, 4], ids=["mma_sync", "tcgen05", "tcgen05_wide"])
 def path(request, w):
-    """Run the test on the streaming mma.sync kernel and on the tensor-memory kernel."""
+    """Run the test on the streaming mma.sync kernel, on the tensor-memory kernel (strip pairs up to
+    128 token rows, its wide mode above), and on the tensor-memory kernel in its wide mode at every M
+    (where K is a multiple of 512; other K fall back to strip pairs)."""
     w.w4a16_debug_force_path(request.param)
     yield request.param
     w.w4a16_debug_force_path(0)
 
 
-# token counts around every 8-row tile edge and the 64-row launch chunk
-M_EDGES = [1, 2, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 100, 128, 129]
+# token counts around every 8-row tile edge, the launch chunks (128 rows in strip pairs, up to 256
+# rows dealt evenly in the wide mode)
+M_EDGES = [1, 2, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 100, 128, 129, 200, 256, 257, 400]
 
 
 @pytest.mark.parametrize("M", M_EDGES)

@@ -10,7 +10,7 @@ import w4a16_testlib as tl
 
 pytestmark = pytest.mark.gpu
 
-PATHS = {"mma_sync": 1, "tcgen05": 2}
+PATHS = {"mma_sync": 1, "tcgen05": 2, "tcgen05_wide": 4}
 
 
 @pytest.fixture(scope="module")

@@ -24,6 +24,13 @@ PLANNED = [
     ("m128_ch1", Config(NA=2, NS=4, CH=1, SW=6, nunits=7, KU=5, kt0=2)),
     ("one_unit_per_cta", Config(NA=3, NS=6, CH=2, SW=3, nunits=1, KU=43, kt0=5)),
     ("short_segments", Config(NA=3, NS=6, CH=2, SW=3, nunits=9, KU=2, kt0=1)),
+    # wide mode (M > 128): one strip per unit, each of the four warpgroups owns one of four A
+    # buffers and one chunk of every four-chunk unit; one issuer; 256 / 192 / 128 token rows
+    ("wide_mb256", Config(NA=4, NS=2, CH=4, SW=2, nunits=24, KU=16, kt0=8, US=1)),
+    ("wide_mb192", Config(NA=4, NS=3, CH=4, SW=2, nunits=24, KU=16, kt0=8, US=1)),
+    ("wide_mb128_big_layer", Config(NA=4, NS=4, CH=4, SW=2, nunits=20, KU=36, kt0=30, US=1)),
+    ("wide_short_segments", Config(NA=4, NS=2, CH=4, SW=2, nunits=9, KU=2, kt0=1, US=1)),
+    ("wide_one_unit_per_cta", Config(NA=4, NS=2, CH=4, SW=2, nunits=1, KU=16, kt0=3, US=1)),
 ]
 
 
@@ -64,3 +71,15 @@ def test_dequant_waiting_for_the_activations_instead_is_safe_too():
     err = explore(Config(NA=3, NS=7, CH=2, SW=3, nunits=10, KU=43, kt0=38, dequant_afull_wait=True), seeds=120)
     assert err is None, err
 
+
+def test_wide_mode_with_three_buffers_is_caught():
+    # four warpgroups round-robin over three A buffers: a warpgroup's wait for a buffer's previous
+    # multiplies can name a phase two behind (the kernel requires four buffers in the wide mode)
+    err = explore(Config(NA=3, NS=2, CH=4, SW=2, nunits=24, KU=16, kt0=8, US=1), seeds=200)
+    assert err is not None
+
+
+def test_wide_mode_without_the_buffer_wait_is_caught():
+    err = explore(Config(NA=4, NS=2, CH=4, SW=2, nunits=24, KU=16, kt0=8, US=1, dequant_consumed_wait=False),
+                  seeds=200)
+    assert err is not None
