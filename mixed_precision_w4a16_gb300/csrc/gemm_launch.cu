@@ -136,11 +136,12 @@ Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin, bool zp, 
   // buffers of 64 columns (128 k of FP16) each.
   pl.ni = pl.us;  // one MMA issuer per strip
   if (wide) {
-    // Four A buffers (one per dequant warpgroup) and an accumulator of up to 256 token
-    // columns; the token rows are dealt evenly to the launches.
+    // An accumulator of up to 256 token columns (the token rows are dealt evenly to the
+    // launches) and as many A buffers as the rest of tensor memory holds: four (one per
+    // dequant warpgroup) at 256 tokens, up to seven for fewer.
     const int launches = (std::max(M, 1) + 255) / 256;
     pl.mb = std::min(256, ((std::max(M, 1) + launches - 1) / launches + 15) / 16 * 16);
-    pl.na = 4;
+    pl.na = std::min(kTcMaxNA, (512 - pl.mb) / 64);
     pl.ch = 4;
   } else {
     pl.mb = std::min(128, (std::max(M, 1) + 15) / 16 * 16);

@@ -21,7 +21,7 @@
 //    w4a16_dequant returns) and writes it with tcgen05.st.16x256b into that
 //    strip's ring of A buffers in tensor memory (the packed word of lane (g, t)
 //    is that store's fragment: rows g and g + 8, k = 4t .. 4t + 3).  In the wide
-//    mode each warpgroup owns one of four A buffers.
+//    mode the four warpgroups take turns over four to seven A buffers.
 //  * Multiply: one thread per strip issues the chunk's eight
 //    tcgen05.mma.kind::f16 (A = the chunk in tensor memory, 128 rows = the
 //    strip's output columns; B = the activation stage through a shared-memory
@@ -183,7 +183,7 @@ constexpr int kBarDrain = kBarDempty + 1;
 constexpr int kBarCount = kBarDrain + 2;
 
 // US: strips per work unit -- 2 (a strip pair, one issuer and two warpgroups per strip), or 1
-// (wide mode: one issuer, four warpgroups each owning one of four A buffers, CH = 4).
+// (wide mode: one issuer, four warpgroups taking turns over four to seven A buffers, CH = 4).
 // ZP: codes carry a zero point per group and column (p.zeros), else the constant 8.
 // BIAS: p.bias is added to C.  All three are compile-time so the plain layer's build is unchanged.
 template <int US, bool ZP, bool BIAS>
@@ -703,10 +703,10 @@ uint32_t tc_idesc(int m, int n) {
 
 cudaError_t launch_gemm_tc(int smem_bytes, const CUtensorMap& tmA, const TcParams& p, cudaStream_t stream) {
   // outside what the ring protocol and tensor memory allow: pair mode 2..3 A buffers per strip and
-  // up to 128 token rows, an even weight ring for one-chunk units; wide mode four A buffers, units
-  // of four chunks and up to 256 token rows
+  // up to 128 token rows, an even weight ring for one-chunk units; wide mode four to seven A
+  // buffers, units of four chunks and up to 256 token rows
   const bool pair_ok = p.us == 2 && p.na >= 2 && p.na <= 3 && p.mb <= 128 && !(p.ch == 1 && (p.w_stages & 1));
-  const bool wide_ok = p.us == 1 && p.na == 4 && p.ch == 4 && p.mb <= 256;
+  const bool wide_ok = p.us == 1 && p.na >= 4 && p.na <= kTcMaxNA && p.ch == 4 && p.mb <= 256;
   if (!(pair_ok || wide_ok) || p.a_stages < 2 || p.a_stages > kTcMaxNS || p.w_stages < 2 ||
       p.w_stages > kTcMaxSW || p.mb < 16 || (p.mb & 15) || p.us * (p.na * kChunkCols + p.mb) > kTmemCols)
     return cudaErrorInvalidConfiguration;

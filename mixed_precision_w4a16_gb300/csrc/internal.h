@@ -134,7 +134,7 @@ cudaError_t launch_gemm_sp24(const MmaConfig& cfg, const CUtensorMap& tmA, const
 // 2 single-thread copy producers, 2 MMA issuers (one per strip of a unit), 16 dequant warps
 constexpr int kTcThreads = 640;
 constexpr int kTcStrips = 2;      // 128-column strips per work unit (pair mode; the wide mode has one)
-constexpr int kTcMaxNA = 4;       // A buffers per strip in tensor memory
+constexpr int kTcMaxNA = 7;       // A buffers per strip in tensor memory
 constexpr int kTcMaxNS = 8;       // activation stages
 constexpr int kTcMaxSW = 8;       // weight stages
 

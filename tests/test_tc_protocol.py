@@ -31,6 +31,12 @@ PLANNED = [
     ("wide_mb128_big_layer", Config(NA=4, NS=4, CH=4, SW=2, nunits=20, KU=36, kt0=30, US=1)),
     ("wide_short_segments", Config(NA=4, NS=2, CH=4, SW=2, nunits=9, KU=2, kt0=1, US=1)),
     ("wide_one_unit_per_cta", Config(NA=4, NS=2, CH=4, SW=2, nunits=1, KU=16, kt0=3, US=1)),
+    # fewer token rows leave room for more A buffers (up to seven): a warpgroup's buffer then
+    # last held another warpgroup's chunk
+    ("wide_mb192_na5", Config(NA=5, NS=3, CH=4, SW=2, nunits=24, KU=16, kt0=8, US=1)),
+    ("wide_mb128_na6", Config(NA=6, NS=4, CH=4, SW=2, nunits=20, KU=36, kt0=30, US=1)),
+    ("wide_mb64_na7", Config(NA=7, NS=8, CH=4, SW=3, nunits=20, KU=36, kt0=30, US=1)),
+    ("wide_mb32_na7_short", Config(NA=7, NS=8, CH=4, SW=4, nunits=9, KU=2, kt0=1, US=1)),
 ]
 
 
