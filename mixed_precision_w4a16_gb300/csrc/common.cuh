@@ -95,6 +95,14 @@ __device__ __forceinline__ bool mbar_wait_bounded_sleep(uint32_t bar, uint32_t p
 // ---------------------------------------------------------------------------
 // L2 cache policies and bulk / tensor copies into shared memory
 // ---------------------------------------------------------------------------
+
+// Warms L2 with `bytes` (a multiple of 16) from the 16-byte aligned global address `src`.  A
+// prefetch cannot make a later read return stale data (device memory is kept coherent in L2), so
+// a kernel may issue it before waiting for the previous kernel of the stream: the weights of its
+// first work units then stream from HBM while that kernel drains.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

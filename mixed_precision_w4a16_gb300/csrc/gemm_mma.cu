@@ -235,6 +235,24 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     flags[2] = 0;
     flags[3] = 0;
     mbar_fence_init();
+    if (!MOE) {
+      // the weights and scales of the first units (as many as the stages hold) into L2 while the
+      // previous kernel drains
+      constexpr uint32_t kPieceWords = SP24 ? kPiece24Words : 1024u;
+      const int NG = p.K / p.G;
+      for (int it = 0, j = u_begin / p.KU, kt = u_begin % p.KU; it < min(S, nunits); ++it) {
+        const int grp0 = (p.G == 128) ? kt * p.srows : 0;
+        prefetch_l2(p.packed + (static_cast<long long>(j) * (p.K / 64) + static_cast<long long>(kt) * KQ) * kPieceWords,
+                    static_cast<uint32_t>(KQ) * kPieceWords * 4u);
+        prefetch_l2(p.scales + (static_cast<long long>(j) * NG + grp0) * 128, static_cast<uint32_t>(p.srows) * 256u);
+        if (ZP)
+          prefetch_l2(p.zeros + (static_cast<long long>(j) * NG + grp0) * 128, static_cast<uint32_t>(p.srows) * 128u);
+        if (++kt == p.KU) {
+          kt = 0;
+          ++j;
+        }
+      }
+    }
   }
   if (!MOE) pdl_wait();  // the previous kernel of the stream has completed: global memory is safe
   __syncthreads();

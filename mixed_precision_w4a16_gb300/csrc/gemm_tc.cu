@@ -244,6 +244,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     for (int i = 0; i < kTcStrips; ++i) mbar_init(bar_drain + 8 * i, 1);
     for (int i = 0; i < 4; ++i) flags[i] = 0;  // flags[4] receives the tensor-memory address
     mbar_fence_init();
+    // the weights and scales of the first units (as many as the weight ring holds) into L2 while
+    // the previous kernel drains
+    const int NG = p.K / p.G;
+    for (int it = 0, j = first_pair, kt = kt0; it < min(SW, nunits); ++it) {
+      const int nst = (US == 2 && 2 * j + 1 < p.strips) ? 2 : 1;
+      const int grp0 = (p.G == 128) ? kt * p.srows : 0;
+      for (int t = 0; t < nst; ++t) {
+        const long long strip = US * j + t;
+        prefetch_l2(p.packed + (strip * (p.K / 64) + static_cast<long long>(kt) * 2 * CH) * 1024,
+                    static_cast<uint32_t>(CH) * kPairBytes);
+        prefetch_l2(p.scales + (strip * NG + grp0) * 128, static_cast<uint32_t>(p.srows) * 256u);
+        if (ZP) prefetch_l2(p.zeros + (strip * NG + grp0) * 128, static_cast<uint32_t>(p.srows) * 128u);
+      }
+      if (++kt == p.KU) {
+        kt = 0;
+        ++j;
+      }
+    }
   }
   if (warp == kIssuerWarp0) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
