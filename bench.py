@@ -226,15 +226,45 @@ def cpu_sample_cols(workload, cores=1):
 GEMM_SOURCES = ("common.cuh", "gemm_launch.cu", "gemm_mma.cu", "gemm_tc.cu", "internal.h")
 
 
-def kernel_source_hash():
-    """Hash of the GEMM kernels' sources and their work planning; profile figures are used only
-    for the build they were taken on."""
+def _code_only(text):
+    """C++ source without comments and with whitespace runs collapsed: what decides the build."""
+    import re
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"' or c == "'":  # string or character literal, copied whole
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return re.sub(r"\s+", " ", "".join(out)).strip()
+
+
+def kernel_source_hash(sources=None):
+    """Hash of the GEMM kernels' code and their work planning (comments and layout excluded);
+    profile figures are used only for the build they were taken on.  `sources` maps file name to
+    text (default: the files in csrc/)."""
     import hashlib
     h = hashlib.sha256()
     for name in GEMM_SOURCES:
         h.update(name.encode())
-        with open(os.path.join(ROOT, "mixed_precision_w4a16_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        if sources is not None:
+            text = sources[name]
+        else:
+            with open(os.path.join(ROOT, "mixed_precision_w4a16_gb300", "csrc", name), encoding="utf-8") as f:
+                text = f.read()
+        h.update(_code_only(text).encode())
     return h.hexdigest()[:16]
 
 

@@ -22,6 +22,9 @@
 //    the 8-wide slot;
 //  * each 64-row piece's FP32 partial product is scaled by its group's FP32
 //    scale with one FMA per accumulator;
+//  * before waiting for the previous kernel of the stream (programmatic
+//    dependent launch), thread 0 prefetches the first units' weights and scales
+//    into L2;
 //  * units are dealt to CTAs in contiguous stripes of T = ceil(units / CTAs)
 //    running down a strip and wrapping into the next (the deep-dive article's
 //    striped partitioning).  At a strip boundary the 4 K-split warps fold

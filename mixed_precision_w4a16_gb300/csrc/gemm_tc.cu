@@ -22,18 +22,22 @@
 //    strip's ring of A buffers in tensor memory (the packed word of lane (g, t)
 //    is that store's fragment: rows g and g + 8, k = 4t .. 4t + 3).  In the wide
 //    mode the four warpgroups take turns over four to seven A buffers.
-//  * Multiply: one thread per strip issues the chunk's eight
+//  * Multiply: one warp per strip (an elected lane) issues the chunk's eight
 //    tcgen05.mma.kind::f16 (A = the chunk in tensor memory, 128 rows = the
 //    strip's output columns; B = the activation stage through a shared-memory
 //    descriptor; D = FP32 [128 x MB] in tensor memory, one accumulator per
-//    strip), then commits the A buffer and the activation stage.  One issuer
-//    per strip completes its chunks in order, which is what makes every parity
-//    wait of the ring protocol name a unique phase.
+//    strip, MB up to 128 in pair mode and 256 in the wide mode), then commits
+//    the A buffer and the activation stage.  One issuer per strip completes its
+//    chunks in order, which is what makes every parity wait of the ring protocol
+//    name a unique phase.
 //  * Epilogue, at the end of each unit-column segment, by all sixteen dequant
 //    warps: tcgen05.ld of the accumulators (one output column per thread, 16
 //    tokens per load), the per-column scale when G = K, the bias, and C -- or,
 //    for pairs split between CTAs, FP32 slots reduced by the last arriver in CTA
 //    order (deterministic, no spin waits).
+//
+// Before waiting for the previous kernel of the stream (programmatic dependent
+// launch), thread 0 prefetches the first units' weights and scales into L2.
 //
 // Every wait is bounded; a timeout records W4A16_ERR_TIMEOUT, stops all roles,
 // drains copies and multiplies in flight and always frees the tensor memory.

@@ -42,6 +42,23 @@ def test_profiled_traffic_is_used_only_for_the_profiled_sources(monkeypatch):
         assert abs(v / bench.gemm_bytes(m, 18432, 73728, 128) - 1) < 0.02, (k, m, v)
 
 
+def test_kernel_source_hash_follows_code_not_comments():
+    srcs = {}
+    for name in bench.GEMM_SOURCES:
+        with open(os.path.join(bench.ROOT, "mixed_precision_w4a16_gb300", "csrc", name), encoding="utf-8") as f:
+            srcs[name] = f.read()
+    h = bench.kernel_source_hash(srcs)
+    assert h == bench.kernel_source_hash()
+    commented = dict(srcs)
+    commented["gemm_tc.cu"] = "// a new comment line\n/* and a block */\n" + srcs["gemm_tc.cu"].replace("\n", "  \n", 3)
+    assert bench.kernel_source_hash(commented) == h
+    changed = dict(srcs)
+    changed["gemm_launch.cu"] = srcs["gemm_launch.cu"].replace("kTcMinRows = 17", "kTcMinRows = 33", 1)
+    assert changed["gemm_launch.cu"] != srcs["gemm_launch.cu"]
+    assert bench.kernel_source_hash(changed) != h
+    assert bench._code_only('x = "// kept"; // dropped') == 'x = "// kept";'
+
+
 def test_oracle_timing_child_reports_gemm_and_repack():
     r = bench.run_cpu_sample("pr1", 1024, repack=True)
     assert r["seconds"] > 0 and r["scaled_seconds"] == pytest.approx(r["seconds"])  # 1024 of 1024 columns
