@@ -524,14 +524,10 @@ def run_ours(args, rank, world, device):
         else:
             w.w4a16_gemm(p["A_d"], packed, sp, p["C_d"], p["M"], p["K"], p["N"], p["G"], ws, max_ws, stream)
 
-    def one_step(it, evs=None):
-        for i, p in enumerate(points):
+    def one_step(it):
+        for p in points:
             packed, sp = p["packs"][it % len(p["packs"])]
-            if evs is not None:
-                evs[i][0].record(stream)
             gemm_call(p, packed, sp)
-            if evs is not None:
-                evs[i][1].record(stream)
 
     for it in range(args.warmup):
         one_step(it)
@@ -547,8 +543,9 @@ def run_ours(args, rank, world, device):
     sampler = make_clock_sampler(uuid) if rank == 0 else None
     time.sleep(0.3)
 
-    # ---- timed region: barrier + sync on both sides, CUDA events on the launching stream
-    per_point = [[] for _ in points]
+    # ---- timed region: barrier + sync on both sides, CUDA events on the launching stream.  The
+    # GEMMs of a step run back to back (no events between them, which would keep a kernel's
+    # set-up from overlapping the previous one's tail); per-GEMM times come from the loop below.
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -556,12 +553,9 @@ def run_ours(args, rank, world, device):
         sampler.start_timing()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    evs_all = []
     ev0.record(stream)
     for it in range(args.steps):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in points]
-        one_step(it, evs)
-        evs_all.append(evs)
+        one_step(it)
     ev1.record(stream)
     torch.cuda.synchronize()
     if sampler:
@@ -569,14 +563,15 @@ def run_ours(args, rank, world, device):
     if world > 1:
         torch.distributed.barrier()
     ms_total = ev0.elapsed_time(ev1)
-    for evs in evs_all:
-        for i, (a, b) in enumerate(evs):
-            per_point[i].append(a.elapsed_time(b))
     status = w.w4a16_get_status(ws)
     if status != 0:
         raise RuntimeError(f"device status error in timed region: {w.w4a16_status_string(status)}")
 
-    # ---- end-to-end through the public API: pinned host A in, host C out, every step
+    # ---- end-to-end through the public API: pinned host A in, host C out, every step.  The
+    # copies run on two copy streams next to the GEMMs' stream: a GEMM's input copy is issued
+    # ahead and its output read starts as soon as it finishes, so copies overlap the other GEMMs.
+    # Events keep every buffer in order: A_d[i] is refilled only after the previous step's GEMM i
+    # read it, and GEMM i writes C_d[i] only after the previous step's read of it finished.
     e2e = None
     if not args.no_e2e:
         hostA = [torch.from_numpy(p["A"]).pin_memory() for p in points]
@@ -584,31 +579,50 @@ def run_ours(args, rank, world, device):
         h2d = sum(p["M"] * p["K"] * 2 for p in points)
         d2h = sum(p["M"] * p["N"] * 2 for p in points)
         e_steps = max(1, min(args.steps, 50))
-        for it in range(2):
+        s_in = torch.cuda.Stream(device)
+        s_out = torch.cuda.Stream(device)
+        in_done = [torch.cuda.Event() for _ in points]
+        gemm_done = [torch.cuda.Event() for _ in points]
+        out_done = [torch.cuda.Event() for _ in points]
+
+        def e2e_step(it, first):
             for i, p in enumerate(points):
-                p["A_d"].copy_(hostA[i], non_blocking=True)
+                if not first:
+                    s_in.wait_event(gemm_done[i])
+                with torch.cuda.stream(s_in):
+                    p["A_d"].copy_(hostA[i], non_blocking=True)
+                in_done[i].record(s_in)
+                stream.wait_event(in_done[i])
+                if not first:
+                    stream.wait_event(out_done[i])
                 packed, sp = p["packs"][it % len(p["packs"])]
                 gemm_call(p, packed, sp)
-                hostC[i].copy_(p["C_d"], non_blocking=True)
+                gemm_done[i].record(stream)
+                s_out.wait_event(gemm_done[i])
+                with torch.cuda.stream(s_out):
+                    hostC[i].copy_(p["C_d"], non_blocking=True)
+                out_done[i].record(s_out)
+
+        for it in range(2):
+            e2e_step(it, it == 0)
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        s_in.wait_event(e0)  # no copy of the timed steps starts before the timed region
         for it in range(e_steps):
-            for i, p in enumerate(points):
-                p["A_d"].copy_(hostA[i], non_blocking=True)
-                packed, sp = p["packs"][it % len(p["packs"])]
-                gemm_call(p, packed, sp)
-                hostC[i].copy_(p["C_d"], non_blocking=True)
+            e2e_step(it, False)
+        stream.wait_event(out_done[-1])  # the last read of C (the read stream runs in order)
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = e0.elapsed_time(e1) / e_steps
         e_ms = reduce_max(e_ms, world, device)
         tb, _ = workload_totals(layers)
         e2e = {"value": world * tb / (e_ms * 1e-3) / 1e12, "unit": "TB/s", "ms_per_step": e_ms,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
+               "copies": "H2D and D2H on two copy streams, overlapped with the GEMMs"}
 
     # ---- per-M statistics: a dedicated loop of at least 50 launches per GEMM (200 when its
     # roofline time is under 10 us), cycling through the L2-rotation copies, one event pair each
@@ -703,7 +717,7 @@ def run_ours(args, rank, world, device):
     bw = peaks["hbm_gbs"] * 1e9
     pk = peaks["bf16_tflops"] * 1e12  # dense FP16 equals dense BF16 on this part
     sweep = []
-    for p, ts, step_ts in zip(points, rep_us, per_point):
+    for p, ts in zip(points, rep_us):
         us = statistics.median(ts) * 1e3
         by = gemm_bytes(p["M"], p["K"], p["N"], p["G"])
         fl = gemm_flops(p["M"], p["K"], p["N"])
@@ -714,8 +728,7 @@ def run_ours(args, rank, world, device):
                       "us_p90": round(sorted(ts)[(9 * len(ts)) // 10] * 1e3, 2),
                       "tb_s": round(by / (us * 1e-6) / 1e12, 3), "tflops": round(fl / (us * 1e-6) / 1e12, 1),
                       "roofline_frac": round(t_roof / (us * 1e-6), 3), "bound": "hbm" if mem_bound else "tensor",
-                      "launches": p["launches"], "kernel": p["kernel"], "reps": len(ts),
-                      "us_in_timed_steps": round(statistics.median(step_ts) * 1e3, 2)})
+                      "launches": p["launches"], "kernel": p["kernel"], "reps": len(ts)})
         if len(sweep) - 1 in graph_us:
             gus, nl = graph_us[len(sweep) - 1]
             sweep[-1]["graph_us"] = round(gus, 2)
