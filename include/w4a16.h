@@ -297,10 +297,13 @@ W4A16_API int w4a16_gemm_24(const uint16_t* A, const uint32_t* packed24, const u
  *                   rise from 0 to M (an expert may own no rows)
  *   C               device, fp16[M][N] row-major, written
  *   max_rows        a bound on the rows of any one expert (<= 0: M).  It picks
- *                   the row-segment height: 8 rows when max_rows <= 8, else
- *                   16; an expert with more rows is split into segments, each
- *                   of which streams that expert's weights once.  A bound that
- *                   is too low only costs speed.
+ *                   the kernel and the row-segment height: up to 16, the
+ *                   streaming mma.sync kernel with segments of 8 rows (when
+ *                   max_rows <= 8) or 16; from 17, the tensor-memory (tcgen05)
+ *                   kernel with segments of max_rows rounded up to 16, at most
+ *                   128.  An expert with more rows than a segment is split into
+ *                   segments, each of which streams that expert's weights once.
+ *                   A bound that is too low only costs speed.
  *
  * Symmetric codes (z = 8), no bias; 1 <= E <= 2048, M <= 2^24, K, N, G as for
  * w4a16_gemm.  The offsets are read on the device only, so the call needs no

@@ -345,7 +345,8 @@ Plan moe_plan(int E, int M, int max_rows, int K, int N, int groupsize, int ablat
   *st = current_device_info(&d);
   if (*st != W4A16_OK) return pl;
   const int rows = (max_rows <= 0 || max_rows > M) ? std::max(M, 1) : max_rows;
-  pl = make_plan_moe(E, std::max(M, 1), rows, K, N, effective_group(K, groupsize), d->sms, d->smem_optin, ablate);
+  pl = make_plan_moe(E, std::max(M, 1), rows, K, N, effective_group(K, groupsize), d->sms, d->smem_optin, ablate,
+                     g_force_path.load());
   // the counters (one per segment and strip) and the unit count stay well inside int
   if (static_cast<long long>(pl.max_seg) * pl.strips * pl.KU > (1LL << 30)) *st = W4A16_ERR_SHAPE;
   return pl;

@@ -289,4 +289,106 @@ __device__ __forceinline__ void decode8(uint32_t w, uint32_t a[4]) {
   decode8_zp(w, NibblePos<0>::offset(8u), NibblePos<1>::offset(8u), a);
 }
 
+// ---------------------------------------------------------------------------
+// Grouped expert GEMM: the row segments of each expert
+// ---------------------------------------------------------------------------
+
+// Column of work units in a grouped expert GEMM: expert e, its row segment ci
+// (rows off[e] + mb * ci ..), unit column j within the segment (a strip, or a
+// strip pair).  pref[e] = row segments of the experts before e, pref[E] = all of them.
+struct SegPos {
+  int e, ci, j;
+};
+
+// Column jj (segment jj / cols, column jj % cols); jj < pref[E] * cols.
+__device__ __forceinline__ SegPos seg_locate(const int* pref, int E, int cols, int jj) {
+  const int seg = jj / cols;
+  int lo = 0, hi = E;  // pref[lo] <= seg < pref[hi]; experts without rows have pref[e] == pref[e + 1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pref[mid] <= seg)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return SegPos{lo, seg - pref[lo], jj - seg * cols};
+}
+
+// The next column (call only while one exists).
+__device__ __forceinline__ void seg_next(SegPos& sp, const int* pref, int E, int cols) {
+  if (++sp.j < cols) return;
+  sp.j = 0;
+  if (++sp.ci < pref[sp.e + 1] - pref[sp.e]) return;
+  sp.ci = 0;
+  do {
+    ++sp.e;
+  } while (sp.e < E && pref[sp.e + 1] == pref[sp.e]);
+}
+
+// Grouped-GEMM prologue, run by all NT threads of the CTA: copies the expert
+// offsets to shared memory (offs[E + 1]), checks them (0 = off[0] <= ... <=
+// off[E] = M) and writes the segment prefix (pref[E + 1], segments of mb rows)
+// with a block-wide scan (scan[1 + NT / 32]).  Returns the number of segments, or
+// -1 (kDevErrValue set in *status) when the offsets are invalid or need more
+// segments than the workspace holds; the result is the same in every thread.
+// The caller's next __syncthreads publishes pref.
+template <int NT>
+__device__ int moe_segments(const int* expert_off, int E, int M, int max_seg, int mb, uint32_t* status, int* pref,
+                            int* offs, int* scan, int warp, int lane) {
+  const int per = (E + NT - 1) / NT;
+  const int e0 = threadIdx.x * per;
+  bool bad = false;
+  long long local = 0;
+  for (int i = 0; i < per; ++i) {
+    const int e = e0 + i;
+    if (e < E) {
+      const int lo = expert_off[e], hi = expert_off[e + 1];
+      offs[e] = lo;
+      const long long rows = static_cast<long long>(hi) - lo;
+      bad |= rows < 0 || rows > M;
+      if (rows > 0 && rows <= M) local += (rows + mb - 1) / mb;
+    }
+  }
+  if (threadIdx.x == 0) {
+    const int last = expert_off[E];
+    offs[E] = last;
+    bad |= expert_off[0] != 0 || last != M;
+  }
+  const int mine = static_cast<int>(min(local, static_cast<long long>(max_seg) + 1));  // no overflow below
+  int incl = mine;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) scan[1 + warp] = incl;
+  bad = __syncthreads_or(bad);
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int w = 0; w < NT / 32; ++w) {
+      const int v = scan[1 + w];
+      scan[1 + w] = run;
+      run += v;
+    }
+    scan[0] = run;
+  }
+  __syncthreads();
+  const int total = scan[0];
+  if (bad || total > max_seg) {
+    if (threadIdx.x == 0) atomicOr(status, kDevErrValue);
+    return -1;
+  }
+  int run = scan[1 + warp] + incl - mine;
+  for (int i = 0; i < per; ++i) {
+    const int e = e0 + i;
+    if (e < E) {
+      pref[e] = run;
+      const int rows = offs[e + 1] - offs[e];
+      if (rows > 0) run += (rows + mb - 1) / mb;
+    }
+  }
+  if (threadIdx.x == 0) pref[E] = total;
+  return total;
+}
+
 }  // namespace w4a16

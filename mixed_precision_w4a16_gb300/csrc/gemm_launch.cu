@@ -125,7 +125,7 @@ GemmParams mma_params(const Plan& pl, const GemmCall& c, uint32_t* status, uint3
 
 // wide: one strip per unit and up to 256 token rows per launch (needs K % 512 == 0), else the
 // strip-pair mode with up to 128.
-Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin, bool zp, int ablate, bool wide) {
+Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin, bool zp, int ablate, bool wide, int moe_E = 0) {
   Plan pl{};
   pl.path = 2;
   wide = wide && K % 512 == 0;
@@ -156,7 +156,7 @@ Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin, bool zp, 
   // activation ring takes the rest (up to 8 stages: it hides the L2 latency of the tiles).
   // Activation tiles of 128 tokens and more are 32 KB and up: there the activation ring gets
   // the larger share.
-  const TcLayout l0 = tc_layout(pl.us, pl.mb, pl.ch, pl.srows, 0, 0, zp);
+  const TcLayout l0 = tc_layout(pl.us, pl.mb, pl.ch, pl.srows, 0, 0, zp, moe_E);
   const int budget = smem_optin - l0.smem_bytes;
   int sw = std::max(2, std::min(kTcMaxSW, (100 * 1024 + l0.w_stage_bytes - 1) / l0.w_stage_bytes));
   if (pl.mb > 64) sw = 2;
@@ -169,7 +169,7 @@ Plan make_plan_tc(int M, int K, int N, int G, int sms, int smem_optin, bool zp, 
   }
   pl.w_stages = sw;
   pl.a_stages = std::max(2, ns);
-  pl.tlay = tc_layout(pl.us, pl.mb, pl.ch, pl.srows, pl.a_stages, pl.w_stages, zp);
+  pl.tlay = tc_layout(pl.us, pl.mb, pl.ch, pl.srows, pl.a_stages, pl.w_stages, zp, moe_E);
   pl.m_chunk = pl.mb;
   pl.k_tile = 128 * pl.ch;
   pl.stages = pl.w_stages;
@@ -216,9 +216,24 @@ int encode_a_map(CUtensorMap* map, const uint16_t* A, int M, int K, int box_rows
   return r == CUDA_SUCCESS ? W4A16_OK : W4A16_ERR_CUDA;
 }
 
-Plan make_plan_moe(int E, int M, int max_rows, int K, int N, int G, int sms, int smem_optin, int ablate) {
-  // experts that can own rows, and the row segments (8 * m_tiles rows of one expert) they can need
+Plan make_plan_moe(int E, int M, int max_rows, int K, int N, int G, int sms, int smem_optin, int ablate,
+                   int forced_path) {
+  // experts that can own rows, and the row segments (m_chunk rows of one expert) they can need
   const int active = std::max(1, std::min(E, M));
+  if (forced_path >= 2 || (forced_path != 1 && max_rows >= kTcMinRows)) {
+    // From 17 rows per expert: the tensor-memory kernel in pair mode, row segments of up to 128
+    // rows (the expert's rows padded to 16, so an expert of up to 128 rows streams its weights once).
+    Plan pl = make_plan_tc(std::min(max_rows, 128), K, N, G, sms, smem_optin, false, ablate, false, E);
+    pl.moe_E = E;
+    pl.max_seg = active + (M + pl.m_chunk - 1) / pl.m_chunk;
+    pl.grid = sms;  // persistent: the kernel spreads the segments it finds over all CTAs
+    pl.units = 0;   // decided on the device
+    pl.T = 0;
+    const size_t counters = static_cast<size_t>(pl.max_seg) * ((pl.strips + kTcStrips - 1) / kTcStrips);
+    pl.workspace = kStatusBytes + (counters * 4 + 255) / 256 * 256 +
+                   2ull * pl.grid * (static_cast<size_t>(kTcStrips) * kStrip * pl.mb) * sizeof(float);
+    return pl;
+  }
   // Segment height: 8 rows when no expert has more, else 16.  Measured on GB300 (8 experts
   // K=4096 N=14336; 128 x K=2048 N=1536; 256 x K=7168 N=4096), 16-row segments beat 32-row
   // ones even at 32 rows per expert on average: an expert streamed twice at the 16-row
@@ -318,9 +333,56 @@ int run_moe_gemm(const Plan& pl, const GemmCall& c, const int* expert_off) {
   uint8_t* ws = static_cast<uint8_t*>(c.workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
   uint32_t* counters = reinterpret_cast<uint32_t*>(ws + kStatusBytes);
-  const size_t ncount = static_cast<size_t>(pl.max_seg) * pl.strips;
+  const int cols = pl.path == 2 ? (pl.strips + kTcStrips - 1) / kTcStrips : pl.strips;  // unit columns per segment
+  const size_t ncount = static_cast<size_t>(pl.max_seg) * cols;
   float* slots = reinterpret_cast<float*>(ws + kStatusBytes + (ncount * 4 + 255) / 256 * 256);
   CUtensorMap map;
+  if (pl.path == 2) {
+    const int er = encode_a_map(&map, c.A, c.M, c.K, pl.m_chunk, 2, true);
+    if (er != W4A16_OK) return er;
+    TcParams p{};
+    p.packed = c.packed;
+    p.scales = c.scales;
+    p.C = c.C;
+    p.status = status;
+    p.counters = counters;
+    p.slots = slots;
+    p.M = c.M;
+    p.m0 = 0;
+    p.K = c.K;
+    p.N = c.N;
+    p.G = c.G;
+    p.strips = pl.strips;
+    p.us = pl.us;
+    p.mb = pl.mb;
+    p.ch = pl.ch;
+    p.na = pl.na;
+    p.srows = pl.srows;
+    p.KU = pl.KU;
+    p.units = 0;
+    p.T = 0;
+    p.grid = pl.grid;
+    p.a_stages = pl.a_stages;
+    p.w_stages = pl.w_stages;
+    p.a_stage_bytes = pl.tlay.a_stage_bytes;
+    p.w_stage_bytes = pl.tlay.w_stage_bytes;
+    p.w_base = pl.tlay.w_base;
+    p.s_off = pl.tlay.s_off;
+    p.z_off = pl.tlay.z_off;
+    p.bar_off = pl.tlay.bar_off;
+    p.flag_off = pl.tlay.flag_off;
+    p.idesc = tc_idesc(128, pl.mb);
+    p.wait_limit = c.wait_limit;
+    p.debug_stall = c.debug_stall;
+    p.ablate = c.ablate & ~kAblateNoSwizzle;
+    p.expert_off = expert_off;
+    p.E = pl.moe_E;
+    p.max_seg = pl.max_seg;
+    p.w_stride = static_cast<long long>(c.K) * c.N / 8;
+    p.s_stride = static_cast<long long>(c.K / c.G) * c.N;
+    p.moe_off = pl.tlay.moe_off;
+    return launch_gemm_tc(pl.smem_bytes, map, p, c.stream) == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+  }
   const int er = encode_a_map(&map, c.A, c.M, c.K, pl.m_chunk, pl.cfg.kq, !(c.ablate & kAblateNoSwizzle));
   if (er != W4A16_OK) return er;
   GemmParams p = mma_params(pl, c, status, counters, slots);

@@ -79,102 +79,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Column of work units in a grouped expert GEMM: expert e, its row segment ci
-// (rows off[e] + MB * ci ..), strip j.  pref[e] = row segments of the experts
-// before e, pref[E] = all of them.
-struct SegPos {
-  int e, ci, j;
-};
-
-// Column jj (segment jj / strips, strip jj % strips); jj < pref[E] * strips.
-__device__ __forceinline__ SegPos seg_locate(const int* pref, int E, int strips, int jj) {
-  const int seg = jj / strips;
-  int lo = 0, hi = E;  // pref[lo] <= seg < pref[hi]; experts without rows have pref[e] == pref[e + 1]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (pref[mid] <= seg)
-      lo = mid;
-    else
-      hi = mid;
-  }
-  return SegPos{lo, seg - pref[lo], jj - seg * strips};
-}
-
-// The next column (call only while one exists).
-__device__ __forceinline__ void seg_next(SegPos& sp, const int* pref, int E, int strips) {
-  if (++sp.j < strips) return;
-  sp.j = 0;
-  if (++sp.ci < pref[sp.e + 1] - pref[sp.e]) return;
-  sp.ci = 0;
-  do {
-    ++sp.e;
-  } while (sp.e < E && pref[sp.e + 1] == pref[sp.e]);
-}
-
-// Grouped-GEMM prologue, run by every thread of the CTA: copies the expert
-// offsets to shared memory (offs), checks them (0 = off[0] <= ... <= off[E] = M)
-// and writes the segment prefix (pref) with a block-wide scan.  Returns the
-// number of segments, or -1 (status flagged) when the offsets are invalid or
-// need more segments than the workspace holds; the result is the same in
-// every thread.  The caller's next __syncthreads publishes pref.
-template <int MB>
-__device__ int moe_prologue(const GemmParams& p, int* pref, int* offs, int* scan, int warp, int lane) {
-  const int E = p.E;
-  const int per = (E + kMmaThreads - 1) / kMmaThreads;
-  const int e0 = threadIdx.x * per;
-  bool bad = false;
-  long long local = 0;
-  for (int i = 0; i < per; ++i) {
-    const int e = e0 + i;
-    if (e < E) {
-      const int lo = p.expert_off[e], hi = p.expert_off[e + 1];
-      offs[e] = lo;
-      const long long rows = static_cast<long long>(hi) - lo;
-      bad |= rows < 0 || rows > p.M;
-      if (rows > 0 && rows <= p.M) local += (rows + MB - 1) / MB;
-    }
-  }
-  if (threadIdx.x == 0) {
-    const int last = p.expert_off[E];
-    offs[E] = last;
-    bad |= p.expert_off[0] != 0 || last != p.M;
-  }
-  const int mine = static_cast<int>(min(local, static_cast<long long>(p.max_seg) + 1));  // no overflow below
-  int incl = mine;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, d);
-    if (lane >= d) incl += v;
-  }
-  if (lane == 31) scan[1 + warp] = incl;
-  bad = __syncthreads_or(bad);
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int w = 0; w < kMmaThreads / 32; ++w) {
-      const int v = scan[1 + w];
-      scan[1 + w] = run;
-      run += v;
-    }
-    scan[0] = run;
-  }
-  __syncthreads();
-  const int total = scan[0];
-  if (bad || total > p.max_seg) {
-    if (threadIdx.x == 0) atomicOr(p.status, kDevErrValue);
-    return -1;
-  }
-  int run = scan[1 + warp] + incl - mine;
-  for (int i = 0; i < per; ++i) {
-    const int e = e0 + i;
-    if (e < E) {
-      pref[e] = run;
-      const int rows = offs[e + 1] - offs[e];
-      if (rows > 0) run += (rows + MB - 1) / MB;
-    }
-  }
-  if (threadIdx.x == 0) pref[E] = total;
-  return total;
-}
 
 __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
   uint32_t v;
@@ -217,7 +121,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     int* s_pref = reinterpret_cast<int*>(smem + p.moe_off);
     int* s_offs = s_pref + (p.E + 1);
     int* scan = s_offs + (p.E + 1);
-    const int nseg = moe_prologue<MB>(p, s_pref, s_offs, scan, warp, lane);
+    const int nseg = moe_segments<kMmaThreads>(p.expert_off, p.E, p.M, p.max_seg, MB, p.status, s_pref, s_offs,
+                                               scan, warp, lane);
     if (nseg < 0) return;  // invalid offsets: every thread leaves here, before any copy
     pref = s_pref;
     offs = s_offs;

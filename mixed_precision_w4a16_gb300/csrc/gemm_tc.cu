@@ -189,10 +189,16 @@ constexpr int kBarCount = kBarDrain + 2;
 // US: strips per work unit -- 2 (a strip pair, one issuer and two warpgroups per strip), or 1
 // (wide mode: one issuer, four warpgroups taking turns over four to seven A buffers, CH = 4).
 // ZP: codes carry a zero point per group and column (p.zeros), else the constant 8.
-// BIAS: p.bias is added to C.  All three are compile-time so the plain layer's build is unchanged.
-template <int US, bool ZP, bool BIAS>
+// BIAS: p.bias is added to C.
+// MOE: grouped expert GEMM over p.E experts (p.expert_off, rows sorted by expert), pair mode: a
+// unit column is (row segment of MB rows of one expert, strip pair), found from the offsets on the
+// device; each segment multiplies its expert's weights.
+// All four are compile-time, and every grouped-GEMM step sits under MOE, so the plain layer's
+// build is unchanged.
+template <int US, bool ZP, bool BIAS, bool MOE>
 __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const TcParams p) {
   static_assert(US == 1 || US == 2, "one or two strips per unit");
+  static_assert(!MOE || (US == 2 && !ZP && !BIAS), "the grouped GEMM runs in pair mode, symmetric, without bias");
   constexpr int RK = 4 / US;  // warpgroups per strip: each takes every RK-th chunk of it
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -222,11 +228,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
-  const int u_begin = cta * p.T;
-  const int u_end = min(p.units, u_begin + p.T);
-  const int nunits = u_end - u_begin;
-  const int first_pair = u_begin / p.KU;
-  const int kt0 = u_begin - first_pair * p.KU;
+  // the CTA's units; the grouped GEMM finds them after its prologue (only it reassigns these)
+  int u_begin = cta * p.T;
+  int u_end = min(p.units, u_begin + p.T);
+  int nunits = u_end - u_begin;
+  int first_pair = u_begin / p.KU;
+  int kt0 = u_begin - first_pair * p.KU;
+  int T_moe = 0, grid_moe = 0;   // grouped GEMM: units per CTA and CTAs
+  const int* pref = nullptr;     // grouped GEMM: segment prefix per expert [E + 1]
+  const int* offs = nullptr;     // grouped GEMM: expert row offsets [E + 1]
+  const int pairs = (p.strips + 1) / 2;  // grouped GEMM: unit columns per row segment
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SW; ++s) {
@@ -249,9 +260,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     for (int i = 0; i < 4; ++i) flags[i] = 0;  // flags[4] receives the tensor-memory address
     mbar_fence_init();
     // the weights and scales of the first units (as many as the weight ring holds) into L2 while
-    // the previous kernel drains
+    // the previous kernel drains (the grouped GEMM learns its units only from the offsets)
     const int NG = p.K / p.G;
-    for (int it = 0, j = first_pair, kt = kt0; it < min(SW, nunits); ++it) {
+    for (int it = 0, j = first_pair, kt = kt0; !MOE && it < min(SW, nunits); ++it) {
       const int nst = (US == 2 && 2 * j + 1 < p.strips) ? 2 : 1;
       const int grp0 = (p.G == 128) ? kt * p.srows : 0;
       for (int t = 0; t < nst; ++t) {
@@ -273,10 +284,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   }
   pdl_launch_dependents();
   pdl_wait();  // the previous kernel of the stream has completed: global memory is safe
+  bool moe_bad = false;
+  if constexpr (MOE) {
+    int* s_pref = reinterpret_cast<int*>(smem + p.moe_off);
+    int* s_offs = s_pref + (p.E + 1);
+    int* scan = s_offs + (p.E + 1);
+    const int nseg = moe_segments<kTcThreads>(p.expert_off, p.E, p.M, p.max_seg, MB, p.status, s_pref, s_offs,
+                                              scan, warp, lane);
+    moe_bad = nseg < 0;  // the same in every thread
+    pref = s_pref;
+    offs = s_offs;
+    const int units = max(nseg, 0) * pairs * p.KU;
+    grid_moe = static_cast<int>(gridDim.x);
+    T_moe = max(1, (units + grid_moe - 1) / grid_moe);
+    u_begin = cta * T_moe;
+    u_end = min(units, u_begin + T_moe);
+    nunits = max(0, u_end - u_begin);
+    first_pair = nunits > 0 ? u_begin / p.KU : 0;
+    kt0 = nunits > 0 ? u_begin - first_pair * p.KU : 0;
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if constexpr (MOE) {
+    if (moe_bad) {  // invalid offsets: nothing copied or written; free the tensor memory
+      if (warp == kIssuerWarp0) tmem_dealloc(tmem, kTmemCols);
+      return;
+    }
+  }
 
   auto raise_abort = [&]() {
     if (!*abort_flag) {
@@ -297,22 +333,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       const uint32_t z_bytes = static_cast<uint32_t>(p.srows) * 128u;
       int s = 0, round = 0;
       int j = first_pair, kt = kt0;
+      SegPos cp{0, 0, 0};  // grouped GEMM: the unit column's expert, row segment and strip pair
+      if constexpr (MOE) {
+        if (nunits > 0) cp = seg_locate(pref, p.E, pairs, first_pair);
+      }
       for (int it = 0; it < nunits; ++it) {
         if (it >= SW && !mbar_wait_bounded_sleep(bar_wempty + 8 * s, (round - 1) & 1, p.wait_limit, abort_flag)) {
           raise_abort();
           break;
         }
         if (!(p.debug_stall && it == 0)) {  // with debug_stall, stage 0 stays empty: nothing completes its barrier
-          const int nst = (US == 2 && 2 * j + 1 < p.strips) ? 2 : 1;
+          const int pr = MOE ? cp.j : j;  // strip pair
+          const int nst = (US == 2 && 2 * pr + 1 < p.strips) ? 2 : 1;
           const uint32_t fb = bar_wfull + 8 * s;
+          const uint32_t* pk = MOE ? p.packed + cp.e * p.w_stride : p.packed;  // the column's expert
+          const uint16_t* sk = MOE ? p.scales + cp.e * p.s_stride : p.scales;
           const uint32_t st = sbase + p.w_base + s * p.w_stage_bytes;
           mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nst) * (w_bytes + s_bytes + (ZP ? z_bytes : 0u)));
           const int grp0 = (p.G == 128) ? kt * p.srows : 0;
           for (int t = 0; t < nst; ++t) {
-            const long long strip = US * j + t;
-            bulk_g2s(st + t * w_bytes, p.packed + (strip * (p.K / 64) + static_cast<long long>(kt) * 2 * CH) * 1024,
+            const long long strip = US * pr + t;
+            bulk_g2s(st + t * w_bytes, pk + (strip * (p.K / 64) + static_cast<long long>(kt) * 2 * CH) * 1024,
                      w_bytes, fb, pol);
-            bulk_g2s(st + p.s_off + t * s_bytes, p.scales + (strip * NG + grp0) * 128, s_bytes, fb, pol_s);
+            bulk_g2s(st + p.s_off + t * s_bytes, sk + (strip * NG + grp0) * 128, s_bytes, fb, pol_s);
             if (ZP)  // the zero codes of the same scale rows, permuted the same way
               bulk_g2s(st + p.z_off + t * z_bytes, p.zeros + (strip * NG + grp0) * 128, z_bytes, fb, pol_s);
           }
@@ -325,6 +368,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         if (++kt == p.KU) {
           kt = 0;
           ++j;
+          if constexpr (MOE) {
+            if (it + 1 < nunits) seg_next(cp, pref, p.E, pairs);
+          }
         }
       }
     }
@@ -349,6 +395,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       const uint32_t a_bytes = static_cast<uint32_t>(MB) * 256u;
       int a = 0, c = 0, kt = kt0;
       uint32_t ph = 0;  // phase bit (gs / NS) & 1
+      SegPos cp{0, 0, 0};  // grouped GEMM: the chunk's unit column
+      if constexpr (MOE) {
+        if (nunits > 0) cp = seg_locate(pref, p.E, pairs, first_pair);
+      }
       for (int gs = 0; gs < nch; ++gs) {
         if (gs >= NS && !mbar_wait_bounded_sleep(bar_aempty + 8 * a, ph ^ 1u, p.wait_limit, abort_flag)) {
           raise_abort();
@@ -356,7 +406,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         }
         if (!(p.debug_stall && gs == 0)) {  // with debug_stall, stage 0 stays empty
           mbar_arrive_expect_tx(bar_afull + 8 * a, a_bytes);
-          tma_load_3d(sbase + a * p.a_stage_bytes, &tmA, 0, p.m0, (kt * CH + c) * 2, bar_afull + 8 * a, pol);
+          const int row0 = MOE ? offs[cp.e] + MB * cp.ci : p.m0;  // the launch's (segment's) first row
+          tma_load_3d(sbase + a * p.a_stage_bytes, &tmA, 0, row0, (kt * CH + c) * 2, bar_afull + 8 * a, pol);
           last = gs;
         }
         if (++a == NS) {
@@ -365,7 +416,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         }
         if (++c == CH) {
           c = 0;
-          if (++kt == p.KU) kt = 0;
+          if (++kt == p.KU) {
+            kt = 0;
+            if constexpr (MOE) {
+              if (gs + 1 < nch) seg_next(cp, pref, p.E, pairs);
+            }
+          }
         }
       }
     }
@@ -397,12 +453,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     const uint32_t box16 = static_cast<uint32_t>(MB * 128) >> 4;
     const uint32_t cfull0 = bar_cfull + 8 * (s * kTcMaxNA), consumed0 = bar_consumed + 8 * (s * kTcMaxNA);
     int a = 0, st = 0, segs = 0, kt = kt0, j = first_pair;
+    SegPos cp{0, 0, 0};  // grouped GEMM: the unit column
+    if constexpr (MOE) {
+      if (nunits > 0) cp = seg_locate(pref, p.E, pairs, first_pair);
+    }
     uint32_t ph = 0, sph = 0;  // phase bits of A buffer a and activation stage st
     bool first = true;         // the next chunk starts the accumulator of a segment
     bool ok = true;
     for (int it = 0; it < nunits; ++it) {
       const bool seg_end = (kt == p.KU - 1) || (it == nunits - 1);
-      const bool real = US * j + s < p.strips;  // the last pair of an odd strip count has one strip
+      const bool real = US * (MOE ? cp.j : j) + s < p.strips;  // the last pair of an odd strip count has one strip
       for (int c = 0; c < CH; ++c) {
         // The A chunk was written after the multiplies of chunk gs - NA completed (the dequant
         // waits for them), and this warp waited for chunk gs - NA's A chunk and activation stage
@@ -441,6 +501,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       if (++kt == p.KU) {
         kt = 0;
         ++j;
+        if constexpr (MOE) {
+          if (it + 1 < nunits) seg_next(cp, pref, p.E, pairs);
+        }
       }
     }
     // wait for every multiply this warp issued before the memory is released
@@ -483,11 +546,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   uint32_t stw = sbase + p.w_base;  // weight stage ws
   int ws = 0, wround = 0, segs = 0;
   int j = first_pair, kt = kt0;
+  SegPos cp{0, 0, 0};  // grouped GEMM: the unit column
+  if constexpr (MOE) {
+    if (nunits > 0) cp = seg_locate(pref, p.E, pairs, first_pair);
+  }
   for (int it = 0; it < nunits; ++it) {
     const bool seg_end = (kt == KU - 1) || (it == nunits - 1);
     // this warpgroup's first chunk of the unit (then every RK-th; the wide mode has CH = 4)
     const int c0 = (US == 2 && (CH & 1)) ? ((r ^ it) & 1) : r;
-    const bool real = US * j + s < strips;
+    const bool real = US * (MOE ? cp.j : j) + s < strips;
     if (c0 < CH) {
       bool have = false;
       if (!*abort_flag) {
@@ -599,20 +666,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       if (!*seg_abort) {
         tc_fence_after();
         const int row = 32 * q + lane;  // output column within its strip
-        const int nst = (US == 2 && 2 * j + 1 < strips) ? 2 : 1;
+        const int pr = MOE ? cp.j : j;  // strip pair (strip, wide mode)
+        const int nst = (US == 2 && 2 * pr + 1 < strips) ? 2 : 1;
         const int ngrp = MB / 16;       // 16-token groups of the accumulator
+        // rows of this column: the launch's, or (grouped GEMM) the segment's within its expert
+        const int row0 = MOE ? offs[cp.e] + MB * cp.ci : p.m0;
+        const int row_end = MOE ? min(offs[cp.e + 1], row0 + MB) : p.M;
         const int ntask = nst * ngrp;   // (strip, token group) read-outs, dealt to the warpgroups
         float scale[2], bias_n[2];
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          const int strip = min(US * j + t, strips - 1);
-          scale[t] = grouped ? 1.f
-                             : __half2float(__ushort_as_half(p.scales[static_cast<long long>(strip) * NG * 128 + scale_pos(row)]));
+          const int strip = min(US * pr + t, strips - 1);
+          const uint16_t* sk = MOE ? p.scales + cp.e * p.s_stride : p.scales;
+          scale[t] = grouped ? 1.f : __half2float(__ushort_as_half(sk[static_cast<long long>(strip) * NG * 128 + scale_pos(row)]));
           bias_n[t] = BIAS ? __half2float(__ushort_as_half(p.bias[strip * kStrip + row])) : 0.f;
         }
         const uint32_t dbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(US * NA * kChunkCols);
-        const int c_first = (j * KU) / p.T;
-        const int c_last = min(((j + 1) * KU - 1) / p.T, p.grid - 1);
+        const int T = MOE ? T_moe : p.T;
+        const int c_first = (j * KU) / T;
+        const int c_last = min(((j + 1) * KU - 1) / T, (MOE ? grid_moe : p.grid) - 1);
         const int slot_floats = US * MB * 128;
         if (c_first == c_last) {
           for (int e = wg; e < ntask; e += 4) {
@@ -620,11 +692,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             uint32_t v[16];
             tmem_ld_32x32b_x16(dbase + static_cast<uint32_t>(t * MB + grp * 16), v);
             tmem_ld_wait();
-            const long long n = static_cast<long long>(US * j + t) * kStrip + row;
+            const long long n = static_cast<long long>(US * pr + t) * kStrip + row;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const int token = p.m0 + grp * 16 + i;
-              if (token < p.M)
+              const int token = row0 + grp * 16 + i;
+              if (token < row_end)
                 p.C[static_cast<long long>(token) * p.N + n] = f32_to_f16_bits(__uint_as_float(v[i]) * scale[t] + bias_n[t]);
             }
           }
@@ -659,13 +731,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
             // independent, so their latencies overlap
             for (int e = wg; e < ntask; e += 4) {
               const int t = e / ngrp, grp = e - t * ngrp;
-              const long long n = static_cast<long long>(US * j + t) * kStrip + row;
-              for (int m = 0; m < 16 && p.m0 + grp * 16 + m < p.M; m += 8) {
+              const long long n = static_cast<long long>(US * pr + t) * kStrip + row;
+              for (int m = 0; m < 16 && row0 + grp * 16 + m < row_end; m += 8) {
                 float acc[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) acc[i] = 0.f;
                 for (int c = c_first; c <= c_last; ++c) {
-                  const int cslot = (j == (c * p.T) / KU) ? 2 * c : 2 * c + 1;
+                  const int cslot = (j == (c * T) / KU) ? 2 * c : 2 * c + 1;
                   const float* src =
                       p.slots + static_cast<long long>(cslot) * slot_floats + (t * MB + grp * 16 + m) * 128 + row;
                   float tv[8];
@@ -676,8 +748,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
                 }
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                  const int token = p.m0 + grp * 16 + m + i;
-                  if (token < p.M) p.C[static_cast<long long>(token) * p.N + n] = f32_to_f16_bits(acc[i] * scale[t] + bias_n[t]);
+                  const int token = row0 + grp * 16 + m + i;
+                  if (token < row_end) p.C[static_cast<long long>(token) * p.N + n] = f32_to_f16_bits(acc[i] * scale[t] + bias_n[t]);
                 }
               }
             }
@@ -696,6 +768,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     if (++kt == KU) {
       kt = 0;
       ++j;
+      if constexpr (MOE) {
+        if (it + 1 < nunits) seg_next(cp, pref, p.E, pairs);
+      }
     }
   }
   named_bar_sync(3, kTcThreads);
@@ -703,7 +778,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
 
 }  // namespace
 
-TcLayout tc_layout(int us, int mb, int ch, int srows, int a_stages, int w_stages, bool zp) {
+TcLayout tc_layout(int us, int mb, int ch, int srows, int a_stages, int w_stages, bool zp, int moe_E) {
   TcLayout l{};
   l.a_stage_bytes = 2 * mb * 128;  // one 128-row chunk: a multiple of 1024 keeps the swizzle atoms aligned
   // weight stage: the unit's strips' packed chunks, their scale rows, then (with zero points) their zero rows
@@ -713,7 +788,10 @@ TcLayout tc_layout(int us, int mb, int ch, int srows, int a_stages, int w_stages
   l.w_base = a_stages * l.a_stage_bytes;
   l.bar_off = l.w_base + w_stages * l.w_stage_bytes;
   l.flag_off = l.bar_off + 8 * kBarCount;
-  l.smem_bytes = 1024 + l.flag_off + 64;
+  l.moe_off = l.flag_off + 64;
+  // grouped GEMM: segment prefix and offsets ([E + 1] ints each), then the scan's 1 + 20 ints
+  const int moe_bytes = moe_E > 0 ? (2 * (moe_E + 1) + 1 + kTcThreads / 32) * 4 : 0;
+  l.smem_bytes = 1024 + l.moe_off + (moe_bytes + 15) / 16 * 16;
   return l;
 }
 
@@ -734,14 +812,16 @@ cudaError_t launch_gemm_tc(int smem_bytes, const CUtensorMap& tmA, const TcParam
     return cudaErrorInvalidConfiguration;
   using Kern = void (*)(const CUtensorMap, const TcParams);
   static const Kern kerns[2][2][2] = {
-      {{gemm_tc_kernel<1, false, false>, gemm_tc_kernel<1, false, true>},
-       {gemm_tc_kernel<1, true, false>, gemm_tc_kernel<1, true, true>}},
-      {{gemm_tc_kernel<2, false, false>, gemm_tc_kernel<2, false, true>},
-       {gemm_tc_kernel<2, true, false>, gemm_tc_kernel<2, true, true>}}};
+      {{gemm_tc_kernel<1, false, false, false>, gemm_tc_kernel<1, false, true, false>},
+       {gemm_tc_kernel<1, true, false, false>, gemm_tc_kernel<1, true, true, false>}},
+      {{gemm_tc_kernel<2, false, false, false>, gemm_tc_kernel<2, false, true, false>},
+       {gemm_tc_kernel<2, true, false, false>, gemm_tc_kernel<2, true, true, false>}}};
+  const bool moe = p.expert_off != nullptr;
+  if (moe && (p.us != 2 || p.zeros || p.bias || p.E < 1)) return cudaErrorInvalidConfiguration;
   const int zp = p.zeros ? 1 : 0, bias = p.bias ? 1 : 0;
-  const Kern kern = kerns[p.us - 1][zp][bias];
-  static int smem_cache[8][64];  // per kernel variant
-  cudaError_t e = ensure_smem(kern, smem_bytes, smem_cache[(p.us - 1) * 4 + zp * 2 + bias]);
+  const Kern kern = moe ? gemm_tc_kernel<2, false, false, true> : kerns[p.us - 1][zp][bias];
+  static int smem_cache[9][64];  // per kernel variant
+  cudaError_t e = ensure_smem(kern, smem_bytes, smem_cache[moe ? 8 : (p.us - 1) * 4 + zp * 2 + bias]);
   if (e != cudaSuccess) return e;
   return launch_overlapped(kern, p.grid, kTcThreads, smem_bytes, stream, tmA, p);
 }

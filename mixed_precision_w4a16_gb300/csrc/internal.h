@@ -142,9 +142,9 @@ constexpr int kTcMaxSW = 8;       // weight stages
 // 1024-aligned base): activation stages, then weight stages (each: both strips' packed
 // chunks, their scale rows at s_off, their zero-code rows at z_off), barriers, flags.
 struct TcLayout {
-  int a_stage_bytes, w_stage_bytes, w_base, s_off, z_off, bar_off, flag_off, smem_bytes;
+  int a_stage_bytes, w_stage_bytes, w_base, s_off, z_off, bar_off, flag_off, moe_off, smem_bytes;
 };
-TcLayout tc_layout(int us, int mb, int ch, int srows, int a_stages, int w_stages, bool zp);
+TcLayout tc_layout(int us, int mb, int ch, int srows, int a_stages, int w_stages, bool zp, int moe_E = 0);
 uint32_t tc_idesc(int m, int n);
 
 struct TcParams {
@@ -170,6 +170,14 @@ struct TcParams {
   long long wait_limit;
   int debug_stall;
   int ablate;               // kAblate* bits (no-swizzle does not apply to this kernel)
+  // grouped expert GEMM only (pair mode; the kernel derives units and T from the offsets, grid =
+  // gridDim.x; counters are per (row segment, strip pair)):
+  const int* expert_off;    // device int32[E + 1], or null for the plain GEMM
+  int E;                    // experts
+  int max_seg;              // row segments the counters were sized for
+  long long w_stride;       // packed words per expert (K * N / 8)
+  long long s_stride;       // permuted scales per expert ((K / G) * N)
+  int moe_off;              // shared-memory offset of the expert tables
 };
 
 cudaError_t launch_gemm_tc(int smem_bytes, const CUtensorMap& tmA, const TcParams& p, cudaStream_t stream);
@@ -239,9 +247,11 @@ struct GemmCall {
 // Launches the planned kernels over all token-row chunks; returns a W4A16 status.
 int run_gemm(const Plan& pl, const GemmCall& c);
 
-// Grouped expert GEMM over M expert-sorted rows (streaming kernel; max_rows bounds the
-// rows of any one expert and picks the row-segment height, 8 or 16).
-Plan make_plan_moe(int E, int M, int max_rows, int K, int N, int G, int sms, int smem_optin, int ablate = 0);
+// Grouped expert GEMM over M expert-sorted rows.  max_rows bounds the rows of any one expert and
+// picks the kernel and the row-segment height: the streaming kernel with 8 or 16 rows up to 16,
+// the tensor-memory kernel (pair mode) with up to 128 rows from 17 (forced_path as for make_plan).
+Plan make_plan_moe(int E, int M, int max_rows, int K, int N, int G, int sms, int smem_optin, int ablate = 0,
+                   int forced_path = 0);
 // c.M = rows of A and C, c.packed / c.scales = E stacked layers; zeros and bias unused.
 int run_moe_gemm(const Plan& pl, const GemmCall& c, const int* expert_off);
 

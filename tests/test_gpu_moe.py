@@ -210,3 +210,122 @@ def test_moe_timeout_is_reported_and_context_survives(w):
     C2 = _run(w, lay, N, 8, packed, sp, ws)
     C_ref, bound = oracle.moe_gemm_ref(lay["A"], lay["offsets"], lay["q"], lay["s"], G)
     tl.assert_within_bound(C2, C_ref, bound, "after timeout")
+
+
+# ---------------------------------------------------------------------------
+# From 17 rows per expert the grouped GEMM runs on the tensor-memory kernel (pair mode, row
+# segments of max_rows rounded up to 16, at most 128 rows): the same checks on that path.
+# ---------------------------------------------------------------------------
+
+TC_CASES = [
+    # counts per expert, K, N, G, max_rows
+    ([21, 3, 0, 17, 8, 19, 0, 12], 1024, 512, 128, 32),     # Mixtral-like: 2 of 8 experts per token
+    ([40, 64, 1, 0], 4096, 1024, 128, 64),                  # 64-row segments
+    ([200, 3, 0, 50], 2048, 768, 128, 200),                 # 200 rows: two 128-row segments of one expert
+    ([33, 31, 32, 1], 768, 384, 128, 48),                   # K / 128 = 6 (256-row units), three strips
+    ([20, 0, 19], 640, 256, -1, 32),                        # K / 128 = 5 (128-row units), per-column scales
+    ([0, 0, 0, 90], 512, 1280, 128, 96),                    # only the last expert owns rows
+]
+
+
+@pytest.mark.parametrize("counts,K,N,G,max_rows", TC_CASES)
+def test_moe_tensor_memory_path_matches_oracle(w, counts, K, N, G, max_rows):
+    assert max_rows >= 17
+    lay = synth.make_moe_layer(0, 0, len(counts), K, N, G, seed=sum(counts) + K, counts=counts)
+    C = _run(w, lay, N, max_rows)
+    C_ref, bound = oracle.moe_gemm_ref(lay["A"], lay["offsets"], lay["q"], lay["s"], G)
+    tl.assert_within_bound(C, C_ref, bound, f"tcgen05 moe counts={counts} K={K} N={N} G={G}")
+    assert w.w4a16_get_status() == 0
+
+
+def test_moe_tensor_memory_identity_rows_are_exact(w):
+    K, N, G = 1024, 512, 128
+    counts = [18, 0, 23, 5]
+    lay = synth.make_moe_layer(0, 0, len(counts), K, N, G, seed=81, counts=counts)
+    M = sum(counts)
+    ks = [(53 * m + 7) % K for m in range(M)]
+    A = np.zeros((M, K), np.float16)
+    for m, k in enumerate(ks):
+        A[m, k] = 1.0
+    lay["A"] = A
+    C = _run(w, lay, N, 32)
+    off = lay["offsets"]
+    for m, k in enumerate(ks):
+        e = int(np.searchsorted(off, m, side="right")) - 1
+        want = oracle.dequant_fp16_bits(lay["q"][e], lay["s"][e], G)[k]
+        assert np.array_equal(C[m].view(np.uint16), want), (m, e, k)
+
+
+def test_moe_forced_tensor_memory_path_with_small_segments(w):
+    """The tensor-memory path forced onto 8-row experts (16-row segments)."""
+    K, N, G = 1024, 384, 128
+    lay = synth.make_moe_layer(24, 2, 8, K, N, G, seed=82, skew=1.0)
+    w.w4a16_debug_force_path(2)
+    try:
+        C = _run(w, lay, N, 8)
+    finally:
+        w.w4a16_debug_force_path(0)
+    C_ref, bound = oracle.moe_gemm_ref(lay["A"], lay["offsets"], lay["q"], lay["s"], G)
+    tl.assert_within_bound(C, C_ref, bound, "forced tcgen05 moe")
+
+
+def test_moe_tensor_memory_repeats_are_bitwise_identical(w):
+    torch = tl.torch_mod()
+    K, N, G = 2048, 1024, 128
+    counts = [30, 12, 0, 27, 31, 1, 19, 8]
+    lay = synth.make_moe_layer(0, 0, len(counts), K, N, G, seed=83, counts=counts)
+    packed, sp = _device_experts(w, lay["q"], lay["s"], G)
+    M = sum(counts)
+    ws = w.moe_workspace_for(len(counts), M, 32, K, N, G)
+    first = _run(w, lay, N, 32, packed, sp, ws)
+    for _ in range(12):
+        again = _run(w, lay, N, 32, packed, sp, ws)
+        assert np.array_equal(first.view(np.uint16), again.view(np.uint16))
+    assert w.w4a16_get_status(ws) == 0
+    C_ref, bound = oracle.moe_gemm_ref(lay["A"], lay["offsets"], lay["q"], lay["s"], G)
+    tl.assert_within_bound(first, C_ref, bound, "tcgen05 moe repeats")
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("bad", [[1, 20, 40], [0, 25, 20], [0, 20, 41]])
+def test_moe_tensor_memory_invalid_offsets(w, bad):
+    torch = tl.torch_mod()
+    K, N, G = 512, 256, 128
+    lay = synth.make_moe_layer(0, 0, 2, K, N, G, seed=84, counts=[20, 20])
+    packed, sp = _device_experts(w, lay["q"], lay["s"], G)
+    M = 40
+    ws = w.moe_workspace_for(2, M, 32, K, N, G)
+    C = torch.full((M, N), 7.0, dtype=torch.float16, device="cuda")
+    w.moe_gemm(tl.to_dev(lay["A"]), packed, sp, tl.to_dev(np.array(bad, np.int32)), N, G, max_rows=32, workspace=ws,
+               out=C)
+    assert w.w4a16_get_status(ws) == 10   # W4A16_ERR_VALUE
+    assert bool((C == 7.0).all())
+    C2 = w.moe_gemm(tl.to_dev(lay["A"]), packed, sp, tl.to_dev(lay["offsets"]), N, G, max_rows=32, workspace=ws)
+    torch.cuda.synchronize()
+    C_ref, bound = oracle.moe_gemm_ref(lay["A"], lay["offsets"], lay["q"], lay["s"], G)
+    tl.assert_within_bound(C2.cpu().numpy(), C_ref, bound, "tcgen05 moe after invalid offsets")
+
+
+def test_moe_tensor_memory_timeout_is_reported_and_context_survives(w):
+    torch = tl.torch_mod()
+    K, N, G = 2048, 1024, 128
+    counts = [20, 30, 0, 18]
+    lay = synth.make_moe_layer(0, 0, len(counts), K, N, G, seed=85, counts=counts)
+    packed, sp = _device_experts(w, lay["q"], lay["s"], G)
+    M = sum(counts)
+    ws = w.moe_workspace_for(len(counts), M, 32, K, N, G)
+    C = torch.full((M, N), 7.0, dtype=torch.float16, device="cuda")
+    A_d, off_d = tl.to_dev(lay["A"]), tl.to_dev(lay["offsets"])
+    try:
+        w.w4a16_debug_set_wait_cycles(2_000_000)  # about a millisecond
+        w.w4a16_debug_inject_stall(True)
+        w.moe_gemm(A_d, packed, sp, off_d, N, G, max_rows=32, workspace=ws, out=C)
+    finally:
+        w.w4a16_debug_inject_stall(False)
+        w.w4a16_debug_set_wait_cycles(0)
+    assert w.w4a16_get_status(ws) == 7
+    assert bool((C == 7.0).all())
+    ws.zero_()
+    C2 = _run(w, lay, N, 32, packed, sp, ws)
+    C_ref, bound = oracle.moe_gemm_ref(lay["A"], lay["offsets"], lay["q"], lay["s"], G)
+    tl.assert_within_bound(C2, C_ref, bound, "tcgen05 moe after timeout")
