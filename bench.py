@@ -64,7 +64,7 @@ WORKLOADS = {
 
 # grouped expert GEMM sweep: (description, experts, top-k, K, N, groupsize, [tokens ...])
 MOE_CONFIGS = [
-    ("8 experts top-2, K=4096 N=14336 (Mixtral-style expert up-projection)", 8, 2, 4096, 14336, 128, [1, 4, 16, 64]),
+    ("8 experts top-2, K=4096 N=14336 (Mixtral-style expert up-projection)", 8, 2, 4096, 14336, 128, [1, 4, 16, 64, 256]),
     ("128 experts top-8, K=2048 N=1536 (Qwen3-30B-A3B-style fused gate/up)", 128, 8, 2048, 1536, 128, [1, 16, 64]),
     ("256 experts top-8, K=7168 N=4096 (DeepSeek-V3-style fused gate/up)", 256, 8, 7168, 4096, 128, [1, 16, 64]),
 ]
@@ -1054,7 +1054,9 @@ def time_moe(w, torch, device, peaks, only_config=None, per_expert_context=True)
             nbytes = len(active) * (K * N // 2 + 2 * NG * N) + 2 * M * K + 2 * M * N
             gbs = nbytes / (res["grouped"] * 1e-6) / 1e9
             out.append({"config": desc, "tokens": tokens, "rows": M, "active_experts": len(active),
-                        "max_rows_per_expert": max_rows, "us": round(res["grouped"], 1), "bytes": nbytes,
+                        "max_rows_per_expert": max_rows,
+                        "kernel": "gemm_tc_kernel" if max_rows >= 17 else "gemm_mma_kernel",  # the library's rule
+                        "us": round(res["grouped"], 1), "bytes": nbytes,
                         "gb_s": round(gbs, 1), "roofline_frac": round(gbs / peaks["hbm_gbs"], 3),
                         "per_expert_launches_us": None if res["per_expert"] is None else round(res["per_expert"], 1)})
             del A_d, C_d, ws, dense_ws
