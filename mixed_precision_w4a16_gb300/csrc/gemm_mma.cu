@@ -354,31 +354,40 @@ if constexpr (SP24) {
           spv[i] = lds32(st + p.s_off + (srow * 128 + nb * 16 + 2 * g) * 2);
           zpv[i] = ZP ? lds_u16(st + p.z_off + srow * 128 + nb * 16 + 2 * g) : 0u;  // (z of row g, z of row g + 8)
         }
+        // k16 step outermost: the kNbw x MT accumulator chains advance together, so consecutive
+        // multiplies are independent (measured: M = 16 about 3 % faster than block by block)
+        uint32_t c_lo[kNbw], c_hi[kNbw];
 #pragma unroll
         for (int i = 0; i < kNbw; ++i) {
-          const uint32_t words[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
-          const uint32_t c_lo = ZP ? zp_const_lo(zpv[i] & 15u) : 0u;
-          const uint32_t c_hi = ZP ? zp_const_hi((zpv[i] >> 8) & 15u) : 0u;
-          float tmp[MT][4];
+          c_lo[i] = ZP ? zp_const_lo(zpv[i] & 15u) : 0u;
+          c_hi[i] = ZP ? zp_const_hi((zpv[i] >> 8) & 15u) : 0u;
+        }
+        float tmp[kNbw][MT][4];
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
+        for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+          for (int i = 0; i < kNbw; ++i) {
+            const uint32_t word = jj == 0 ? wv[i].x : jj == 1 ? wv[i].y : jj == 2 ? wv[i].z : wv[i].w;
             uint32_t a[4];
             if (ZP)
-              decode8_zp(words[jj], c_lo, c_hi, a);
+              decode8_zp(word, c_lo[i], c_hi[i], a);
             else
-              decode8(words[jj], a);
+              decode8(word, a);
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
-              mma_16816(tmp[mt], a, bf[jj][mt][0], bf[jj][mt][1], jj == 0 ? zero4 : tmp[mt]);
+              mma_16816(tmp[i][mt], a, bf[jj][mt][0], bf[jj][mt][1], jj == 0 ? zero4 : tmp[i][mt]);
           }
+        }
+#pragma unroll
+        for (int i = 0; i < kNbw; ++i) {
           const float s_lo = __half2float(__ushort_as_half(static_cast<uint16_t>(spv[i] & 0xffffu)));
           const float s_hi = __half2float(__ushort_as_half(static_cast<uint16_t>(spv[i] >> 16)));
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
-            acc[i][mt][0] = fmaf(s_lo, tmp[mt][0], acc[i][mt][0]);
-            acc[i][mt][1] = fmaf(s_lo, tmp[mt][1], acc[i][mt][1]);
-            acc[i][mt][2] = fmaf(s_hi, tmp[mt][2], acc[i][mt][2]);
-            acc[i][mt][3] = fmaf(s_hi, tmp[mt][3], acc[i][mt][3]);
+            acc[i][mt][0] = fmaf(s_lo, tmp[i][mt][0], acc[i][mt][0]);
+            acc[i][mt][1] = fmaf(s_lo, tmp[i][mt][1], acc[i][mt][1]);
+            acc[i][mt][2] = fmaf(s_hi, tmp[i][mt][2], acc[i][mt][2]);
+            acc[i][mt][3] = fmaf(s_hi, tmp[i][mt][3], acc[i][mt][3]);
           }
         }
         }
