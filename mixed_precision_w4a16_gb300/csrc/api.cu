@@ -170,7 +170,7 @@ int w4a16_repack(const uint8_t* q, const uint16_t* s, int K, int N, int groupsiz
   DeviceInfo* d = nullptr;
   const int r = current_device_info(&d);
   if (r != W4A16_OK) return r;
-  const cudaError_t e = launch_repack(q, s, K, N, effective_group(K, groupsize), packed, scales_p,
+  const cudaError_t e = launch_repack(q, s, K, N, effective_group(K, groupsize), packed, scales_p, d->sms,
                                       static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
 }
@@ -191,7 +191,7 @@ int w4a16_quantize_repack_zp(const uint16_t* w, const uint16_t* s, const uint8_t
   const int r = current_device_info(&d);
   if (r != W4A16_OK) return r;
   const cudaError_t e = launch_quantize_repack(w, s, z, K, N, effective_group(K, groupsize), packed, scales_p,
-                                               static_cast<cudaStream_t>(stream));
+                                               d->sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
 }
 

@@ -182,10 +182,11 @@ struct TcParams {
 
 cudaError_t launch_gemm_tc(int smem_bytes, const CUtensorMap& tmA, const TcParams& p, cudaStream_t stream);
 
+// sms: the device's SM count (the tile walkers are persistent)
 cudaError_t launch_repack(const uint8_t* q, const uint16_t* s, int K, int N, int G, uint32_t* packed,
-                          uint16_t* scales_p, cudaStream_t stream);
+                          uint16_t* scales_p, int sms, cudaStream_t stream);
 cudaError_t launch_quantize_repack(const uint16_t* w, const uint16_t* s, const uint8_t* z, int K, int N, int G,
-                                   uint32_t* packed, uint16_t* scales_p, cudaStream_t stream);
+                                   uint32_t* packed, uint16_t* scales_p, int sms, cudaStream_t stream);
 cudaError_t launch_minmax_scales(const uint16_t* w, int K, int N, int G, uint16_t* s, uint8_t* z,
                                  cudaStream_t stream);
 cudaError_t launch_repack_zeros(const uint8_t* z, int K, int N, int G, uint8_t* zeros_p, cudaStream_t stream);

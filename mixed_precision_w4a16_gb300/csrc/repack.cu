@@ -19,6 +19,8 @@
 // packed stream is a coalesced 16-byte store.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 #include "sparse24.h"
@@ -54,114 +56,328 @@ __device__ __forceinline__ void slot_rc(int slot, int g, int t, int& r, int& c) 
   c = 4 * t + 2 * (reg >> 1) + e;
 }
 
-// One CTA of 256 threads per 64-row x 128-column tile (one strip, one 64-row block):
-// the tile's codes are read row by row into shared memory (coalesced 16-byte loads),
-// then thread (block b, lane) assembles its four words from there and writes its
-// 16-byte vector; the CTA's 256 vectors are consecutive in the packed stream.  The
-// rows are padded so that the four lanes t of a quad, which read rows 4 apart, hit
-// different banks.
+// Both tile walkers below are persistent: CTA c takes the tiles [c*T, (c+1)*T) of the packed
+// stream's order (strip by strip, 64-row blocks down each strip), so its output is one
+// contiguous range and consecutive tiles of a strip share their scale group.  A tile is 64 rows
+// x 128 columns (one strip, one 64-row block); its 256 output vectors (16 bytes, one per
+// thread: warp b = 16-column block, lane = fragment lane) are consecutive in the packed stream.
+// Tiles are copied into a ring of three shared buffers (cp.async, 16 bytes per copy), two tiles
+// ahead of the one being packed; one block barrier per tile both publishes the tile's copies and
+// frees the buffer the next copy overwrites (the one packed in the previous iteration).
 constexpr int kTileThreads = 256;
-constexpr int kCodeRow = 136;  // bytes per shared row of codes (128 + 8)
-constexpr int kHalfRow = 132;  // halves per shared row of FP16 weights (128 + 4)
+constexpr int kTileCtasPerSm = 4;
+constexpr int kTileStages = 3;
 
-__global__ void __launch_bounds__(kTileThreads) repack_codes_kernel(const uint8_t* __restrict__ q, int K, int N,
-                                                                    uint4* __restrict__ packed) {
-  __shared__ __align__(16) uint8_t tile[64][kCodeRow];
-  const int kTiles = K / 64;
-  const int kb = static_cast<int>(blockIdx.x % kTiles);
-  const long long strip = blockIdx.x / kTiles;
-  for (int i = threadIdx.x; i < 64 * 8; i += kTileThreads) {  // 64 rows x 8 16-byte pieces
-    const int r = i >> 3, c16 = i & 7;
-    const uint4 v = *reinterpret_cast<const uint4*>(q + (kb * 64LL + r) * N + strip * 128 + 16 * c16);
-    *reinterpret_cast<uint2*>(&tile[r][16 * c16]) = make_uint2(v.x, v.y);
-    *reinterpret_cast<uint2*>(&tile[r][16 * c16 + 8]) = make_uint2(v.z, v.w);
-  }
-  __syncthreads();
-  const int b = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-  uint32_t words[4];
-  uint32_t bad = 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint32_t w = 0;
-#pragma unroll
-    for (int slot = 0; slot < 8; ++slot) {
-      int r, c;
-      slot_rc(slot, g, t, r, c);
-      const uint32_t code = tile[16 * j + c][16 * b + r];
-      bad |= code > 15u;
-      w |= (code & 15u) << (4 * slot);
-    }
-    words[j] = w;
-  }
-  if (bad) atomicOr(&g_repack_flag, kDevErrCodeRange);
-  packed[static_cast<long long>(blockIdx.x) * kTileThreads + threadIdx.x] = make_uint4(words[0], words[1], words[2], words[3]);
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// wait until at most kTileStages - 2 committed groups (the tiles after this one) are in flight
+__device__ __forceinline__ void cp_async_wait_tile() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(kTileStages - 2) : "memory");
 }
 
-// Quantise FP16 weights with their FP16 scales straight into the packed layout
-// (the original Layer.pack step, deep-dive article section "可复现的调用链"):
-// q = clamp(rint(w / s) + 8, 0, 15), the quotient an IEEE float32 division,
-// rint rounding half to even.  Same word-side walk as repack_codes_kernel.
-// z: zero codes uint8[K/G][N] row-major, or null for the symmetric offset 8.  Tiled like
-// repack_codes_kernel: the 64-row tile lies inside one group (G is 128 or K), so its 128
-// scales (and zero codes) are one row.
-__global__ void __launch_bounds__(kTileThreads) quantize_codes_kernel(const uint16_t* __restrict__ w,
-                                                                      const uint16_t* __restrict__ s,
-                                                                      const uint8_t* __restrict__ z, int K, int N,
-                                                                      int G, uint4* __restrict__ packed) {
-  __shared__ __align__(16) uint16_t tile[64][kHalfRow];
-  __shared__ float scale[128];
-  __shared__ float recip[128];
-  __shared__ float offset[128];
-  const int kTiles = K / 64;
-  const int kb = static_cast<int>(blockIdx.x % kTiles);
-  const long long strip = blockIdx.x / kTiles;
-  for (int i = threadIdx.x; i < 64 * 16; i += kTileThreads) {  // 64 rows x 16 16-byte pieces
-    const int r = i >> 4, c8 = i & 15;
-    const uint4 v = *reinterpret_cast<const uint4*>(w + (kb * 64LL + r) * N + strip * 128 + 8 * c8);
-    *reinterpret_cast<uint2*>(&tile[r][8 * c8]) = make_uint2(v.x, v.y);
-    *reinterpret_cast<uint2*>(&tile[r][8 * c8 + 4]) = make_uint2(v.z, v.w);
+struct TileRange {
+  long long t0, t1;
+};
+__device__ __forceinline__ TileRange tile_range(int T, long long tiles) {
+  const long long t0 = static_cast<long long>(blockIdx.x) * T;
+  return {t0, t0 + T < tiles ? t0 + T : tiles};
+}
+
+// (strip, 64-row block) of a tile, stepped along the CTA's range without dividing per tile
+struct TilePos {
+  int strip;
+  int kb;
+  __device__ __forceinline__ TilePos next(int kTiles) const {
+    return kb + 1 == kTiles ? TilePos{strip + 1, 0} : TilePos{strip, kb + 1};
   }
-  if (threadIdx.x < 128) {
-    const long long gi = ((kb * 64LL) / G) * N + strip * 128 + threadIdx.x;
-    const float sf = __half2float(__ushort_as_half(s[gi]));
-    scale[threadIdx.x] = sf;
-    recip[threadIdx.x] = __frcp_rn(sf);
-    offset[threadIdx.x] = z ? static_cast<float>(z[gi]) : 8.0f;
-  }
-  __syncthreads();
-  const int b = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-  uint32_t words[4];
-  bool bad = false;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint32_t word = 0;
-#pragma unroll
-    for (int slot = 0; slot < 8; ++slot) {
-      int r, c;
-      slot_rc(slot, g, t, r, c);
-      const int col = 16 * b + r;
-      const float wf = __half2float(__ushort_as_half(tile[16 * j + c][col]));
-      // w * RN(1/s) is within 1.5 ulp of w / s; away from the half-integers it rounds to the
-      // same integer as the correctly rounded quotient, which is taken only near them
-      const float approx = wf * recip[col];
-      const float frac = fabsf(approx - truncf(approx));
-      const bool near_tie = fabsf(frac - 0.5f) <= 0x1p-22f * fabsf(approx);  // twice the error bound 2^-23 |w/s|
-      const float quot = (isfinite(approx) && !near_tie) ? approx : __fdiv_rn(wf, scale[col]);
-      uint32_t code = 8u;
-      if (isfinite(quot)) {
-        const float qf = fminf(fmaxf(rintf(quot) + offset[col], 0.0f), 15.0f);
-        code = static_cast<uint32_t>(qf);
-      } else {
-        bad = true;
-      }
-      word |= code << (4 * slot);
+};
+
+// The copy side of the ring: issue(pos, stage) copies one tile; every call commits exactly one
+// group (empty past the range's end), so the group count per iteration stays uniform.
+template <class Issue>
+struct TileFeed {
+  Issue issue;
+  TilePos pos;      // next tile to copy
+  long long left;   // tiles of the range not yet copied
+  int kTiles;
+  __device__ __forceinline__ void push(int stage) {
+    if (left > 0) {
+      issue(pos, stage);
+      pos = pos.next(kTiles);
+      --left;
     }
-    words[j] = word;
+    cp_async_commit();
+  }
+};
+
+// Codes: a tile is 64 rows of 128 bytes in shared memory.  In one load instruction the lanes of
+// a warp read rows 4t + c (t = 0..3, c fixed) at the same 16-byte chunk b, so chunk b of row k is
+// stored at chunk b ^ ((k >> 2) & 3): the four rows then sit in four different bank groups.
+__device__ __forceinline__ int code_chunk(int k, int chunk) { return chunk ^ ((k >> 2) & 3); }
+
+__global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
+    repack_codes_kernel(const uint8_t* __restrict__ q, int K, int N, int T, long long tiles,
+                        uint4* __restrict__ packed) {
+  __shared__ __align__(16) uint8_t buf[kTileStages][64][128];
+  const TileRange tr = tile_range(T, tiles);
+  if (tr.t0 >= tr.t1) return;
+  const int kTiles = K / 64;
+  const int tid = threadIdx.x;
+  auto issue = [&](TilePos tp, int stage) {
+    const uint8_t* src = q + tp.kb * 64LL * N + tp.strip * 128;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {  // 64 rows x 8 chunks
+      const int c = tid + kTileThreads * i, r = c >> 3, ch = c & 7;
+      cp_async16(smem_u32(&buf[stage][r][16 * code_chunk(r, ch)]), src + static_cast<long long>(r) * N + 16 * ch);
+    }
+  };
+  TileFeed<decltype(issue)> feed{issue, {static_cast<int>(tr.t0 / kTiles), static_cast<int>(tr.t0 % kTiles)},
+                                 tr.t1 - tr.t0, kTiles};
+  for (int st = 0; st < kTileStages - 1; ++st) feed.push(st);
+  const int b = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  uint32_t seen = 0;  // OR of every code read: a code above 15 sets a bit above the nibble
+  int stage = 0;
+  for (long long tile = tr.t0; tile < tr.t1; ++tile) {
+    cp_async_wait_tile();
+    __syncthreads();
+    feed.push(stage == 0 ? kTileStages - 1 : stage - 1);
+    uint32_t words[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      // nibble slots 7 .. 0, most significant first; a code above 15 is masked to its nibble
+      uint32_t w = 0;
+#pragma unroll
+      for (int slot_i = 7; slot_i >= 0; --slot_i) {
+        int r, c;
+        slot_rc(slot_i, g, t, r, c);
+        const int k = 16 * j + c;
+        const uint32_t code = buf[stage][k][16 * code_chunk(k, b) + r];
+        seen |= code;
+        w = (w << 4) | (code & 15u);
+      }
+      words[j] = w;
+    }
+    packed[tile * kTileThreads + tid] = make_uint4(words[0], words[1], words[2], words[3]);
+    stage = stage + 1 == kTileStages ? 0 : stage + 1;
+  }
+  if (seen > 15u) atomicOr(&g_repack_flag, kDevErrCodeRange);
+}
+
+// FP16 weights: a tile is 64 rows of 128 halves, each shared row padded to 136 halves (272
+// bytes, 17 16-byte chunks).  The packing reads it with transposed 8x8 matrix loads: matrix m of
+// 16-row block j holds rows 16j + 4i' + 2(m >> 1) + {0, 1} (i' = 0..3) of columns 16b + 8(m & 1)
+// + 0..7, which hands lane (g, t) exactly its register m (reduction rows 4t + 2(m >> 1) + {0, 1}
+// of column g + 8(m & 1)).  Rows k and k + 8 would share a bank group, so rows with bit 3 set swap
+// row pairs (k ^ 2): the eight rows of one matrix then fall into eight different groups.
+constexpr int kHalfRow = 136;
+// one stage: the tile, then the 128 scales and 128 zero codes of its group row
+constexpr int kQuantTileBytes = 64 * kHalfRow * 2;
+constexpr int kQuantStageBytes = kQuantTileBytes + 128 * 2 + 128;
+constexpr int kQuantSmem = kTileStages * kQuantStageBytes;
+__device__ __forceinline__ int half_row(int k) { return k ^ (((k >> 3) & 1) << 1); }
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t d[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+               : "r"(addr));
+}
+
+// Per column (and scale group) constants of the quantiser's fast path.
+struct QuantCol {
+  float s;       // the scale
+  float lo;      // -offset: the smallest rint(w / s) that still stores as code 0 or above
+  float hi;      // 15 - offset
+  float off;     // the offset: 8, or the zero code
+  uint64_t y2;   // RN(1 / s), twice (a float pair)
+  uint64_t ns2;  // -s, twice
+  bool bad;      // s is zero, infinite or NaN: the fast path does not apply to the column
+};
+__device__ __forceinline__ uint64_t f32_pair(float x) {
+  return (static_cast<uint64_t>(__float_as_uint(x)) << 32) | __float_as_uint(x);
+}
+__device__ __forceinline__ QuantCol quant_col(uint16_t s_bits, float off) {
+  QuantCol c;
+  c.s = __half2float(__ushort_as_half(s_bits));
+  c.off = off;
+  c.lo = -c.off;
+  c.hi = 15.0f - c.off;
+  c.y2 = f32_pair(__frcp_rn(c.s));
+  c.ns2 = f32_pair(-c.s);
+  c.bad = (c.s == 0.0f) || !isfinite(c.s);
+  return c;
+}
+
+// Both FP16 halves of a fragment register (the same column, reduction rows k and k + 1): their
+// float32 quotients by the column's scale (packed pairs: q0 = RN(w y), r = fma(q0, -s, w),
+// q1 = fma(r, y, q0)), clamped to [lo, hi], plus 1.5 * 2^23 (packed); returns the two sums' bits.
+// nan_acc = fma(halves, 0, nan_acc) stays zero unless a half is infinite or NaN.
+__device__ __forceinline__ void quant_pair(uint32_t d, const QuantCol& c, uint32_t& v_lo, uint32_t& v_hi,
+                                           uint32_t& nan_acc) {
+  asm("{\n"
+      "  .reg .b16 h0, h1;\n"
+      "  .reg .f32 w0, w1, a0, a1;\n"
+      "  .reg .b64 w2, q0, r2, q1, m2;\n"
+      "  .reg .b32 zero;\n"
+      "  mov.b32 zero, 0;\n"
+      "  mov.b32 {h0, h1}, %3;\n"
+      "  cvt.f32.f16 w0, h0;\n"
+      "  cvt.f32.f16 w1, h1;\n"
+      "  fma.rn.f16x2 %2, %3, zero, %2;\n"
+      "  mov.b64 w2, {w0, w1};\n"
+      "  mul.rn.f32x2 q0, w2, %4;\n"
+      "  fma.rn.f32x2 r2, q0, %5, w2;\n"
+      "  fma.rn.f32x2 q1, r2, %4, q0;\n"
+      "  mov.b64 {a0, a1}, q1;\n"
+      "  max.f32 a0, a0, %6;\n"
+      "  max.f32 a1, a1, %6;\n"
+      "  min.f32 a0, a0, %7;\n"
+      "  min.f32 a1, a1, %7;\n"
+      "  mov.b64 q1, {a0, a1};\n"
+      "  add.rn.f32x2 m2, q1, %8;\n"
+      "  mov.b64 {%0, %1}, m2;\n"
+      "}\n"
+      : "=r"(v_lo), "=r"(v_hi), "+r"(nan_acc)
+      : "r"(d), "l"(c.y2), "l"(c.ns2), "f"(c.lo), "f"(c.hi), "l"(0x4B4000004B400000ull));
+}
+
+// The reference rule for one weight: the IEEE float32 quotient, rounded half to even, plus the
+// offset, clamped; a non-finite quotient gives code 8 and flags the call.
+__device__ __forceinline__ uint32_t quant_exact(float wf, const QuantCol& c, bool& bad) {
+  const float quot = __fdiv_rn(wf, c.s);
+  if (!isfinite(quot)) {
+    bad = true;
+    return 8u;
+  }
+  return static_cast<uint32_t>(fminf(fmaxf(rintf(quot) + c.off, 0.0f), 15.0f));
+}
+
+__device__ __forceinline__ float half_of(const uint32_t d[4], int si) {
+  const int m = si & 3;
+  return __half2float(__ushort_as_half(static_cast<uint16_t>(si >= 4 ? d[m] >> 16 : d[m] & 0xffffu)));
+}
+
+// Quantise FP16 weights with their FP16 scales straight into the packed layout (the original
+// Layer.pack step, deep-dive article section "可复现的调用链"): q = clamp(rint(w / s) + 8, 0, 15)
+// (or + z), the quotient an IEEE float32 division, rint rounding half to even.
+//
+// The quotient is formed without a division: with y = RN(1/s), q0 = RN(w y), the residual
+// r = fma(-q0, s, w) (exact) and q1 = fma(r, y, q0).  For FP16 operands q1 equals the correctly
+// rounded float32 quotient RN(w/s): this one-step correction (Markstein's) holds whenever no
+// intermediate under- or overflows, true for every FP16 pair (|w/s| lies in [2^-40, 2^40]), and
+// an exhaustive check over all pairs of FP16 significands at several exponent offsets found no
+// exception.  Clamping q1 to [-offset, 15 - offset] commutes with rounding to an integer (the
+// bounds are integers), and adding 1.5 * 2^23 rounds it half to even into the low mantissa bits;
+// the eight slots are summed into the word with their offsets added back.  Both halves of a
+// fragment register share their column, so the quotient and the rounding run on float pairs.
+// An infinite or NaN weight is caught by fma(w, 0, acc) accumulated over the thread's tile; its
+// words, and the columns whose scale is zero, infinite or NaN, are recomputed with the
+// reference rule slot by slot.
+// z: zero codes uint8[K/G][N] row-major, or null for the symmetric offset 8.
+__global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
+    quantize_codes_kernel(const uint16_t* __restrict__ w, const uint16_t* __restrict__ s,
+                          const uint8_t* __restrict__ z, int K, int N, int G, int T, long long tiles,
+                          uint4* __restrict__ packed) {
+  extern __shared__ __align__(16) uint8_t qbuf[];  // kTileStages x (tile, scales, zero codes)
+  const TileRange tr = tile_range(T, tiles);
+  if (tr.t0 >= tr.t1) return;
+  const int kTiles = K / 64;
+  const int tid = threadIdx.x;
+  const uint32_t qbase = smem_u32(qbuf);
+  auto row_addr = [&](int stage, int row) {
+    return qbase + static_cast<uint32_t>(stage * kQuantStageBytes + row * kHalfRow * 2);
+  };
+  auto issue = [&](TilePos tp, int stage) {
+    const uint16_t* src = w + tp.kb * 64LL * N + tp.strip * 128LL;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // 64 rows x 16 chunks
+      const int c = tid + kTileThreads * i, r = c >> 4, ch = c & 15;
+      cp_async16(row_addr(stage, half_row(r)) + 16 * ch, src + static_cast<long long>(r) * N + 8 * ch);
+    }
+    // the group row's 128 scales (16 chunks) and zero codes (8 chunks)
+    const long long gi = static_cast<long long>(G == 128 ? tp.kb >> 1 : 0) * N + tp.strip * 128LL;
+    const uint32_t sdst = qbase + static_cast<uint32_t>(stage * kQuantStageBytes + kQuantTileBytes);
+    if (tid < 16)
+      cp_async16(sdst + 16 * tid, s + gi + 8 * tid);
+    else if (z && tid < 24)
+      cp_async16(sdst + 256 + 16 * (tid - 16), z + gi + 16 * (tid - 16));
+  };
+  TilePos pos{static_cast<int>(tr.t0 / kTiles), static_cast<int>(tr.t0 % kTiles)};
+  TileFeed<decltype(issue)> feed{issue, pos, tr.t1 - tr.t0, kTiles};
+  for (int st = 0; st < kTileStages - 1; ++st) feed.push(st);
+  const int b = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2;
+  // this lane's row and column in the transposed matrix loads
+  const int mi = lane >> 3, ri = lane & 7;
+  const int ld_row = 4 * (ri >> 1) + 2 * (mi >> 1) + (ri & 1);
+  const int ld_col = 16 * b + 8 * (mi & 1);
+  constexpr uint32_t kMagicBits = 0x4B400000u;              // bits of 1.5 * 2^23
+  constexpr uint32_t kMagicSum = kMagicBits * 0x11111111u;  // its sum over the eight nibble slots
+  bool bad = false;
+  QuantCol col[2];
+  uint32_t word_add = 0;  // per word: the offsets of the eight slots minus the magic constants
+  int kb = pos.kb;
+  bool first = true;
+  int stage = 0;
+  for (long long tile = tr.t0; tile < tr.t1; ++tile) {
+    cp_async_wait_tile();
+    __syncthreads();
+    feed.push(stage == 0 ? kTileStages - 1 : stage - 1);
+    // a new scale group starts at every strip's first tile and, for G = 128, every even block
+    if (first || (G == 128 ? (kb & 1) == 0 : kb == 0)) {  // uniform over the CTA
+      first = false;
+      const uint8_t* sg = qbuf + stage * kQuantStageBytes + kQuantTileBytes;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int n = 16 * b + 8 * h + g;
+        col[h] = quant_col(reinterpret_cast<const uint16_t*>(sg)[n], z ? static_cast<float>(sg[256 + n]) : 8.0f);
+      }
+      // even slots belong to column g, odd slots to column g + 8
+      word_add = static_cast<uint32_t>(col[0].off) * 0x01010101u + static_cast<uint32_t>(col[1].off) * 0x10101010u -
+                 kMagicSum;
+    }
+    kb = kb + 1 == kTiles ? 0 : kb + 1;
+    uint32_t words[4];
+    uint32_t need = (col[0].bad || col[1].bad) ? 15u : 0u;  // bit j: word j takes the reference rule
+    uint32_t nan_acc = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t d[4];
+      ldmatrix_x4_trans(row_addr(stage, half_row(16 * j + ld_row)) + 2 * ld_col, d);
+      // slot m + 4e holds half e of register m (column half m & 1): slots 0-3 in the low and
+      // slots 4-7 in the high half of the word
+      uint32_t acc_lo = 0, acc_hi = 0;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        uint32_t v_lo, v_hi;
+        quant_pair(d[m], col[m & 1], v_lo, v_hi, nan_acc);
+        acc_lo += v_lo << (4 * m);
+        acc_hi += v_hi << (4 * m);
+      }
+      words[j] = acc_lo + (acc_hi << 16) + word_add;
+    }
+    if (nan_acc & 0x7fff7fffu) need = 15u;  // an infinite or NaN weight in this thread's tile
+    if (__any_sync(0xffffffffu, need != 0)) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (__any_sync(0xffffffffu, (need >> j) & 1u)) {  // warp-uniform: the matrix load is collective
+          uint32_t d[4];
+          ldmatrix_x4_trans(row_addr(stage, half_row(16 * j + ld_row)) + 2 * ld_col, d);
+          if ((need >> j) & 1u) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int si = 7; si >= 0; --si) word = (word << 4) | quant_exact(half_of(d, si), col[si & 1], bad);
+            words[j] = word;
+          }
+        }
+      }
+    }
+    packed[tile * kTileThreads + tid] = make_uint4(words[0], words[1], words[2], words[3]);
+    stage = stage + 1 == kTileStages ? 0 : stage + 1;
   }
   if (bad) atomicOr(&g_repack_flag, kDevErrValue);
-  packed[static_cast<long long>(blockIdx.x) * kTileThreads + threadIdx.x] = make_uint4(words[0], words[1], words[2], words[3]);
 }
 
 // permuted position p inside a 16-column block -> fragment row r
@@ -318,10 +534,18 @@ inline unsigned grid_for(long long n, int block) { return static_cast<unsigned>(
 
 }  // namespace
 
+// T tiles per CTA, for kTileCtasPerSm CTAs on every SM
+inline int tiles_per_cta(long long tiles, int sms) {
+  const long long ctas = static_cast<long long>(std::max(sms, 1)) * kTileCtasPerSm;
+  return static_cast<int>((tiles + ctas - 1) / ctas);
+}
+
 cudaError_t launch_repack(const uint8_t* q, const uint16_t* s, int K, int N, int G, uint32_t* packed,
-                          uint16_t* scales_p, cudaStream_t stream) {
-  const unsigned tiles = static_cast<unsigned>(static_cast<long long>(N / 128) * (K / 64));
-  repack_codes_kernel<<<tiles, kTileThreads, 0, stream>>>(q, K, N, reinterpret_cast<uint4*>(packed));
+                          uint16_t* scales_p, int sms, cudaStream_t stream) {
+  const long long tiles = static_cast<long long>(N / 128) * (K / 64);
+  const int T = tiles_per_cta(tiles, sms);
+  repack_codes_kernel<<<grid_for(tiles, T), kTileThreads, 0, stream>>>(q, K, N, T, tiles,
+                                                                       reinterpret_cast<uint4*>(packed));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long ns = static_cast<long long>(K / G) * N;
@@ -330,10 +554,14 @@ cudaError_t launch_repack(const uint8_t* q, const uint16_t* s, int K, int N, int
 }
 
 cudaError_t launch_quantize_repack(const uint16_t* w, const uint16_t* s, const uint8_t* z, int K, int N, int G,
-                                   uint32_t* packed, uint16_t* scales_p, cudaStream_t stream) {
-  const unsigned tiles = static_cast<unsigned>(static_cast<long long>(N / 128) * (K / 64));
-  quantize_codes_kernel<<<tiles, kTileThreads, 0, stream>>>(w, s, z, K, N, G, reinterpret_cast<uint4*>(packed));
-  cudaError_t e = cudaGetLastError();
+                                   uint32_t* packed, uint16_t* scales_p, int sms, cudaStream_t stream) {
+  const long long tiles = static_cast<long long>(N / 128) * (K / 64);
+  const int T = tiles_per_cta(tiles, sms);
+  cudaError_t e = cudaFuncSetAttribute(quantize_codes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmem);
+  if (e != cudaSuccess) return e;
+  quantize_codes_kernel<<<grid_for(tiles, T), kTileThreads, kQuantSmem, stream>>>(
+      w, s, z, K, N, G, T, tiles, reinterpret_cast<uint4*>(packed));
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long ns = static_cast<long long>(K / G) * N;
   permute_scales_kernel<<<grid_for(ns, 256), 256, 0, stream>>>(s, scales_p, N, K / G, ns, 0);

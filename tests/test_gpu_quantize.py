@@ -77,6 +77,26 @@ def test_zero_scale_is_reported_and_cleared(w):
     assert np.array_equal(got_packed, oracle.repack(ref_q, s, G)[0])
 
 
+def test_non_finite_weights_are_reported_and_stored_as_8(w):
+    """Infinite and NaN weights make the quotient non-finite: the call flags W4A16_ERR_VALUE and
+    stores code 8 there; every other code (including the rest of those words) is the oracle's."""
+    K, N, G = 256, 256, 128
+    wt, s = synth.make_fp16_weights(K, N, G, seed=6)
+    bad_at = [(3, 5), (70, 130), (130, 255), (255, 0), (17, 17)]
+    for (r, c), v in zip(bad_at, [np.inf, -np.inf, np.nan, np.inf, np.nan]):
+        wt[r, c] = np.float16(v)
+    got_packed, _ = _quantize_on_device(w, wt, s, G)
+    assert w.w4a16_get_status() == 10  # W4A16_ERR_VALUE
+    assert w.w4a16_get_status() == 0
+    ok = wt.copy()
+    for r, c in bad_at:
+        ok[r, c] = 0
+    ref_q = oracle.quantize(ok, s, G)
+    for r, c in bad_at:
+        ref_q[r, c] = 8
+    assert np.array_equal(got_packed, oracle.repack(ref_q, s, G)[0])
+
+
 def test_quantize_full_k_sampled_strips(w):
     """K = 18432 (the big layer's depth), N = 8192; four 128-column strips checked byte for byte."""
     K, N, G = 18432, 8192, 128
