@@ -41,10 +41,11 @@ Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin, bool zp,
   // Unit depth KT = 64 * kq (kq up to 16: each of the 4 K-split warps takes every
   // fourth piece).  Per-SM time of a unit is modelled from copy-engine measurements
   // on GB300: ~89 ns per 4 KB of weights streamed plus ~80 ns of fixed cost for the
-  // unit's three copy operations.  Pick the kq minimising T * unit time among those
-  // that keep >= 2 pipeline stages in shared memory (measured: two 64 KB stages beat
-  // three 48 KB and five 32 KB ones, with fewer bytes in flight -- the per-unit costs
-  // weigh more than the pipeline depth).
+  // unit's three copy operations; each strip segment a CTA's range touches adds ~1 us
+  // (the split-strip epilogue: slots, fence, arrival count).  Pick the kq minimising
+  // T * unit time + segments * 1 us among those that keep >= 2 pipeline stages in
+  // shared memory (measured: two 64 KB stages beat three 48 KB and five 32 KB ones,
+  // with fewer bytes in flight -- the per-unit costs weigh more than the pipeline depth).
   const long long piece_ns = 89LL * piece_bytes / 4096;
   int best_kq = 0;
   long long best_cost = 0;
@@ -56,9 +57,12 @@ Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin, bool zp,
     const MmaLayout l0 = mma_layout(mt, kq, srows, 0, zp, moe_E, piece_bytes);
     const int stages = (smem_optin - l0.smem_bytes) / (l0.stage_bytes + 16);
     if (stages < 2) continue;
-    const long long units = static_cast<long long>(pl.strips) * moe_cols * (K / (64 * kq));
+    const long long KU = K / (64 * kq);
+    const long long units = static_cast<long long>(pl.strips) * moe_cols * KU;
     const long long T = (units + sms - 1) / sms;
-    const long long cost = T * (piece_ns * kq + 80);
+    // strip segments in a range of T units over strips of KU units, at most
+    const long long segs = (KU % T == 0) ? 1 : (T % KU == 0) ? T / KU : (T - 1) / KU + 2;
+    const long long cost = T * (piece_ns * kq + 80) + segs * 1000;
     if (best_kq == 0 || cost < best_cost) {
       best_kq = kq;
       best_cost = cost;
