@@ -242,6 +242,22 @@ def test_big_layer_plans_are_the_measured_ones(w):
         assert (p["path"], p["k_tile"], p["n_tile"], p["m_chunk"]) == (2, 512, 256, M)
 
 
+# (K, N) -> unit depth (rows) of the streaming kernel at M <= 16 on 152 SMs, as measured inside a
+# CUDA graph: the deeper unit was faster where it is chosen and the shallower one where it is not
+# (8192 x 10240: 512-row units 14.9 us against 15.4; 5120 x 5120: 9.0 against 9.5)
+MEASURED_UNIT_ROWS = [((4096, 4096), 1024), ((4096, 22016), 1024), ((8192, 8192), 1024), ((8192, 10240), 512),
+                      ((2048, 7168), 1024), ((7168, 2048), 1024), ((1024, 12288), 1024), ((18432, 4096), 768),
+                      ((5120, 5120), 512), ((7168, 4096), 512), ((18432, 73728), 1024)]
+
+
+@pytest.mark.parametrize("shape,rows", MEASURED_UNIT_ROWS, ids=[f"{k}x{n}" for (k, n), _ in MEASURED_UNIT_ROWS])
+def test_streaming_unit_depth_is_the_measured_best(w, shape, rows):
+    K, N = shape
+    for M in (1, 8, 16):
+        p = w.w4a16_plan(M, K, N, 128, 152)
+        assert p["path"] == 1 and p["k_tile"] == rows, (M, p["k_tile"])
+
+
 @pytest.mark.parametrize("M", [17, 32, 48, 64, 80, 128, 129, 256, 1000])
 @pytest.mark.parametrize("K,N", [(11008, 4096), (2816, 4096), (18432, 73728), (8192, 28672), (384, 384), (128, 640)])
 @pytest.mark.parametrize("force", [2, 3, 4])
