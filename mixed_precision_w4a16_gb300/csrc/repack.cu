@@ -437,19 +437,41 @@ __global__ void minmax_scales_kernel(const uint16_t* __restrict__ w, int N, int 
   if (bad0 || bad1) atomicOr(&g_repack_flag, kDevErrValue);
 }
 
+// One thread per 16-column block of one scale row: permuted position p of the block holds natural
+// column perm_row(p), i.e. positions 2k and 2k + 1 hold columns k and k + 8, so the 16 permuted
+// scales are the two natural 8-column halves interleaved.  Both sides are 32 contiguous bytes
+// (two 16-byte loads and stores).  Forward (inverse = 0): s natural -> sp permuted; inverse = 1:
+// s permuted -> sp natural.
 __global__ void permute_scales_kernel(const uint16_t* __restrict__ s, uint16_t* __restrict__ sp, int N, int NG,
-                                      long long count, int inverse) {
+                                      long long nblocks, int inverse) {
   const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
-  if (i >= count) return;
-  const int p = static_cast<int>(i & 127);
-  const long long t = i >> 7;
-  const int g = static_cast<int>(t % NG);
-  const long long strip = t / NG;
-  const long long n = strip * 128 + (p & ~15) + perm_row(p & 15);
-  if (!inverse)
-    sp[i] = s[g * static_cast<long long>(N) + n];  // forward: natural -> permuted
-  else
-    sp[g * static_cast<long long>(N) + n] = s[i];  // inverse: permuted -> natural
+  if (i >= nblocks) return;
+  const int per_strip = NG * 8;
+  const long long strip = i / per_strip;
+  const int r = static_cast<int>(i - strip * per_strip);
+  const int g = r >> 3, blk = r & 7;
+  const long long nat = static_cast<long long>(g) * N + strip * 128 + blk * 16;  // natural: row g, 16 columns
+  const long long per = (strip * NG + g) * 128 + blk * 16;                      // permuted: 16 positions
+  const uint4* src = reinterpret_cast<const uint4*>(s + (inverse ? per : nat));
+  uint4* dst = reinterpret_cast<uint4*>(sp + (inverse ? nat : per));
+  const uint4 x0 = src[0], x1 = src[1];
+  const uint32_t a[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+  uint32_t o[8];
+  if (!inverse) {
+    // permuted word m = (column m, column m + 8): low or high halves of natural words m/2, 4 + m/2
+#pragma unroll
+    for (int m = 0; m < 8; ++m) o[m] = __byte_perm(a[m >> 1], a[4 + (m >> 1)], (m & 1) ? 0x7632 : 0x5410);
+  } else {
+    // natural word k of the first half = low halves of permuted words 2k, 2k + 1; of the second
+    // half, their high halves
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      o[k] = __byte_perm(a[2 * k], a[2 * k + 1], 0x5410);
+      o[4 + k] = __byte_perm(a[2 * k], a[2 * k + 1], 0x7632);
+    }
+  }
+  dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+  dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
 __global__ void unpack_codes_kernel(const uint4* __restrict__ packed, int K, int N, uint8_t* __restrict__ q,
@@ -549,7 +571,7 @@ cudaError_t launch_repack(const uint8_t* q, const uint16_t* s, int K, int N, int
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long ns = static_cast<long long>(K / G) * N;
-  permute_scales_kernel<<<grid_for(ns, 256), 256, 0, stream>>>(s, scales_p, N, K / G, ns, 0);
+  permute_scales_kernel<<<grid_for(ns / 16, 256), 256, 0, stream>>>(s, scales_p, N, K / G, ns / 16, 0);
   return cudaGetLastError();
 }
 
@@ -564,7 +586,7 @@ cudaError_t launch_quantize_repack(const uint16_t* w, const uint16_t* s, const u
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long ns = static_cast<long long>(K / G) * N;
-  permute_scales_kernel<<<grid_for(ns, 256), 256, 0, stream>>>(s, scales_p, N, K / G, ns, 0);
+  permute_scales_kernel<<<grid_for(ns / 16, 256), 256, 0, stream>>>(s, scales_p, N, K / G, ns / 16, 0);
   return cudaGetLastError();
 }
 
@@ -577,7 +599,7 @@ cudaError_t launch_minmax_scales(const uint16_t* w, int K, int N, int G, uint16_
 
 cudaError_t launch_permute_scales(const uint16_t* s, int K, int N, int G, uint16_t* scales_p, cudaStream_t stream) {
   const long long ns = static_cast<long long>(K / G) * N;
-  permute_scales_kernel<<<grid_for(ns, 256), 256, 0, stream>>>(s, scales_p, N, K / G, ns, 0);
+  permute_scales_kernel<<<grid_for(ns / 16, 256), 256, 0, stream>>>(s, scales_p, N, K / G, ns / 16, 0);
   return cudaGetLastError();
 }
 
@@ -589,7 +611,7 @@ cudaError_t launch_unpack(const uint32_t* packed, const uint16_t* scales_p, int 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long ns = static_cast<long long>(K / G) * N;
-  permute_scales_kernel<<<grid_for(ns, 256), 256, 0, stream>>>(scales_p, s, N, K / G, ns, 1);
+  permute_scales_kernel<<<grid_for(ns / 16, 256), 256, 0, stream>>>(scales_p, s, N, K / G, ns / 16, 1);
   return cudaGetLastError();
 }
 
