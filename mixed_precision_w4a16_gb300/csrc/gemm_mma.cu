@@ -89,7 +89,10 @@ __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
 // ZP: codes carry a zero point per group and column (p.zeros), else the constant 8.
 // MOE: grouped expert GEMM over p.E experts (p.expert_off), else one GEMM on rows p.m0 ..
 // SP24: p.packed is the 2:4-sparse stream (no zero points, no experts).
-template <int MT, bool ZP, bool MOE, bool SP24>
+// FINAL8: the small-layer build (dense, at most two units per CTA), whose last split-strip sum is
+// shared by all eight consumer warps; kept a separate build because the larger epilogue costs the
+// other layers' main loop ~1.6 % through code generation.
+template <int MT, bool ZP, bool MOE, bool SP24, bool FINAL8>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     gemm_mma_kernel(const __grid_constant__ CUtensorMap tmA, const GemmParams p) {
   constexpr int MB = 8 * MT;
@@ -429,104 +432,198 @@ if constexpr (SP24) {
           }
     }
     named_bar_sync(1, kConsumerWarps * 32);
-    const bool skip = *seg_abort != 0;  // the same in every consumer warp
-    const int c_first = (j * p.KU) / T;
-    const int c_last = min(((j + 1) * p.KU - 1) / T, static_cast<int>(gridDim.x) - 1);
-    int strip = j, row0 = p.m0, row_end = p.M;
-    if (MOE) {
-      strip = sp.j;
-      row0 = offs[sp.e] + MB * sp.ci;
-      row_end = min(row0 + MB, offs[sp.e + 1]);
-    }
-    // C for 16-column block i of this warp's column half (+ bias, FP32 -> FP16 RNE)
-    auto store_block = [&](int i, const float (&v)[MT][4]) {
-      const int n_base = strip * kStrip + (ng * kNbw + i) * 16 + g;
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int token = row0 + mt * 8 + 2 * t + (e & 1);
-          const int n = n_base + 8 * (e >> 1);
-          float c = v[mt][e];
-          if (p.bias) c += __half2float(__ushort_as_half(p.bias[n]));
-          if (token < row_end) p.C[static_cast<long long>(token) * p.N + n] = f32_to_f16_bits(c);
-        }
-    };
-    if (c_first == c_last) {
-      // the strip lies inside this CTA: the folded sums are the result
-      if (kq0 == 0 && !skip) {
-#pragma unroll
-        for (int i = 0; i < kNbw; ++i) store_block(i, acc[i]);
+    if constexpr (FINAL8) {
+      // small layers (at most two units per CTA): at a CTA's last segment all eight consumer
+      // warps share the last arriver's sum of a split strip
+      const bool skip = *seg_abort != 0;  // the same in every consumer warp
+      const int c_first = (j * p.KU) / T;
+      const int c_last = min(((j + 1) * p.KU - 1) / T, static_cast<int>(gridDim.x) - 1);
+      int strip = j, row0 = p.m0, row_end = p.M;
+      if (MOE) {
+        strip = sp.j;
+        row0 = offs[sp.e] + MB * sp.ci;
+        row_end = min(row0 + MB, offs[sp.e + 1]);
       }
-    } else if (!skip) {
-      // 2) this strip is split between CTAs: the folded warps publish the partial, one thread
-      // counts the arrival.  Mid-range, only the two folded warps take part (the other six go on
-      // decoding the next unit); at the CTA's last segment all eight share the last arriver's sum.
-      const bool all8 = (it == nunits - 1);
-      const bool part = all8 || kq0 == 0;
-      auto sync = [&]() {
-        if (all8)
-          named_bar_sync(1, kConsumerWarps * 32);
-        else if (kq0 == 0)
-          named_bar_sync(2, 2 * 32);
+      // C for 16-column block i of this warp's column half (+ bias, FP32 -> FP16 RNE)
+      auto store_block = [&](int i, const float (&v)[MT][4]) {
+        const int n_base = strip * kStrip + (ng * kNbw + i) * 16 + g;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int token = row0 + mt * 8 + 2 * t + (e & 1);
+            const int n = n_base + 8 * (e >> 1);
+            float c = v[mt][e];
+            if (p.bias) c += __half2float(__ushort_as_half(p.bias[n]));
+            if (token < row_end) p.C[static_cast<long long>(token) * p.N + n] = f32_to_f16_bits(c);
+          }
       };
-      if (kq0 == 0) {
-        const int slot = (j == first_col) ? 2 * cta : 2 * cta + 1;
-        float* dst = p.slots + static_cast<long long>(slot) * SLOT + ng * kNbw * MT * 4 * 32 + lane;
+      if (c_first == c_last) {
+        // the strip lies inside this CTA: the folded sums are the result
+        if (kq0 == 0 && !skip) {
 #pragma unroll
-        for (int i = 0; i < kNbw; ++i)
+          for (int i = 0; i < kNbw; ++i) store_block(i, acc[i]);
+        }
+      } else if (!skip) {
+        // 2) this strip is split between CTAs: the folded warps publish the partial, one thread
+        // counts the arrival.  Mid-range, only the two folded warps take part (the other six go on
+        // decoding the next unit); at the CTA's last segment all eight share the last arriver's sum.
+        const bool all8 = (it == nunits - 1);
+        const bool part = all8 || kq0 == 0;
+        auto sync = [&]() {
+          if (all8)
+            named_bar_sync(1, kConsumerWarps * 32);
+          else if (kq0 == 0)
+            named_bar_sync(2, 2 * 32);
+        };
+        if (kq0 == 0) {
+          const int slot = (j == first_col) ? 2 * cta : 2 * cta + 1;
+          float* dst = p.slots + static_cast<long long>(slot) * SLOT + ng * kNbw * MT * 4 * 32 + lane;
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt)
+          for (int i = 0; i < kNbw; ++i)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) dst[((i * MT + mt) * 4 + e) * 32] = acc[i][mt][e];
-        __threadfence();
-      }
-      sync();
-      if (warp == 0 && lane == 0) {
-        const unsigned old = atomicAdd(p.counters + j, 1u);
-        *last_flag = (old == static_cast<unsigned>(c_last - c_first)) ? 1 : 0;
-      }
-      sync();
-      if (part && *last_flag != 0) {
-        // 3) last arriver: sum every CTA's slot in CTA order (deterministic), block by block (all
-        // blocks in a folded warp, or block kq0 in each of the eight); the loads of kU CTAs
-        // (16 floats a thread) are in flight together
-        constexpr int kU = 4 / MT;
-        __threadfence();
-        const int i_begin = all8 ? kq0 : 0, i_end = all8 ? kq0 + 1 : kNbw;
-        for (int i = i_begin; i < i_end; ++i) {
-          float sum[MT][4];
+            for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt)
+              for (int e = 0; e < 4; ++e) dst[((i * MT + mt) * 4 + e) * 32] = acc[i][mt][e];
+          __threadfence();
+        }
+        sync();
+        if (warp == 0 && lane == 0) {
+          const unsigned old = atomicAdd(p.counters + j, 1u);
+          *last_flag = (old == static_cast<unsigned>(c_last - c_first)) ? 1 : 0;
+        }
+        sync();
+        if (part && *last_flag != 0) {
+          // 3) last arriver: sum every CTA's slot in CTA order (deterministic)
+          __threadfence();
+          if (all8) {
+            // each of the eight warps sums its block i = kq0; the loads of kU CTAs (16 floats a
+            // thread) are in flight together
+            constexpr int kU = 4 / MT;
+            float sum[MT][4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sum[mt][e] = 0.f;
-          const int sidx = (ng * kNbw + i) * MT * 4 * 32 + lane;
-          for (int c0 = c_first; c0 <= c_last; c0 += kU) {
-            float v[kU][MT][4];
+            for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-            for (int u = 0; u < kU; ++u) {
-              const int c = c0 + u;
-              if (c <= c_last) {
-                const int cslot = (j == (c * T) / p.KU) ? 2 * c : 2 * c + 1;
-                const float* src = p.slots + static_cast<long long>(cslot) * SLOT + sidx;
+              for (int e = 0; e < 4; ++e) sum[mt][e] = 0.f;
+            const int sidx = (ng * kNbw + kq0) * MT * 4 * 32 + lane;
+            for (int c0 = c_first; c0 <= c_last; c0 += kU) {
+              float v[kU][MT][4];
+#pragma unroll
+              for (int u = 0; u < kU; ++u) {
+                const int c = c0 + u;
+                if (c <= c_last) {
+                  const int cslot = (j == (c * T) / p.KU) ? 2 * c : 2 * c + 1;
+                  const float* src = p.slots + static_cast<long long>(cslot) * SLOT + sidx;
+#pragma unroll
+                  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) v[u][mt][e] = __ldcg(src + (mt * 4 + e) * 32);
+                }
+              }
+#pragma unroll
+              for (int u = 0; u < kU; ++u)
+                if (c0 + u <= c_last) {
+#pragma unroll
+                  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sum[mt][e] += v[u][mt][e];
+                }
+            }
+            store_block(kq0, sum);
+          } else {
+            // the two folded warps sum all their blocks, one CTA's slot (all blocks' loads in
+            // flight together) at a time
+#pragma unroll
+            for (int i = 0; i < kNbw; ++i)
+#pragma unroll
+              for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[i][mt][e] = 0.f;
+            for (int c = c_first; c <= c_last; ++c) {
+              const int cslot = (j == (c * T) / p.KU) ? 2 * c : 2 * c + 1;
+              const float* src = p.slots + static_cast<long long>(cslot) * SLOT + ng * kNbw * MT * 4 * 32 + lane;
+#pragma unroll
+              for (int i = 0; i < kNbw; ++i)
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                  for (int e = 0; e < 4; ++e) v[u][mt][e] = __ldcg(src + (mt * 4 + e) * 32);
-              }
+                  for (int e = 0; e < 4; ++e) acc[i][mt][e] += __ldcg(src + ((i * MT + mt) * 4 + e) * 32);
             }
 #pragma unroll
-            for (int u = 0; u < kU; ++u)
-              if (c0 + u <= c_last) {
+            for (int i = 0; i < kNbw; ++i) store_block(i, acc[i]);
+          }
+          if (warp == 0 && lane == 0) p.counters[j] = 0u;
+        }
+      }
+    } else {
+      const bool skip = *seg_abort != 0;
+      if (kq0 == 0 && !skip) {
+        const int c_first = (j * p.KU) / T;
+        const int c_last = min(((j + 1) * p.KU - 1) / T, static_cast<int>(gridDim.x) - 1);
+        const int sidx0 = ng * kNbw * MT * 4 * 32 + lane;  // this warp's part of a strip partial
+        bool write_now = true;
+        if (c_first != c_last) {
+          // 2) this strip is split between CTAs: publish the partial, count arrivals
+          const int slot = (j == first_col) ? 2 * cta : 2 * cta + 1;
+          float* dst = p.slots + static_cast<long long>(slot) * SLOT + sidx0;
+#pragma unroll
+          for (int i = 0; i < kNbw; ++i)
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) dst[((i * MT + mt) * 4 + e) * 32] = acc[i][mt][e];
+          __threadfence();
+          named_bar_sync(2, 2 * 32);
+          if (warp == 0 && lane == 0) {
+            const unsigned old = atomicAdd(p.counters + j, 1u);
+            *last_flag = (old == static_cast<unsigned>(c_last - c_first)) ? 1 : 0;
+          }
+          named_bar_sync(2, 2 * 32);
+          write_now = *last_flag != 0;
+          if (write_now) {
+            // 3) last arriver: sum every CTA's slot in CTA order (deterministic)
+            __threadfence();
+#pragma unroll
+            for (int i = 0; i < kNbw; ++i)
+#pragma unroll
+              for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[i][mt][e] = 0.f;
+            for (int c = c_first; c <= c_last; ++c) {
+              const int cslot = (j == (c * T) / p.KU) ? 2 * c : 2 * c + 1;
+              const float* src = p.slots + static_cast<long long>(cslot) * SLOT + sidx0;
+#pragma unroll
+              for (int i = 0; i < kNbw; ++i)
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                  for (int e = 0; e < 4; ++e) sum[mt][e] += v[u][mt][e];
+                  for (int e = 0; e < 4; ++e) acc[i][mt][e] += __ldcg(src + ((i * MT + mt) * 4 + e) * 32);
+            }
+            if (warp == 0 && lane == 0) p.counters[j] = 0u;
+          }
+        }
+        if (write_now) {
+          int strip = j, row0 = p.m0, row_end = p.M;
+          if (MOE) {
+            strip = sp.j;
+            row0 = offs[sp.e] + MB * sp.ci;
+            row_end = min(row0 + MB, offs[sp.e + 1]);
+          }
+#pragma unroll
+          for (int i = 0; i < kNbw; ++i) {
+            const int n_base = strip * kStrip + (ng * kNbw + i) * 16 + g;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int token = row0 + mt * 8 + 2 * t + (e & 1);
+                const int n = n_base + 8 * (e >> 1);
+                float c = acc[i][mt][e];
+                if (p.bias) c += __half2float(__ushort_as_half(p.bias[n]));
+                if (token < row_end) p.C[static_cast<long long>(token) * p.N + n] = f32_to_f16_bits(c);
               }
           }
-          store_block(i, sum);
         }
-        if (warp == 0 && lane == 0) p.counters[j] = 0u;
       }
     }
 #pragma unroll
@@ -541,9 +638,9 @@ if constexpr (SP24) {
   named_bar_sync(3, kMmaThreads);
 }
 
-template <int MT, bool ZP, bool MOE = false, bool SP24 = false>
+template <int MT, bool ZP, bool MOE = false, bool SP24 = false, bool FINAL8 = false>
 cudaError_t launch_one(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream) {
-  auto kern = gemm_mma_kernel<MT, ZP, MOE, SP24>;
+  auto kern = gemm_mma_kernel<MT, ZP, MOE, SP24, FINAL8>;
   static int smem_cache[64];
   cudaError_t e = ensure_smem(kern, cfg.smem_bytes, smem_cache);
   if (e != cudaSuccess) return e;
@@ -573,6 +670,17 @@ MmaLayout mma_layout(int m_tiles, int kq, int srows, int stages, bool zp, int mo
 
 cudaError_t launch_gemm_mma(const MmaConfig& cfg, const CUtensorMap& tmA, const GemmParams& p, cudaStream_t stream) {
   const bool zp = p.zeros != nullptr;
+  if (cfg.final8) {
+    switch (cfg.m_tiles) {
+      case 1:
+        return zp ? launch_one<1, true, false, false, true>(cfg, tmA, p, stream)
+                  : launch_one<1, false, false, false, true>(cfg, tmA, p, stream);
+      case 2:
+        return zp ? launch_one<2, true, false, false, true>(cfg, tmA, p, stream)
+                  : launch_one<2, false, false, false, true>(cfg, tmA, p, stream);
+      default: break;
+    }
+  }
   switch (cfg.m_tiles) {
     case 1: return zp ? launch_one<1, true>(cfg, tmA, p, stream) : launch_one<1, false>(cfg, tmA, p, stream);
     case 2: return zp ? launch_one<2, true>(cfg, tmA, p, stream) : launch_one<2, false>(cfg, tmA, p, stream);

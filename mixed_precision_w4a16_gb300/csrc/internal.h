@@ -114,10 +114,11 @@ constexpr int kMoeMaxExperts = 2048;
 
 struct MmaConfig {
   int m_tiles;      // 8-row token tiles (1, 2, 4)
-  int kq;           // 64-row pieces per unit (2, 4, 8)
+  int kq;           // 64-row pieces per unit (2, 4, 8, 12, 16)
   int stages;
   int smem_bytes;
   int threads;
+  bool final8;      // small-layer build: dense, at most two units per CTA (see gemm_mma.cu)
 };
 
 constexpr int kMmaThreads = 288;  // 8 consumer warps + 1 producer warp
