@@ -88,9 +88,11 @@ Plan make_plan_mma(int M, int K, int N, int G, int sms, int smem_optin, bool zp,
   pl.smem_bytes = pl.lay.smem_bytes;
   pl.threads = kMmaThreads;
   finish_split(pl, K, sms, static_cast<size_t>(kStrip) * 8 * mt);
-  // Small dense layers (at most two units per CTA, so the last segment's epilogue is a large part
-  // of a launch) take the build whose last split-strip sum all eight consumer warps share.
-  pl.cfg.final8 = moe_E == 0 && !sp24 && mt <= 2 && pl.T <= 2;
+  // The build whose last split-strip sum all eight consumer warps share (dense layers only):
+  // measured as fast or faster for two token tiles at every layer size (1-5 %), and for one tile
+  // only where a CTA has at most two units (its larger epilogue costs the one-tile main loop
+  // 0.3-1.7 % through code generation, which the shorter sum repays only on the smallest layers).
+  pl.cfg.final8 = moe_E == 0 && !sp24 && (mt == 2 || (mt == 1 && pl.T <= 2));
   return pl;
 }
 

@@ -89,9 +89,10 @@ __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
 // ZP: codes carry a zero point per group and column (p.zeros), else the constant 8.
 // MOE: grouped expert GEMM over p.E experts (p.expert_off), else one GEMM on rows p.m0 ..
 // SP24: p.packed is the 2:4-sparse stream (no zero points, no experts).
-// FINAL8: the small-layer build (dense, at most two units per CTA), whose last split-strip sum is
-// shared by all eight consumer warps; kept a separate build because the larger epilogue costs the
-// other layers' main loop ~1.6 % through code generation.
+// FINAL8: the build whose last split-strip sum is shared by all eight consumer warps (dense
+// layers with two token tiles, or one tile and at most two units per CTA); a separate build
+// because with one token tile the larger epilogue costs the main loop up to ~1.7 % through code
+// generation.
 template <int MT, bool ZP, bool MOE, bool SP24, bool FINAL8>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     gemm_mma_kernel(const __grid_constant__ CUtensorMap tmA, const GemmParams p) {

@@ -118,7 +118,7 @@ struct MmaConfig {
   int stages;
   int smem_bytes;
   int threads;
-  bool final8;      // small-layer build: dense, at most two units per CTA (see gemm_mma.cu)
+  bool final8;      // build with the eight-warp last split-strip sum (see gemm_mma.cu)
 };
 
 constexpr int kMmaThreads = 288;  // 8 consumer warps + 1 producer warp
