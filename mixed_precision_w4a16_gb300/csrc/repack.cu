@@ -495,20 +495,23 @@ __global__ void unpack_codes_kernel(const uint4* __restrict__ packed, int K, int
   }
 }
 
-// Bhat[k][n] = RNE(s * (q - 8)): the exact decode of the GEMM, then one FP16 multiply.
-// zero codes uint8[K/G][N] -> the scales' permuted order (uint8[N/128][K/G][128]); codes above 15 flag
+// Zero codes uint8[K/G][N] -> the scales' permuted order (uint8[N/128][K/G][128]), one thread per
+// 16-column block of one row: permuted bytes 2k and 2k + 1 hold columns k and k + 8 (one 16-byte
+// load and store, byte permutes for the interleave).  Codes above 15 are masked to 4 bits and flag.
 __global__ void permute_zeros_kernel(const uint8_t* __restrict__ z, uint8_t* __restrict__ zp, int N, int NG,
-                                     long long count) {
+                                     long long nblocks) {
   const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
-  if (i >= count) return;
-  const int p = static_cast<int>(i & 127);
-  const long long t = i >> 7;
-  const int g = static_cast<int>(t % NG);
-  const long long strip = t / NG;
-  const long long n = strip * 128 + (p & ~15) + perm_row(p & 15);
-  const uint8_t code = z[g * static_cast<long long>(N) + n];
-  if (code > 15) atomicOr(&g_repack_flag, kDevErrCodeRange);
-  zp[i] = code & 15;
+  if (i >= nblocks) return;
+  const int per_strip = NG * 8;
+  const long long strip = i / per_strip;
+  const int r = static_cast<int>(i - strip * per_strip);
+  const int g = r >> 3, blk = r & 7;
+  const uint4 x = *reinterpret_cast<const uint4*>(z + static_cast<long long>(g) * N + strip * 128 + blk * 16);
+  if ((x.x | x.y | x.z | x.w) & 0xF0F0F0F0u) atomicOr(&g_repack_flag, kDevErrCodeRange);
+  const uint32_t w0 = x.x & 0x0F0F0F0Fu, w1 = x.y & 0x0F0F0F0Fu, w2 = x.z & 0x0F0F0F0Fu, w3 = x.w & 0x0F0F0F0Fu;
+  *reinterpret_cast<uint4*>(zp + (strip * NG + g) * 128 + blk * 16) =
+      make_uint4(__byte_perm(w0, w2, 0x5140), __byte_perm(w0, w2, 0x7362), __byte_perm(w1, w3, 0x5140),
+                 __byte_perm(w1, w3, 0x7362));
 }
 
 // Bhat[k][n] = RNE(s * (q - z)): the exact decode of the GEMM (z = 8 without zero points), then one
@@ -624,8 +627,8 @@ cudaError_t launch_dequant(const uint32_t* packed, const uint16_t* scales_p, con
 }
 
 cudaError_t launch_repack_zeros(const uint8_t* z, int K, int N, int G, uint8_t* zeros_p, cudaStream_t stream) {
-  const long long count = static_cast<long long>(K / G) * N;
-  permute_zeros_kernel<<<grid_for(count, 256), 256, 0, stream>>>(z, zeros_p, N, K / G, count);
+  const long long nblocks = static_cast<long long>(K / G) * N / 16;
+  permute_zeros_kernel<<<grid_for(nblocks, 256), 256, 0, stream>>>(z, zeros_p, N, K / G, nblocks);
   return cudaGetLastError();
 }
 
