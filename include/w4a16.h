@@ -381,6 +381,9 @@ typedef struct {
   int stages;        /* shared-memory pipeline depth */
   int smem_bytes;    /* dynamic shared memory per CTA */
   int threads;       /* threads per CTA */
+  int final_sum_warps; /* warps that sum a split strip's FP32 slots at a CTA's last segment:
+                          path 1: 8 with two token tiles, or one tile and at most two units per
+                          CTA (measured faster there), else 2; path 2: the 16 dequant warps */
 } w4a16_plan_t;
 
 W4A16_API int w4a16_plan(int M, int K, int N, int groupsize, int num_sms, w4a16_plan_t* out);

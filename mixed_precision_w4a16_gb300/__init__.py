@@ -50,7 +50,7 @@ class W4A16Error(RuntimeError):
 class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "path", "m_tiles", "m_chunk", "n_tile", "k_tile", "units", "units_per_cta", "grid",
-        "stages", "smem_bytes", "threads")]
+        "stages", "smem_bytes", "threads", "final_sum_warps")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

@@ -141,6 +141,7 @@ int w4a16_plan(int M, int K, int N, int groupsize, int num_sms, w4a16_plan_t* ou
   out->stages = pl.stages;
   out->smem_bytes = pl.smem_bytes;
   out->threads = pl.threads;
+  out->final_sum_warps = pl.path == 2 ? 16 : (pl.cfg.final8 ? 8 : 2);
   return W4A16_OK;
 }
 

@@ -258,6 +258,21 @@ def test_streaming_unit_depth_is_the_measured_best(w, shape, rows):
         assert p["path"] == 1 and p["k_tile"] == rows, (M, p["k_tile"])
 
 
+# (K, N, M) -> warps that sum a split strip at a CTA's last segment on 152 SMs, as chosen from
+# same-box measurements of both streaming builds: eight with two token tiles at every layer size,
+# and with one tile only where a CTA has at most two units; the tcgen05 kernel's 16 dequant warps
+MEASURED_FINAL_SUM_WARPS = [((4096, 4096, 1), 8), ((4096, 4096, 16), 8), ((11008, 4096, 1), 2),
+                            ((11008, 4096, 16), 8), ((8192, 8192, 8), 2), ((18432, 73728, 1), 2),
+                            ((18432, 73728, 16), 8), ((2048, 7168, 1), 8), ((18432, 73728, 32), 16)]
+
+
+@pytest.mark.parametrize("shape,warps", MEASURED_FINAL_SUM_WARPS,
+                         ids=[f"{k}x{n}_m{m}" for (k, n, m), _ in MEASURED_FINAL_SUM_WARPS])
+def test_split_strip_sum_build_is_the_measured_one(w, shape, warps):
+    K, N, M = shape
+    assert w.w4a16_plan(M, K, N, 128, 152)["final_sum_warps"] == warps
+
+
 @pytest.mark.parametrize("M", [17, 32, 48, 64, 80, 128, 129, 256, 1000])
 @pytest.mark.parametrize("K,N", [(11008, 4096), (2816, 4096), (18432, 73728), (8192, 28672), (384, 384), (128, 640)])
 @pytest.mark.parametrize("force", [2, 3, 4])
